@@ -1,0 +1,126 @@
+"""Plain fp64 CPU oracle for the Gaussian Mixture Attention forward.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package; the product path
+(``gaussian_mixture_latent_gb300`` and its CUDA library) never does.
+
+The arithmetic lives in ``gma_oracle.c`` (double precision, written from the
+equations of "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+Probabilistic Latent Routing", section 3 -- Eqs. 3, 3b, 5-8, 6b, 8b, 14-16).
+This module only marshals numpy arrays into it.
+
+Every function here is pinned by ``tests/test_oracle.py`` against things the
+paper and the mathematics fix (a textbook density routine, the explicit N x N
+affinity, closed forms and invariants); see that file.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gma_oracle.c")
+_SO = os.path.join(_HERE, "libgma_oracle.so")
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler (no fast-math)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        cc = os.environ.get("CC", "gcc")
+        tmp = _SO + ".tmp%d" % os.getpid()
+        subprocess.check_call([cc, "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC,
+                               "-lm", "-lpthread"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        i, d = ctypes.c_int, ctypes.c_double
+        lib.gma_oracle_scores.argtypes = [i, i, i, _dp, _dp, _dp, _dp, d, _dp]
+        lib.gma_oracle_responsibilities.argtypes = [i, i, i, _dp, _dp, _dp, _dp, d, _dp]
+        lib.gma_oracle_forward_head.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d, d,
+                                                i, _dp, _dp, _dp]
+        lib.gma_oracle_forward.argtypes = [i, i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d, d,
+                                           i, _dp, i]
+        for fn in (lib.gma_oracle_scores, lib.gma_oracle_responsibilities,
+                   lib.gma_oracle_forward_head, lib.gma_oracle_forward):
+            fn.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _c(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise RuntimeError(f"oracle {what} failed with code {rc}")
+
+
+def scores(X, mu, omega, alpha, var_floor: float) -> np.ndarray:
+    """Eq. (16) log-density scores s [N, K] for the rows of X [N, d]."""
+    X, mu, omega, alpha = _c(X), _c(mu), _c(omega), _c(alpha)
+    N, d = X.shape
+    K = mu.shape[0]
+    out = np.empty((N, K), dtype=np.float64)
+    _check(_load().gma_oracle_scores(N, d, K, _p(X), _p(mu), _p(omega), _p(alpha),
+                                     float(var_floor), _p(out)), "scores")
+    return out
+
+
+def responsibilities(X, mu, omega, alpha, var_floor: float) -> np.ndarray:
+    """Eq. (3)/(3b) responsibilities Gamma [N, K] for the rows of X [N, d]."""
+    X, mu, omega, alpha = _c(X), _c(mu), _c(omega), _c(alpha)
+    N, d = X.shape
+    K = mu.shape[0]
+    out = np.empty((N, K), dtype=np.float64)
+    _check(_load().gma_oracle_responsibilities(N, d, K, _p(X), _p(mu), _p(omega), _p(alpha),
+                                               float(var_floor), _p(out)), "responsibilities")
+    return out
+
+
+def forward_head(Qx, Kx, V, mu, omega, alpha, var_floor: float, eps: float, causal: bool,
+                 return_memory: bool = False):
+    """One head: O [N, dv] (Eq. 7-8, or 8b when causal).  With ``return_memory`` also
+    the latent memory Vt [K, dv] and normaliser Z [K] (Eq. 5-6; for the causal
+    variant the prefix memory after the last position)."""
+    Qx, Kx, V, mu, omega, alpha = map(_c, (Qx, Kx, V, mu, omega, alpha))
+    N, d = Qx.shape
+    K = mu.shape[0]
+    dv = V.shape[1]
+    out = np.empty((N, dv), dtype=np.float64)
+    Vt = np.empty((K, dv), dtype=np.float64)
+    Z = np.empty((K,), dtype=np.float64)
+    _check(_load().gma_oracle_forward_head(N, d, K, dv, _p(Qx), _p(Kx), _p(V), _p(mu), _p(omega),
+                                           _p(alpha), float(var_floor), float(eps), int(causal),
+                                           _p(out), _p(Vt), _p(Z)), "forward_head")
+    return (out, Vt, Z) if return_memory else out
+
+
+def forward(Qx, Kx, V, mu, omega, alpha, var_floor: float, eps: float, causal: bool,
+            threads: int = 1) -> np.ndarray:
+    """All heads: Qx, Kx [B, H, N, d], V [B, H, N, dv], parameters [H, K, d] / [H, K]
+    -> O [B, H, N, dv] in float64.  Heads run on ``threads`` POSIX threads."""
+    Qx, Kx, V, mu, omega, alpha = map(_c, (Qx, Kx, V, mu, omega, alpha))
+    B, H, N, d = Qx.shape
+    K = mu.shape[1]
+    dv = V.shape[3]
+    out = np.empty((B, H, N, dv), dtype=np.float64)
+    _check(_load().gma_oracle_forward(B, H, N, d, K, dv, _p(Qx), _p(Kx), _p(V), _p(mu), _p(omega),
+                                      _p(alpha), float(var_floor), float(eps), int(causal),
+                                      _p(out), int(threads)), "forward")
+    return out

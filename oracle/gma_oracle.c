@@ -1,0 +1,252 @@
+/*
+ * Plain fp64 CPU oracle for the Gaussian Mixture Attention (GMA) forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg load this library.  The CUDA library shares no
+ * code with it and never calls it.
+ *
+ * Source: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+ * Probabilistic Latent Routing" (Huang & Raza, 2026), section 3.  Every
+ * function below evaluates the paper's definitions directly, in double
+ * precision, in the order the equations are written:
+ *
+ *   Eq. (14)  sigma^2_{k,m} = log(1 + exp(omega_{k,m})) + eps_sigma
+ *   Eq. (15)  pi_k = softmax(alpha)_k              (used as log pi_k)
+ *   Eq. (16)  s_{i,k} = log pi_k - (d/2) log(2 pi) - (1/2) log|Sigma_k|
+ *                       - (1/2) (x_i - mu_k)^T Sigma_k^{-1} (x_i - mu_k)
+ *   Eq. (3b)  gamma_{i,k} = exp(s_{i,k}) / sum_l exp(s_{i,l})
+ *   Eq. (5-6) Vt_k = sum_j gamma^K_{j,k} V_j,  Z_k = sum_j gamma^K_{j,k}
+ *   Eq. (7-8) O_i = sum_k gamma^Q_{i,k} Vt_k / (sum_k gamma^Q_{i,k} Z_k + eps)
+ *   Eq. (6b)  causal prefix memory: sums over j <= i (inclusive)
+ *   Eq. (8b)  causal read from the prefix memory of position i
+ *
+ * Readings where the paper leaves a step open:
+ *   - softplus is evaluated as max(w,0) + log1p(exp(-|w|)), which equals
+ *     log(1+exp(w)) exactly in real arithmetic and does not overflow;
+ *   - the softmax subtracts the row maximum before exponentiating (the
+ *     paper fixes the value, not the evaluation order);
+ *   - the causal prefix is inclusive (row i reads its own key), following
+ *     the j <= i of Eq. (6b);
+ *   - eps is added once to the scalar denominator of each row (Eq. 8/8b).
+ *
+ * Layouts: row-major.  X [N, d], V [N, dv], out [N, dv] per head;
+ * mu, omega [K, d], alpha [K] per head.  Multi-head drivers take
+ * Qx, Kx [G, N, d], V [G, N, dv], out [G, N, dv] with G = B*H heads, and
+ * parameters [H, K, d] / [H, K] shared across the batch (head g uses
+ * parameter set g % H).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define GMA_ORACLE_LOG_2PI 1.8378770664093454835606594728112
+
+/* Eq. (14): diagonal variance from its unconstrained parameter. */
+static double variance_from_omega(double w, double var_floor)
+{
+    double softplus = (w > 0.0 ? w : 0.0) + log1p(exp(-fabs(w)));
+    return softplus + var_floor;
+}
+
+/* Eq. (15): log of the softmax-normalised mixture priors. */
+static void log_priors(int K, const double *alpha, double *logpi)
+{
+    double m = alpha[0];
+    for (int k = 1; k < K; ++k)
+        if (alpha[k] > m) m = alpha[k];
+    double sum = 0.0;
+    for (int k = 0; k < K; ++k) sum += exp(alpha[k] - m);
+    double lse = m + log(sum);
+    for (int k = 0; k < K; ++k) logpi[k] = alpha[k] - lse;
+}
+
+/*
+ * Eq. (16): pre-normalised log-density scores s [N, K] of the rows of X.
+ * Direct Mahalanobis form, one (i, k) pair at a time.
+ */
+int gma_oracle_scores(int N, int d, int K, const double *X, const double *mu,
+                      const double *omega, const double *alpha, double var_floor,
+                      double *s)
+{
+    if (N < 0 || d <= 0 || K <= 0) return 1;
+    double *logpi = (double *)malloc(sizeof(double) * K);
+    double *var = (double *)malloc(sizeof(double) * (size_t)K * d);
+    if (!logpi || !var) { free(logpi); free(var); return 2; }
+    log_priors(K, alpha, logpi);
+    for (int k = 0; k < K; ++k)
+        for (int m = 0; m < d; ++m)
+            var[(size_t)k * d + m] = variance_from_omega(omega[(size_t)k * d + m], var_floor);
+    for (int i = 0; i < N; ++i) {
+        const double *x = X + (size_t)i * d;
+        for (int k = 0; k < K; ++k) {
+            const double *mk = mu + (size_t)k * d;
+            const double *vk = var + (size_t)k * d;
+            double logdet = 0.0, maha = 0.0;
+            for (int m = 0; m < d; ++m) {
+                double diff = x[m] - mk[m];
+                logdet += log(vk[m]);
+                maha += diff * diff / vk[m];
+            }
+            s[(size_t)i * K + k] = logpi[k] - 0.5 * d * GMA_ORACLE_LOG_2PI - 0.5 * logdet - 0.5 * maha;
+        }
+    }
+    free(logpi);
+    free(var);
+    return 0;
+}
+
+/* Eq. (3b): responsibilities gamma [N, K], each row a softmax of its scores. */
+int gma_oracle_responsibilities(int N, int d, int K, const double *X, const double *mu,
+                                const double *omega, const double *alpha, double var_floor,
+                                double *gamma)
+{
+    int rc = gma_oracle_scores(N, d, K, X, mu, omega, alpha, var_floor, gamma);
+    if (rc) return rc;
+    for (int i = 0; i < N; ++i) {
+        double *row = gamma + (size_t)i * K;
+        double m = row[0];
+        for (int k = 1; k < K; ++k)
+            if (row[k] > m) m = row[k];
+        double sum = 0.0;
+        for (int k = 0; k < K; ++k) {
+            row[k] = exp(row[k] - m);
+            sum += row[k];
+        }
+        for (int k = 0; k < K; ++k) row[k] /= sum;
+    }
+    return 0;
+}
+
+/*
+ * One head of the forward.  causal = 0: Eq. (5)-(8).  causal = 1: Eq. (6b),
+ * (8b), evaluated as one pass over positions that first adds position i to
+ * the prefix memory and then reads it.
+ * Optional outputs (may be NULL): Vt [K, dv] and Z [K] -- the full-sequence
+ * memory (bidirectional) or the memory after the last position (causal).
+ */
+int gma_oracle_forward_head(int N, int d, int K, int dv, const double *Qx, const double *Kx,
+                            const double *V, const double *mu, const double *omega,
+                            const double *alpha, double var_floor, double eps, int causal,
+                            double *out, double *Vt_out, double *Z_out)
+{
+    if (N < 0 || d <= 0 || K <= 0 || dv <= 0) return 1;
+    size_t nk = (size_t)N * K;
+    double *gq = (double *)malloc(sizeof(double) * (nk ? nk : 1));
+    double *gk = (double *)malloc(sizeof(double) * (nk ? nk : 1));
+    double *Vt = (double *)calloc((size_t)K * dv, sizeof(double));
+    double *Z = (double *)calloc((size_t)K, sizeof(double));
+    int rc = 2;
+    if (!gq || !gk || !Vt || !Z) goto done;
+    rc = gma_oracle_responsibilities(N, d, K, Qx, mu, omega, alpha, var_floor, gq);
+    if (rc) goto done;
+    rc = gma_oracle_responsibilities(N, d, K, Kx, mu, omega, alpha, var_floor, gk);
+    if (rc) goto done;
+
+    if (!causal) {
+        /* Eq. (5)-(6): latent memory and normaliser over the whole sequence. */
+        for (int j = 0; j < N; ++j)
+            for (int k = 0; k < K; ++k) {
+                double g = gk[(size_t)j * K + k];
+                Z[k] += g;
+                for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += g * V[(size_t)j * dv + c];
+            }
+        /* Eq. (7)-(8): normalised read. */
+        for (int i = 0; i < N; ++i) {
+            double den = 0.0;
+            for (int k = 0; k < K; ++k) den += gq[(size_t)i * K + k] * Z[k];
+            den += eps;
+            for (int c = 0; c < dv; ++c) {
+                double num = 0.0;
+                for (int k = 0; k < K; ++k) num += gq[(size_t)i * K + k] * Vt[(size_t)k * dv + c];
+                out[(size_t)i * dv + c] = num / den;
+            }
+        }
+    } else {
+        /* Eq. (6b), (8b): prefix memory including position i, then the read. */
+        for (int i = 0; i < N; ++i) {
+            for (int k = 0; k < K; ++k) {
+                double g = gk[(size_t)i * K + k];
+                Z[k] += g;
+                for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += g * V[(size_t)i * dv + c];
+            }
+            double den = 0.0;
+            for (int k = 0; k < K; ++k) den += gq[(size_t)i * K + k] * Z[k];
+            den += eps;
+            for (int c = 0; c < dv; ++c) {
+                double num = 0.0;
+                for (int k = 0; k < K; ++k) num += gq[(size_t)i * K + k] * Vt[(size_t)k * dv + c];
+                out[(size_t)i * dv + c] = num / den;
+            }
+        }
+    }
+    if (Vt_out) memcpy(Vt_out, Vt, sizeof(double) * (size_t)K * dv);
+    if (Z_out) memcpy(Z_out, Z, sizeof(double) * (size_t)K);
+    rc = 0;
+done:
+    free(gq);
+    free(gk);
+    free(Vt);
+    free(Z);
+    return rc;
+}
+
+/* ---- multi-head driver: heads are independent; one POSIX thread per stripe ---- */
+
+typedef struct {
+    int G, H, N, d, K, dv, causal, first, stride;
+    const double *Qx, *Kx, *V, *mu, *omega, *alpha;
+    double var_floor, eps;
+    double *out;
+    int rc;
+} oracle_job;
+
+static void *oracle_worker(void *arg)
+{
+    oracle_job *j = (oracle_job *)arg;
+    j->rc = 0;
+    for (int g = j->first; g < j->G; g += j->stride) {
+        int h = g % j->H;
+        int rc = gma_oracle_forward_head(
+            j->N, j->d, j->K, j->dv, j->Qx + (size_t)g * j->N * j->d,
+            j->Kx + (size_t)g * j->N * j->d, j->V + (size_t)g * j->N * j->dv,
+            j->mu + (size_t)h * j->K * j->d, j->omega + (size_t)h * j->K * j->d,
+            j->alpha + (size_t)h * j->K, j->var_floor, j->eps, j->causal,
+            j->out + (size_t)g * j->N * j->dv, NULL, NULL);
+        if (rc) j->rc = rc;
+    }
+    return NULL;
+}
+
+/*
+ * All G = B*H heads.  threads <= 0 means one thread.  Returns 0 on success.
+ */
+int gma_oracle_forward(int B, int H, int N, int d, int K, int dv, const double *Qx,
+                       const double *Kx, const double *V, const double *mu, const double *omega,
+                       const double *alpha, double var_floor, double eps, int causal,
+                       double *out, int threads)
+{
+    if (B <= 0 || H <= 0) return 1;
+    int G = B * H;
+    if (threads <= 0) threads = 1;
+    if (threads > G) threads = G;
+    oracle_job *jobs = (oracle_job *)calloc((size_t)threads, sizeof(oracle_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)threads, sizeof(pthread_t));
+    if (!jobs || !tid) { free(jobs); free(tid); return 2; }
+    for (int t = 0; t < threads; ++t) {
+        oracle_job j = {G, H, N, d, K, dv, causal, t, threads, Qx, Kx, V, mu, omega, alpha,
+                        var_floor, eps, out, 0};
+        jobs[t] = j;
+    }
+    int rc = 0;
+    for (int t = 1; t < threads; ++t)
+        if (pthread_create(&tid[t], NULL, oracle_worker, &jobs[t])) { jobs[t].rc = 3; tid[t] = 0; }
+    oracle_worker(&jobs[0]);
+    for (int t = 1; t < threads; ++t)
+        if (tid[t]) pthread_join(tid[t], NULL);
+    for (int t = 0; t < threads; ++t)
+        if (jobs[t].rc) rc = jobs[t].rc;
+    free(jobs);
+    free(tid);
+    return rc;
+}
