@@ -1,0 +1,423 @@
+#!/usr/bin/env python3
+"""GMA forward benchmark on one GB300 (or N independent replicas under torchrun).
+
+Metric: tokens*heads per second of the Gaussian Mixture Attention forward.
+One step = one bidirectional forward plus one causal forward over the
+N = 8192 workload (B=8, H=12, N=8192, d=64, K=64, dv=64, bf16 inputs and
+outputs), so every step of the path runs: parameter prologue,
+responsibilities, latent write, read, and the causal chunked scan.
+A step processes 2 * B * H * N tokens*heads.
+
+Inputs are synthetic (seeded, see gaussian_mixture_latent_gb300/inputs.py).
+Two input sets of 302 MB each (more than the 129 MB L2) alternate between
+steps, so every step streams its inputs from HBM.
+
+Output: one JSON line (rank 0).  --impl reference times the CPU fp64 oracle
+on the host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from gaussian_mixture_latent_gb300 import accounting, inputs  # noqa: E402
+
+WORKLOAD = "causal_bf16_n8192"
+METRIC = "GMA fwd tokens·heads/s (bidir & causal, N=8192); % of HBM/tensor roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 3 s, 20..5000)")
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "sm_max_mhz": p.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def fp32_simt_peak_tflops(sm_mhz):
+    # 152 SMs x 128 FP32 lanes x 2 flops per FMA x clock
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "gaussian_mixture_latent_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def known_traffic(kernel):
+    path = os.path.join(ROOT, "profiles", "kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(kernel)
+    if not e or e.get("csrc_hash") != csrc_hash() or e.get("workload") != WORKLOAD:
+        return None
+    return e["bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_id_for(dev_index):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if dev_index < len(ids):
+            return ids[dev_index]
+    return str(dev_index)
+
+
+def cpu_baseline(w, seconds_hint=20.0):
+    """Time the fp64 oracle, as it stands, on a bounded sample of the workload:
+    the first `heads` heads, full sequence, both directions, one thread per head."""
+    import oracle
+    cores = max(1, len(os.sched_getaffinity(0)))
+    heads = min(w.G, cores)
+    p = inputs.gen_params(w)
+    data = []
+    for g in range(heads):
+        data.append({n: inputs.widen(inputs.gen_head(w, n, g, p), w.dtype) for n in ("Qx", "Kx", "V")})
+    Q = np.stack([x["Qx"] for x in data])[None]
+    Kx = np.stack([x["Kx"] for x in data])[None]
+    V = np.stack([x["V"] for x in data])[None]
+    hs = [g % w.H for g in range(heads)]
+    mu, rho, al = p["mu"][hs], p["rho"][hs], p["alpha"][hs]
+    t0 = time.perf_counter()
+    oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, False, threads=heads)
+    oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, True, threads=heads)
+    dt = time.perf_counter() - t0
+    units = 2 * heads * w.N
+    return {"value": units / dt, "unit": "tokens·heads/s", "cores": heads, "kind": "oracle",
+            "sample": f"{heads} heads x N={w.N} of the {w.name} workload, bidirectional + causal "
+                      f"(fp64 C oracle, one thread per head), {dt:.2f} s wall"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    w = inputs.WORKLOADS[args.workload]
+    import oracle
+    oracle.build()
+    cores = max(1, len(os.sched_getaffinity(0)))
+    heads = min(w.G, cores)
+    p = inputs.gen_params(w)
+    data = [{n: inputs.widen(inputs.gen_head(w, n, g, p), w.dtype) for n in ("Qx", "Kx", "V")}
+            for g in range(heads)]
+    Q = np.stack([x["Qx"] for x in data])[None]
+    Kx = np.stack([x["Kx"] for x in data])[None]
+    V = np.stack([x["V"] for x in data])[None]
+    hs = [g % w.H for g in range(heads)]
+    mu, rho, al = p["mu"][hs], p["rho"][hs], p["alpha"][hs]
+
+    def step():
+        oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, False, threads=heads)
+        oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, True, threads=heads)
+
+    steps = args.steps if args.steps is not None else 3
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    value = 2 * heads * w.N / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens·heads/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                                        "K": w.K, "dv": w.dv, "step": "bidirectional + causal forward",
+                                        "sample_heads": heads},
+        "cpu_baseline": {"value": value, "unit": "tokens·heads/s", "cores": heads, "kind": "oracle",
+                         "sample": f"each step: {heads} heads x N={w.N}, bidirectional + causal"},
+        "e2e": {"value": value, "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+    import gaussian_mixture_latent_gb300 as gma
+    from gaussian_mixture_latent_gb300 import _build
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    w = inputs.WORKLOADS[args.workload]
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    # two resident input sets (each larger than L2), generated on the host
+    def make_set(seed):
+        ws = w.replace(seed=seed)
+        x = inputs.gen_all(ws)
+        def t(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(a).to(dev)
+        return {k: t(v) for k, v in x.items()}, x
+
+    sets = [make_set(0), make_set(1)]
+    dsets = [s[0] for s in sets]
+    outs = {c: torch.empty((w.B, w.H, w.N, w.dv), dtype=tdt, device=dev) for c in (False, True)}
+    plan = {c: gma.gma_forward_plan(w.B, w.H, w.N, w.d, w.K, w.dv, tdt, causal=c) for c in (False, True)}
+    stream = torch.cuda.current_stream()
+
+    def forward(x, causal, events=None):
+        return gma.gma_forward(x["Qx"], x["Kx"], x["V"], x["mu"], x["rho"], x["alpha"], eps=w.eps,
+                               causal=causal, out=outs[causal], var_floor=w.var_floor,
+                               events=events)
+
+    # warm-up with every launch bracketed by events: finds the dominant kernel
+    per = {}
+    for it in range(max(3, args.warmup)):
+        evs = {}
+        for c in (False, True):
+            evs[c] = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(plan[c]))]
+            forward(dsets[it % 2], c, evs[c])
+        torch.cuda.synchronize()
+        if it >= 1:
+            for c in (False, True):
+                for i, name in enumerate(plan[c]):
+                    per.setdefault((c, name), []).append(evs[c][2 * i].elapsed_time(evs[c][2 * i + 1]))
+    status = gma.gma_get_status()
+    if status:
+        raise RuntimeError("device status after warm-up: " + gma.gma_status_string(status))
+    share = {k: statistics.median(v) for k, v in per.items()}
+    dom_c, dom_name = max(share, key=share.get)
+    dom_idx = plan[dom_c].index(dom_name)
+
+    # step count
+    step_ms_est = sum(share.values())
+    steps = args.steps if args.steps is not None else int(min(5000, max(20, 3000.0 / max(step_ms_est, 1e-3))))
+
+    # timed region: events only around the dominant kernel
+    dom_events = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                  for _ in range(steps)]
+    sampler = ClockSampler(gpu_id_for(local))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for it in range(steps):
+        x = dsets[it % 2]
+        for c in (False, True):
+            if c == dom_c:
+                evs = [None] * (2 * len(plan[c]))
+                evs[2 * dom_idx], evs[2 * dom_idx + 1] = dom_events[it]
+                forward(x, c, evs)
+            else:
+                forward(x, c)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms_per_step = t_start.elapsed_time(t_end) / steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_per_step = float(tt.item())
+        dist.barrier()
+    status = gma.gma_get_status()
+    if status:
+        raise RuntimeError("device status after timed region: " + gma.gma_status_string(status))
+    dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom_events)
+    units_per_step = 2 * w.G * w.N
+    value = world * units_per_step / (ms_per_step / 1e3)
+
+    # roofline of the dominant kernel
+    pk = peaks()
+    bound, amount, unit = accounting.kernel_work(dom_name, w.G, w.N, w.d, w.K, w.dv, w.dtype,
+                                                 w.dtype, H=w.H)
+    if bound == "hbm":
+        achieved = amount / (dom_ms / 1e3) / 1e9
+        peak, runit = pk["hbm_gbs"], "GB/s"
+    elif bound == "tensor":
+        achieved = amount / (dom_ms / 1e3) / 1e12
+        peak, runit = pk["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved = amount / (dom_ms / 1e3) / 1e12
+        peak, runit = fp32_simt_peak_tflops(pk["sm_max_mhz"]), "TFLOP/s"
+        bound = "alu"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
+                "frac": achieved / peak, "traffic": known_traffic(dom_name), "kernel": dom_name,
+                "kernel_ms": dom_ms, "peak_source": pk["source"] if bound != "alu" else
+                "derived: 152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}
+
+    # whole-path roofline of one step (both directions)
+    alg_bytes = 2 * accounting.algorithmic_bytes(w.G, w.N, w.d, w.K, w.dv, w.dtype, w.dtype, H=w.H)
+    alg_flops = 2 * accounting.algorithmic_flops(w.G, w.N, w.d, w.K, w.dv)
+    t_roof = max(alg_bytes / (pk["hbm_gbs"] * 1e9), alg_flops / (pk["bf16_tflops"] * 1e12))
+    path = {"algorithmic_bytes_per_step": alg_bytes, "algorithmic_flops_per_step": alg_flops,
+            "roofline_ms_per_step": t_roof * 1e3, "frac": t_roof * 1e3 / ms_per_step,
+            "per_kernel_ms": {f"{'causal' if c else 'bidir'}:{n}": round(v, 5) for (c, n), v in share.items()}}
+
+    # end to end through the public API from pinned host memory
+    e2e = None
+    if args.e2e_steps > 0:
+        host = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in dsets]
+        hout = {c: torch.empty(outs[c].shape, dtype=tdt, pin_memory=True) for c in (False, True)}
+        staging = {k: torch.empty_like(v) for k, v in dsets[0].items()}
+        h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+        d2h = sum(v.numel() * v.element_size() for v in hout.values())
+
+        def e2e_step(i):
+            for k, v in host[i % 2].items():
+                staging[k].copy_(v, non_blocking=True)
+            for c in (False, True):
+                forward(staging, c)
+                hout[c].copy_(outs[c], non_blocking=True)
+
+        for i in range(2):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / args.e2e_steps
+        e2e = {"value": world * units_per_step / (e2e_ms / 1e3), "unit": "tokens·heads/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        launches = steps * (len(plan[False]) + len(plan[True]))
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens·heads/s", "n_gpus": world,
+            "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K,
+                       "dv": w.dv, "step": "bidirectional + causal forward",
+                       "l2": "two alternating input sets of %d MB each (> 129 MB L2)" %
+                             (sum(v.numel() * v.element_size() for v in dsets[0].values()) // 2**20),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline, "path_roofline": path, "clocks": clocks,
+            "gpu_launches": launches, "kernels": {"bidir": plan[False], "causal": plan[True]},
+            "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_gpu(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

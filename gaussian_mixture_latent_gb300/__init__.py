@@ -1,0 +1,247 @@
+"""GB300 (sm_103a) Gaussian Mixture Attention forward -- Python binding.
+
+A thin ``ctypes`` layer over the C ABI in ``include/gma.h`` (library
+``libgma.so`` next to this file).  Functions carry the C names; they only
+check and marshal torch tensors (device pointers, sizes, the current CUDA
+stream).  Every step of the computation runs in the library's CUDA kernels:
+there is no Python or CPU implementation behind these calls, and they raise
+if the library has not been built.
+
+Method: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+Probabilistic Latent Routing" (Huang & Raza, 2026), sections 3.2-3.6.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "GmaError", "gma_desc", "gma_workspace_size", "gma_workspace_init", "gma_forward",
+    "gma_forward_ex", "gma_forward_plan",
+    "gma_responsibilities", "gma_get_status", "gma_status_string", "gma_version",
+    "Workspace", "library_path",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libgma.so")
+_lib = None
+
+GMA_F32, GMA_BF16 = 0, 1
+_DTYPES = {torch.float32: GMA_F32, torch.bfloat16: GMA_BF16}
+_STATUS = {0: "GMA_OK", 1: "GMA_ERR_INVALID_ARG", 2: "GMA_ERR_UNSUPPORTED",
+           3: "GMA_ERR_WORKSPACE", 4: "GMA_ERR_CUDA", 5: "GMA_ERR_TIMEOUT"}
+
+
+class GmaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {gma_status_string(code)}")
+        self.code = code
+
+
+class gma_desc(ctypes.Structure):
+    """Mirror of ``gma_desc`` in include/gma.h."""
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int),
+                ("d", ctypes.c_int), ("K", ctypes.c_int), ("dv", ctypes.c_int),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("var_floor", ctypes.c_float), ("chunk", ctypes.c_int)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            "libgma.so is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(the GMA forward has no fallback implementation)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, sz, i, f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+    dp = ctypes.POINTER(gma_desc)
+    lib.gma_workspace_size.argtypes = [dp, i, ctypes.POINTER(sz)]
+    lib.gma_workspace_init.argtypes = [vp, sz, vp]
+    lib.gma_forward.argtypes = [dp, vp, vp, vp, vp, vp, vp, f, i, vp, vp, sz, vp]
+    lib.gma_forward_ex.argtypes = [dp, vp, vp, vp, vp, vp, vp, f, i, vp, vp, sz, vp,
+                                   ctypes.POINTER(vp), i]
+    lib.gma_forward_plan.argtypes = [dp, i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_char_p), i]
+    lib.gma_responsibilities.argtypes = [dp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.gma_get_status.argtypes = [vp, vp]
+    lib.gma_status_string.argtypes = [i]
+    lib.gma_status_string.restype = ctypes.c_char_p
+    lib.gma_version.argtypes = []
+    for fn in (lib.gma_workspace_size, lib.gma_workspace_init, lib.gma_forward,
+               lib.gma_forward_ex, lib.gma_forward_plan, lib.gma_responsibilities, lib.gma_get_status, lib.gma_version):
+        fn.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def gma_status_string(code: int) -> str:
+    try:
+        return _load().gma_status_string(int(code)).decode()
+    except RuntimeError:
+        return _STATUS.get(int(code), "unknown gma_status")
+
+
+def gma_version() -> int:
+    return _load().gma_version()
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _make_desc(B, H, N, d, K, dv, in_dtype, out_dtype, var_floor, chunk) -> gma_desc:
+    return gma_desc(B, H, N, d, K, dv, _DTYPES[in_dtype], _DTYPES[out_dtype], float(var_floor),
+                    int(chunk))
+
+
+def gma_workspace_size(desc: gma_desc, causal: bool) -> int:
+    n = ctypes.c_size_t(0)
+    rc = _load().gma_workspace_size(ctypes.byref(desc), int(bool(causal)), ctypes.byref(n))
+    if rc:
+        raise GmaError(rc, "gma_workspace_size")
+    return n.value
+
+
+def gma_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    rc = _load().gma_workspace_init(_ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    if rc:
+        raise GmaError(rc, "gma_workspace_init")
+
+
+class Workspace:
+    """A device workspace buffer that grows on demand (bytes, uint8)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, nbytes: int, stream=None) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            gma_workspace_init(self.buf, stream)
+        return self.buf
+
+
+_default_ws: dict = {}
+
+
+def _workspace_for(device, nbytes, workspace, stream):
+    if workspace is not None:
+        if workspace.numel() < nbytes:
+            raise GmaError(3, "gma_forward")
+        return workspace
+    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    ws = _default_ws.setdefault(key, Workspace(torch.device("cuda", key)))
+    return ws.get(nbytes, stream)
+
+
+def _check(t: torch.Tensor, name: str, shape, dtypes):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def gma_forward_plan(B, H, N, d, K, dv, dtype=torch.bfloat16, causal=False, out_dtype=None,
+                     var_floor: float = 1e-4, chunk: int = 0):
+    """Kernel names gma_forward launches for this problem (nothing runs)."""
+    desc = _make_desc(B, H, N, d, K, dv, dtype, out_dtype or dtype, var_floor, chunk)
+    n = ctypes.c_int(0)
+    names = (ctypes.c_char_p * 16)()
+    rc = _load().gma_forward_plan(ctypes.byref(desc), int(bool(causal)), ctypes.byref(n), names, 16)
+    if rc:
+        raise GmaError(rc, "gma_forward_plan")
+    return [names[i].decode() for i in range(min(n.value, 16))]
+
+
+def gma_forward_ex(*args, events=None, **kw):
+    """gma_forward with torch.cuda.Event objects recorded around each kernel launch
+    (events[2i] before launch i, events[2i+1] after it)."""
+    return gma_forward(*args, events=events, **kw)
+
+
+def gma_forward(Qx, Kx, V, mu, rho, pi_logits, eps: float = 1e-6, causal: bool = False,
+                out=None, workspace=None, var_floor: float = 1e-4, out_dtype=None,
+                chunk: int = 0, stream=None, events=None):
+    """GMA forward (Eq. 5-8; causal Eq. 6b, 8b).  Qx, Kx [B,H,N,d], V [B,H,N,dv]
+    (float32 or bfloat16), mu, rho [H,K,d], pi_logits [H,K] float32 -> out [B,H,N,dv]."""
+    B, H, N, d = Qx.shape
+    dv = V.shape[-1]
+    K = mu.shape[1]
+    in_dtype = Qx.dtype
+    out_dtype = out_dtype or in_dtype
+    _check(Qx, "Qx", (B, H, N, d), (torch.float32, torch.bfloat16))
+    _check(Kx, "Kx", (B, H, N, d), (in_dtype,))
+    _check(V, "V", (B, H, N, dv), (in_dtype,))
+    _check(mu, "mu", (H, K, d), (torch.float32,))
+    _check(rho, "rho", (H, K, d), (torch.float32,))
+    _check(pi_logits, "pi_logits", (H, K), (torch.float32,))
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=out_dtype, device=Qx.device)
+    _check(out, "out", (B, H, N, dv), (out_dtype,))
+    desc = _make_desc(B, H, N, d, K, dv, in_dtype, out_dtype, var_floor, chunk)
+    nbytes = gma_workspace_size(desc, causal)
+    ws = _workspace_for(Qx.device, nbytes, workspace, stream)
+    common = (ctypes.byref(desc), _ptr(Qx), _ptr(Kx), _ptr(V), _ptr(mu), _ptr(rho),
+              _ptr(pi_logits), float(eps), int(bool(causal)), _ptr(out), _ptr(ws), ws.numel(),
+              _stream_ptr(stream))
+    if events is None:
+        rc = _load().gma_forward(*common)
+    else:
+        handles = (ctypes.c_void_p * len(events))(*[e.cuda_event if e is not None else None
+                                                    for e in events])
+        rc = _load().gma_forward_ex(*common, handles, len(events))
+    if rc:
+        raise GmaError(rc, "gma_forward")
+    return out
+
+
+def gma_responsibilities(X, mu, rho, pi_logits, var_floor: float = 1e-4, out=None,
+                         workspace=None, stream=None):
+    """Responsibilities (Eq. 3) of the rows of X [B,H,N,d] -> float32 [B,H,N,K]."""
+    B, H, N, d = X.shape
+    K = mu.shape[1]
+    _check(X, "X", (B, H, N, d), (torch.float32, torch.bfloat16))
+    _check(mu, "mu", (H, K, d), (torch.float32,))
+    _check(rho, "rho", (H, K, d), (torch.float32,))
+    _check(pi_logits, "pi_logits", (H, K), (torch.float32,))
+    if out is None:
+        out = torch.empty((B, H, N, K), dtype=torch.float32, device=X.device)
+    _check(out, "out", (B, H, N, K), (torch.float32,))
+    desc = _make_desc(B, H, N, d, K, 1, X.dtype, X.dtype, var_floor, 0)
+    nbytes = gma_workspace_size(desc, False)
+    ws = _workspace_for(X.device, nbytes, workspace, stream)
+    rc = _load().gma_responsibilities(ctypes.byref(desc), _ptr(X), _ptr(mu), _ptr(rho),
+                                      _ptr(pi_logits), _ptr(out), _ptr(ws), ws.numel(),
+                                      _stream_ptr(stream))
+    if rc:
+        raise GmaError(rc, "gma_responsibilities")
+    return out
+
+
+def gma_get_status(workspace=None, stream=None) -> int:
+    """Synchronise, read and clear the device status word; returns the gma_status code."""
+    if workspace is None:
+        key = torch.cuda.current_device()
+        if key not in _default_ws or _default_ws[key].buf is None:
+            return 0
+        workspace = _default_ws[key].buf
+    return _load().gma_get_status(_ptr(workspace), _stream_ptr(stream))

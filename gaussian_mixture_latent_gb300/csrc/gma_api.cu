@@ -1,0 +1,225 @@
+// Host side of the C ABI declared in include/gma.h: argument validation,
+// workspace sizing and carving, and the launch plan of each request.
+//
+// A request becomes a Plan: an ordered list of named kernel launches on one
+// stream.  gma_forward() runs the plan; gma_forward_ex() runs it with
+// caller-owned CUDA events recorded around each launch (per-kernel timing);
+// gma_forward_plan() reports the launches without running anything.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+
+#include "gma_internal.h"
+
+namespace gma {
+namespace {
+
+constexpr size_t kMaxDynSmem = 227 * 1024;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gma_status validate_desc(const gma_desc *d) {
+    if (!d) return GMA_ERR_INVALID_ARG;
+    if (d->B <= 0 || d->H <= 0 || d->N < 0) return GMA_ERR_INVALID_ARG;
+    if (d->d <= 0 || d->K <= 0 || d->dv <= 0) return GMA_ERR_INVALID_ARG;
+    if (d->in_dtype != GMA_F32 && d->in_dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (d->out_dtype != GMA_F32 && d->out_dtype != GMA_BF16) return GMA_ERR_INVALID_ARG;
+    if (!(d->var_floor > 0.f) || !std::isfinite(d->var_floor)) return GMA_ERR_INVALID_ARG;
+    if (d->chunk < 0) return GMA_ERR_INVALID_ARG;
+    if (d->d > 256 || d->K > 256 || d->dv > 256) return GMA_ERR_UNSUPPORTED;
+    // Grid dimensions and row counts are 32-bit.
+    if ((long long)d->B * d->H > 65535 || (long long)d->B * d->H * d->N > (1LL << 31))
+        return GMA_ERR_UNSUPPORTED;
+    return GMA_OK;
+}
+
+Problem make_problem(const gma_desc *d, int causal, float eps) {
+    Problem p{};
+    p.B = d->B; p.H = d->H; p.N = d->N; p.d = d->d; p.K = d->K; p.dv = d->dv;
+    p.G = d->B * d->H;
+    p.in_dtype = d->in_dtype; p.out_dtype = d->out_dtype;
+    p.var_floor = d->var_floor; p.eps = eps; p.causal = causal ? 1 : 0; p.chunk = d->chunk;
+    return p;
+}
+
+struct Launch {
+    const char *name;
+    std::function<cudaError_t(cudaStream_t)> run;
+};
+
+struct Plan {
+    static constexpr int kMax = 16;
+    Launch step[kMax];
+    int n = 0;
+    size_t workspace = 0;
+    void add(const char *name, std::function<cudaError_t(cudaStream_t)> f) { step[n++] = {name, std::move(f)}; }
+};
+
+struct Args {
+    const void *Qx, *Kx, *V;
+    const float *mu, *rho, *alpha;
+    void *out;
+    char *ws;
+};
+
+// Builds the launch list.  With args == nullptr only names and sizes are filled.
+gma_status build_forward_plan(const Problem &p, const Args *a, Plan &plan) {
+    const SimtLayout L = simt_layout(p);
+    if (p.causal && simt_causal_smem(p) > kMaxDynSmem) return GMA_ERR_UNSUPPORTED;
+    plan.workspace = L.total;
+    Args z{};
+    const Args A = a ? *a : z;
+    char *ws = A.ws;
+    float *lam = reinterpret_cast<float *>(ws + L.lam);
+    float *cdir = reinterpret_cast<float *>(ws + L.cdir);
+    plan.add("simt_params", [=](cudaStream_t s) { return simt_params(p, A.rho, A.alpha, lam, cdir, s); });
+    plan.add("simt_gamma_q", [=](cudaStream_t s) {
+        return simt_gamma(p, A.Qx, A.mu, lam, cdir, reinterpret_cast<float *>(ws + L.gq), s); });
+    plan.add("simt_gamma_k", [=](cudaStream_t s) {
+        return simt_gamma(p, A.Kx, A.mu, lam, cdir, reinterpret_cast<float *>(ws + L.gk), s); });
+    plan.add("simt_write", [=](cudaStream_t s) { return simt_write(p, A.V, ws, L, s); });
+    plan.add("simt_reduce", [=](cudaStream_t s) { return simt_reduce(p, ws, L, s); });
+    if (p.causal)
+        plan.add("simt_causal_chunk", [=](cudaStream_t s) { return simt_causal(p, A.V, ws, L, A.out, s); });
+    else
+        plan.add("simt_read", [=](cudaStream_t s) { return simt_read(p, ws, L, A.out, s); });
+    return GMA_OK;
+}
+
+gma_status run_plan(const Plan &plan, cudaStream_t s, void *const *events, int n_events) {
+    for (int i = 0; i < plan.n; ++i) {
+        if (events && 2 * i + 1 < n_events && events[2 * i])
+            if (cudaEventRecord(static_cast<cudaEvent_t>(events[2 * i]), s) != cudaSuccess) return GMA_ERR_CUDA;
+        if (plan.step[i].run(s) != cudaSuccess) return GMA_ERR_CUDA;
+        if (events && 2 * i + 1 < n_events && events[2 * i + 1])
+            if (cudaEventRecord(static_cast<cudaEvent_t>(events[2 * i + 1]), s) != cudaSuccess) return GMA_ERR_CUDA;
+    }
+    return GMA_OK;
+}
+
+gma_status check_forward_args(const gma_desc *desc, const void *Qx, const void *Kx, const void *V,
+                              const float *mu, const float *rho, const float *pi_logits, float eps,
+                              int causal, void *out, void *workspace) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return GMA_ERR_INVALID_ARG;
+    if (!mu || !rho || !pi_logits) return GMA_ERR_INVALID_ARG;
+    if (desc->N > 0 && (!Qx || !Kx || !V || !out)) return GMA_ERR_INVALID_ARG;
+    const void *ptrs[] = {Qx, Kx, V, out, mu, rho, pi_logits, workspace};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
+    return GMA_OK;
+}
+
+}  // namespace
+}  // namespace gma
+
+using namespace gma;
+
+extern "C" {
+
+gma_status gma_workspace_size(const gma_desc *desc, int causal, size_t *bytes) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!bytes) return GMA_ERR_INVALID_ARG;
+    Plan plan;
+    st = build_forward_plan(make_problem(desc, causal, 0.f), nullptr, plan);
+    if (st != GMA_OK) return st;
+    *bytes = plan.workspace;
+    return GMA_OK;
+}
+
+gma_status gma_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace || workspace_bytes < kHeaderBytes) return GMA_ERR_WORKSPACE;
+    return cudaMemsetAsync(workspace, 0, kHeaderBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GMA_OK : GMA_ERR_CUDA;
+}
+
+gma_status gma_forward_ex(const gma_desc *desc, const void *Qx, const void *Kx, const void *V,
+                          const float *mu, const float *rho, const float *pi_logits, float eps,
+                          int causal, void *out, void *workspace, size_t workspace_bytes,
+                          void *stream, void *const *events, int n_events) {
+    gma_status st = check_forward_args(desc, Qx, Kx, V, mu, rho, pi_logits, eps, causal, out, workspace);
+    if (st != GMA_OK) return st;
+    const Problem p = make_problem(desc, causal, eps);
+    const Args a{Qx, Kx, V, mu, rho, pi_logits, out, static_cast<char *>(workspace)};
+    Plan plan;
+    st = build_forward_plan(p, &a, plan);
+    if (st != GMA_OK) return st;
+    if (!workspace || workspace_bytes < plan.workspace) return GMA_ERR_WORKSPACE;
+    if (p.N == 0) return GMA_OK;
+    return run_plan(plan, static_cast<cudaStream_t>(stream), events, n_events);
+}
+
+gma_status gma_forward(const gma_desc *desc, const void *Qx, const void *Kx, const void *V,
+                       const float *mu, const float *rho, const float *pi_logits, float eps,
+                       int causal, void *out, void *workspace, size_t workspace_bytes,
+                       void *stream) {
+    return gma_forward_ex(desc, Qx, Kx, V, mu, rho, pi_logits, eps, causal, out, workspace,
+                          workspace_bytes, stream, nullptr, 0);
+}
+
+gma_status gma_forward_plan(const gma_desc *desc, int causal, int *n_launches, const char **names,
+                            int capacity) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!n_launches || causal < 0 || causal > 1) return GMA_ERR_INVALID_ARG;
+    Plan plan;
+    st = build_forward_plan(make_problem(desc, causal, 0.f), nullptr, plan);
+    if (st != GMA_OK) return st;
+    *n_launches = desc->N > 0 ? plan.n : 0;
+    for (int i = 0; names && i < capacity && i < plan.n; ++i) names[i] = plan.step[i].name;
+    return GMA_OK;
+}
+
+gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float *mu,
+                                const float *rho, const float *pi_logits, float *gamma_out,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!mu || !rho || !pi_logits) return GMA_ERR_INVALID_ARG;
+    if (desc->N > 0 && (!X || !gamma_out)) return GMA_ERR_INVALID_ARG;
+    const void *ptrs[] = {X, gamma_out, mu, rho, pi_logits, workspace};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
+    const Problem p = make_problem(desc, 0, 0.f);
+    const SimtLayout L = simt_layout(p);
+    if (!workspace || workspace_bytes < L.total) return GMA_ERR_WORKSPACE;
+    if (p.N == 0) return GMA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    float *lam = reinterpret_cast<float *>(ws + L.lam);
+    float *cdir = reinterpret_cast<float *>(ws + L.cdir);
+    if (simt_params(p, rho, pi_logits, lam, cdir, s) != cudaSuccess) return GMA_ERR_CUDA;
+    return simt_gamma(p, X, mu, lam, cdir, gamma_out, s) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
+gma_status gma_get_status(void *workspace, void *stream) {
+    if (!workspace) return GMA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return GMA_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return GMA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GMA_ERR_CUDA;
+    if (word & kDevErrTimeout) return GMA_ERR_TIMEOUT;
+    return GMA_OK;
+}
+
+const char *gma_status_string(gma_status status) {
+    switch (status) {
+        case GMA_OK: return "GMA_OK";
+        case GMA_ERR_INVALID_ARG: return "GMA_ERR_INVALID_ARG: invalid argument";
+        case GMA_ERR_UNSUPPORTED: return "GMA_ERR_UNSUPPORTED: shape or dtype outside the supported range";
+        case GMA_ERR_WORKSPACE: return "GMA_ERR_WORKSPACE: workspace missing or too small";
+        case GMA_ERR_CUDA: return "GMA_ERR_CUDA: CUDA runtime error or failed launch";
+        case GMA_ERR_TIMEOUT: return "GMA_ERR_TIMEOUT: a device-side bounded wait ran out";
+    }
+    return "unknown gma_status";
+}
+
+int gma_version(void) { return 100; }
+
+}  // extern "C"

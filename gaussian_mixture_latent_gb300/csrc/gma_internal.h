@@ -1,0 +1,56 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/gma.h"
+
+namespace gma {
+
+// Device status word bits (first 4 bytes of the workspace header).
+enum : unsigned {
+    kDevErrTimeout = 1u,     // a bounded mbarrier / flag wait ran out
+};
+
+constexpr size_t kHeaderBytes = 256;
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+// Problem geometry after validation.
+struct Problem {
+    int B, H, N, d, K, dv, G;
+    gma_dtype in_dtype, out_dtype;
+    float var_floor;
+    float eps;
+    int causal;
+    int chunk;
+};
+
+// ----- workspace carving (byte offsets from the workspace base) -----
+struct SimtLayout {
+    size_t lam, cdir;            // parameter prologue outputs
+    size_t gq, gk;               // materialised responsibilities [G][N][K] f32
+    size_t part;                 // [G][P][K][dv+1] f32 partial / segment totals
+    size_t mem;                  // [G][P or 1][K][dv+1] f32 reduced memory / exclusive prefixes
+    size_t total;
+    int P;                       // N-splits (bidirectional) or segments (causal)
+};
+SimtLayout simt_layout(const Problem &p);
+
+// ----- SIMT (CUDA-core, fp32) path: gma_simt.cu -----
+cudaError_t simt_params(const Problem &p, const float *rho, const float *alpha, float *lam,
+                        float *cdir, cudaStream_t s);
+cudaError_t simt_gamma(const Problem &p, const void *X, const float *mu, const float *lam,
+                       const float *cdir, float *gamma, cudaStream_t s);
+cudaError_t simt_write(const Problem &p, const void *V, char *ws, const SimtLayout &L,
+                       cudaStream_t s);
+cudaError_t simt_reduce(const Problem &p, char *ws, const SimtLayout &L, cudaStream_t s);
+cudaError_t simt_read(const Problem &p, char *ws, const SimtLayout &L, void *out, cudaStream_t s);
+cudaError_t simt_causal(const Problem &p, const void *V, char *ws, const SimtLayout &L, void *out,
+                        cudaStream_t s);
+size_t simt_causal_smem(const Problem &p);
+
+}  // namespace gma

@@ -1,0 +1,142 @@
+/*
+ * gma.h -- C ABI of the GB300 (sm_103a) Gaussian Mixture Attention forward.
+ *
+ * Method: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+ * Probabilistic Latent Routing" (Huang & Raza, 2026).  Per head, with
+ * routing vectors Qx, Kx [N, d], values V [N, dv] and K diagonal Gaussian
+ * components (means mu [K, d], variance parameters rho [K, d], prior logits
+ * alpha [K]):
+ *
+ *   sigma^2 = softplus(rho) + var_floor                    (section 3.6, Eq. 14)
+ *   pi      = softmax(alpha)                               (section 3.6, Eq. 15)
+ *   Gamma^Q, Gamma^K = posterior responsibilities of the rows of Qx, Kx
+ *                                                          (section 3.2, Eq. 3; Eq. 16 / 3b)
+ *   bidirectional:  Vt = Gamma^K^T V,  Z = Gamma^K^T 1     (section 3.3, Eq. 5-6)
+ *                   O  = Gamma^Q Vt / (Gamma^Q Z + eps)    (section 3.3, Eq. 7-8)
+ *   causal:         prefix memories over j <= i           (section 3.5, Eq. 6b)
+ *                   O_i = gamma^Q_i Vt^(i) / (gamma^Q_i Z^(i) + eps)   (Eq. 8b)
+ *
+ * Layout of every tensor argument (row-major, contiguous, no padding):
+ *   Qx, Kx     [B, H, N, d]   in_dtype
+ *   V          [B, H, N, dv]  in_dtype
+ *   out        [B, H, N, dv]  out_dtype
+ *   mu, rho    [H, K, d]      float32   (one mixture per head, shared by the batch)
+ *   pi_logits  [H, K]         float32
+ * All pointers are DEVICE pointers (CUDA global memory of the current device)
+ * unless a function says otherwise; base addresses must be 16-byte aligned.
+ * `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *
+ * Ownership: the caller owns every buffer, including the workspace.  The
+ * library allocates no device memory, keeps no global state between calls
+ * and is re-entrant; calls on different streams with different workspaces
+ * may run concurrently.
+ *
+ * Asynchrony and errors: argument errors are returned synchronously and
+ * launch nothing.  A failed kernel launch returns GMA_ERR_CUDA.  Errors found
+ * on the device (a bounded wait that ran out) are posted to the status word
+ * at the start of the workspace and read back with gma_get_status().  No
+ * function except gma_get_status() synchronises.
+ */
+#ifndef GMA_H_
+#define GMA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GMA_OK = 0,
+    GMA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer      */
+    GMA_ERR_UNSUPPORTED = 2,   /* valid request outside the implemented range     */
+    GMA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required      */
+    GMA_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed     */
+    GMA_ERR_TIMEOUT = 5        /* a device-side bounded wait ran out              */
+} gma_status;
+
+typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype;
+
+typedef struct {
+    int B, H, N;        /* batch, heads, sequence length (N >= 0)                 */
+    int d;              /* routing dimension d_r, 1..256                          */
+    int K;              /* number of Gaussian components, 1..256                  */
+    int dv;             /* value dimension, 1..256                                */
+    gma_dtype in_dtype; /* dtype of Qx, Kx and V                                  */
+    gma_dtype out_dtype;/* dtype of out                                           */
+    float var_floor;    /* eps_sigma of Eq. 14 (> 0)                              */
+    int chunk;          /* causal chunk length in rows; 0 = library's choice      */
+} gma_desc;
+
+/*
+ * Size in bytes of the device workspace that gma_forward() needs for this
+ * problem and direction (causal = 0 bidirectional, 1 causal).  Pure host
+ * computation.  Before its first use a workspace's first 256 bytes must be
+ * zero (gma_workspace_init() does that); later calls keep them zero unless
+ * a device error was posted.
+ */
+gma_status gma_workspace_size(const gma_desc *desc, int causal, size_t *bytes);
+
+/* Zero the workspace header (the device status word) on `stream`. */
+gma_status gma_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The GMA forward (section 3.3, Eq. 5-8; causal: section 3.5, Eq. 6b, 8b),
+ * with the parameterisation of section 3.6 (Eq. 14-15) and the
+ * responsibilities of section 3.2 (Eq. 3).  Writes out [B, H, N, dv].
+ * eps >= 0 is added once to each row's denominator.  Enqueued on `stream`;
+ * returns without synchronising.  Inputs are not modified.  `out` must not
+ * overlap any input or the workspace.
+ */
+gma_status gma_forward(const gma_desc *desc, const void *Qx, const void *Kx, const void *V,
+                       const float *mu, const float *rho, const float *pi_logits, float eps,
+                       int causal, void *out, void *workspace, size_t workspace_bytes,
+                       void *stream);
+
+/*
+ * gma_forward() with per-launch timing: when `events` is not NULL it holds
+ * n_events cudaEvent_t handles (as void*, created by the caller); the
+ * library records events[2i] on `stream` just before its i-th kernel launch
+ * and events[2i+1] just after it, for every i with 2i+1 < n_events.  NULL
+ * entries are skipped.  Everything else is as for gma_forward().
+ */
+gma_status gma_forward_ex(const gma_desc *desc, const void *Qx, const void *Kx, const void *V,
+                          const float *mu, const float *rho, const float *pi_logits, float eps,
+                          int causal, void *out, void *workspace, size_t workspace_bytes,
+                          void *stream, void *const *events, int n_events);
+
+/*
+ * The kernel launches gma_forward() makes for this problem, without running
+ * anything: their number in *n_launches (0 when N == 0) and, when `names` is
+ * not NULL, the first `capacity` kernel names (static strings).
+ */
+gma_status gma_forward_plan(const gma_desc *desc, int causal, int *n_launches, const char **names,
+                            int capacity);
+
+/*
+ * Responsibilities of the rows of X [B, H, N, d] (section 3.2, Eq. 3, in the
+ * softmax form of Eq. 16 / 3b), written as float32 to gamma_out [B, H, N, K].
+ * A diagnostic export: the forward never writes Gamma to memory.  Needs the
+ * workspace of gma_workspace_size(desc, 0, ...).
+ */
+gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float *mu,
+                                const float *rho, const float *pi_logits, float *gamma_out,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, reads the device status word of `workspace`, clears
+ * it, and returns GMA_OK or the device error that was posted (GMA_ERR_TIMEOUT).
+ */
+gma_status gma_get_status(void *workspace, void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *gma_status_string(gma_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int gma_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GMA_H_ */

@@ -1,0 +1,87 @@
+"""The C ABI library loads and exports every entry point include/gma.h declares;
+host-only argument checks return the documented codes (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import gaussian_mixture_latent_gb300 as gma
+    return gma._load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gma.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gma_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gma_forward", "gma_workspace_size", "gma_responsibilities",
+                     "gma_get_status", "gma_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_has_sm103a_code_only():
+    import subprocess
+    import gaussian_mixture_latent_gb300 as gma
+    r = subprocess.run(["cuobjdump", "--list-elf", gma.library_path()], capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    archs = set(re.findall(r"sm_\d+a?", r.stdout))
+    assert archs == {"sm_103a"}, archs
+
+
+def _desc(**kw):
+    import gaussian_mixture_latent_gb300 as gma
+    base = dict(B=2, H=3, N=100, d=16, K=8, dv=32, in_dtype=1, out_dtype=1, var_floor=1e-4, chunk=0)
+    base.update(kw)
+    return gma.gma_desc(**base)
+
+
+def test_workspace_size_and_argument_errors(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.gma_workspace_size(ctypes.byref(_desc()), 0, ctypes.byref(n)) == 0
+    assert n.value >= 256
+    assert lib.gma_workspace_size(ctypes.byref(_desc()), 1, ctypes.byref(n)) == 0
+    assert lib.gma_workspace_size(None, 0, ctypes.byref(n)) == 1
+    for bad in (dict(B=0), dict(H=-1), dict(N=-5), dict(d=0), dict(K=0), dict(dv=0),
+                dict(in_dtype=7), dict(var_floor=0.0), dict(var_floor=float("nan")), dict(chunk=-1)):
+        assert lib.gma_workspace_size(ctypes.byref(_desc(**bad)), 0, ctypes.byref(n)) == 1, bad
+    for unsup in (dict(d=257), dict(K=300), dict(dv=1024)):
+        assert lib.gma_workspace_size(ctypes.byref(_desc(**unsup)), 0, ctypes.byref(n)) == 2, unsup
+
+
+def test_forward_rejects_bad_arguments_before_launching(lib):
+    import gaussian_mixture_latent_gb300 as gma
+    d = _desc()
+    p = ctypes.c_void_p(4096)      # never dereferenced: every case fails validation first
+    odd = ctypes.c_void_p(4100)    # not 16-byte aligned
+    f = lib.gma_forward
+    args = lambda **o: [ctypes.byref(o.get("desc", d)), o.get("Q", p), p, p, p, p, p,
+                        o.get("eps", 1e-6), o.get("causal", 0), o.get("out", p),
+                        o.get("ws", p), o.get("wsb", 1 << 40), None]
+    assert f(*args(desc=_desc(K=0))) == 1
+    assert f(*args(eps=-1.0)) == 1
+    assert f(*args(eps=float("inf"))) == 1
+    assert f(*args(causal=2)) == 1
+    assert f(*args(Q=None)) == 1
+    assert f(*args(Q=odd)) == 1
+    assert f(*args(out=None)) == 1
+    assert f(*args(ws=None)) == 3
+    assert f(*args(wsb=16)) == 3
+    assert gma.gma_status_string(3).startswith("GMA_ERR_WORKSPACE")
+    assert lib.gma_version() >= 100
