@@ -262,6 +262,13 @@ def run_gpu(args, rank, world, local):
     plan = {c: gma.gma_forward_plan(w.B, w.H, w.N, w.d, w.K, w.dv, tdt, causal=c) for c in (False, True)}
     stream = torch.cuda.current_stream()
 
+    def new_event():
+        # torch creates the CUDA event lazily at its first record(); the library
+        # re-records it at the launch it brackets.
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
+
     def forward(x, causal, events=None):
         return gma.gma_forward(x["Qx"], x["Kx"], x["V"], x["mu"], x["rho"], x["alpha"], eps=w.eps,
                                causal=causal, out=outs[causal], var_floor=w.var_floor,
@@ -272,7 +279,7 @@ def run_gpu(args, rank, world, local):
     for it in range(max(3, args.warmup)):
         evs = {}
         for c in (False, True):
-            evs[c] = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(plan[c]))]
+            evs[c] = [new_event() for _ in range(2 * len(plan[c]))]
             forward(dsets[it % 2], c, evs[c])
         torch.cuda.synchronize()
         if it >= 1:
@@ -291,8 +298,7 @@ def run_gpu(args, rank, world, local):
     steps = args.steps if args.steps is not None else int(min(5000, max(20, 3000.0 / max(step_ms_est, 1e-3))))
 
     # timed region: events only around the dominant kernel
-    dom_events = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-                  for _ in range(steps)]
+    dom_events = [[new_event(), new_event()] for _ in range(steps)]
     sampler = ClockSampler(gpu_id_for(local))
     if world > 1:
         import torch.distributed as dist
