@@ -123,6 +123,34 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
                                 const float *rho, const float *pi_logits, float *gamma_out,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the fixed scratch buffer gma_forward_noalloc() uses: 32 MiB. */
+#define GMA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * gma_forward() for callers that cannot allocate device memory.  The paper
+ * has no counterpart to this entry point; it exists for callers that must not
+ * call cudaMalloc -- code whose device memory is owned by another memory
+ * manager (a framework's caching allocator, a server's per-model budget) and
+ * latency-sensitive loops that cannot take cudaMalloc's device-wide
+ * synchronisation.
+ *
+ * Same arguments and results as gma_forward() minus the workspace: the
+ * library uses a scratch array of GMA_NOALLOC_SCRATCH_BYTES compiled into it,
+ * which every GPU that loads the library holds until the process exits.  The
+ * call allocates nothing.  A request whose gma_workspace_size() is larger than
+ * GMA_NOALLOC_SCRATCH_BYTES returns GMA_ERR_WORKSPACE and launches nothing.
+ * The first call on a device looks up the array's device address on that
+ * device (the device must be current); make that first call before any
+ * stream capture.  All calls on a device share the array: calls whose GPU
+ * work overlaps (other streams, or before an earlier call has finished) race
+ * on it.  Each call clears the array's status word at its start; device-side
+ * errors of these calls are not reported through gma_get_status().
+ */
+gma_status gma_forward_noalloc(const gma_desc *desc, const void *Qx, const void *Kx,
+                               const void *V, const float *mu, const float *rho,
+                               const float *pi_logits, float eps, int causal, void *out,
+                               void *stream);
+
 /*
  * Synchronises `stream`, reads the device status word of `workspace`, clears
  * it, and returns GMA_OK or the device error that was posted (GMA_ERR_TIMEOUT).
