@@ -65,10 +65,21 @@ struct Args {
 
 // Builds the launch list.  With args == nullptr only names and sizes are filled.
 gma_status build_forward_plan(const Problem &p, const Args *a, Plan &plan) {
+    Args z{};
+    if (tc_bidir_supported(p)) {
+        const TcLayout T = tc_layout(p);
+        plan.workspace = T.total;
+        const Args A = a ? *a : z;
+        char *ws = A.ws;
+        plan.add("tc_params", [=](cudaStream_t s) { return tc_params(p, T, A.mu, A.rho, A.alpha, ws, s); });
+        plan.add("tc_write", [=](cudaStream_t s) { return tc_write(p, T, A.Kx, A.V, ws, s); });
+        plan.add("tc_reduce", [=](cudaStream_t s) { return tc_reduce(p, T, ws, s); });
+        plan.add("tc_read", [=](cudaStream_t s) { return tc_read(p, T, A.Qx, A.out, ws, s); });
+        return GMA_OK;
+    }
     const SimtLayout L = simt_layout(p);
     if (p.causal && simt_causal_smem(p) > kMaxDynSmem) return GMA_ERR_UNSUPPORTED;
     plan.workspace = L.total;
-    Args z{};
     const Args A = a ? *a : z;
     char *ws = A.ws;
     float *lam = reinterpret_cast<float *>(ws + L.lam);

@@ -40,6 +40,23 @@ struct SimtLayout {
 };
 SimtLayout simt_layout(const Problem &p);
 
+// ----- tensor-core bidirectional path: gma_tc.cu -----
+constexpr int kMaxCtas = 256;        // upper bound on persistent CTAs (partial slots are sized for it)
+struct TcLayout {
+    size_t params, part, mem, total;   // workspace byte offsets
+    uint32_t param_stride, mem_stride;
+    int T, Ttot, ncta;                 // tiles per head, tiles in total, persistent CTAs
+};
+bool tc_bidir_supported(const Problem &p);
+TcLayout tc_layout(const Problem &p);
+cudaError_t tc_params(const Problem &p, const TcLayout &L, const float *mu, const float *rho,
+                      const float *alpha, char *ws, cudaStream_t s);
+cudaError_t tc_write(const Problem &p, const TcLayout &L, const void *Kx, const void *V, char *ws,
+                     cudaStream_t s);
+cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s);
+cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,
+                    cudaStream_t s);
+
 // ----- SIMT (CUDA-core, fp32) path: gma_simt.cu -----
 cudaError_t simt_params(const Problem &p, const float *rho, const float *alpha, float *lam,
                         float *cdir, cudaStream_t s);

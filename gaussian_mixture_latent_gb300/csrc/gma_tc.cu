@@ -1,0 +1,973 @@
+// Tensor-core (tcgen05) path of the bidirectional GMA forward for bf16
+// inputs and outputs, routing dimension d = 64, value dimension dv = 64 and
+// K = 64 or 128 components.
+//
+// "Gaussian Mixture Attention" (Huang & Raza, 2026): responsibilities
+// (section 3.2 Eq. 3, in the log-density form of section 4.1 Eq. 16 / 3b),
+// latent write (section 3.3 Eq. 5-6) and normalised read (Eq. 7-8), with the
+// parameterisation of section 3.6 (Eq. 14-15).
+//
+// The log-density of all K diagonal Gaussians for a tile of 128 rows is one
+// contraction:  s = [x, x^2 / 256] . W^T + c  with
+//   W_k = [mu_k * lam_k, 256 * (-lam_k / 2 - beta)] * log2(e),   lam = 1 / var,
+//   c_k = (log pi_k - 1/2 sum_m log var_km - 1/2 sum_m mu_km^2 lam_km) * log2(e),
+// where beta_m = mean_k(-lam_km / 2) is a k-independent shift (it changes every
+// score of a row by the same amount, which the softmax cancels) that centres
+// the quadratic coefficients.  Scores are in log2 units, so exp2 gives the
+// responsibilities.  Operands are fp16 (x exact; x^2 and W rounded to 11
+// bits; W carries a per-head power-of-two scale), accumulation fp32.
+//
+// Kernels (tc_write / tc_read are persistent, one CTA per SM, each CTA owns a
+// contiguous range of the (head, 128-row tile) list):
+//   tc_params  per head: fp16 W in the MMA's shared-memory layout, c, scale
+//   tc_write   per tile of Kx, V:  [x, x^2] -> TMEM; MMA -> scores in TMEM;
+//              softmax -> Gamma^K (bf16, shared memory); MMA accumulates
+//              [V | 1]^T Gamma^K (= [Vt | Z]^T) in TMEM; drained per head to a
+//              fp32 partial slot (slot index = cta + head)
+//   tc_reduce  per head: fixed-order sum of the partial slots -> [Vt | Z | 1]^T
+//              as the bf16 B operand of the read
+//   tc_read    per tile of Qx: scores as above; unnormalised exp2 -> TMEM (bf16);
+//              MMA with [Vt | Z | 1]; out = num / (den + eps * sum) -> TMA store
+//
+// Warp roles inside tc_write / tc_read (352 threads): warp 0 issues every TMA
+// and bulk copy from one thread that polls its rings without blocking; warp 1
+// allocates TMEM and issues the log-density MMAs; warp 2 issues the
+// write / read MMAs (two issuers, because an MMA issue blocks while the tensor
+// pipe fills); warps 3-10 are two compute warpgroups that take alternate
+// tiles (one thread per row), each with its own TMEM columns, so one group's
+// softmax overlaps the other's MMAs.  Every mbarrier wait is bounded; a
+// timeout posts GMA_ERR_TIMEOUT to the workspace status word and the CTA
+// winds down.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "gma_internal.h"
+#include "gma_sm100.cuh"
+
+namespace gma {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int TM = 128;            // rows per tile
+constexpr int DR = 64;             // routing dimension handled by this path
+constexpr int DVV = 64;            // value dimension handled by this path
+constexpr int kThreads = 352;      // 11 warps
+constexpr int kWarpProducer = 0, kWarpMma1 = 1, kWarpMma2 = 2, kWarpCompute = 3;
+constexpr int kWgThreads = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kTileBytes = TM * 128;   // one 128-row x 128-byte swizzled tile
+
+__host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+
+// Per-head parameter block: W chunk 0 (K x 128 B), W chunk 1 (K x 128 B), c[K] f32, scale f32 (+pad).
+__host__ __device__ constexpr uint32_t param_bytes(int K) { return 256u * K + 4u * K + 16u; }
+// Per-head read operand: ceil(K/64) chunks of 80 rows x 128 B.
+__host__ __device__ constexpr uint32_t mem_bytes(int K) { return (uint32_t)((K + 63) / 64) * 80u * 128u; }
+
+struct TcArgs {
+    int G, H, N, T, Ttot, K;
+    const uint8_t *params;   // [H][param_stride]
+    uint32_t param_stride;
+    float *partials;         // [slots][DVV + 1][K]
+    uint8_t *mem;            // [G][mem_stride]
+    uint32_t mem_stride;
+    float eps;
+    unsigned *status;
+};
+
+__device__ __forceinline__ void cta_range(int Ttot, int &t0, int &t1) {
+    t0 = (int)(((long long)blockIdx.x * Ttot) / gridDim.x);
+    t1 = (int)(((long long)(blockIdx.x + 1) * Ttot) / gridDim.x);
+}
+
+// Walks the CTA's tiles in steps of `step` without dividing inside the loop:
+// i = local tile index, g = head, j = tile within the head, hl = g - first head.
+struct TileCursor {
+    int i, g, j, hl, T, n, step;
+    __device__ TileCursor(int t0, int n_, int T_, int start, int step_) : T(T_), n(n_), step(step_) {
+        i = start;
+        g = (t0 + start) / T_;
+        j = (t0 + start) - g * T_;
+        hl = g - t0 / T_;
+    }
+    __device__ bool valid() const { return i < n; }
+    __device__ bool first() const { return j == 0 || i == 0; }
+    __device__ bool last() const { return j == T - 1 || i == n - 1; }
+    __device__ void next() {
+        i += step;
+        j += step;
+        while (j >= T) { j -= T; ++g; ++hl; }
+    }
+};
+
+// ------------------------------------------------------------------ tc_params
+
+constexpr int kParamThreads = 512;
+
+__global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float var_floor,
+                                                                  const float *__restrict__ mu,
+                                                                  const float *__restrict__ rho,
+                                                                  const float *__restrict__ alpha,
+                                                                  uint8_t *__restrict__ out, uint32_t stride) {
+    extern __shared__ float sm[];
+    float *a = sm;                 // [K][DR]
+    float *b = a + K * DR;         // [K][DR]
+    float *red = b + K * DR;       // [64] scratch
+    float *colmean = red + 64;     // [DR]
+    const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int NW = kParamThreads / 32;
+    const float *mu_h = mu + (size_t)h * K * DR, *rho_h = rho + (size_t)h * K * DR;
+    const float *al = alpha + (size_t)h * K;
+    uint8_t *blk = out + (size_t)h * stride;
+
+    // log-sum-exp of the prior logits (Eq. 15)
+    float m = -INFINITY;
+    for (int k = tid; k < K; k += kParamThreads) m = fmaxf(m, al[k]);
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(~0u, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+    for (int w = 1; w < NW; ++w) m = fmaxf(m, red[w]);
+    __syncthreads();
+    float s = 0.f;
+    for (int k = tid; k < K; k += kParamThreads) s += expf(al[k] - m);
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(~0u, s, o);
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    s = 0.f;
+    for (int w = 0; w < NW; ++w) s += red[w];
+    const float lse = m + logf(s);
+    __syncthreads();
+
+    // Eq. 14: variances; linear and quadratic coefficients in log2 units
+    for (int e = tid; e < K * DR; e += kParamThreads) {
+        const float w = rho_h[e];
+        const float var = fmaxf(w, 0.f) + log1pf(expf(-fabsf(w))) + var_floor;
+        const float lam = 1.0f / var;
+        a[e] = mu_h[e] * lam * kLog2e;
+        b[e] = -0.5f * lam * kLog2e;
+    }
+    __syncthreads();
+    // per-component constant c_k, one warp per component
+    float *cvec = reinterpret_cast<float *>(blk + 256u * K);
+    for (int k = warp; k < K; k += NW) {
+        float logdet = 0.f, musq = 0.f;
+        for (int j = lane; j < DR; j += 32) {
+            const float var = -0.5f * kLog2e / b[k * DR + j];     // b = -log2(e) / (2 var)
+            logdet += logf(var);
+            musq += mu_h[k * DR + j] * a[k * DR + j];            // mu^2 lam log2(e)
+        }
+        for (int o = 16; o; o >>= 1) {
+            logdet += __shfl_xor_sync(~0u, logdet, o);
+            musq += __shfl_xor_sync(~0u, musq, o);
+        }
+        if (lane == 0) cvec[k] = (al[k] - lse) * kLog2e - 0.5f * kLog2e * logdet - 0.5f * musq;
+    }
+    // mean over components of each quadratic coefficient column (8 threads per column)
+    {
+        const int col = tid >> 3, part = tid & 7;
+        float acc = 0.f;
+        if (col < DR)
+            for (int k = part; k < K; k += 8) acc += b[k * DR + col];
+        acc += __shfl_xor_sync(~0u, acc, 1);
+        acc += __shfl_xor_sync(~0u, acc, 2);
+        acc += __shfl_xor_sync(~0u, acc, 4);
+        if (col < DR && part == 0) colmean[col] = acc / (float)K;
+    }
+    __syncthreads();
+    // centre the quadratic coefficients over k, rescale for the x^2/256 operand, and find max |W|
+    float amax = 0.f;
+    for (int e = tid; e < K * DR; e += kParamThreads) {
+        const float q = (b[e] - colmean[e % DR]) * 256.0f;
+        b[e] = q;
+        amax = fmaxf(amax, fmaxf(fabsf(a[e]), fabsf(q)));
+    }
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
+    if (lane == 0) red[32 + warp] = amax;
+    __syncthreads();
+    amax = 0.f;
+    for (int w = 0; w < NW; ++w) amax = fmaxf(amax, red[32 + w]);
+    // power-of-two scale so that max |W| / scale lies in [2^13, 2^14]
+    int ex = 0;
+    if (amax > 0.f && isfinite(amax)) ex = (int)ceilf(log2f(amax)) - 14;
+    const float inv = exp2f((float)-ex);
+    if (tid == 0) *reinterpret_cast<float *>(blk + 256u * K + 4u * K) = exp2f((float)ex);
+    // fp16 W in the K-major 128-byte-swizzled layout: row k, 8-element chunk j/8, element j%8
+    for (int e = tid; e < K * DR / 2; e += kParamThreads) {
+        const int k = (2 * e) / DR, j = (2 * e) % DR;
+        const uint32_t off = sw128_off(k, j >> 3) + (j & 7) * 2;
+        *reinterpret_cast<uint32_t *>(blk + off) = pack_f16(a[2 * e] * inv, a[2 * e + 1] * inv);
+        *reinterpret_cast<uint32_t *>(blk + 128u * K + off) = pack_f16(b[2 * e] * inv, b[2 * e + 1] * inv);
+    }
+}
+
+// ------------------------------------------------------------------ wind-down helpers
+
+// Bounded wait that runs to completion (or its time limit) even after another
+// thread raised the CTA's abort flag: used before the CTA releases shared memory
+// or TMEM that in-flight copies or MMAs still touch.
+__device__ __forceinline__ void wait_ignoring_abort(uint64_t *bar, uint32_t parity, unsigned *status) {
+    int never = 0;
+    mbar_wait(bar, parity, Abort{&never, status}, kDevErrTimeout);
+}
+
+// Every TMA load issued into an S-stage ring has landed: waits for the last
+// fill of each stage (fills are issued round-robin, so that is the newest phase).
+__device__ __forceinline__ void wind_down_ring(uint64_t *full, int S, int issued, unsigned *status) {
+    for (int i = issued > S ? issued - S : 0; i < issued; ++i) wait_ignoring_abort(&full[i % S], (i / S) & 1, status);
+}
+
+// ------------------------------------------------------------------ compute helpers
+//
+// Compute warpgroup wg (0 or 1) is warps 3+4wg .. 6+4wg; thread r of the group
+// owns tile row r (= TMEM lane r): warp w accesses TMEM lanes 32*(w % 4) ...
+
+struct RowThread {
+    uint32_t r;          // tile row = TMEM lane
+    uint32_t lane_off;   // TMEM lane field of this warp
+    int wg;              // compute warpgroup
+    int wtid;            // 0..127 inside the group
+};
+
+__device__ __forceinline__ bool wg_all(const RowThread &t, bool v) { return group_all(v, 1 + t.wg, kWgThreads); }
+__device__ __forceinline__ void wg_sync(const RowThread &t) { group_sync(1 + t.wg, kWgThreads); }
+
+// Convert a bf16 row (128 B, swizzled) into the fp16 [x, x^2/256] row of the
+// log-density A operand in TMEM (columns 0-31: x pairs, 32-63: x^2/256 pairs).
+__device__ __forceinline__ void convert_row(const uint8_t *xs, uint32_t r, uint32_t tcol_a) {
+    uint32_t px[32], pq[32];
+    const uint64_t k16 = f2_pack(0.0625f, 0.0625f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(xs + sw128_off(r, j));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float lo = bf16_lo(w[u]), hi = bf16_hi(w[u]);
+            px[4 * j + u] = pack_f16(lo, hi);
+            const uint64_t y = f2_mul(f2_pack(lo, hi), k16);   // x / 16, exact
+            float qa, qb;
+            f2_unpack(f2_mul(y, y), qa, qb);                   // x^2 / 256
+            pq[4 * j + u] = pack_f16(qa, qb);
+        }
+    }
+    tmem_st32(tcol_a, px);
+    tmem_st32(tcol_a + 32, pq);
+}
+
+// All K log2-domain scores s = d * scale + c of this thread's row (one TMEM
+// round trip) and their maximum.
+template <int K>
+__device__ __forceinline__ float row_scores(uint32_t taddr, const float *cvec, uint64_t sc2, float (&s)[K]) {
+    uint32_t d[K];
+#pragma unroll
+    for (int cc = 0; cc < K / 32; ++cc) tmem_ld32(taddr + 32 * cc, d + 32 * cc);
+    tmem_ld_wait();
+#pragma unroll
+    for (int t = 0; t < K; t += 2) {
+        const float2 c = *reinterpret_cast<const float2 *>(cvec + t);
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(d[t]), __uint_as_float(d[t + 1])), sc2, f2_pack(c.x, c.y)),
+                  s[t], s[t + 1]);
+    }
+    float m[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+    for (int t = 4; t + 8 <= K; t += 8) {
+        m[0] = max3(m[0], s[t], s[t + 1]);
+        m[1] = max3(m[1], s[t + 2], s[t + 3]);
+        m[2] = max3(m[2], s[t + 4], s[t + 5]);
+        m[3] = max3(m[3], s[t + 6], s[t + 7]);
+    }
+    m[0] = max3(m[0], s[K - 4], s[K - 3]);
+    m[1] = max3(m[1], s[K - 2], s[K - 1]);
+    return fmaxf(max3(m[0], m[1], m[2]), m[3]);
+}
+
+// 2^(s - m) for K scores, as K/2 bf16 pairs.
+template <int K>
+__device__ __forceinline__ void row_exp(const float (&s)[K], float m, uint32_t (&e)[K / 2]) {
+    const uint64_t nm2 = f2_pack(-m, -m);
+#pragma unroll
+    for (int t = 0; t < K; t += 2) {
+        float a, b;
+        f2_unpack(f2_add(f2_pack(s[t], s[t + 1]), nm2), a, b);
+        e[t / 2] = ex2_bf16x2(pack_bf16(a, b));
+    }
+}
+
+// ------------------------------------------------------------------ tc_write
+
+template <int K>
+struct WriteCfg {
+    static constexpr int KCH = (K + 63) / 64;
+    static constexpr int SX = K <= 64 ? 4 : 3;                       // X ring stages
+    static constexpr int SV = K <= 64 ? 4 : 3;                       // V ring stages
+    static constexpr int PN = K <= 64 ? 2 : 1;                       // parameter buffers
+    static constexpr uint32_t PB = align1k(param_bytes(K));
+    static constexpr uint32_t OFF_X = 0;
+    static constexpr uint32_t OFF_V = OFF_X + SX * kTileBytes;
+    static constexpr uint32_t OFF_ONES = OFF_V + SV * kTileBytes;      // after every V stage (positive LBO)
+    static constexpr uint32_t OFF_G = OFF_ONES + kTileBytes;           // one Gamma buffer per warpgroup
+    static constexpr uint32_t OFF_P = OFF_G + 2 * KCH * kTileBytes;
+    static constexpr uint32_t OFF_BAR = OFF_P + PN * PB;
+    static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;            // barriers + alignment slack
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t wg_cols = 64 + K;
+    static constexpr uint32_t col_a(int w) { return w * wg_cols; }
+    static constexpr uint32_t col_d1(int w) { return w * wg_cols + 64; }
+    static constexpr uint32_t COL_D2 = 2 * wg_cols;
+};
+
+template <int K>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, TcArgs A) {
+    using C = WriteCfg<K>;
+    constexpr int SX = C::SX, SV = C::SV, PN = C::PN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
+    uint64_t *xfull = bars, *xempty = xfull + SX;
+    uint64_t *vfull = xempty + SX, *vempty = vfull + SV;
+    uint64_t *a_full = vempty + SV, *d1_full = a_full + 2, *g_full = d1_full + 2, *g_empty = g_full + 2;
+    uint64_t *w_full = g_empty + 2, *w_empty = w_full + PN;
+    uint64_t *d2_full = w_empty + PN, *d2_empty = d2_full + 1, *fin1 = d2_empty + 1, *fin2 = fin1 + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int t0, t1;
+    cta_range(A.Ttot, t0, t1);
+    const int n = t1 - t0;
+    const int g_first = t0 / A.T;
+    const int nheads = n > 0 ? (t1 - 1) / A.T - g_first + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
+        for (int s = 0; s < SV; ++s) { mbar_init(&vfull[s], 1); mbar_init(&vempty[s], 1); }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&a_full[b], 1); mbar_init(&d1_full[b], 1); mbar_init(&g_full[b], 1); mbar_init(&g_empty[b], 1);
+        }
+        for (int b = 0; b < PN; ++b) { mbar_init(&w_full[b], 1); mbar_init(&w_empty[b], 3); }
+        mbar_init(d2_full, 1); mbar_init(d2_empty, 1); mbar_init(fin1, 1); mbar_init(fin2, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // ONES atom column: element 0 of every row is 1.0 (bf16), the rest 0.
+    for (uint32_t e = threadIdx.x; e < kTileBytes / 16; e += blockDim.x)
+        reinterpret_cast<uint4 *>(sm + C::OFF_ONES)[e] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (threadIdx.x < TM) *reinterpret_cast<uint16_t *>(sm + C::OFF_ONES + sw128_off(threadIdx.x, 0)) = 0x3F80u;
+    if (warp == kWarpMma1) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Abort ab{abort_flag, A.status};
+
+    if (warp == kWarpProducer) {
+        if (lane == 0 && n > 0) {
+            TileCursor cx(t0, n, A.T, 0, 1), cv(t0, n, A.T, 0, 1);
+            int p_loaded = -1;
+            long long last = clock64();
+            while ((cx.valid() || cv.valid()) && !*abort_flag) {
+                bool progress = false;
+                if (cx.valid()) {
+                    const int xi = cx.i;
+                    bool can = true;
+                    if (cx.hl > p_loaded) {
+                        const int b = cx.hl % PN;
+                        if (cx.hl >= PN && !mbar_test(&w_empty[b], ((cx.hl / PN) - 1) & 1)) can = false;
+                        else {
+                            mbar_arrive_expect_tx(&w_full[b], param_bytes(K));
+                            bulk_load(sm + C::OFF_P + b * C::PB, A.params + (size_t)(cx.g % A.H) * A.param_stride,
+                                      param_bytes(K), &w_full[b]);
+                            p_loaded = cx.hl;
+                            progress = true;
+                        }
+                    }
+                    if (can && (xi < SX || mbar_test(&xempty[xi % SX], ((xi / SX) - 1) & 1))) {
+                        mbar_arrive_expect_tx(&xfull[xi % SX], kTileBytes);
+                        tma_load_3d(sm + C::OFF_X + (xi % SX) * kTileBytes, &tm_k, &xfull[xi % SX], 0, cx.j * TM, cx.g);
+                        cx.next();
+                        progress = true;
+                    }
+                }
+                if (cv.valid()) {
+                    const int vi = cv.i;
+                    if (vi < SV || mbar_test(&vempty[vi % SV], ((vi / SV) - 1) & 1)) {
+                        mbar_arrive_expect_tx(&vfull[vi % SV], kTileBytes);
+                        tma_load_3d(sm + C::OFF_V + (vi % SV) * kTileBytes, &tm_v, &vfull[vi % SV], 0, cv.j * TM, cv.g);
+                        cv.next();
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    last = clock64();
+                } else {
+                    __nanosleep(64);                       // nothing to issue: yield the issue slots
+                    if (clock64() - last > kWaitLimitCycles) {
+                        *abort_flag = 1;
+                        atomicOr(A.status, kDevErrTimeout);
+                    }
+                }
+            }
+            wind_down_ring(xfull, SX, cx.i < n ? cx.i : n, A.status);
+            wind_down_ring(vfull, SV, cv.i < n ? cv.i : n, A.status);
+            for (int hl = p_loaded - PN + 1 < 0 ? 0 : p_loaded - PN + 1; hl <= p_loaded; ++hl)
+                wait_ignoring_abort(&w_full[hl % PN], (hl / PN) & 1, A.status);
+        }
+    } else if (warp == kWarpMma1) {
+        // log-density MMAs: scores(i) = [x, x^2/256](i) . W^T into D1 of warpgroup i & 1
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idesc = idesc_f16(0, 0, 0, 0, TM, K);
+            for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
+                const int i = c.i, b = c.hl % PN, w = i & 1;
+                if (c.first() && !mbar_wait(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait(&a_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
+                tc_fence_after();
+                const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_P + b * C::PB), 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ts(tmem + C::col_d1(w), tmem + C::col_a(w) + ks * 8,
+                           bd + (uint64_t)(((ks >> 2) * 128u * K + (ks & 3) * 32u) >> 4), idesc, ks > 0);
+                mma_commit(&d1_full[w]);
+                if (c.last()) mma_commit(&w_empty[b]);
+            }
+            mma_commit(fin1);
+            wait_ignoring_abort(fin1, 0, A.status);
+        }
+    } else if (warp == kWarpMma2) {
+        // write MMAs: D2 [value row x K] += [V | 1 | 0]^T (128 x rows) . Gamma (rows x K)
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idesc = idesc_f16(1, 1, 1, 1, TM, K);
+            const uint32_t ones = smem_u32(sm + C::OFF_ONES);
+            for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
+                const int i = c.i, s = i % SV, w = i & 1;
+                if (!mbar_wait(&g_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait(&vfull[s], (i / SV) & 1, ab, kDevErrTimeout)) break;
+                if (c.first() && c.hl >= 1 && !mbar_wait(d2_empty, (c.hl - 1) & 1, ab, kDevErrTimeout)) break;
+                tc_fence_after();
+                const uint32_t va = smem_u32(sm + C::OFF_V + s * kTileBytes);
+                const uint64_t ad = sdesc_sw128(va, ones - va, 1024);
+                const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_G + w * C::KCH * kTileBytes), kTileBytes, 1024);
+                const bool first = c.first();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tmem + C::COL_D2, ad + (uint64_t)(ks * 128), bd + (uint64_t)(ks * 128), idesc,
+                           !(first && ks == 0));
+                mma_commit(&g_empty[w]);
+                mma_commit(&vempty[s]);
+                if (c.last()) mma_commit(d2_full);
+            }
+            mma_commit(fin2);
+            wait_ignoring_abort(fin2, 0, A.status);
+        }
+    } else {
+        // ---------------- two compute warpgroups, alternate tiles
+        RowThread rt;
+        rt.wg = (warp - kWarpCompute) >> 2;
+        rt.r = 32u * (warp & 3) + lane;
+        rt.lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        rt.wtid = threadIdx.x - kWarpCompute * 32 - rt.wg * kWgThreads;
+        const int w = rt.wg;
+        const bool elected = rt.wtid == 0;
+        int release_next = 0;
+        auto release_upto = [&](int hl_excl) {
+            for (; release_next < hl_excl; ++release_next)
+                if (elected) mbar_arrive(&w_empty[release_next % PN]);
+        };
+        TileCursor c(t0, n, A.T, w, 2);
+        release_upto(c.valid() ? c.hl : nheads);
+        for (; c.valid(); c.next()) {
+            const int i = c.i, hl = c.hl;
+            // convert tile i into this group's A operand
+            bool ok = mbar_wait(&xfull[i % SX], (i / SX) & 1, ab, kDevErrTimeout);
+            if (!wg_all(rt, ok)) break;
+            convert_row(sm + C::OFF_X + (i % SX) * kTileBytes, rt.r, tmem + rt.lane_off + C::col_a(w));
+            tmem_st_wait();
+            tc_fence_before();
+            wg_sync(rt);
+            if (elected) { mbar_arrive(&a_full[w]); mbar_arrive(&xempty[i % SX]); }
+            // softmax of tile i (Eq. 3b); rows past the sequence end get Gamma = 0
+            ok = mbar_wait(&d1_full[w], (i >> 1) & 1, ab, kDevErrTimeout);
+            ok = ok && mbar_wait(&w_full[hl % PN], (hl / PN) & 1, ab, kDevErrTimeout);
+            if (i >= 2) ok = ok && mbar_wait(&g_empty[w], ((i >> 1) - 1) & 1, ab, kDevErrTimeout);
+            if (!wg_all(rt, ok)) break;
+            tc_fence_after();
+            const uint8_t *pblk = sm + C::OFF_P + (hl % PN) * C::PB;
+            const float *cvec = reinterpret_cast<const float *>(pblk + 256u * K);
+            const float scale = *reinterpret_cast<const float *>(pblk + 256u * K + 4u * K);
+            float sc[K];
+            const float mx = row_scores<K>(tmem + rt.lane_off + C::col_d1(w), cvec, f2_pack(scale, scale), sc);
+            uint32_t e[K / 2];
+            row_exp<K>(sc, mx, e);
+            uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int t = 0; t < K / 2; ++t) acc[t & 3] = f2_add(acc[t & 3], f2_pack(bf16_lo(e[t]), bf16_hi(e[t])));
+            float s0, s1, s2, s3, s4, s5, s6, s7;
+            f2_unpack(acc[0], s0, s1); f2_unpack(acc[1], s2, s3);
+            f2_unpack(acc[2], s4, s5); f2_unpack(acc[3], s6, s7);
+            const float total = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+            const bool valid = c.j * TM + (int)rt.r < A.N;
+            const float inv = valid ? 1.0f / total : 0.f;
+            const uint64_t inv2 = f2_pack(inv, inv);
+            uint8_t *gbuf = sm + C::OFF_G + w * C::KCH * kTileBytes;
+#pragma unroll
+            for (int j = 0; j < K / 8; ++j) {
+                uint32_t wv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float ga, gb;
+                    f2_unpack(f2_mul(f2_pack(bf16_lo(e[4 * j + u]), bf16_hi(e[4 * j + u])), inv2), ga, gb);
+                    wv[u] = pack_bf16(ga, gb);
+                }
+                *reinterpret_cast<uint4 *>(gbuf + (j >> 3) * kTileBytes + sw128_off(rt.r, j & 7)) =
+                    make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            wg_sync(rt);
+            if (elected) mbar_arrive(&g_full[w]);
+            const bool last = c.last();
+            const int g = c.g;
+            {
+                TileCursor nx = c;
+                nx.next();
+                release_upto(nx.valid() ? nx.hl : nheads);
+            }
+            if (last) {
+                // drain [Vt | Z]^T of this head into partial slot (cta + head)
+                ok = mbar_wait(d2_full, hl & 1, ab, kDevErrTimeout);
+                if (!wg_all(rt, ok)) break;
+                tc_fence_after();
+                float *dst = A.partials + ((size_t)(blockIdx.x + g) * (DVV + 1) + rt.r) * K;
+                uint32_t v[K];
+#pragma unroll
+                for (int cc = 0; cc < K / 32; ++cc) tmem_ld32(tmem + rt.lane_off + C::COL_D2 + 32 * cc, v + 32 * cc);
+                tmem_ld_wait();
+                if (rt.r <= DVV) {
+#pragma unroll
+                    for (int t = 0; t < K; t += 4)
+                        *reinterpret_cast<float4 *>(dst + t) = make_float4(
+                            __uint_as_float(v[t]), __uint_as_float(v[t + 1]), __uint_as_float(v[t + 2]),
+                            __uint_as_float(v[t + 3]));
+                }
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) mbar_arrive(d2_empty);
+            }
+        }
+        release_upto(nheads);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma1) {
+        __syncwarp();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ tc_reduce
+
+// Fixed-order sum over the CTAs that covered head g (blockIdx.y), then the bf16
+// B operand [n][k] of the read (n = value column, dv -> Z, dv+1 -> 1, rest 0)
+// in the K-major 128-byte-swizzled layout, ceil(K/64) chunks of 80 rows.
+__global__ void __launch_bounds__(256) tc_reduce_kernel(int K, int T, int Ttot, int ncta,
+                                                        const float *__restrict__ partials,
+                                                        uint8_t *__restrict__ mem, uint32_t mem_stride) {
+    const int g = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= 80 * K) return;
+    const int lo = g * T, hi = (g + 1) * T;
+    // CTA c owns tiles [c*Ttot/ncta, (c+1)*Ttot/ncta): those meeting [lo, hi) are c_lo..c_hi.
+    int c_lo = (int)(((long long)lo * ncta) / Ttot);
+    while (c_lo > 0 && ((long long)c_lo * Ttot) / ncta > lo) --c_lo;
+    while (((long long)(c_lo + 1) * Ttot) / ncta <= lo) ++c_lo;
+    const int nrow = e / K, k = e % K;
+    float v = 0.f;
+    if (nrow <= DVV) {
+        for (int c = c_lo; c < ncta && ((long long)c * Ttot) / ncta < hi; ++c)
+            v += partials[((size_t)(c + g) * (DVV + 1) + nrow) * K + k];
+    } else if (nrow == DVV + 1) {
+        v = 1.f;
+    }
+    const uint32_t off = (uint32_t)(k >> 6) * 80u * 128u + sw128_off(nrow, (k & 63) >> 3) + (k & 7) * 2;
+    *reinterpret_cast<__nv_bfloat16 *>(mem + (size_t)g * mem_stride + off) = __float2bfloat16_rn(v);
+}
+
+// ------------------------------------------------------------------ tc_read
+
+template <int K>
+struct ReadCfg {
+    static constexpr int SX = K <= 64 ? 6 : 5;
+    static constexpr int PN = 2;
+    static constexpr uint32_t PB = align1k(param_bytes(K));
+    static constexpr uint32_t MB = align1k(mem_bytes(K));
+    static constexpr uint32_t OFF_X = 0;
+    static constexpr uint32_t OFF_O = OFF_X + SX * kTileBytes;         // one output staging tile per group
+    static constexpr uint32_t OFF_P = OFF_O + 2 * kTileBytes;
+    static constexpr uint32_t OFF_M = OFF_P + PN * PB;
+    static constexpr uint32_t OFF_BAR = OFF_M + PN * MB;
+    static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int NOUT = 80;                                    // [Vt | Z | 1 | 0...]
+    static constexpr uint32_t wg_cols = NOUT + K;
+    static constexpr uint32_t col_a(int w) { return w * wg_cols; }     // A operand, later D2 (same columns)
+    static constexpr uint32_t col_d1(int w) { return w * wg_cols + NOUT; }
+};
+
+template <int K>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o, TcArgs A) {
+    using C = ReadCfg<K>;
+    constexpr int SX = C::SX, PN = C::PN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
+    uint64_t *xfull = bars, *xempty = xfull + SX;
+    uint64_t *a_full = xempty + SX, *d1_full = a_full + 2, *e_full = d1_full + 2, *d2_full = e_full + 2;
+    uint64_t *w_full = d2_full + 2, *w_empty = w_full + PN;
+    uint64_t *fin1 = w_empty + PN, *fin2 = fin1 + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int t0, t1;
+    cta_range(A.Ttot, t0, t1);
+    const int n = t1 - t0;
+    const int g_first = t0 / A.T;
+    const int nheads = n > 0 ? (t1 - 1) / A.T - g_first + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&a_full[b], 1); mbar_init(&d1_full[b], 1); mbar_init(&e_full[b], 1); mbar_init(&d2_full[b], 1);
+        }
+        for (int b = 0; b < PN; ++b) { mbar_init(&w_full[b], 1); mbar_init(&w_empty[b], 3); }
+        mbar_init(fin1, 1); mbar_init(fin2, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma1) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Abort ab{abort_flag, A.status};
+
+    if (warp == kWarpProducer) {
+        if (lane == 0 && n > 0) {
+            TileCursor cx(t0, n, A.T, 0, 1);
+            int p_loaded = -1;
+            long long last = clock64();
+            while (cx.valid() && !*abort_flag) {
+                bool progress = false;
+                const int xi = cx.i;
+                bool can = true;
+                if (cx.hl > p_loaded) {
+                    const int b = cx.hl % PN;
+                    if (cx.hl >= PN && !mbar_test(&w_empty[b], ((cx.hl / PN) - 1) & 1)) can = false;
+                    else {
+                        mbar_arrive_expect_tx(&w_full[b], param_bytes(K) + mem_bytes(K));
+                        bulk_load(sm + C::OFF_P + b * C::PB, A.params + (size_t)(cx.g % A.H) * A.param_stride,
+                                  param_bytes(K), &w_full[b]);
+                        bulk_load(sm + C::OFF_M + b * C::MB, A.mem + (size_t)cx.g * A.mem_stride, mem_bytes(K),
+                                  &w_full[b]);
+                        p_loaded = cx.hl;
+                        progress = true;
+                    }
+                }
+                if (can && (xi < SX || mbar_test(&xempty[xi % SX], ((xi / SX) - 1) & 1))) {
+                    mbar_arrive_expect_tx(&xfull[xi % SX], kTileBytes);
+                    tma_load_3d(sm + C::OFF_X + (xi % SX) * kTileBytes, &tm_q, &xfull[xi % SX], 0, cx.j * TM, cx.g);
+                    cx.next();
+                    progress = true;
+                }
+                if (progress) {
+                    last = clock64();
+                } else {
+                    __nanosleep(64);                       // nothing to issue: yield the issue slots
+                    if (clock64() - last > kWaitLimitCycles) {
+                        *abort_flag = 1;
+                        atomicOr(A.status, kDevErrTimeout);
+                    }
+                }
+            }
+            wind_down_ring(xfull, SX, cx.i < n ? cx.i : n, A.status);
+            for (int hl = p_loaded - PN + 1 < 0 ? 0 : p_loaded - PN + 1; hl <= p_loaded; ++hl)
+                wait_ignoring_abort(&w_full[hl % PN], (hl / PN) & 1, A.status);
+        }
+    } else if (warp == kWarpMma1) {
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idesc = idesc_f16(0, 0, 0, 0, TM, K);
+            for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
+                const int i = c.i, b = c.hl % PN, w = i & 1;
+                if (c.first() && !mbar_wait(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait(&a_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
+                tc_fence_after();
+                const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_P + b * C::PB), 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ts(tmem + C::col_d1(w), tmem + C::col_a(w) + ks * 8,
+                           bd + (uint64_t)(((ks >> 2) * 128u * K + (ks & 3) * 32u) >> 4), idesc, ks > 0);
+                mma_commit(&d1_full[w]);
+            }
+            mma_commit(fin1);
+            wait_ignoring_abort(fin1, 0, A.status);
+        }
+    } else if (warp == kWarpMma2) {
+        // read MMAs: D2 (128 rows x 80) = e (rows x K, bf16 in TMEM) . [Vt | Z | 1 | 0] (K x 80)
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idesc = idesc_f16(1, 1, 0, 0, TM, C::NOUT);
+            for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
+                const int i = c.i, b = c.hl % PN, w = i & 1;
+                if (!mbar_wait(&e_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
+                tc_fence_after();
+                const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_M + b * C::MB), 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks)
+                    mma_ts(tmem + C::col_a(w), tmem + C::col_d1(w) + ks * 8,
+                           bd + (uint64_t)(((ks >> 2) * 80u * 128u + (ks & 3) * 32u) >> 4), idesc, ks > 0);
+                mma_commit(&d2_full[w]);
+                if (c.last()) mma_commit(&w_empty[b]);
+            }
+            mma_commit(fin2);
+            wait_ignoring_abort(fin2, 0, A.status);
+        }
+    } else {
+        RowThread rt;
+        rt.wg = (warp - kWarpCompute) >> 2;
+        rt.r = 32u * (warp & 3) + lane;
+        rt.lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        rt.wtid = threadIdx.x - kWarpCompute * 32 - rt.wg * kWgThreads;
+        const int w = rt.wg;
+        const bool elected = rt.wtid == 0;
+        int release_next = 0;
+        auto release_upto = [&](int hl_excl) {
+            for (; release_next < hl_excl; ++release_next)
+                if (elected) mbar_arrive(&w_empty[release_next % PN]);
+        };
+        TileCursor c(t0, n, A.T, w, 2);
+        release_upto(c.valid() ? c.hl : nheads);
+        for (; c.valid(); c.next()) {
+            const int i = c.i, hl = c.hl;
+            bool ok = mbar_wait(&xfull[i % SX], (i / SX) & 1, ab, kDevErrTimeout);
+            if (!wg_all(rt, ok)) break;
+            convert_row(sm + C::OFF_X + (i % SX) * kTileBytes, rt.r, tmem + rt.lane_off + C::col_a(w));
+            tmem_st_wait();
+            tc_fence_before();
+            wg_sync(rt);
+            if (elected) { mbar_arrive(&a_full[w]); mbar_arrive(&xempty[i % SX]); }
+            ok = mbar_wait(&d1_full[w], (i >> 1) & 1, ab, kDevErrTimeout);
+            ok = ok && mbar_wait(&w_full[hl % PN], (hl / PN) & 1, ab, kDevErrTimeout);
+            if (!wg_all(rt, ok)) break;
+            tc_fence_after();
+            const uint8_t *pblk = sm + C::OFF_P + (hl % PN) * C::PB;
+            const float *cvec = reinterpret_cast<const float *>(pblk + 256u * K);
+            const float scale = *reinterpret_cast<const float *>(pblk + 256u * K + 4u * K);
+            const uint32_t d1 = tmem + rt.lane_off + C::col_d1(w);
+            {
+                // unnormalised responsibilities (the row scale cancels in num / den),
+                // bf16 pairs written over the first K/2 score columns
+                float sc[K];
+                const float mx = row_scores<K>(d1, cvec, f2_pack(scale, scale), sc);
+                uint32_t e[K / 2];
+                row_exp<K>(sc, mx, e);
+#pragma unroll
+                for (int cc = 0; cc < K / 64; ++cc) tmem_st32(d1 + 32 * cc, e + 32 * cc);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            wg_sync(rt);
+            if (elected) mbar_arrive(&e_full[w]);
+            const int g = c.g, row0 = c.j * TM;
+            {
+                TileCursor nx = c;
+                nx.next();
+                release_upto(nx.valid() ? nx.hl : nheads);
+            }
+            // epilogue: out = num / (den + eps * sum_k e_k)
+            ok = mbar_wait(&d2_full[w], (i >> 1) & 1, ab, kDevErrTimeout);
+            if (!wg_all(rt, ok)) break;
+            tc_fence_after();
+            uint32_t v0[32], v1[32], dz[4];
+            tmem_ld32(tmem + rt.lane_off + C::col_a(w), v0);
+            tmem_ld32(tmem + rt.lane_off + C::col_a(w) + 32, v1);
+            tmem_ld4(tmem + rt.lane_off + C::col_a(w) + 64, dz);
+            tmem_ld_wait();
+            const float rd = 1.0f / (__uint_as_float(dz[0]) + A.eps * __uint_as_float(dz[1]));
+            const uint64_t rd2 = f2_pack(rd, rd);
+            uint8_t *ob = sm + C::OFF_O + w * kTileBytes;
+            if (elected) bulk_wait_group_read<0>();          // this group's previous store left the buffer
+            wg_sync(rt);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t *src = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+                uint32_t o[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float oa, obv;
+                    f2_unpack(f2_mul(f2_pack(__uint_as_float(src[2 * u]), __uint_as_float(src[2 * u + 1])), rd2), oa, obv);
+                    o[u] = pack_bf16(oa, obv);
+                }
+                *reinterpret_cast<uint4 *>(ob + sw128_off(rt.r, j)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            wg_sync(rt);
+            if (elected) {
+                tma_store_3d(&tm_o, ob, 0, row0, g);
+                bulk_commit_group();
+            }
+        }
+        release_upto(nheads);
+        if (elected) bulk_wait_group<0>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma1) {
+        __syncwarp();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+// 3D bf16 tensor map over [G][N][width], box [1][128][64], 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, int G, int N, int width) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)N, (cuuint64_t)G};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * N};
+    const cuuint32_t box[3] = {64, TM, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int K>
+cudaError_t launch_write(const Problem &p, const TcLayout &L, const void *Kx, const void *V, char *ws,
+                         cudaStream_t s) {
+    CUtensorMap tk, tv;
+    if (!make_map(&tk, Kx, p.G, p.N, DR) || !make_map(&tv, V, p.G, p.N, DVV)) return cudaErrorInvalidValue;
+    TcArgs a{};
+    a.G = p.G; a.H = p.H; a.N = p.N; a.T = L.T; a.Ttot = L.Ttot; a.K = K;
+    a.params = reinterpret_cast<const uint8_t *>(ws + L.params); a.param_stride = L.param_stride;
+    a.partials = reinterpret_cast<float *>(ws + L.part);
+    a.status = reinterpret_cast<unsigned *>(ws);
+    auto kern = tc_write_kernel<K>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WriteCfg<K>::BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<L.ncta, kThreads, WriteCfg<K>::BYTES, s>>>(tk, tv, a);
+    return cudaGetLastError();
+}
+
+template <int K>
+cudaError_t launch_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,
+                        cudaStream_t s) {
+    CUtensorMap tq, to;
+    if (!make_map(&tq, Qx, p.G, p.N, DR) || !make_map(&to, out, p.G, p.N, DVV)) return cudaErrorInvalidValue;
+    TcArgs a{};
+    a.G = p.G; a.H = p.H; a.N = p.N; a.T = L.T; a.Ttot = L.Ttot; a.K = K;
+    a.params = reinterpret_cast<const uint8_t *>(ws + L.params); a.param_stride = L.param_stride;
+    a.mem = reinterpret_cast<uint8_t *>(ws + L.mem); a.mem_stride = L.mem_stride;
+    a.eps = p.eps;
+    a.status = reinterpret_cast<unsigned *>(ws);
+    auto kern = tc_read_kernel<K>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ReadCfg<K>::BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<L.ncta, kThreads, ReadCfg<K>::BYTES, s>>>(tq, to, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_bidir_supported(const Problem &p) {
+    return p.in_dtype == GMA_BF16 && p.out_dtype == GMA_BF16 && !p.causal && p.d == DR && p.dv == DVV &&
+           (p.K == 64 || p.K == 128) && p.N > 0;
+}
+
+TcLayout tc_layout(const Problem &p) {
+    TcLayout L{};
+    L.T = (p.N + TM - 1) / TM;
+    L.Ttot = L.T * p.G;
+    const int nsm = sm_count();
+    L.ncta = std::max(1, std::min({nsm > 0 ? nsm : kMaxCtas, kMaxCtas, L.Ttot}));
+    L.param_stride = align1k(param_bytes(p.K));
+    L.mem_stride = align1k(mem_bytes(p.K));
+    size_t off = kHeaderBytes;
+    L.params = align_up(off);
+    off = L.params + (size_t)p.H * L.param_stride;
+    L.part = align_up(off);
+    off = L.part + sizeof(float) * (size_t)(kMaxCtas + p.G) * (DVV + 1) * p.K;
+    L.mem = align_up(off);
+    off = L.mem + (size_t)p.G * L.mem_stride;
+    L.total = align_up(off);
+    return L;
+}
+
+cudaError_t tc_params(const Problem &p, const TcLayout &L, const float *mu, const float *rho,
+                      const float *alpha, char *ws, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (2 * (size_t)p.K * DR + 64 + DR);
+    cudaError_t e = cudaFuncSetAttribute(tc_params_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    tc_params_kernel<<<p.H, kParamThreads, smem, s>>>(p.K, p.var_floor, mu, rho, alpha,
+                                            reinterpret_cast<uint8_t *>(ws + L.params), L.param_stride);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_write(const Problem &p, const TcLayout &L, const void *Kx, const void *V, char *ws,
+                     cudaStream_t s) {
+    return p.K == 64 ? launch_write<64>(p, L, Kx, V, ws, s) : launch_write<128>(p, L, Kx, V, ws, s);
+}
+
+cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s) {
+    dim3 grid((80 * p.K + 255) / 256, p.G);
+    tc_reduce_kernel<<<grid, 256, 0, s>>>(p.K, L.T, L.Ttot, L.ncta, reinterpret_cast<const float *>(ws + L.part),
+                                         reinterpret_cast<uint8_t *>(ws + L.mem), L.mem_stride);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,
+                    cudaStream_t s) {
+    return p.K == 64 ? launch_read<64>(p, L, Qx, out, ws, s) : launch_read<128>(p, L, Qx, out, ws, s);
+}
+
+}  // namespace gma

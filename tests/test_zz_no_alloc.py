@@ -77,9 +77,11 @@ def test_noalloc_matches_gma_forward_on_two_calls_in_a_row(lib):
 
 
 def test_noalloc_refuses_problems_larger_than_its_scratch(lib):
-    w = inputs.Workload("noalloc_big", B=8, H=8, N=4096, d=64, K=64, dv=64, dtype="bf16", causal=False)
+    # float32 inputs take the CUDA-core path, whose workspace holds both
+    # responsibility matrices: 64 heads x 4096 rows x 64 components x 8 bytes.
+    w = inputs.Workload("noalloc_big", B=8, H=8, N=4096, d=64, K=64, dv=64, dtype="f32", causal=False)
     import gaussian_mixture_latent_gb300 as gma
-    tdt = torch.bfloat16
+    tdt = torch.float32
     desc = gma._make_desc(w.B, w.H, w.N, w.d, w.K, w.dv, tdt, tdt, w.var_floor, 0)
     need = gma.gma_workspace_size(desc, False)
     limit = 32 << 20
