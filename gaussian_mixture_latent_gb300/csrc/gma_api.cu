@@ -77,6 +77,15 @@ gma_status build_forward_plan(const Problem &p, const Args *a, Plan &plan) {
         plan.add("tc_read", [=](cudaStream_t s) { return tc_read(p, T, A.Qx, A.out, ws, s); });
         return GMA_OK;
     }
+    if (tc_causal_supported(p)) {
+        const TcLayout T = tc_causal_layout(p);
+        plan.workspace = T.total;
+        const Args A = a ? *a : z;
+        char *ws = A.ws;
+        plan.add("tc_params", [=](cudaStream_t s) { return tc_params(p, T, A.mu, A.rho, A.alpha, ws, s); });
+        plan.add("tc_causal", [=](cudaStream_t s) { return tc_causal(p, T, A.Qx, A.Kx, A.V, A.out, ws, s); });
+        return GMA_OK;
+    }
     const SimtLayout L = simt_layout(p);
     if (p.causal && simt_causal_smem(p) > kMaxDynSmem) return GMA_ERR_UNSUPPORTED;
     plan.workspace = L.total;

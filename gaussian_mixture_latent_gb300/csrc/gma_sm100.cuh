@@ -30,10 +30,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-// Potentially blocking test: the thread may sleep in hardware until the phase
-// completes or about kSuspendNs nanoseconds pass, instead of spinning.
-constexpr uint32_t kSuspendNs = 20000;
-
+// Potentially blocking test of a phase (the hardware may briefly suspend the thread).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -273,6 +270,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;   // descriptor version for tcgen05
     d |= (uint64_t)2 << 61;   // SWIZZLE_128B
+    return d;
+}
+
+// Shared-memory matrix descriptor without swizzle (K-major): 8-row x 16-byte
+// core matrices; lbo = byte offset between the two 8-element halves of a
+// 16-element K step, sbo = byte offset between 8-row groups.
+__device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version for tcgen05; layout type 0 = no swizzle
     return d;
 }
 

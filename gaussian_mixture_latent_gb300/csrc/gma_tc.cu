@@ -49,28 +49,17 @@
 
 #include "gma_internal.h"
 #include "gma_sm100.cuh"
+#include "gma_tc_common.cuh"
 
 namespace gma {
 
 using namespace sm100;
+using namespace tc;
 
 namespace {
 
-constexpr int TM = 128;            // rows per tile
-constexpr int DR = 64;             // routing dimension handled by this path
-constexpr int DVV = 64;            // value dimension handled by this path
 constexpr int kThreads = 352;      // 11 warps
 constexpr int kWarpProducer = 0, kWarpMma1 = 1, kWarpMma2 = 2, kWarpCompute = 3;
-constexpr int kWgThreads = 128;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kTileBytes = TM * 128;   // one 128-row x 128-byte swizzled tile
-
-__host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
-
-// Per-head parameter block: W chunk 0 (K x 128 B), W chunk 1 (K x 128 B), c[K] f32, scale f32 (+pad).
-__host__ __device__ constexpr uint32_t param_bytes(int K) { return 256u * K + 4u * K + 16u; }
-// Per-head read operand: ceil(K/64) chunks of 80 rows x 128 B.
-__host__ __device__ constexpr uint32_t mem_bytes(int K) { return (uint32_t)((K + 63) / 64) * 80u * 128u; }
 
 struct TcArgs {
     int G, H, N, T, Ttot, K;
@@ -88,26 +77,6 @@ __device__ __forceinline__ void cta_range(int Ttot, int &t0, int &t1) {
     t1 = (int)(((long long)(blockIdx.x + 1) * Ttot) / gridDim.x);
 }
 
-// Walks the CTA's tiles in steps of `step` without dividing inside the loop:
-// i = local tile index, g = head, j = tile within the head, hl = g - first head.
-struct TileCursor {
-    int i, g, j, hl, T, n, step;
-    __device__ TileCursor(int t0, int n_, int T_, int start, int step_) : T(T_), n(n_), step(step_) {
-        i = start;
-        g = (t0 + start) / T_;
-        j = (t0 + start) - g * T_;
-        hl = g - t0 / T_;
-    }
-    __device__ bool valid() const { return i < n; }
-    __device__ bool first() const { return j == 0 || i == 0; }
-    __device__ bool last() const { return j == T - 1 || i == n - 1; }
-    __device__ void next() {
-        i += step;
-        j += step;
-        while (j >= T) { j -= T; ++g; ++hl; }
-    }
-};
-
 // ------------------------------------------------------------------ tc_params
 
 constexpr int kParamThreads = 512;
@@ -122,6 +91,7 @@ __global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float v
     float *b = a + K * DR;         // [K][DR]
     float *red = b + K * DR;       // [64] scratch
     float *colmean = red + 64;     // [DR]
+    float *cbuf = colmean + DR;    // [K] per-component constants
     const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int NW = kParamThreads / 32;
     const float *mu_h = mu + (size_t)h * K * DR, *rho_h = rho + (size_t)h * K * DR;
@@ -157,7 +127,6 @@ __global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float v
     }
     __syncthreads();
     // per-component constant c_k, one warp per component
-    float *cvec = reinterpret_cast<float *>(blk + 256u * K);
     for (int k = warp; k < K; k += NW) {
         float logdet = 0.f, musq = 0.f;
         for (int j = lane; j < DR; j += 32) {
@@ -169,7 +138,7 @@ __global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float v
             logdet += __shfl_xor_sync(~0u, logdet, o);
             musq += __shfl_xor_sync(~0u, musq, o);
         }
-        if (lane == 0) cvec[k] = (al[k] - lse) * kLog2e - 0.5f * kLog2e * logdet - 0.5f * musq;
+        if (lane == 0) cbuf[k] = (al[k] - lse) * kLog2e - 0.5f * kLog2e * logdet - 0.5f * musq;
     }
     // mean over components of each quadratic coefficient column (8 threads per column)
     {
@@ -184,121 +153,45 @@ __global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float v
     }
     __syncthreads();
     // centre the quadratic coefficients over k, rescale for the x^2/256 operand, and find max |W|
-    float amax = 0.f;
+    float amax = 0.f, cmax = 0.f;
     for (int e = tid; e < K * DR; e += kParamThreads) {
         const float q = (b[e] - colmean[e % DR]) * 256.0f;
         b[e] = q;
         amax = fmaxf(amax, fmaxf(fabsf(a[e]), fabsf(q)));
     }
-    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
-    if (lane == 0) red[32 + warp] = amax;
+    for (int k = tid; k < K; k += kParamThreads) cmax = fmaxf(cmax, fabsf(cbuf[k]));
+    for (int o = 16; o; o >>= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
+        cmax = fmaxf(cmax, __shfl_xor_sync(~0u, cmax, o));
+    }
+    if (lane == 0) { red[warp] = amax; red[32 + warp] = cmax; }
     __syncthreads();
     amax = 0.f;
-    for (int w = 0; w < NW; ++w) amax = fmaxf(amax, red[32 + w]);
-    // power-of-two scale so that max |W| / scale lies in [2^13, 2^14]
+    cmax = 0.f;
+    for (int w = 0; w < NW; ++w) { amax = fmaxf(amax, red[w]); cmax = fmaxf(cmax, red[32 + w]); }
+    // power-of-two scale: max |W| / scale <= 2^14 and max |c| / scale <= 2^15 (fp16 range)
     int ex = 0;
     if (amax > 0.f && isfinite(amax)) ex = (int)ceilf(log2f(amax)) - 14;
+    if (cmax > 0.f && isfinite(cmax)) ex = max(ex, (int)ceilf(log2f(cmax)) - 15);
     const float inv = exp2f((float)-ex);
-    if (tid == 0) *reinterpret_cast<float *>(blk + 256u * K + 4u * K) = exp2f((float)ex);
+    if (tid == 0) *reinterpret_cast<float *>(blk + param_scale_off(K)) = exp2f((float)ex);
+    // Wc: [c_hi, c_lo, 0 x 14] per component, c_hi + c_lo = c / scale to about 22 bits
+    for (int e = tid; e < K * 2; e += kParamThreads) {
+        const int k = e >> 1, half = e & 1;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (half == 0) {
+            const float cs = cbuf[k] * inv;
+            const float hi = __half2float(__float2half_rn(cs));
+            v.x = pack_f16(hi, cs - hi);
+        }
+        *reinterpret_cast<uint4 *>(blk + param_wc_off(K) + nosw16_off(k, 8 * half)) = v;
+    }
     // fp16 W in the K-major 128-byte-swizzled layout: row k, 8-element chunk j/8, element j%8
     for (int e = tid; e < K * DR / 2; e += kParamThreads) {
         const int k = (2 * e) / DR, j = (2 * e) % DR;
         const uint32_t off = sw128_off(k, j >> 3) + (j & 7) * 2;
         *reinterpret_cast<uint32_t *>(blk + off) = pack_f16(a[2 * e] * inv, a[2 * e + 1] * inv);
         *reinterpret_cast<uint32_t *>(blk + 128u * K + off) = pack_f16(b[2 * e] * inv, b[2 * e + 1] * inv);
-    }
-}
-
-// ------------------------------------------------------------------ wind-down helpers
-
-// Bounded wait that runs to completion (or its time limit) even after another
-// thread raised the CTA's abort flag: used before the CTA releases shared memory
-// or TMEM that in-flight copies or MMAs still touch.
-__device__ __forceinline__ void wait_ignoring_abort(uint64_t *bar, uint32_t parity, unsigned *status) {
-    int never = 0;
-    mbar_wait(bar, parity, Abort{&never, status}, kDevErrTimeout);
-}
-
-// Every TMA load issued into an S-stage ring has landed: waits for the last
-// fill of each stage (fills are issued round-robin, so that is the newest phase).
-__device__ __forceinline__ void wind_down_ring(uint64_t *full, int S, int issued, unsigned *status) {
-    for (int i = issued > S ? issued - S : 0; i < issued; ++i) wait_ignoring_abort(&full[i % S], (i / S) & 1, status);
-}
-
-// ------------------------------------------------------------------ compute helpers
-//
-// Compute warpgroup wg (0 or 1) is warps 3+4wg .. 6+4wg; thread r of the group
-// owns tile row r (= TMEM lane r): warp w accesses TMEM lanes 32*(w % 4) ...
-
-struct RowThread {
-    uint32_t r;          // tile row = TMEM lane
-    uint32_t lane_off;   // TMEM lane field of this warp
-    int wg;              // compute warpgroup
-    int wtid;            // 0..127 inside the group
-};
-
-__device__ __forceinline__ bool wg_all(const RowThread &t, bool v) { return group_all(v, 1 + t.wg, kWgThreads); }
-__device__ __forceinline__ void wg_sync(const RowThread &t) { group_sync(1 + t.wg, kWgThreads); }
-
-// Convert a bf16 row (128 B, swizzled) into the fp16 [x, x^2/256] row of the
-// log-density A operand in TMEM (columns 0-31: x pairs, 32-63: x^2/256 pairs).
-__device__ __forceinline__ void convert_row(const uint8_t *xs, uint32_t r, uint32_t tcol_a) {
-    uint32_t px[32], pq[32];
-    const uint64_t k16 = f2_pack(0.0625f, 0.0625f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(xs + sw128_off(r, j));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float lo = bf16_lo(w[u]), hi = bf16_hi(w[u]);
-            px[4 * j + u] = pack_f16(lo, hi);
-            const uint64_t y = f2_mul(f2_pack(lo, hi), k16);   // x / 16, exact
-            float qa, qb;
-            f2_unpack(f2_mul(y, y), qa, qb);                   // x^2 / 256
-            pq[4 * j + u] = pack_f16(qa, qb);
-        }
-    }
-    tmem_st32(tcol_a, px);
-    tmem_st32(tcol_a + 32, pq);
-}
-
-// All K log2-domain scores s = d * scale + c of this thread's row (one TMEM
-// round trip) and their maximum.
-template <int K>
-__device__ __forceinline__ float row_scores(uint32_t taddr, const float *cvec, uint64_t sc2, float (&s)[K]) {
-    uint32_t d[K];
-#pragma unroll
-    for (int cc = 0; cc < K / 32; ++cc) tmem_ld32(taddr + 32 * cc, d + 32 * cc);
-    tmem_ld_wait();
-#pragma unroll
-    for (int t = 0; t < K; t += 2) {
-        const float2 c = *reinterpret_cast<const float2 *>(cvec + t);
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(d[t]), __uint_as_float(d[t + 1])), sc2, f2_pack(c.x, c.y)),
-                  s[t], s[t + 1]);
-    }
-    float m[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-    for (int t = 4; t + 8 <= K; t += 8) {
-        m[0] = max3(m[0], s[t], s[t + 1]);
-        m[1] = max3(m[1], s[t + 2], s[t + 3]);
-        m[2] = max3(m[2], s[t + 4], s[t + 5]);
-        m[3] = max3(m[3], s[t + 6], s[t + 7]);
-    }
-    m[0] = max3(m[0], s[K - 4], s[K - 3]);
-    m[1] = max3(m[1], s[K - 2], s[K - 1]);
-    return fmaxf(max3(m[0], m[1], m[2]), m[3]);
-}
-
-// 2^(s - m) for K scores, as K/2 bf16 pairs.
-template <int K>
-__device__ __forceinline__ void row_exp(const float (&s)[K], float m, uint32_t (&e)[K / 2]) {
-    const uint64_t nm2 = f2_pack(-m, -m);
-#pragma unroll
-    for (int t = 0; t < K; t += 2) {
-        float a, b;
-        f2_unpack(f2_add(f2_pack(s[t], s[t + 1]), nm2), a, b);
-        e[t / 2] = ex2_bf16x2(pack_bf16(a, b));
     }
 }
 
@@ -316,13 +209,15 @@ struct WriteCfg {
     static constexpr uint32_t OFF_ONES = OFF_V + SV * kTileBytes;      // after every V stage (positive LBO)
     static constexpr uint32_t OFF_G = OFF_ONES + kTileBytes;           // one Gamma buffer per warpgroup
     static constexpr uint32_t OFF_P = OFF_G + 2 * KCH * kTileBytes;
-    static constexpr uint32_t OFF_BAR = OFF_P + PN * PB;
+    static constexpr uint32_t OFF_CA = OFF_P + PN * PB;               // constant [1, 1, 0...] A block
+    static constexpr uint32_t OFF_BAR = OFF_CA + kConstABytes;
     static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;            // barriers + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t wg_cols = 64 + K;
     static constexpr uint32_t col_a(int w) { return w * wg_cols; }
     static constexpr uint32_t col_d1(int w) { return w * wg_cols + 64; }
     static constexpr uint32_t COL_D2 = 2 * wg_cols;
+    static_assert(BYTES <= 232448 && COL_D2 + K <= TMEM_COLS, "write kernel exceeds shared memory or TMEM");
 };
 
 template <int K>
@@ -337,7 +232,10 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     uint64_t *vfull = xempty + SX, *vempty = vfull + SV;
     uint64_t *a_full = vempty + SV, *d1_full = a_full + 2, *g_full = d1_full + 2, *g_empty = g_full + 2;
     uint64_t *w_full = g_empty + 2, *w_empty = w_full + PN;
-    uint64_t *d2_full = w_empty + PN, *d2_empty = d2_full + 1, *fin1 = d2_empty + 1, *fin2 = fin1 + 1;
+    // d2_full[hl & 1]: the accumulation of local head hl is complete.  Two barriers, so the group
+    // that drains head hl (which has seen the accumulation of head hl - 2 complete) is never
+    // more than one phase ahead of the barrier it waits on.
+    uint64_t *d2_full = w_empty + PN, *d2_empty = d2_full + 2, *fin1 = d2_empty + 1, *fin2 = fin1 + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -345,8 +243,6 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     int t0, t1;
     cta_range(A.Ttot, t0, t1);
     const int n = t1 - t0;
-    const int g_first = t0 / A.T;
-    const int nheads = n > 0 ? (t1 - 1) / A.T - g_first + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
@@ -354,11 +250,13 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         for (int b = 0; b < 2; ++b) {
             mbar_init(&a_full[b], 1); mbar_init(&d1_full[b], 1); mbar_init(&g_full[b], 1); mbar_init(&g_empty[b], 1);
         }
-        for (int b = 0; b < PN; ++b) { mbar_init(&w_full[b], 1); mbar_init(&w_empty[b], 3); }
-        mbar_init(d2_full, 1); mbar_init(d2_empty, 1); mbar_init(fin1, 1); mbar_init(fin2, 1);
+        for (int b = 0; b < PN; ++b) { mbar_init(&w_full[b], 1); mbar_init(&w_empty[b], 1); }
+        mbar_init(&d2_full[0], 1); mbar_init(&d2_full[1], 1); mbar_init(d2_empty, 1);
+        mbar_init(fin1, 1); mbar_init(fin2, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
+    init_const_a(sm + C::OFF_CA, threadIdx.x, blockDim.x);
     // ONES atom column: element 0 of every row is 1.0 (bf16), the rest 0.
     for (uint32_t e = threadIdx.x; e < kTileBytes / 16; e += blockDim.x)
         reinterpret_cast<uint4 *>(sm + C::OFF_ONES)[e] = make_uint4(0, 0, 0, 0);
@@ -427,17 +325,13 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     } else if (warp == kWarpMma1) {
         // log-density MMAs: scores(i) = [x, x^2/256](i) . W^T into D1 of warpgroup i & 1
         if (lane == 0 && n > 0) {
-            constexpr uint32_t idesc = idesc_f16(0, 0, 0, 0, TM, K);
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
                 const int i = c.i, b = c.hl % PN, w = i & 1;
                 if (c.first() && !mbar_wait(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
                 if (!mbar_wait(&a_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
-                const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_P + b * C::PB), 16, 1024);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tmem + C::col_d1(w), tmem + C::col_a(w) + ks * 8,
-                           bd + (uint64_t)(((ks >> 2) * 128u * K + (ks & 3) * 32u) >> 4), idesc, ks > 0);
+                issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
+                                    smem_u32(sm + C::OFF_CA));
                 mma_commit(&d1_full[w]);
                 if (c.last()) mma_commit(&w_empty[b]);
             }
@@ -465,7 +359,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                            !(first && ks == 0));
                 mma_commit(&g_empty[w]);
                 mma_commit(&vempty[s]);
-                if (c.last()) mma_commit(d2_full);
+                if (c.last()) mma_commit(&d2_full[c.hl & 1]);
             }
             mma_commit(fin2);
             wait_ignoring_abort(fin2, 0, A.status);
@@ -479,13 +373,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         rt.wtid = threadIdx.x - kWarpCompute * 32 - rt.wg * kWgThreads;
         const int w = rt.wg;
         const bool elected = rt.wtid == 0;
-        int release_next = 0;
-        auto release_upto = [&](int hl_excl) {
-            for (; release_next < hl_excl; ++release_next)
-                if (elected) mbar_arrive(&w_empty[release_next % PN]);
-        };
         TileCursor c(t0, n, A.T, w, 2);
-        release_upto(c.valid() ? c.hl : nheads);
         for (; c.valid(); c.next()) {
             const int i = c.i, hl = c.hl;
             // convert tile i into this group's A operand
@@ -497,18 +385,13 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             wg_sync(rt);
             if (elected) { mbar_arrive(&a_full[w]); mbar_arrive(&xempty[i % SX]); }
             // softmax of tile i (Eq. 3b); rows past the sequence end get Gamma = 0
+            const float scale = head_scale(A.params, A.param_stride, c.g % A.H, K);
             ok = mbar_wait(&d1_full[w], (i >> 1) & 1, ab, kDevErrTimeout);
-            ok = ok && mbar_wait(&w_full[hl % PN], (hl / PN) & 1, ab, kDevErrTimeout);
             if (i >= 2) ok = ok && mbar_wait(&g_empty[w], ((i >> 1) - 1) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
-            const uint8_t *pblk = sm + C::OFF_P + (hl % PN) * C::PB;
-            const float *cvec = reinterpret_cast<const float *>(pblk + 256u * K);
-            const float scale = *reinterpret_cast<const float *>(pblk + 256u * K + 4u * K);
-            float sc[K];
-            const float mx = row_scores<K>(tmem + rt.lane_off + C::col_d1(w), cvec, f2_pack(scale, scale), sc);
             uint32_t e[K / 2];
-            row_exp<K>(sc, mx, e);
+            row_exp_scaled<K>(tmem + rt.lane_off + C::col_d1(w), scale, e);
             uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int t = 0; t < K / 2; ++t) acc[t & 3] = f2_add(acc[t & 3], f2_pack(bf16_lo(e[t]), bf16_hi(e[t])));
@@ -536,16 +419,10 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             tc_fence_before();
             wg_sync(rt);
             if (elected) mbar_arrive(&g_full[w]);
-            const bool last = c.last();
             const int g = c.g;
-            {
-                TileCursor nx = c;
-                nx.next();
-                release_upto(nx.valid() ? nx.hl : nheads);
-            }
-            if (last) {
+            if (c.last()) {
                 // drain [Vt | Z]^T of this head into partial slot (cta + head)
-                ok = mbar_wait(d2_full, hl & 1, ab, kDevErrTimeout);
+                ok = mbar_wait(&d2_full[hl & 1], (hl >> 1) & 1, ab, kDevErrTimeout);
                 if (!wg_all(rt, ok)) break;
                 tc_fence_after();
                 float *dst = A.partials + ((size_t)(blockIdx.x + g) * (DVV + 1) + rt.r) * K;
@@ -565,7 +442,6 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 if (elected) mbar_arrive(d2_empty);
             }
         }
-        release_upto(nheads);
     }
     tc_fence_before();
     __syncthreads();
@@ -608,7 +484,7 @@ __global__ void __launch_bounds__(256) tc_reduce_kernel(int K, int T, int Ttot, 
 
 template <int K>
 struct ReadCfg {
-    static constexpr int SX = K <= 64 ? 6 : 5;
+    static constexpr int SX = K <= 64 ? 6 : 4;
     static constexpr int PN = 2;
     static constexpr uint32_t PB = align1k(param_bytes(K));
     static constexpr uint32_t MB = align1k(mem_bytes(K));
@@ -616,13 +492,15 @@ struct ReadCfg {
     static constexpr uint32_t OFF_O = OFF_X + SX * kTileBytes;         // one output staging tile per group
     static constexpr uint32_t OFF_P = OFF_O + 2 * kTileBytes;
     static constexpr uint32_t OFF_M = OFF_P + PN * PB;
-    static constexpr uint32_t OFF_BAR = OFF_M + PN * MB;
+    static constexpr uint32_t OFF_CA = OFF_M + PN * MB;                // constant [1, 1, 0...] A block
+    static constexpr uint32_t OFF_BAR = OFF_CA + kConstABytes;
     static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int NOUT = 80;                                    // [Vt | Z | 1 | 0...]
     static constexpr uint32_t wg_cols = NOUT + K;
     static constexpr uint32_t col_a(int w) { return w * wg_cols; }     // A operand, later D2 (same columns)
     static constexpr uint32_t col_d1(int w) { return w * wg_cols + NOUT; }
+    static_assert(BYTES <= 232448 && 2 * wg_cols <= TMEM_COLS, "read kernel exceeds shared memory or TMEM");
 };
 
 template <int K>
@@ -644,20 +522,20 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     int t0, t1;
     cta_range(A.Ttot, t0, t1);
     const int n = t1 - t0;
-    const int g_first = t0 / A.T;
-    const int nheads = n > 0 ? (t1 - 1) / A.T - g_first + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&a_full[b], 1); mbar_init(&d1_full[b], 1); mbar_init(&e_full[b], 1); mbar_init(&d2_full[b], 1);
         }
-        for (int b = 0; b < PN; ++b) { mbar_init(&w_full[b], 1); mbar_init(&w_empty[b], 3); }
+        for (int b = 0; b < PN; ++b) { mbar_init(&w_full[b], 1); mbar_init(&w_empty[b], 1); }
         mbar_init(fin1, 1); mbar_init(fin2, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
+    init_const_a(sm + C::OFF_CA, threadIdx.x, blockDim.x);
     if (warp == kWarpMma1) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -708,17 +586,13 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     } else if (warp == kWarpMma1) {
         if (lane == 0 && n > 0) {
-            constexpr uint32_t idesc = idesc_f16(0, 0, 0, 0, TM, K);
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
                 const int i = c.i, b = c.hl % PN, w = i & 1;
                 if (c.first() && !mbar_wait(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
                 if (!mbar_wait(&a_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
-                const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_P + b * C::PB), 16, 1024);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tmem + C::col_d1(w), tmem + C::col_a(w) + ks * 8,
-                           bd + (uint64_t)(((ks >> 2) * 128u * K + (ks & 3) * 32u) >> 4), idesc, ks > 0);
+                issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
+                                    smem_u32(sm + C::OFF_CA));
                 mma_commit(&d1_full[w]);
             }
             mma_commit(fin1);
@@ -751,15 +625,9 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         rt.wtid = threadIdx.x - kWarpCompute * 32 - rt.wg * kWgThreads;
         const int w = rt.wg;
         const bool elected = rt.wtid == 0;
-        int release_next = 0;
-        auto release_upto = [&](int hl_excl) {
-            for (; release_next < hl_excl; ++release_next)
-                if (elected) mbar_arrive(&w_empty[release_next % PN]);
-        };
         TileCursor c(t0, n, A.T, w, 2);
-        release_upto(c.valid() ? c.hl : nheads);
         for (; c.valid(); c.next()) {
-            const int i = c.i, hl = c.hl;
+            const int i = c.i;
             bool ok = mbar_wait(&xfull[i % SX], (i / SX) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             convert_row(sm + C::OFF_X + (i % SX) * kTileBytes, rt.r, tmem + rt.lane_off + C::col_a(w));
@@ -767,21 +635,16 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_before();
             wg_sync(rt);
             if (elected) { mbar_arrive(&a_full[w]); mbar_arrive(&xempty[i % SX]); }
+            const float scale = head_scale(A.params, A.param_stride, c.g % A.H, K);
             ok = mbar_wait(&d1_full[w], (i >> 1) & 1, ab, kDevErrTimeout);
-            ok = ok && mbar_wait(&w_full[hl % PN], (hl / PN) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
-            const uint8_t *pblk = sm + C::OFF_P + (hl % PN) * C::PB;
-            const float *cvec = reinterpret_cast<const float *>(pblk + 256u * K);
-            const float scale = *reinterpret_cast<const float *>(pblk + 256u * K + 4u * K);
             const uint32_t d1 = tmem + rt.lane_off + C::col_d1(w);
             {
                 // unnormalised responsibilities (the row scale cancels in num / den),
                 // bf16 pairs written over the first K/2 score columns
-                float sc[K];
-                const float mx = row_scores<K>(d1, cvec, f2_pack(scale, scale), sc);
                 uint32_t e[K / 2];
-                row_exp<K>(sc, mx, e);
+                row_exp_scaled<K>(d1, scale, e);
 #pragma unroll
                 for (int cc = 0; cc < K / 64; ++cc) tmem_st32(d1 + 32 * cc, e + 32 * cc);
             }
@@ -790,11 +653,6 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             wg_sync(rt);
             if (elected) mbar_arrive(&e_full[w]);
             const int g = c.g, row0 = c.j * TM;
-            {
-                TileCursor nx = c;
-                nx.next();
-                release_upto(nx.valid() ? nx.hl : nheads);
-            }
             // epilogue: out = num / (den + eps * sum_k e_k)
             ok = mbar_wait(&d2_full[w], (i >> 1) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
@@ -829,7 +687,6 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 bulk_commit_group();
             }
         }
-        release_upto(nheads);
         if (elected) bulk_wait_group<0>();
     }
     tc_fence_before();
@@ -842,45 +699,6 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 }
 
 // ------------------------------------------------------------------ host side
-
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                 CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn() {
-    static EncodeTiled fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(p);
-    });
-    return fn;
-}
-
-// 3D bf16 tensor map over [G][N][width], box [1][128][64], 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, int G, int N, int width) {
-    EncodeTiled enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)N, (cuuint64_t)G};
-    const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * N};
-    const cuuint32_t box[3] = {64, TM, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
 
 template <int K>
 cudaError_t launch_write(const Problem &p, const TcLayout &L, const void *Kx, const void *V, char *ws,
@@ -945,7 +763,7 @@ TcLayout tc_layout(const Problem &p) {
 
 cudaError_t tc_params(const Problem &p, const TcLayout &L, const float *mu, const float *rho,
                       const float *alpha, char *ws, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (2 * (size_t)p.K * DR + 64 + DR);
+    const size_t smem = sizeof(float) * (2 * (size_t)p.K * DR + 64 + DR + p.K);
     cudaError_t e = cudaFuncSetAttribute(tc_params_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     tc_params_kernel<<<p.H, kParamThreads, smem, s>>>(p.K, p.var_floor, mu, rho, alpha,

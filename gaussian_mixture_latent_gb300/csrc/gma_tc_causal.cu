@@ -1,0 +1,478 @@
+// Tensor-core (tcgen05) causal GMA forward as a chunked scan, for bf16 inputs
+// and outputs, d = 64, dv = 64, K = 64.
+//
+// "Gaussian Mixture Attention" (Huang & Raza, 2026), section 3.5: prefix
+// memories over j <= i (Eq. 6b) read by each position (Eq. 8b), equivalently
+// the masked affinity of Eq. 9b-10b.  Positions are processed in chunks of
+// 128 rows; for chunk c with rows i, j inside the chunk:
+//
+//   e^Q_i      = 2^(s_i - max s_i)      unnormalised query responsibilities
+//   gamma^K_j  = softmax(s_j)           key responsibilities (Eq. 3b)
+//   T_ij       = [j <= i] e^Q_i . gamma^K_j                  (intra-chunk, Eq. 9b)
+//   num_i      = e^Q_i S_{c-1} + sum_j T_ij V_j
+//   den_i      = e^Q_i z_{c-1} + sum_j T_ij + eps * sum_k e^Q_ik
+//   O_i        = num_i / den_i
+//   [S | z]_c  = [S | z]_{c-1} + gamma^K^T [V | 1]           (state after the chunk)
+//
+// The unnormalised e^Q scales numerator and denominator by the same factor,
+// so only eps needs sum_k e^Q_ik.  The state [S | z]^T accumulates in TMEM in
+// fp32 and is snapshotted as a bf16 MMA operand once per chunk; every
+// reduction has a fixed order, so results are bitwise reproducible, and row i
+// never reads rows after i (the mask selects, it does not multiply).
+//
+// One CTA per head.  Warps: 0 TMA producer; 1 TMEM owner and issuer of the
+// log-density MMAs (keys, then queries); 2 issuer of the chained MMAs (T, the
+// state update, the read); 3-6 key group (convert, softmax, state snapshot);
+// 7-10 query group (convert, exp); 11-14 output group (mask, epilogue, store).
+// Every mbarrier wait is bounded; a timeout posts GMA_ERR_TIMEOUT.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "gma_internal.h"
+#include "gma_sm100.cuh"
+#include "gma_tc_common.cuh"
+
+namespace gma {
+
+using namespace sm100;
+using namespace tc;
+
+namespace {
+
+constexpr int KC = 64;                 // components handled by this kernel
+constexpr int kCThreads = 480;         // 15 warps
+constexpr int kWProd = 0, kWIss1 = 1, kWIss2 = 2, kWGroups = 3;
+constexpr int NOUT = 80;               // [S | z | 1 | 0...] and [V | 1 | 0...] widths
+
+struct CausalArgs {
+    int G, H, N, nch;
+    const uint8_t *params;
+    uint32_t param_stride;
+    float eps;
+    unsigned *status;
+};
+
+struct CausalCfg {
+    static constexpr uint32_t PB = align1k(param_bytes(KC));
+    static constexpr uint32_t SBB = 80u * 128u;                        // state operand [80 rows][64 k] bf16
+    static constexpr uint32_t OFF_Q = 0;                               // 2 stages
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * kTileBytes;          // 2 stages
+    static constexpr uint32_t OFF_V = OFF_K + 2 * kTileBytes;          // 2 stages
+    static constexpr uint32_t OFF_ONES = OFF_V + 2 * kTileBytes;       // after the V stages (positive LBO)
+    static constexpr uint32_t OFF_G = OFF_ONES + kTileBytes;           // gamma^K [row][k]
+    static constexpr uint32_t OFF_TB = OFF_G + kTileBytes;             // masked T, bf16 [row][key], 2 chunks
+    static constexpr uint32_t OFF_SB = OFF_TB + 2 * kTileBytes;        // state operand, 2 buffers
+    static constexpr uint32_t OFF_P = OFF_SB + 2 * SBB;
+    static constexpr uint32_t OFF_O = OFF_P + PB;                      // output staging tile
+    static constexpr uint32_t OFF_CA = OFF_O + kTileBytes;             // constant [1, 1, 0...] A block
+    static constexpr uint32_t OFF_BAR = OFF_CA + kConstABytes;
+    static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;
+    // TMEM columns
+    static constexpr uint32_t COL_AQ = 0, COL_D1Q = 64, COL_AK = 128, COL_D1K = 192;
+    static constexpr uint32_t COL_TD = 256;                            // T (128 fp32), then the read result
+    static constexpr uint32_t COL_S = 384;                             // [S | z]^T state, 64 columns
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+static_assert(CausalCfg::OFF_SB % 1024 == 0 && CausalCfg::OFF_P % 1024 == 0 && CausalCfg::OFF_O % 1024 == 0,
+              "operand blocks must be 1024-byte aligned");
+static_assert(CausalCfg::BYTES <= 232448, "causal kernel exceeds the shared-memory opt-in limit");
+
+__global__ void __launch_bounds__(kCThreads, 1)
+tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 CausalArgs A) {
+    using C = CausalCfg;
+    constexpr int K = KC;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
+    uint64_t *qfull = bars, *qempty = qfull + 2, *kfull = qempty + 2, *kempty = kfull + 2;
+    uint64_t *vfull = kempty + 2, *vempty = vfull + 2;
+    uint64_t *w_full = vempty + 2, *ak_full = w_full + 1, *d1k_full = ak_full + 1, *aq_full = d1k_full + 1;
+    uint64_t *d1q_full = aq_full + 1, *g_full = d1q_full + 1, *g_empty = g_full + 1, *e_full = g_empty + 1;
+    uint64_t *t_full = e_full + 1, *tb_full = t_full + 1, *d3_full = tb_full + 1, *d3_empty = d3_full + 1;
+    uint64_t *s_upd = d3_empty + 1, *s_ready = s_upd + 1, *sb_empty = s_ready + 2;
+    uint64_t *fin1 = sb_empty + 2, *fin2 = fin1 + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = blockIdx.x, nch = A.nch;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&qfull[s], 1); mbar_init(&qempty[s], 1); mbar_init(&kfull[s], 1); mbar_init(&kempty[s], 1);
+            mbar_init(&vfull[s], 1); mbar_init(&vempty[s], 1); mbar_init(&s_ready[s], 1); mbar_init(&sb_empty[s], 1);
+        }
+        for (uint64_t *b = w_full; b <= s_upd; ++b) mbar_init(b, 1);
+        mbar_init(fin1, 1); mbar_init(fin2, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // ONES atom column (element 0 of every row = 1.0 bf16) and the constant rows of both
+    // state operands: row 65 = 1 (gives sum_k e^Q_ik), rows 66..79 = 0, rows 0..64 of buffer 0 = 0
+    // (the state before the first chunk).
+    for (uint32_t e = threadIdx.x; e < kTileBytes / 16; e += blockDim.x)
+        reinterpret_cast<uint4 *>(sm + C::OFF_ONES)[e] = make_uint4(0, 0, 0, 0);
+    for (uint32_t e = threadIdx.x; e < 2 * C::SBB / 16; e += blockDim.x) {
+        const uint32_t row = (e * 16u % C::SBB) / 128u;
+        const uint32_t v = row == DVV + 1 ? 0x3F803F80u : 0u;
+        reinterpret_cast<uint4 *>(sm + C::OFF_SB)[e] = make_uint4(v, v, v, v);
+    }
+    init_const_a(sm + C::OFF_CA, threadIdx.x, blockDim.x);
+    __syncthreads();
+    if (threadIdx.x < TM) *reinterpret_cast<uint16_t *>(sm + C::OFF_ONES + sw128_off(threadIdx.x, 0)) = 0x3F80u;
+    if (warp == kWIss1) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Abort ab{abort_flag, A.status};
+    if (threadIdx.x == 0) mbar_arrive(&s_ready[0]);              // state operand for chunk 0 is ready
+
+    if (warp == kWProd) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(w_full, param_bytes(K));
+            bulk_load(sm + C::OFF_P, A.params + (size_t)(g % A.H) * A.param_stride, param_bytes(K), w_full);
+            int qi = 0, ki = 0, vi = 0;
+            long long last = clock64();
+            while ((qi < nch || ki < nch || vi < nch) && !*abort_flag) {
+                bool progress = false;
+                if (ki < nch && (ki < 2 || mbar_test(&kempty[ki & 1], ((ki >> 1) - 1) & 1))) {
+                    mbar_arrive_expect_tx(&kfull[ki & 1], kTileBytes);
+                    tma_load_3d(sm + C::OFF_K + (ki & 1) * kTileBytes, &tm_k, &kfull[ki & 1], 0, ki * TM, g);
+                    ++ki;
+                    progress = true;
+                }
+                if (qi < nch && (qi < 2 || mbar_test(&qempty[qi & 1], ((qi >> 1) - 1) & 1))) {
+                    mbar_arrive_expect_tx(&qfull[qi & 1], kTileBytes);
+                    tma_load_3d(sm + C::OFF_Q + (qi & 1) * kTileBytes, &tm_q, &qfull[qi & 1], 0, qi * TM, g);
+                    ++qi;
+                    progress = true;
+                }
+                if (vi < nch && (vi < 2 || mbar_test(&vempty[vi & 1], ((vi >> 1) - 1) & 1))) {
+                    mbar_arrive_expect_tx(&vfull[vi & 1], kTileBytes);
+                    tma_load_3d(sm + C::OFF_V + (vi & 1) * kTileBytes, &tm_v, &vfull[vi & 1], 0, vi * TM, g);
+                    ++vi;
+                    progress = true;
+                }
+                if (progress) {
+                    last = clock64();
+                } else {
+                    __nanosleep(64);
+                    if (clock64() - last > kWaitLimitCycles) {
+                        *abort_flag = 1;
+                        atomicOr(A.status, kDevErrTimeout);
+                    }
+                }
+            }
+            wind_down_ring(kfull, 2, ki, A.status);
+            wind_down_ring(qfull, 2, qi, A.status);
+            wind_down_ring(vfull, 2, vi, A.status);
+            wait_ignoring_abort(w_full, 0, A.status);
+        }
+    } else if (warp == kWIss1) {
+        // log-density MMAs: scores = [x, x^2/256] . W^T, keys then queries of each chunk
+        if (lane == 0) {
+            const uint32_t pw = smem_u32(sm + C::OFF_P), ca = smem_u32(sm + C::OFF_CA);
+            bool ok = mbar_wait(w_full, 0, ab, kDevErrTimeout);
+            for (int c = 0; c < nch && ok; ++c) {
+                if (!(ok = mbar_wait(ak_full, c & 1, ab, kDevErrTimeout))) break;
+                tc_fence_after();
+                issue_logdensity<K>(tmem + C::COL_D1K, tmem + C::COL_AK, pw, ca);
+                mma_commit(d1k_full);
+                if (!(ok = mbar_wait(aq_full, c & 1, ab, kDevErrTimeout))) break;
+                // the query scores overwrite e^Q of the previous chunk: wait for its last reader
+                if (c >= 1 && !(ok = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout))) break;
+                tc_fence_after();
+                issue_logdensity<K>(tmem + C::COL_D1Q, tmem + C::COL_AQ, pw, ca);
+                mma_commit(d1q_full);
+            }
+            mma_commit(fin1);
+            wait_ignoring_abort(fin1, 0, A.status);
+        }
+    } else if (warp == kWIss2) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_t = idesc_f16(1, 1, 0, 0, TM, TM);      // e^Q (TMEM) . gamma^K^T
+            constexpr uint32_t idesc_u = idesc_f16(1, 1, 1, 1, TM, K);       // [V | 1]^T . gamma^K
+            constexpr uint32_t idesc_r1 = idesc_f16(1, 1, 0, 0, TM, NOUT);   // e^Q . [S | z | 1]
+            constexpr uint32_t idesc_r2 = idesc_f16(1, 1, 0, 1, TM, NOUT);   // T . [V | 1]
+            const uint32_t gaddr = smem_u32(sm + C::OFF_G), ones = smem_u32(sm + C::OFF_ONES);
+            const uint64_t gk = sdesc_sw128(gaddr, 16, 1024);                // gamma^K as K-major B (N = keys)
+            const uint64_t gm = sdesc_sw128(gaddr, kTileBytes, 1024);        // gamma^K as MN-major B (N = k)
+            const uint64_t tbd = sdesc_sw128(smem_u32(sm + C::OFF_TB), 16, 1024);
+            bool ok = true;
+            for (int c = 0; c < nch && ok; ++c) {
+                const int s = c & 1;
+                // T(c) = e^Q(c) . gamma^K(c)^T into the T / read columns
+                ok = mbar_wait(e_full, c & 1, ab, kDevErrTimeout) && mbar_wait(g_full, c & 1, ab, kDevErrTimeout);
+                if (ok && c >= 1) ok = mbar_wait(d3_empty, (c - 1) & 1, ab, kDevErrTimeout);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks)
+                    mma_ts(tmem + C::COL_TD, tmem + C::COL_D1Q + ks * 8, gk + (uint64_t)((ks * 32u) >> 4), idesc_t,
+                           ks > 0);
+                mma_commit(t_full);
+                // state update: [S | z]^T += [V | 1 | 0]^T . gamma^K, once the previous state is snapshotted
+                if (!(ok = mbar_wait(&vfull[s], (c >> 1) & 1, ab, kDevErrTimeout) &&
+                           mbar_wait(&s_ready[c & 1], (c >> 1) & 1, ab, kDevErrTimeout)))
+                    break;
+                tc_fence_after();
+                const uint32_t va = smem_u32(sm + C::OFF_V + s * kTileBytes);
+                const uint64_t vd = sdesc_sw128(va, ones - va, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tmem + C::COL_S, vd + (uint64_t)(ks * 128), gm + (uint64_t)(ks * 128), idesc_u,
+                           !(c == 0 && ks == 0));
+                mma_commit(s_upd);
+                mma_commit(g_empty);
+                // read: e^Q . [S | z | 1]_{c-1} + mask(T) . [V | 1]
+                if (!(ok = mbar_wait(tb_full, c & 1, ab, kDevErrTimeout))) break;
+                tc_fence_after();
+                const uint64_t sbd = sdesc_sw128(smem_u32(sm + C::OFF_SB + (c & 1) * C::SBB), 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks)
+                    mma_ts(tmem + C::COL_TD, tmem + C::COL_D1Q + ks * 8, sbd + (uint64_t)((ks * 32u) >> 4), idesc_r1,
+                           ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tmem + C::COL_TD, tbd + (uint64_t)(((ks >> 2) * kTileBytes + (ks & 3) * 32u) >> 4),
+                           vd + (uint64_t)(ks * 128), idesc_r2, 1);
+                mma_commit(d3_full);
+                mma_commit(&sb_empty[c & 1]);
+                mma_commit(&vempty[s]);
+            }
+            mma_commit(fin2);
+            wait_ignoring_abort(fin2, 0, A.status);
+        }
+    } else {
+        RowThread rt;
+        rt.wg = (warp - kWGroups) >> 2;
+        rt.r = 32u * (warp & 3) + lane;
+        rt.lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        rt.wtid = threadIdx.x - kWGroups * 32 - rt.wg * kWgThreads;
+        const bool elected = rt.wtid == 0;
+        const float scale = head_scale(A.params, A.param_stride, g % A.H, K);
+
+        if (rt.wg == 0) {
+            // ---------------- key group
+            auto convert_k = [&](int c) -> bool {
+                const bool w = mbar_wait(&kfull[c & 1], (c >> 1) & 1, ab, kDevErrTimeout);
+                if (!wg_all(rt, w)) return false;
+                convert_row(sm + C::OFF_K + (c & 1) * kTileBytes, rt.r, tmem + rt.lane_off + C::COL_AK);
+                tmem_st_wait();
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) { mbar_arrive(ak_full); mbar_arrive(&kempty[c & 1]); }
+                return true;
+            };
+            bool ok = convert_k(0);
+            for (int c = 0; c < nch && ok; ++c) {
+                bool w = mbar_wait(d1k_full, c & 1, ab, kDevErrTimeout);
+                if (c >= 1) w = w && mbar_wait(g_empty, (c - 1) & 1, ab, kDevErrTimeout);
+                if (!(ok = wg_all(rt, w))) break;
+                tc_fence_after();
+                // gamma^K = softmax of the key scores; rows past the sequence end get 0
+                uint32_t e[K / 2];
+                row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1K, scale, e);
+                uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int t = 0; t < K / 2; ++t) acc[t & 3] = f2_add(acc[t & 3], f2_pack(bf16_lo(e[t]), bf16_hi(e[t])));
+                float s0, s1, s2, s3, s4, s5, s6, s7;
+                f2_unpack(acc[0], s0, s1); f2_unpack(acc[1], s2, s3);
+                f2_unpack(acc[2], s4, s5); f2_unpack(acc[3], s6, s7);
+                const float total = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+                const float inv = c * TM + (int)rt.r < A.N ? 1.0f / total : 0.f;
+                const uint64_t inv2 = f2_pack(inv, inv);
+#pragma unroll
+                for (int j = 0; j < K / 8; ++j) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float ga, gb;
+                        f2_unpack(f2_mul(f2_pack(bf16_lo(e[4 * j + u]), bf16_hi(e[4 * j + u])), inv2), ga, gb);
+                        wv[u] = pack_bf16(ga, gb);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + C::OFF_G + sw128_off(rt.r, j)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) mbar_arrive(g_full);
+                if (c + 1 >= nch) break;
+                if (!(ok = convert_k(c + 1))) break;
+                // bf16 snapshot of the state after chunk c, the read operand of chunk c + 1
+                const int b = (c + 1) & 1;
+                w = mbar_wait(s_upd, c & 1, ab, kDevErrTimeout);
+                if (c + 1 >= 2) w = w && mbar_wait(&sb_empty[b], (((c + 1) >> 1) - 1) & 1, ab, kDevErrTimeout);
+                if (!(ok = wg_all(rt, w))) break;
+                tc_fence_after();
+                uint32_t v[K];
+                tmem_ld32(tmem + rt.lane_off + C::COL_S, v);
+                tmem_ld32(tmem + rt.lane_off + C::COL_S + 32, v + 32);
+                tmem_ld_wait();
+                if (rt.r <= DVV) {
+                    uint8_t *row = sm + C::OFF_SB + b * C::SBB;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 o;
+                        o.x = pack_bf16(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                        o.y = pack_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                        o.z = pack_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                        o.w = pack_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                        *reinterpret_cast<uint4 *>(row + sw128_off(rt.r, j)) = o;
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) mbar_arrive(&s_ready[b]);
+            }
+        } else if (rt.wg == 1) {
+            // ---------------- query group
+            auto convert_q = [&](int c) -> bool {
+                const bool w = mbar_wait(&qfull[c & 1], (c >> 1) & 1, ab, kDevErrTimeout);
+                if (!wg_all(rt, w)) return false;
+                convert_row(sm + C::OFF_Q + (c & 1) * kTileBytes, rt.r, tmem + rt.lane_off + C::COL_AQ);
+                tmem_st_wait();
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) { mbar_arrive(aq_full); mbar_arrive(&qempty[c & 1]); }
+                return true;
+            };
+            bool ok = convert_q(0);
+            for (int c = 0; c < nch && ok; ++c) {
+                const bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
+                if (!(ok = wg_all(rt, w))) break;
+                tc_fence_after();
+                const uint32_t d1 = tmem + rt.lane_off + C::COL_D1Q;
+                {
+                    uint32_t e[K / 2];
+                    row_exp_scaled<K>(d1, scale, e);
+                    tmem_st32(d1, e);                      // e^Q as bf16 pairs over the scores
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) mbar_arrive(e_full);
+                if (c + 1 < nch && !(ok = convert_q(c + 1))) break;
+            }
+        } else {
+            // ---------------- output group
+            for (int c = 0; c < nch; ++c) {
+                bool w = mbar_wait(t_full, c & 1, ab, kDevErrTimeout);
+                if (!wg_all(rt, w)) break;
+                tc_fence_after();
+                // causal mask inside the chunk: keep key j <= query row r (selected, never multiplied)
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + rt.lane_off + C::COL_TD + 32 * cc, v);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const uint32_t j0 = 32u * cc + 2 * t;
+                        const float a = j0 <= rt.r ? __uint_as_float(v[2 * t]) : 0.f;
+                        const float b2 = j0 + 1 <= rt.r ? __uint_as_float(v[2 * t + 1]) : 0.f;
+                        pk[t] = pack_bf16(a, b2);
+                    }
+                    uint8_t *tb = sm + C::OFF_TB + (cc >> 1) * kTileBytes;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        *reinterpret_cast<uint4 *>(tb + sw128_off(rt.r, (cc & 1) * 4 + q4)) =
+                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) mbar_arrive(tb_full);
+                // epilogue: out = num / (den + eps * sum_k e^Q_k)
+                w = mbar_wait(d3_full, c & 1, ab, kDevErrTimeout);
+                if (!wg_all(rt, w)) break;
+                tc_fence_after();
+                uint32_t v0[32], v1[32], dz[4];
+                tmem_ld32(tmem + rt.lane_off + C::COL_TD, v0);
+                tmem_ld32(tmem + rt.lane_off + C::COL_TD + 32, v1);
+                tmem_ld4(tmem + rt.lane_off + C::COL_TD + 64, dz);
+                tmem_ld_wait();
+                const float rd = 1.0f / (__uint_as_float(dz[0]) + A.eps * __uint_as_float(dz[1]));
+                const uint64_t rd2 = f2_pack(rd, rd);
+                if (elected) bulk_wait_group_read<0>();          // the previous store has left the staging tile
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) mbar_arrive(d3_empty);
+                uint8_t *ob = sm + C::OFF_O;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t *src = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+                    uint32_t o[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float oa, obv;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(src[2 * u]), __uint_as_float(src[2 * u + 1])), rd2),
+                                  oa, obv);
+                        o[u] = pack_bf16(oa, obv);
+                    }
+                    *reinterpret_cast<uint4 *>(ob + sw128_off(rt.r, j)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                fence_proxy_async_smem();
+                wg_sync(rt);
+                if (elected) {
+                    tma_store_3d(&tm_o, ob, 0, c * TM, g);
+                    bulk_commit_group();
+                }
+            }
+            if (elected) bulk_wait_group<0>();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWIss1) {
+        __syncwarp();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+bool tc_causal_supported(const Problem &p) {
+    return p.in_dtype == GMA_BF16 && p.out_dtype == GMA_BF16 && p.causal && p.d == DR && p.dv == DVV &&
+           p.K == KC && p.N > 0;
+}
+
+TcLayout tc_causal_layout(const Problem &p) {
+    TcLayout L{};
+    L.T = (p.N + TM - 1) / TM;
+    L.Ttot = L.T * p.G;
+    L.ncta = p.G;
+    L.param_stride = align1k(param_bytes(p.K));
+    L.params = align_up(kHeaderBytes);
+    L.part = L.mem = L.params + (size_t)p.H * L.param_stride;
+    L.total = align_up(L.part);
+    return L;
+}
+
+cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
+                      void *out, char *ws, cudaStream_t s) {
+    CUtensorMap tq, tk, tv, to;
+    if (!make_map(&tq, Qx, p.G, p.N, DR) || !make_map(&tk, Kx, p.G, p.N, DR) || !make_map(&tv, V, p.G, p.N, DVV) ||
+        !make_map(&to, out, p.G, p.N, DVV))
+        return cudaErrorInvalidValue;
+    CausalArgs a{};
+    a.G = p.G; a.H = p.H; a.N = p.N; a.nch = L.T;
+    a.params = reinterpret_cast<const uint8_t *>(ws + L.params);
+    a.param_stride = L.param_stride;
+    a.eps = p.eps;
+    a.status = reinterpret_cast<unsigned *>(ws);
+    cudaError_t e = cudaFuncSetAttribute(tc_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         CausalCfg::BYTES);
+    if (e != cudaSuccess) return e;
+    tc_causal_kernel<<<p.G, kCThreads, CausalCfg::BYTES, s>>>(tq, tk, tv, to, a);
+    return cudaGetLastError();
+}
+
+}  // namespace gma

@@ -1,0 +1,227 @@
+// Shared pieces of the tensor-core kernels (bidirectional and causal):
+// tile geometry, the per-head parameter block produced by tc_params, the
+// conversion of a bf16 routing tile into the fp16 [x, x^2/256] MMA operand,
+// the row softmax helpers, wind-down waits, and host-side TMA descriptors.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "gma_sm100.cuh"
+
+namespace gma {
+namespace tc {
+
+using namespace sm100;
+
+constexpr int TM = 128;            // rows per tile
+constexpr int DR = 64;             // routing dimension handled by this path
+constexpr int DVV = 64;            // value dimension handled by this path
+constexpr int kWgThreads = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kTileBytes = TM * 128;   // one 128-row x 128-byte swizzled tile
+
+__host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+
+// Per-head parameter block written by tc_params, all fp16 MMA B operands:
+//   W chunk 0 (K x 128 B, 128-byte swizzle): linear coefficients
+//   W chunk 1 (K x 128 B, 128-byte swizzle): quadratic coefficients
+//   Wc        (K x 32 B, no swizzle): [c_hi, c_lo, 0...] so that the constant
+//             k-step [1, 1, 0...] adds c_k exactly to ~22 bits
+//   scale     f32 (+ pad): the power of two W was divided by
+__host__ __device__ constexpr uint32_t param_wc_off(int K) { return 256u * K; }
+__host__ __device__ constexpr uint32_t param_scale_off(int K) { return 288u * K; }
+__host__ __device__ constexpr uint32_t param_bytes(int K) { return 288u * K + 16u; }
+constexpr uint32_t kConstABytes = TM * 32;   // [1, 1, 0 x 14] fp16 for every tile row, no swizzle
+
+// Byte offset of fp16 element (row, col < 16) in a no-swizzle K-major block of
+// 16-column rows: 8-row x 16-byte core matrices, column halves 128 B apart,
+// 8-row groups 256 B apart.
+__host__ __device__ constexpr uint32_t nosw16_off(uint32_t row, uint32_t col) {
+    return (row >> 3) * 256u + (col >> 3) * 128u + (row & 7u) * 16u + (col & 7u) * 2u;
+}
+// Per-head read operand: ceil(K/64) chunks of 80 rows x 128 B.
+__host__ __device__ constexpr uint32_t mem_bytes(int K) { return (uint32_t)((K + 63) / 64) * 80u * 128u; }
+
+// Walks the CTA's tiles in steps of `step` without dividing inside the loop:
+// i = local tile index, g = head, j = tile within the head, hl = g - first head.
+struct TileCursor {
+    int i, g, j, hl, T, n, step;
+    __device__ TileCursor(int t0, int n_, int T_, int start, int step_) : T(T_), n(n_), step(step_) {
+        i = start;
+        g = (t0 + start) / T_;
+        j = (t0 + start) - g * T_;
+        hl = g - t0 / T_;
+    }
+    __device__ bool valid() const { return i < n; }
+    __device__ bool first() const { return j == 0 || i == 0; }
+    __device__ bool last() const { return j == T - 1 || i == n - 1; }
+    __device__ void next() {
+        i += step;
+        j += step;
+        while (j >= T) { j -= T; ++g; ++hl; }
+    }
+};
+
+// ------------------------------------------------------------------ wind-down helpers
+
+// Bounded wait that runs to completion (or its time limit) even after another
+// thread raised the CTA's abort flag: used before the CTA releases shared memory
+// or TMEM that in-flight copies or MMAs still touch.
+__device__ __forceinline__ void wait_ignoring_abort(uint64_t *bar, uint32_t parity, unsigned *status) {
+    int never = 0;
+    mbar_wait(bar, parity, Abort{&never, status}, kDevErrTimeout);
+}
+
+// Every TMA load issued into an S-stage ring has landed: waits for the last
+// fill of each stage (fills are issued round-robin, so that is the newest phase).
+__device__ __forceinline__ void wind_down_ring(uint64_t *full, int S, int issued, unsigned *status) {
+    for (int i = issued > S ? issued - S : 0; i < issued; ++i) wait_ignoring_abort(&full[i % S], (i / S) & 1, status);
+}
+
+// ------------------------------------------------------------------ compute helpers
+//
+// A compute warpgroup is four consecutive warps; thread r of the group owns
+// tile row r (= TMEM lane r): warp w may access TMEM lanes 32*(w % 4) ... +31.
+
+struct RowThread {
+    uint32_t r;          // tile row = TMEM lane
+    uint32_t lane_off;   // TMEM lane field of this warp
+    int wg;              // compute warpgroup
+    int wtid;            // 0..127 inside the group
+};
+
+// Named barrier 1 + wg synchronises one 128-thread compute warpgroup.
+__device__ __forceinline__ bool wg_all(const RowThread &t, bool v) { return group_all(v, 1 + t.wg, kWgThreads); }
+__device__ __forceinline__ void wg_sync(const RowThread &t) { group_sync(1 + t.wg, kWgThreads); }
+
+// Convert a bf16 row (128 B, swizzled) into the fp16 [x, x^2/256] row of the
+// log-density A operand in TMEM (columns 0-31: x pairs, 32-63: x^2/256 pairs).
+__device__ __forceinline__ void convert_row(const uint8_t *xs, uint32_t r, uint32_t tcol_a) {
+    uint32_t px[32], pq[32];
+    const uint64_t k16 = f2_pack(0.0625f, 0.0625f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(xs + sw128_off(r, j));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float lo = bf16_lo(w[u]), hi = bf16_hi(w[u]);
+            px[4 * j + u] = pack_f16(lo, hi);
+            const uint64_t y = f2_mul(f2_pack(lo, hi), k16);   // x / 16, exact
+            float qa, qb;
+            f2_unpack(f2_mul(y, y), qa, qb);                   // x^2 / 256
+            pq[4 * j + u] = pack_f16(qa, qb);
+        }
+    }
+    tmem_st32(tcol_a, px);
+    tmem_st32(tcol_a + 32, pq);
+}
+
+// The constant A block of the log-density MMA: row r = [1, 1, 0 x 14] (fp16).
+__device__ __forceinline__ void init_const_a(uint8_t *blk, int tid, int nthreads) {
+    for (int e = tid; e < (int)(kConstABytes / 16); e += nthreads) {
+        const uint32_t off = (uint32_t)e * 16u;
+        const bool first_half = ((off >> 7) & 1u) == 0;          // column half 0 holds columns 0..7
+        reinterpret_cast<uint4 *>(blk)[e] = make_uint4(first_half ? 0x3C003C00u : 0u, 0u, 0u, 0u);
+    }
+}
+
+// Issue the log-density MMA of one 128-row tile:  D = [x, x^2/256] . W^T + [1, 1] . [c_hi, c_lo]^T.
+// a_tmem holds [x, x^2/256] (64 columns of fp16 pairs); pblk / consta are shared addresses.
+template <int K>
+__device__ __forceinline__ void issue_logdensity(uint32_t d_tmem, uint32_t a_tmem, uint32_t pblk, uint32_t consta) {
+    constexpr uint32_t idesc = idesc_f16(0, 0, 0, 0, TM, K);
+    const uint64_t wd = sdesc_sw128(pblk, 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+        mma_ts(d_tmem, a_tmem + ks * 8, wd + (uint64_t)(((ks >> 2) * 128u * K + (ks & 3) * 32u) >> 4), idesc, ks > 0);
+    mma_ss(d_tmem, sdesc_none(consta, 128, 256), sdesc_none(pblk + param_wc_off(K), 128, 256), idesc, 1);
+}
+
+// e = 2^(scale * (d - max d)) for the K raw scores d of this thread's row in
+// TMEM (one round trip), as K/2 bf16 pairs.  scale > 0, so max commutes with it.
+// The exponent stays in fp32 and only the result is rounded to bf16, so every e
+// carries a relative error of at most 2^-9.  (Rounding the argument to bf16
+// first would cost ln2 * |arg| * 2^-9 relative: about 2% at arg = -20, which
+// shows in causal rows whose query routing barely overlaps the prefix keys,
+// where the output is a ratio of such tail probabilities.)
+template <int K>
+__device__ __forceinline__ void row_exp_scaled(uint32_t taddr, float scale, uint32_t (&e)[K / 2]) {
+    uint32_t d[K];
+#pragma unroll
+    for (int cc = 0; cc < K / 32; ++cc) tmem_ld32(taddr + 32 * cc, d + 32 * cc);
+    tmem_ld_wait();
+    float m[4] = {__uint_as_float(d[0]), __uint_as_float(d[1]), __uint_as_float(d[2]), __uint_as_float(d[3])};
+#pragma unroll
+    for (int t = 4; t + 8 <= K; t += 8) {
+        m[0] = max3(m[0], __uint_as_float(d[t]), __uint_as_float(d[t + 1]));
+        m[1] = max3(m[1], __uint_as_float(d[t + 2]), __uint_as_float(d[t + 3]));
+        m[2] = max3(m[2], __uint_as_float(d[t + 4]), __uint_as_float(d[t + 5]));
+        m[3] = max3(m[3], __uint_as_float(d[t + 6]), __uint_as_float(d[t + 7]));
+    }
+    m[0] = max3(m[0], __uint_as_float(d[K - 4]), __uint_as_float(d[K - 3]));
+    m[1] = max3(m[1], __uint_as_float(d[K - 2]), __uint_as_float(d[K - 1]));
+    const float mx = fmaxf(max3(m[0], m[1], m[2]), m[3]);
+    const uint64_t sc2 = f2_pack(scale, scale), nm2 = f2_pack(-mx * scale, -mx * scale);
+#pragma unroll
+    for (int t = 0; t < K; t += 2) {
+        float a, b;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(d[t]), __uint_as_float(d[t + 1])), sc2, nm2), a, b);
+        e[t / 2] = pack_bf16(ex2_approx(a), ex2_approx(b));
+    }
+}
+
+// Per-head scale of the coefficient matrix, read from the parameter block in global memory.
+__device__ __forceinline__ float head_scale(const uint8_t *params, uint32_t stride, int h, int K) {
+    return __ldg(reinterpret_cast<const float *>(params + (size_t)h * stride + param_scale_off(K)));
+}
+
+// ------------------------------------------------------------------ host helpers
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+inline EncodeTiled encode_fn() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+// 3D bf16 tensor map over [G][N][width], box [1][128][64], 128-byte swizzle.
+inline bool make_map(CUtensorMap *m, const void *base, int G, int N, int width) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)N, (cuuint64_t)G};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * N};
+    const cuuint32_t box[3] = {64, TM, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace tc
+}  // namespace gma

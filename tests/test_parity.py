@@ -63,6 +63,10 @@ SMALL = [
     ("bf16_k128", 1, 2, 777, 64, 128, 64, "bf16", False),
     ("bf16_k256_dv128", 1, 2, 640, 64, 256, 128, "bf16", True),
     ("bf16_odd", 1, 1, 515, 24, 40, 48, "bf16", True),
+    # many short heads per persistent CTA: head switches, parameter-buffer reuse
+    ("bf16_many_heads", 8, 64, 200, 64, 64, 64, "bf16", False),
+    ("bf16_many_heads_k128", 4, 32, 300, 64, 128, 64, "bf16", False),
+    ("bf16_many_heads_causal", 4, 48, 300, 64, 64, 64, "bf16", True),
 ]
 
 
