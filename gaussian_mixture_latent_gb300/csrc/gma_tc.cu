@@ -80,6 +80,7 @@ __device__ __forceinline__ void cta_range(int Ttot, int &t0, int &t1) {
 // ------------------------------------------------------------------ tc_params
 
 constexpr int kParamThreads = 512;
+constexpr int kParamV4 = 256 * DR / 4 / kParamThreads;   // float4 loads per thread and array at K <= 256
 
 __global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float var_floor,
                                                                   const float *__restrict__ mu,
@@ -94,52 +95,73 @@ __global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float v
     float *cbuf = colmean + DR;    // [K] per-component constants
     const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int NW = kParamThreads / 32;
-    const float *mu_h = mu + (size_t)h * K * DR, *rho_h = rho + (size_t)h * K * DR;
+    const float4 *mu4 = reinterpret_cast<const float4 *>(mu + (size_t)h * K * DR);
+    const float4 *rho4 = reinterpret_cast<const float4 *>(rho + (size_t)h * K * DR);
     const float *al = alpha + (size_t)h * K;
     uint8_t *blk = out + (size_t)h * stride;
 
+    // every global load of the head is issued before the first use: one memory round trip
+    const int n4 = K * DR / 4;
+    float4 mv[kParamV4], rv[kParamV4];
+#pragma unroll
+    for (int u = 0; u < kParamV4; ++u) {
+        const int e4 = tid + u * kParamThreads;
+        if (e4 < n4) { mv[u] = __ldg(mu4 + e4); rv[u] = __ldg(rho4 + e4); }
+    }
+    const float alk = tid < K ? __ldg(al + tid) : -INFINITY;
+
     // log-sum-exp of the prior logits (Eq. 15)
-    float m = -INFINITY;
-    for (int k = tid; k < K; k += kParamThreads) m = fmaxf(m, al[k]);
+    float m = alk;
     for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(~0u, m, o));
     if (lane == 0) red[warp] = m;
     __syncthreads();
     m = red[0];
     for (int w = 1; w < NW; ++w) m = fmaxf(m, red[w]);
     __syncthreads();
-    float s = 0.f;
-    for (int k = tid; k < K; k += kParamThreads) s += expf(al[k] - m);
+    float s = tid < K ? expf(alk - m) : 0.f;
     for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(~0u, s, o);
     if (lane == 0) red[warp] = s;
     __syncthreads();
     s = 0.f;
     for (int w = 0; w < NW; ++w) s += red[w];
     const float lse = m + logf(s);
-    __syncthreads();
 
-    // Eq. 14: variances; linear and quadratic coefficients in log2 units
-    for (int e = tid; e < K * DR; e += kParamThreads) {
-        const float w = rho_h[e];
-        const float var = fmaxf(w, 0.f) + log1pf(expf(-fabsf(w))) + var_floor;
-        const float lam = 1.0f / var;
-        a[e] = mu_h[e] * lam * kLog2e;
-        b[e] = -0.5f * lam * kLog2e;
-    }
-    __syncthreads();
-    // per-component constant c_k, one warp per component
-    for (int k = warp; k < K; k += NW) {
+    // Eq. 14: variances; linear and quadratic coefficients in log2 units.  The 16
+    // float4s of component k sit in 16 consecutive threads, which also reduce
+    // sum_m log var_km and sum_m mu_km^2 lambda_km for the constant c_k (Eq. 16).
+#pragma unroll
+    for (int u = 0; u < kParamV4; ++u) {
+        const int e4 = tid + u * kParamThreads;
+        if (u * kParamThreads >= n4) break;                     // uniform across the block
+        const bool valid = e4 < n4;
+        const float mq[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
+        const float rq[4] = {rv[u].x, rv[u].y, rv[u].z, rv[u].w};
         float logdet = 0.f, musq = 0.f;
-        for (int j = lane; j < DR; j += 32) {
-            const float var = -0.5f * kLog2e / b[k * DR + j];     // b = -log2(e) / (2 var)
-            logdet += logf(var);
-            musq += mu_h[k * DR + j] * a[k * DR + j];            // mu^2 lam log2(e)
+        if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                // SFU forms (relative error near 2^-21): the coefficients are rounded to
+                // fp16 (2^-12) and the constant to about 22 bits afterwards
+                const float w = rq[q];
+                const float var = fmaxf(w, 0.f) + __logf(1.0f + __expf(-fabsf(w))) + var_floor;
+                const float lam = __frcp_rn(var);
+                const float av = mq[q] * lam * kLog2e;
+                a[4 * e4 + q] = av;
+                b[4 * e4 + q] = -0.5f * lam * kLog2e;
+                logdet += __logf(var);
+                musq += mq[q] * av;
+            }
         }
-        for (int o = 16; o; o >>= 1) {
+        for (int o = 1; o < 16; o <<= 1) {
             logdet += __shfl_xor_sync(~0u, logdet, o);
             musq += __shfl_xor_sync(~0u, musq, o);
         }
-        if (lane == 0) cbuf[k] = (al[k] - lse) * kLog2e - 0.5f * kLog2e * logdet - 0.5f * musq;
+        if (valid && (tid & 15) == 0) {
+            const int k = e4 >> 4;
+            cbuf[k] = (__ldg(al + k) - lse) * kLog2e - 0.5f * kLog2e * logdet - 0.5f * musq;
+        }
     }
+    __syncthreads();
     // mean over components of each quadratic coefficient column (8 threads per column)
     {
         const int col = tid >> 3, part = tid & 7;
@@ -462,16 +484,26 @@ __global__ void __launch_bounds__(256) tc_reduce_kernel(int K, int T, int Ttot, 
                                                         uint8_t *__restrict__ mem, uint32_t mem_stride) {
     const int g = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    // CTA c owns tiles [c*Ttot/ncta, (c+1)*Ttot/ncta): those meeting [g*T, (g+1)*T) are
+    // c_lo..c_hi - 1, found once per block
+    __shared__ int crange[2];
+    if (threadIdx.x == 0) {
+        const long long lo = (long long)g * T, hi = (long long)(g + 1) * T;
+        int c = (int)((lo * ncta) / Ttot);
+        while (c > 0 && ((long long)c * Ttot) / ncta > lo) --c;
+        while (((long long)(c + 1) * Ttot) / ncta <= lo) ++c;
+        int c_hi = c;
+        while (c_hi < ncta && ((long long)c_hi * Ttot) / ncta < hi) ++c_hi;
+        crange[0] = c;
+        crange[1] = c_hi;
+    }
+    __syncthreads();
     if (e >= 80 * K) return;
-    const int lo = g * T, hi = (g + 1) * T;
-    // CTA c owns tiles [c*Ttot/ncta, (c+1)*Ttot/ncta): those meeting [lo, hi) are c_lo..c_hi.
-    int c_lo = (int)(((long long)lo * ncta) / Ttot);
-    while (c_lo > 0 && ((long long)c_lo * Ttot) / ncta > lo) --c_lo;
-    while (((long long)(c_lo + 1) * Ttot) / ncta <= lo) ++c_lo;
+    const int c_lo = crange[0], c_hi = crange[1];
     const int nrow = e / K, k = e % K;
     float v = 0.f;
     if (nrow <= DVV) {
-        for (int c = c_lo; c < ncta && ((long long)c * Ttot) / ncta < hi; ++c)
+        for (int c = c_lo; c < c_hi; ++c)
             v += partials[((size_t)(c + g) * (DVV + 1) + nrow) * K + k];
     } else if (nrow == DVV + 1) {
         v = 1.f;
