@@ -24,6 +24,12 @@
 // log-density MMAs (keys, then queries); 2 issuer of the chained MMAs (T, the
 // state update, the read); 3-6 key group (convert, softmax, state snapshot);
 // 7-10 query group (convert, exp); 11-14 output group (mask, epilogue, store).
+//
+// T is formed in two 64-key halves through one 64-column TMEM buffer: rows
+// 0..63 never see keys 64..127, so that half of the masked tile stays zero.
+// e^Q, T and the read result have TMEM columns of their own, so chunk c + 1's
+// query scores and T proceed while chunk c is read, and the output group runs
+// chunk c - 1's epilogue while the second half of T(c) is computed.
 // Every mbarrier wait is bounded; a timeout posts GMA_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -69,8 +75,10 @@ struct CausalCfg {
     static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;
     // TMEM columns
     static constexpr uint32_t COL_AQ = 0, COL_D1Q = 64, COL_AK = 128, COL_D1K = 192;
-    static constexpr uint32_t COL_TD = 256;                            // T (128 fp32), then the read result
-    static constexpr uint32_t COL_S = 384;                             // [S | z]^T state, 64 columns
+    static constexpr uint32_t COL_T = 256;                             // one 64-key half of T (fp32)
+    static constexpr uint32_t COL_D3 = 320;                            // read result [num | den | sum e^Q], 80
+    static constexpr uint32_t COL_S = 416;                             // [S | z]^T state, 64 columns
+    static constexpr uint32_t COL_EQ = 480;                            // e^Q as bf16 pairs, 32 columns
     static constexpr uint32_t TMEM_COLS = 512;
 };
 static_assert(CausalCfg::OFF_SB % 1024 == 0 && CausalCfg::OFF_P % 1024 == 0 && CausalCfg::OFF_O % 1024 == 0,
@@ -90,7 +98,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint64_t *vfull = kempty + 2, *vempty = vfull + 2;
     uint64_t *w_full = vempty + 2, *ak_full = w_full + 1, *d1k_full = ak_full + 1, *aq_full = d1k_full + 1;
     uint64_t *d1q_full = aq_full + 1, *g_full = d1q_full + 1, *g_empty = g_full + 1, *e_full = g_empty + 1;
-    uint64_t *t_full = e_full + 1, *tb_full = t_full + 1, *d3_full = tb_full + 1, *d3_empty = d3_full + 1;
+    // T buffer: ta_full (first half computed), ta_free (first half read), tb2_full (second half
+    // computed), t_empty (second half read); tb_full: the masked bf16 tile is complete
+    uint64_t *ta_full = e_full + 1, *ta_free = ta_full + 1, *tb2_full = ta_free + 1, *t_empty = tb2_full + 1;
+    uint64_t *tb_full = t_empty + 1, *d3_full = tb_full + 1, *d3_empty = d3_full + 1;
     uint64_t *s_upd = d3_empty + 1, *s_ready = s_upd + 1, *sb_empty = s_ready + 2;
     uint64_t *fin1 = sb_empty + 2, *fin2 = fin1 + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
@@ -114,6 +125,9 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // (the state before the first chunk).
     for (uint32_t e = threadIdx.x; e < kTileBytes / 16; e += blockDim.x)
         reinterpret_cast<uint4 *>(sm + C::OFF_ONES)[e] = make_uint4(0, 0, 0, 0);
+    // masked T tile: groups of 32 keys above a row quarter's diagonal are never written
+    for (uint32_t e = threadIdx.x; e < 2 * kTileBytes / 16; e += blockDim.x)
+        reinterpret_cast<uint4 *>(sm + C::OFF_TB)[e] = make_uint4(0, 0, 0, 0);
     for (uint32_t e = threadIdx.x; e < 2 * C::SBB / 16; e += blockDim.x) {
         const uint32_t row = (e * 16u % C::SBB) / 128u;
         const uint32_t v = row == DVV + 1 ? 0x3F803F80u : 0u;
@@ -183,8 +197,6 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 issue_logdensity<K>(tmem + C::COL_D1K, tmem + C::COL_AK, pw, ca);
                 mma_commit(d1k_full);
                 if (!(ok = mbar_wait(aq_full, c & 1, ab, kDevErrTimeout))) break;
-                // the query scores overwrite e^Q of the previous chunk: wait for its last reader
-                if (c >= 1 && !(ok = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout))) break;
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::COL_D1Q, tmem + C::COL_AQ, pw, ca);
                 mma_commit(d1q_full);
@@ -194,7 +206,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
     } else if (warp == kWIss2) {
         if (lane == 0) {
-            constexpr uint32_t idesc_t = idesc_f16(1, 1, 0, 0, TM, TM);      // e^Q (TMEM) . gamma^K^T
+            constexpr uint32_t idesc_t = idesc_f16(1, 1, 0, 0, TM, 64);       // e^Q (TMEM) . gamma^K^T, 64 keys
             constexpr uint32_t idesc_u = idesc_f16(1, 1, 1, 1, TM, K);       // [V | 1]^T . gamma^K
             constexpr uint32_t idesc_r1 = idesc_f16(1, 1, 0, 0, TM, NOUT);   // e^Q . [S | z | 1]
             constexpr uint32_t idesc_r2 = idesc_f16(1, 1, 0, 1, TM, NOUT);   // T . [V | 1]
@@ -202,19 +214,19 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint64_t gk = sdesc_sw128(gaddr, 16, 1024);                // gamma^K as K-major B (N = keys)
             const uint64_t gm = sdesc_sw128(gaddr, kTileBytes, 1024);        // gamma^K as MN-major B (N = k)
             const uint64_t tbd = sdesc_sw128(smem_u32(sm + C::OFF_TB), 16, 1024);
+            const uint32_t eq = tmem + C::COL_EQ;
             bool ok = true;
             for (int c = 0; c < nch && ok; ++c) {
                 const int s = c & 1;
-                // T(c) = e^Q(c) . gamma^K(c)^T into the T / read columns
+                // T(c), keys 0..63 = e^Q(c) . gamma^K(c)[0:64]^T
                 ok = mbar_wait(e_full, c & 1, ab, kDevErrTimeout) && mbar_wait(g_full, c & 1, ab, kDevErrTimeout);
-                if (ok && c >= 1) ok = mbar_wait(d3_empty, (c - 1) & 1, ab, kDevErrTimeout);
+                if (ok && c >= 1) ok = mbar_wait(t_empty, (c - 1) & 1, ab, kDevErrTimeout);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
-                    mma_ts(tmem + C::COL_TD, tmem + C::COL_D1Q + ks * 8, gk + (uint64_t)((ks * 32u) >> 4), idesc_t,
-                           ks > 0);
-                mma_commit(t_full);
+                    mma_ts(tmem + C::COL_T, eq + ks * 8, gk + (uint64_t)((ks * 32u) >> 4), idesc_t, ks > 0);
+                mma_commit(ta_full);
                 // state update: [S | z]^T += [V | 1 | 0]^T . gamma^K, once the previous state is snapshotted
                 if (!(ok = mbar_wait(&vfull[s], (c >> 1) & 1, ab, kDevErrTimeout) &&
                            mbar_wait(&s_ready[c & 1], (c >> 1) & 1, ab, kDevErrTimeout)))
@@ -227,18 +239,27 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mma_ss(tmem + C::COL_S, vd + (uint64_t)(ks * 128), gm + (uint64_t)(ks * 128), idesc_u,
                            !(c == 0 && ks == 0));
                 mma_commit(s_upd);
+                // T(c), keys 64..127, once the first half has been read
+                if (!(ok = mbar_wait(ta_free, c & 1, ab, kDevErrTimeout))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks)
+                    mma_ts(tmem + C::COL_T, eq + ks * 8, gk + (uint64_t)((64u * 128u + ks * 32u) >> 4), idesc_t,
+                           ks > 0);
+                mma_commit(tb2_full);
                 mma_commit(g_empty);
                 // read: e^Q . [S | z | 1]_{c-1} + mask(T) . [V | 1]
-                if (!(ok = mbar_wait(tb_full, c & 1, ab, kDevErrTimeout))) break;
+                ok = mbar_wait(tb_full, c & 1, ab, kDevErrTimeout);
+                if (ok && c >= 1) ok = mbar_wait(d3_empty, (c - 1) & 1, ab, kDevErrTimeout);
+                if (!ok) break;
                 tc_fence_after();
                 const uint64_t sbd = sdesc_sw128(smem_u32(sm + C::OFF_SB + (c & 1) * C::SBB), 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
-                    mma_ts(tmem + C::COL_TD, tmem + C::COL_D1Q + ks * 8, sbd + (uint64_t)((ks * 32u) >> 4), idesc_r1,
-                           ks > 0);
+                    mma_ts(tmem + C::COL_D3, eq + ks * 8, sbd + (uint64_t)((ks * 32u) >> 4), idesc_r1, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tmem + C::COL_TD, tbd + (uint64_t)(((ks >> 2) * kTileBytes + (ks & 3) * 32u) >> 4),
+                    mma_ss(tmem + C::COL_D3, tbd + (uint64_t)(((ks >> 2) * kTileBytes + (ks & 3) * 32u) >> 4),
                            vd + (uint64_t)(ks * 128), idesc_r2, 1);
                 mma_commit(d3_full);
                 mma_commit(&sb_empty[c & 1]);
@@ -344,59 +365,62 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             };
             bool ok = convert_q(0);
             for (int c = 0; c < nch && ok; ++c) {
-                const bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
+                bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
                 if (!(ok = wg_all(rt, w))) break;
                 tc_fence_after();
-                const uint32_t d1 = tmem + rt.lane_off + C::COL_D1Q;
-                {
-                    uint32_t e[K / 2];
-                    row_exp_scaled<K>(d1, scale, e);
-                    tmem_st32(d1, e);                      // e^Q as bf16 pairs over the scores
+                uint32_t e[K / 2];
+                row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1Q, scale, e);
+                // e^Q(c) replaces e^Q(c - 1) once the read of chunk c - 1 has consumed it
+                if (c >= 1) {
+                    w = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
+                    if (!(ok = wg_all(rt, w))) break;
+                    tc_fence_after();
                 }
+                tmem_st32(tmem + rt.lane_off + C::COL_EQ, e);
                 tmem_st_wait();
                 tc_fence_before();
                 wg_sync(rt);
                 if (elected) mbar_arrive(e_full);
+                // the scores of chunk c have been read: the next query tile may overwrite them
                 if (c + 1 < nch && !(ok = convert_q(c + 1))) break;
             }
         } else {
             // ---------------- output group
-            for (int c = 0; c < nch; ++c) {
-                bool w = mbar_wait(t_full, c & 1, ab, kDevErrTimeout);
-                if (!wg_all(rt, w)) break;
-                tc_fence_after();
-                // causal mask inside the chunk: keep key j <= query row r (selected, never multiplied)
+            // Row quarter q = warp & 3 holds rows 32q..32q+31.  A group of 32 keys is copied
+            // whole below the quarter's diagonal, selected (j <= r) on it, and never touched
+            // above it (those entries of the masked tile stay zero from the start).
+            const int q = warp & 3;
+            auto mask_group = [&](const uint32_t *v, int key0, bool diag, uint8_t *half, int cc) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + rt.lane_off + C::COL_TD + 32 * cc, v);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const uint32_t j0 = 32u * cc + 2 * t;
-                        const float a = j0 <= rt.r ? __uint_as_float(v[2 * t]) : 0.f;
-                        const float b2 = j0 + 1 <= rt.r ? __uint_as_float(v[2 * t + 1]) : 0.f;
-                        pk[t] = pack_bf16(a, b2);
-                    }
-                    uint8_t *tb = sm + C::OFF_TB + (cc >> 1) * kTileBytes;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        *reinterpret_cast<uint4 *>(tb + sw128_off(rt.r, (cc & 1) * 4 + q4)) =
-                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                for (int t = 0; t < 16; ++t) {
+                    const uint32_t j0 = (uint32_t)key0 + 2u * t;
+                    const float a = !diag || j0 <= rt.r ? __uint_as_float(v[2 * t]) : 0.f;
+                    const float b2 = !diag || j0 + 1 <= rt.r ? __uint_as_float(v[2 * t + 1]) : 0.f;
+                    pk[t] = pack_bf16(a, b2);
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                wg_sync(rt);
-                if (elected) mbar_arrive(tb_full);
-                // epilogue: out = num / (den + eps * sum_k e^Q_k)
-                w = mbar_wait(d3_full, c & 1, ab, kDevErrTimeout);
-                if (!wg_all(rt, w)) break;
-                tc_fence_after();
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4 *>(half + sw128_off(rt.r, cc * 4 + q4)) =
+                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            };
+            // one half of T (64 keys starting at key0) from TMEM into the masked bf16 tile
+            auto mask_half = [&](int key0, uint8_t *half) {
+                const int g0 = key0 / 32;                     // global index of the half's first group
+                if (q < g0) return;                           // the whole half lies above the diagonal
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tmem + rt.lane_off + C::COL_T, v0);
+                tmem_ld32(tmem + rt.lane_off + C::COL_T + 32, v1);
+                tmem_ld_wait();
+                mask_group(v0, key0, q == g0, half, 0);
+                if (q > g0) mask_group(v1, key0 + 32, q == g0 + 1, half, 1);
+            };
+            auto epilogue = [&](int c) {
+                // out = num / (den + eps * sum_k e^Q_k)
                 uint32_t v0[32], v1[32], dz[4];
-                tmem_ld32(tmem + rt.lane_off + C::COL_TD, v0);
-                tmem_ld32(tmem + rt.lane_off + C::COL_TD + 32, v1);
-                tmem_ld4(tmem + rt.lane_off + C::COL_TD + 64, dz);
+                tmem_ld32(tmem + rt.lane_off + C::COL_D3, v0);
+                tmem_ld32(tmem + rt.lane_off + C::COL_D3 + 32, v1);
+                tmem_ld4(tmem + rt.lane_off + C::COL_D3 + 64, dz);
                 tmem_ld_wait();
                 const float rd = 1.0f / (__uint_as_float(dz[0]) + A.eps * __uint_as_float(dz[1]));
                 const uint64_t rd2 = f2_pack(rd, rd);
@@ -423,6 +447,36 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (elected) {
                     tma_store_3d(&tm_o, ob, 0, c * TM, g);
                     bulk_commit_group();
+                }
+            };
+            bool ok = true;
+            for (int c = 0; c < nch && ok; ++c) {
+                // keys 0..63 of T(c); the masked tile is free once the read of chunk c - 1 is done
+                bool w = mbar_wait(ta_full, c & 1, ab, kDevErrTimeout);
+                if (c >= 1) w = w && mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
+                if (!(ok = wg_all(rt, w))) break;
+                tc_fence_after();
+                mask_half(0, sm + C::OFF_TB);
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) mbar_arrive(ta_free);
+                // chunk c - 1's epilogue while the second half of T(c) is computed
+                if (c >= 1) epilogue(c - 1);
+                // keys 64..127 of T(c)
+                w = mbar_wait(tb2_full, c & 1, ab, kDevErrTimeout);
+                if (!(ok = wg_all(rt, w))) break;
+                tc_fence_after();
+                mask_half(64, sm + C::OFF_TB + kTileBytes);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) { mbar_arrive(t_empty); mbar_arrive(tb_full); }
+            }
+            if (ok) {
+                const bool w = mbar_wait(d3_full, (nch - 1) & 1, ab, kDevErrTimeout);
+                if (wg_all(rt, w)) {
+                    tc_fence_after();
+                    epilogue(nch - 1);
                 }
             }
             if (elected) bulk_wait_group<0>();
