@@ -108,6 +108,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch.  grid_dep_launch: this CTA no longer holds back
+// the launch of the next kernel in the stream.  grid_dep_wait: block until the
+// previous kernel in the stream has completed and its writes are visible (a no-op
+// when the kernel was not launched as a programmatic dependent).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -58,8 +58,11 @@ using namespace tc;
 
 namespace {
 
-constexpr int kThreads = 352;      // 11 warps
 constexpr int kWarpProducer = 0, kWarpMma1 = 1, kWarpMma2 = 2, kWarpCompute = 3;
+// Compute groups per CTA: three at K = 64 (TMEM holds three groups' operands and
+// scores), two at K = 128.  More groups hide more of each group's serial
+// convert -> log-density MMA -> softmax latency.
+__host__ __device__ constexpr int groups_for(int K) { return K <= 64 ? 3 : 2; }
 
 struct TcArgs {
     int G, H, N, T, Ttot, K;
@@ -93,6 +96,7 @@ __global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float v
     float *red = b + K * DR;       // [64] scratch
     float *colmean = red + 64;     // [DR]
     float *cbuf = colmean + DR;    // [K] per-component constants
+    grid_dep_launch();
     const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int NW = kParamThreads / 32;
     const float4 *mu4 = reinterpret_cast<const float4 *>(mu + (size_t)h * K * DR);
@@ -222,15 +226,17 @@ __global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float v
 template <int K>
 struct WriteCfg {
     static constexpr int KCH = (K + 63) / 64;
+    static constexpr int NW = groups_for(K);
+    static constexpr int THREADS = (kWarpCompute + 4 * NW) * 32;
     static constexpr int SX = K <= 64 ? 4 : 3;                       // X ring stages
     static constexpr int SV = K <= 64 ? 4 : 3;                       // V ring stages
-    static constexpr int PN = K <= 64 ? 2 : 1;                       // parameter buffers
+    static constexpr int PN = 1;                                     // parameter buffers
     static constexpr uint32_t PB = align1k(param_bytes(K));
     static constexpr uint32_t OFF_X = 0;
     static constexpr uint32_t OFF_V = OFF_X + SX * kTileBytes;
     static constexpr uint32_t OFF_ONES = OFF_V + SV * kTileBytes;      // after every V stage (positive LBO)
     static constexpr uint32_t OFF_G = OFF_ONES + kTileBytes;           // one Gamma buffer per warpgroup
-    static constexpr uint32_t OFF_P = OFF_G + 2 * KCH * kTileBytes;
+    static constexpr uint32_t OFF_P = OFF_G + NW * KCH * kTileBytes;
     static constexpr uint32_t OFF_CA = OFF_P + PN * PB;               // constant [1, 1, 0...] A block
     static constexpr uint32_t OFF_BAR = OFF_CA + kConstABytes;
     static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;            // barriers + alignment slack
@@ -238,29 +244,30 @@ struct WriteCfg {
     static constexpr uint32_t wg_cols = 64 + K;
     static constexpr uint32_t col_a(int w) { return w * wg_cols; }
     static constexpr uint32_t col_d1(int w) { return w * wg_cols + 64; }
-    static constexpr uint32_t COL_D2 = 2 * wg_cols;
+    static constexpr uint32_t COL_D2 = NW * wg_cols;
     static_assert(BYTES <= 232448 && COL_D2 + K <= TMEM_COLS, "write kernel exceeds shared memory or TMEM");
 };
 
 template <int K>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(WriteCfg<K>::THREADS, 1)
 tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, TcArgs A) {
     using C = WriteCfg<K>;
-    constexpr int SX = C::SX, SV = C::SV, PN = C::PN;
+    constexpr int SX = C::SX, SV = C::SV, PN = C::PN, NW = C::NW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
     uint64_t *xfull = bars, *xempty = xfull + SX;
     uint64_t *vfull = xempty + SX, *vempty = vfull + SV;
-    uint64_t *a_full = vempty + SV, *d1_full = a_full + 2, *g_full = d1_full + 2, *g_empty = g_full + 2;
-    uint64_t *w_full = g_empty + 2, *w_empty = w_full + PN;
-    // d2_full[hl & 1]: the accumulation of local head hl is complete.  Two barriers, so the group
-    // that drains head hl (which has seen the accumulation of head hl - 2 complete) is never
-    // more than one phase ahead of the barrier it waits on.
-    uint64_t *d2_full = w_empty + PN, *d2_empty = d2_full + 2, *fin1 = d2_empty + 1, *fin2 = fin1 + 1;
+    uint64_t *a_full = vempty + SV, *d1_full = a_full + NW, *g_full = d1_full + NW, *g_empty = g_full + NW;
+    uint64_t *w_full = g_empty + NW, *w_empty = w_full + PN;
+    // d2_full[hl % NW]: the accumulation of local head hl is complete.  The group that drains
+    // head hl has seen the write MMA of its previous tile (tile - NW) complete, hence every head
+    // up to hl - NW, so it is never more than one phase ahead of the barrier it waits on.
+    uint64_t *d2_full = w_empty + PN, *d2_empty = d2_full + NW, *fin1 = d2_empty + 1, *fin2 = fin1 + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
+    grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int t0, t1;
     cta_range(A.Ttot, t0, t1);
@@ -269,11 +276,12 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
         for (int s = 0; s < SV; ++s) { mbar_init(&vfull[s], 1); mbar_init(&vempty[s], 1); }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NW; ++b) {
             mbar_init(&a_full[b], 1); mbar_init(&d1_full[b], 1); mbar_init(&g_full[b], 1); mbar_init(&g_empty[b], 1);
+            mbar_init(&d2_full[b], 1);
         }
         for (int b = 0; b < PN; ++b) { mbar_init(&w_full[b], 1); mbar_init(&w_empty[b], 1); }
-        mbar_init(&d2_full[0], 1); mbar_init(&d2_full[1], 1); mbar_init(d2_empty, 1);
+        mbar_init(d2_empty, 1);
         mbar_init(fin1, 1); mbar_init(fin2, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -295,7 +303,20 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (warp == kWarpProducer) {
         if (lane == 0 && n > 0) {
             TileCursor cx(t0, n, A.T, 0, 1), cv(t0, n, A.T, 0, 1);
-            int p_loaded = -1;
+            // the first head's routing and value tiles do not depend on the previous kernel
+            for (; cx.valid() && cx.hl == 0 && cx.i < SX; cx.next()) {
+                mbar_arrive_expect_tx(&xfull[cx.i], kTileBytes);
+                tma_load_3d(sm + C::OFF_X + cx.i * kTileBytes, &tm_k, &xfull[cx.i], 0, cx.j * TM, cx.g);
+            }
+            for (; cv.valid() && cv.hl == 0 && cv.i < SV; cv.next()) {
+                mbar_arrive_expect_tx(&vfull[cv.i], kTileBytes);
+                tma_load_3d(sm + C::OFF_V + cv.i * kTileBytes, &tm_v, &vfull[cv.i], 0, cv.j * TM, cv.g);
+            }
+            grid_dep_wait();                               // the parameter blocks are written
+            mbar_arrive_expect_tx(&w_full[0], param_bytes(K));
+            bulk_load(sm + C::OFF_P, A.params + (size_t)((t0 / A.T) % A.H) * A.param_stride, param_bytes(K),
+                      &w_full[0]);
+            int p_loaded = 0;
             long long last = clock64();
             while ((cx.valid() || cv.valid()) && !*abort_flag) {
                 bool progress = false;
@@ -345,12 +366,12 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 wait_ignoring_abort(&w_full[hl % PN], (hl / PN) & 1, A.status);
         }
     } else if (warp == kWarpMma1) {
-        // log-density MMAs: scores(i) = [x, x^2/256](i) . W^T into D1 of warpgroup i & 1
+        // log-density MMAs: scores(i) = [x, x^2/256](i) . W^T into D1 of group i % NW
         if (lane == 0 && n > 0) {
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
-                const int i = c.i, b = c.hl % PN, w = i & 1;
+                const int i = c.i, b = c.hl % PN, w = i % NW;
                 if (c.first() && !mbar_wait(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
-                if (!mbar_wait(&a_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait(&a_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
                                     smem_u32(sm + C::OFF_CA));
@@ -366,8 +387,8 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             constexpr uint32_t idesc = idesc_f16(1, 1, 1, 1, TM, K);
             const uint32_t ones = smem_u32(sm + C::OFF_ONES);
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
-                const int i = c.i, s = i % SV, w = i & 1;
-                if (!mbar_wait(&g_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
+                const int i = c.i, s = i % SV, w = i % NW;
+                if (!mbar_wait(&g_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
                 if (!mbar_wait(&vfull[s], (i / SV) & 1, ab, kDevErrTimeout)) break;
                 if (c.first() && c.hl >= 1 && !mbar_wait(d2_empty, (c.hl - 1) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
@@ -381,7 +402,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                            !(first && ks == 0));
                 mma_commit(&g_empty[w]);
                 mma_commit(&vempty[s]);
-                if (c.last()) mma_commit(&d2_full[c.hl & 1]);
+                if (c.last()) mma_commit(&d2_full[c.hl % NW]);
             }
             mma_commit(fin2);
             wait_ignoring_abort(fin2, 0, A.status);
@@ -395,7 +416,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         rt.wtid = threadIdx.x - kWarpCompute * 32 - rt.wg * kWgThreads;
         const int w = rt.wg;
         const bool elected = rt.wtid == 0;
-        TileCursor c(t0, n, A.T, w, 2);
+        TileCursor c(t0, n, A.T, w, NW);
         for (; c.valid(); c.next()) {
             const int i = c.i, hl = c.hl;
             // convert tile i into this group's A operand
@@ -407,9 +428,10 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             wg_sync(rt);
             if (elected) { mbar_arrive(&a_full[w]); mbar_arrive(&xempty[i % SX]); }
             // softmax of tile i (Eq. 3b); rows past the sequence end get Gamma = 0
+            if (i < NW) grid_dep_wait();                   // the parameter blocks are written
             const float scale = head_scale(A.params, A.param_stride, c.g % A.H, K);
-            ok = mbar_wait(&d1_full[w], (i >> 1) & 1, ab, kDevErrTimeout);
-            if (i >= 2) ok = ok && mbar_wait(&g_empty[w], ((i >> 1) - 1) & 1, ab, kDevErrTimeout);
+            ok = mbar_wait(&d1_full[w], (i / NW) & 1, ab, kDevErrTimeout);
+            if (i >= NW) ok = ok && mbar_wait(&g_empty[w], ((i / NW) - 1) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
             uint32_t e[K / 2];
@@ -444,7 +466,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             const int g = c.g;
             if (c.last()) {
                 // drain [Vt | Z]^T of this head into partial slot (cta + head)
-                ok = mbar_wait(&d2_full[hl & 1], (hl >> 1) & 1, ab, kDevErrTimeout);
+                ok = mbar_wait(&d2_full[hl % NW], (hl / NW) & 1, ab, kDevErrTimeout);
                 if (!wg_all(rt, ok)) break;
                 tc_fence_after();
                 float *dst = A.partials + ((size_t)(blockIdx.x + g) * (DVV + 1) + rt.r) * K;
@@ -482,6 +504,8 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 __global__ void __launch_bounds__(256) tc_reduce_kernel(int K, int T, int Ttot, int ncta,
                                                         const float *__restrict__ partials,
                                                         uint8_t *__restrict__ mem, uint32_t mem_stride) {
+    grid_dep_launch();
+    grid_dep_wait();                                       // the partial slots are written
     const int g = blockIdx.y;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     // CTA c owns tiles [c*Ttot/ncta, (c+1)*Ttot/ncta): those meeting [g*T, (g+1)*T) are
@@ -516,13 +540,15 @@ __global__ void __launch_bounds__(256) tc_reduce_kernel(int K, int T, int Ttot, 
 
 template <int K>
 struct ReadCfg {
+    static constexpr int NW = groups_for(K);
+    static constexpr int THREADS = (kWarpCompute + 4 * NW) * 32;
     static constexpr int SX = K <= 64 ? 6 : 4;
     static constexpr int PN = 2;
     static constexpr uint32_t PB = align1k(param_bytes(K));
     static constexpr uint32_t MB = align1k(mem_bytes(K));
     static constexpr uint32_t OFF_X = 0;
     static constexpr uint32_t OFF_O = OFF_X + SX * kTileBytes;         // one output staging tile per group
-    static constexpr uint32_t OFF_P = OFF_O + 2 * kTileBytes;
+    static constexpr uint32_t OFF_P = OFF_O + NW * kTileBytes;
     static constexpr uint32_t OFF_M = OFF_P + PN * PB;
     static constexpr uint32_t OFF_CA = OFF_M + PN * MB;                // constant [1, 1, 0...] A block
     static constexpr uint32_t OFF_BAR = OFF_CA + kConstABytes;
@@ -532,24 +558,25 @@ struct ReadCfg {
     static constexpr uint32_t wg_cols = NOUT + K;
     static constexpr uint32_t col_a(int w) { return w * wg_cols; }     // A operand, later D2 (same columns)
     static constexpr uint32_t col_d1(int w) { return w * wg_cols + NOUT; }
-    static_assert(BYTES <= 232448 && 2 * wg_cols <= TMEM_COLS, "read kernel exceeds shared memory or TMEM");
+    static_assert(BYTES <= 232448 && NW * wg_cols <= TMEM_COLS, "read kernel exceeds shared memory or TMEM");
 };
 
 template <int K>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(ReadCfg<K>::THREADS, 1)
 tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o, TcArgs A) {
     using C = ReadCfg<K>;
-    constexpr int SX = C::SX, PN = C::PN;
+    constexpr int SX = C::SX, PN = C::PN, NW = C::NW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
     uint64_t *xfull = bars, *xempty = xfull + SX;
-    uint64_t *a_full = xempty + SX, *d1_full = a_full + 2, *e_full = d1_full + 2, *d2_full = e_full + 2;
-    uint64_t *w_full = d2_full + 2, *w_empty = w_full + PN;
+    uint64_t *a_full = xempty + SX, *d1_full = a_full + NW, *e_full = d1_full + NW, *d2_full = e_full + NW;
+    uint64_t *w_full = d2_full + NW, *w_empty = w_full + PN;
     uint64_t *fin1 = w_empty + PN, *fin2 = fin1 + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
+    grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int t0, t1;
     cta_range(A.Ttot, t0, t1);
@@ -557,7 +584,7 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NW; ++b) {
             mbar_init(&a_full[b], 1); mbar_init(&d1_full[b], 1); mbar_init(&e_full[b], 1); mbar_init(&d2_full[b], 1);
         }
         for (int b = 0; b < PN; ++b) { mbar_init(&w_full[b], 1); mbar_init(&w_empty[b], 1); }
@@ -577,7 +604,19 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (warp == kWarpProducer) {
         if (lane == 0 && n > 0) {
             TileCursor cx(t0, n, A.T, 0, 1);
-            int p_loaded = -1;
+            // the first head's query tiles do not depend on the previous kernel
+            for (; cx.valid() && cx.hl == 0 && cx.i < SX; cx.next()) {
+                mbar_arrive_expect_tx(&xfull[cx.i], kTileBytes);
+                tma_load_3d(sm + C::OFF_X + cx.i * kTileBytes, &tm_q, &xfull[cx.i], 0, cx.j * TM, cx.g);
+            }
+            grid_dep_wait();                               // parameter blocks and read operands are written
+            {
+                const int g0 = t0 / A.T;
+                mbar_arrive_expect_tx(&w_full[0], param_bytes(K) + mem_bytes(K));
+                bulk_load(sm + C::OFF_P, A.params + (size_t)(g0 % A.H) * A.param_stride, param_bytes(K), &w_full[0]);
+                bulk_load(sm + C::OFF_M, A.mem + (size_t)g0 * A.mem_stride, mem_bytes(K), &w_full[0]);
+            }
+            int p_loaded = 0;
             long long last = clock64();
             while (cx.valid() && !*abort_flag) {
                 bool progress = false;
@@ -619,9 +658,9 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     } else if (warp == kWarpMma1) {
         if (lane == 0 && n > 0) {
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
-                const int i = c.i, b = c.hl % PN, w = i & 1;
+                const int i = c.i, b = c.hl % PN, w = i % NW;
                 if (c.first() && !mbar_wait(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
-                if (!mbar_wait(&a_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait(&a_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
                                     smem_u32(sm + C::OFF_CA));
@@ -635,8 +674,8 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane == 0 && n > 0) {
             constexpr uint32_t idesc = idesc_f16(1, 1, 0, 0, TM, C::NOUT);
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
-                const int i = c.i, b = c.hl % PN, w = i & 1;
-                if (!mbar_wait(&e_full[w], (i >> 1) & 1, ab, kDevErrTimeout)) break;
+                const int i = c.i, b = c.hl % PN, w = i % NW;
+                if (!mbar_wait(&e_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
                 const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_M + b * C::MB), 16, 1024);
 #pragma unroll
@@ -657,7 +696,7 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         rt.wtid = threadIdx.x - kWarpCompute * 32 - rt.wg * kWgThreads;
         const int w = rt.wg;
         const bool elected = rt.wtid == 0;
-        TileCursor c(t0, n, A.T, w, 2);
+        TileCursor c(t0, n, A.T, w, NW);
         for (; c.valid(); c.next()) {
             const int i = c.i;
             bool ok = mbar_wait(&xfull[i % SX], (i / SX) & 1, ab, kDevErrTimeout);
@@ -667,8 +706,9 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_before();
             wg_sync(rt);
             if (elected) { mbar_arrive(&a_full[w]); mbar_arrive(&xempty[i % SX]); }
+            if (i < NW) grid_dep_wait();                   // the parameter blocks are written
             const float scale = head_scale(A.params, A.param_stride, c.g % A.H, K);
-            ok = mbar_wait(&d1_full[w], (i >> 1) & 1, ab, kDevErrTimeout);
+            ok = mbar_wait(&d1_full[w], (i / NW) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
             const uint32_t d1 = tmem + rt.lane_off + C::col_d1(w);
@@ -686,7 +726,7 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (elected) mbar_arrive(&e_full[w]);
             const int g = c.g, row0 = c.j * TM;
             // epilogue: out = num / (den + eps * sum_k e_k)
-            ok = mbar_wait(&d2_full[w], (i >> 1) & 1, ab, kDevErrTimeout);
+            ok = mbar_wait(&d2_full[w], (i / NW) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
             uint32_t v0[32], v1[32], dz[4];
@@ -745,8 +785,7 @@ cudaError_t launch_write(const Problem &p, const TcLayout &L, const void *Kx, co
     auto kern = tc_write_kernel<K>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WriteCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<L.ncta, kThreads, WriteCfg<K>::BYTES, s>>>(tk, tv, a);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(L.ncta), dim3(WriteCfg<K>::THREADS), WriteCfg<K>::BYTES, s, tk, tv, a);
 }
 
 template <int K>
@@ -763,8 +802,7 @@ cudaError_t launch_read(const Problem &p, const TcLayout &L, const void *Qx, voi
     auto kern = tc_read_kernel<K>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ReadCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<L.ncta, kThreads, ReadCfg<K>::BYTES, s>>>(tq, to, a);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(L.ncta), dim3(ReadCfg<K>::THREADS), ReadCfg<K>::BYTES, s, tq, to, a);
 }
 
 }  // namespace
@@ -810,9 +848,9 @@ cudaError_t tc_write(const Problem &p, const TcLayout &L, const void *Kx, const 
 
 cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s) {
     dim3 grid((80 * p.K + 255) / 256, p.G);
-    tc_reduce_kernel<<<grid, 256, 0, s>>>(p.K, L.T, L.Ttot, L.ncta, reinterpret_cast<const float *>(ws + L.part),
-                                         reinterpret_cast<uint8_t *>(ws + L.mem), L.mem_stride);
-    return cudaGetLastError();
+    return launch_dependent(tc_reduce_kernel, grid, dim3(256), 0, s, p.K, L.T, L.Ttot, L.ncta,
+                            reinterpret_cast<const float *>(ws + L.part), reinterpret_cast<uint8_t *>(ws + L.mem),
+                            L.mem_stride);
 }
 
 cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,

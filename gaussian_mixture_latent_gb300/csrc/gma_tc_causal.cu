@@ -109,6 +109,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.x, nch = A.nch;
+    grid_dep_launch();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -147,9 +148,23 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (warp == kWProd) {
         if (lane == 0) {
+            // the first tiles do not depend on the previous kernel; the parameter block does
+            int qi = 0, ki = 0, vi = 0;
+            for (; ki < 2 && ki < nch; ++ki) {
+                mbar_arrive_expect_tx(&kfull[ki], kTileBytes);
+                tma_load_3d(sm + C::OFF_K + ki * kTileBytes, &tm_k, &kfull[ki], 0, ki * TM, g);
+            }
+            for (; qi < 2 && qi < nch; ++qi) {
+                mbar_arrive_expect_tx(&qfull[qi], kTileBytes);
+                tma_load_3d(sm + C::OFF_Q + qi * kTileBytes, &tm_q, &qfull[qi], 0, qi * TM, g);
+            }
+            for (; vi < 2 && vi < nch; ++vi) {
+                mbar_arrive_expect_tx(&vfull[vi], kTileBytes);
+                tma_load_3d(sm + C::OFF_V + vi * kTileBytes, &tm_v, &vfull[vi], 0, vi * TM, g);
+            }
+            grid_dep_wait();
             mbar_arrive_expect_tx(w_full, param_bytes(K));
             bulk_load(sm + C::OFF_P, A.params + (size_t)(g % A.H) * A.param_stride, param_bytes(K), w_full);
-            int qi = 0, ki = 0, vi = 0;
             long long last = clock64();
             while ((qi < nch || ki < nch || vi < nch) && !*abort_flag) {
                 bool progress = false;
@@ -275,7 +290,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         rt.lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         rt.wtid = threadIdx.x - kWGroups * 32 - rt.wg * kWgThreads;
         const bool elected = rt.wtid == 0;
-        const float scale = head_scale(A.params, A.param_stride, g % A.H, K);
+        float scale = 0.f;                                 // read once the parameter blocks are written
 
         if (rt.wg == 0) {
             // ---------------- key group
@@ -295,6 +310,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (c >= 1) w = w && mbar_wait(g_empty, (c - 1) & 1, ab, kDevErrTimeout);
                 if (!(ok = wg_all(rt, w))) break;
                 tc_fence_after();
+                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, K); }
                 // gamma^K = softmax of the key scores; rows past the sequence end get 0
                 uint32_t e[K / 2];
                 row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1K, scale, e);
@@ -368,6 +384,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
                 if (!(ok = wg_all(rt, w))) break;
                 tc_fence_after();
+                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, K); }
                 uint32_t e[K / 2];
                 row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1Q, scale, e);
                 // e^Q(c) replaces e^Q(c - 1) once the read of chunk c - 1 has consumed it
@@ -525,8 +542,7 @@ cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const
     cudaError_t e = cudaFuncSetAttribute(tc_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CausalCfg::BYTES);
     if (e != cudaSuccess) return e;
-    tc_causal_kernel<<<p.G, kCThreads, CausalCfg::BYTES, s>>>(tq, tk, tv, to, a);
-    return cudaGetLastError();
+    return launch_dependent(tc_causal_kernel, dim3(p.G), dim3(kCThreads), CausalCfg::BYTES, s, tq, tk, tv, to, a);
 }
 
 }  // namespace gma
