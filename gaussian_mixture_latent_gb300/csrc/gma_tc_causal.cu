@@ -23,13 +23,13 @@
 // One CTA per head.  Warps: 0 TMA producer; 1 TMEM owner and issuer of the
 // log-density MMAs (keys, then queries); 2 issuer of the chained MMAs (T, the
 // state update, the read); 3-6 key group (convert, softmax, state snapshot);
-// 7-10 query group (convert, exp); 11-14 output group (mask, epilogue, store).
+// 7-10 query group (convert, exp, epilogue and store); 11-14 mask group.
 //
 // T is formed in two 64-key halves through one 64-column TMEM buffer: rows
 // 0..63 never see keys 64..127, so that half of the masked tile stays zero.
 // e^Q, T and the read result have TMEM columns of their own, so chunk c + 1's
-// query scores and T proceed while chunk c is read, and the output group runs
-// chunk c - 1's epilogue while the second half of T(c) is computed.
+// query scores and T proceed while chunk c is read, and the query group runs
+// chunk c - 1's epilogue once it has published e^Q(c).
 // Every mbarrier wait is bounded; a timeout posts GMA_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -379,60 +379,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (elected) { mbar_arrive(aq_full); mbar_arrive(&qempty[c & 1]); }
                 return true;
             };
-            bool ok = convert_q(0);
-            for (int c = 0; c < nch && ok; ++c) {
-                bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
-                if (!(ok = wg_all(rt, w))) break;
-                tc_fence_after();
-                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, K); }
-                uint32_t e[K / 2];
-                row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1Q, scale, e);
-                // e^Q(c) replaces e^Q(c - 1) once the read of chunk c - 1 has consumed it
-                if (c >= 1) {
-                    w = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
-                    if (!(ok = wg_all(rt, w))) break;
-                    tc_fence_after();
-                }
-                tmem_st32(tmem + rt.lane_off + C::COL_EQ, e);
-                tmem_st_wait();
-                tc_fence_before();
-                wg_sync(rt);
-                if (elected) mbar_arrive(e_full);
-                // the scores of chunk c have been read: the next query tile may overwrite them
-                if (c + 1 < nch && !(ok = convert_q(c + 1))) break;
-            }
-        } else {
-            // ---------------- output group
-            // Row quarter q = warp & 3 holds rows 32q..32q+31.  A group of 32 keys is copied
-            // whole below the quarter's diagonal, selected (j <= r) on it, and never touched
-            // above it (those entries of the masked tile stay zero from the start).
-            const int q = warp & 3;
-            auto mask_group = [&](const uint32_t *v, int key0, bool diag, uint8_t *half, int cc) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const uint32_t j0 = (uint32_t)key0 + 2u * t;
-                    const float a = !diag || j0 <= rt.r ? __uint_as_float(v[2 * t]) : 0.f;
-                    const float b2 = !diag || j0 + 1 <= rt.r ? __uint_as_float(v[2 * t + 1]) : 0.f;
-                    pk[t] = pack_bf16(a, b2);
-                }
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4 *>(half + sw128_off(rt.r, cc * 4 + q4)) =
-                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-            };
-            // one half of T (64 keys starting at key0) from TMEM into the masked bf16 tile
-            auto mask_half = [&](int key0, uint8_t *half) {
-                const int g0 = key0 / 32;                     // global index of the half's first group
-                if (q < g0) return;                           // the whole half lies above the diagonal
-                uint32_t v0[32], v1[32];
-                tmem_ld32(tmem + rt.lane_off + C::COL_T, v0);
-                tmem_ld32(tmem + rt.lane_off + C::COL_T + 32, v1);
-                tmem_ld_wait();
-                mask_group(v0, key0, q == g0, half, 0);
-                if (q > g0) mask_group(v1, key0 + 32, q == g0 + 1, half, 1);
-            };
             auto epilogue = [&](int c) {
+                // called once read(c) is known complete (d3_full(c) waited)
                 // out = num / (den + eps * sum_k e^Q_k)
                 uint32_t v0[32], v1[32], dz[4];
                 tmem_ld32(tmem + rt.lane_off + C::COL_D3, v0);
@@ -466,6 +414,69 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     bulk_commit_group();
                 }
             };
+            bool ok = convert_q(0);
+            for (int c = 0; c < nch && ok; ++c) {
+                bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
+                if (!(ok = wg_all(rt, w))) break;
+                tc_fence_after();
+                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, K); }
+                uint32_t e[K / 2];
+                row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1Q, scale, e);
+                // e^Q(c) replaces e^Q(c - 1) once the read of chunk c - 1 has consumed it
+                if (c >= 1) {
+                    w = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
+                    if (!(ok = wg_all(rt, w))) break;
+                    tc_fence_after();
+                }
+                tmem_st32(tmem + rt.lane_off + C::COL_EQ, e);
+                tmem_st_wait();
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) mbar_arrive(e_full);
+                // read(c - 1) is complete (waited above): its epilogue, off the critical chain
+                if (c >= 1) epilogue(c - 1);
+                // the scores of chunk c have been read: the next query tile may overwrite them
+                if (c + 1 < nch && !(ok = convert_q(c + 1))) break;
+            }
+            if (ok) {
+                const bool w = mbar_wait(d3_full, (nch - 1) & 1, ab, kDevErrTimeout);
+                if (wg_all(rt, w)) {
+                    tc_fence_after();
+                    epilogue(nch - 1);
+                }
+            }
+            if (elected) bulk_wait_group<0>();
+        } else {
+            // ---------------- output group
+            // Row quarter q = warp & 3 holds rows 32q..32q+31.  A group of 32 keys is copied
+            // whole below the quarter's diagonal, selected (j <= r) on it, and never touched
+            // above it (those entries of the masked tile stay zero from the start).
+            const int q = warp & 3;
+            auto mask_group = [&](const uint32_t *v, int key0, bool diag, uint8_t *half, int cc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const uint32_t j0 = (uint32_t)key0 + 2u * t;
+                    const float a = !diag || j0 <= rt.r ? __uint_as_float(v[2 * t]) : 0.f;
+                    const float b2 = !diag || j0 + 1 <= rt.r ? __uint_as_float(v[2 * t + 1]) : 0.f;
+                    pk[t] = pack_bf16(a, b2);
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4 *>(half + sw128_off(rt.r, cc * 4 + q4)) =
+                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            };
+            // one half of T (64 keys starting at key0) from TMEM into the masked bf16 tile
+            auto mask_half = [&](int key0, uint8_t *half) {
+                const int g0 = key0 / 32;                     // global index of the half's first group
+                if (q < g0) return;                           // the whole half lies above the diagonal
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tmem + rt.lane_off + C::COL_T, v0);
+                tmem_ld32(tmem + rt.lane_off + C::COL_T + 32, v1);
+                tmem_ld_wait();
+                mask_group(v0, key0, q == g0, half, 0);
+                if (q > g0) mask_group(v1, key0 + 32, q == g0 + 1, half, 1);
+            };
             bool ok = true;
             for (int c = 0; c < nch && ok; ++c) {
                 // keys 0..63 of T(c); the masked tile is free once the read of chunk c - 1 is done
@@ -477,8 +488,6 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_before();
                 wg_sync(rt);
                 if (elected) mbar_arrive(ta_free);
-                // chunk c - 1's epilogue while the second half of T(c) is computed
-                if (c >= 1) epilogue(c - 1);
                 // keys 64..127 of T(c)
                 w = mbar_wait(tb2_full, c & 1, ab, kDevErrTimeout);
                 if (!(ok = wg_all(rt, w))) break;
@@ -489,14 +498,6 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 wg_sync(rt);
                 if (elected) { mbar_arrive(t_empty); mbar_arrive(tb_full); }
             }
-            if (ok) {
-                const bool w = mbar_wait(d3_full, (nch - 1) & 1, ab, kDevErrTimeout);
-                if (wg_all(rt, w)) {
-                    tc_fence_after();
-                    epilogue(nch - 1);
-                }
-            }
-            if (elected) bulk_wait_group<0>();
         }
     }
     tc_fence_before();
