@@ -85,15 +85,19 @@ def csrc_hash():
 
 
 def known_traffic(kernel):
-    path = os.path.join(ROOT, "profiles", "kernel_traffic.json")
+    """DRAM bytes (read + write) per launch of `kernel` on this workload, from an ncu
+    capture recorded in profiles/kernel_traffic.txt, or None when the recorded capture
+    was taken on different CUDA sources (any change to csrc invalidates it)."""
+    path = os.path.join(ROOT, "profiles", "kernel_traffic.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        t = json.load(f)
-    e = t.get(kernel)
-    if not e or e.get("csrc_hash") != csrc_hash() or e.get("workload") != WORKLOAD:
-        return None
-    return e["bytes_per_launch"]
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == WORKLOAD \
+                    and parts[2] == csrc_hash():
+                return int(parts[3])
+    return None
 
 
 class ClockSampler:
