@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--direction", choices=["both", "bidir", "causal"], default="both",
+                    help="which forward(s) one step runs (default: both, the headline step)")
     return ap.parse_args()
 
 
@@ -166,7 +168,7 @@ def gpu_id_for(dev_index):
     return str(dev_index)
 
 
-def cpu_baseline(w, seconds=12.0):
+def cpu_baseline(w, dirs=(False, True), seconds=12.0):
     """Time the fp64 oracle, as it stands, on a bounded sample of the workload:
     the first `heads` heads, full sequence, both directions, one thread per head,
     repeated until about `seconds` of wall time have passed."""
@@ -184,15 +186,16 @@ def cpu_baseline(w, seconds=12.0):
     mu, rho, al = p["mu"][hs], p["rho"][hs], p["alpha"][hs]
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, False, threads=heads)
-        oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, True, threads=heads)
+        for causal in dirs:
+            oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, causal, threads=heads)
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= seconds:
             break
-    units = 2 * heads * w.N * reps
+    units = len(dirs) * heads * w.N * reps
+    what = " + ".join("causal" if c else "bidirectional" for c in dirs)
     return {"value": units / dt, "unit": "tokens·heads/s", "cores": heads, "kind": "oracle",
-            "sample": f"{heads} heads x N={w.N} of the {w.name} workload, bidirectional + causal, "
+            "sample": f"{heads} heads x N={w.N} of the {w.name} workload, {what}, "
                       f"{reps} passes (fp64 C oracle, one thread per head), {dt:.1f} s wall"}
 
 
@@ -213,9 +216,12 @@ def run_reference(args, rank, world):
     hs = [g % w.H for g in range(heads)]
     mu, rho, al = p["mu"][hs], p["rho"][hs], p["alpha"][hs]
 
+    dirs = {"both": (False, True), "bidir": (False,), "causal": (True,)}[args.direction]
+    what = " + ".join("causal" if c else "bidirectional" for c in dirs)
+
     def step():
-        oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, False, threads=heads)
-        oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, True, threads=heads)
+        for causal in dirs:
+            oracle.forward(Q, Kx, V, mu, rho, al, w.var_floor, w.eps, causal, threads=heads)
 
     steps = args.steps if args.steps is not None else 3
     for _ in range(args.warmup):
@@ -224,16 +230,16 @@ def run_reference(args, rank, world):
     for _ in range(steps):
         step()
     dt = (time.perf_counter() - t0) / steps
-    value = 2 * heads * w.N / dt
+    value = len(dirs) * heads * w.N / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens·heads/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                                        "K": w.K, "dv": w.dv, "step": "bidirectional + causal forward",
+                                        "K": w.K, "dv": w.dv, "step": what + " forward",
                                         "sample_heads": heads},
         "cpu_baseline": {"value": value, "unit": "tokens·heads/s", "cores": heads, "kind": "oracle",
-                         "sample": f"each step: {heads} heads x N={w.N}, bidirectional + causal"},
+                         "sample": f"each step: {heads} heads x N={w.N}, {what}"},
         "e2e": {"value": value, "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -267,8 +273,9 @@ def run_gpu(args, rank, world, local):
 
     sets = [make_set(0), make_set(1)]
     dsets = [s[0] for s in sets]
-    outs = {c: torch.empty((w.B, w.H, w.N, w.dv), dtype=tdt, device=dev) for c in (False, True)}
-    plan = {c: gma.gma_forward_plan(w.B, w.H, w.N, w.d, w.K, w.dv, tdt, causal=c) for c in (False, True)}
+    dirs = {"both": (False, True), "bidir": (False,), "causal": (True,)}[args.direction]
+    outs = {c: torch.empty((w.B, w.H, w.N, w.dv), dtype=tdt, device=dev) for c in dirs}
+    plan = {c: gma.gma_forward_plan(w.B, w.H, w.N, w.d, w.K, w.dv, tdt, causal=c) for c in dirs}
     stream = torch.cuda.current_stream()
 
     def new_event():
@@ -287,14 +294,14 @@ def run_gpu(args, rank, world, local):
     per = {}
     for it in range(max(3, args.warmup)):
         evs = {}
-        for c in (False, True):
+        for c in dirs:
             evs[c] = [new_event() for _ in range(2 * len(plan[c]))]
             # keep the GPU busy while the host enqueues, so the events bracket GPU time only
             torch.cuda._sleep(2_000_000)
             forward(dsets[it % 2], c, evs[c])
         torch.cuda.synchronize()
         if it >= 1:
-            for c in (False, True):
+            for c in dirs:
                 for i, name in enumerate(plan[c]):
                     per.setdefault((c, name), []).append(evs[c][2 * i].elapsed_time(evs[c][2 * i + 1]))
     status = gma.gma_get_status()
@@ -321,7 +328,7 @@ def run_gpu(args, rank, world, local):
     t_start.record(stream)
     for it in range(steps):
         x = dsets[it % 2]
-        for c in (False, True):
+        for c in dirs:
             if c == dom_c:
                 evs = [None] * (2 * len(plan[c]))
                 evs[2 * dom_idx], evs[2 * dom_idx + 1] = dom_events[it]
@@ -342,7 +349,7 @@ def run_gpu(args, rank, world, local):
     if status:
         raise RuntimeError("device status after timed region: " + gma.gma_status_string(status))
     dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom_events)
-    units_per_step = 2 * w.G * w.N
+    units_per_step = len(dirs) * w.G * w.N
     value = world * units_per_step / (ms_per_step / 1e3)
 
     # roofline of the dominant kernel
@@ -365,8 +372,8 @@ def run_gpu(args, rank, world, local):
                 "derived: 152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}
 
     # whole-path roofline of one step (both directions)
-    alg_bytes = 2 * accounting.algorithmic_bytes(w.G, w.N, w.d, w.K, w.dv, w.dtype, w.dtype, H=w.H)
-    alg_flops = 2 * accounting.algorithmic_flops(w.G, w.N, w.d, w.K, w.dv)
+    alg_bytes = len(dirs) * accounting.algorithmic_bytes(w.G, w.N, w.d, w.K, w.dv, w.dtype, w.dtype, H=w.H)
+    alg_flops = len(dirs) * accounting.algorithmic_flops(w.G, w.N, w.d, w.K, w.dv)
     t_roof = max(alg_bytes / (pk["hbm_gbs"] * 1e9), alg_flops / (pk["bf16_tflops"] * 1e12))
     path = {"algorithmic_bytes_per_step": alg_bytes, "algorithmic_flops_per_step": alg_flops,
             "roofline_ms_per_step": t_roof * 1e3, "frac": t_roof * 1e3 / ms_per_step,
@@ -376,7 +383,7 @@ def run_gpu(args, rank, world, local):
     e2e = None
     if args.e2e_steps > 0:
         host = [{k: v.cpu().pin_memory() for k, v in d.items()} for d in dsets]
-        hout = {c: torch.empty(outs[c].shape, dtype=tdt, pin_memory=True) for c in (False, True)}
+        hout = {c: torch.empty(outs[c].shape, dtype=tdt, pin_memory=True) for c in dirs}
         staging = {k: torch.empty_like(v) for k, v in dsets[0].items()}
         h2d = sum(v.numel() * v.element_size() for v in host[0].values())
         d2h = sum(v.numel() * v.element_size() for v in hout.values())
@@ -384,7 +391,7 @@ def run_gpu(args, rank, world, local):
         def e2e_step(i):
             for k, v in host[i % 2].items():
                 staging[k].copy_(v, non_blocking=True)
-            for c in (False, True):
+            for c in dirs:
                 forward(staging, c)
                 hout[c].copy_(outs[c], non_blocking=True)
 
@@ -403,22 +410,23 @@ def run_gpu(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w)
+        cpu = cpu_baseline(w, dirs)
 
     if rank == 0:
-        launches = steps * (len(plan[False]) + len(plan[True]))
+        launches = steps * sum(len(plan[c]) for c in dirs)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens·heads/s", "n_gpus": world,
             "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K,
-                       "dv": w.dv, "step": "bidirectional + causal forward",
+                       "dv": w.dv, "step": {"both": "bidirectional + causal forward", "bidir": "bidirectional forward",
+                                "causal": "causal forward"}[args.direction],
                        "l2": "two alternating input sets of %d MB each (> 129 MB L2)" %
                              (sum(v.numel() * v.element_size() for v in dsets[0].values()) // 2**20),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "path_roofline": path, "clocks": clocks,
-            "gpu_launches": launches, "kernels": {"bidir": plan[False], "causal": plan[True]},
+            "gpu_launches": launches, "kernels": {("causal" if c else "bidir"): plan[c] for c in dirs},
             "e2e": e2e, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
