@@ -176,3 +176,28 @@ def test_responsibilities_export_matches_oracle():
                                           x["rho"][h], x["alpha"][h], w.var_floor)
             assert np.abs(got[0, h] - ref).max() <= tol
             np.testing.assert_allclose(got[0, h].sum(1), 1.0, atol=1e-5)
+
+
+def test_back_to_back_forwards_do_not_interfere():
+    # Kernels of one forward start while the previous kernel drains (programmatic
+    # dependent launch); consecutive forwards on different inputs, in both
+    # directions and with shared workspace, must each equal a forward run alone.
+    import gaussian_mixture_latent_gb300 as gma
+    w = inputs.Workload("b2b", B=2, H=4, N=1500, d=64, K=64, dv=64, dtype="bf16", causal=False)
+    sets = [inputs.gen_all(w.replace(seed=s)) for s in (11, 12)]
+    dev = [{k: to_device(v) for k, v in x.items()} for x in sets]
+
+    def fwd(x, causal):
+        return gma.gma_forward(x["Qx"], x["Kx"], x["V"], x["mu"], x["rho"], x["alpha"], eps=w.eps,
+                               causal=causal, var_floor=w.var_floor)
+
+    alone = {}
+    for i in range(2):
+        for causal in (False, True):
+            alone[i, causal] = to_f64(fwd(dev[i], causal))
+            torch.cuda.synchronize()
+    outs = [(i % 2, causal, fwd(dev[i % 2], causal)) for i in range(6) for causal in (False, True)]
+    torch.cuda.synchronize()
+    assert gma.gma_get_status() == 0
+    for i, causal, o in outs:
+        assert np.array_equal(to_f64(o), alone[i, causal])
