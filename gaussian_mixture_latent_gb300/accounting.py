@@ -69,4 +69,14 @@ def kernel_work(name: str, G, N, d, K, dv, in_dtype="bf16", out_dtype="bf16", H=
         return "hbm", rows * (e_in * d + e_out * dv), "byte"
     if name == "tc_causal":
         return "hbm", rows * (e_in * (2 * d + dv) + e_out * dv), "byte"
+    if name == "tc_causal_slices":
+        # the component-sliced scan does all of the path's contractions
+        return "tensor", algorithmic_flops(G, N, d, K, dv), "flop"
+    if name == "tc_rowstats":
+        return "hbm", rows * e_in * 2 * d, "byte"
+    if name == "tc_combine":
+        # executed (not algorithmic) traffic: the bf16 partial numerators and fp32
+        # partial denominators of every component slice in, the output out
+        ns = max(1, K // 64)
+        return "hbm", rows * (ns * (2 * dv + 4) + e_out * dv), "byte"
     return None, 0, None

@@ -86,6 +86,17 @@ gma_status build_forward_plan(const Problem &p, const Args *a, Plan &plan) {
         plan.add("tc_causal", [=](cudaStream_t s) { return tc_causal(p, T, A.Qx, A.Kx, A.V, A.out, ws, s); });
         return GMA_OK;
     }
+    if (tc_slice_supported(p)) {
+        const TcLayout T = tc_slice_layout(p);
+        plan.workspace = T.total;
+        const Args A = a ? *a : z;
+        char *ws = A.ws;
+        plan.add("tc_params", [=](cudaStream_t s) { return tc_params(p, T, A.mu, A.rho, A.alpha, ws, s); });
+        plan.add("tc_rowstats", [=](cudaStream_t s) { return tc_rowstats(p, T, A.Qx, A.Kx, ws, s); });
+        plan.add("tc_causal_slices", [=](cudaStream_t s) { return tc_causal_slices(p, T, A.Qx, A.Kx, A.V, ws, s); });
+        plan.add("tc_combine", [=](cudaStream_t s) { return tc_combine(p, T, A.out, ws, s); });
+        return GMA_OK;
+    }
     const SimtLayout L = simt_layout(p);
     if (p.causal && simt_causal_smem(p) > kMaxDynSmem) return GMA_ERR_UNSUPPORTED;
     plan.workspace = L.total;

@@ -44,6 +44,8 @@ SimtLayout simt_layout(const Problem &p);
 constexpr int kMaxCtas = 256;        // upper bound on persistent CTAs (partial slots are sized for it)
 struct TcLayout {
     size_t params, part, mem, total;   // workspace byte offsets
+    size_t stats, pnum, pden;          // component-sliced causal path: row statistics, partials
+    int ns, nt;                        // component slices and value slices of 64
     uint32_t param_stride, mem_stride;
     int T, Ttot, ncta;                 // tiles per head, tiles in total, persistent CTAs
 };
@@ -60,6 +62,14 @@ cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *o
 // ----- tensor-core causal path: gma_tc_causal.cu (uses tc_params for the coefficients) -----
 bool tc_causal_supported(const Problem &p);
 TcLayout tc_causal_layout(const Problem &p);
+// component-sliced causal path (gma_tc_slice.cu + gma_tc_causal.cu): larger K or dv
+bool tc_slice_supported(const Problem &p);
+TcLayout tc_slice_layout(const Problem &p);
+cudaError_t tc_rowstats(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, char *ws,
+                        cudaStream_t s);
+cudaError_t tc_causal_slices(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
+                             char *ws, cudaStream_t s);
+cudaError_t tc_combine(const Problem &p, const TcLayout &L, void *out, char *ws, cudaStream_t s);
 cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
                       void *out, char *ws, cudaStream_t s);
 

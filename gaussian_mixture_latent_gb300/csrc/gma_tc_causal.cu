@@ -56,6 +56,13 @@ struct CausalArgs {
     uint32_t param_stride;
     float eps;
     unsigned *status;
+    // component-sliced form (larger K or dv): this CTA takes components [64 s, 64 s + 64) of a
+    // Kfull-component head and value columns [64 t, 64 t + 64) of a dvt-wide V
+    int Kfull, dvt;
+    const float *mrow_q;   // [G][N] max_k scores of each query row (log2 units, scaled)
+    const float *lse_k;    // [G][N] log2 sum_k 2^score of each key row
+    uint16_t *pnum;        // [ns][G][N][dvt] bf16 partial numerators
+    float *pden;           // [ns][G][N] partial denominators
 };
 
 struct CausalCfg {
@@ -85,6 +92,13 @@ static_assert(CausalCfg::OFF_SB % 1024 == 0 && CausalCfg::OFF_P % 1024 == 0 && C
               "operand blocks must be 1024-byte aligned");
 static_assert(CausalCfg::BYTES <= 232448, "causal kernel exceeds the shared-memory opt-in limit");
 
+// SLICE = false: one head per CTA, O written directly.  SLICE = true: one (head,
+// component slice, value slice) per CTA (grid G x Kfull/64 x dvt/64); the key
+// responsibilities are normalised over all Kfull components with the row's
+// log-sum-exp, e^Q is taken relative to the row's maximum over all components,
+// and the CTA writes its partial numerator and denominator, which the combine
+// kernel sums over component slices (every term is a sum over components).
+template <bool SLICE>
 __global__ void __launch_bounds__(kCThreads, 1)
 tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -109,6 +123,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.x, nch = A.nch;
+    const int ks = SLICE ? (int)blockIdx.y : 0, vs = SLICE ? (int)blockIdx.z : 0;   // component / value slice
     grid_dep_launch();
 
     if (threadIdx.x == 0) {
@@ -160,11 +175,23 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             for (; vi < 2 && vi < nch; ++vi) {
                 mbar_arrive_expect_tx(&vfull[vi], kTileBytes);
-                tma_load_3d(sm + C::OFF_V + vi * kTileBytes, &tm_v, &vfull[vi], 0, vi * TM, g);
+                tma_load_3d(sm + C::OFF_V + vi * kTileBytes, &tm_v, &vfull[vi], 64 * vs, vi * TM, g);
             }
             grid_dep_wait();
-            mbar_arrive_expect_tx(w_full, param_bytes(K));
-            bulk_load(sm + C::OFF_P, A.params + (size_t)(g % A.H) * A.param_stride, param_bytes(K), w_full);
+            const uint8_t *blk = A.params + (size_t)(g % A.H) * A.param_stride;
+            if (SLICE) {
+                // the slice's 64 rows of each part of a Kfull-component block, in the K = 64 layout
+                // (row groups of 8 keep their 1 KB swizzle atoms and no-swizzle core matrices)
+                constexpr uint32_t kRows = 64u * 128u, kWc = 64u * 32u;
+                mbar_arrive_expect_tx(w_full, 2 * kRows + kWc + 16u);
+                bulk_load(sm + C::OFF_P, blk + (size_t)ks * kRows, kRows, w_full);
+                bulk_load(sm + C::OFF_P + kRows, blk + 128u * A.Kfull + (size_t)ks * kRows, kRows, w_full);
+                bulk_load(sm + C::OFF_P + param_wc_off(K), blk + param_wc_off(A.Kfull) + (size_t)ks * kWc, kWc, w_full);
+                bulk_load(sm + C::OFF_P + param_scale_off(K), blk + param_scale_off(A.Kfull), 16u, w_full);
+            } else {
+                mbar_arrive_expect_tx(w_full, param_bytes(K));
+                bulk_load(sm + C::OFF_P, blk, param_bytes(K), w_full);
+            }
             long long last = clock64();
             while ((qi < nch || ki < nch || vi < nch) && !*abort_flag) {
                 bool progress = false;
@@ -182,7 +209,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 if (vi < nch && (vi < 2 || mbar_test(&vempty[vi & 1], ((vi >> 1) - 1) & 1))) {
                     mbar_arrive_expect_tx(&vfull[vi & 1], kTileBytes);
-                    tma_load_3d(sm + C::OFF_V + (vi & 1) * kTileBytes, &tm_v, &vfull[vi & 1], 0, vi * TM, g);
+                    tma_load_3d(sm + C::OFF_V + (vi & 1) * kTileBytes, &tm_v, &vfull[vi & 1], 64 * vs, vi * TM, g);
                     ++vi;
                     progress = true;
                 }
@@ -310,18 +337,28 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (c >= 1) w = w && mbar_wait(g_empty, (c - 1) & 1, ab, kDevErrTimeout);
                 if (!(ok = wg_all(rt, w))) break;
                 tc_fence_after();
-                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, K); }
+                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull); }
                 // gamma^K = softmax of the key scores; rows past the sequence end get 0
                 uint32_t e[K / 2];
-                row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1K, scale, e);
-                uint64_t acc[4] = {0, 0, 0, 0};
+                float inv;
+                if (SLICE) {
+                    // normalised over all components by the row's log-sum-exp
+                    const int row = c * TM + (int)rt.r;
+                    row_exp_offset<K>(tmem + rt.lane_off + C::COL_D1K, scale,
+                                      row < A.N ? __ldg(A.lse_k + (size_t)g * A.N + row) : INFINITY, e);
+                    inv = 1.0f;
+                } else {
+                    row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1K, scale, e);
+                    uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-                for (int t = 0; t < K / 2; ++t) acc[t & 3] = f2_add(acc[t & 3], f2_pack(bf16_lo(e[t]), bf16_hi(e[t])));
-                float s0, s1, s2, s3, s4, s5, s6, s7;
-                f2_unpack(acc[0], s0, s1); f2_unpack(acc[1], s2, s3);
-                f2_unpack(acc[2], s4, s5); f2_unpack(acc[3], s6, s7);
-                const float total = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-                const float inv = c * TM + (int)rt.r < A.N ? 1.0f / total : 0.f;
+                    for (int t = 0; t < K / 2; ++t)
+                        acc[t & 3] = f2_add(acc[t & 3], f2_pack(bf16_lo(e[t]), bf16_hi(e[t])));
+                    float s0, s1, s2, s3, s4, s5, s6, s7;
+                    f2_unpack(acc[0], s0, s1); f2_unpack(acc[1], s2, s3);
+                    f2_unpack(acc[2], s4, s5); f2_unpack(acc[3], s6, s7);
+                    const float total = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+                    inv = c * TM + (int)rt.r < A.N ? 1.0f / total : 0.f;
+                }
                 const uint64_t inv2 = f2_pack(inv, inv);
 #pragma unroll
                 for (int j = 0; j < K / 8; ++j) {
@@ -387,7 +424,29 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tmem_ld32(tmem + rt.lane_off + C::COL_D3 + 32, v1);
                 tmem_ld4(tmem + rt.lane_off + C::COL_D3 + 64, dz);
                 tmem_ld_wait();
-                const float rd = 1.0f / (__uint_as_float(dz[0]) + A.eps * __uint_as_float(dz[1]));
+                const float den = __uint_as_float(dz[0]) + A.eps * __uint_as_float(dz[1]);
+                if (SLICE) {
+                    // partial numerator (bf16) and denominator of this component slice
+                    tc_fence_before();
+                    wg_sync(rt);
+                    if (elected) mbar_arrive(d3_empty);
+                    const int row = c * TM + (int)rt.r;
+                    if (row < A.N) {
+                        const size_t pr = ((size_t)ks * A.G + g) * A.N + row;
+                        uint4 *dst = reinterpret_cast<uint4 *>(A.pnum + pr * A.dvt + 64 * vs);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t *src = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+                            dst[j] = make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                                pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                                pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                                                pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
+                        }
+                        if (vs == 0) A.pden[pr] = den;
+                    }
+                    return;
+                }
+                const float rd = 1.0f / den;
                 const uint64_t rd2 = f2_pack(rd, rd);
                 if (elected) bulk_wait_group_read<0>();          // the previous store has left the staging tile
                 tc_fence_before();
@@ -419,9 +478,16 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
                 if (!(ok = wg_all(rt, w))) break;
                 tc_fence_after();
-                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, K); }
+                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull); }
                 uint32_t e[K / 2];
-                row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1Q, scale, e);
+                if (SLICE) {
+                    // relative to the row's maximum over all components
+                    const int row = c * TM + (int)rt.r;
+                    row_exp_offset<K>(tmem + rt.lane_off + C::COL_D1Q, scale,
+                                      row < A.N ? __ldg(A.mrow_q + (size_t)g * A.N + row) : 0.f, e);
+                } else {
+                    row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1Q, scale, e);
+                }
                 // e^Q(c) replaces e^Q(c - 1) once the read of chunk c - 1 has consumed it
                 if (c >= 1) {
                     w = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
@@ -516,11 +582,17 @@ bool tc_causal_supported(const Problem &p) {
            p.K == KC && p.N > 0;
 }
 
+bool tc_slice_supported(const Problem &p) {
+    return p.in_dtype == GMA_BF16 && p.out_dtype == GMA_BF16 && p.causal && p.d == DR && p.N > 0 &&
+           p.K % KC == 0 && p.K <= 256 && p.dv % DVV == 0 && p.dv <= 256 && !tc_causal_supported(p);
+}
+
 TcLayout tc_causal_layout(const Problem &p) {
     TcLayout L{};
     L.T = (p.N + TM - 1) / TM;
     L.Ttot = L.T * p.G;
     L.ncta = p.G;
+    L.ns = L.nt = 1;
     L.param_stride = align1k(param_bytes(p.K));
     L.params = align_up(kHeaderBytes);
     L.part = L.mem = L.params + (size_t)p.H * L.param_stride;
@@ -528,11 +600,29 @@ TcLayout tc_causal_layout(const Problem &p) {
     return L;
 }
 
-cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
-                      void *out, char *ws, cudaStream_t s) {
+TcLayout tc_slice_layout(const Problem &p) {
+    TcLayout L{};
+    L.T = (p.N + TM - 1) / TM;
+    L.Ttot = L.T * p.G;
+    L.ns = p.K / KC;
+    L.nt = p.dv / DVV;
+    L.ncta = p.G * L.ns * L.nt;
+    L.param_stride = align1k(param_bytes(p.K));
+    L.params = align_up(kHeaderBytes);
+    const size_t rows = (size_t)p.G * p.N;
+    L.stats = align_up(L.params + (size_t)p.H * L.param_stride);              // [2][G][N] f32
+    L.pnum = align_up(L.stats + 2 * rows * sizeof(float));                     // [ns][G][N][dv] bf16
+    L.pden = align_up(L.pnum + (size_t)L.ns * rows * p.dv * 2);                // [ns][G][N] f32
+    L.part = L.mem = L.pden;
+    L.total = align_up(L.pden + (size_t)L.ns * rows * sizeof(float));
+    return L;
+}
+
+static cudaError_t launch_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
+                                 void *out, char *ws, cudaStream_t s, bool slices) {
     CUtensorMap tq, tk, tv, to;
-    if (!make_map(&tq, Qx, p.G, p.N, DR) || !make_map(&tk, Kx, p.G, p.N, DR) || !make_map(&tv, V, p.G, p.N, DVV) ||
-        !make_map(&to, out, p.G, p.N, DVV))
+    if (!make_map(&tq, Qx, p.G, p.N, DR) || !make_map(&tk, Kx, p.G, p.N, DR) || !make_map(&tv, V, p.G, p.N, p.dv) ||
+        !make_map(&to, slices ? V : out, p.G, p.N, p.dv))
         return cudaErrorInvalidValue;
     CausalArgs a{};
     a.G = p.G; a.H = p.H; a.N = p.N; a.nch = L.T;
@@ -540,10 +630,28 @@ cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const
     a.param_stride = L.param_stride;
     a.eps = p.eps;
     a.status = reinterpret_cast<unsigned *>(ws);
-    cudaError_t e = cudaFuncSetAttribute(tc_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         CausalCfg::BYTES);
+    a.Kfull = p.K;
+    a.dvt = p.dv;
+    if (slices) {
+        a.mrow_q = reinterpret_cast<const float *>(ws + L.stats);
+        a.lse_k = a.mrow_q + (size_t)p.G * p.N;
+        a.pnum = reinterpret_cast<uint16_t *>(ws + L.pnum);
+        a.pden = reinterpret_cast<float *>(ws + L.pden);
+    }
+    auto kern = slices ? tc_causal_kernel<true> : tc_causal_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CausalCfg::BYTES);
     if (e != cudaSuccess) return e;
-    return launch_dependent(tc_causal_kernel, dim3(p.G), dim3(kCThreads), CausalCfg::BYTES, s, tq, tk, tv, to, a);
+    return launch_dependent(kern, dim3(p.G, L.ns, L.nt), dim3(kCThreads), CausalCfg::BYTES, s, tq, tk, tv, to, a);
+}
+
+cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
+                      void *out, char *ws, cudaStream_t s) {
+    return launch_causal(p, L, Qx, Kx, V, out, ws, s, false);
+}
+
+cudaError_t tc_causal_slices(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
+                             char *ws, cudaStream_t s) {
+    return launch_causal(p, L, Qx, Kx, V, nullptr, ws, s, true);
 }
 
 }  // namespace gma

@@ -177,6 +177,24 @@ __device__ __forceinline__ void row_exp_scaled(uint32_t taddr, float scale, uint
     }
 }
 
+// e = 2^(scale * d - off) for the K raw scores d of this thread's row (one TMEM
+// round trip), as K/2 bf16 pairs: the same rounding as row_exp_scaled, with the
+// row's offset (its maximum or log-sum-exp over a wider component set) given.
+template <int K>
+__device__ __forceinline__ void row_exp_offset(uint32_t taddr, float scale, float off, uint32_t (&e)[K / 2]) {
+    uint32_t d[K];
+#pragma unroll
+    for (int cc = 0; cc < K / 32; ++cc) tmem_ld32(taddr + 32 * cc, d + 32 * cc);
+    tmem_ld_wait();
+    const uint64_t sc2 = f2_pack(scale, scale), no2 = f2_pack(-off, -off);
+#pragma unroll
+    for (int t = 0; t < K; t += 2) {
+        float a, b;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(d[t]), __uint_as_float(d[t + 1])), sc2, no2), a, b);
+        e[t / 2] = pack_bf16(ex2_approx(a), ex2_approx(b));
+    }
+}
+
 // Per-head scale of the coefficient matrix, read from the parameter block in global memory.
 __device__ __forceinline__ float head_scale(const uint8_t *params, uint32_t stride, int h, int K) {
     return __ldg(reinterpret_cast<const float *>(params + (size_t)h * stride + param_scale_off(K)));

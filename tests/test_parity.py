@@ -67,6 +67,10 @@ SMALL = [
     ("bf16_many_heads", 8, 64, 200, 64, 64, 64, "bf16", False),
     ("bf16_many_heads_k128", 4, 32, 300, 64, 128, 64, "bf16", False),
     ("bf16_many_heads_causal", 4, 48, 300, 64, 64, 64, "bf16", True),
+    # component-sliced causal path: K > 64 or dv > 64
+    ("bf16_k128_causal", 2, 3, 700, 64, 128, 64, "bf16", True),
+    ("bf16_k192_causal_ragged", 1, 2, 301, 64, 192, 64, "bf16", True),
+    ("bf16_k64_dv128_causal", 1, 2, 333, 64, 64, 128, "bf16", True),
 ]
 
 
@@ -106,12 +110,13 @@ def test_parity_full_size(name):
     print(f"{name}: max relative error {err:.3e} over heads {heads if len(heads) < 8 else len(heads)}")
 
 
-def test_causal_prefix_is_exact_and_future_rows_do_not_leak():
+@pytest.mark.parametrize("K,dv", [(64, 64), (256, 128)], ids=["direct", "sliced"])
+def test_causal_prefix_is_exact_and_future_rows_do_not_leak(K, dv):
     # Section 5.3 of the paper checks a maximum prefix error of exactly zero.
     # Future routing rows become NaN; future values become large finite values
     # (a masked tensor-core tile multiplies them by an exact 0, and 0 * NaN is
     # NaN in IEEE arithmetic, so NaN values are not part of this check).
-    w = inputs.Workload("causal_leak", B=1, H=2, N=1100, d=64, K=64, dv=64, dtype="bf16", causal=True)
+    w = inputs.Workload("causal_leak", B=1, H=2, N=1100, d=64, K=K, dv=dv, dtype="bf16", causal=True)
     x = inputs.gen_all(w)
     base = to_f64(run_gpu(w, x))
     cut = 517
