@@ -367,11 +367,11 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         }
     } else if (warp == kWarpMma1) {
         // log-density MMAs: scores(i) = [x, x^2/256](i) . W^T into D1 of group i % NW
-        if (lane == 0 && n > 0) {
+        if (n > 0) {                                 // the whole warp, converged
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
                 const int i = c.i, b = c.hl % PN, w = i % NW;
-                if (c.first() && !mbar_wait(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
-                if (!mbar_wait(&a_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
+                if (c.first() && !mbar_wait_warp(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait_warp(&a_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
                                     smem_u32(sm + C::OFF_CA));
@@ -383,14 +383,14 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         }
     } else if (warp == kWarpMma2) {
         // write MMAs: D2 [value row x K] += [V | 1 | 0]^T (128 x rows) . Gamma (rows x K)
-        if (lane == 0 && n > 0) {
+        if (n > 0) {                                 // the whole warp, converged
             constexpr uint32_t idesc = idesc_f16(1, 1, 1, 1, TM, K);
             const uint32_t ones = smem_u32(sm + C::OFF_ONES);
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
                 const int i = c.i, s = i % SV, w = i % NW;
-                if (!mbar_wait(&g_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
-                if (!mbar_wait(&vfull[s], (i / SV) & 1, ab, kDevErrTimeout)) break;
-                if (c.first() && c.hl >= 1 && !mbar_wait(d2_empty, (c.hl - 1) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait_warp(&g_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait_warp(&vfull[s], (i / SV) & 1, ab, kDevErrTimeout)) break;
+                if (c.first() && c.hl >= 1 && !mbar_wait_warp(d2_empty, (c.hl - 1) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
                 const uint32_t va = smem_u32(sm + C::OFF_V + s * kTileBytes);
                 const uint64_t ad = sdesc_sw128(va, ones - va, 1024);
@@ -656,11 +656,11 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 wait_ignoring_abort(&w_full[hl % PN], (hl / PN) & 1, A.status);
         }
     } else if (warp == kWarpMma1) {
-        if (lane == 0 && n > 0) {
+        if (n > 0) {                                 // the whole warp, converged
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
                 const int i = c.i, b = c.hl % PN, w = i % NW;
-                if (c.first() && !mbar_wait(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
-                if (!mbar_wait(&a_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
+                if (c.first() && !mbar_wait_warp(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait_warp(&a_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
                                     smem_u32(sm + C::OFF_CA));
@@ -671,11 +671,11 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     } else if (warp == kWarpMma2) {
         // read MMAs: D2 (128 rows x 80) = e (rows x K, bf16 in TMEM) . [Vt | Z | 1 | 0] (K x 80)
-        if (lane == 0 && n > 0) {
+        if (n > 0) {                                 // the whole warp, converged
             constexpr uint32_t idesc = idesc_f16(1, 1, 0, 0, TM, C::NOUT);
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
                 const int i = c.i, b = c.hl % PN, w = i % NW;
-                if (!mbar_wait(&e_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
+                if (!mbar_wait_warp(&e_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
                 tc_fence_after();
                 const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_M + b * C::MB), 16, 1024);
 #pragma unroll

@@ -230,15 +230,15 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
     } else if (warp == kWIss1) {
         // log-density MMAs: scores = [x, x^2/256] . W^T, keys then queries of each chunk
-        if (lane == 0) {
+        if (true) {                                  // the whole warp, converged
             const uint32_t pw = smem_u32(sm + C::OFF_P), ca = smem_u32(sm + C::OFF_CA);
-            bool ok = mbar_wait(w_full, 0, ab, kDevErrTimeout);
+            bool ok = mbar_wait_warp(w_full, 0, ab, kDevErrTimeout);
             for (int c = 0; c < nch && ok; ++c) {
-                if (!(ok = mbar_wait(ak_full, c & 1, ab, kDevErrTimeout))) break;
+                if (!(ok = mbar_wait_warp(ak_full, c & 1, ab, kDevErrTimeout))) break;
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::COL_D1K, tmem + C::COL_AK, pw, ca);
                 mma_commit(d1k_full);
-                if (!(ok = mbar_wait(aq_full, c & 1, ab, kDevErrTimeout))) break;
+                if (!(ok = mbar_wait_warp(aq_full, c & 1, ab, kDevErrTimeout))) break;
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::COL_D1Q, tmem + C::COL_AQ, pw, ca);
                 mma_commit(d1q_full);
@@ -247,7 +247,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             wait_ignoring_abort(fin1, 0, A.status);
         }
     } else if (warp == kWIss2) {
-        if (lane == 0) {
+        if (true) {                                  // the whole warp, converged
             constexpr uint32_t idesc_t = idesc_f16(1, 1, 0, 0, TM, 64);       // e^Q (TMEM) . gamma^K^T, 64 keys
             constexpr uint32_t idesc_u = idesc_f16(1, 1, 1, 1, TM, K);       // [V | 1]^T . gamma^K
             constexpr uint32_t idesc_r1 = idesc_f16(1, 1, 0, 0, TM, NOUT);   // e^Q . [S | z | 1]
@@ -261,8 +261,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int c = 0; c < nch && ok; ++c) {
                 const int s = c & 1;
                 // T(c), keys 0..63 = e^Q(c) . gamma^K(c)[0:64]^T
-                ok = mbar_wait(e_full, c & 1, ab, kDevErrTimeout) && mbar_wait(g_full, c & 1, ab, kDevErrTimeout);
-                if (ok && c >= 1) ok = mbar_wait(t_empty, (c - 1) & 1, ab, kDevErrTimeout);
+                ok = mbar_wait_warp(e_full, c & 1, ab, kDevErrTimeout) && mbar_wait_warp(g_full, c & 1, ab, kDevErrTimeout);
+                if (ok && c >= 1) ok = mbar_wait_warp(t_empty, (c - 1) & 1, ab, kDevErrTimeout);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -270,8 +270,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mma_ts(tmem + C::COL_T, eq + ks * 8, gk + (uint64_t)((ks * 32u) >> 4), idesc_t, ks > 0);
                 mma_commit(ta_full);
                 // state update: [S | z]^T += [V | 1 | 0]^T . gamma^K, once the previous state is snapshotted
-                if (!(ok = mbar_wait(&vfull[s], (c >> 1) & 1, ab, kDevErrTimeout) &&
-                           mbar_wait(&s_ready[c & 1], (c >> 1) & 1, ab, kDevErrTimeout)))
+                if (!(ok = mbar_wait_warp(&vfull[s], (c >> 1) & 1, ab, kDevErrTimeout) &&
+                           mbar_wait_warp(&s_ready[c & 1], (c >> 1) & 1, ab, kDevErrTimeout)))
                     break;
                 tc_fence_after();
                 const uint32_t va = smem_u32(sm + C::OFF_V + s * kTileBytes);
@@ -282,7 +282,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                            !(c == 0 && ks == 0));
                 mma_commit(s_upd);
                 // T(c), keys 64..127, once the first half has been read
-                if (!(ok = mbar_wait(ta_free, c & 1, ab, kDevErrTimeout))) break;
+                if (!(ok = mbar_wait_warp(ta_free, c & 1, ab, kDevErrTimeout))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
@@ -291,8 +291,8 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 mma_commit(tb2_full);
                 mma_commit(g_empty);
                 // read: e^Q . [S | z | 1]_{c-1} + mask(T) . [V | 1]
-                ok = mbar_wait(tb_full, c & 1, ab, kDevErrTimeout);
-                if (ok && c >= 1) ok = mbar_wait(d3_empty, (c - 1) & 1, ab, kDevErrTimeout);
+                ok = mbar_wait_warp(tb_full, c & 1, ab, kDevErrTimeout);
+                if (ok && c >= 1) ok = mbar_wait_warp(d3_empty, (c - 1) & 1, ab, kDevErrTimeout);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t sbd = sdesc_sw128(smem_u32(sm + C::OFF_SB + (c & 1) * C::SBB), 16, 1024);

@@ -136,19 +136,19 @@ tc_rowstats_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
     } else if (warp == 1) {
         // log-density MMA of tile i into the score columns, once tile i - 1's scores are read
-        if (lane == 0 && n > 0) {
+        if (n > 0) {                                 // the whole warp, converged
             const uint32_t ca = smem_u32(sm + C::OFF_CA), pw = smem_u32(sm + C::OFF_P);
             int hp = -1, nloads = 0;
             bool ok = true;
             for (TileCursor c(t0, n, A.T, 0, 1); c.valid() && ok; c.next()) {
                 const int i = c.i, head = c.g >> 1;
                 if (head != hp) {
-                    if (!(ok = mbar_wait(w_full, nloads & 1, ab, kDevErrTimeout))) break;
+                    if (!(ok = mbar_wait_warp(w_full, nloads & 1, ab, kDevErrTimeout))) break;
                     hp = head;
                     ++nloads;
                 }
-                ok = mbar_wait(&a_full[i & 1], (i >> 1) & 1, ab, kDevErrTimeout);
-                if (ok && i >= 1) ok = mbar_wait(d_empty, (i - 1) & 1, ab, kDevErrTimeout);
+                ok = mbar_wait_warp(&a_full[i & 1], (i >> 1) & 1, ab, kDevErrTimeout);
+                if (ok && i >= 1) ok = mbar_wait_warp(d_empty, (i - 1) & 1, ab, kDevErrTimeout);
                 if (!ok) break;
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::COL_D, tmem + C::COL_A + (i & 1) * 64, pw, ca);
