@@ -61,6 +61,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, device="cpu"):
+    """The largest per-rank value of `x` over the process group (the slowest rank's step
+    time); `x` itself outside a multi-rank run."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms_per_step):
+    """Units per second of the whole job: every rank processes `units_per_rank` per step
+    (heads are independent: weak scaling, no data-path collective), timed by the slowest."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -338,19 +356,16 @@ def run_gpu(args, rank, world, local):
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    ms_per_step = t_start.elapsed_time(t_end) / steps
+    ms_per_step = max_over_ranks(t_start.elapsed_time(t_end) / steps, device=dev)
     if world > 1:
         import torch.distributed as dist
-        tt = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_per_step = float(tt.item())
         dist.barrier()
     status = gma.gma_get_status()
     if status:
         raise RuntimeError("device status after timed region: " + gma.gma_status_string(status))
     dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom_events)
     units_per_step = len(dirs) * w.G * w.N
-    value = world * units_per_step / (ms_per_step / 1e3)
+    value = whole_job_rate(units_per_step, world, ms_per_step)
 
     # roofline of the dominant kernel
     pk = peaks()
@@ -431,8 +446,8 @@ def run_gpu(args, rank, world, local):
         s_down.wait_stream(s_up)
         b.record(s_down)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / args.e2e_steps
-        e2e = {"value": world * units_per_step / (e2e_ms / 1e3), "unit": "tokens·heads/s",
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.e2e_steps, device=dev)
+        e2e = {"value": whole_job_rate(units_per_step, world, e2e_ms), "unit": "tokens·heads/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     cpu = None
