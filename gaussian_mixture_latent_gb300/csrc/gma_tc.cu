@@ -500,16 +500,20 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 // Fixed-order sum over the CTAs that covered head g (blockIdx.y), then the bf16
 // B operand [n][k] of the read (n = value column, dv -> Z, dv+1 -> 1, rest 0)
-// in the K-major 128-byte-swizzled layout, ceil(K/64) chunks of 80 rows.
-__global__ void __launch_bounds__(256) tc_reduce_kernel(int K, int T, int Ttot, int ncta,
-                                                        const float *__restrict__ partials,
-                                                        uint8_t *__restrict__ mem, uint32_t mem_stride) {
+// in the K-major 128-byte-swizzled layout, ceil(K/64) chunks of 80 rows.  Each
+// thread owns four consecutive k of one row (a float4 of every partial), so a
+// head takes 20 K / 4 threads and the grid fits on the GPU in one wave while
+// the write kernel drains.
+constexpr int kReduceThreads = 256;
+
+__global__ void __launch_bounds__(kReduceThreads) tc_reduce_kernel(int K, int T, int Ttot, int ncta,
+                                                                   const float *__restrict__ partials,
+                                                                   uint8_t *__restrict__ mem, uint32_t mem_stride) {
     grid_dep_launch();
-    grid_dep_wait();                                       // the partial slots are written
     const int g = blockIdx.y;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int q = blockIdx.x * blockDim.x + threadIdx.x;   // float4 index in the 80 x K operand
     // CTA c owns tiles [c*Ttot/ncta, (c+1)*Ttot/ncta): those meeting [g*T, (g+1)*T) are
-    // c_lo..c_hi - 1, found once per block
+    // c_lo..c_hi - 1 (depends only on the launch shape: found before the wait)
     __shared__ int crange[2];
     if (threadIdx.x == 0) {
         const long long lo = (long long)g * T, hi = (long long)(g + 1) * T;
@@ -522,18 +526,35 @@ __global__ void __launch_bounds__(256) tc_reduce_kernel(int K, int T, int Ttot, 
         crange[1] = c_hi;
     }
     __syncthreads();
-    if (e >= 80 * K) return;
+    grid_dep_wait();                                       // the partial slots are written
+    const int kq = K / 4;
+    if (q >= 80 * kq) return;
     const int c_lo = crange[0], c_hi = crange[1];
-    const int nrow = e / K, k = e % K;
-    float v = 0.f;
+    const int nrow = q / kq, k = 4 * (q % kq);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (nrow <= DVV) {
-        for (int c = c_lo; c < c_hi; ++c)
-            v += partials[((size_t)(c + g) * (DVV + 1) + nrow) * K + k];
+        // slots c + g in increasing c; loads of four slots are in flight together
+        const size_t step = (size_t)(DVV + 1) * kq;
+        const float4 *src = reinterpret_cast<const float4 *>(partials) + ((size_t)(c_lo + g) * (DVV + 1) + nrow) * kq +
+                            (k >> 2);
+        int c = c_lo;
+        for (; c + 4 <= c_hi; c += 4, src += 4 * step) {
+            const float4 a0 = src[0], a1 = src[step], a2 = src[2 * step], a3 = src[3 * step];
+            v.x = (((v.x + a0.x) + a1.x) + a2.x) + a3.x;
+            v.y = (((v.y + a0.y) + a1.y) + a2.y) + a3.y;
+            v.z = (((v.z + a0.z) + a1.z) + a2.z) + a3.z;
+            v.w = (((v.w + a0.w) + a1.w) + a2.w) + a3.w;
+        }
+        for (; c < c_hi; ++c, src += step) {
+            const float4 a = *src;
+            v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+        }
     } else if (nrow == DVV + 1) {
-        v = 1.f;
+        v = make_float4(1.f, 1.f, 1.f, 1.f);
     }
     const uint32_t off = (uint32_t)(k >> 6) * 80u * 128u + sw128_off(nrow, (k & 63) >> 3) + (k & 7) * 2;
-    *reinterpret_cast<__nv_bfloat16 *>(mem + (size_t)g * mem_stride + off) = __float2bfloat16_rn(v);
+    *reinterpret_cast<uint2 *>(mem + (size_t)g * mem_stride + off) =
+        make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
 }
 
 // ------------------------------------------------------------------ tc_read
@@ -847,8 +868,8 @@ cudaError_t tc_write(const Problem &p, const TcLayout &L, const void *Kx, const 
 }
 
 cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s) {
-    dim3 grid((80 * p.K + 255) / 256, p.G);
-    return launch_dependent(tc_reduce_kernel, grid, dim3(256), 0, s, p.K, L.T, L.Ttot, L.ncta,
+    dim3 grid((20 * p.K + kReduceThreads - 1) / kReduceThreads, p.G);
+    return launch_dependent(tc_reduce_kernel, grid, dim3(kReduceThreads), 0, s, p.K, L.T, L.Ttot, L.ncta,
                             reinterpret_cast<const float *>(ws + L.part), reinterpret_cast<uint8_t *>(ws + L.mem),
                             L.mem_stride);
 }
