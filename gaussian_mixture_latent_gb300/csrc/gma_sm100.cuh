@@ -66,23 +66,30 @@ struct Abort {
 
 constexpr long long kWaitLimitCycles = 2000000000LL;   // about one second at 2 GHz
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const Abort &ab,
-                                          unsigned err_bit) {
-    const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
+// The spin loop is one out-of-line copy per kernel: a kernel has dozens of wait
+// sites, and inlining the loop at each of them grows the code that every warp
+// role cycles through (instruction-cache misses showed as no_instruction stalls).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, volatile int *flag,
+                                                   unsigned *status, unsigned err_bit) {
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait(a, parity)) return true;
-        if (*ab.flag) return false;
+        if (*flag) return false;
         if (clock64() - t0 > kWaitLimitCycles) {
-            *ab.flag = 1;
-            atomicOr(ab.status, err_bit);
+            *flag = 1;
+            atomicOr(status, err_bit);
             return false;
         }
     }
 }
 
-// The same wait by every lane of a converged warp, with one outcome for all lanes.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const Abort &ab,
+                                          unsigned err_bit) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    return mbar_wait_slow(a, parity, ab.flag, ab.status, err_bit);
+}
+
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const Abort &ab, unsigned err_bit) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, err_bit));
 }

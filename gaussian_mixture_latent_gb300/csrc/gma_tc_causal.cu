@@ -324,7 +324,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             auto convert_k = [&](int c) -> bool {
                 const bool w = mbar_wait(&kfull[c & 1], (c >> 1) & 1, ab, kDevErrTimeout);
                 if (!wg_all(rt, w)) return false;
-                convert_row(sm + C::OFF_K + (c & 1) * kTileBytes, rt.r, tmem + rt.lane_off + C::COL_AK);
+                convert_row_call(sm + C::OFF_K + (c & 1) * kTileBytes, rt.r, tmem + rt.lane_off + C::COL_AK);
                 tmem_st_wait();
                 tc_fence_before();
                 wg_sync(rt);
@@ -409,7 +409,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             auto convert_q = [&](int c) -> bool {
                 const bool w = mbar_wait(&qfull[c & 1], (c >> 1) & 1, ab, kDevErrTimeout);
                 if (!wg_all(rt, w)) return false;
-                convert_row(sm + C::OFF_Q + (c & 1) * kTileBytes, rt.r, tmem + rt.lane_off + C::COL_AQ);
+                convert_row_call(sm + C::OFF_Q + (c & 1) * kTileBytes, rt.r, tmem + rt.lane_off + C::COL_AQ);
                 tmem_st_wait();
                 tc_fence_before();
                 wg_sync(rt);
@@ -474,42 +474,42 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
             };
             bool ok = convert_q(0);
-            for (int c = 0; c < nch && ok; ++c) {
-                bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
-                if (!(ok = wg_all(rt, w))) break;
-                tc_fence_after();
-                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull); }
-                uint32_t e[K / 2];
-                if (SLICE) {
-                    // relative to the row's maximum over all components
-                    const int row = c * TM + (int)rt.r;
-                    row_exp_offset<K>(tmem + rt.lane_off + C::COL_D1Q, scale,
-                                      row < A.N ? __ldg(A.mrow_q + (size_t)g * A.N + row) : 0.f, e);
+            for (int c = 0; c <= nch && ok; ++c) {
+                if (c < nch) {
+                    bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
+                    if (!(ok = wg_all(rt, w))) break;
+                    tc_fence_after();
+                    if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull); }
+                    uint32_t e[K / 2];
+                    if (SLICE) {
+                        // relative to the row's maximum over all components
+                        const int row = c * TM + (int)rt.r;
+                        row_exp_offset<K>(tmem + rt.lane_off + C::COL_D1Q, scale,
+                                          row < A.N ? __ldg(A.mrow_q + (size_t)g * A.N + row) : 0.f, e);
+                    } else {
+                        row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1Q, scale, e);
+                    }
+                    // e^Q(c) replaces e^Q(c - 1) once the read of chunk c - 1 has consumed it
+                    if (c >= 1) {
+                        w = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
+                        if (!(ok = wg_all(rt, w))) break;
+                        tc_fence_after();
+                    }
+                    tmem_st32(tmem + rt.lane_off + C::COL_EQ, e);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    wg_sync(rt);
+                    if (elected) mbar_arrive(e_full);
                 } else {
-                    row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1Q, scale, e);
-                }
-                // e^Q(c) replaces e^Q(c - 1) once the read of chunk c - 1 has consumed it
-                if (c >= 1) {
-                    w = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
+                    // after the last chunk: wait for its read
+                    const bool w = mbar_wait(d3_full, (nch - 1) & 1, ab, kDevErrTimeout);
                     if (!(ok = wg_all(rt, w))) break;
                     tc_fence_after();
                 }
-                tmem_st32(tmem + rt.lane_off + C::COL_EQ, e);
-                tmem_st_wait();
-                tc_fence_before();
-                wg_sync(rt);
-                if (elected) mbar_arrive(e_full);
                 // read(c - 1) is complete (waited above): its epilogue, off the critical chain
                 if (c >= 1) epilogue(c - 1);
                 // the scores of chunk c have been read: the next query tile may overwrite them
                 if (c + 1 < nch && !(ok = convert_q(c + 1))) break;
-            }
-            if (ok) {
-                const bool w = mbar_wait(d3_full, (nch - 1) & 1, ab, kDevErrTimeout);
-                if (wg_all(rt, w)) {
-                    tc_fence_after();
-                    epilogue(nch - 1);
-                }
             }
             if (elected) bulk_wait_group<0>();
         } else {
@@ -545,24 +545,27 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             };
             bool ok = true;
             for (int c = 0; c < nch && ok; ++c) {
-                // keys 0..63 of T(c); the masked tile is free once the read of chunk c - 1 is done
-                bool w = mbar_wait(ta_full, c & 1, ab, kDevErrTimeout);
-                if (c >= 1) w = w && mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
-                if (!(ok = wg_all(rt, w))) break;
-                tc_fence_after();
-                mask_half(0, sm + C::OFF_TB);
-                tc_fence_before();
-                wg_sync(rt);
-                if (elected) mbar_arrive(ta_free);
-                // keys 64..127 of T(c)
-                w = mbar_wait(tb2_full, c & 1, ab, kDevErrTimeout);
-                if (!(ok = wg_all(rt, w))) break;
-                tc_fence_after();
-                mask_half(64, sm + C::OFF_TB + kTileBytes);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                wg_sync(rt);
-                if (elected) { mbar_arrive(t_empty); mbar_arrive(tb_full); }
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    // half hh (keys 64 hh .. 64 hh + 63) of T(c); the masked tile is free for chunk c
+                    // once the read of chunk c - 1 is done
+                    bool w = mbar_wait(hh == 0 ? ta_full : tb2_full, c & 1, ab, kDevErrTimeout);
+                    if (hh == 0 && c >= 1) w = w && mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
+                    if (!(ok = wg_all(rt, w))) break;
+                    tc_fence_after();
+                    mask_half(64 * hh, sm + C::OFF_TB + hh * kTileBytes);
+                    if (hh == 1) fence_proxy_async_smem();
+                    tc_fence_before();
+                    wg_sync(rt);
+                    if (elected) {
+                        if (hh == 0) {
+                            mbar_arrive(ta_free);
+                        } else {
+                            mbar_arrive(t_empty);
+                            mbar_arrive(tb_full);
+                        }
+                    }
+                }
             }
         }
     }

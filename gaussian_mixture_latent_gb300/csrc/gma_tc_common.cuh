@@ -123,6 +123,12 @@ __device__ __forceinline__ void convert_row(const uint8_t *xs, uint32_t r, uint3
     tmem_st32(tcol_a + 32, pq);
 }
 
+// One out-of-line copy of convert_row, for kernels that convert in more than
+// one warp role or at more than one site (keeps their code footprint small).
+static __device__ __noinline__ void convert_row_call(const uint8_t *xs, uint32_t r, uint32_t tcol_a) {
+    convert_row(xs, r, tcol_a);
+}
+
 // The constant A block of the log-density MMA: row r = [1, 1, 0 x 14] (fp16).
 __device__ __forceinline__ void init_const_a(uint8_t *blk, int tid, int nthreads) {
     for (int e = tid; e < (int)(kConstABytes / 16); e += nthreads) {
