@@ -318,6 +318,17 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         rt.wtid = threadIdx.x - kWGroups * 32 - rt.wg * kWgThreads;
         const bool elected = rt.wtid == 0;
         float scale = 0.f;                                 // read once the parameter blocks are written
+        // component-sliced form: this row's key log-sum-exp / query maximum in chunk c (rows past
+        // the sequence end: gamma^K = 0, e^Q finite); read after the grid-dependency wait
+        float stat_next = 0.f;
+        auto lse_row = [&](int c) -> float {
+            const int row = c * TM + (int)rt.r;
+            return row < A.N ? __ldg(A.lse_k + (size_t)g * A.N + row) : INFINITY;
+        };
+        auto max_row = [&](int c) -> float {
+            const int row = c * TM + (int)rt.r;
+            return row < A.N ? __ldg(A.mrow_q + (size_t)g * A.N + row) : 0.f;
+        };
 
         if (rt.wg == 0) {
             // ---------------- key group
@@ -337,15 +348,19 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (c >= 1) w = w && mbar_wait(g_empty, (c - 1) & 1, ab, kDevErrTimeout);
                 if (!(ok = wg_all(rt, w))) break;
                 tc_fence_after();
-                if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull); }
+                if (c == 0) {
+                    grid_dep_wait();
+                    scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull);
+                    if (SLICE) stat_next = lse_row(0);
+                }
                 // gamma^K = softmax of the key scores; rows past the sequence end get 0
                 uint32_t e[K / 2];
                 float inv;
                 if (SLICE) {
-                    // normalised over all components by the row's log-sum-exp
-                    const int row = c * TM + (int)rt.r;
-                    row_exp_offset<K>(tmem + rt.lane_off + C::COL_D1K, scale,
-                                      row < A.N ? __ldg(A.lse_k + (size_t)g * A.N + row) : INFINITY, e);
+                    // normalised over all components by the row's log-sum-exp (loaded a chunk ahead)
+                    const float off = stat_next;
+                    if (c + 1 < nch) stat_next = lse_row(c + 1);
+                    row_exp_offset<K>(tmem + rt.lane_off + C::COL_D1K, scale, off, e);
                     inv = 1.0f;
                 } else {
                     row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1K, scale, e);
@@ -479,13 +494,17 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
                     if (!(ok = wg_all(rt, w))) break;
                     tc_fence_after();
-                    if (c == 0) { grid_dep_wait(); scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull); }
+                    if (c == 0) {
+                        grid_dep_wait();
+                        scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull);
+                        if (SLICE) stat_next = max_row(0);
+                    }
                     uint32_t e[K / 2];
                     if (SLICE) {
-                        // relative to the row's maximum over all components
-                        const int row = c * TM + (int)rt.r;
-                        row_exp_offset<K>(tmem + rt.lane_off + C::COL_D1Q, scale,
-                                          row < A.N ? __ldg(A.mrow_q + (size_t)g * A.N + row) : 0.f, e);
+                        // relative to the row's maximum over all components (loaded a chunk ahead)
+                        const float off = stat_next;
+                        if (c + 1 < nch) stat_next = max_row(c + 1);
+                        row_exp_offset<K>(tmem + rt.lane_off + C::COL_D1Q, scale, off, e);
                     } else {
                         row_exp_scaled<K>(tmem + rt.lane_off + C::COL_D1Q, scale, e);
                     }
@@ -520,12 +539,20 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int q = warp & 3;
             auto mask_group = [&](const uint32_t *v, int key0, bool diag, uint8_t *half, int cc) {
                 uint32_t pk[16];
+                if (diag) {
+                    // the group straddles the diagonal: keep keys key0 + u with u <= r - key0
+                    const int rr = (int)rt.r - key0;
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const uint32_t j0 = (uint32_t)key0 + 2u * t;
-                    const float a = !diag || j0 <= rt.r ? __uint_as_float(v[2 * t]) : 0.f;
-                    const float b2 = !diag || j0 + 1 <= rt.r ? __uint_as_float(v[2 * t + 1]) : 0.f;
-                    pk[t] = pack_bf16(a, b2);
+                    for (int t = 0; t < 16; ++t) {
+                        const float a = 2 * t <= rr ? __uint_as_float(v[2 * t]) : 0.f;
+                        const float b2 = 2 * t + 1 <= rr ? __uint_as_float(v[2 * t + 1]) : 0.f;
+                        pk[t] = pack_bf16(a, b2);
+                    }
+                } else {
+                    // wholly below the diagonal (warp-uniform branch): convert only
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        pk[t] = pack_bf16(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
                 }
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
