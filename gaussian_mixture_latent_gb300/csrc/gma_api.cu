@@ -82,8 +82,8 @@ gma_status build_forward_plan(const Problem &p, const Args *a, Plan &plan) {
         plan.workspace = T.total;
         const Args A = a ? *a : z;
         char *ws = A.ws;
-        plan.add("tc_params", [=](cudaStream_t s) { return tc_params(p, T, A.mu, A.rho, A.alpha, ws, s); });
-        plan.add("tc_causal", [=](cudaStream_t s) { return tc_causal(p, T, A.Qx, A.Kx, A.V, A.out, ws, s); });
+        plan.add("tc_causal", [=](cudaStream_t s) {
+            return tc_causal(p, T, A.Qx, A.Kx, A.V, A.mu, A.rho, A.alpha, A.out, ws, s); });
         return GMA_OK;
     }
     if (tc_slice_supported(p)) {

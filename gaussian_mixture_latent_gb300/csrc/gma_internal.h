@@ -59,7 +59,7 @@ cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_
 cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,
                     cudaStream_t s);
 
-// ----- tensor-core causal path: gma_tc_causal.cu (uses tc_params for the coefficients) -----
+// ----- tensor-core causal path: gma_tc_causal.cu (one kernel; each CTA builds its head's coefficients) -----
 bool tc_causal_supported(const Problem &p);
 TcLayout tc_causal_layout(const Problem &p);
 // component-sliced causal path (gma_tc_slice.cu + gma_tc_causal.cu): larger K or dv
@@ -71,7 +71,7 @@ cudaError_t tc_causal_slices(const Problem &p, const TcLayout &L, const void *Qx
                              char *ws, cudaStream_t s);
 cudaError_t tc_combine(const Problem &p, const TcLayout &L, void *out, char *ws, cudaStream_t s);
 cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
-                      void *out, char *ws, cudaStream_t s);
+                      const float *mu, const float *rho, const float *alpha, void *out, char *ws, cudaStream_t s);
 
 // ----- SIMT (CUDA-core, fp32) path: gma_simt.cu -----
 cudaError_t simt_params(const Problem &p, const float *rho, const float *alpha, float *lam,

@@ -83,142 +83,19 @@ __device__ __forceinline__ void cta_range(int Ttot, int &t0, int &t1) {
 // ------------------------------------------------------------------ tc_params
 
 constexpr int kParamThreads = 512;
-constexpr int kParamV4 = 256 * DR / 4 / kParamThreads;   // float4 loads per thread and array at K <= 256
 
-__global__ void __launch_bounds__(kParamThreads) tc_params_kernel(int K, float var_floor,
-                                                                  const float *__restrict__ mu,
+template <int K>
+__global__ void __launch_bounds__(kParamThreads) tc_params_kernel(float var_floor, const float *__restrict__ mu,
                                                                   const float *__restrict__ rho,
                                                                   const float *__restrict__ alpha,
                                                                   uint8_t *__restrict__ out, uint32_t stride) {
-    extern __shared__ float sm[];
-    float *a = sm;                 // [K][DR]
-    float *b = a + K * DR;         // [K][DR]
-    float *red = b + K * DR;       // [64] scratch
-    float *colmean = red + 64;     // [DR]
-    float *cbuf = colmean + DR;    // [K] per-component constants
+    __shared__ __align__(16) float scratch[param_scratch_floats(K, kParamThreads)];
     grid_dep_launch();
-    const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    constexpr int NW = kParamThreads / 32;
-    const float4 *mu4 = reinterpret_cast<const float4 *>(mu + (size_t)h * K * DR);
-    const float4 *rho4 = reinterpret_cast<const float4 *>(rho + (size_t)h * K * DR);
-    const float *al = alpha + (size_t)h * K;
-    uint8_t *blk = out + (size_t)h * stride;
-
-    // every global load of the head is issued before the first use: one memory round trip
-    const int n4 = K * DR / 4;
-    float4 mv[kParamV4], rv[kParamV4];
-#pragma unroll
-    for (int u = 0; u < kParamV4; ++u) {
-        const int e4 = tid + u * kParamThreads;
-        if (e4 < n4) { mv[u] = __ldg(mu4 + e4); rv[u] = __ldg(rho4 + e4); }
-    }
-    const float alk = tid < K ? __ldg(al + tid) : -INFINITY;
-
-    // log-sum-exp of the prior logits (Eq. 15)
-    float m = alk;
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(~0u, m, o));
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    m = red[0];
-    for (int w = 1; w < NW; ++w) m = fmaxf(m, red[w]);
-    __syncthreads();
-    float s = tid < K ? expf(alk - m) : 0.f;
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(~0u, s, o);
-    if (lane == 0) red[warp] = s;
-    __syncthreads();
-    s = 0.f;
-    for (int w = 0; w < NW; ++w) s += red[w];
-    const float lse = m + logf(s);
-
-    // Eq. 14: variances; linear and quadratic coefficients in log2 units.  The 16
-    // float4s of component k sit in 16 consecutive threads, which also reduce
-    // sum_m log var_km and sum_m mu_km^2 lambda_km for the constant c_k (Eq. 16).
-#pragma unroll
-    for (int u = 0; u < kParamV4; ++u) {
-        const int e4 = tid + u * kParamThreads;
-        if (u * kParamThreads >= n4) break;                     // uniform across the block
-        const bool valid = e4 < n4;
-        const float mq[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
-        const float rq[4] = {rv[u].x, rv[u].y, rv[u].z, rv[u].w};
-        float logdet = 0.f, musq = 0.f;
-        if (valid) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                // SFU forms (relative error near 2^-21): the coefficients are rounded to
-                // fp16 (2^-12) and the constant to about 22 bits afterwards
-                const float w = rq[q];
-                const float var = fmaxf(w, 0.f) + __logf(1.0f + __expf(-fabsf(w))) + var_floor;
-                const float lam = __frcp_rn(var);
-                const float av = mq[q] * lam * kLog2e;
-                a[4 * e4 + q] = av;
-                b[4 * e4 + q] = -0.5f * lam * kLog2e;
-                logdet += __logf(var);
-                musq += mq[q] * av;
-            }
-        }
-        for (int o = 1; o < 16; o <<= 1) {
-            logdet += __shfl_xor_sync(~0u, logdet, o);
-            musq += __shfl_xor_sync(~0u, musq, o);
-        }
-        if (valid && (tid & 15) == 0) {
-            const int k = e4 >> 4;
-            cbuf[k] = (__ldg(al + k) - lse) * kLog2e - 0.5f * kLog2e * logdet - 0.5f * musq;
-        }
-    }
-    __syncthreads();
-    // mean over components of each quadratic coefficient column (8 threads per column)
-    {
-        const int col = tid >> 3, part = tid & 7;
-        float acc = 0.f;
-        if (col < DR)
-            for (int k = part; k < K; k += 8) acc += b[k * DR + col];
-        acc += __shfl_xor_sync(~0u, acc, 1);
-        acc += __shfl_xor_sync(~0u, acc, 2);
-        acc += __shfl_xor_sync(~0u, acc, 4);
-        if (col < DR && part == 0) colmean[col] = acc / (float)K;
-    }
-    __syncthreads();
-    // centre the quadratic coefficients over k, rescale for the x^2/256 operand, and find max |W|
-    float amax = 0.f, cmax = 0.f;
-    for (int e = tid; e < K * DR; e += kParamThreads) {
-        const float q = (b[e] - colmean[e % DR]) * 256.0f;
-        b[e] = q;
-        amax = fmaxf(amax, fmaxf(fabsf(a[e]), fabsf(q)));
-    }
-    for (int k = tid; k < K; k += kParamThreads) cmax = fmaxf(cmax, fabsf(cbuf[k]));
-    for (int o = 16; o; o >>= 1) {
-        amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
-        cmax = fmaxf(cmax, __shfl_xor_sync(~0u, cmax, o));
-    }
-    if (lane == 0) { red[warp] = amax; red[32 + warp] = cmax; }
-    __syncthreads();
-    amax = 0.f;
-    cmax = 0.f;
-    for (int w = 0; w < NW; ++w) { amax = fmaxf(amax, red[w]); cmax = fmaxf(cmax, red[32 + w]); }
-    // power-of-two scale: max |W| / scale <= 2^14 and max |c| / scale <= 2^15 (fp16 range)
-    int ex = 0;
-    if (amax > 0.f && isfinite(amax)) ex = (int)ceilf(log2f(amax)) - 14;
-    if (cmax > 0.f && isfinite(cmax)) ex = max(ex, (int)ceilf(log2f(cmax)) - 15);
-    const float inv = exp2f((float)-ex);
-    if (tid == 0) *reinterpret_cast<float *>(blk + param_scale_off(K)) = exp2f((float)ex);
-    // Wc: [c_hi, c_lo, 0 x 14] per component, c_hi + c_lo = c / scale to about 22 bits
-    for (int e = tid; e < K * 2; e += kParamThreads) {
-        const int k = e >> 1, half = e & 1;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (half == 0) {
-            const float cs = cbuf[k] * inv;
-            const float hi = __half2float(__float2half_rn(cs));
-            v.x = pack_f16(hi, cs - hi);
-        }
-        *reinterpret_cast<uint4 *>(blk + param_wc_off(K) + nosw16_off(k, 8 * half)) = v;
-    }
-    // fp16 W in the K-major 128-byte-swizzled layout: row k, 8-element chunk j/8, element j%8
-    for (int e = tid; e < K * DR / 2; e += kParamThreads) {
-        const int k = (2 * e) / DR, j = (2 * e) % DR;
-        const uint32_t off = sw128_off(k, j >> 3) + (j & 7) * 2;
-        *reinterpret_cast<uint32_t *>(blk + off) = pack_f16(a[2 * e] * inv, a[2 * e + 1] * inv);
-        *reinterpret_cast<uint32_t *>(blk + 128u * K + off) = pack_f16(b[2 * e] * inv, b[2 * e + 1] * inv);
-    }
+    const int h = blockIdx.x;
+    ParamLoads<K, kParamThreads> ld;
+    ld.issue(threadIdx.x, mu + (size_t)h * K * DR, rho + (size_t)h * K * DR, alpha + (size_t)h * K);
+    build_param_block<K, kParamThreads>(threadIdx.x, ld, var_floor, out + (size_t)h * stride, scratch,
+                                        [] { __syncthreads(); });
 }
 
 // ------------------------------------------------------------------ tc_write
@@ -854,11 +731,11 @@ TcLayout tc_layout(const Problem &p) {
 
 cudaError_t tc_params(const Problem &p, const TcLayout &L, const float *mu, const float *rho,
                       const float *alpha, char *ws, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (2 * (size_t)p.K * DR + 64 + DR + p.K);
-    cudaError_t e = cudaFuncSetAttribute(tc_params_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    tc_params_kernel<<<p.H, kParamThreads, smem, s>>>(p.K, p.var_floor, mu, rho, alpha,
-                                            reinterpret_cast<uint8_t *>(ws + L.params), L.param_stride);
+    auto kern = p.K <= 64 ? tc_params_kernel<64> : p.K <= 128 ? tc_params_kernel<128>
+              : p.K <= 192 ? tc_params_kernel<192> : tc_params_kernel<256>;
+    if (p.K != 64 && p.K != 128 && p.K != 192 && p.K != 256) return cudaErrorInvalidValue;
+    kern<<<p.H, kParamThreads, 0, s>>>(p.var_floor, mu, rho, alpha, reinterpret_cast<uint8_t *>(ws + L.params),
+                                          L.param_stride);
     return cudaGetLastError();
 }
 

@@ -20,7 +20,9 @@
 // reduction has a fixed order, so results are bitwise reproducible, and row i
 // never reads rows after i (the mask selects, it does not multiply).
 //
-// One CTA per head.  Warps: 0 TMA producer; 1 TMEM owner and issuer of the
+// One CTA per head, and the forward is this one kernel: the three compute groups
+// first build the head's parameter block (Eq. 14-16, the same code as tc_params)
+// in shared memory while the first tiles load.  Warps: 0 TMA producer; 1 TMEM owner and issuer of the
 // log-density MMAs (keys, then queries); 2 issuer of the chained MMAs (T, the
 // state update, the read); 3-6 key group (convert, softmax, state snapshot);
 // 7-10 query group (convert, exp, epilogue and store); 11-14 mask group.
@@ -63,6 +65,9 @@ struct CausalArgs {
     const float *lse_k;    // [G][N] log2 sum_k 2^score of each key row
     uint16_t *pnum;        // [ns][G][N][dvt] bf16 partial numerators
     float *pden;           // [ns][G][N] partial denominators
+    // one head per CTA: the CTA builds its head's parameter block from these
+    const float *mu, *rho, *alpha;   // [H][K][d], [H][K][d], [H][K]
+    float var_floor;
 };
 
 struct CausalCfg {
@@ -91,6 +96,14 @@ struct CausalCfg {
 static_assert(CausalCfg::OFF_SB % 1024 == 0 && CausalCfg::OFF_P % 1024 == 0 && CausalCfg::OFF_O % 1024 == 0,
               "operand blocks must be 1024-byte aligned");
 static_assert(CausalCfg::BYTES <= 232448, "causal kernel exceeds the shared-memory opt-in limit");
+static_assert(param_scratch_floats(KC, 3 * kWgThreads) * 4 <= (int)kTileBytes,
+              "the parameter build's scratch must fit the gamma buffer");
+
+// The parameter build as one out-of-line call, keeping it out of the compute groups' loop code.
+static __device__ __noinline__ void build_param_block_team(int tid, ParamLoads<KC, 3 * kWgThreads> ld, float var_floor,
+                                                           uint8_t *blk, float *scratch) {
+    build_param_block<KC, 3 * kWgThreads>(tid, ld, var_floor, blk, scratch, [] { group_sync(4, 3 * kWgThreads); });
+}
 
 // SLICE = false: one head per CTA, O written directly.  SLICE = true: one (head,
 // component slice, value slice) per CTA (grid G x Kfull/64 x dvt/64); the key
@@ -125,6 +138,14 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int g = blockIdx.x, nch = A.nch;
     const int ks = SLICE ? (int)blockIdx.y : 0, vs = SLICE ? (int)blockIdx.z : 0;   // component / value slice
     grid_dep_launch();
+    // direct form: the compute groups put the head's parameter loads in flight before the prologue
+    constexpr int kTeam = 3 * kWgThreads, kTeamBar = 4;
+    const int ttid = (int)threadIdx.x - kWGroups * 32;
+    ParamLoads<K, kTeam> pld;
+    if (!SLICE && ttid >= 0) {
+        const int h = g % A.H;
+        pld.issue(ttid, A.mu + (size_t)h * K * DR, A.rho + (size_t)h * K * DR, A.alpha + (size_t)h * K);
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -177,9 +198,9 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 mbar_arrive_expect_tx(&vfull[vi], kTileBytes);
                 tma_load_3d(sm + C::OFF_V + vi * kTileBytes, &tm_v, &vfull[vi], 64 * vs, vi * TM, g);
             }
-            grid_dep_wait();
-            const uint8_t *blk = A.params + (size_t)(g % A.H) * A.param_stride;
             if (SLICE) {
+                grid_dep_wait();
+                const uint8_t *blk = A.params + (size_t)(g % A.H) * A.param_stride;
                 // the slice's 64 rows of each part of a Kfull-component block, in the K = 64 layout
                 // (row groups of 8 keep their 1 KB swizzle atoms and no-swizzle core matrices)
                 constexpr uint32_t kRows = 64u * 128u, kWc = 64u * 32u;
@@ -188,9 +209,6 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 bulk_load(sm + C::OFF_P + kRows, blk + 128u * A.Kfull + (size_t)ks * kRows, kRows, w_full);
                 bulk_load(sm + C::OFF_P + param_wc_off(K), blk + param_wc_off(A.Kfull) + (size_t)ks * kWc, kWc, w_full);
                 bulk_load(sm + C::OFF_P + param_scale_off(K), blk + param_scale_off(A.Kfull), 16u, w_full);
-            } else {
-                mbar_arrive_expect_tx(w_full, param_bytes(K));
-                bulk_load(sm + C::OFF_P, blk, param_bytes(K), w_full);
             }
             long long last = clock64();
             while ((qi < nch || ki < nch || vi < nch) && !*abort_flag) {
@@ -226,7 +244,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             wind_down_ring(kfull, 2, ki, A.status);
             wind_down_ring(qfull, 2, qi, A.status);
             wind_down_ring(vfull, 2, vi, A.status);
-            wait_ignoring_abort(w_full, 0, A.status);
+            if (SLICE) wait_ignoring_abort(w_full, 0, A.status);
         }
     } else if (warp == kWIss1) {
         // log-density MMAs: scores = [x, x^2/256] . W^T, keys then queries of each chunk
@@ -329,6 +347,15 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int row = c * TM + (int)rt.r;
             return row < A.N ? __ldg(A.mrow_q + (size_t)g * A.N + row) : 0.f;
         };
+        if (!SLICE) {
+            // The three groups build the head's parameter block straight into the operand block
+            // the log-density MMAs read (scratch: the gamma buffer, which holds nothing yet).
+            build_param_block_team(ttid, pld, A.var_floor, sm + C::OFF_P, reinterpret_cast<float *>(sm + C::OFF_G));
+            fence_proxy_async_smem();
+            group_sync(kTeamBar, kTeam);
+            scale = *reinterpret_cast<const float *>(sm + C::OFF_P + param_scale_off(K));
+            if (ttid == 0) mbar_arrive(w_full);
+        }
 
         if (rt.wg == 0) {
             // ---------------- key group
@@ -348,10 +375,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (c >= 1) w = w && mbar_wait(g_empty, (c - 1) & 1, ab, kDevErrTimeout);
                 if (!(ok = wg_all(rt, w))) break;
                 tc_fence_after();
-                if (c == 0) {
+                if (SLICE && c == 0) {
                     grid_dep_wait();
                     scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull);
-                    if (SLICE) stat_next = lse_row(0);
+                    stat_next = lse_row(0);
                 }
                 // gamma^K = softmax of the key scores; rows past the sequence end get 0
                 uint32_t e[K / 2];
@@ -494,10 +521,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     bool w = mbar_wait(d1q_full, c & 1, ab, kDevErrTimeout);
                     if (!(ok = wg_all(rt, w))) break;
                     tc_fence_after();
-                    if (c == 0) {
+                    if (SLICE && c == 0) {
                         grid_dep_wait();
                         scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull);
-                        if (SLICE) stat_next = max_row(0);
+                        stat_next = max_row(0);
                     }
                     uint32_t e[K / 2];
                     if (SLICE) {
@@ -624,9 +651,8 @@ TcLayout tc_causal_layout(const Problem &p) {
     L.ncta = p.G;
     L.ns = L.nt = 1;
     L.param_stride = align1k(param_bytes(p.K));
-    L.params = align_up(kHeaderBytes);
-    L.part = L.mem = L.params + (size_t)p.H * L.param_stride;
-    L.total = align_up(L.part);
+    L.params = L.part = L.mem = align_up(kHeaderBytes);          // only the status header
+    L.total = L.params;
     return L;
 }
 
@@ -649,7 +675,8 @@ TcLayout tc_slice_layout(const Problem &p) {
 }
 
 static cudaError_t launch_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
-                                 void *out, char *ws, cudaStream_t s, bool slices) {
+                                 const float *mu, const float *rho, const float *alpha, void *out, char *ws,
+                                 cudaStream_t s, bool slices) {
     CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, Qx, p.G, p.N, DR) || !make_map(&tk, Kx, p.G, p.N, DR) || !make_map(&tv, V, p.G, p.N, p.dv) ||
         !make_map(&to, slices ? V : out, p.G, p.N, p.dv))
@@ -667,21 +694,30 @@ static cudaError_t launch_causal(const Problem &p, const TcLayout &L, const void
         a.lse_k = a.mrow_q + (size_t)p.G * p.N;
         a.pnum = reinterpret_cast<uint16_t *>(ws + L.pnum);
         a.pden = reinterpret_cast<float *>(ws + L.pden);
+    } else {
+        a.mu = mu; a.rho = rho; a.alpha = alpha;
+        a.var_floor = p.var_floor;
     }
     auto kern = slices ? tc_causal_kernel<true> : tc_causal_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CausalCfg::BYTES);
     if (e != cudaSuccess) return e;
+    if (!slices) {
+        // the first kernel of its forward: an ordinary launch, so that every input is final when
+        // its CTAs start
+        kern<<<dim3(p.G), dim3(kCThreads), CausalCfg::BYTES, s>>>(tq, tk, tv, to, a);
+        return cudaGetLastError();
+    }
     return launch_dependent(kern, dim3(p.G, L.ns, L.nt), dim3(kCThreads), CausalCfg::BYTES, s, tq, tk, tv, to, a);
 }
 
 cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
-                      void *out, char *ws, cudaStream_t s) {
-    return launch_causal(p, L, Qx, Kx, V, out, ws, s, false);
+                      const float *mu, const float *rho, const float *alpha, void *out, char *ws, cudaStream_t s) {
+    return launch_causal(p, L, Qx, Kx, V, mu, rho, alpha, out, ws, s, false);
 }
 
 cudaError_t tc_causal_slices(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
                              char *ws, cudaStream_t s) {
-    return launch_causal(p, L, Qx, Kx, V, nullptr, ws, s, true);
+    return launch_causal(p, L, Qx, Kx, V, nullptr, nullptr, nullptr, nullptr, ws, s, true);
 }
 
 }  // namespace gma

@@ -201,6 +201,176 @@ __device__ __forceinline__ void row_exp_offset(uint32_t taddr, float scale, floa
     }
 }
 
+// ------------------------------------------------------------------ parameter block
+//
+// The per-head parameter block of the log-density MMA ("Gaussian Mixture
+// Attention", section 3.6 Eq. 14-15 and section 4.1 Eq. 16): variances
+// var = softplus(rho) + var_floor, log priors log_softmax(alpha), and in log2
+// units the linear coefficients mu * lambda, the quadratic coefficients
+// -lambda / 2 centred over the components (a per-column shift common to every
+// component cancels in the softmax) and rescaled for the x^2 / 256 operand, and
+// the per-component constant c_k.  Everything is divided by one power-of-two
+// scale so that the fp16 operands keep their range.  Written to `blk`:
+//   [0, 128 K)          linear coefficients, fp16, K-major 128-byte swizzle
+//   [128 K, 256 K)      quadratic coefficients, same layout
+//   [256 K, 288 K)      [c_hi, c_lo, 0 x 14] per component (fp16, no swizzle)
+//   [288 K, 288 K + 4)  the scale (fp32)
+//
+// Built by a team of NT threads (a multiple of 32) with team index `tid`:
+// thread tid owns float4 e4 = tid + u NT (u < V4) of the head's [K][d] arrays,
+// i.e. component e4 / 16 and columns 4 (e4 % 16) .. + 3, and keeps its
+// coefficients in registers until it writes them.  The loads are issued first
+// (ParamLoads), so a kernel can put them in flight before its own prologue.
+// `sync` is a barrier over the team; `scratch` holds param_scratch_floats(K, NT)
+// floats.  Every reduction has a fixed order for a given NT.
+__host__ __device__ constexpr int param_scratch_floats(int K, int NT) { return 64 + (NT / 32) * DR + K; }
+
+template <int K, int NT>
+struct ParamLoads {
+    static constexpr int n4 = K * DR / 4;
+    static constexpr int V4 = (n4 + NT - 1) / NT;
+    float4 mv[V4], rv[V4];
+    float alk;
+    __device__ __forceinline__ void issue(int tid, const float *__restrict__ mu_h, const float *__restrict__ rho_h,
+                                          const float *__restrict__ al) {
+        const float4 *mu4 = reinterpret_cast<const float4 *>(mu_h);
+        const float4 *rho4 = reinterpret_cast<const float4 *>(rho_h);
+#pragma unroll
+        for (int u = 0; u < V4; ++u) {
+            const int e4 = tid + u * NT;
+            if (e4 < n4) { mv[u] = __ldg(mu4 + e4); rv[u] = __ldg(rho4 + e4); }
+        }
+        alk = tid < K ? __ldg(al + tid) : -INFINITY;
+    }
+};
+
+template <int K, int NT, class Sync>
+__device__ __forceinline__ void build_param_block(int tid, const ParamLoads<K, NT> &ld, float var_floor,
+                                                  uint8_t *blk, float *scratch, Sync sync) {
+    static_assert(NT % 32 == 0 && NT / 32 <= 32 && K <= NT && K % 2 == 0, "team size");
+    constexpr int NWT = NT / 32, n4 = ParamLoads<K, NT>::n4, V4 = ParamLoads<K, NT>::V4;
+    float *red = scratch;                 // [64]: two reductions of NWT warps each
+    float *colpart = red + 64;            // [NWT][DR]: per-warp column sums of the quadratic coefficients
+    float *cbuf = colpart + NWT * DR;     // [K]: per-component constants
+    const int warp = tid >> 5, lane = tid & 31, j = tid & 15;   // j: this thread's column group
+    if (tid < K) cbuf[tid] = ld.alk;                            // alpha_k, replaced by c_k below
+
+    // log-sum-exp of the prior logits (Eq. 15)
+    float m = ld.alk;
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(~0u, m, o));
+    if (lane == 0) red[warp] = m;
+    sync();
+    m = red[0];
+    for (int w = 1; w < NWT; ++w) m = fmaxf(m, red[w]);
+    float s = tid < K ? expf(ld.alk - m) : 0.f;
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(~0u, s, o);
+    sync();                                                     // every thread has read red[]
+    if (lane == 0) red[warp] = s;
+    sync();
+    s = 0.f;
+    for (int w = 0; w < NWT; ++w) s += red[w];
+    const float lse = m + logf(s);
+
+    // Eq. 14: variances; linear and quadratic coefficients in log2 units.  The 16
+    // threads sharing component k (aligned, consecutive) also reduce sum_m log var_km
+    // and sum_m mu_km^2 lambda_km for the constant c_k (Eq. 16).
+    float av[V4][4], bq[V4][4];
+    float colacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < V4; ++u) {
+        if (u * NT >= n4) break;                                // uniform across the team
+        const int e4 = tid + u * NT;
+        const bool valid = e4 < n4;
+        const float mq[4] = {ld.mv[u].x, ld.mv[u].y, ld.mv[u].z, ld.mv[u].w};
+        const float rq[4] = {ld.rv[u].x, ld.rv[u].y, ld.rv[u].z, ld.rv[u].w};
+        float logdet = 0.f, musq = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // SFU forms (relative error near 2^-21): the coefficients are rounded to
+            // fp16 (2^-12) and the constant to about 22 bits afterwards
+            const float w = rq[q];
+            const float var = fmaxf(w, 0.f) + __logf(1.0f + __expf(-fabsf(w))) + var_floor;
+            const float lam = __frcp_rn(var);
+            av[u][q] = valid ? mq[q] * lam * kLog2e : 0.f;
+            bq[u][q] = valid ? -0.5f * lam * kLog2e : 0.f;
+            logdet += valid ? __logf(var) : 0.f;
+            musq += valid ? mq[q] * av[u][q] : 0.f;
+            colacc[q] += bq[u][q];
+        }
+        for (int o = 1; o < 16; o <<= 1) {
+            logdet += __shfl_xor_sync(~0u, logdet, o);
+            musq += __shfl_xor_sync(~0u, musq, o);
+        }
+        if (valid && j == 0) {
+            const int k = e4 >> 4;
+            cbuf[k] = (cbuf[k] - lse) * kLog2e - 0.5f * kLog2e * logdet - 0.5f * musq;
+        }
+    }
+    // column sums over this warp's components: lanes l and l ^ 16 share the columns
+#pragma unroll
+    for (int q = 0; q < 4; ++q) colacc[q] += __shfl_xor_sync(~0u, colacc[q], 16);
+    if (lane < 16)
+        *reinterpret_cast<float4 *>(colpart + warp * DR + 4 * j) = make_float4(colacc[0], colacc[1], colacc[2], colacc[3]);
+    sync();
+    // column means (fixed warp order), centred and rescaled quadratic coefficients, max |W|
+    float cm[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int w = 0; w < NWT; ++w) {
+        const float4 p = *reinterpret_cast<const float4 *>(colpart + w * DR + 4 * j);
+        cm[0] += p.x; cm[1] += p.y; cm[2] += p.z; cm[3] += p.w;
+    }
+    float amax = 0.f, cmax = 0.f;
+#pragma unroll
+    for (int u = 0; u < V4; ++u) {
+        if (u * NT >= n4) break;
+        const bool valid = tid + u * NT < n4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            bq[u][q] = valid ? (bq[u][q] - cm[q] / (float)K) * 256.0f : 0.f;
+            amax = fmaxf(amax, fmaxf(fabsf(av[u][q]), fabsf(bq[u][q])));
+        }
+    }
+    for (int k = tid; k < K; k += NT) cmax = fmaxf(cmax, fabsf(cbuf[k]));
+    for (int o = 16; o; o >>= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, o));
+        cmax = fmaxf(cmax, __shfl_xor_sync(~0u, cmax, o));
+    }
+    if (lane == 0) { red[warp] = amax; red[32 + warp] = cmax; }
+    sync();
+    amax = 0.f;
+    cmax = 0.f;
+    for (int w = 0; w < NWT; ++w) { amax = fmaxf(amax, red[w]); cmax = fmaxf(cmax, red[32 + w]); }
+    // power-of-two scale: max |W| / scale <= 2^14 and max |c| / scale <= 2^15 (fp16 range)
+    int ex = 0;
+    if (amax > 0.f && isfinite(amax)) ex = (int)ceilf(log2f(amax)) - 14;
+    if (cmax > 0.f && isfinite(cmax)) ex = max(ex, (int)ceilf(log2f(cmax)) - 15);
+    const float inv = exp2f((float)-ex);
+    if (tid == 0) *reinterpret_cast<float *>(blk + param_scale_off(K)) = exp2f((float)ex);
+    // Wc: [c_hi, c_lo, 0 x 14] per component, c_hi + c_lo = c / scale to about 22 bits
+    for (int e = tid; e < K * 2; e += NT) {
+        const int k = e >> 1, half = e & 1;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (half == 0) {
+            const float cs = cbuf[k] * inv;
+            const float hi = __half2float(__float2half_rn(cs));
+            v.x = pack_f16(hi, cs - hi);
+        }
+        *reinterpret_cast<uint4 *>(blk + param_wc_off(K) + nosw16_off(k, 8 * half)) = v;
+    }
+    // fp16 W from registers, K-major 128-byte swizzle: row k, 8-element chunk, element
+#pragma unroll
+    for (int u = 0; u < V4; ++u) {
+        const int e4 = tid + u * NT;
+        if (u * NT >= n4) break;
+        if (e4 >= n4) continue;
+        const int k = e4 >> 4, m0 = 4 * j;
+        const uint32_t off = sw128_off(k, m0 >> 3) + (m0 & 7) * 2;
+        *reinterpret_cast<uint2 *>(blk + off) =
+            make_uint2(pack_f16(av[u][0] * inv, av[u][1] * inv), pack_f16(av[u][2] * inv, av[u][3] * inv));
+        *reinterpret_cast<uint2 *>(blk + 128u * K + off) =
+            make_uint2(pack_f16(bq[u][0] * inv, bq[u][1] * inv), pack_f16(bq[u][2] * inv, bq[u][3] * inv));
+    }
+}
+
 // Per-head scale of the coefficient matrix, read from the parameter block in global memory.
 __device__ __forceinline__ float head_scale(const uint8_t *params, uint32_t stride, int h, int K) {
     return __ldg(reinterpret_cast<const float *>(params + (size_t)h * stride + param_scale_off(K)));
