@@ -244,28 +244,61 @@ tc_rowstats_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
 // ------------------------------------------------------------------ tc_combine
 
-// O[g][i][:] = sum_s num[s][g][i][:] / sum_s den[s][g][i], one warp per row,
-// four value columns per lane, a fixed order over slices.
-__global__ void __launch_bounds__(256) tc_combine_kernel(int ns, int G, int N, int dv,
-                                                         const uint16_t *__restrict__ pnum,
-                                                         const float *__restrict__ pden, uint16_t *__restrict__ out) {
+// O[g][i][:] = sum_s num[s][g][i][:] / sum_s den[s][g][i], a fixed order over slices.
+// A thread owns 16-byte pieces (eight value columns of one row); it issues the
+// loads of all NS slices of two pieces before it uses any of them.
+constexpr int kCombineThreads = 256;
+
+template <int NS>
+__device__ __forceinline__ void combine_piece(size_t rows, int dv, size_t piece, const uint16_t *__restrict__ pnum,
+                                              const float *__restrict__ pden, uint16_t *__restrict__ out,
+                                              const uint4 (&v)[NS], const float (&d)[NS]) {
+    const int per_row = dv / 8;
+    const size_t row = piece / per_row;
+    const int c0 = 8 * (int)(piece % per_row);
+    float den = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        den += d[s];
+        const uint32_t w[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) { acc[2 * u] += bf16_lo(w[u]); acc[2 * u + 1] += bf16_hi(w[u]); }
+    }
+    const float rd = 1.0f / den;
+    *reinterpret_cast<uint4 *>(out + row * dv + c0) =
+        make_uint4(pack_bf16(acc[0] * rd, acc[1] * rd), pack_bf16(acc[2] * rd, acc[3] * rd),
+                   pack_bf16(acc[4] * rd, acc[5] * rd), pack_bf16(acc[6] * rd, acc[7] * rd));
+}
+
+template <int NS>
+__global__ void __launch_bounds__(kCombineThreads) tc_combine_kernel(int G, int N, int dv,
+                                                                     const uint16_t *__restrict__ pnum,
+                                                                     const float *__restrict__ pden,
+                                                                     uint16_t *__restrict__ out) {
     grid_dep_launch();
     grid_dep_wait();                                       // the partial numerators and denominators are written
-    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= (size_t)G * N) return;
-    float den = 0.f;
-    for (int s = 0; s < ns; ++s) den += __ldg(pden + (size_t)s * G * N + row);
-    const float rd = 1.0f / den;
-    for (int c0 = 4 * lane; c0 < dv; c0 += 128) {
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(pnum + ((size_t)s * G * N + row) * dv + c0));
-            a0 += bf16_lo(v.x); a1 += bf16_hi(v.x); a2 += bf16_lo(v.y); a3 += bf16_hi(v.y);
+    const size_t rows = (size_t)G * N, pieces = rows * (dv / 8);
+    const size_t half = (pieces + 1) / 2;                  // a thread takes pieces p and p + half
+    const size_t p0 = (size_t)blockIdx.x * kCombineThreads + threadIdx.x;
+    if (p0 >= half) return;
+    const size_t p1 = p0 + half;
+    const bool two = p1 < pieces;
+    const int per_row = dv / 8;
+    uint4 v0[NS], v1[NS];
+    float d0[NS], d1[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        const size_t r0 = p0 / per_row, r1 = p1 / per_row;
+        v0[s] = __ldg(reinterpret_cast<const uint4 *>(pnum + ((size_t)s * rows + r0) * dv + 8 * (p0 % per_row)));
+        d0[s] = __ldg(pden + (size_t)s * rows + r0);
+        if (two) {
+            v1[s] = __ldg(reinterpret_cast<const uint4 *>(pnum + ((size_t)s * rows + r1) * dv + 8 * (p1 % per_row)));
+            d1[s] = __ldg(pden + (size_t)s * rows + r1);
         }
-        *reinterpret_cast<uint2 *>(out + row * dv + c0) =
-            make_uint2(pack_bf16(a0 * rd, a1 * rd), pack_bf16(a2 * rd, a3 * rd));
     }
+    combine_piece<NS>(rows, dv, p0, pnum, pden, out, v0, d0);
+    if (two) combine_piece<NS>(rows, dv, p1, pnum, pden, out, v1, d1);
 }
 
 template <int K>
@@ -301,10 +334,18 @@ cudaError_t tc_rowstats(const Problem &p, const TcLayout &L, const void *Qx, con
 }
 
 cudaError_t tc_combine(const Problem &p, const TcLayout &L, void *out, char *ws, cudaStream_t s) {
-    const size_t rows = (size_t)p.G * p.N;
-    return launch_dependent(tc_combine_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, L.ns, p.G, p.N,
-                            p.dv, reinterpret_cast<const uint16_t *>(ws + L.pnum),
-                            reinterpret_cast<const float *>(ws + L.pden), static_cast<uint16_t *>(out));
+    const size_t pieces = (size_t)p.G * p.N * (p.dv / 8), half = (pieces + 1) / 2;
+    const dim3 grid((unsigned)((half + kCombineThreads - 1) / kCombineThreads));
+    const auto *pn = reinterpret_cast<const uint16_t *>(ws + L.pnum);
+    const auto *pd = reinterpret_cast<const float *>(ws + L.pden);
+    auto *o = static_cast<uint16_t *>(out);
+    switch (L.ns) {
+        case 1: return launch_dependent(tc_combine_kernel<1>, grid, dim3(kCombineThreads), 0, s, p.G, p.N, p.dv, pn, pd, o);
+        case 2: return launch_dependent(tc_combine_kernel<2>, grid, dim3(kCombineThreads), 0, s, p.G, p.N, p.dv, pn, pd, o);
+        case 3: return launch_dependent(tc_combine_kernel<3>, grid, dim3(kCombineThreads), 0, s, p.G, p.N, p.dv, pn, pd, o);
+        case 4: return launch_dependent(tc_combine_kernel<4>, grid, dim3(kCombineThreads), 0, s, p.G, p.N, p.dv, pn, pd, o);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace gma
