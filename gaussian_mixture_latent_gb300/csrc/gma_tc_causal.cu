@@ -126,10 +126,12 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint64_t *w_full = vempty + 2, *ak_full = w_full + 1, *d1k_full = ak_full + 1, *aq_full = d1k_full + 1;
     uint64_t *d1q_full = aq_full + 1, *g_full = d1q_full + 1, *g_empty = g_full + 1, *e_full = g_empty + 1;
     // T buffer: ta_full (first half computed), ta_free (first half read), tb2_full (second half
-    // computed), t_empty (second half read); tb_full: the masked bf16 tile is complete
-    uint64_t *ta_full = e_full + 1, *ta_free = ta_full + 1, *tb2_full = ta_free + 1, *t_empty = tb2_full + 1;
-    uint64_t *tb_full = t_empty + 1, *d3_full = tb_full + 1, *d3_empty = d3_full + 1;
-    uint64_t *s_upd = d3_empty + 1, *s_ready = s_upd + 1, *sb_empty = s_ready + 2;
+    // computed); tb_full: the masked bf16 tile is complete (T read).  The read of chunk c
+    // commits tb0_free once it has consumed the first half of the masked tile and eq_free once
+    // it has consumed e^Q(c).
+    uint64_t *ta_full = e_full + 1, *ta_free = ta_full + 1, *tb2_full = ta_free + 1, *tb0_free = tb2_full + 1;
+    uint64_t *tb_full = tb0_free + 1, *d3_full = tb_full + 1, *d3_empty = d3_full + 1, *eq_free = d3_empty + 1;
+    uint64_t *s_upd = eq_free + 1, *s_ready = s_upd + 1, *sb_empty = s_ready + 2;
     uint64_t *fin1 = sb_empty + 2, *fin2 = fin1 + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -275,18 +277,30 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint64_t gm = sdesc_sw128(gaddr, kTileBytes, 1024);        // gamma^K as MN-major B (N = k)
             const uint64_t tbd = sdesc_sw128(smem_u32(sm + C::OFF_TB), 16, 1024);
             const uint32_t eq = tmem + C::COL_EQ;
-            bool ok = true;
-            for (int c = 0; c < nch && ok; ++c) {
-                const int s = c & 1;
-                // T(c), keys 0..63 = e^Q(c) . gamma^K(c)[0:64]^T
-                ok = mbar_wait_warp(e_full, c & 1, ab, kDevErrTimeout) && mbar_wait_warp(g_full, c & 1, ab, kDevErrTimeout);
-                if (ok && c >= 1) ok = mbar_wait_warp(t_empty, (c - 1) & 1, ab, kDevErrTimeout);
-                if (!ok) break;
+            // T(c), keys 0..63 = e^Q(c) . gamma^K(c)[0:64]^T, once e^Q(c) and gamma^K(c) are in place
+            // (the T buffer is free: its previous chunk's second half has been masked)
+            auto t_first_half = [&](int c) -> bool {
+                if (!(mbar_wait_warp(e_full, c & 1, ab, kDevErrTimeout) &&
+                      mbar_wait_warp(g_full, c & 1, ab, kDevErrTimeout)))
+                    return false;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
                     mma_ts(tmem + C::COL_T, eq + ks * 8, gk + (uint64_t)((ks * 32u) >> 4), idesc_t, ks > 0);
                 mma_commit(ta_full);
+                return true;
+            };
+            bool ok = t_first_half(0);
+            for (int c = 0; c < nch && ok; ++c) {
+                const int s = c & 1;
+                // T(c), keys 64..127, once the first half has been read
+                if (!(ok = mbar_wait_warp(ta_free, c & 1, ab, kDevErrTimeout))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks)
+                    mma_ts(tmem + C::COL_T, eq + ks * 8, gk + (uint64_t)((64u * 128u + ks * 32u) >> 4), idesc_t,
+                           ks > 0);
+                mma_commit(tb2_full);
                 // state update: [S | z]^T += [V | 1 | 0]^T . gamma^K, once the previous state is snapshotted
                 if (!(ok = mbar_wait_warp(&vfull[s], (c >> 1) & 1, ab, kDevErrTimeout) &&
                            mbar_wait_warp(&s_ready[c & 1], (c >> 1) & 1, ab, kDevErrTimeout)))
@@ -299,27 +313,28 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mma_ss(tmem + C::COL_S, vd + (uint64_t)(ks * 128), gm + (uint64_t)(ks * 128), idesc_u,
                            !(c == 0 && ks == 0));
                 mma_commit(s_upd);
-                // T(c), keys 64..127, once the first half has been read
-                if (!(ok = mbar_wait_warp(ta_free, c & 1, ab, kDevErrTimeout))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < K / 16; ++ks)
-                    mma_ts(tmem + C::COL_T, eq + ks * 8, gk + (uint64_t)((64u * 128u + ks * 32u) >> 4), idesc_t,
-                           ks > 0);
-                mma_commit(tb2_full);
                 mma_commit(g_empty);
-                // read: e^Q . [S | z | 1]_{c-1} + mask(T) . [V | 1]
+                // read(c) = mask(T) . [V | 1] + e^Q(c) . [S | z | 1]_{c-1}, in the order that frees
+                // what chunk c + 1 needs first: the first half of the masked tile, then e^Q; T(c + 1)'s
+                // first half enters the tensor pipe before the rest of the read.
                 ok = mbar_wait_warp(tb_full, c & 1, ab, kDevErrTimeout);
                 if (ok && c >= 1) ok = mbar_wait_warp(d3_empty, (c - 1) & 1, ab, kDevErrTimeout);
                 if (!ok) break;
                 tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_ss(tmem + C::COL_D3, tbd + (uint64_t)((ks * 32u) >> 4), vd + (uint64_t)(ks * 128), idesc_r2,
+                           ks > 0);
+                mma_commit(tb0_free);
                 const uint64_t sbd = sdesc_sw128(smem_u32(sm + C::OFF_SB + (c & 1) * C::SBB), 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks)
-                    mma_ts(tmem + C::COL_D3, eq + ks * 8, sbd + (uint64_t)((ks * 32u) >> 4), idesc_r1, ks > 0);
+                    mma_ts(tmem + C::COL_D3, eq + ks * 8, sbd + (uint64_t)((ks * 32u) >> 4), idesc_r1, 1);
+                mma_commit(eq_free);
+                if (c + 1 < nch && !(ok = t_first_half(c + 1))) break;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tmem + C::COL_D3, tbd + (uint64_t)(((ks >> 2) * kTileBytes + (ks & 3) * 32u) >> 4),
+                for (int ks = 4; ks < 8; ++ks)
+                    mma_ss(tmem + C::COL_D3, tbd + (uint64_t)((kTileBytes + (ks & 3) * 32u) >> 4),
                            vd + (uint64_t)(ks * 128), idesc_r2, 1);
                 mma_commit(d3_full);
                 mma_commit(&sb_empty[c & 1]);
@@ -417,34 +432,37 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_before();
                 wg_sync(rt);
                 if (elected) mbar_arrive(g_full);
+                // bf16 snapshot of the state after chunk c - 1, the read operand of chunk c (its
+                // update went into the tensor pipe a chunk ago; the update of chunk c waits for it)
+                if (c >= 1) {
+                    const int b = c & 1;
+                    w = mbar_wait(s_upd, (c - 1) & 1, ab, kDevErrTimeout);
+                    if (c >= 2) w = w && mbar_wait(&sb_empty[b], ((c >> 1) - 1) & 1, ab, kDevErrTimeout);
+                    if (!(ok = wg_all(rt, w))) break;
+                    tc_fence_after();
+                    uint32_t v[K];
+                    tmem_ld32(tmem + rt.lane_off + C::COL_S, v);
+                    tmem_ld32(tmem + rt.lane_off + C::COL_S + 32, v + 32);
+                    tmem_ld_wait();
+                    if (rt.r <= DVV) {
+                        uint8_t *row = sm + C::OFF_SB + b * C::SBB;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            uint4 o;
+                            o.x = pack_bf16(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                            o.y = pack_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                            o.z = pack_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                            o.w = pack_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                            *reinterpret_cast<uint4 *>(row + sw128_off(rt.r, j)) = o;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    wg_sync(rt);
+                    if (elected) mbar_arrive(&s_ready[b]);
+                }
                 if (c + 1 >= nch) break;
                 if (!(ok = convert_k(c + 1))) break;
-                // bf16 snapshot of the state after chunk c, the read operand of chunk c + 1
-                const int b = (c + 1) & 1;
-                w = mbar_wait(s_upd, c & 1, ab, kDevErrTimeout);
-                if (c + 1 >= 2) w = w && mbar_wait(&sb_empty[b], (((c + 1) >> 1) - 1) & 1, ab, kDevErrTimeout);
-                if (!(ok = wg_all(rt, w))) break;
-                tc_fence_after();
-                uint32_t v[K];
-                tmem_ld32(tmem + rt.lane_off + C::COL_S, v);
-                tmem_ld32(tmem + rt.lane_off + C::COL_S + 32, v + 32);
-                tmem_ld_wait();
-                if (rt.r <= DVV) {
-                    uint8_t *row = sm + C::OFF_SB + b * C::SBB;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint4 o;
-                        o.x = pack_bf16(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-                        o.y = pack_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-                        o.z = pack_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-                        o.w = pack_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-                        *reinterpret_cast<uint4 *>(row + sw128_off(rt.r, j)) = o;
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                wg_sync(rt);
-                if (elected) mbar_arrive(&s_ready[b]);
             }
         } else if (rt.wg == 1) {
             // ---------------- query group
@@ -537,7 +555,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     // e^Q(c) replaces e^Q(c - 1) once the read of chunk c - 1 has consumed it
                     if (c >= 1) {
-                        w = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
+                        w = mbar_wait(eq_free, (c - 1) & 1, ab, kDevErrTimeout);
                         if (!(ok = wg_all(rt, w))) break;
                         tc_fence_after();
                     }
@@ -546,16 +564,16 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc_fence_before();
                     wg_sync(rt);
                     if (elected) mbar_arrive(e_full);
-                } else {
-                    // after the last chunk: wait for its read
-                    const bool w = mbar_wait(d3_full, (nch - 1) & 1, ab, kDevErrTimeout);
+                    // the scores of chunk c have been read: the next query tile may overwrite them
+                    if (c + 1 < nch && !(ok = convert_q(c + 1))) break;
+                }
+                // read(c - 1): its epilogue, off the chunk-to-chunk chain
+                if (c >= 1) {
+                    const bool w = mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
                     if (!(ok = wg_all(rt, w))) break;
                     tc_fence_after();
+                    epilogue(c - 1);
                 }
-                // read(c - 1) is complete (waited above): its epilogue, off the critical chain
-                if (c >= 1) epilogue(c - 1);
-                // the scores of chunk c have been read: the next query tile may overwrite them
-                if (c + 1 < nch && !(ok = convert_q(c + 1))) break;
             }
             if (elected) bulk_wait_group<0>();
         } else {
@@ -601,10 +619,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int c = 0; c < nch && ok; ++c) {
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
-                    // half hh (keys 64 hh .. 64 hh + 63) of T(c); the masked tile is free for chunk c
-                    // once the read of chunk c - 1 is done
+                    // half hh (keys 64 hh .. 64 hh + 63) of T(c); that half of the masked tile is free
+                    // once the read of chunk c - 1 has passed it (its first four k-steps / all of it)
                     bool w = mbar_wait(hh == 0 ? ta_full : tb2_full, c & 1, ab, kDevErrTimeout);
-                    if (hh == 0 && c >= 1) w = w && mbar_wait(d3_full, (c - 1) & 1, ab, kDevErrTimeout);
+                    if (c >= 1) w = w && mbar_wait(hh == 0 ? tb0_free : d3_full, (c - 1) & 1, ab, kDevErrTimeout);
                     if (!(ok = wg_all(rt, w))) break;
                     tc_fence_after();
                     mask_half(64 * hh, sm + C::OFF_TB + hh * kTileBytes);
@@ -612,12 +630,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc_fence_before();
                     wg_sync(rt);
                     if (elected) {
-                        if (hh == 0) {
-                            mbar_arrive(ta_free);
-                        } else {
-                            mbar_arrive(t_empty);
-                            mbar_arrive(tb_full);
-                        }
+                        mbar_arrive(hh == 0 ? ta_free : tb_full);
                     }
                 }
             }
