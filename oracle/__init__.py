@@ -51,8 +51,10 @@ def _load():
                                                 i, _dp, _dp, _dp]
         lib.gma_oracle_forward.argtypes = [i, i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d, d,
                                            i, _dp, i]
+        lib.gma_oracle_diagnostics.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, d, _dp, _dp,
+                                               ctypes.POINTER(ctypes.c_int)]
         for fn in (lib.gma_oracle_scores, lib.gma_oracle_responsibilities,
-                   lib.gma_oracle_forward_head, lib.gma_oracle_forward):
+                   lib.gma_oracle_forward_head, lib.gma_oracle_forward, lib.gma_oracle_diagnostics):
             fn.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -124,3 +126,19 @@ def forward(Qx, Kx, V, mu, omega, alpha, var_floor: float, eps: float, causal: b
                                       _p(alpha), float(var_floor), float(eps), int(causal),
                                       _p(out), int(threads)), "forward")
     return out
+
+
+def diagnostics(Qx, mu, omega, alpha, var_floor: float):
+    """Responsibility diagnostics (section 5.4, Eqs. 24-29) over the query
+    responsibilities of every head: Qx [B, H, N, d], parameters [H, K, d] / [H, K]
+    -> (p [K], H_usage, H_token, R_max, z [B, N] int32)."""
+    Qx, mu, omega, alpha = map(_c, (Qx, mu, omega, alpha))
+    B, H, N, d = Qx.shape
+    K = mu.shape[1]
+    p = np.empty((K,), dtype=np.float64)
+    stats = np.empty((3,), dtype=np.float64)
+    z = np.empty((B, N), dtype=np.int32)
+    _check(_load().gma_oracle_diagnostics(B, H, N, d, K, _p(Qx), _p(mu), _p(omega), _p(alpha),
+                                          float(var_floor), _p(p), _p(stats),
+                                          z.ctypes.data_as(ctypes.POINTER(ctypes.c_int))), "diagnostics")
+    return p, float(stats[0]), float(stats[1]), float(stats[2]), z

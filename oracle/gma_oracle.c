@@ -250,3 +250,70 @@ int gma_oracle_forward(int B, int H, int N, int d, int K, int dv, const double *
     free(tid);
     return rc;
 }
+
+/*
+ * Responsibility diagnostics ("Gaussian Mixture Attention", section 5.4,
+ * Eqs. 24-29), on the query responsibilities of every head:
+ *
+ *   Eq. (24)  gbar_{t,k} = (1/H) sum_h gamma^Q_{t,h,k}    (t = (b, position): one token)
+ *   Eq. (25)  p_k        = (1/T) sum_t gbar_{t,k}          (T = B N tokens)
+ *   Eq. (26)  H_usage    = -sum_k p_k log p_k / log K
+ *   Eq. (27)  H_token    = (1/T) sum_t [ -sum_k gbar_{t,k} log gbar_{t,k} ] / log K
+ *   Eq. (28)  R_max      = (1/T) sum_t max_k gbar_{t,k}
+ *   Eq. (29)  z_t        = argmax_k gbar_{t,k}
+ *
+ * Readings: 0 log 0 = 0 (the limit); an argmax tie goes to the lowest index;
+ * K >= 2 (the normalisation by log K).  Qx [B, H, N, d] (head g = b H + h uses
+ * parameter set h).  Outputs: p [K], stats = {H_usage, H_token, R_max}, z [B N]
+ * (may be NULL).
+ */
+int gma_oracle_diagnostics(int B, int H, int N, int d, int K, const double *Qx, const double *mu,
+                           const double *omega, const double *alpha, double var_floor, double *p,
+                           double *stats, int *z)
+{
+    if (B <= 0 || H <= 0 || N < 0 || K < 2) return 1;
+    double *gam = (double *)malloc(sizeof(double) * (size_t)H * N * K);     /* one batch entry, all heads */
+    double *gbar = (double *)malloc(sizeof(double) * (size_t)K);
+    if (!gam || !gbar) { free(gam); free(gbar); return 2; }
+    for (int k = 0; k < K; ++k) p[k] = 0.0;
+    double htok = 0.0, rmax = 0.0;
+    const double T = (double)B * (double)N;
+    int rc = 0;
+    for (int b = 0; b < B && !rc; ++b) {
+        for (int h = 0; h < H && !rc; ++h)
+            rc = gma_oracle_responsibilities(N, d, K, Qx + ((size_t)b * H + h) * N * d,
+                                             mu + (size_t)h * K * d, omega + (size_t)h * K * d,
+                                             alpha + (size_t)h * K, var_floor, gam + (size_t)h * N * K);
+        for (int i = 0; i < N && !rc; ++i) {
+            /* Eq. (24) */
+            for (int k = 0; k < K; ++k) {
+                double s = 0.0;
+                for (int h = 0; h < H; ++h) s += gam[((size_t)h * N + i) * K + k];
+                gbar[k] = s / H;
+            }
+            double ent = 0.0, mx = gbar[0];
+            int arg = 0;
+            for (int k = 0; k < K; ++k) {
+                p[k] += gbar[k];                                            /* Eq. (25), summed */
+                if (gbar[k] > 0.0) ent -= gbar[k] * log(gbar[k]);           /* Eq. (27) term */
+                if (gbar[k] > mx) { mx = gbar[k]; arg = k; }                /* Eq. (28), (29) */
+            }
+            htok += ent;
+            rmax += mx;
+            if (z) z[(size_t)b * N + i] = arg;
+        }
+    }
+    if (!rc) {
+        double husage = 0.0;
+        for (int k = 0; k < K; ++k) {
+            p[k] /= T;
+            if (p[k] > 0.0) husage -= p[k] * log(p[k]);                     /* Eq. (26) */
+        }
+        stats[0] = husage / log((double)K);
+        stats[1] = htok / T / log((double)K);
+        stats[2] = rmax / T;
+    }
+    free(gam);
+    free(gbar);
+    return rc;
+}

@@ -280,3 +280,91 @@ def test_multi_head_driver_matches_per_head():
                 oh = oracle.forward_head(Qx[b, h], Kx[b, h], V[b, h], mu[h], om[h], al[h],
                                          1e-4, 1e-6, causal)
                 assert np.array_equal(o[b, h], oh)
+
+
+# ---------------------------------------------------------------- diagnostics (section 5.4)
+
+def make_heads(B=2, H=3, N=30, d=5, K=6, seed=7, mu_std=1.0):
+    r = np.random.default_rng(seed)
+    return dict(Qx=r.normal(size=(B, H, N, d)), mu=mu_std * r.normal(size=(H, K, d)),
+                omega=0.5 * r.normal(size=(H, K, d)), alpha=r.normal(size=(H, K)))
+
+
+def test_diagnostics_match_textbook_head_average():
+    # Eq. (24)-(29) from scipy's densities and scipy's entropy routine
+    x = make_heads()
+    B, H, N, _ = x["Qx"].shape
+    K = x["mu"].shape[1]
+    gbar = np.zeros((B, N, K))
+    for b in range(B):
+        for h in range(H):
+            gbar[b] += textbook_gamma(x["Qx"][b, h], x["mu"][h], x["omega"][h], x["alpha"][h], 1e-4) / H
+    flat = gbar.reshape(B * N, K)
+    p_ref = flat.mean(axis=0)
+    p, husage, htoken, rmax, z = oracle.diagnostics(x["Qx"], x["mu"], x["omega"], x["alpha"], 1e-4)
+    np.testing.assert_allclose(p, p_ref, rtol=1e-10, atol=1e-13)
+    assert husage == pytest.approx(stats.entropy(p_ref) / np.log(K), rel=1e-10)
+    assert htoken == pytest.approx(np.mean([stats.entropy(row) for row in flat]) / np.log(K), rel=1e-10)
+    assert rmax == pytest.approx(flat.max(axis=1).mean(), rel=1e-12)
+    assert np.array_equal(z.reshape(-1), flat.argmax(axis=1))
+
+
+def test_diagnostics_identical_components_are_uniform():
+    # identical components and priors: gamma = 1/K everywhere -> p = 1/K, both entropies 1,
+    # R_max = 1/K, every argmax tie resolved to component 0
+    x = make_heads(K=5)
+    x["mu"][:] = x["mu"][:, :1]
+    x["omega"][:] = x["omega"][:, :1]
+    x["alpha"][:] = 0.3
+    p, husage, htoken, rmax, z = oracle.diagnostics(x["Qx"], x["mu"], x["omega"], x["alpha"], 1e-4)
+    np.testing.assert_allclose(p, 0.2, rtol=1e-12)
+    assert husage == pytest.approx(1.0, rel=1e-12)
+    assert htoken == pytest.approx(1.0, rel=1e-12)
+    assert rmax == pytest.approx(0.2, rel=1e-12)
+    assert (z == 0).all()
+
+
+def test_diagnostics_one_hot_limit():
+    # tokens on well-separated component means with tiny variances: gamma is one-hot, so
+    # z is the planted component, p its frequency, H_usage that frequency's entropy,
+    # H_token = 0 and R_max = 1
+    B, H, N, d, K = 1, 2, 24, 3, 4
+    r = np.random.default_rng(3)
+    mu1 = 10.0 * np.eye(K, d) + np.arange(K)[:, None] * 7.0
+    mu = np.stack([mu1, mu1])
+    omega = np.full((H, K, d), -30.0)
+    alpha = np.zeros((H, K))
+    lab = np.array([0] * 12 + [1] * 6 + [2] * 6)           # component 3 unused
+    r.shuffle(lab)
+    Qx = np.stack([mu1[lab], mu1[lab]])[None]
+    p, husage, htoken, rmax, z = oracle.diagnostics(Qx, mu, omega, alpha, 1e-4)
+    freq = np.bincount(lab, minlength=K) / N
+    np.testing.assert_allclose(p, freq, atol=1e-12)
+    assert husage == pytest.approx(-(0.5 * np.log(0.5) + 2 * 0.25 * np.log(0.25)) / np.log(K), rel=1e-12)
+    assert htoken == pytest.approx(0.0, abs=1e-12)
+    assert rmax == pytest.approx(1.0, abs=1e-12)
+    assert np.array_equal(z[0], lab)
+
+
+def test_diagnostics_invariants_and_head_symmetry():
+    x = make_heads(B=3, H=4, N=20, K=7, seed=11)
+    K = 7
+    p, husage, htoken, rmax, z = oracle.diagnostics(x["Qx"], x["mu"], x["omega"], x["alpha"], 1e-4)
+    assert p.sum() == pytest.approx(1.0, rel=1e-12) and (p > 0).all()
+    # Jensen: the entropy of the mean is at least the mean entropy
+    assert 0.0 <= htoken <= husage <= 1.0
+    assert 1.0 / K <= rmax <= 1.0
+    assert z.min() >= 0 and z.max() < K
+    # the head average does not depend on the order of the heads
+    perm = np.array([2, 0, 3, 1])
+    y = oracle.diagnostics(x["Qx"][:, perm], x["mu"][perm], x["omega"][perm], x["alpha"][perm], 1e-4)
+    np.testing.assert_allclose(y[0], p, rtol=1e-12)
+    assert y[1:4] == pytest.approx((husage, htoken, rmax), rel=1e-12)
+    assert np.array_equal(y[4], z)
+    # H copies of one head give that head's own diagnostics
+    one = {k: v[:, :1] if k == "Qx" else v[:1] for k, v in x.items()}
+    rep = {k: np.repeat(v, 3, axis=1 if k == "Qx" else 0) for k, v in one.items()}
+    a = oracle.diagnostics(one["Qx"], one["mu"], one["omega"], one["alpha"], 1e-4)
+    b = oracle.diagnostics(rep["Qx"], rep["mu"], rep["omega"], rep["alpha"], 1e-4)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-12)
+    assert a[1:4] == pytest.approx(b[1:4], rel=1e-12)
