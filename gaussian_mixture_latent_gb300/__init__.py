@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "GmaError", "gma_desc", "gma_workspace_size", "gma_workspace_init", "gma_forward",
     "gma_forward_ex", "gma_forward_plan",
-    "gma_responsibilities", "gma_get_status", "gma_status_string", "gma_version",
+    "gma_responsibilities", "gma_diagnostics", "gma_get_status", "gma_status_string", "gma_version",
     "Workspace", "library_path",
 ]
 
@@ -70,12 +70,15 @@ def _load():
                                    ctypes.POINTER(vp), i]
     lib.gma_forward_plan.argtypes = [dp, i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_char_p), i]
     lib.gma_responsibilities.argtypes = [dp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.gma_diagnostics_workspace_size.argtypes = [dp, ctypes.POINTER(sz)]
+    lib.gma_diagnostics.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gma_get_status.argtypes = [vp, vp]
     lib.gma_status_string.argtypes = [i]
     lib.gma_status_string.restype = ctypes.c_char_p
     lib.gma_version.argtypes = []
     for fn in (lib.gma_workspace_size, lib.gma_workspace_init, lib.gma_forward,
-               lib.gma_forward_ex, lib.gma_forward_plan, lib.gma_responsibilities, lib.gma_get_status, lib.gma_version):
+               lib.gma_forward_ex, lib.gma_forward_plan, lib.gma_responsibilities, lib.gma_get_status, lib.gma_version,
+               lib.gma_diagnostics_workspace_size, lib.gma_diagnostics):
         fn.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -235,6 +238,33 @@ def gma_responsibilities(X, mu, rho, pi_logits, var_floor: float = 1e-4, out=Non
     if rc:
         raise GmaError(rc, "gma_responsibilities")
     return out
+
+
+def gma_diagnostics(Qx, mu, rho, pi_logits, var_floor: float = 1e-4, z=True, workspace=None, stream=None):
+    """Responsibility diagnostics (section 5.4, Eqs. 24-29) of the query routing vectors
+    Qx [B,H,N,d] (bf16, d = 64, K in {64, 128}) -> (p [K] float32, stats [3] float32 =
+    (H_usage, H_token, R_max), z [B,N] int32 argmax or None), all on Qx's device."""
+    B, H, N, d = Qx.shape
+    K = mu.shape[1]
+    _check(Qx, "Qx", (B, H, N, d), (torch.bfloat16, torch.float32))
+    _check(mu, "mu", (H, K, d), (torch.float32,))
+    _check(rho, "rho", (H, K, d), (torch.float32,))
+    _check(pi_logits, "pi_logits", (H, K), (torch.float32,))
+    p = torch.empty((K,), dtype=torch.float32, device=Qx.device)
+    stats = torch.empty((3,), dtype=torch.float32, device=Qx.device)
+    zt = torch.empty((B, N), dtype=torch.int32, device=Qx.device) if z else None
+    desc = _make_desc(B, H, N, d, K, 1, Qx.dtype, Qx.dtype, var_floor, 0)
+    nbytes = ctypes.c_size_t(0)
+    rc = _load().gma_diagnostics_workspace_size(ctypes.byref(desc), ctypes.byref(nbytes))
+    if rc:
+        raise GmaError(rc, "gma_diagnostics_workspace_size")
+    ws = _workspace_for(Qx.device, nbytes.value, workspace, stream)
+    rc = _load().gma_diagnostics(ctypes.byref(desc), _ptr(Qx), _ptr(mu), _ptr(rho), _ptr(pi_logits),
+                                 _ptr(p), _ptr(stats), _ptr(zt) if zt is not None else None, _ptr(ws),
+                                 ws.numel(), _stream_ptr(stream))
+    if rc:
+        raise GmaError(rc, "gma_diagnostics")
+    return p, stats, zt
 
 
 def gma_get_status(workspace=None, stream=None) -> int:

@@ -227,6 +227,41 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
     return simt_gamma(p, X, mu, lam, cdir, gamma_out, s) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
+gma_status gma_diagnostics_workspace_size(const gma_desc *desc, size_t *bytes) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!bytes) return GMA_ERR_INVALID_ARG;
+    const Problem p = make_problem(desc, 0, 0.f);
+    if (p.N > 0 && !tc_diag_supported(p)) return GMA_ERR_UNSUPPORTED;
+    *bytes = p.N > 0 ? tc_diag_layout(p).total : align_up(kHeaderBytes);
+    return GMA_OK;
+}
+
+gma_status gma_diagnostics(const gma_desc *desc, const void *Qx, const float *mu, const float *rho,
+                           const float *pi_logits, float *p_out, float *stats_out, int *z_out,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!mu || !rho || !pi_logits || !p_out || !stats_out) return GMA_ERR_INVALID_ARG;
+    if (desc->N > 0 && !Qx) return GMA_ERR_INVALID_ARG;
+    const void *ptrs[] = {Qx, mu, rho, pi_logits, workspace};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(p_out) | reinterpret_cast<uintptr_t>(stats_out) |
+         reinterpret_cast<uintptr_t>(z_out)) & 3u)
+        return GMA_ERR_INVALID_ARG;
+    const Problem p = make_problem(desc, 0, 0.f);
+    if (p.N == 0) return GMA_OK;
+    if (!tc_diag_supported(p)) return GMA_ERR_UNSUPPORTED;
+    const TcLayout L = tc_diag_layout(p);
+    if (!workspace || workspace_bytes < L.total) return GMA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    if (tc_params(p, L, mu, rho, pi_logits, ws, s) != cudaSuccess) return GMA_ERR_CUDA;
+    if (tc_diag(p, L, Qx, z_out, ws, s) != cudaSuccess) return GMA_ERR_CUDA;
+    return tc_diag_finalize(p, L, p_out, stats_out, ws, s) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
 gma_status gma_get_status(void *workspace, void *stream) {
     if (!workspace) return GMA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -73,6 +73,13 @@ cudaError_t tc_combine(const Problem &p, const TcLayout &L, void *out, char *ws,
 cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
                       const float *mu, const float *rho, const float *alpha, void *out, char *ws, cudaStream_t s);
 
+// ----- responsibility diagnostics (section 5.4): gma_tc_diag.cu (uses tc_params) -----
+bool tc_diag_supported(const Problem &p);
+TcLayout tc_diag_layout(const Problem &p);
+cudaError_t tc_diag(const Problem &p, const TcLayout &L, const void *Qx, int *z, char *ws, cudaStream_t s);
+cudaError_t tc_diag_finalize(const Problem &p, const TcLayout &L, float *p_out, float *stats_out, char *ws,
+                             cudaStream_t s);
+
 // ----- SIMT (CUDA-core, fp32) path: gma_simt.cu -----
 cudaError_t simt_params(const Problem &p, const float *rho, const float *alpha, float *lam,
                         float *cdir, cudaStream_t s);

@@ -123,6 +123,27 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
                                 const float *rho, const float *pi_logits, float *gamma_out,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Responsibility diagnostics of the query routing ("Gaussian Mixture
+ * Attention", section 5.4, Eqs. 24-29).  With gamma^Q the responsibilities of
+ * the rows of Qx [B, H, N, d] (Eq. 3b, per head) and T = B N tokens:
+ *   gbar_t   = (1/H) sum_h gamma^Q_{t,h}              head average (Eq. 24)
+ *   p_out[k] = (1/T) sum_t gbar_{t,k}                 marginal usage, p_out [K] float32 (Eq. 25)
+ *   stats_out[0] = H_usage = -sum_k p_k log p_k / log K                  (Eq. 26)
+ *   stats_out[1] = H_token = (1/T) sum_t -sum_k gbar log gbar / log K    (Eq. 27)
+ *   stats_out[2] = R_max   = (1/T) sum_t max_k gbar_{t,k}               (Eq. 28)
+ *   z_out[t]     = argmax_k gbar_{t,k}, ties to the lowest k, int32 [B, N] (Eq. 29);
+ *                  z_out may be NULL
+ * All outputs are device pointers.  Implemented for in_dtype = GMA_BF16,
+ * d = 64, K in {64, 128} (GMA_ERR_UNSUPPORTED otherwise); desc->dv and
+ * desc->out_dtype are validated as for gma_forward() but not used.  N = 0
+ * launches nothing.  Needs gma_diagnostics_workspace_size() bytes.
+ */
+gma_status gma_diagnostics_workspace_size(const gma_desc *desc, size_t *bytes);
+gma_status gma_diagnostics(const gma_desc *desc, const void *Qx, const float *mu, const float *rho,
+                           const float *pi_logits, float *p_out, float *stats_out, int *z_out,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
 /* Size of the fixed scratch buffer gma_forward_noalloc() uses: 32 MiB. */
 #define GMA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
