@@ -49,8 +49,9 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--direction", choices=["both", "bidir", "causal"], default="both",
-                    help="which forward(s) one step runs (default: both, the headline step)")
+    ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics"], default="both",
+                    help="which forward(s) one step runs (default: both, the headline step); "
+                         "diagnostics: one step is gma_diagnostics over the workload's query vectors")
     return ap.parse_args()
 
 
@@ -484,9 +485,170 @@ def run_gpu(args, rank, world, local):
     return 0
 
 
+DIAG_METRIC = "GMA responsibility diagnostics tokens·heads/s (Eqs. 24-29); % of HBM roofline"
+
+
+def diag_units(w):
+    return w.B * w.H * w.N          # token-head responsibility vectors per step
+
+
+def diag_oracle_sample(w, seconds):
+    """The oracle's diagnostics on a bounded sample: sequence 0, all heads, the first n rows
+    (n doubled until one call takes about `seconds` / 4); returns (token-heads per second, n)."""
+    import oracle
+    oracle.build()
+    x = inputs.gen_all(w.replace(B=1))
+    Q = inputs.widen(x["Qx"], w.dtype)
+    n, dt = 256, 0.0
+    while True:
+        n = min(n, w.N)
+        t0 = time.perf_counter()
+        oracle.diagnostics(Q[:, :, :n], x["mu"], x["rho"], x["alpha"], w.var_floor)
+        dt = time.perf_counter() - t0
+        if dt >= seconds / 4 or n == w.N:
+            break
+        n *= 2
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        oracle.diagnostics(Q[:, :, :n], x["mu"], x["rho"], x["alpha"], w.var_floor)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    return w.H * n / dt, n, reps, dt
+
+
+def run_diagnostics(args, rank, world, local):
+    """Responsibility diagnostics (section 5.4, Eqs. 24-29): one step is one gma_diagnostics
+    call over the query routing vectors of the whole workload (every head of every sequence)."""
+    import torch
+    import gaussian_mixture_latent_gb300 as gma
+    from gaussian_mixture_latent_gb300 import _build
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        rate, n, reps, dt = diag_oracle_sample(w, 12.0)
+        sample = f"sequence 0, {w.H} heads x the first {n} rows of {w.name}, {reps} calls, one thread"
+        line = {"impl": "reference", "metric": DIAG_METRIC, "value": rate, "unit": "tokens·heads/s",
+                "n_gpus": args.gpus, "steps": reps, "warmup": 0, "ms_per_step": dt * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": w.name, "step": "diagnostics (sampled)"},
+                "cpu_baseline": {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": rate, "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    host = [inputs.gen_all(w.replace(seed=s)) for s in (0, 1)]
+    dsets = [{k: to_dev(x[k]) for k in ("Qx", "mu", "rho", "alpha")} for x in host]
+    stream = torch.cuda.current_stream()
+
+    def step(x):
+        return gma.gma_diagnostics(x["Qx"], x["mu"], x["rho"], x["alpha"], var_floor=w.var_floor)
+
+    for it in range(max(3, args.warmup)):
+        step(dsets[it % 2])
+    torch.cuda.synchronize()
+    if gma.gma_get_status():
+        raise RuntimeError("device status after warm-up")
+    steps = args.steps if args.steps is not None else 200
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(gpu_id_for(local))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    # a GPU spin ahead of the loop lets the host enqueue every step before the GPU reaches them,
+    # so each step's events bracket GPU time (one step's kernels take less than its host call)
+    torch.cuda._sleep(int(2.0e6 * steps * 0.25))
+    for it in range(steps):
+        evs[it][0].record(stream)
+        step(dsets[it % 2])
+        evs[it][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if gma.gma_get_status():
+        raise RuntimeError("device status after the timed region")
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), device=dev)
+    value = whole_job_rate(diag_units(w), world, ms)
+
+    # end to end: Qx uploaded from pinned host memory, p, the statistics and z read back, every step
+    hq = [torch.from_numpy(x["Qx"].view(np.int16)).view(torch.bfloat16).pin_memory() for x in host]
+    dq = [torch.empty_like(d["Qx"]) for d in dsets]
+    hp = torch.empty((w.K,), dtype=torch.float32).pin_memory()
+    hs = torch.empty((3,), dtype=torch.float32).pin_memory()
+    hz = torch.empty((w.B, w.N), dtype=torch.int32).pin_memory()
+    e_steps = 10
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for it in range(e_steps):
+        dq[it % 2].copy_(hq[it % 2], non_blocking=True)
+        x = dict(dsets[it % 2], Qx=dq[it % 2])
+        p, st, z = step(x)
+        hp.copy_(p, non_blocking=True)
+        hs.copy_(st, non_blocking=True)
+        hz.copy_(z, non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e_steps, device=dev)
+    h2d = hq[0].numel() * 2
+    d2h = (w.K + 3 + w.B * w.N) * 4
+
+    pk = peaks()
+    rows = w.B * w.H * w.N
+    bytes_alg = rows * w.d * 2 + w.B * w.N * 4 + 4 * w.H * (2 * w.K * w.d + w.K)
+    flops_alg = rows * 2 * w.K * (2 * w.d + 16)
+    t_hbm = bytes_alg / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops_alg / (pk["bf16_tflops"] * 1e12)
+    achieved = bytes_alg / (ms / 1e3) / 1e9
+    roofline = {"bound": "hbm" if t_hbm >= t_tc else "tensor", "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                "kernel": "tc_params + tc_diag + tc_diag_finalize (whole call)", "kernel_ms": ms,
+                "peak_source": pk["source"],
+                "tensor_frac": flops_alg / (ms / 1e3) / 1e12 / pk["bf16_tflops"]}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, n, reps, dt = diag_oracle_sample(w, 12.0)
+        cpu = {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
+               "sample": f"sequence 0, {w.H} heads x the first {n} rows of {w.name}, {reps} calls, one thread"}
+    if rank == 0:
+        line = {"metric": DIAG_METRIC, "value": value, "unit": "tokens·heads/s", "n_gpus": world,
+                "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K,
+                           "step": "responsibility diagnostics of the query vectors",
+                           "l2": "two alternating input sets of %d MB each" %
+                                 (dsets[0]["Qx"].numel() * 2 // 2**20),
+                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "roofline": roofline, "clocks": clocks, "gpu_launches": 3 * steps,
+                "e2e": {"value": whole_job_rate(diag_units(w), world, e2e_ms), "unit": "tokens·heads/s",
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.direction == "diagnostics":
+        return run_diagnostics(args, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_gpu(args, rank, world, local)

@@ -240,6 +240,9 @@ def gma_responsibilities(X, mu, rho, pi_logits, var_floor: float = 1e-4, out=Non
     return out
 
 
+_diag_ws_bytes = {}
+
+
 def gma_diagnostics(Qx, mu, rho, pi_logits, var_floor: float = 1e-4, z=True, workspace=None, stream=None):
     """Responsibility diagnostics (section 5.4, Eqs. 24-29) of the query routing vectors
     Qx [B,H,N,d] (bf16, d = 64, K in {64, 128}) -> (p [K] float32, stats [3] float32 =
@@ -254,11 +257,14 @@ def gma_diagnostics(Qx, mu, rho, pi_logits, var_floor: float = 1e-4, z=True, wor
     stats = torch.empty((3,), dtype=torch.float32, device=Qx.device)
     zt = torch.empty((B, N), dtype=torch.int32, device=Qx.device) if z else None
     desc = _make_desc(B, H, N, d, K, 1, Qx.dtype, Qx.dtype, var_floor, 0)
-    nbytes = ctypes.c_size_t(0)
-    rc = _load().gma_diagnostics_workspace_size(ctypes.byref(desc), ctypes.byref(nbytes))
-    if rc:
-        raise GmaError(rc, "gma_diagnostics_workspace_size")
-    ws = _workspace_for(Qx.device, nbytes.value, workspace, stream)
+    key = (B, H, N, d, K, Qx.dtype)
+    if key not in _diag_ws_bytes:
+        nbytes = ctypes.c_size_t(0)
+        rc = _load().gma_diagnostics_workspace_size(ctypes.byref(desc), ctypes.byref(nbytes))
+        if rc:
+            raise GmaError(rc, "gma_diagnostics_workspace_size")
+        _diag_ws_bytes[key] = nbytes.value
+    ws = _workspace_for(Qx.device, _diag_ws_bytes[key], workspace, stream)
     rc = _load().gma_diagnostics(ctypes.byref(desc), _ptr(Qx), _ptr(mu), _ptr(rho), _ptr(pi_logits),
                                  _ptr(p), _ptr(stats), _ptr(zt) if zt is not None else None, _ptr(ws),
                                  ws.numel(), _stream_ptr(stream))

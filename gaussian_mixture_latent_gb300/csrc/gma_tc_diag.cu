@@ -18,10 +18,12 @@
 // head each thread (one token) has gbar in registers: its entropy, maximum and
 // argmax, and a warp transpose-reduce adds the tile's column sums to per-warp
 // partials of p.  Responsibilities never leave the SM.
-// tc_diag_finalize: one CTA sums the per-CTA partials in a fixed order (double)
-// and writes p [K] and {H_usage, H_token, R_max}.
+// tc_diag_finalize: one CTA sums the per-CTA partials in a fixed order and
+// writes p [K] and {H_usage, H_token, R_max}.
 // Warps: 0 TMA producer (Qx tiles and parameter blocks); 1 TMEM owner and MMA
-// issuer; 2-5 one compute group.  Every mbarrier wait is bounded.
+// issuer; 2-5 the epilogue group; 6-9 the convert group (bf16 tile -> [x, x^2/256]
+// operand, double-buffered, overlapping the previous step's epilogue).  Every
+// mbarrier wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -38,7 +40,7 @@ using namespace tc;
 
 namespace {
 
-constexpr int kDiagThreads = 192;
+constexpr int kDiagThreads = 320;        // warps: producer, MMA, epilogue group, convert group
 constexpr int kDiagX = 4;                 // routing-tile ring stages
 constexpr int kDiagMaxHeads = 1024;       // head scales kept in shared memory
 
@@ -93,7 +95,7 @@ tc_diag_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
     uint64_t *xfull = bars, *xempty = xfull + kDiagX, *a_full = xempty + kDiagX;   // a_full[2]
     uint64_t *d_full = a_full + 2, *d_empty = d_full + 1, *w_full = d_empty + 1;   // w_full[2]
-    uint64_t *w_empty = w_full + 2, *fin = w_empty + 2;                            // w_empty[2]
+    uint64_t *w_empty = w_full + 2, *a_empty = w_empty + 2, *fin = a_empty + 2;   // w_empty[2], a_empty[2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *scales = reinterpret_cast<float *>(sm + C::OFF_SC);
@@ -174,9 +176,30 @@ tc_diag_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
                 mma_commit(d_full);
                 mma_commit(&xempty[s % kDiagX]);
                 mma_commit(&w_empty[s & 1]);
+                mma_commit(&a_empty[s & 1]);
             }
             mma_commit(fin);
             wait_ignoring_abort(fin, 0, A.status);
+        }
+    } else if (warp >= 6) {
+        // convert group: step s's [x, x^2/256] operand into buffer s & 1 once the MMA of step
+        // s - 2 has read that buffer
+        RowThread rt;
+        rt.wg = 1;
+        rt.r = 32u * (warp & 3) + lane;
+        rt.lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        rt.wtid = threadIdx.x - 192;
+        const bool elected = rt.wtid == 0;
+        for (int s = 0; s < nsteps; ++s) {
+            bool w = mbar_wait(&xfull[s % kDiagX], (s / kDiagX) & 1, ab, kDevErrTimeout);
+            if (s >= 2) w = w && mbar_wait(&a_empty[s & 1], ((s >> 1) - 1) & 1, ab, kDevErrTimeout);
+            if (!wg_all(rt, w)) break;
+            tc_fence_after();
+            convert_row(sm + C::OFF_X + (s % kDiagX) * kTileBytes, rt.r, tmem + rt.lane_off + C::COL_A + (s & 1) * 64);
+            tmem_st_wait();
+            tc_fence_before();
+            wg_sync(rt);
+            if (elected) mbar_arrive(&a_full[s & 1]);
         }
     } else {
         RowThread rt;
@@ -190,23 +213,11 @@ tc_diag_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
         const int hs = A.H < kDiagMaxHeads ? A.H : kDiagMaxHeads;
         for (int h = rt.wtid; h < hs; h += kWgThreads) scales[h] = head_scale(A.params, A.param_stride, h, K);
         wg_sync(rt);
-        auto convert = [&](int s) -> bool {
-            const bool w = mbar_wait(&xfull[s % kDiagX], (s / kDiagX) & 1, ab, kDevErrTimeout);
-            if (!wg_all(rt, w)) return false;
-            convert_row(sm + C::OFF_X + (s % kDiagX) * kTileBytes, rt.r, tmem + rt.lane_off + C::COL_A + (s & 1) * 64);
-            tmem_st_wait();
-            tc_fence_before();
-            wg_sync(rt);
-            if (elected) mbar_arrive(&a_full[s & 1]);
-            return true;
-        };
         const uint32_t dcol = tmem + rt.lane_off + C::COL_D, acol = tmem + rt.lane_off + C::COL_ACC;
         float ent_sum = 0.f, max_sum = 0.f;       // over this thread's tokens
-        bool ok = nsteps > 0 && convert(0);
+        bool ok = true;
         for (int s = 0; s < nsteps && ok; ++s) {
             const int h = step_head(s), u = step_tile(s), b = u / A.T, j = u % A.T;
-            // step s + 1's operand (its buffer was read by the MMA of step s - 1, complete)
-            if (s + 1 < nsteps && !(ok = convert(s + 1))) break;
             const float scale = h < kDiagMaxHeads ? scales[h] : head_scale(A.params, A.param_stride, h, K);
             const bool w = mbar_wait(d_full, s & 1, ab, kDevErrTimeout);
             if (!(ok = wg_all(rt, w))) break;
@@ -310,34 +321,50 @@ tc_diag_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
     }
 }
 
-// p [K] and {H_usage, H_token, R_max} from the per-CTA partials: fixed-order sums in
-// double, one thread per partial column.
-constexpr int kFinThreads = 160;                   // >= K + 2 for K <= 128
+// p [K] and {H_usage, H_token, R_max} from the per-CTA partials (at most kMaxCtas of them, fp32
+// sums suffice).  Thread (q, k) sums column k of the CTAs c = q (mod kFinGroups) with four
+// independent accumulators (the loads stay in flight); the groups' sums and the p log p terms
+// are combined in a fixed order.
+constexpr int kFinGroups = 6, kFinCols = 160;      // kFinCols >= K + 2 for K <= 128
 
-__global__ void __launch_bounds__(kFinThreads) tc_diag_finalize_kernel(int K, int ncta, double T,
-                                                                       const float *__restrict__ part,
-                                                                       float *__restrict__ p_out,
-                                                                       float *__restrict__ stats_out) {
+__global__ void __launch_bounds__(kFinGroups * kFinCols) tc_diag_finalize_kernel(int K, int ncta, float T,
+                                                                                const float *__restrict__ part,
+                                                                                float *__restrict__ p_out,
+                                                                                float *__restrict__ stats_out) {
     grid_dep_launch();
     grid_dep_wait();                                       // the partials are written
-    __shared__ double colsum[kFinThreads];
-    const int k = threadIdx.x;
-    double acc = 0.0;
-    if (k < K + 2)
-        for (int c = 0; c < ncta; ++c) acc += (double)part[(size_t)c * (K + 2) + k];
-    colsum[k] = acc;
-    __syncthreads();
-    if (k < K) p_out[k] = (float)(acc / T);
-    if (k == 0) {
-        const double logK = log((double)K);
-        double hu = 0.0;
-        for (int kk = 0; kk < K; ++kk) {
-            const double p = colsum[kk] / T;
-            if (p > 0.0) hu -= p * log(p);
+    __shared__ float gsum[kFinGroups][kFinCols];
+    __shared__ float term[kFinCols];
+    const int k = threadIdx.x % kFinCols, q = threadIdx.x / kFinCols, w = K + 2;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    if (k < w) {
+        int c = q;
+        for (; c + 3 * kFinGroups < ncta; c += 4 * kFinGroups) {
+            a0 += part[(size_t)c * w + k];
+            a1 += part[(size_t)(c + kFinGroups) * w + k];
+            a2 += part[(size_t)(c + 2 * kFinGroups) * w + k];
+            a3 += part[(size_t)(c + 3 * kFinGroups) * w + k];
         }
-        stats_out[0] = (float)(hu / logK);
-        stats_out[1] = (float)(colsum[K] / T / logK);
-        stats_out[2] = (float)(colsum[K + 1] / T);
+        for (; c < ncta; c += kFinGroups) a0 += part[(size_t)c * w + k];
+    }
+    gsum[q][k] = (a0 + a1) + (a2 + a3);
+    __syncthreads();
+    if (q == 0) {
+        float acc = 0.f;
+        for (int g = 0; g < kFinGroups; ++g) acc += gsum[g][k];
+        const float pk = acc / T;
+        term[k] = k < K && pk > 0.f ? -pk * logf(pk) : 0.f;
+        if (k < K) p_out[k] = pk;
+        if (k == K || k == K + 1) gsum[0][k] = acc;        // read back by thread 0 below
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float hu = 0.f;
+        for (int kk = 0; kk < K; ++kk) hu += term[kk];
+        const float logK = logf((float)K);
+        stats_out[0] = hu / logK;
+        stats_out[1] = gsum[0][K] / T / logK;
+        stats_out[2] = gsum[0][K + 1] / T;
     }
 }
 
@@ -384,8 +411,8 @@ cudaError_t tc_diag(const Problem &p, const TcLayout &L, const void *Qx, int *z,
 
 cudaError_t tc_diag_finalize(const Problem &p, const TcLayout &L, float *p_out, float *stats_out, char *ws,
                              cudaStream_t s) {
-    return launch_dependent(tc_diag_finalize_kernel, dim3(1), dim3(kFinThreads), 0, s, p.K, L.ncta,
-                            (double)p.B * (double)p.N, reinterpret_cast<const float *>(ws + L.part), p_out,
+    return launch_dependent(tc_diag_finalize_kernel, dim3(1), dim3(kFinGroups * kFinCols), 0, s, p.K, L.ncta,
+                            (float)((double)p.B * (double)p.N), reinterpret_cast<const float *>(ws + L.part), p_out,
                             stats_out);
 }
 
