@@ -63,7 +63,7 @@ def kernel_work(name: str, G, N, d, K, dv, in_dtype="bf16", out_dtype="bf16", H=
         return "alu", 2 * rows * K * (dv + 1), "flop"
     if name == "simt_causal_chunk":
         return "alu", 4 * rows * K * (dv + 1), "flop"
-    if name in ("tc_write", "tc_segment_totals"):
+    if name == "tc_write":
         return "hbm", rows * (e_in * (d + dv)), "byte"
     if name == "tc_read":
         return "hbm", rows * (e_in * d + e_out * dv), "byte"
