@@ -53,8 +53,10 @@ def _load():
                                            i, _dp, i]
         lib.gma_oracle_diagnostics.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, d, _dp, _dp,
                                                ctypes.POINTER(ctypes.c_int)]
+        lib.gma_oracle_cross_head.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d, d, _dp]
         for fn in (lib.gma_oracle_scores, lib.gma_oracle_responsibilities,
-                   lib.gma_oracle_forward_head, lib.gma_oracle_forward, lib.gma_oracle_diagnostics):
+                   lib.gma_oracle_forward_head, lib.gma_oracle_forward, lib.gma_oracle_diagnostics,
+                   lib.gma_oracle_cross_head):
             fn.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -142,3 +144,17 @@ def diagnostics(Qx, mu, omega, alpha, var_floor: float):
                                           float(var_floor), _p(p), _p(stats),
                                           z.ctypes.data_as(ctypes.POINTER(ctypes.c_int))), "diagnostics")
     return p, float(stats[0]), float(stats[1]), float(stats[2]), z
+
+
+def cross_head(Qx, Ky, Vy, mu, omega, alpha, var_floor: float, eps: float) -> np.ndarray:
+    """Cross-attention GMA for one head (sections 3.1, 6): queries Qx [Nq, d] read the
+    memory of a context Ky [Nkv, d], Vy [Nkv, dv] -> O [Nq, dv] (Eq. 5-8, bidirectional)."""
+    Qx, Ky, Vy, mu, omega, alpha = map(_c, (Qx, Ky, Vy, mu, omega, alpha))
+    Nq, d = Qx.shape
+    Nkv = Ky.shape[0]
+    K = mu.shape[0]
+    dv = Vy.shape[1]
+    out = np.empty((Nq, dv), dtype=np.float64)
+    _check(_load().gma_oracle_cross_head(Nq, Nkv, d, K, dv, _p(Qx), _p(Ky), _p(Vy), _p(mu), _p(omega),
+                                         _p(alpha), float(var_floor), float(eps), _p(out)), "cross_head")
+    return out

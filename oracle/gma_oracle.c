@@ -317,3 +317,54 @@ int gma_oracle_diagnostics(int B, int H, int N, int d, int K, const double *Qx, 
     free(gbar);
     return rc;
 }
+
+/*
+ * Cross-attention GMA, one head ("Gaussian Mixture Attention", section 3.1 and
+ * section 6): queries from a query-side sequence X (Nq rows), keys and values
+ * from a context sequence Y (Nkv rows), responsibilities Gamma^Q_X and
+ * Gamma^K_Y under the head's one mixture; then Eq. (5)-(8) with the context's
+ * memory: Vt = Gamma^K_Y^T V_Y, Z = Gamma^K_Y^T 1, O = Gamma^Q_X Vt / (Gamma^Q_X Z + eps).
+ * Bidirectional only (no causal order exists between two sequences).
+ * Qx [Nq, d], Ky [Nkv, d], Vy [Nkv, dv] -> out [Nq, dv].
+ */
+int gma_oracle_cross_head(int Nq, int Nkv, int d, int K, int dv, const double *Qx, const double *Ky,
+                          const double *Vy, const double *mu, const double *omega, const double *alpha,
+                          double var_floor, double eps, double *out)
+{
+    if (Nq < 0 || Nkv < 0 || d <= 0 || K <= 0 || dv <= 0) return 1;
+    double *gq = (double *)malloc(sizeof(double) * ((size_t)Nq * K + 1));
+    double *gk = (double *)malloc(sizeof(double) * ((size_t)Nkv * K + 1));
+    double *Vt = (double *)calloc((size_t)K * dv, sizeof(double));
+    double *Z = (double *)calloc((size_t)K, sizeof(double));
+    int rc = 2;
+    if (!gq || !gk || !Vt || !Z) goto done;
+    rc = gma_oracle_responsibilities(Nq, d, K, Qx, mu, omega, alpha, var_floor, gq);
+    if (rc) goto done;
+    rc = gma_oracle_responsibilities(Nkv, d, K, Ky, mu, omega, alpha, var_floor, gk);
+    if (rc) goto done;
+    /* Eq. (5)-(6) over the context */
+    for (int j = 0; j < Nkv; ++j)
+        for (int k = 0; k < K; ++k) {
+            double g = gk[(size_t)j * K + k];
+            Z[k] += g;
+            for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += g * Vy[(size_t)j * dv + c];
+        }
+    /* Eq. (7)-(8) for the queries */
+    for (int i = 0; i < Nq; ++i) {
+        double den = 0.0;
+        for (int k = 0; k < K; ++k) den += gq[(size_t)i * K + k] * Z[k];
+        den += eps;
+        for (int c = 0; c < dv; ++c) {
+            double num = 0.0;
+            for (int k = 0; k < K; ++k) num += gq[(size_t)i * K + k] * Vt[(size_t)k * dv + c];
+            out[(size_t)i * dv + c] = num / den;
+        }
+    }
+    rc = 0;
+done:
+    free(gq);
+    free(gk);
+    free(Vt);
+    free(Z);
+    return rc;
+}

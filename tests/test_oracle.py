@@ -368,3 +368,42 @@ def test_diagnostics_invariants_and_head_symmetry():
     b = oracle.diagnostics(rep["Qx"], rep["mu"], rep["omega"], rep["alpha"], 1e-4)
     np.testing.assert_allclose(a[0], b[0], rtol=1e-12)
     assert a[1:4] == pytest.approx(b[1:4], rel=1e-12)
+
+
+# ---------------------------------------------------------------- cross-attention (sections 3.1, 6)
+
+def brute_force_cross(Qx, Ky, Vy, mu, omega, alpha, var_floor, eps):
+    """Explicit Nq x Nkv affinity Gamma^Q_X Gamma^K_Y^T, row-normalised, applied to Vy."""
+    At = textbook_gamma(Qx, mu, omega, alpha, var_floor) @ textbook_gamma(Ky, mu, omega, alpha, var_floor).T
+    return (At / (At.sum(axis=1, keepdims=True) + eps)) @ Vy
+
+
+@pytest.mark.parametrize("Nq,Nkv,eps", [(17, 40, 1e-6), (50, 3, 0.2), (1, 1, 1e-6), (9, 9, 0.05)])
+def test_cross_matches_explicit_affinity(Nq, Nkv, eps):
+    r = np.random.default_rng(Nq * 100 + Nkv)
+    d, K, dv = 4, 6, 5
+    Qx, Ky, Vy = r.normal(size=(Nq, d)), r.normal(size=(Nkv, d)), r.normal(size=(Nkv, dv))
+    mu, omega, alpha = r.normal(size=(K, d)), 0.5 * r.normal(size=(K, d)), r.normal(size=(K,))
+    got = oracle.cross_head(Qx, Ky, Vy, mu, omega, alpha, 1e-4, eps)
+    np.testing.assert_allclose(got, brute_force_cross(Qx, Ky, Vy, mu, omega, alpha, 1e-4, eps), rtol=1e-9,
+                               atol=1e-12)
+
+
+def test_cross_with_the_sequence_itself_is_self_attention():
+    x = make(N=33)
+    got = oracle.cross_head(x["Qx"], x["Kx"], x["V"], x["mu"], x["omega"], x["alpha"], 1e-4, 1e-6)
+    ref = oracle.forward_head(x["Qx"], x["Kx"], x["V"], x["mu"], x["omega"], x["alpha"], 1e-4, 1e-6, False)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_cross_context_order_does_not_matter_and_queries_are_independent():
+    r = np.random.default_rng(5)
+    d, K, dv, Nq, Nkv = 3, 4, 2, 12, 30
+    Qx, Ky, Vy = r.normal(size=(Nq, d)), r.normal(size=(Nkv, d)), r.normal(size=(Nkv, dv))
+    mu, omega, alpha = r.normal(size=(K, d)), 0.5 * r.normal(size=(K, d)), r.normal(size=(K,))
+    base = oracle.cross_head(Qx, Ky, Vy, mu, omega, alpha, 1e-4, 1e-6)
+    perm = r.permutation(Nkv)
+    np.testing.assert_allclose(oracle.cross_head(Qx, Ky[perm], Vy[perm], mu, omega, alpha, 1e-4, 1e-6), base,
+                               rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(oracle.cross_head(Qx[:5], Ky, Vy, mu, omega, alpha, 1e-4, 1e-6), base[:5],
+                               rtol=1e-12, atol=1e-14)
