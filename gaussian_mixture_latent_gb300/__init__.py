@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "GmaError", "gma_desc", "gma_workspace_size", "gma_workspace_init", "gma_forward",
     "gma_forward_ex", "gma_forward_plan",
-    "gma_responsibilities", "gma_diagnostics", "gma_get_status", "gma_status_string", "gma_version",
+    "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_get_status", "gma_status_string", "gma_version",
     "Workspace", "library_path",
 ]
 
@@ -72,13 +72,16 @@ def _load():
     lib.gma_responsibilities.argtypes = [dp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gma_diagnostics_workspace_size.argtypes = [dp, ctypes.POINTER(sz)]
     lib.gma_diagnostics.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.gma_cross_workspace_size.argtypes = [dp, i, ctypes.POINTER(sz)]
+    lib.gma_forward_cross.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, f, vp, vp, sz, vp]
     lib.gma_get_status.argtypes = [vp, vp]
     lib.gma_status_string.argtypes = [i]
     lib.gma_status_string.restype = ctypes.c_char_p
     lib.gma_version.argtypes = []
     for fn in (lib.gma_workspace_size, lib.gma_workspace_init, lib.gma_forward,
                lib.gma_forward_ex, lib.gma_forward_plan, lib.gma_responsibilities, lib.gma_get_status, lib.gma_version,
-               lib.gma_diagnostics_workspace_size, lib.gma_diagnostics):
+               lib.gma_diagnostics_workspace_size, lib.gma_diagnostics, lib.gma_cross_workspace_size,
+               lib.gma_forward_cross):
         fn.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -237,6 +240,37 @@ def gma_responsibilities(X, mu, rho, pi_logits, var_floor: float = 1e-4, out=Non
                                       _stream_ptr(stream))
     if rc:
         raise GmaError(rc, "gma_responsibilities")
+    return out
+
+
+def gma_forward_cross(Qx, Ky, Vy, mu, rho, pi_logits, eps: float = 1e-6, var_floor: float = 1e-4, out=None,
+                      workspace=None, stream=None):
+    """Cross-attention GMA (sections 3.1, 6): the queries Qx [B,H,N,d] read the memory of the
+    context Ky [B,H,Nkv,d], Vy [B,H,Nkv,dv] -> out [B,H,N,dv] (bidirectional, Eq. 5-8)."""
+    B, H, N, d = Qx.shape
+    Nkv = Ky.shape[2]
+    dv = Vy.shape[3]
+    K = mu.shape[1]
+    _check(Qx, "Qx", (B, H, N, d), (torch.float32, torch.bfloat16))
+    _check(Ky, "Ky", (B, H, Nkv, d), (Qx.dtype,))
+    _check(Vy, "Vy", (B, H, Nkv, dv), (Qx.dtype,))
+    _check(mu, "mu", (H, K, d), (torch.float32,))
+    _check(rho, "rho", (H, K, d), (torch.float32,))
+    _check(pi_logits, "pi_logits", (H, K), (torch.float32,))
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=Qx.dtype, device=Qx.device)
+    _check(out, "out", (B, H, N, dv), (Qx.dtype,))
+    desc = _make_desc(B, H, N, d, K, dv, Qx.dtype, out.dtype, var_floor, 0)
+    nbytes = ctypes.c_size_t(0)
+    rc = _load().gma_cross_workspace_size(ctypes.byref(desc), Nkv, ctypes.byref(nbytes))
+    if rc:
+        raise GmaError(rc, "gma_cross_workspace_size")
+    ws = _workspace_for(Qx.device, nbytes.value, workspace, stream)
+    rc = _load().gma_forward_cross(ctypes.byref(desc), Nkv, _ptr(Qx), _ptr(Ky), _ptr(Vy), _ptr(mu), _ptr(rho),
+                                   _ptr(pi_logits), float(eps), _ptr(out), _ptr(ws), ws.numel(),
+                                   _stream_ptr(stream))
+    if rc:
+        raise GmaError(rc, "gma_forward_cross")
     return out
 
 

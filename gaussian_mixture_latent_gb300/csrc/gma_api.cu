@@ -38,6 +38,7 @@ Problem make_problem(const gma_desc *d, int causal, float eps) {
     Problem p{};
     p.B = d->B; p.H = d->H; p.N = d->N; p.d = d->d; p.K = d->K; p.dv = d->dv;
     p.G = d->B * d->H;
+    p.Nkv = d->N;
     p.in_dtype = d->in_dtype; p.out_dtype = d->out_dtype;
     p.var_floor = d->var_floor; p.eps = eps; p.causal = causal ? 1 : 0; p.chunk = d->chunk;
     return p;
@@ -190,6 +191,45 @@ gma_status gma_forward(const gma_desc *desc, const void *Qx, const void *Kx, con
                        void *stream) {
     return gma_forward_ex(desc, Qx, Kx, V, mu, rho, pi_logits, eps, causal, out, workspace,
                           workspace_bytes, stream, nullptr, 0);
+}
+
+gma_status gma_cross_workspace_size(const gma_desc *desc, int Nkv, size_t *bytes) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!bytes || Nkv < 0 || (desc->N > 0 && Nkv == 0)) return GMA_ERR_INVALID_ARG;
+    if ((long long)desc->B * desc->H * Nkv > (1LL << 31)) return GMA_ERR_UNSUPPORTED;
+    Problem p = make_problem(desc, 0, 0.f);
+    p.Nkv = Nkv;
+    if (p.N == 0) { *bytes = align_up(kHeaderBytes); return GMA_OK; }
+    if (!tc_bidir_supported(p)) return GMA_ERR_UNSUPPORTED;
+    *bytes = tc_layout(p).total;
+    return GMA_OK;
+}
+
+gma_status gma_forward_cross(const gma_desc *desc, int Nkv, const void *Qx, const void *Ky, const void *Vy,
+                             const float *mu, const float *rho, const float *pi_logits, float eps, void *out,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (Nkv < 0 || (desc->N > 0 && Nkv == 0) || !(eps >= 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
+    if (!mu || !rho || !pi_logits) return GMA_ERR_INVALID_ARG;
+    if (desc->N > 0 && (!Qx || !Ky || !Vy || !out)) return GMA_ERR_INVALID_ARG;
+    const void *ptrs[] = {Qx, Ky, Vy, out, mu, rho, pi_logits, workspace};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
+    if ((long long)desc->B * desc->H * Nkv > (1LL << 31)) return GMA_ERR_UNSUPPORTED;
+    Problem p = make_problem(desc, 0, eps);
+    p.Nkv = Nkv;
+    if (p.N == 0) return GMA_OK;
+    if (!tc_bidir_supported(p)) return GMA_ERR_UNSUPPORTED;
+    const TcLayout L = tc_layout(p);
+    if (!workspace || workspace_bytes < L.total) return GMA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    if (tc_params(p, L, mu, rho, pi_logits, ws, s) != cudaSuccess) return GMA_ERR_CUDA;
+    if (tc_write(p, L, Ky, Vy, ws, s) != cudaSuccess) return GMA_ERR_CUDA;
+    if (tc_reduce(p, L, ws, s) != cudaSuccess) return GMA_ERR_CUDA;
+    return tc_read(p, L, Qx, out, ws, s) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
 gma_status gma_forward_plan(const gma_desc *desc, int causal, int *n_launches, const char **names,

@@ -22,6 +22,7 @@ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a
 // Problem geometry after validation.
 struct Problem {
     int B, H, N, d, K, dv, G;
+    int Nkv;                     // rows of Kx and V: N, or the context length of cross-attention
     gma_dtype in_dtype, out_dtype;
     float var_floor;
     float eps;
@@ -47,7 +48,8 @@ struct TcLayout {
     size_t stats, pnum, pden;          // component-sliced causal path: row statistics, partials
     int ns, nt;                        // component slices and value slices of 64
     uint32_t param_stride, mem_stride;
-    int T, Ttot, ncta;                 // tiles per head, tiles in total, persistent CTAs
+    int T, Ttot, ncta;                 // tiles per head, tiles in total, persistent CTAs (queries / read)
+    int Tkv, Ttot_kv, ncta_kv;         // the same for the key/value rows (write, reduce)
 };
 bool tc_bidir_supported(const Problem &p);
 TcLayout tc_layout(const Problem &p);

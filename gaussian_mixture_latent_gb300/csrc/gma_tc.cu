@@ -674,16 +674,16 @@ template <int K>
 cudaError_t launch_write(const Problem &p, const TcLayout &L, const void *Kx, const void *V, char *ws,
                          cudaStream_t s) {
     CUtensorMap tk, tv;
-    if (!make_map(&tk, Kx, p.G, p.N, DR) || !make_map(&tv, V, p.G, p.N, DVV)) return cudaErrorInvalidValue;
+    if (!make_map(&tk, Kx, p.G, p.Nkv, DR) || !make_map(&tv, V, p.G, p.Nkv, DVV)) return cudaErrorInvalidValue;
     TcArgs a{};
-    a.G = p.G; a.H = p.H; a.N = p.N; a.T = L.T; a.Ttot = L.Ttot; a.K = K;
+    a.G = p.G; a.H = p.H; a.N = p.Nkv; a.T = L.Tkv; a.Ttot = L.Ttot_kv; a.K = K;
     a.params = reinterpret_cast<const uint8_t *>(ws + L.params); a.param_stride = L.param_stride;
     a.partials = reinterpret_cast<float *>(ws + L.part);
     a.status = reinterpret_cast<unsigned *>(ws);
     auto kern = tc_write_kernel<K>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WriteCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
-    return launch_dependent(kern, dim3(L.ncta), dim3(WriteCfg<K>::THREADS), WriteCfg<K>::BYTES, s, tk, tv, a);
+    return launch_dependent(kern, dim3(L.ncta_kv), dim3(WriteCfg<K>::THREADS), WriteCfg<K>::BYTES, s, tk, tv, a);
 }
 
 template <int K>
@@ -707,7 +707,7 @@ cudaError_t launch_read(const Problem &p, const TcLayout &L, const void *Qx, voi
 
 bool tc_bidir_supported(const Problem &p) {
     return p.in_dtype == GMA_BF16 && p.out_dtype == GMA_BF16 && !p.causal && p.d == DR && p.dv == DVV &&
-           (p.K == 64 || p.K == 128) && p.N > 0;
+           (p.K == 64 || p.K == 128) && p.N > 0 && p.Nkv > 0;
 }
 
 TcLayout tc_layout(const Problem &p) {
@@ -716,6 +716,9 @@ TcLayout tc_layout(const Problem &p) {
     L.Ttot = L.T * p.G;
     const int nsm = sm_count();
     L.ncta = std::max(1, std::min({nsm > 0 ? nsm : kMaxCtas, kMaxCtas, L.Ttot}));
+    L.Tkv = (p.Nkv + TM - 1) / TM;
+    L.Ttot_kv = L.Tkv * p.G;
+    L.ncta_kv = std::max(1, std::min({nsm > 0 ? nsm : kMaxCtas, kMaxCtas, L.Ttot_kv}));
     L.param_stride = align1k(param_bytes(p.K));
     L.mem_stride = align1k(mem_bytes(p.K));
     size_t off = kHeaderBytes;
@@ -746,7 +749,7 @@ cudaError_t tc_write(const Problem &p, const TcLayout &L, const void *Kx, const 
 
 cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s) {
     dim3 grid((20 * p.K + kReduceThreads - 1) / kReduceThreads, p.G);
-    return launch_dependent(tc_reduce_kernel, grid, dim3(kReduceThreads), 0, s, p.K, L.T, L.Ttot, L.ncta,
+    return launch_dependent(tc_reduce_kernel, grid, dim3(kReduceThreads), 0, s, p.K, L.Tkv, L.Ttot_kv, L.ncta_kv,
                             reinterpret_cast<const float *>(ws + L.part), reinterpret_cast<uint8_t *>(ws + L.mem),
                             L.mem_stride);
 }

@@ -124,6 +124,23 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Cross-attention GMA ("Gaussian Mixture Attention", section 3.1 and section 6):
+ * the queries Qx [B, H, N, d] of one sequence read the latent memory of a
+ * context sequence, Ky [B, H, Nkv, d] and Vy [B, H, Nkv, dv], through the head's
+ * one mixture:  Vt = Gamma^K_Y^T Vy,  Z = Gamma^K_Y^T 1,
+ * out [B, H, N, dv] = Gamma^Q_X Vt / (Gamma^Q_X Z + eps)   (Eq. 5-8 with the context's memory).
+ * Bidirectional only: there is no causal order between two sequences.  desc->N
+ * is the query length; Nkv >= 1 when N >= 1 (an empty context has no memory:
+ * GMA_ERR_INVALID_ARG).  Implemented on the tensor-core path (bf16 in and out,
+ * d = dv = 64, K in {64, 128}); GMA_ERR_UNSUPPORTED otherwise.  Workspace:
+ * gma_cross_workspace_size().  Errors as for gma_forward().
+ */
+gma_status gma_cross_workspace_size(const gma_desc *desc, int Nkv, size_t *bytes);
+gma_status gma_forward_cross(const gma_desc *desc, int Nkv, const void *Qx, const void *Ky, const void *Vy,
+                             const float *mu, const float *rho, const float *pi_logits, float eps, void *out,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Responsibility diagnostics of the query routing ("Gaussian Mixture
  * Attention", section 5.4, Eqs. 24-29).  With gamma^Q the responsibilities of
  * the rows of Qx [B, H, N, d] (Eq. 3b, per head) and T = B N tokens:
