@@ -49,9 +49,12 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics"], default="both",
+    ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics", "cross"], default="both",
                     help="which forward(s) one step runs (default: both, the headline step); "
-                         "diagnostics: one step is gma_diagnostics over the workload's query vectors")
+                         "diagnostics: one step is gma_diagnostics over the workload's query vectors; "
+                         "cross: one step is gma_forward_cross, the workload's queries reading a context")
+    ap.add_argument("--context", type=int, default=0,
+                    help="context length of --direction cross (default: 4 x the workload's N)")
     return ap.parse_args()
 
 
@@ -644,11 +647,145 @@ def run_diagnostics(args, rank, world, local):
     return 0
 
 
+CROSS_METRIC = "GMA cross-attention query tokens·heads/s (Eq. 5-8, context memory); % of HBM roofline"
+
+
+def cross_oracle_sample(w, Nkv, seconds):
+    """The oracle's cross head on a bounded sample: head 0, the whole context, the first n
+    query rows (n doubled until one call takes about `seconds` / 4)."""
+    import oracle
+    oracle.build()
+    q = inputs.gen_all(w.replace(B=1, H=1))
+    c = inputs.gen_all(w.replace(B=1, H=1, N=Nkv, seed=w.seed + 1000))
+    Q, Ky, Vy = (inputs.widen(a[0, 0], w.dtype) for a in (q["Qx"], c["Kx"], c["V"]))
+    n = 256
+    while True:
+        n = min(n, w.N)
+        t0 = time.perf_counter()
+        oracle.cross_head(Q[:n], Ky, Vy, q["mu"][0], q["rho"][0], q["alpha"][0], w.var_floor, w.eps)
+        if time.perf_counter() - t0 >= seconds / 4 or n == w.N:
+            break
+        n *= 2
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        oracle.cross_head(Q[:n], Ky, Vy, q["mu"][0], q["rho"][0], q["alpha"][0], w.var_floor, w.eps)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    return n / dt, n, reps, dt
+
+
+def run_cross(args, rank, world, local):
+    """Cross-attention (sections 3.1, 6): one step is one gma_forward_cross call, the workload's
+    queries [B, H, N, d] reading the memory of a context of --context rows (the write over the
+    context, the read over the queries)."""
+    import torch
+    import gaussian_mixture_latent_gb300 as gma
+    from gaussian_mixture_latent_gb300 import _build
+    w = inputs.WORKLOADS[args.workload]
+    Nkv = args.context or 4 * w.N
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        rate, n, reps, dt = cross_oracle_sample(w, Nkv, 12.0)
+        sample = f"head 0: the first {n} queries of {w.name} reading a {Nkv}-row context, {reps} calls, one thread"
+        print(json.dumps({"impl": "reference", "metric": CROSS_METRIC, "value": rate, "unit": "tokens·heads/s",
+                          "n_gpus": args.gpus, "steps": reps, "warmup": 0, "ms_per_step": dt * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": {"workload": w.name, "context": Nkv,
+                                                          "step": "cross-attention (sampled)"},
+                          "cpu_baseline": {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
+                                           "sample": sample},
+                          "e2e": {"value": rate, "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    sets = []
+    for seed in (0, 1):
+        q = inputs.gen_all(w.replace(seed=seed))
+        c = inputs.gen_all(w.replace(N=Nkv, seed=seed + 1000))
+        sets.append({"Qx": to_dev(q["Qx"]), "Ky": to_dev(c["Kx"]), "Vy": to_dev(c["V"]),
+                     **{k: to_dev(q[k]) for k in ("mu", "rho", "alpha")}})
+    out = torch.empty((w.B, w.H, w.N, w.dv), dtype=sets[0]["Qx"].dtype, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(x):
+        gma.gma_forward_cross(x["Qx"], x["Ky"], x["Vy"], x["mu"], x["rho"], x["alpha"], eps=w.eps,
+                              var_floor=w.var_floor, out=out)
+
+    for it in range(max(3, args.warmup)):
+        step(sets[it % 2])
+    torch.cuda.synchronize()
+    if gma.gma_get_status():
+        raise RuntimeError("device status after warm-up")
+    steps = args.steps if args.steps is not None else 100
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(gpu_id_for(local))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda._sleep(int(2.0e6 * 20))                     # let the host enqueue ahead of the GPU
+    for it in range(steps):
+        evs[it][0].record(stream)
+        step(sets[it % 2])
+        evs[it][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if gma.gma_get_status():
+        raise RuntimeError("device status after the timed region")
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), device=dev)
+    units = w.B * w.H * w.N
+    value = whole_job_rate(units, world, ms)
+    pk = peaks()
+    e = 2
+    bytes_alg = w.B * w.H * (w.N * e * (w.d + w.dv) + Nkv * e * (w.d + w.dv))
+    achieved = bytes_alg / (ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                "kernel": "tc_params + tc_write + tc_reduce + tc_read (whole call)", "kernel_ms": ms,
+                "peak_source": pk["source"]}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, n, reps, dt = cross_oracle_sample(w, Nkv, 12.0)
+        cpu = {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
+               "sample": f"head 0: the first {n} queries of {w.name} reading a {Nkv}-row context, {reps} calls"}
+    if rank == 0:
+        print(json.dumps({"metric": CROSS_METRIC, "value": value, "unit": "tokens·heads/s", "n_gpus": world,
+                          "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                          "data": "synthetic",
+                          "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "context": Nkv, "d": w.d,
+                                     "K": w.K, "dv": w.dv, "step": "cross-attention forward",
+                                     "l2": "two alternating input sets",
+                                     "parallelism": "replicas" if world > 1 else "single GPU"},
+                          "roofline": roofline, "clocks": clocks, "gpu_launches": 4 * steps,
+                          "cpu_baseline": cpu}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.direction == "diagnostics":
         return run_diagnostics(args, rank, world, local)
+    if args.direction == "cross":
+        return run_cross(args, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_gpu(args, rank, world, local)
