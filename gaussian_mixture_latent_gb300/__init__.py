@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "GmaError", "gma_desc", "gma_workspace_size", "gma_workspace_init", "gma_forward",
     "gma_forward_ex", "gma_forward_plan",
-    "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_get_status", "gma_status_string", "gma_version",
+    "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_decode", "gma_get_status", "gma_status_string", "gma_version",
     "Workspace", "library_path",
 ]
 
@@ -74,6 +74,8 @@ def _load():
     lib.gma_diagnostics.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gma_cross_workspace_size.argtypes = [dp, i, ctypes.POINTER(sz)]
     lib.gma_forward_cross.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, f, vp, vp, sz, vp]
+    lib.gma_decode_workspace_size.argtypes = [dp, ctypes.POINTER(sz)]
+    lib.gma_decode.argtypes = [dp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp, sz, vp]
     lib.gma_get_status.argtypes = [vp, vp]
     lib.gma_status_string.argtypes = [i]
     lib.gma_status_string.restype = ctypes.c_char_p
@@ -81,7 +83,7 @@ def _load():
     for fn in (lib.gma_workspace_size, lib.gma_workspace_init, lib.gma_forward,
                lib.gma_forward_ex, lib.gma_forward_plan, lib.gma_responsibilities, lib.gma_get_status, lib.gma_version,
                lib.gma_diagnostics_workspace_size, lib.gma_diagnostics, lib.gma_cross_workspace_size,
-               lib.gma_forward_cross):
+               lib.gma_forward_cross, lib.gma_decode_workspace_size, lib.gma_decode):
         fn.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -271,6 +273,38 @@ def gma_forward_cross(Qx, Ky, Vy, mu, rho, pi_logits, eps: float = 1e-6, var_flo
                                    _stream_ptr(stream))
     if rc:
         raise GmaError(rc, "gma_forward_cross")
+    return out
+
+
+def gma_decode(Qx, Kx, V, mu, rho, pi_logits, state, eps: float = 1e-6, var_floor: float = 1e-4, out=None,
+               workspace=None, stream=None):
+    """Causal decode with a carried state (section 3.5, Eq. 6b / 8b as a recurrence): appends the
+    N new positions of Qx, Kx [B,H,N,d], V [B,H,N,dv] to each head's sequence.  `state`
+    [B,H,K,dv+1] float32 holds [S | z] of the positions so far and is updated in place;
+    returns out [B,H,N,dv]."""
+    B, H, N, d = Qx.shape
+    dv = V.shape[3]
+    K = mu.shape[1]
+    _check(Qx, "Qx", (B, H, N, d), (torch.float32, torch.bfloat16))
+    _check(Kx, "Kx", (B, H, N, d), (Qx.dtype,))
+    _check(V, "V", (B, H, N, dv), (Qx.dtype,))
+    _check(mu, "mu", (H, K, d), (torch.float32,))
+    _check(rho, "rho", (H, K, d), (torch.float32,))
+    _check(pi_logits, "pi_logits", (H, K), (torch.float32,))
+    _check(state, "state", (B, H, K, dv + 1), (torch.float32,))
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=Qx.dtype, device=Qx.device)
+    _check(out, "out", (B, H, N, dv), (torch.float32, torch.bfloat16))
+    desc = _make_desc(B, H, N, d, K, dv, Qx.dtype, out.dtype, var_floor, 0)
+    nbytes = ctypes.c_size_t(0)
+    rc = _load().gma_decode_workspace_size(ctypes.byref(desc), ctypes.byref(nbytes))
+    if rc:
+        raise GmaError(rc, "gma_decode_workspace_size")
+    ws = _workspace_for(Qx.device, nbytes.value, workspace, stream)
+    rc = _load().gma_decode(ctypes.byref(desc), _ptr(Qx), _ptr(Kx), _ptr(V), _ptr(mu), _ptr(rho), _ptr(pi_logits),
+                            float(eps), _ptr(state), _ptr(out), _ptr(ws), ws.numel(), _stream_ptr(stream))
+    if rc:
+        raise GmaError(rc, "gma_decode")
     return out
 
 

@@ -232,6 +232,39 @@ gma_status gma_forward_cross(const gma_desc *desc, int Nkv, const void *Qx, cons
     return tc_read(p, L, Qx, out, ws, s) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
+gma_status gma_decode_workspace_size(const gma_desc *desc, size_t *bytes) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!bytes) return GMA_ERR_INVALID_ARG;
+    const Problem p = make_problem(desc, 1, 0.f);
+    if (!decode_supported(p)) return GMA_ERR_UNSUPPORTED;
+    *bytes = decode_layout(p).total;
+    return GMA_OK;
+}
+
+gma_status gma_decode(const gma_desc *desc, const void *Qx, const void *Kx, const void *V, const float *mu,
+                      const float *rho, const float *pi_logits, float eps, float *state, void *out,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!(eps >= 0.f) || !std::isfinite(eps) || !mu || !rho || !pi_logits || !state) return GMA_ERR_INVALID_ARG;
+    if (desc->N > 0 && (!Qx || !Kx || !V || !out)) return GMA_ERR_INVALID_ARG;
+    const void *ptrs[] = {Qx, Kx, V, out, mu, rho, pi_logits, state, workspace};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
+    const Problem p = make_problem(desc, 1, eps);
+    if (!decode_supported(p)) return GMA_ERR_UNSUPPORTED;
+    const DecodeLayout L = decode_layout(p);
+    if (!workspace || workspace_bytes < L.total) return GMA_ERR_WORKSPACE;
+    if (p.N == 0) return GMA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    float *lam = reinterpret_cast<float *>(ws + L.lam);
+    float *cdir = reinterpret_cast<float *>(ws + L.cdir);
+    if (simt_params(p, rho, pi_logits, lam, cdir, s) != cudaSuccess) return GMA_ERR_CUDA;
+    return decode_step(p, Qx, Kx, V, mu, lam, cdir, state, out, s) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
 gma_status gma_forward_plan(const gma_desc *desc, int causal, int *n_launches, const char **names,
                             int capacity) {
     gma_status st = validate_desc(desc);

@@ -82,6 +82,15 @@ cudaError_t tc_diag(const Problem &p, const TcLayout &L, const void *Qx, int *z,
 cudaError_t tc_diag_finalize(const Problem &p, const TcLayout &L, float *p_out, float *stats_out, char *ws,
                              cudaStream_t s);
 
+// ----- causal decode with a carried state: gma_decode.cu (uses simt_params) -----
+struct DecodeLayout {
+    size_t lam, cdir, total;
+};
+bool decode_supported(const Problem &p);
+DecodeLayout decode_layout(const Problem &p);
+cudaError_t decode_step(const Problem &p, const void *Qx, const void *Kx, const void *V, const float *mu,
+                        const float *lam, const float *cdir, float *state, void *out, cudaStream_t s);
+
 // ----- SIMT (CUDA-core, fp32) path: gma_simt.cu -----
 cudaError_t simt_params(const Problem &p, const float *rho, const float *alpha, float *lam,
                         float *cdir, cudaStream_t s);

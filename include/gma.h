@@ -124,6 +124,26 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Causal decode with a carried state ("Gaussian Mixture Attention", section
+ * 3.5, Eq. 6b and 8b as a recurrence): appends desc->N new positions to each
+ * head's causal sequence.  state [B, H, K, dv + 1] float32, in and out, holds
+ * [S | z] = sum over the positions so far of gamma^K_j [V_j | 1] (zeros for an
+ * empty prefix).  For each new position t, in order:
+ *   [S | z] += gamma^K(Kx_t) [V_t | 1]                   (the prefix includes t)
+ *   out_t    = gamma^Q(Qx_t) S / (gamma^Q(Qx_t) z + eps)
+ * Qx, Kx [B, H, N, d] and V [B, H, N, dv] in in_dtype, out [B, H, N, dv] in
+ * out_dtype; responsibilities in fp32 from the direct form of Eq. 16.  Any
+ * shape whose per-head state fits a CTA's shared memory (K (dv + 1) floats,
+ * about 200 KB); GMA_ERR_UNSUPPORTED otherwise.  Workspace:
+ * gma_decode_workspace_size().  The state is read and written on `stream`;
+ * calls on one state must be ordered on one stream.
+ */
+gma_status gma_decode_workspace_size(const gma_desc *desc, size_t *bytes);
+gma_status gma_decode(const gma_desc *desc, const void *Qx, const void *Kx, const void *V, const float *mu,
+                      const float *rho, const float *pi_logits, float eps, float *state, void *out,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Cross-attention GMA ("Gaussian Mixture Attention", section 3.1 and section 6):
  * the queries Qx [B, H, N, d] of one sequence read the latent memory of a
  * context sequence, Ky [B, H, Nkv, d] and Vy [B, H, Nkv, dv], through the head's
