@@ -49,10 +49,11 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics", "cross"], default="both",
+    ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics", "cross", "decode"], default="both",
                     help="which forward(s) one step runs (default: both, the headline step); "
                          "diagnostics: one step is gma_diagnostics over the workload's query vectors; "
-                         "cross: one step is gma_forward_cross, the workload's queries reading a context")
+                         "cross: one step is gma_forward_cross, the workload's queries reading a context; "
+                         "decode: one step is gma_decode of one new token for every head")
     ap.add_argument("--context", type=int, default=0,
                     help="context length of --direction cross (default: 4 x the workload's N)")
     return ap.parse_args()
@@ -779,9 +780,112 @@ def run_cross(args, rank, world, local):
     return 0
 
 
+DECODE_METRIC = "GMA causal decode token·heads/s (one new token per head, carried state, Eq. 6b/8b)"
+
+
+def decode_oracle_sample(w, seconds):
+    """The oracle's causal recurrence, one token per head (sampled: 16 heads), timed as the
+    cost of extending a sequence by one position from its memory."""
+    import oracle
+    oracle.build()
+    x = inputs.gen_all(w.replace(B=1, H=min(w.H, 16), N=1))
+    H = x["Qx"].shape[1]
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for h in range(H):
+            oracle.forward_head(*(inputs.widen(x[n][0, h], w.dtype) for n in ("Qx", "Kx", "V")), x["mu"][h],
+                                x["rho"][h], x["alpha"][h], w.var_floor, w.eps, True)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    return H / dt, H, reps, dt
+
+
+def run_decode(args, rank, world, local):
+    """Causal decode (section 3.5): one step is one gma_decode call appending one token to every
+    head of the workload (B x H heads) from a carried state."""
+    import torch
+    import gaussian_mixture_latent_gb300 as gma
+    from gaussian_mixture_latent_gb300 import _build
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        rate, H, reps, dt = decode_oracle_sample(w, 5.0)
+        print(json.dumps({"impl": "reference", "metric": DECODE_METRIC, "value": rate, "unit": "tokens·heads/s",
+                          "n_gpus": args.gpus, "steps": reps, "warmup": 0, "ms_per_step": dt * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": {"workload": w.name, "step": "decode (sampled)"},
+                          "cpu_baseline": {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
+                                           "sample": f"{H} heads, one token each, {reps} passes"},
+                          "e2e": {"value": rate, "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+    steps = args.steps if args.steps is not None else 500
+    x = inputs.gen_all(w.replace(N=steps + 8))
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    d = {n: to_dev(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha")}
+    toks = [{n: d[n][:, :, t:t + 1].contiguous() for n in ("Qx", "Kx", "V")} for t in range(steps + 8)]
+    state = torch.zeros((w.B, w.H, w.K, w.dv + 1), dtype=torch.float32, device=dev)
+    out = torch.empty((w.B, w.H, 1, w.dv), dtype=d["Qx"].dtype, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(t):
+        gma.gma_decode(toks[t]["Qx"], toks[t]["Kx"], toks[t]["V"], d["mu"], d["rho"], d["alpha"], state,
+                       eps=w.eps, var_floor=w.var_floor, out=out)
+
+    for t in range(8):                                     # warm-up: the first 8 tokens
+        step(t)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(gpu_id_for(local))
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda._sleep(int(2.0e6 * 40))                     # let the host enqueue ahead of the GPU
+    for t in range(steps):
+        evs[t][0].record(stream)
+        step(8 + t)
+        evs[t][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if gma.gma_get_status():
+        raise RuntimeError("device status after the timed region")
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    pk = peaks()
+    e = 2 if w.dtype == "bf16" else 4
+    bytes_alg = w.B * w.H * (2 * 4 * w.K * (w.dv + 1) + e * (2 * w.d + 2 * w.dv)) + 4 * w.H * w.K * (2 * w.d + 1)
+    achieved = bytes_alg / (ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, H, reps, dt = decode_oracle_sample(w, 5.0)
+        cpu = {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
+               "sample": f"{H} heads, one token each, {reps} passes"}
+    print(json.dumps({"metric": DECODE_METRIC, "value": w.B * w.H / (ms / 1e3), "unit": "tokens·heads/s",
+                      "n_gpus": 1, "steps": steps, "warmup": 8, "ms_per_step": ms, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                      "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "K": w.K, "dv": w.dv,
+                                 "step": "decode one token per head (median call time)"},
+                      "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                   "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                                   "kernel": "decode (one launch)", "kernel_ms": ms,
+                                   "peak_source": pk["source"]},
+                      "clocks": clocks, "gpu_launches": steps, "cpu_baseline": cpu}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.direction == "decode":
+        return run_decode(args, rank, world, local)
     if args.direction == "diagnostics":
         return run_diagnostics(args, rank, world, local)
     if args.direction == "cross":

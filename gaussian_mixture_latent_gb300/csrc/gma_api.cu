@@ -9,10 +9,36 @@
 #include <cstdint>
 #include <cstring>
 #include <functional>
+#include <mutex>
+#include <vector>
 
 #include "gma_internal.h"
 
 namespace gma {
+
+cudaError_t set_dyn_smem(const void *kern, int bytes) {
+    struct Entry {
+        const void *kern;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> seen;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (Entry &x : seen)
+        if (x.kern == kern && x.dev == dev) {
+            if (x.bytes >= bytes) return cudaSuccess;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (e == cudaSuccess) x.bytes = bytes;
+            return e;
+        }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) seen.push_back({kern, dev, bytes});
+    return e;
+}
+
 namespace {
 
 constexpr size_t kMaxDynSmem = 227 * 1024;
@@ -238,7 +264,7 @@ gma_status gma_decode_workspace_size(const gma_desc *desc, size_t *bytes) {
     if (!bytes) return GMA_ERR_INVALID_ARG;
     const Problem p = make_problem(desc, 1, 0.f);
     if (!decode_supported(p)) return GMA_ERR_UNSUPPORTED;
-    *bytes = decode_layout(p).total;
+    *bytes = decode_workspace(p);
     return GMA_OK;
 }
 
@@ -254,15 +280,12 @@ gma_status gma_decode(const gma_desc *desc, const void *Qx, const void *Kx, cons
         if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
     const Problem p = make_problem(desc, 1, eps);
     if (!decode_supported(p)) return GMA_ERR_UNSUPPORTED;
-    const DecodeLayout L = decode_layout(p);
-    if (!workspace || workspace_bytes < L.total) return GMA_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < decode_workspace(p)) return GMA_ERR_WORKSPACE;
     if (p.N == 0) return GMA_OK;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    char *ws = static_cast<char *>(workspace);
-    float *lam = reinterpret_cast<float *>(ws + L.lam);
-    float *cdir = reinterpret_cast<float *>(ws + L.cdir);
-    if (simt_params(p, rho, pi_logits, lam, cdir, s) != cudaSuccess) return GMA_ERR_CUDA;
-    return decode_step(p, Qx, Kx, V, mu, lam, cdir, state, out, s) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+    return decode_step(p, Qx, Kx, V, mu, rho, pi_logits, state, out, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? GMA_OK
+               : GMA_ERR_CUDA;
 }
 
 gma_status gma_forward_plan(const gma_desc *desc, int causal, int *n_launches, const char **names,

@@ -41,6 +41,11 @@ struct SimtLayout {
 };
 SimtLayout simt_layout(const Problem &p);
 
+// Raise a kernel's dynamic shared-memory limit on the current device to `bytes`:
+// the attribute is set the first time a (kernel, device) pair needs that much
+// and remembered, so steady-state launches make no attribute call (gma_api.cu).
+cudaError_t set_dyn_smem(const void *kern, int bytes);
+
 // ----- tensor-core bidirectional path: gma_tc.cu -----
 constexpr int kMaxCtas = 256;        // upper bound on persistent CTAs (partial slots are sized for it)
 struct TcLayout {
@@ -82,14 +87,11 @@ cudaError_t tc_diag(const Problem &p, const TcLayout &L, const void *Qx, int *z,
 cudaError_t tc_diag_finalize(const Problem &p, const TcLayout &L, float *p_out, float *stats_out, char *ws,
                              cudaStream_t s);
 
-// ----- causal decode with a carried state: gma_decode.cu (uses simt_params) -----
-struct DecodeLayout {
-    size_t lam, cdir, total;
-};
+// ----- causal decode with a carried state: gma_decode.cu (one launch) -----
 bool decode_supported(const Problem &p);
-DecodeLayout decode_layout(const Problem &p);
+size_t decode_workspace(const Problem &p);
 cudaError_t decode_step(const Problem &p, const void *Qx, const void *Kx, const void *V, const float *mu,
-                        const float *lam, const float *cdir, float *state, void *out, cudaStream_t s);
+                        const float *rho, const float *alpha, float *state, void *out, cudaStream_t s);
 
 // ----- SIMT (CUDA-core, fp32) path: gma_simt.cu -----
 cudaError_t simt_params(const Problem &p, const float *rho, const float *alpha, float *lam,

@@ -415,7 +415,7 @@ cudaError_t causal_t(const Problem &p, const void *V, char *ws, const SimtLayout
     const int rpp = (p.N + L.P - 1) / L.P;
     const size_t smem = sizeof(float) * ((size_t)p.K * W + 2 * C * p.K + C * W + C * C + C * W);
     auto kern = causal_chunk_kernel<T, Tout>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(L.P, p.G);
     kern<<<grid, 256, smem, s>>>(p.N, p.K, p.dv, L.P, rpp, p.eps,

@@ -681,7 +681,7 @@ cudaError_t launch_write(const Problem &p, const TcLayout &L, const void *Kx, co
     a.partials = reinterpret_cast<float *>(ws + L.part);
     a.status = reinterpret_cast<unsigned *>(ws);
     auto kern = tc_write_kernel<K>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WriteCfg<K>::BYTES);
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), WriteCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, dim3(L.ncta_kv), dim3(WriteCfg<K>::THREADS), WriteCfg<K>::BYTES, s, tk, tv, a);
 }
@@ -698,7 +698,7 @@ cudaError_t launch_read(const Problem &p, const TcLayout &L, const void *Qx, voi
     a.eps = p.eps;
     a.status = reinterpret_cast<unsigned *>(ws);
     auto kern = tc_read_kernel<K>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ReadCfg<K>::BYTES);
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), ReadCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, dim3(L.ncta), dim3(ReadCfg<K>::THREADS), ReadCfg<K>::BYTES, s, tq, to, a);
 }

@@ -712,7 +712,7 @@ static cudaError_t launch_causal(const Problem &p, const TcLayout &L, const void
         a.var_floor = p.var_floor;
     }
     auto kern = slices ? tc_causal_kernel<true> : tc_causal_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CausalCfg::BYTES);
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), CausalCfg::BYTES);
     if (e != cudaSuccess) return e;
     if (!slices) {
         // the first kernel of its forward: an ordinary launch, so that every input is final when

@@ -380,7 +380,7 @@ cudaError_t launch_diag(const Problem &p, const TcLayout &L, const void *Qx, int
     a.z = z;
     a.status = reinterpret_cast<unsigned *>(ws);
     auto kern = tc_diag_kernel<K>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DiagCfg<K>::BYTES);
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), DiagCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, dim3(L.ncta), dim3(kDiagThreads), DiagCfg<K>::BYTES, s, tq, a);
 }

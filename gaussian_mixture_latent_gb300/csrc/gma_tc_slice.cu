@@ -314,7 +314,7 @@ cudaError_t launch_rowstats(const Problem &p, const TcLayout &L, const void *Qx,
     a.lse_k = a.mrow_q + (size_t)p.G * p.N;
     a.status = reinterpret_cast<unsigned *>(ws);
     auto kern = tc_rowstats_kernel<K>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, StatCfg<K>::BYTES);
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), StatCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
     const int ncta = std::max(1, std::min(sm_count() > 0 ? sm_count() : kMaxCtas, a.Ttot));
     return launch_dependent(kern, dim3(ncta), dim3(kStatThreads), StatCfg<K>::BYTES, s, tq, tk, a);

@@ -133,8 +133,9 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
  *   out_t    = gamma^Q(Qx_t) S / (gamma^Q(Qx_t) z + eps)
  * Qx, Kx [B, H, N, d] and V [B, H, N, dv] in in_dtype, out [B, H, N, dv] in
  * out_dtype; responsibilities in fp32 from the direct form of Eq. 16.  Any
- * shape whose per-head state fits a CTA's shared memory (K (dv + 1) floats,
- * about 200 KB); GMA_ERR_UNSUPPORTED otherwise.  Workspace:
+ * shape whose per-head state and precisions fit a CTA's shared memory
+ * (K (dv + 1 + d) floats, about 220 KB); GMA_ERR_UNSUPPORTED otherwise.  The
+ * workspace holds only the status word.  Workspace:
  * gma_decode_workspace_size().  The state is read and written on `stream`;
  * calls on one state must be ordered on one stream.
  */
