@@ -6,7 +6,8 @@ benchmark's CPU-baseline leg may import this package; the product path
 
 The arithmetic lives in ``gma_oracle.c`` (double precision, written from the
 equations of "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
-Probabilistic Latent Routing", section 3 -- Eqs. 3, 3b, 5-8, 6b, 8b, 14-16).
+Probabilistic Latent Routing", section 3 -- Eqs. 3, 3b, 5-8, 6b, 8b, 14-16 -- and,
+for the backward pass, section 4.1 -- Eqs. 17-20).
 This module only marshals numpy arrays into it.
 
 Every function here is pinned by ``tests/test_oracle.py`` against things the
@@ -54,9 +55,11 @@ def _load():
         lib.gma_oracle_diagnostics.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, d, _dp, _dp,
                                                ctypes.POINTER(ctypes.c_int)]
         lib.gma_oracle_cross_head.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d, d, _dp]
+        lib.gma_oracle_backward_head.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d, d, i, _dp,
+                                                 _dp, _dp, _dp, _dp, _dp, _dp]
         for fn in (lib.gma_oracle_scores, lib.gma_oracle_responsibilities,
                    lib.gma_oracle_forward_head, lib.gma_oracle_forward, lib.gma_oracle_diagnostics,
-                   lib.gma_oracle_cross_head):
+                   lib.gma_oracle_cross_head, lib.gma_oracle_backward_head):
             fn.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -158,3 +161,20 @@ def cross_head(Qx, Ky, Vy, mu, omega, alpha, var_floor: float, eps: float) -> np
     _check(_load().gma_oracle_cross_head(Nq, Nkv, d, K, dv, _p(Qx), _p(Ky), _p(Vy), _p(mu), _p(omega),
                                          _p(alpha), float(var_floor), float(eps), _p(out)), "cross_head")
     return out
+
+
+def backward_head(Qx, Kx, V, mu, omega, alpha, var_floor: float, eps: float, causal: bool, dO):
+    """Backward pass of one head (section 4.1, Eqs. 17-20, with Eqs. 14-15 and the memory
+    products of Eqs. 5-8 / 6b, 8b): given dO = dL/dO [N, dv], returns the dict of
+    dL/dQx, dL/dKx [N, d], dL/dV [N, dv], dL/dmu, dL/domega [K, d], dL/dalpha [K]."""
+    Qx, Kx, V, mu, omega, alpha, dO = map(_c, (Qx, Kx, V, mu, omega, alpha, dO))
+    N, d = Qx.shape
+    K = mu.shape[0]
+    dv = V.shape[1]
+    g = {"Qx": np.empty((N, d)), "Kx": np.empty((N, d)), "V": np.empty((N, dv)),
+         "mu": np.empty((K, d)), "omega": np.empty((K, d)), "alpha": np.empty((K,))}
+    _check(_load().gma_oracle_backward_head(N, d, K, dv, _p(Qx), _p(Kx), _p(V), _p(mu), _p(omega),
+                                            _p(alpha), float(var_floor), float(eps), int(causal), _p(dO),
+                                            _p(g["Qx"]), _p(g["Kx"]), _p(g["V"]), _p(g["mu"]),
+                                            _p(g["omega"]), _p(g["alpha"])), "backward_head")
+    return g

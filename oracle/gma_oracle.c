@@ -368,3 +368,158 @@ done:
     free(Z);
     return rc;
 }
+
+/*
+ * One head of the backward pass: gradients of a loss L with respect to Qx, Kx,
+ * V, mu, omega and alpha, given dO = dL/dO.  Section 4.1 fixes its structure
+ * (the extraction of the paper lacks Appendix D): the upstream gradient g at a
+ * responsibility vector enters the scores through the softmax Jacobian,
+ * Eq. (17)-(18), ds_{i,k} = gamma_{i,k} (g_{i,k} - sum_j gamma_{i,j} g_{i,j});
+ * every quantity that enters a score then collects sum_i sum_k ds_{i,k}
+ * ds_{i,k}/dtheta, Eq. (19), with the score of Eq. (16) differentiated by hand:
+ *   d s_{i,k} / d mu_k      =  Sigma_k^{-1} (x_i - mu_k)                 Eq. (20)
+ *   d s_{i,k} / d x_i       = -Sigma_k^{-1} (x_i - mu_k)                 section 4.3
+ *   d s_{i,k} / d var_{k,m} = (1/2) ((x_im - mu_km)^2 / var_km^2 - 1 / var_km)
+ *   d s_{i,k} / d log pi_k  = 1
+ * then var through Eq. (14) (d softplus / d omega = sigmoid(omega)) and
+ * log pi through Eq. (15) (the log-softmax Jacobian).  The memory operations
+ * are differentiated as the products they are: with den_i = gamma^Q_i . Z + eps
+ * and O_i = gamma^Q_i Vt / den_i (Eq. 7-8), a_i = dO_i / den_i and
+ * b_i = -(dO_i . O_i) / den_i give
+ *   g^Q_i = Vt a_i + Z b_i,
+ *   R = sum_i gamma^Q_i a_i^T,  r = sum_i gamma^Q_i b_i   (over the rows that read the memory),
+ *   g^K_j = R v_j + r,  dV_j = R^T gamma^K_j.
+ * causal = 1 uses the prefix memory of Eq. (6b)/(8b): row i reads the memory of
+ * rows j <= i, so key j collects R and r over the rows i >= j (a suffix sum).
+ * Every output is overwritten.  Layouts as for the forward: dQx, dKx [N, d],
+ * dV [N, dv], dmu, domega [K, d], dalpha [K].
+ */
+int gma_oracle_backward_head(int N, int d, int K, int dv, const double *Qx, const double *Kx,
+                             const double *V, const double *mu, const double *omega,
+                             const double *alpha, double var_floor, double eps, int causal,
+                             const double *dO, double *dQx, double *dKx, double *dV, double *dmu,
+                             double *domega, double *dalpha)
+{
+    if (N < 0 || d <= 0 || K <= 0 || dv <= 0) return 1;
+    size_t nk = (size_t)N * K, kdv = (size_t)K * dv, kd = (size_t)K * d;
+    double *gq = (double *)malloc(sizeof(double) * (nk ? nk : 1));
+    double *gk = (double *)malloc(sizeof(double) * (nk ? nk : 1));
+    double *dgq = (double *)calloc(nk ? nk : 1, sizeof(double));
+    double *dgk = (double *)calloc(nk ? nk : 1, sizeof(double));
+    double *a = (double *)calloc((size_t)(N ? N : 1) * dv, sizeof(double));
+    double *b = (double *)calloc(N ? N : 1, sizeof(double));
+    double *Vt = (double *)calloc(kdv, sizeof(double));
+    double *Z = (double *)calloc(K, sizeof(double));
+    double *R = (double *)calloc(kdv, sizeof(double));
+    double *r = (double *)calloc(K, sizeof(double));
+    double *var = (double *)malloc(sizeof(double) * kd);
+    double *dvar = (double *)calloc(kd, sizeof(double));
+    double *dlogpi = (double *)calloc(K, sizeof(double));
+    double *logpi = (double *)malloc(sizeof(double) * K);
+    int rc = 2;
+    if (!gq || !gk || !dgq || !dgk || !a || !b || !Vt || !Z || !R || !r || !var || !dvar || !dlogpi || !logpi)
+        goto done;
+    rc = gma_oracle_responsibilities(N, d, K, Qx, mu, omega, alpha, var_floor, gq);
+    if (rc) goto done;
+    rc = gma_oracle_responsibilities(N, d, K, Kx, mu, omega, alpha, var_floor, gk);
+    if (rc) goto done;
+    for (size_t e = 0; e < kd; ++e) var[e] = variance_from_omega(omega[e], var_floor);
+    log_priors(K, alpha, logpi);
+
+    /* Eq. (5)-(6) over the whole sequence (bidirectional); the causal memory grows below. */
+    if (!causal)
+        for (int j = 0; j < N; ++j)
+            for (int k = 0; k < K; ++k) {
+                double g = gk[(size_t)j * K + k];
+                Z[k] += g;
+                for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += g * V[(size_t)j * dv + c];
+            }
+    /* the read of each row (Eq. 7-8 or 8b) and its gradient with respect to gamma^Q_i */
+    for (int i = 0; i < N; ++i) {
+        if (causal)
+            for (int k = 0; k < K; ++k) {
+                double g = gk[(size_t)i * K + k];
+                Z[k] += g;
+                for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += g * V[(size_t)i * dv + c];
+            }
+        const double *gi = gq + (size_t)i * K;
+        double den = eps;
+        for (int k = 0; k < K; ++k) den += gi[k] * Z[k];
+        double dot = 0.0;
+        for (int c = 0; c < dv; ++c) {
+            double num = 0.0;
+            for (int k = 0; k < K; ++k) num += gi[k] * Vt[(size_t)k * dv + c];
+            dot += dO[(size_t)i * dv + c] * (num / den);
+            a[(size_t)i * dv + c] = dO[(size_t)i * dv + c] / den;
+        }
+        b[i] = -dot / den;
+        for (int k = 0; k < K; ++k) {
+            double g = Z[k] * b[i];
+            for (int c = 0; c < dv; ++c) g += Vt[(size_t)k * dv + c] * a[(size_t)i * dv + c];
+            dgq[(size_t)i * K + k] = g;
+        }
+    }
+    /* R, r over the rows that read key j's memory; g^K_j and dV_j */
+    if (!causal)
+        for (int i = 0; i < N; ++i)
+            for (int k = 0; k < K; ++k) {
+                double g = gq[(size_t)i * K + k];
+                r[k] += g * b[i];
+                for (int c = 0; c < dv; ++c) R[(size_t)k * dv + c] += g * a[(size_t)i * dv + c];
+            }
+    for (int j = N - 1; j >= 0; --j) {
+        if (causal)
+            for (int k = 0; k < K; ++k) {
+                double g = gq[(size_t)j * K + k];
+                r[k] += g * b[j];
+                for (int c = 0; c < dv; ++c) R[(size_t)k * dv + c] += g * a[(size_t)j * dv + c];
+            }
+        for (int k = 0; k < K; ++k) {
+            double g = r[k];
+            for (int c = 0; c < dv; ++c) g += R[(size_t)k * dv + c] * V[(size_t)j * dv + c];
+            dgk[(size_t)j * K + k] = g;
+        }
+        for (int c = 0; c < dv; ++c) {
+            double s = 0.0;
+            for (int k = 0; k < K; ++k) s += R[(size_t)k * dv + c] * gk[(size_t)j * K + k];
+            dV[(size_t)j * dv + c] = s;
+        }
+    }
+    /* Eq. (18) then Eq. (19)-(20) for the query rows and the key rows alike */
+    for (size_t e = 0; e < kd; ++e) dmu[e] = 0.0;
+    for (int side = 0; side < 2; ++side) {
+        const double *X = side ? Kx : Qx;
+        const double *gam = side ? gk : gq;
+        const double *dg = side ? dgk : dgq;
+        double *dX = side ? dKx : dQx;
+        for (int i = 0; i < N; ++i) {
+            const double *gi = gam + (size_t)i * K, *dgi = dg + (size_t)i * K;
+            double mean = 0.0;
+            for (int k = 0; k < K; ++k) mean += gi[k] * dgi[k];
+            for (int m = 0; m < d; ++m) dX[(size_t)i * d + m] = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double ds = gi[k] * (dgi[k] - mean);
+                dlogpi[k] += ds;
+                for (int m = 0; m < d; ++m) {
+                    double diff = X[(size_t)i * d + m] - mu[(size_t)k * d + m];
+                    double vk = var[(size_t)k * d + m];
+                    dX[(size_t)i * d + m] -= ds * diff / vk;
+                    dmu[(size_t)k * d + m] += ds * diff / vk;
+                    dvar[(size_t)k * d + m] += ds * 0.5 * (diff * diff / (vk * vk) - 1.0 / vk);
+                }
+            }
+        }
+    }
+    /* Eq. (14): d var / d omega = sigmoid(omega); Eq. (15): the log-softmax Jacobian */
+    for (size_t e = 0; e < kd; ++e) domega[e] = dvar[e] / (1.0 + exp(-omega[e]));
+    {
+        double tot = 0.0;
+        for (int k = 0; k < K; ++k) tot += dlogpi[k];
+        for (int k = 0; k < K; ++k) dalpha[k] = dlogpi[k] - exp(logpi[k]) * tot;
+    }
+    rc = 0;
+done:
+    free(gq); free(gk); free(dgq); free(dgk); free(a); free(b); free(Vt); free(Z); free(R); free(r);
+    free(var); free(dvar); free(dlogpi); free(logpi);
+    return rc;
+}

@@ -407,3 +407,84 @@ def test_cross_context_order_does_not_matter_and_queries_are_independent():
                                rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(oracle.cross_head(Qx[:5], Ky, Vy, mu, omega, alpha, 1e-4, 1e-6), base[:5],
                                rtol=1e-12, atol=1e-14)
+
+
+# ---- backward pass (section 4.1, Eqs. 17-20; Eqs. 14-15 for the reparameterised parameters) ----
+
+BWD_INPUTS = ("Qx", "Kx", "V", "mu", "omega", "alpha")
+
+
+def loss_brute_force(x, dO, var_floor, eps, causal):
+    """L = sum(dO * O) with O from the explicit affinity of Eq. (9)-(10) / (9b)-(10b)
+    and scipy's densities: shares no code with the oracle."""
+    O, _, _ = brute_force(x["Qx"], x["Kx"], x["V"], x["mu"], x["omega"], x["alpha"], var_floor, eps, causal)
+    return float((dO * O).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_central_differences_of_the_explicit_affinity(causal):
+    # every input entry perturbed in turn; eps large enough that its placement matters
+    var_floor, eps, h = 1e-3, 0.1, 1e-5
+    x = make(N=6, d=2, K=3, dv=2, seed=21 + causal)
+    dO = np.random.default_rng(5).normal(size=(6, 2))
+    g = oracle.backward_head(x["Qx"], x["Kx"], x["V"], x["mu"], x["omega"], x["alpha"], var_floor, eps,
+                             causal, dO)
+    for name in BWD_INPUTS:
+        fd = np.zeros_like(x[name])
+        for idx in np.ndindex(x[name].shape):
+            xp = {k: v.copy() for k, v in x.items()}
+            xm = {k: v.copy() for k, v in x.items()}
+            xp[name][idx] += h
+            xm[name][idx] -= h
+            fd[idx] = (loss_brute_force(xp, dO, var_floor, eps, causal) -
+                       loss_brute_force(xm, dO, var_floor, eps, causal)) / (2 * h)
+        scale = max(np.abs(fd).max(), 1e-3)
+        assert np.abs(g[name] - fd).max() <= 1e-6 * scale, (name, g[name], fd)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_directional_derivative_on_a_larger_head(causal):
+    # all inputs moved along one random direction at once, at K = 9, N = 60
+    var_floor, eps, h = 1e-4, 1e-3, 1e-6
+    x = make(N=60, d=6, K=9, dv=5, seed=30 + causal)
+    r = np.random.default_rng(31)
+    dO = r.normal(size=(60, 5))
+    delta = {k: r.normal(size=v.shape) for k, v in x.items()}
+    g = oracle.backward_head(*(x[k] for k in BWD_INPUTS), var_floor, eps, causal, dO)
+
+    def loss(s):
+        y = {k: x[k] + s * delta[k] for k in x}
+        return float((dO * oracle.forward_head(*(y[k] for k in BWD_INPUTS), var_floor, eps, causal)).sum())
+
+    fd = (loss(h) - loss(-h)) / (2 * h)
+    an = sum(float((g[k] * delta[k]).sum()) for k in BWD_INPUTS)
+    assert abs(fd - an) <= 1e-6 * max(abs(an), 1.0), (fd, an)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_invariants(causal):
+    var_floor, eps = 1e-4, 1e-3
+    x = make(N=50, d=4, K=6, dv=3, seed=40 + causal)
+    dO = np.random.default_rng(41).normal(size=(50, 3))
+    g = oracle.backward_head(*(x[k] for k in BWD_INPUTS), var_floor, eps, causal, dO)
+    O = oracle.forward_head(*(x[k] for k in BWD_INPUTS), var_floor, eps, causal)
+    # a common shift of every routing vector and every mean leaves each score unchanged
+    shift = g["Qx"].sum(axis=0) + g["Kx"].sum(axis=0) + g["mu"].sum(axis=0)
+    assert np.abs(shift).max() <= 1e-10 * max(np.abs(g["mu"]).max(), 1.0)
+    # O is homogeneous of degree one in V (Eq. 7-8): Euler's identity
+    assert abs((g["V"] * x["V"]).sum() - (dO * O).sum()) <= 1e-10 * np.abs(dO * O).sum()
+    # the priors enter through log_softmax(alpha) (Eq. 15): a common shift of alpha does nothing
+    assert abs(g["alpha"].sum()) <= 1e-12 * max(np.abs(g["alpha"]).max(), 1.0)
+
+
+def test_causal_backward_reaches_only_the_prefix():
+    # dO nonzero at row t only: queries other than t get nothing, keys and values after t nothing
+    var_floor, eps, t = 1e-4, 1e-3, 23
+    x = make(N=40, d=4, K=5, dv=3, seed=50)
+    dO = np.zeros((40, 3))
+    dO[t] = np.random.default_rng(51).normal(size=3)
+    g = oracle.backward_head(*(x[k] for k in BWD_INPUTS), var_floor, eps, True, dO)
+    others = np.arange(40) != t
+    assert np.abs(g["Qx"][others]).max() == 0.0 and np.abs(g["Qx"][t]).max() > 0
+    assert np.abs(g["Kx"][t + 1:]).max() == 0.0 and np.abs(g["V"][t + 1:]).max() == 0.0
+    assert np.abs(g["Kx"][:t + 1]).max() > 0 and np.abs(g["V"][:t + 1]).max() > 0
