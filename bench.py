@@ -49,7 +49,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics", "cross", "decode"], default="both",
+    ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics", "cross", "decode", "backward"],
+                    default="both",
                     help="which forward(s) one step runs (default: both, the headline step); "
                          "diagnostics: one step is gma_diagnostics over the workload's query vectors; "
                          "cross: one step is gma_forward_cross, the workload's queries reading a context; "
@@ -881,6 +882,123 @@ def run_decode(args, rank, world, local):
     return 0
 
 
+BWD_METRIC = "GMA bidirectional backward token·heads/s (gradients of Qx, Kx, V, mu, rho, alpha; section 4.1)"
+# fp32 flops per row of one head in the backward kernels (2 per multiply-add): the memory pass
+# (scores 2(2d)K, memory 2K(dv+1)), the query pass (scores, read 2K dv, g^Q 2 dv K, dQx 4Kd,
+# [R | r] 2K(dv+1), parameter sums 4Kd) and the key pass (scores, g^K, dV, dKx, parameter sums)
+def bwd_flops_per_row(w):
+    sc = 2 * 2 * w.d * w.K
+    return (sc + 2 * w.K * (w.dv + 1)) + (sc + 4 * w.K * w.dv + 4 * w.K * w.d + 2 * w.K * (w.dv + 1) + 4 * w.K * w.d) \
+        + (sc + 4 * w.K * w.dv + 4 * w.K * w.d + 4 * w.K * w.d)
+
+
+def bwd_oracle_sample(w, seconds):
+    """The oracle's backward of whole heads of the workload (one thread), repeated for about
+    ``seconds``."""
+    import oracle
+    oracle.build()
+    x = inputs.gen_all(w.replace(B=1, H=1))
+    z = inputs.normal(inputs.stream_key(w.seed, "dO"), 0, w.N * w.dv).reshape(w.N, w.dv)
+    dO = inputs.widen(inputs.f32_to_bf16_bits(z.astype(np.float32)), "bf16") if w.dtype == "bf16" else z
+    reps, t0 = 0, time.perf_counter()
+    while reps == 0 or time.perf_counter() - t0 < seconds:
+        oracle.backward_head(*(inputs.widen(x[n][0, 0], w.dtype) for n in ("Qx", "Kx", "V")), x["mu"][0],
+                             x["rho"][0], x["alpha"][0], w.var_floor, w.eps, False, dO)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    return w.N / dt, reps, dt
+
+
+def run_backward(args, rank, world, local):
+    """Backward pass (section 4.1): one step is one gma_backward call over the workload's
+    B x H heads (bidirectional), from the inputs and dL/dO to every gradient."""
+    import torch
+    import gaussian_mixture_latent_gb300 as gma
+    from gaussian_mixture_latent_gb300 import _build
+    w = inputs.WORKLOADS[args.workload].replace(causal=False)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        rate, reps, dt = bwd_oracle_sample(w, 12.0)
+        print(json.dumps({"impl": "reference", "metric": BWD_METRIC, "value": rate, "unit": "tokens·heads/s",
+                          "n_gpus": args.gpus, "steps": reps, "warmup": 0, "ms_per_step": dt * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": {"workload": w.name, "step": "backward (sampled)"},
+                          "cpu_baseline": {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
+                                           "sample": f"one head of {w.name} (N = {w.N}), {reps} passes"},
+                          "e2e": {"value": rate, "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    sets = []
+    for seed in (0, 1):
+        x = inputs.gen_all(w.replace(seed=seed))
+        z = inputs.normal(inputs.stream_key(seed, "dO"), 0, w.B * w.H * w.N * w.dv).astype(np.float32)
+        x["dO"] = (inputs.f32_to_bf16_bits(z) if w.dtype == "bf16" else z).reshape(w.B, w.H, w.N, w.dv)
+        sets.append({k: to_dev(x[k]) for k in ("Qx", "Kx", "V", "mu", "rho", "alpha", "dO")})
+    f32 = dict(dtype=torch.float32, device=dev)
+    grads = (torch.empty((w.B, w.H, w.N, w.d), **f32), torch.empty((w.B, w.H, w.N, w.d), **f32),
+             torch.empty((w.B, w.H, w.N, w.dv), **f32), torch.empty((w.H, w.K, w.d), **f32),
+             torch.empty((w.H, w.K, w.d), **f32), torch.empty((w.H, w.K), **f32))
+    stream = torch.cuda.current_stream()
+
+    def step(x):
+        gma.gma_backward(x["Qx"], x["Kx"], x["V"], x["mu"], x["rho"], x["alpha"], x["dO"], eps=w.eps,
+                         var_floor=w.var_floor, grads=grads)
+
+    warm = max(3, args.warmup)
+    for it in range(warm):
+        step(sets[it % 2])
+    torch.cuda.synchronize()
+    if gma.gma_get_status():
+        raise RuntimeError("device status after warm-up")
+    steps = args.steps if args.steps is not None else 20
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(gpu_id_for(local))
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for it in range(steps):
+        evs[it][0].record(stream)
+        step(sets[it % 2])
+        evs[it][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if gma.gma_get_status():
+        raise RuntimeError("device status after the timed region")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    units = w.B * w.H * w.N
+    flops = units * bwd_flops_per_row(w)
+    alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12            # fp32 lanes x 2 flops x max SM clock, TFLOP/s
+    achieved = flops / (ms / 1e3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, reps, dt = bwd_oracle_sample(w, 12.0)
+        cpu = {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
+               "sample": f"one head of {w.name} (N = {w.N}), {reps} passes"}
+    print(json.dumps({"metric": BWD_METRIC, "value": units / (ms / 1e3), "unit": "tokens·heads/s", "n_gpus": 1,
+                      "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                      "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K, "dv": w.dv,
+                                 "inputs": w.dtype, "step": "bidirectional backward, all gradients",
+                                 "l2": "two alternating input sets (> 129 MB L2)", "parallelism": "single GPU"},
+                      "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                                   "frac": achieved / alu_peak, "traffic": None,
+                                   "kernel": "gma_backward (whole call: 7 launches)", "kernel_ms": ms,
+                                   "flops_per_row": bwd_flops_per_row(w),
+                                   "peak_source": "fp32 lanes x 2 x 2070 MHz"},
+                      "clocks": clocks, "gpu_launches": 7 * steps, "cpu_baseline": cpu}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -890,6 +1008,8 @@ def main():
         return run_diagnostics(args, rank, world, local)
     if args.direction == "cross":
         return run_cross(args, rank, world, local)
+    if args.direction == "backward":
+        return run_backward(args, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_gpu(args, rank, world, local)

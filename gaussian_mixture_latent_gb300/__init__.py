@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "GmaError", "gma_desc", "gma_workspace_size", "gma_workspace_init", "gma_forward",
     "gma_forward_ex", "gma_forward_plan",
-    "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_decode", "gma_get_status", "gma_status_string", "gma_version",
+    "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_decode", "gma_backward", "gma_get_status", "gma_status_string", "gma_version",
     "Workspace", "library_path",
 ]
 
@@ -76,6 +76,8 @@ def _load():
     lib.gma_forward_cross.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, f, vp, vp, sz, vp]
     lib.gma_decode_workspace_size.argtypes = [dp, ctypes.POINTER(sz)]
     lib.gma_decode.argtypes = [dp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp, sz, vp]
+    lib.gma_backward_workspace_size.argtypes = [dp, i, ctypes.POINTER(sz)]
+    lib.gma_backward.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gma_get_status.argtypes = [vp, vp]
     lib.gma_status_string.argtypes = [i]
     lib.gma_status_string.restype = ctypes.c_char_p
@@ -83,7 +85,8 @@ def _load():
     for fn in (lib.gma_workspace_size, lib.gma_workspace_init, lib.gma_forward,
                lib.gma_forward_ex, lib.gma_forward_plan, lib.gma_responsibilities, lib.gma_get_status, lib.gma_version,
                lib.gma_diagnostics_workspace_size, lib.gma_diagnostics, lib.gma_cross_workspace_size,
-               lib.gma_forward_cross, lib.gma_decode_workspace_size, lib.gma_decode):
+               lib.gma_forward_cross, lib.gma_decode_workspace_size, lib.gma_decode,
+               lib.gma_backward_workspace_size, lib.gma_backward):
         fn.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -274,6 +277,44 @@ def gma_forward_cross(Qx, Ky, Vy, mu, rho, pi_logits, eps: float = 1e-6, var_flo
     if rc:
         raise GmaError(rc, "gma_forward_cross")
     return out
+
+
+def gma_backward(Qx, Kx, V, mu, rho, pi_logits, dO, eps: float = 1e-6, var_floor: float = 1e-4, causal=False,
+                 grads=None, workspace=None, stream=None):
+    """Backward pass (section 4.1, Eqs. 17-20): given dO = dL/dO [B,H,N,dv] of the forward
+    gma_forward(Qx, Kx, V, mu, rho, pi_logits), returns the float32 gradients
+    (dQx, dKx, dV, dmu, drho, dpi_logits); parameter gradients are summed over the batch.
+    `grads`, if given, is that tuple of preallocated outputs (overwritten)."""
+    B, H, N, d = Qx.shape
+    dv = V.shape[3]
+    K = mu.shape[1]
+    _check(Qx, "Qx", (B, H, N, d), (torch.float32, torch.bfloat16))
+    _check(Kx, "Kx", (B, H, N, d), (Qx.dtype,))
+    _check(V, "V", (B, H, N, dv), (Qx.dtype,))
+    _check(dO, "dO", (B, H, N, dv), (Qx.dtype,))
+    _check(mu, "mu", (H, K, d), (torch.float32,))
+    _check(rho, "rho", (H, K, d), (torch.float32,))
+    _check(pi_logits, "pi_logits", (H, K), (torch.float32,))
+    if grads is None:
+        f32 = dict(dtype=torch.float32, device=Qx.device)
+        grads = (torch.empty((B, H, N, d), **f32), torch.empty((B, H, N, d), **f32),
+                 torch.empty((B, H, N, dv), **f32), torch.empty((H, K, d), **f32),
+                 torch.empty((H, K, d), **f32), torch.empty((H, K), **f32))
+    shapes = ((B, H, N, d), (B, H, N, d), (B, H, N, dv), (H, K, d), (H, K, d), (H, K))
+    for t, shp, name in zip(grads, shapes, ("dQx", "dKx", "dV", "dmu", "drho", "dpi_logits")):
+        _check(t, name, shp, (torch.float32,))
+    desc = _make_desc(B, H, N, d, K, dv, Qx.dtype, Qx.dtype, var_floor, 0)
+    nbytes = ctypes.c_size_t(0)
+    rc = _load().gma_backward_workspace_size(ctypes.byref(desc), int(bool(causal)), ctypes.byref(nbytes))
+    if rc:
+        raise GmaError(rc, "gma_backward_workspace_size")
+    ws = _workspace_for(Qx.device, nbytes.value, workspace, stream)
+    rc = _load().gma_backward(ctypes.byref(desc), int(bool(causal)), _ptr(Qx), _ptr(Kx), _ptr(V), _ptr(mu),
+                              _ptr(rho), _ptr(pi_logits), float(eps), _ptr(dO), *(_ptr(t) for t in grads),
+                              _ptr(ws), ws.numel(), _stream_ptr(stream))
+    if rc:
+        raise GmaError(rc, "gma_backward")
+    return grads
 
 
 def gma_decode(Qx, Kx, V, mu, rho, pi_logits, state, eps: float = 1e-6, var_floor: float = 1e-4, out=None,

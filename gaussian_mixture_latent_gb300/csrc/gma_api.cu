@@ -258,6 +258,46 @@ gma_status gma_forward_cross(const gma_desc *desc, int Nkv, const void *Qx, cons
     return tc_read(p, L, Qx, out, ws, s) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
+gma_status gma_backward_workspace_size(const gma_desc *desc, int causal, size_t *bytes) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (!bytes || causal < 0 || causal > 1) return GMA_ERR_INVALID_ARG;
+    const Problem p = make_problem(desc, causal, 0.f);
+    if (!bwd_supported(p) || p.out_dtype != p.in_dtype) return GMA_ERR_UNSUPPORTED;
+    *bytes = bwd_layout(p).total;
+    return GMA_OK;
+}
+
+gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const void *Kx, const void *V,
+                        const float *mu, const float *rho, const float *pi_logits, float eps, const void *dO,
+                        float *dQx, float *dKx, float *dV, float *dmu, float *drho, float *dpi_logits,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    gma_status st = validate_desc(desc);
+    if (st != GMA_OK) return st;
+    if (causal < 0 || causal > 1 || !(eps >= 0.f) || !std::isfinite(eps)) return GMA_ERR_INVALID_ARG;
+    if (!mu || !rho || !pi_logits || !dmu || !drho || !dpi_logits) return GMA_ERR_INVALID_ARG;
+    if (desc->N > 0 && (!Qx || !Kx || !V || !dO || !dQx || !dKx || !dV)) return GMA_ERR_INVALID_ARG;
+    const void *ptrs[] = {Qx, Kx, V, dO, dQx, dKx, dV, mu, rho, pi_logits, dmu, drho, dpi_logits, workspace};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
+    const Problem p = make_problem(desc, causal, eps);
+    if (!bwd_supported(p) || p.out_dtype != p.in_dtype) return GMA_ERR_UNSUPPORTED;
+    const BwdLayout L = bwd_layout(p);
+    if (!workspace || workspace_bytes < L.total) return GMA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.N == 0) {     // the loss does not depend on the parameters
+        const size_t kd = sizeof(float) * (size_t)p.H * p.K * p.d;
+        if (cudaMemsetAsync(dmu, 0, kd, s) != cudaSuccess || cudaMemsetAsync(drho, 0, kd, s) != cudaSuccess ||
+            cudaMemsetAsync(dpi_logits, 0, sizeof(float) * (size_t)p.H * p.K, s) != cudaSuccess)
+            return GMA_ERR_CUDA;
+        return GMA_OK;
+    }
+    return bwd_run(p, L, Qx, Kx, V, mu, rho, pi_logits, dO, dQx, dKx, dV, dmu, drho, dpi_logits,
+                   static_cast<char *>(workspace), s) == cudaSuccess
+               ? GMA_OK
+               : GMA_ERR_CUDA;
+}
+
 gma_status gma_decode_workspace_size(const gma_desc *desc, size_t *bytes) {
     gma_status st = validate_desc(desc);
     if (st != GMA_OK) return st;

@@ -1,0 +1,515 @@
+// Backward pass of bidirectional GMA on the CUDA cores (fp32 arithmetic).
+//
+// "Gaussian Mixture Attention" (Huang & Raza, 2026), section 4.1: the upstream
+// gradient g at a responsibility vector enters the scores through the softmax
+// Jacobian, ds_ik = gamma_ik (g_ik - sum_j gamma_ij g_ij) (Eq. 17-18); every
+// quantity that enters a score collects sum_i sum_k ds_ik ds_ik/dtheta (Eq. 19),
+// with ds_ik/dmu_k = Sigma_k^-1 (x_i - mu_k) (Eq. 20), ds_ik/dx_i =
+// -Sigma_k^-1 (x_i - mu_k) (section 4.3), the variance derivative of the score
+// of Eq. 16, and Eq. 14-15 for rho and alpha.  The memory products of
+// Eq. 5-8 are differentiated as products: with den_i = gamma^Q_i . Z + eps,
+// a_i = dO_i / den_i and b_i = -(dO_i . O_i) / den_i,
+//   g^Q_i = Vt a_i + Z b_i,   R = sum_i gamma^Q_i a_i^T,   r = sum_i gamma^Q_i b_i,
+//   g^K_j = R v_j + r,        dV_j = R^T gamma^K_j.
+//
+// Three passes of one kernel over 64-row tiles (one CTA per (row chunk, head),
+// 256 threads), each recomputing the responsibilities of its rows:
+//   MEM  key rows:   [Vt | Z] partials  (Eq. 5-6)
+//   QRY  query rows: a, b, g^Q, ds, dQx; partials of [R | r] and of the parameter sums
+//   KEY  key rows:   g^K, dV, ds, dKx; partials of the parameter sums
+// with fixed-order reductions of the partials in between and a finalize that
+// turns the parameter sums P1 = sum ds x, P2 = sum ds x^2, P0 = sum ds into
+// dmu, drho, dalpha.  Every product is a 4 x 4 register-blocked loop over
+// shared memory; the scores use the expanded form
+//   s_ik = c'_k + sum_j (lambda mu)_kj x_ij - (1/2) sum_j lambda_kj x_ij^2,
+//   c'_k = log pi_k - (1/2) log|Sigma_k| - (1/2) sum_j lambda_kj mu_kj^2,
+// so that the score is one product [x, x^2] . W.  Shapes: d = dv = K = 64.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cfloat>
+#include <cstdint>
+
+#include "gma_internal.h"
+
+namespace gma {
+namespace {
+
+constexpr int kBT = 256;          // threads of a pass CTA
+constexpr int kTN = 64;           // rows per tile
+constexpr int kK = 64, kD = 64, kDV = 64;
+constexpr int kW = kDV + 1;       // [value columns | normaliser] of a memory
+constexpr int kPW = 2 * kD + 1;   // parameter sums per component: P1 [d], P2 [d], P0
+constexpr int kRS = 68;           // row stride of the per-tile arrays (16-byte rows, spread banks)
+
+enum BwdMode { kMem = 0, kQry = 1, kKey = 2 };
+
+// Shared memory of one pass CTA, in floats.
+constexpr int OFF_W = 0;                         // [2d][K]  score weights: lambda mu, then -lambda / 2
+constexpr int OFF_CP = OFF_W + 2 * kD * kK;      // [K]      c'_k
+constexpr int OFF_LAM = OFF_CP + kK;             // [K][d]   lambda
+constexpr int OFF_LMU = OFF_LAM + kK * kD;       // [K][d]   lambda mu
+constexpr int OFF_M = OFF_LMU + kK * kD;         // [K][dv]  Vt (QRY) or R (KEY)
+constexpr int OFF_MT = OFF_M + kK * kDV;         // [dv][K]  its transpose
+constexpr int OFF_ZR = OFF_MT + kDV * kK;        // [K]      Z (QRY) or r (KEY)
+constexpr int OFF_X = OFF_ZR + kK;               // [TN][kRS] routing rows
+constexpr int OFF_A = OFF_X + kTN * kRS;         // [TN][kRS] values (MEM, KEY) / dO then a (QRY)
+constexpr int OFF_G = OFF_A + kTN * kRS;         // [TN][kRS] scores, then gamma
+constexpr int OFF_S = OFF_G + kTN * kRS;         // [TN][kRS] g, then ds
+constexpr int OFF_DEN = OFF_S + kTN * kRS;       // [TN]     den (QRY)
+constexpr int OFF_B = OFF_DEN + kTN;             // [TN]     b (QRY)
+constexpr int kBwdSmemFloats = OFF_B + kTN;
+constexpr size_t kBwdSmemBytes = sizeof(float) * kBwdSmemFloats;
+static_assert(kBwdSmemBytes <= 227 * 1024, "pass CTA shared memory");
+static_assert((OFF_X | OFF_A | OFF_G | OFF_S | OFF_M | OFF_MT | OFF_LAM | OFF_LMU | OFF_W) % 4 == 0, "float4 rows");
+
+struct BwdArgs {
+    int N, H, C, rows_per_chunk;       // rows per head, heads per batch entry, chunks per head
+    float eps;
+    const void *X;                     // Qx (QRY) or Kx (MEM, KEY)  [G][N][d]
+    const void *U;                     // V (MEM, KEY) or dO (QRY)   [G][N][dv]
+    const float *mu, *lam, *cdir;      // [H][K][d], [H][K][d], [H][K]
+    const float *mem;                  // [G][K][W]: [Vt | Z] (QRY) or [R | r] (KEY)
+    float *dX;                         // dQx (QRY) or dKx (KEY)     [G][N][d]
+    float *dV;                         // KEY                        [G][N][dv]
+    float *part_m;                     // MEM, QRY: [G][C][K][W]
+    float *part_p;                     // QRY, KEY: [G][C][K][2d + 1]
+};
+
+__device__ __forceinline__ float bwd_load(const float *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float bwd_load(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
+
+__device__ __forceinline__ float bwd_warp_sum(float v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(~0u, v, o);
+    return v;
+}
+__device__ __forceinline__ float bwd_warp_max(float v) {
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(~0u, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+__device__ __forceinline__ void fma4x4(float (&c)[4][4], const float (&a)[4], const float4 b) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        c[i][0] = fmaf(a[i], b.x, c[i][0]);
+        c[i][1] = fmaf(a[i], b.y, c[i][1]);
+        c[i][2] = fmaf(a[i], b.z, c[i][2]);
+        c[i][3] = fmaf(a[i], b.w, c[i][3]);
+    }
+}
+
+__device__ __forceinline__ void zero4x4(float (&c)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[i][j] = 0.f;
+}
+
+// c[i][j] += sum_{s < S} A[(r0 + i) * as + s] * B[s * bs + c0 + j]: A row-major with the
+// summed index contiguous (scalar loads, shared by a half-warp), B with the summed index
+// outermost (one float4 per step).
+template <int S>
+__device__ __forceinline__ void mm_rows(float (&c)[4][4], const float *A, int as, int r0, const float *B, int bs,
+                                        int c0) {
+#pragma unroll 4
+    for (int s = 0; s < S; ++s) {
+        const float a[4] = {A[(r0 + 0) * as + s], A[(r0 + 1) * as + s], A[(r0 + 2) * as + s],
+                            A[(r0 + 3) * as + s]};
+        fma4x4(c, a, ld4(B + s * bs + c0));
+    }
+}
+
+// c[i][j] += sum_{m < TN} A[m * as + r0 + i] * B[m * bs + c0 + j]: both operands with the
+// summed row index outermost (the accumulations over a tile's rows).
+__device__ __forceinline__ void mm_cols(float (&c)[4][4], const float *A, int as, int r0, const float *B, int bs,
+                                        int c0) {
+#pragma unroll 4
+    for (int m = 0; m < kTN; ++m) {
+        const float4 a4 = ld4(A + m * as + r0);
+        const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+        fma4x4(c, a, ld4(B + m * bs + c0));
+    }
+}
+
+// One pass over the rows [chunk * rows_per_chunk, +rows_per_chunk) of head g = blockIdx.y.
+// Thread t owns the 4 x 4 output block (rows (t / 16) * 4.., columns (t % 16) * 4..) of
+// every 64 x 64 product, and the same block of the accumulated memory and parameter sums.
+template <int MODE, typename TI>
+__global__ void __launch_bounds__(kBT, 1) bwd_pass_kernel(BwdArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    float *W = sm + OFF_W, *cp = sm + OFF_CP, *lam = sm + OFF_LAM, *lmu = sm + OFF_LMU;
+    float *M = sm + OFF_M, *MT = sm + OFF_MT, *zr = sm + OFF_ZR;
+    float *xs = sm + OFF_X, *us = sm + OFF_A, *gs = sm + OFF_G, *ss = sm + OFF_S;
+    float *den = sm + OFF_DEN, *bb = sm + OFF_B;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
+    const int ch = blockIdx.x, g = blockIdx.y, h = g % a.H;
+    const TI *X = static_cast<const TI *>(a.X) + (size_t)g * a.N * kD;
+    const TI *U = static_cast<const TI *>(a.U) + (size_t)g * a.N * kDV;
+
+    // the head's precisions, lambda mu, the score weights and constants (Eq. 14-16)
+    const float *lam_h = a.lam + (size_t)h * kK * kD, *mu_h = a.mu + (size_t)h * kK * kD;
+    for (int e = tid; e < kK * kD; e += kBT) {
+        const float l = lam_h[e];
+        lam[e] = l;
+        lmu[e] = l * mu_h[e];
+    }
+    __syncthreads();
+    for (int e = tid; e < 2 * kD * kK; e += kBT) {
+        const int q = e / kK, k = e % kK;
+        W[e] = q < kD ? lmu[k * kD + q] : -0.5f * lam[k * kD + q - kD];
+    }
+    if (tid < kK) {
+        float s = 0.f;
+        for (int j = 0; j < kD; ++j) s = fmaf(lmu[tid * kD + j], mu_h[tid * kD + j], s);
+        cp[tid] = a.cdir[(size_t)h * kK + tid] - 0.5f * s;
+    }
+    if (MODE != kMem) {
+        const float *mg = a.mem + (size_t)g * kK * kW;
+        for (int e = tid; e < kK * kW; e += kBT) {
+            const int k = e / kW, c = e - k * kW;
+            const float v = mg[e];
+            if (c < kDV) {
+                M[k * kDV + c] = v;
+                MT[c * kK + k] = v;
+            } else {
+                zr[k] = v;
+            }
+        }
+    }
+    float accM[4][4], accP1[4][4], accP2[4][4];
+    zero4x4(accM);
+    zero4x4(accP1);
+    zero4x4(accP2);
+    float ex_m = 0.f, ex_p = 0.f;     // the memory's last column (threads < K); P0 (threads K..2K-1)
+    __syncthreads();
+
+    const int row_begin = ch * a.rows_per_chunk;
+    const int row_end = min(a.N, row_begin + a.rows_per_chunk);
+    for (int t0 = row_begin; t0 < row_end; t0 += kTN) {
+        const int mv = min(kTN, row_end - t0);
+        for (int e = tid; e < kTN * kD; e += kBT) {
+            const int m = e / kD, j = e % kD;
+            const bool live = m < mv;
+            xs[m * kRS + j] = live ? bwd_load(X, (size_t)(t0 + m) * kD + j) : 0.f;
+            us[m * kRS + j] = live ? bwd_load(U, (size_t)(t0 + m) * kDV + j) : 0.f;
+        }
+        __syncthreads();
+        // Eq. 16, expanded: s = c' + x . (lambda mu) - (1/2) x^2 . lambda
+        {
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kD>(c, xs, kRS, r0, W, kK, c0);
+#pragma unroll 4
+            for (int s = 0; s < kD; ++s) {
+                float x2[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float v = xs[(r0 + i) * kRS + s];
+                    x2[i] = v * v;
+                }
+                fma4x4(c, x2, ld4(W + (kD + s) * kK + c0));
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) gs[(r0 + i) * kRS + c0 + j] = cp[c0 + j] + c[i][j];
+        }
+        __syncthreads();
+        // Eq. 3b, a warp per row; rows past the end get gamma = 0 and so contribute nothing
+        for (int m = warp; m < kTN; m += kBT / 32) {
+            const float s0 = gs[m * kRS + lane], s1 = gs[m * kRS + lane + 32];
+            const float mx = bwd_warp_max(fmaxf(s0, s1));
+            float e0 = expf(s0 - mx), e1 = expf(s1 - mx);
+            const float inv = 1.0f / bwd_warp_sum(e0 + e1);
+            const bool live = m < mv;
+            e0 = live ? e0 * inv : 0.f;
+            e1 = live ? e1 * inv : 0.f;
+            gs[m * kRS + lane] = e0;
+            gs[m * kRS + lane + 32] = e1;
+            if (MODE == kQry) {
+                const float z = bwd_warp_sum(e0 * zr[lane] + e1 * zr[lane + 32]);
+                if (lane == 0) den[m] = z + a.eps;
+            }
+        }
+        __syncthreads();
+        if (MODE == kQry) {
+            // Eq. 7-8: O = gamma Vt / den; a = dO / den, b = -(dO . O) / den (in place of dO)
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kK>(c, gs, kRS, r0, M, kDV, c0);
+            float dot[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float dn = den[r0 + i];
+                float p = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float *q = us + (r0 + i) * kRS + c0 + j;
+                    p = fmaf(*q, c[i][j] / dn, p);
+                    *q = *q / dn;
+                }
+                dot[i] = p;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                for (int o = 8; o; o >>= 1) dot[i] += __shfl_xor_sync(~0u, dot[i], o);   // the row block's 16 threads
+            if ((tid & 15) == 0)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) bb[r0 + i] = -dot[i] / den[r0 + i];
+            __syncthreads();
+            // g^Q = a Vt^T + b Z
+            zero4x4(c);
+            mm_rows<kDV>(c, us, kRS, r0, MT, kK, c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ss[(r0 + i) * kRS + c0 + j] = fmaf(bb[r0 + i], zr[c0 + j], c[i][j]);
+            __syncthreads();
+        } else if (MODE == kKey) {
+            // g^K = R v + r and dV = gamma^K R
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kDV>(c, us, kRS, r0, MT, kK, c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ss[(r0 + i) * kRS + c0 + j] = c[i][j] + zr[c0 + j];
+            zero4x4(c);
+            mm_rows<kK>(c, gs, kRS, r0, M, kDV, c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (r0 + i < mv)
+                    *reinterpret_cast<float4 *>(a.dV + ((size_t)g * a.N + t0 + r0 + i) * kDV + c0) =
+                        make_float4(c[i][0], c[i][1], c[i][2], c[i][3]);
+            __syncthreads();
+        }
+        if (MODE != kMem) {
+            // Eq. 18: ds = gamma (g - gamma . g), a warp per row
+            for (int m = warp; m < kTN; m += kBT / 32) {
+                const float g0 = gs[m * kRS + lane], g1 = gs[m * kRS + lane + 32];
+                const float u0 = ss[m * kRS + lane], u1 = ss[m * kRS + lane + 32];
+                const float mean = bwd_warp_sum(g0 * u0 + g1 * u1);
+                ss[m * kRS + lane] = g0 * (u0 - mean);
+                ss[m * kRS + lane + 32] = g1 * (u1 - mean);
+            }
+            __syncthreads();
+            // section 4.3: dx = -sum_k ds_k lambda_k (x - mu_k) = ds . (lambda mu) - x (ds . lambda)
+            float c1[4][4], c2[4][4];
+            zero4x4(c1);
+            zero4x4(c2);
+#pragma unroll 4
+            for (int s = 0; s < kK; ++s) {
+                const float d4[4] = {ss[(r0 + 0) * kRS + s], ss[(r0 + 1) * kRS + s], ss[(r0 + 2) * kRS + s],
+                                     ss[(r0 + 3) * kRS + s]};
+                fma4x4(c1, d4, ld4(lam + s * kD + c0));
+                fma4x4(c2, d4, ld4(lmu + s * kD + c0));
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (r0 + i >= mv) continue;
+                const float *x = xs + (r0 + i) * kRS + c0;
+                *reinterpret_cast<float4 *>(a.dX + ((size_t)g * a.N + t0 + r0 + i) * kD + c0) =
+                    make_float4(fmaf(-x[0], c1[i][0], c2[i][0]), fmaf(-x[1], c1[i][1], c2[i][1]),
+                                fmaf(-x[2], c1[i][2], c2[i][2]), fmaf(-x[3], c1[i][3], c2[i][3]));
+            }
+            // Eq. 19-20 and the variance derivative, as sums over the rows: P1 = sum ds x, P2 = sum ds x^2
+#pragma unroll 4
+            for (int m = 0; m < kTN; ++m) {
+                const float4 d4 = ld4(ss + m * kRS + r0);
+                const float dk[4] = {d4.x, d4.y, d4.z, d4.w};
+                const float4 x4 = ld4(xs + m * kRS + c0);
+                fma4x4(accP1, dk, x4);
+                fma4x4(accP2, dk, make_float4(x4.x * x4.x, x4.y * x4.y, x4.z * x4.z, x4.w * x4.w));
+            }
+            if (tid >= kK && tid < 2 * kK)
+                for (int m = 0; m < kTN; ++m) ex_p += ss[m * kRS + tid - kK];
+        }
+        if (MODE != kKey) {
+            // Eq. 5-6 (MEM: [Vt | Z]) or the same product for the backward memory (QRY: [R | r])
+            mm_cols(accM, gs, kRS, r0, us, kRS, c0);
+            if (tid < kK)
+                for (int m = 0; m < kTN; ++m) ex_m = fmaf(gs[m * kRS + tid], MODE == kMem ? 1.f : bb[m], ex_m);
+        }
+        __syncthreads();
+    }
+
+    const size_t slot = (size_t)g * a.C + ch;
+    if (MODE != kKey) {
+        float *pm = a.part_m + slot * kK * kW;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pm[(r0 + i) * kW + c0 + j] = accM[i][j];
+        if (tid < kK) pm[tid * kW + kDV] = ex_m;
+    }
+    if (MODE != kMem) {
+        float *pp = a.part_p + slot * kK * kPW;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                pp[(r0 + i) * kPW + c0 + j] = accP1[i][j];
+                pp[(r0 + i) * kPW + kD + c0 + j] = accP2[i][j];
+            }
+        if (tid >= kK && tid < 2 * kK) pp[(tid - kK) * kPW + 2 * kD] = ex_p;
+    }
+}
+
+// out[g][e] = sum over the C chunk slots of head g, in slot order.
+__global__ void bwd_sum_kernel(int C, int E, const float *__restrict__ part, float *__restrict__ out) {
+    const int g = blockIdx.y, e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    float s = 0.f;
+    for (int c = 0; c < C; ++c) s += part[((size_t)g * C + c) * E + e];
+    out[(size_t)g * E + e] = s;
+}
+
+// Parameter gradients of head h from the sums over its query and key rows of every batch
+// entry (fixed order: queries then keys, batch entries, chunks):
+//   Q1 = sum ds (x - mu) = P1 - mu P0,  Q2 = sum ds (x - mu)^2 = P2 - 2 mu P1 + mu^2 P0
+//   dmu = lambda Q1                                             (Eq. 20)
+//   dvar = (1/2) (lambda^2 Q2 - lambda P0),  drho = dvar sigmoid(rho)   (Eq. 16, 14)
+//   dalpha_k = P0_k - pi_k sum_l P0_l                           (Eq. 15)
+__global__ void bwd_param_kernel(int B, int H, int C, const float *__restrict__ pq, const float *__restrict__ pk,
+                                 const float *__restrict__ mu, const float *__restrict__ lam,
+                                 const float *__restrict__ rho, const float *__restrict__ alpha,
+                                 float *__restrict__ dmu, float *__restrict__ drho, float *__restrict__ dalpha) {
+    __shared__ float p0[kK];
+    __shared__ float red[2];
+    const int h = blockIdx.x;
+    auto psum = [&](int k, int q) {
+        float s = 0.f;
+        for (int side = 0; side < 2; ++side) {
+            const float *p = side ? pk : pq;
+            for (int b = 0; b < B; ++b)
+                for (int c = 0; c < C; ++c) s += p[(((size_t)(b * H + h) * C + c) * kK + k) * kPW + q];
+        }
+        return s;
+    };
+    for (int k = threadIdx.x; k < kK; k += blockDim.x) p0[k] = psum(k, 2 * kD);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kK * kD; e += blockDim.x) {
+        const int k = e / kD, j = e % kD;
+        const size_t o = (size_t)h * kK * kD + e;
+        const float P1 = psum(k, j), P2 = psum(k, kD + j), P0 = p0[k];
+        const float m = mu[o], l = lam[o];
+        const float q1 = fmaf(-m, P0, P1);
+        const float q2 = fmaf(m, fmaf(m, P0, -2.f * P1), P2);
+        dmu[o] = l * q1;
+        const float dvar = 0.5f * l * fmaf(l, q2, -P0);
+        drho[o] = dvar / (1.f + expf(-rho[o]));
+    }
+    if (threadIdx.x == 0) {                   // sum_l P0_l and the softmax of alpha, in order
+        const float *al = alpha + (size_t)h * kK;
+        float tot = 0.f, mx = -FLT_MAX, se = 0.f;
+        for (int k = 0; k < kK; ++k) {
+            tot += p0[k];
+            mx = fmaxf(mx, al[k]);
+        }
+        for (int k = 0; k < kK; ++k) se += expf(al[k] - mx);
+        red[0] = tot;
+        red[1] = mx + logf(se);
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < kK; k += blockDim.x)
+        dalpha[(size_t)h * kK + k] = fmaf(-expf(alpha[(size_t)h * kK + k] - red[1]), red[0], p0[k]);
+}
+
+template <int MODE>
+cudaError_t launch_pass(const Problem &p, const BwdLayout &L, const BwdArgs &a, cudaStream_t s) {
+    auto kern = p.in_dtype == GMA_BF16 ? bwd_pass_kernel<MODE, __nv_bfloat16> : bwd_pass_kernel<MODE, float>;
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), (int)kBwdSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(L.C, p.G), kBT, kBwdSmemBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+bool bwd_supported(const Problem &p) { return p.d == kD && p.K == kK && p.dv == kDV && !p.causal; }
+
+BwdLayout bwd_layout(const Problem &p) {
+    BwdLayout L{};
+    // chunks per head: one CTA per SM (the shared memory of a pass CTA), so pick the chunk count
+    // that minimises (waves of G C CTAs) / C, the smallest such count within 2 %
+    const int sms = std::max(1, device_sms() > 0 ? device_sms() : 148);
+    const int tiles = std::max(1, (p.N + kTN - 1) / kTN);
+    const int cmax = std::min(tiles, 64);
+    double best = 1e30;
+    int bestC = 1;
+    for (int c = 1; c <= cmax; ++c) {
+        const double cost = (double)((p.G * c + sms - 1) / sms) / c;
+        if (cost < best * 0.98) {
+            best = cost;
+            bestC = c;
+        }
+    }
+    L.C = bestC;
+    L.rows_per_chunk = ((tiles + L.C - 1) / L.C) * kTN;
+    L.lam = align_up(kHeaderBytes);
+    L.cdir = align_up(L.lam + sizeof(float) * (size_t)p.H * kK * kD);
+    L.mem_s = align_up(L.cdir + sizeof(float) * (size_t)p.H * kK);
+    L.mem_r = align_up(L.mem_s + sizeof(float) * (size_t)p.G * kK * kW);
+    L.part_m = align_up(L.mem_r + sizeof(float) * (size_t)p.G * kK * kW);
+    L.part_q = align_up(L.part_m + sizeof(float) * (size_t)p.G * L.C * kK * kW);
+    L.part_k = align_up(L.part_q + sizeof(float) * (size_t)p.G * L.C * kK * kPW);
+    L.total = align_up(L.part_k + sizeof(float) * (size_t)p.G * L.C * kK * kPW);
+    return L;
+}
+
+cudaError_t bwd_run(const Problem &p, const BwdLayout &L, const void *Qx, const void *Kx, const void *V,
+                    const float *mu, const float *rho, const float *alpha, const void *dO, float *dQx, float *dKx,
+                    float *dV, float *dmu, float *drho, float *dalpha, char *ws, cudaStream_t s) {
+    float *lam = reinterpret_cast<float *>(ws + L.lam), *cdir = reinterpret_cast<float *>(ws + L.cdir);
+    float *mem_s = reinterpret_cast<float *>(ws + L.mem_s), *mem_r = reinterpret_cast<float *>(ws + L.mem_r);
+    float *part_m = reinterpret_cast<float *>(ws + L.part_m);
+    float *part_q = reinterpret_cast<float *>(ws + L.part_q), *part_k = reinterpret_cast<float *>(ws + L.part_k);
+    cudaError_t e = simt_params(p, rho, alpha, lam, cdir, s);
+    if (e != cudaSuccess) return e;
+    BwdArgs a{};
+    a.N = p.N;
+    a.H = p.H;
+    a.C = L.C;
+    a.rows_per_chunk = L.rows_per_chunk;
+    a.eps = p.eps;
+    a.mu = mu;
+    a.lam = lam;
+    a.cdir = cdir;
+    const dim3 sum_grid((kK * kW + 255) / 256, p.G);
+    // the forward memory [Vt | Z] (Eq. 5-6)
+    a.X = Kx;
+    a.U = V;
+    a.part_m = part_m;
+    if ((e = launch_pass<kMem>(p, L, a, s)) != cudaSuccess) return e;
+    bwd_sum_kernel<<<sum_grid, 256, 0, s>>>(L.C, kK * kW, part_m, mem_s);
+    // the query rows: dQx, [R | r], parameter sums
+    a.X = Qx;
+    a.U = dO;
+    a.mem = mem_s;
+    a.dX = dQx;
+    a.part_p = part_q;
+    if ((e = launch_pass<kQry>(p, L, a, s)) != cudaSuccess) return e;
+    bwd_sum_kernel<<<sum_grid, 256, 0, s>>>(L.C, kK * kW, part_m, mem_r);
+    // the key rows: dKx, dV, parameter sums
+    a.X = Kx;
+    a.U = V;
+    a.mem = mem_r;
+    a.dX = dKx;
+    a.dV = dV;
+    a.part_p = part_k;
+    if ((e = launch_pass<kKey>(p, L, a, s)) != cudaSuccess) return e;
+    bwd_param_kernel<<<p.H, 256, 0, s>>>(p.B, p.H, L.C, part_q, part_k, mu, lam, rho, alpha, dmu, drho, dalpha);
+    return cudaGetLastError();
+}
+
+}  // namespace gma

@@ -87,6 +87,21 @@ cudaError_t tc_diag(const Problem &p, const TcLayout &L, const void *Qx, int *z,
 cudaError_t tc_diag_finalize(const Problem &p, const TcLayout &L, float *p_out, float *stats_out, char *ws,
                              cudaStream_t s);
 
+// ----- backward pass, bidirectional, CUDA cores: gma_bwd.cu (uses simt_params) -----
+struct BwdLayout {
+    size_t lam, cdir;            // parameter prologue outputs
+    size_t mem_s, mem_r;         // [G][K][dv+1]: the forward memory [Vt | Z] and the backward [R | r]
+    size_t part_m;               // [G][C][K][dv+1] per-chunk partials of either memory
+    size_t part_q, part_k;       // [G][C][K][2d+1] per-chunk parameter sums over query / key rows
+    size_t total;
+    int C, rows_per_chunk;       // row chunks per head
+};
+bool bwd_supported(const Problem &p);
+BwdLayout bwd_layout(const Problem &p);
+cudaError_t bwd_run(const Problem &p, const BwdLayout &L, const void *Qx, const void *Kx, const void *V,
+                    const float *mu, const float *rho, const float *alpha, const void *dO, float *dQx, float *dKx,
+                    float *dV, float *dmu, float *drho, float *dalpha, char *ws, cudaStream_t s);
+
 // ----- causal decode with a carried state: gma_decode.cu (one launch) -----
 bool decode_supported(const Problem &p);
 size_t decode_workspace(const Problem &p);

@@ -46,6 +46,7 @@ STREAM = {
     "Qx": 1, "Kx": 2, "V": 3, "mu": 4, "rho": 5, "alpha": 6,
     "Qx_mix_sel": 7, "Qx_mix_comp": 8, "Qx_mix_noise": 9,
     "Kx_mix_sel": 10, "Kx_mix_comp": 11, "Kx_mix_noise": 12,
+    "dO": 13,                    # upstream gradient of the backward pass
 }
 
 

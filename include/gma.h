@@ -124,6 +124,26 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Backward pass ("Gaussian Mixture Attention", section 4.1, Eq. 17-20, through
+ * Eq. 14-15 and the memory products of Eq. 5-8): given dO = dL/dO
+ * [B, H, N, dv] for the forward output O = gma_forward(...), writes
+ *   dQx, dKx [B, H, N, d], dV [B, H, N, dv]          (float32)
+ *   dmu, drho [H, K, d], dpi_logits [H, K]            (float32, summed over the batch)
+ * every output overwritten, not accumulated.  Qx, Kx, V in desc->in_dtype and
+ * dO in desc->out_dtype, which must be the same type.  Responsibilities and
+ * every product in fp32 on the CUDA cores; deterministic (fixed-order
+ * reductions).  Implemented: bidirectional (causal = 0), d = dv = K = 64;
+ * GMA_ERR_UNSUPPORTED otherwise (the causal backward included).  N = 0 writes
+ * zero parameter gradients.  Workspace: gma_backward_workspace_size().  Errors
+ * as for gma_forward().
+ */
+gma_status gma_backward_workspace_size(const gma_desc *desc, int causal, size_t *bytes);
+gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const void *Kx, const void *V,
+                        const float *mu, const float *rho, const float *pi_logits, float eps, const void *dO,
+                        float *dQx, float *dKx, float *dV, float *dmu, float *drho, float *dpi_logits,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Causal decode with a carried state ("Gaussian Mixture Attention", section
  * 3.5, Eq. 6b and 8b as a recurrence): appends desc->N new positions to each
  * head's causal sequence.  state [B, H, K, dv + 1] float32, in and out, holds
