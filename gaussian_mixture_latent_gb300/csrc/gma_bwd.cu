@@ -76,9 +76,6 @@ struct BwdArgs {
     float *part_p;                     // QRY, KEY: [G][C][K][2d + 1]
 };
 
-__device__ __forceinline__ float bwd_load(const float *p, size_t i) { return p[i]; }
-__device__ __forceinline__ float bwd_load(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
-
 __device__ __forceinline__ float bwd_warp_sum(float v) {
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(~0u, v, o);
     return v;
@@ -89,6 +86,40 @@ __device__ __forceinline__ float bwd_warp_max(float v) {
 }
 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+// Sixteen consecutive elements of one row (a quarter of a 64-wide row), held in registers
+// between their global load and their store into shared memory, so that the next tile's
+// rows are in flight while the current tile computes.
+template <typename TI> struct Row16;
+template <> struct Row16<float> {
+    float4 v[4];
+    __device__ void load(const float *src, bool live) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = live ? reinterpret_cast<const float4 *>(src)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __device__ void store(float *dst) const {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) reinterpret_cast<float4 *>(dst)[i] = v[i];
+    }
+};
+template <> struct Row16<__nv_bfloat16> {
+    uint4 v[2];
+    __device__ void load(const __nv_bfloat16 *src, bool live) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) v[i] = live ? reinterpret_cast<const uint4 *>(src)[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __device__ void store(float *dst) const {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {           // bf16 -> fp32 is a 16-bit shift
+                dst[8 * i + 2 * q] = __uint_as_float(w[q] << 16);
+                dst[8 * i + 2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+            }
+        }
+    }
+};
 
 __device__ __forceinline__ void fma4x4(float (&c)[4][4], const float (&a)[4], const float4 b) {
 #pragma unroll
@@ -113,7 +144,7 @@ __device__ __forceinline__ void zero4x4(float (&c)[4][4]) {
 template <int S>
 __device__ __forceinline__ void mm_rows(float (&c)[4][4], const float *A, int as, int r0, const float *B, int bs,
                                         int c0) {
-#pragma unroll 4
+#pragma unroll 8
     for (int s = 0; s < S; ++s) {
         const float a[4] = {A[(r0 + 0) * as + s], A[(r0 + 1) * as + s], A[(r0 + 2) * as + s],
                             A[(r0 + 3) * as + s]};
@@ -125,7 +156,7 @@ __device__ __forceinline__ void mm_rows(float (&c)[4][4], const float *A, int as
 // summed row index outermost (the accumulations over a tile's rows).
 __device__ __forceinline__ void mm_cols(float (&c)[4][4], const float *A, int as, int r0, const float *B, int bs,
                                         int c0) {
-#pragma unroll 4
+#pragma unroll 8
     for (int m = 0; m < kTN; ++m) {
         const float4 a4 = ld4(A + m * as + r0);
         const float a[4] = {a4.x, a4.y, a4.z, a4.w};
@@ -188,15 +219,24 @@ __global__ void __launch_bounds__(kBT, 1) bwd_pass_kernel(BwdArgs a) {
 
     const int row_begin = ch * a.rows_per_chunk;
     const int row_end = min(a.N, row_begin + a.rows_per_chunk);
+    // thread t carries row t / 4, elements (t % 4) * 16 .. +15, of the X and U tiles
+    const int lm = tid >> 2, lj = (tid & 3) * 16;
+    Row16<TI> rx, ru;
+    if (row_begin < row_end) {
+        const bool live = row_begin + lm < row_end;
+        rx.load(X + (size_t)(row_begin + lm) * kD + lj, live);
+        ru.load(U + (size_t)(row_begin + lm) * kDV + lj, live);
+    }
     for (int t0 = row_begin; t0 < row_end; t0 += kTN) {
         const int mv = min(kTN, row_end - t0);
-        for (int e = tid; e < kTN * kD; e += kBT) {
-            const int m = e / kD, j = e % kD;
-            const bool live = m < mv;
-            xs[m * kRS + j] = live ? bwd_load(X, (size_t)(t0 + m) * kD + j) : 0.f;
-            us[m * kRS + j] = live ? bwd_load(U, (size_t)(t0 + m) * kDV + j) : 0.f;
-        }
+        rx.store(xs + lm * kRS + lj);
+        ru.store(us + lm * kRS + lj);
         __syncthreads();
+        if (t0 + kTN < row_end) {               // the next tile's rows, in flight during this tile
+            const bool live = t0 + kTN + lm < row_end;
+            rx.load(X + (size_t)(t0 + kTN + lm) * kD + lj, live);
+            ru.load(U + (size_t)(t0 + kTN + lm) * kDV + lj, live);
+        }
         // Eq. 16, expanded: s = c' + x . (lambda mu) - (1/2) x^2 . lambda
         {
             float c[4][4];
@@ -367,55 +407,62 @@ __global__ void bwd_sum_kernel(int C, int E, const float *__restrict__ part, flo
     out[(size_t)g * E + e] = s;
 }
 
-// Parameter gradients of head h from the sums over its query and key rows of every batch
-// entry (fixed order: queries then keys, batch entries, chunks):
+// Parameter gradients of component k = blockIdx.x of head h = blockIdx.y from the sums over
+// its query and key rows of every batch entry (fixed order: queries then keys, batch
+// entries, chunks); 128 threads, thread t < d sums P1 of dimension t, thread d + t sums P2:
 //   Q1 = sum ds (x - mu) = P1 - mu P0,  Q2 = sum ds (x - mu)^2 = P2 - 2 mu P1 + mu^2 P0
 //   dmu = lambda Q1                                             (Eq. 20)
 //   dvar = (1/2) (lambda^2 Q2 - lambda P0),  drho = dvar sigmoid(rho)   (Eq. 16, 14)
-//   dalpha_k = P0_k - pi_k sum_l P0_l                           (Eq. 15)
-__global__ void bwd_param_kernel(int B, int H, int C, const float *__restrict__ pq, const float *__restrict__ pk,
-                                 const float *__restrict__ mu, const float *__restrict__ lam,
-                                 const float *__restrict__ rho, const float *__restrict__ alpha,
-                                 float *__restrict__ dmu, float *__restrict__ drho, float *__restrict__ dalpha) {
+//   dalpha_k = P0_k - pi_k sum_l P0_l                           (Eq. 15; every CTA of the
+//   head sums the P0 column, the K values of one row of partials at a stride)
+__global__ void __launch_bounds__(2 * kD) bwd_param_kernel(int B, int H, int C, const float *__restrict__ pq,
+                                                           const float *__restrict__ pk,
+                                                           const float *__restrict__ mu,
+                                                           const float *__restrict__ lam,
+                                                           const float *__restrict__ rho,
+                                                           const float *__restrict__ alpha,
+                                                           float *__restrict__ dmu, float *__restrict__ drho,
+                                                           float *__restrict__ dalpha) {
+    __shared__ float p12[2 * kD];
     __shared__ float p0[kK];
     __shared__ float red[2];
-    const int h = blockIdx.x;
-    auto psum = [&](int k, int q) {
+    const int k = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
+    auto psum = [&](int kk, int q) {
         float s = 0.f;
         for (int side = 0; side < 2; ++side) {
             const float *p = side ? pk : pq;
             for (int b = 0; b < B; ++b)
-                for (int c = 0; c < C; ++c) s += p[(((size_t)(b * H + h) * C + c) * kK + k) * kPW + q];
+                for (int c = 0; c < C; ++c) s += p[(((size_t)(b * H + h) * C + c) * kK + kk) * kPW + q];
         }
         return s;
     };
-    for (int k = threadIdx.x; k < kK; k += blockDim.x) p0[k] = psum(k, 2 * kD);
+    p12[t] = psum(k, t);                       // P1 (t < d), P2 (t >= d)
+    if (t < kK) p0[t] = psum(t, 2 * kD);
     __syncthreads();
-    for (int e = threadIdx.x; e < kK * kD; e += blockDim.x) {
-        const int k = e / kD, j = e % kD;
-        const size_t o = (size_t)h * kK * kD + e;
-        const float P1 = psum(k, j), P2 = psum(k, kD + j), P0 = p0[k];
+    if (t == 0) {                              // sum_l P0_l and log-sum-exp of alpha, in order
+        const float *al = alpha + (size_t)h * kK;
+        float tot = 0.f, mx = -FLT_MAX, se = 0.f;
+        for (int l = 0; l < kK; ++l) {
+            tot += p0[l];
+            mx = fmaxf(mx, al[l]);
+        }
+        for (int l = 0; l < kK; ++l) se += expf(al[l] - mx);
+        red[0] = tot;
+        red[1] = mx + logf(se);
+    }
+    __syncthreads();
+    if (t < kD) {
+        const size_t o = ((size_t)h * kK + k) * kD + t;
+        const float P1 = p12[t], P2 = p12[kD + t], P0 = p0[k];
         const float m = mu[o], l = lam[o];
         const float q1 = fmaf(-m, P0, P1);
         const float q2 = fmaf(m, fmaf(m, P0, -2.f * P1), P2);
         dmu[o] = l * q1;
         const float dvar = 0.5f * l * fmaf(l, q2, -P0);
         drho[o] = dvar / (1.f + expf(-rho[o]));
-    }
-    if (threadIdx.x == 0) {                   // sum_l P0_l and the softmax of alpha, in order
-        const float *al = alpha + (size_t)h * kK;
-        float tot = 0.f, mx = -FLT_MAX, se = 0.f;
-        for (int k = 0; k < kK; ++k) {
-            tot += p0[k];
-            mx = fmaxf(mx, al[k]);
-        }
-        for (int k = 0; k < kK; ++k) se += expf(al[k] - mx);
-        red[0] = tot;
-        red[1] = mx + logf(se);
-    }
-    __syncthreads();
-    for (int k = threadIdx.x; k < kK; k += blockDim.x)
+    } else if (t == kD) {
         dalpha[(size_t)h * kK + k] = fmaf(-expf(alpha[(size_t)h * kK + k] - red[1]), red[0], p0[k]);
+    }
 }
 
 template <int MODE>
@@ -508,7 +555,8 @@ cudaError_t bwd_run(const Problem &p, const BwdLayout &L, const void *Qx, const 
     a.dV = dV;
     a.part_p = part_k;
     if ((e = launch_pass<kKey>(p, L, a, s)) != cudaSuccess) return e;
-    bwd_param_kernel<<<p.H, 256, 0, s>>>(p.B, p.H, L.C, part_q, part_k, mu, lam, rho, alpha, dmu, drho, dalpha);
+    bwd_param_kernel<<<dim3(kK, p.H), 2 * kD, 0, s>>>(p.B, p.H, L.C, part_q, part_k, mu, lam, rho, alpha, dmu, drho,
+                                                    dalpha);
     return cudaGetLastError();
 }
 
