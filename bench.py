@@ -102,9 +102,22 @@ def fp32_simt_peak_tflops(sm_mhz):
     return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
-def csrc_hash():
+# The sources that define each measured kernel: its translation unit and the device headers
+# it includes.  A recorded traffic figure holds while these files are unchanged.
+KERNEL_SOURCES = {
+    "tc_causal": ("gma_tc_causal.cu", "gma_tc_common.cuh", "gma_sm100.cuh"),
+    "tc_write": ("gma_tc.cu", "gma_tc_common.cuh", "gma_sm100.cuh"),
+    "tc_read": ("gma_tc.cu", "gma_tc_common.cuh", "gma_sm100.cuh"),
+}
+
+
+def csrc_hash(kernel=None):
+    """Hash of the CUDA sources of `kernel` (every file of csrc when it is not listed)."""
+    csrc = os.path.join(ROOT, "gaussian_mixture_latent_gb300", "csrc")
+    names = KERNEL_SOURCES.get(kernel)
+    paths = [os.path.join(csrc, n) for n in names] if names else sorted(glob.glob(os.path.join(csrc, "*")))
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "gaussian_mixture_latent_gb300", "csrc", "*"))):
+    for p in paths:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -116,7 +129,7 @@ DOM_EVERY = 8   # the dominant kernel is bracketed by CUDA events on every 8th t
 def known_traffic(kernel):
     """DRAM bytes (read + write) per launch of `kernel` on this workload, from an ncu
     capture recorded in profiles/kernel_traffic.txt, or None when the recorded capture
-    was taken on different CUDA sources (any change to csrc invalidates it)."""
+    was taken on different sources of that kernel (csrc_hash(kernel))."""
     path = os.path.join(ROOT, "profiles", "kernel_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -124,7 +137,7 @@ def known_traffic(kernel):
         for line in f:
             parts = line.split()
             if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == WORKLOAD \
-                    and parts[2] == csrc_hash():
+                    and parts[2] == csrc_hash(kernel):
                 return int(parts[3])
     return None
 
