@@ -49,7 +49,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics", "cross", "decode", "backward"],
+    ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics", "cross", "decode", "backward",
+                                            "backward_causal"],
                     default="both",
                     help="which forward(s) one step runs (default: both, the headline step); "
                          "diagnostics: one step is gma_diagnostics over the workload's query vectors; "
@@ -895,14 +896,25 @@ def run_decode(args, rank, world, local):
     return 0
 
 
-BWD_METRIC = "GMA bidirectional backward token·heads/s (gradients of Qx, Kx, V, mu, rho, alpha; section 4.1)"
-# fp32 flops per row of one head in the backward kernels (2 per multiply-add): the memory pass
-# (scores 2(2d)K, memory 2K(dv+1)), the query pass (scores, read 2K dv, g^Q 2 dv K, dQx 4Kd,
-# [R | r] 2K(dv+1), parameter sums 4Kd) and the key pass (scores, g^K, dV, dKx, parameter sums)
+BWD_METRIC = "GMA {} backward token·heads/s (gradients of Qx, Kx, V, mu, rho, alpha; section 4.1)"
+
+
 def bwd_flops_per_row(w):
-    sc = 2 * 2 * w.d * w.K
-    return (sc + 2 * w.K * (w.dv + 1)) + (sc + 4 * w.K * w.dv + 4 * w.K * w.d + 2 * w.K * (w.dv + 1) + 4 * w.K * w.d) \
-        + (sc + 4 * w.K * w.dv + 4 * w.K * w.d + 4 * w.K * w.d)
+    """fp32 flops the backward kernels compute per row of one head (2 per multiply-add; the
+    masked 64 x 64 tile products of the causal passes counted in full)."""
+    sc = 2 * 2 * w.d * w.K                                   # scores [x, x^2] . W
+    mem = sc + 2 * w.K * (w.dv + 1)                          # memory pass
+    rows = 4 * w.K * w.d + 4 * w.K * w.d                     # dX (two products) + parameter sums
+    if not w.causal:
+        qry = sc + 4 * w.K * w.dv + 2 * w.K * (w.dv + 1) + rows
+        key = sc + 4 * w.K * w.dv + rows
+        return mem + qry + key
+    t = 2 * 64                                               # one 64-row tile product per row, per K/dv column
+    qry = 2 * sc + t * w.K + 2 * w.K * w.dv + t * w.dv + t * w.dv + 2 * w.dv * w.K + t * w.K \
+        + 2 * w.K * w.dv + 2 * w.K * w.dv                    # A, num, Bm, g^Q, [R | r] totals, state update
+    key = 2 * sc + t * w.dv + t * w.K + 2 * w.dv * w.K + t * w.K + t * w.dv + 2 * w.K * w.dv \
+        + 2 * w.K * w.dv                                     # Ct, g^K, Dt, dV, state update
+    return mem + qry + key + 2 * rows
 
 
 def bwd_oracle_sample(w, seconds):
@@ -916,7 +928,7 @@ def bwd_oracle_sample(w, seconds):
     reps, t0 = 0, time.perf_counter()
     while reps == 0 or time.perf_counter() - t0 < seconds:
         oracle.backward_head(*(inputs.widen(x[n][0, 0], w.dtype) for n in ("Qx", "Kx", "V")), x["mu"][0],
-                             x["rho"][0], x["alpha"][0], w.var_floor, w.eps, False, dO)
+                             x["rho"][0], x["alpha"][0], w.var_floor, w.eps, w.causal, dO)
         reps += 1
     dt = (time.perf_counter() - t0) / reps
     return w.N / dt, reps, dt
@@ -928,12 +940,13 @@ def run_backward(args, rank, world, local):
     import torch
     import gaussian_mixture_latent_gb300 as gma
     from gaussian_mixture_latent_gb300 import _build
-    w = inputs.WORKLOADS[args.workload].replace(causal=False)
+    w = inputs.WORKLOADS[args.workload].replace(causal=args.direction == "backward_causal")
+    metric = BWD_METRIC.format("causal" if w.causal else "bidirectional")
     if args.impl == "reference":
         if rank != 0:
             return 0
         rate, reps, dt = bwd_oracle_sample(w, 12.0)
-        print(json.dumps({"impl": "reference", "metric": BWD_METRIC, "value": rate, "unit": "tokens·heads/s",
+        print(json.dumps({"impl": "reference", "metric": metric, "value": rate, "unit": "tokens·heads/s",
                           "n_gpus": args.gpus, "steps": reps, "warmup": 0, "ms_per_step": dt * 1e3,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                           "data": "synthetic", "config": {"workload": w.name, "step": "backward (sampled)"},
@@ -965,7 +978,7 @@ def run_backward(args, rank, world, local):
 
     def step(x):
         gma.gma_backward(x["Qx"], x["Kx"], x["V"], x["mu"], x["rho"], x["alpha"], x["dO"], eps=w.eps,
-                         var_floor=w.var_floor, grads=grads)
+                         var_floor=w.var_floor, causal=w.causal, grads=grads)
 
     warm = max(3, args.warmup)
     for it in range(warm):
@@ -997,18 +1010,21 @@ def run_backward(args, rank, world, local):
         rate, reps, dt = bwd_oracle_sample(w, 12.0)
         cpu = {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
                "sample": f"one head of {w.name} (N = {w.N}), {reps} passes"}
-    print(json.dumps({"metric": BWD_METRIC, "value": units / (ms / 1e3), "unit": "tokens·heads/s", "n_gpus": 1,
+    print(json.dumps({"metric": metric, "value": units / (ms / 1e3), "unit": "tokens·heads/s", "n_gpus": 1,
                       "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
                       "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                       "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K, "dv": w.dv,
-                                 "inputs": w.dtype, "step": "bidirectional backward, all gradients",
+                                 "inputs": w.dtype,
+                                 "step": f"{'causal' if w.causal else 'bidirectional'} backward, all gradients",
                                  "l2": "two alternating input sets (> 129 MB L2)", "parallelism": "single GPU"},
                       "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
                                    "frac": achieved / alu_peak, "traffic": None,
-                                   "kernel": "gma_backward (whole call: 7 launches)", "kernel_ms": ms,
+                                   "kernel": f"gma_backward (whole call: {9 if w.causal else 7} launches)",
+                                   "kernel_ms": ms,
                                    "flops_per_row": bwd_flops_per_row(w),
                                    "peak_source": "fp32 lanes x 2 x 2070 MHz"},
-                      "clocks": clocks, "gpu_launches": 7 * steps, "cpu_baseline": cpu}), flush=True)
+                      "clocks": clocks, "gpu_launches": (9 if w.causal else 7) * steps, "cpu_baseline": cpu}),
+          flush=True)
     return 0
 
 
@@ -1021,7 +1037,7 @@ def main():
         return run_diagnostics(args, rank, world, local)
     if args.direction == "cross":
         return run_cross(args, rank, world, local)
-    if args.direction == "backward":
+    if args.direction in ("backward", "backward_causal"):
         return run_backward(args, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, rank, world)

@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_pass_kernel(BwdArgs a) {
             gs[m * kRS + lane + 32] = e1;
             if (MODE == kQry) {
                 const float z = bwd_warp_sum(e0 * zr[lane] + e1 * zr[lane + 32]);
-                if (lane == 0) den[m] = z + a.eps;
+                if (lane == 0) den[m] = live ? z + a.eps : 1.f;      // rows past the end: a = b = 0 even at eps = 0
             }
         }
         __syncthreads();
@@ -465,12 +465,522 @@ __global__ void __launch_bounds__(2 * kD) bwd_param_kernel(int B, int H, int C, 
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Causal backward (prefix memories of Eq. 6b / 8b).  Each CTA walks the tiles of its row
+// chunk in order (queries) or in reverse (keys), carrying the memory of everything before
+// (S, z) or after (R, r) the tile.  Within a tile, with the causal mask [j <= i]:
+//   A  = tril(G^Q G^K^T),  num = G^Q S + A V,  den = G^Q z + A 1 + eps
+//   Bm = tril(a V^T + b 1^T),  g^Q = a S^T + b z^T + Bm G^K
+//   Ct = (tril(a V^T + b 1^T))^T,  g^K = Ct G^Q + V R^T + r
+//   Dt = (tril(G^Q G^K^T))^T,      dV  = Dt a + G^K R
+// ds of either side goes to global memory; bwd_rows_kernel turns it into dX and the
+// parameter sums.
+
+constexpr int kTile = kTN * kRS;                  // one [TN][kRS] tile buffer
+constexpr int CC_W = 0;                           // [2d][K]
+constexpr int CC_CP = CC_W + 2 * kD * kK;         // [K]
+constexpr int CC_M = CC_CP + kK;                  // [K][dv]   S (queries) or R (keys)
+constexpr int CC_MT = CC_M + kK * kDV;            // [dv][K]   its transpose
+constexpr int CC_ZR = CC_MT + kDV * kK;           // [K]       z or r
+constexpr int CC_T = CC_ZR + kK;                  // nine tile buffers
+constexpr int CC_DEN = CC_T + 9 * kTile;          // [TN]
+constexpr int CC_B = CC_DEN + kTN;                // [TN]
+constexpr int kCSmemFloats = CC_B + kTN;
+constexpr size_t kCSmemBytes = sizeof(float) * kCSmemFloats;
+static_assert(kCSmemBytes <= 227 * 1024, "causal pass CTA shared memory");
+static_assert((CC_M | CC_MT | CC_T | kTile) % 4 == 0, "float4 rows");
+
+struct BwdCArgs {
+    int N, H, C, rows_per_chunk;
+    float eps;
+    const void *Qx, *Kx, *V, *dO;                 // [G][N][d] / [G][N][dv]
+    const float *mu, *lam, *cdir;
+    const float *mem;                             // [G][C][K][W]: S|z before (queries) / R|r after (keys) the chunk
+    float *ab;                                    // [G][N][kRS]: a (dv columns), b, zeros
+    float *ds;                                    // [G][N][K]
+    float *dV;                                    // keys: [G][N][dv]
+    float *part_m;                                // queries: [G][C][K][W] chunk totals of [R | r]
+};
+
+// W, c' (Eq. 16, expanded) and the chunk's starting memory, from global memory.
+__device__ void causal_prologue(const BwdCArgs &a, float *sm, int h, const float *mem_chunk) {
+    const float *lam_h = a.lam + (size_t)h * kK * kD, *mu_h = a.mu + (size_t)h * kK * kD;
+    float *W = sm + CC_W, *cp = sm + CC_CP, *M = sm + CC_M, *MT = sm + CC_MT, *zr = sm + CC_ZR;
+    for (int e = threadIdx.x; e < 2 * kD * kK; e += kBT) {
+        const int q = e / kK, k = e % kK;
+        W[e] = q < kD ? lam_h[k * kD + q] * mu_h[k * kD + q] : -0.5f * lam_h[k * kD + q - kD];
+    }
+    if (threadIdx.x < kK) {
+        const int k = threadIdx.x;
+        float s = 0.f;
+        for (int j = 0; j < kD; ++j) {
+            const float m = mu_h[k * kD + j];
+            s = fmaf(lam_h[k * kD + j] * m, m, s);
+        }
+        cp[k] = a.cdir[(size_t)h * kK + k] - 0.5f * s;
+    }
+    for (int e = threadIdx.x; e < kK * kW; e += kBT) {
+        const int k = e / kW, c = e - k * kW;
+        const float v = mem_chunk[e];
+        if (c < kDV) {
+            M[k * kDV + c] = v;
+            MT[c * kK + k] = v;
+        } else {
+            zr[k] = v;
+        }
+    }
+}
+
+// Rows t0 .. t0 + mv - 1 of a [G][N][64] input (head base `src`) into a tile buffer; zeros below.
+template <typename TI>
+__device__ __forceinline__ void load_tile(float *dst, const TI *src, int t0, int mv) {
+    const int lm = threadIdx.x >> 2, lj = (threadIdx.x & 3) * 16;
+    Row16<TI> r;
+    r.load(src + (size_t)(t0 + lm) * kD + lj, lm < mv);
+    r.store(dst + lm * kRS + lj);
+}
+
+// Scores of the tile rows in xs into gs: s = c' + [x, x^2] . W (Eq. 16, expanded).
+__device__ __forceinline__ void tile_scores(const float *W, const float *cp, const float *xs, float *gs, int r0,
+                                            int c0) {
+    float c[4][4];
+    zero4x4(c);
+    mm_rows<kD>(c, xs, kRS, r0, W, kK, c0);
+#pragma unroll 4
+    for (int s = 0; s < kD; ++s) {
+        float x2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float v = xs[(r0 + i) * kRS + s];
+            x2[i] = v * v;
+        }
+        fma4x4(c, x2, ld4(W + (kD + s) * kK + c0));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) gs[(r0 + i) * kRS + c0 + j] = cp[c0 + j] + c[i][j];
+}
+
+// Eq. 3b over the rows of gs, a warp per row; rows >= mv get 0.  gT, if given, receives the
+// transpose ([k][row], stride kRS).
+__device__ __forceinline__ void tile_softmax(float *gs, float *gT, int mv) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int m = warp; m < kTN; m += kBT / 32) {
+        const float s0 = gs[m * kRS + lane], s1 = gs[m * kRS + lane + 32];
+        const float mx = bwd_warp_max(fmaxf(s0, s1));
+        float e0 = expf(s0 - mx), e1 = expf(s1 - mx);
+        const float inv = 1.0f / bwd_warp_sum(e0 + e1);
+        const bool live = m < mv;
+        e0 = live ? e0 * inv : 0.f;
+        e1 = live ? e1 * inv : 0.f;
+        gs[m * kRS + lane] = e0;
+        gs[m * kRS + lane + 32] = e1;
+        if (gT) {
+            gT[lane * kRS + m] = e0;
+            gT[(lane + 32) * kRS + m] = e1;
+        }
+    }
+}
+
+// Eq. 18 over the rows of gg (the upstream gradient g), in place: ds = gamma (g - gamma . g);
+// the live rows also go to global memory (head base `out`, rows from t0).
+__device__ __forceinline__ void tile_ds(const float *gam, float *gg, float *out, int t0, int mv) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int m = warp; m < kTN; m += kBT / 32) {
+        const float g0 = gam[m * kRS + lane], g1 = gam[m * kRS + lane + 32];
+        const float u0 = gg[m * kRS + lane], u1 = gg[m * kRS + lane + 32];
+        const float mean = bwd_warp_sum(g0 * u0 + g1 * u1);
+        const float d0 = g0 * (u0 - mean), d1 = g1 * (u1 - mean);
+        gg[m * kRS + lane] = d0;
+        gg[m * kRS + lane + 32] = d1;
+        if (m < mv) {
+            out[(size_t)(t0 + m) * kK + lane] = d0;
+            out[(size_t)(t0 + m) * kK + lane + 32] = d1;
+        }
+    }
+}
+
+// Queries, tiles in order, carrying S and z (the prefix memory of Eq. 6b before the tile).
+template <typename TI>
+__global__ void __launch_bounds__(kBT, 1) bwd_cq_kernel(BwdCArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
+    const int ch = blockIdx.x, g = blockIdx.y, h = g % a.H;
+    float *W = sm + CC_W, *cp = sm + CC_CP, *M = sm + CC_M, *MT = sm + CC_MT, *zr = sm + CC_ZR;
+    float *XS = sm + CC_T, *VS = XS + kTile, *VT = VS + kTile, *US = VT + kTile, *GQ = US + kTile;
+    float *GK = GQ + kTile, *GKT = GK + kTile, *AS = GKT + kTile, *GG = AS + kTile;
+    float *den = sm + CC_DEN, *bb = sm + CC_B;
+    const size_t slot = (size_t)g * a.C + ch;
+    causal_prologue(a, sm, h, a.mem + slot * kK * kW);
+    const TI *Qx = static_cast<const TI *>(a.Qx) + (size_t)g * a.N * kD;
+    const TI *Kx = static_cast<const TI *>(a.Kx) + (size_t)g * a.N * kD;
+    const TI *V = static_cast<const TI *>(a.V) + (size_t)g * a.N * kDV;
+    const TI *dO = static_cast<const TI *>(a.dO) + (size_t)g * a.N * kDV;
+    float *dsq = a.ds + (size_t)g * a.N * kK, *ab = a.ab + (size_t)g * a.N * kRS;
+    float accM[4][4];
+    zero4x4(accM);
+    float ex_m = 0.f;
+    __syncthreads();
+    const int row_begin = ch * a.rows_per_chunk, row_end = min(a.N, row_begin + a.rows_per_chunk);
+    for (int t0 = row_begin; t0 < row_end; t0 += kTN) {
+        const int mv = min(kTN, row_end - t0);
+        // the tile's keys: gamma^K (and its transpose), V (and its transpose)
+        load_tile(XS, Kx, t0, mv);
+        load_tile(VS, V, t0, mv);
+        __syncthreads();
+        for (int e = tid; e < kTN * kDV; e += kBT) {
+            const int j = e % kTN, c = e / kTN;
+            VT[c * kRS + j] = VS[j * kRS + c];
+        }
+        tile_scores(W, cp, XS, GK, r0, c0);
+        __syncthreads();
+        tile_softmax(GK, GKT, mv);
+        __syncthreads();
+        // the tile's queries: gamma^Q, dO, den = gamma^Q . z (the causal part added below)
+        load_tile(XS, Qx, t0, mv);
+        load_tile(US, dO, t0, mv);
+        __syncthreads();
+        tile_scores(W, cp, XS, GQ, r0, c0);
+        __syncthreads();
+        tile_softmax(GQ, nullptr, mv);
+        __syncthreads();
+        for (int m = warp; m < kTN; m += kBT / 32) {
+            const float z = bwd_warp_sum(GQ[m * kRS + lane] * zr[lane] + GQ[m * kRS + lane + 32] * zr[lane + 32]);
+            if (lane == 0) den[m] = z;
+        }
+        {   // A = tril(gamma^Q gamma^K^T): rows i (queries), columns j (keys)
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kK>(c, GQ, kRS, r0, GKT, kRS, c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) AS[(r0 + i) * kRS + c0 + j] = c0 + j <= r0 + i ? c[i][j] : 0.f;
+        }
+        __syncthreads();
+        for (int m = warp; m < kTN; m += kBT / 32) {
+            const float s = bwd_warp_sum(AS[m * kRS + lane] + AS[m * kRS + lane + 32]);
+            if (lane == 0) den[m] = m < mv ? den[m] + s + a.eps : 1.f;   // rows past the end: a = b = 0
+        }
+        __syncthreads();
+        {   // num = gamma^Q S + A V; O = num / den; a = dO / den, b = -(dO . O) / den
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kK>(c, GQ, kRS, r0, M, kDV, c0);
+            mm_rows<kTN>(c, AS, kRS, r0, VS, kRS, c0);
+            float dot[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float dn = den[r0 + i];
+                float p = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float *q = US + (r0 + i) * kRS + c0 + j;
+                    p = fmaf(*q, c[i][j] / dn, p);
+                    *q = *q / dn;
+                }
+                dot[i] = p;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                for (int o = 8; o; o >>= 1) dot[i] += __shfl_xor_sync(~0u, dot[i], o);
+            if ((tid & 15) == 0)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) bb[r0 + i] = -dot[i] / den[r0 + i];
+        }
+        __syncthreads();
+        {   // Bm = tril(a V^T + b 1^T)
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kDV>(c, US, kRS, r0, VT, kRS, c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    AS[(r0 + i) * kRS + c0 + j] = c0 + j <= r0 + i ? c[i][j] + bb[r0 + i] : 0.f;
+        }
+        __syncthreads();
+        {   // g^Q = a S^T + b z^T + Bm gamma^K
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kDV>(c, US, kRS, r0, MT, kK, c0);
+            mm_rows<kTN>(c, AS, kRS, r0, GK, kRS, c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) GG[(r0 + i) * kRS + c0 + j] = fmaf(bb[r0 + i], zr[c0 + j], c[i][j]);
+        }
+        __syncthreads();
+        tile_ds(GQ, GG, dsq, t0, mv);
+        // a | b of the live rows for the key pass
+        for (int e = tid; e < mv * kRS; e += kBT) {
+            const int m = e / kRS, c = e - m * kRS;
+            ab[(size_t)(t0 + m) * kRS + c] = c < kDV ? US[m * kRS + c] : (c == kDV ? bb[m] : 0.f);
+        }
+        // chunk totals of [R | r] = sum_i gamma^Q_i [a_i | b_i]
+        mm_cols(accM, GQ, kRS, r0, US, kRS, c0);
+        if (tid < kK)
+            for (int m = 0; m < kTN; ++m) ex_m = fmaf(GQ[m * kRS + tid], bb[m], ex_m);
+        {   // the prefix memory now includes the tile: S += gamma^K^T V, z += gamma^K^T 1
+            float u[4][4];
+            zero4x4(u);
+            mm_cols(u, GK, kRS, r0, VS, kRS, c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    M[(r0 + i) * kDV + c0 + j] += u[i][j];
+                    MT[(c0 + j) * kK + r0 + i] += u[i][j];
+                }
+            if (tid >= kK && tid < 2 * kK) {
+                float zs = 0.f;
+                for (int m = 0; m < kTN; ++m) zs += GK[m * kRS + tid - kK];
+                zr[tid - kK] += zs;
+            }
+        }
+        __syncthreads();
+    }
+    float *pm = a.part_m + slot * kK * kW;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pm[(r0 + i) * kW + c0 + j] = accM[i][j];
+    if (tid < kK) pm[tid * kW + kDV] = ex_m;
+}
+
+// Keys, tiles in reverse order, carrying R and r (the rows after the tile).
+template <typename TI>
+__global__ void __launch_bounds__(kBT, 1) bwd_ck_kernel(BwdCArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const int tid = threadIdx.x;
+    const int r0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
+    const int ch = blockIdx.x, g = blockIdx.y, h = g % a.H;
+    float *W = sm + CC_W, *cp = sm + CC_CP, *M = sm + CC_M, *MT = sm + CC_MT, *zr = sm + CC_ZR;
+    float *XS = sm + CC_T, *GQ = XS + kTile, *GQT = GQ + kTile, *US = GQT + kTile, *AT = US + kTile;
+    float *GK = AT + kTile, *VS = GK + kTile, *CM = VS + kTile, *GG = CM + kTile;
+    const size_t slot = (size_t)g * a.C + ch;
+    causal_prologue(a, sm, h, a.mem + slot * kK * kW);
+    const TI *Qx = static_cast<const TI *>(a.Qx) + (size_t)g * a.N * kD;
+    const TI *Kx = static_cast<const TI *>(a.Kx) + (size_t)g * a.N * kD;
+    const TI *V = static_cast<const TI *>(a.V) + (size_t)g * a.N * kDV;
+    const float *ab = a.ab + (size_t)g * a.N * kRS;
+    float *dsk = a.ds + (size_t)g * a.N * kK, *dV = a.dV + (size_t)g * a.N * kDV;
+    __syncthreads();
+    const int row_begin = ch * a.rows_per_chunk, row_end = min(a.N, row_begin + a.rows_per_chunk);
+    const int ntiles = row_end > row_begin ? (row_end - row_begin + kTN - 1) / kTN : 0;
+    for (int tt = ntiles - 1; tt >= 0; --tt) {
+        const int t0 = row_begin + tt * kTN, mv = min(kTN, row_end - t0);
+        // the tile's queries: gamma^Q (and its transpose), a | b (and a's transpose)
+        load_tile(XS, Qx, t0, mv);
+        for (int e = tid; e < kTN * (kRS / 4); e += kBT) {
+            const int m = e / (kRS / 4), q = e - m * (kRS / 4);
+            reinterpret_cast<float4 *>(US + m * kRS)[q] =
+                m < mv ? reinterpret_cast<const float4 *>(ab + (size_t)(t0 + m) * kRS)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();
+        for (int e = tid; e < kTN * kDV; e += kBT) {
+            const int i = e % kTN, c = e / kTN;
+            AT[c * kRS + i] = US[i * kRS + c];
+        }
+        tile_scores(W, cp, XS, GQ, r0, c0);
+        __syncthreads();
+        tile_softmax(GQ, GQT, mv);
+        __syncthreads();
+        // the tile's keys: gamma^K, V
+        load_tile(XS, Kx, t0, mv);
+        load_tile(VS, V, t0, mv);
+        __syncthreads();
+        tile_scores(W, cp, XS, GK, r0, c0);
+        __syncthreads();
+        tile_softmax(GK, nullptr, mv);
+        __syncthreads();
+        {   // Ct[j][i] = [i >= j] (v_j . a_i + b_i): rows j (keys), columns i (queries)
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kDV>(c, VS, kRS, r0, AT, kRS, c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    CM[(r0 + j) * kRS + c0 + i] = c0 + i >= r0 + j ? c[j][i] + US[(c0 + i) * kRS + kDV] : 0.f;
+        }
+        __syncthreads();
+        {   // g^K = Ct gamma^Q + V R^T + r
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kTN>(c, CM, kRS, r0, GQ, kRS, c0);
+            mm_rows<kDV>(c, VS, kRS, r0, MT, kK, c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) GG[(r0 + j) * kRS + c0 + k] = c[j][k] + zr[c0 + k];
+        }
+        __syncthreads();
+        {   // Dt[j][i] = [i >= j] gamma^K_j . gamma^Q_i
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kK>(c, GK, kRS, r0, GQT, kRS, c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) CM[(r0 + j) * kRS + c0 + i] = c0 + i >= r0 + j ? c[j][i] : 0.f;
+        }
+        __syncthreads();
+        {   // dV = Dt a + gamma^K R
+            float c[4][4];
+            zero4x4(c);
+            mm_rows<kTN>(c, CM, kRS, r0, US, kRS, c0);
+            mm_rows<kK>(c, GK, kRS, r0, M, kDV, c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (r0 + j < mv)
+                    *reinterpret_cast<float4 *>(dV + (size_t)(t0 + r0 + j) * kDV + c0) =
+                        make_float4(c[j][0], c[j][1], c[j][2], c[j][3]);
+        }
+        tile_ds(GK, GG, dsk, t0, mv);
+        __syncthreads();
+        {   // the memory of the rows after the next tile: R += gamma^Q^T a, r += gamma^Q^T b
+            float u[4][4];
+            zero4x4(u);
+            mm_cols(u, GQ, kRS, r0, US, kRS, c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    M[(r0 + i) * kDV + c0 + j] += u[i][j];
+                    MT[(c0 + j) * kK + r0 + i] += u[i][j];
+                }
+            if (tid < kK) {
+                float rs = 0.f;
+                for (int m = 0; m < kTN; ++m) rs = fmaf(GQ[m * kRS + tid], US[m * kRS + kDV], rs);
+                zr[tid] += rs;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// dX = -sum_k ds_k lambda_k (x - mu_k) (section 4.3) and the parameter sums P1 = sum ds x,
+// P2 = sum ds x^2, P0 = sum ds of the rows of one side, from ds in global memory.
+template <typename TI>
+__global__ void __launch_bounds__(kBT, 1) bwd_rows_kernel(int N, int H, int C, int rows_per_chunk,
+                                                          const void *Xv, const float *__restrict__ ds,
+                                                          const float *__restrict__ mu,
+                                                          const float *__restrict__ lam, float *__restrict__ dX,
+                                                          float *__restrict__ part_p) {
+    extern __shared__ __align__(16) float sm[];
+    float *LAM = sm, *LMU = LAM + kK * kD, *XS = LMU + kK * kD, *DS = XS + kTile;
+    const int tid = threadIdx.x;
+    const int r0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
+    const int ch = blockIdx.x, g = blockIdx.y, h = g % H;
+    const float *lam_h = lam + (size_t)h * kK * kD, *mu_h = mu + (size_t)h * kK * kD;
+    for (int e = tid; e < kK * kD; e += kBT) {
+        const float l = lam_h[e];
+        LAM[e] = l;
+        LMU[e] = l * mu_h[e];
+    }
+    const TI *X = static_cast<const TI *>(Xv) + (size_t)g * N * kD;
+    const float *dsg = ds + (size_t)g * N * kK;
+    float *dXg = dX + (size_t)g * N * kD;
+    float accP1[4][4], accP2[4][4];
+    zero4x4(accP1);
+    zero4x4(accP2);
+    float ex_p = 0.f;
+    __syncthreads();
+    const int row_begin = ch * rows_per_chunk, row_end = min(N, row_begin + rows_per_chunk);
+    for (int t0 = row_begin; t0 < row_end; t0 += kTN) {
+        const int mv = min(kTN, row_end - t0);
+        load_tile(XS, X, t0, mv);
+        for (int e = tid; e < kTN * (kK / 4); e += kBT) {
+            const int m = e / (kK / 4), q = e - m * (kK / 4);
+            reinterpret_cast<float4 *>(DS + m * kRS)[q] =
+                m < mv ? reinterpret_cast<const float4 *>(dsg + (size_t)(t0 + m) * kK)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();
+        float c1[4][4], c2[4][4];
+        zero4x4(c1);
+        zero4x4(c2);
+#pragma unroll 4
+        for (int s = 0; s < kK; ++s) {
+            const float d4[4] = {DS[(r0 + 0) * kRS + s], DS[(r0 + 1) * kRS + s], DS[(r0 + 2) * kRS + s],
+                                 DS[(r0 + 3) * kRS + s]};
+            fma4x4(c1, d4, ld4(LAM + s * kD + c0));
+            fma4x4(c2, d4, ld4(LMU + s * kD + c0));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (r0 + i >= mv) continue;
+            const float *x = XS + (r0 + i) * kRS + c0;
+            *reinterpret_cast<float4 *>(dXg + (size_t)(t0 + r0 + i) * kD + c0) =
+                make_float4(fmaf(-x[0], c1[i][0], c2[i][0]), fmaf(-x[1], c1[i][1], c2[i][1]),
+                            fmaf(-x[2], c1[i][2], c2[i][2]), fmaf(-x[3], c1[i][3], c2[i][3]));
+        }
+#pragma unroll 4
+        for (int m = 0; m < kTN; ++m) {
+            const float4 d4 = ld4(DS + m * kRS + r0);
+            const float dk[4] = {d4.x, d4.y, d4.z, d4.w};
+            const float4 x4 = ld4(XS + m * kRS + c0);
+            fma4x4(accP1, dk, x4);
+            fma4x4(accP2, dk, make_float4(x4.x * x4.x, x4.y * x4.y, x4.z * x4.z, x4.w * x4.w));
+        }
+        if (tid >= kK && tid < 2 * kK)
+            for (int m = 0; m < kTN; ++m) ex_p += DS[m * kRS + tid - kK];
+        __syncthreads();
+    }
+    float *pp = part_p + ((size_t)g * C + ch) * kK * kPW;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            pp[(r0 + i) * kPW + c0 + j] = accP1[i][j];
+            pp[(r0 + i) * kPW + kD + c0 + j] = accP2[i][j];
+        }
+    if (tid >= kK && tid < 2 * kK) pp[(tid - kK) * kPW + 2 * kD] = ex_p;
+}
+
+// out[g][c] = sum of part[g][c'] over the chunks before c (reverse: after c), in chunk order.
+__global__ void bwd_scan_kernel(int C, int E, int reverse, const float *__restrict__ part, float *__restrict__ out) {
+    const int g = blockIdx.y, e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    float run = 0.f;
+    for (int i = 0; i < C; ++i) {
+        const int c = reverse ? C - 1 - i : i;
+        const size_t o = ((size_t)g * C + c) * E + e;
+        out[o] = run;
+        run += part[o];
+    }
+}
+
 template <int MODE>
 cudaError_t launch_pass(const Problem &p, const BwdLayout &L, const BwdArgs &a, cudaStream_t s) {
     auto kern = p.in_dtype == GMA_BF16 ? bwd_pass_kernel<MODE, __nv_bfloat16> : bwd_pass_kernel<MODE, float>;
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), (int)kBwdSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<dim3(L.C, p.G), kBT, kBwdSmemBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <template <typename> class KERN>
+cudaError_t launch_causal(const Problem &p, const BwdLayout &L, const BwdCArgs &a, cudaStream_t s) {
+    auto kern = p.in_dtype == GMA_BF16 ? KERN<__nv_bfloat16>::fn : KERN<float>::fn;
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), (int)kCSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(L.C, p.G), kBT, kCSmemBytes, s>>>(a);
+    return cudaGetLastError();
+}
+template <typename TI> struct CqKernel { static constexpr auto fn = bwd_cq_kernel<TI>; };
+template <typename TI> struct CkKernel { static constexpr auto fn = bwd_ck_kernel<TI>; };
+
+constexpr size_t kRowsSmemBytes = sizeof(float) * (2 * kK * kD + 2 * kTile);
+
+cudaError_t launch_rows(const Problem &p, const BwdLayout &L, const void *X, const float *ds, const float *mu,
+                        const float *lam, float *dX, float *part_p, cudaStream_t s) {
+    auto kern = p.in_dtype == GMA_BF16 ? bwd_rows_kernel<__nv_bfloat16> : bwd_rows_kernel<float>;
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), (int)kRowsSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(L.C, p.G), kBT, kRowsSmemBytes, s>>>(p.N, p.H, L.C, L.rows_per_chunk, X, ds, mu, lam, dX, part_p);
     return cudaGetLastError();
 }
 
@@ -483,7 +993,7 @@ int device_sms() {
 
 }  // namespace
 
-bool bwd_supported(const Problem &p) { return p.d == kD && p.K == kK && p.dv == kDV && !p.causal; }
+bool bwd_supported(const Problem &p) { return p.d == kD && p.K == kK && p.dv == kDV; }
 
 BwdLayout bwd_layout(const Problem &p) {
     BwdLayout L{};
@@ -511,6 +1021,14 @@ BwdLayout bwd_layout(const Problem &p) {
     L.part_q = align_up(L.part_m + sizeof(float) * (size_t)p.G * L.C * kK * kW);
     L.part_k = align_up(L.part_q + sizeof(float) * (size_t)p.G * L.C * kK * kPW);
     L.total = align_up(L.part_k + sizeof(float) * (size_t)p.G * L.C * kK * kPW);
+    if (p.causal) {     // per-chunk starting memories, a | b and ds of every row
+        L.mem_pc = L.total;
+        L.mem_rc = align_up(L.mem_pc + sizeof(float) * (size_t)p.G * L.C * kK * kW);
+        L.ab = align_up(L.mem_rc + sizeof(float) * (size_t)p.G * L.C * kK * kW);
+        L.dsq = align_up(L.ab + sizeof(float) * (size_t)p.G * p.N * kRS);
+        L.dsk = align_up(L.dsq + sizeof(float) * (size_t)p.G * p.N * kK);
+        L.total = align_up(L.dsk + sizeof(float) * (size_t)p.G * p.N * kK);
+    }
     return L;
 }
 
@@ -533,6 +1051,47 @@ cudaError_t bwd_run(const Problem &p, const BwdLayout &L, const void *Qx, const 
     a.lam = lam;
     a.cdir = cdir;
     const dim3 sum_grid((kK * kW + 255) / 256, p.G);
+    if (p.causal) {
+        float *mem_pc = reinterpret_cast<float *>(ws + L.mem_pc), *mem_rc = reinterpret_cast<float *>(ws + L.mem_rc);
+        float *ab = reinterpret_cast<float *>(ws + L.ab);
+        float *dsq = reinterpret_cast<float *>(ws + L.dsq), *dsk = reinterpret_cast<float *>(ws + L.dsk);
+        // chunk totals of [S | z] (Eq. 6b), then each chunk's starting prefix
+        a.X = Kx;
+        a.U = V;
+        a.part_m = part_m;
+        if ((e = launch_pass<kMem>(p, L, a, s)) != cudaSuccess) return e;
+        bwd_scan_kernel<<<sum_grid, 256, 0, s>>>(L.C, kK * kW, 0, part_m, mem_pc);
+        BwdCArgs c{};
+        c.N = p.N;
+        c.H = p.H;
+        c.C = L.C;
+        c.rows_per_chunk = L.rows_per_chunk;
+        c.eps = p.eps;
+        c.Qx = Qx;
+        c.Kx = Kx;
+        c.V = V;
+        c.dO = dO;
+        c.mu = mu;
+        c.lam = lam;
+        c.cdir = cdir;
+        c.ab = ab;
+        // queries in order: ds^Q, a | b, chunk totals of [R | r]
+        c.mem = mem_pc;
+        c.ds = dsq;
+        c.part_m = part_m;
+        if ((e = launch_causal<CqKernel>(p, L, c, s)) != cudaSuccess) return e;
+        bwd_scan_kernel<<<sum_grid, 256, 0, s>>>(L.C, kK * kW, 1, part_m, mem_rc);
+        // keys in reverse: ds^K, dV
+        c.mem = mem_rc;
+        c.ds = dsk;
+        c.dV = dV;
+        if ((e = launch_causal<CkKernel>(p, L, c, s)) != cudaSuccess) return e;
+        if ((e = launch_rows(p, L, Qx, dsq, mu, lam, dQx, part_q, s)) != cudaSuccess) return e;
+        if ((e = launch_rows(p, L, Kx, dsk, mu, lam, dKx, part_k, s)) != cudaSuccess) return e;
+        bwd_param_kernel<<<dim3(kK, p.H), 2 * kD, 0, s>>>(p.B, p.H, L.C, part_q, part_k, mu, lam, rho, alpha, dmu,
+                                                        drho, dalpha);
+        return cudaGetLastError();
+    }
     // the forward memory [Vt | Z] (Eq. 5-6)
     a.X = Kx;
     a.U = V;

@@ -87,12 +87,14 @@ cudaError_t tc_diag(const Problem &p, const TcLayout &L, const void *Qx, int *z,
 cudaError_t tc_diag_finalize(const Problem &p, const TcLayout &L, float *p_out, float *stats_out, char *ws,
                              cudaStream_t s);
 
-// ----- backward pass, bidirectional, CUDA cores: gma_bwd.cu (uses simt_params) -----
+// ----- backward pass, bidirectional and causal, CUDA cores: gma_bwd.cu (uses simt_params) -----
 struct BwdLayout {
     size_t lam, cdir;            // parameter prologue outputs
     size_t mem_s, mem_r;         // [G][K][dv+1]: the forward memory [Vt | Z] and the backward [R | r]
     size_t part_m;               // [G][C][K][dv+1] per-chunk partials of either memory
     size_t part_q, part_k;       // [G][C][K][2d+1] per-chunk parameter sums over query / key rows
+    size_t mem_pc, mem_rc;       // causal: [G][C][K][dv+1] memories before / after each chunk
+    size_t ab, dsq, dsk;         // causal: [G][N][68] a | b rows, [G][N][K] ds of queries / keys
     size_t total;
     int C, rows_per_chunk;       // row chunks per head
 };

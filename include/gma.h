@@ -132,10 +132,12 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
  * every output overwritten, not accumulated.  Qx, Kx, V in desc->in_dtype and
  * dO in desc->out_dtype, which must be the same type.  Responsibilities and
  * every product in fp32 on the CUDA cores; deterministic (fixed-order
- * reductions).  Implemented: bidirectional (causal = 0), d = dv = K = 64;
- * GMA_ERR_UNSUPPORTED otherwise (the causal backward included).  N = 0 writes
- * zero parameter gradients.  Workspace: gma_backward_workspace_size().  Errors
- * as for gma_forward().
+ * reductions).  causal = 1 differentiates the prefix memories of Eq. 6b / 8b
+ * (each key collects the gradient of the rows at or after it).  Implemented for
+ * d = dv = K = 64; GMA_ERR_UNSUPPORTED otherwise.  N = 0 writes zero parameter
+ * gradients.  Workspace: gma_backward_workspace_size() (the causal workspace
+ * also holds a | b and ds of every row, about 0.8 KB per row of a head).
+ * Errors as for gma_forward().
  */
 gma_status gma_backward_workspace_size(const gma_desc *desc, int causal, size_t *bytes);
 gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const void *Kx, const void *V,

@@ -42,8 +42,8 @@ def gen_dO(shape, dtype, seed):
     return inputs.f32_to_bf16_bits(z) if dtype == "bf16" else z
 
 
-def make(B, H, N, dtype, seed):
-    w = inputs.Workload("bwd", B=B, H=H, N=N, d=64, K=64, dv=64, dtype=dtype, causal=False, seed=seed)
+def make(B, H, N, dtype, seed, causal=False, eps=1e-6):
+    w = inputs.Workload("bwd", B=B, H=H, N=N, d=64, K=64, dv=64, dtype=dtype, causal=causal, seed=seed, eps=eps)
     x = inputs.gen_all(w)
     x["dO"] = gen_dO((B, H, N, 64), dtype, seed)
     return w, x
@@ -52,7 +52,7 @@ def make(B, H, N, dtype, seed):
 def run_gpu(w, x):
     import gaussian_mixture_latent_gb300 as gma
     g = gma.gma_backward(*(to_device(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha", "dO")), eps=w.eps,
-                         var_floor=w.var_floor)
+                         var_floor=w.var_floor, causal=w.causal)
     torch.cuda.synchronize()
     assert gma.gma_get_status() == 0
     return [t.double().cpu().numpy() for t in g]
@@ -62,7 +62,7 @@ def oracle_grads(w, x, b, h):
     import oracle
     wid = lambda a: inputs.widen(a, w.dtype)
     return oracle.backward_head(wid(x["Qx"][b, h]), wid(x["Kx"][b, h]), wid(x["V"][b, h]), x["mu"][h],
-                                x["rho"][h], x["alpha"][h], w.var_floor, w.eps, False, wid(x["dO"][b, h]))
+                                x["rho"][h], x["alpha"][h], w.var_floor, w.eps, w.causal, wid(x["dO"][b, h]))
 
 
 def rel(a, b, floor=0.0):
@@ -99,21 +99,44 @@ def check(w, x, got, heads=None, param_heads=None):
 
 
 CASES = [
-    # B, H, N, dtype
-    (1, 1, 1, "f32"),
-    (2, 3, 63, "f32"),
-    (1, 2, 65, "bf16"),
-    (2, 2, 200, "bf16"),
-    (1, 4, 1000, "f32"),
-    (3, 2, 777, "bf16"),
+    # B, H, N, dtype, causal, eps
+    (1, 1, 1, "f32", False, 1e-6),
+    (2, 3, 63, "f32", False, 1e-6),
+    (1, 2, 65, "bf16", False, 1e-6),
+    (2, 2, 200, "bf16", False, 1e-6),
+    (1, 4, 1000, "f32", False, 1e-6),
+    (3, 2, 777, "bf16", False, 1e-6),
+    (1, 2, 130, "bf16", False, 0.0),
+    (1, 1, 1, "f32", True, 1e-6),
+    (2, 3, 63, "f32", True, 1e-6),
+    (1, 2, 65, "bf16", True, 1e-6),
+    (2, 2, 300, "bf16", True, 1e-6),
+    (1, 3, 1500, "f32", True, 1e-6),
+    (1, 2, 130, "bf16", True, 0.0),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}H{c[1]}N{c[2]}_{c[3]}" for c in CASES])
+@pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}H{c[1]}N{c[2]}_{c[3]}_{'causal' if c[4] else 'bidir'}"
+                                             f"{'_eps0' if c[5] == 0 else ''}" for c in CASES])
 def test_backward_parity(case):
-    B, H, N, dtype = case
-    w, x = make(B, H, N, dtype, seed=N)
+    B, H, N, dtype, causal, eps = case
+    w, x = make(B, H, N, dtype, seed=N, causal=causal, eps=eps)
     check(w, x, run_gpu(w, x))
+
+
+def test_causal_backward_reaches_only_the_prefix():
+    # dO nonzero at row t only: the exact gradient of every other query row, and of every key
+    # and value row after t, is zero, and the kernels produce exact zeros there
+    w, x = make(1, 2, 300, "bf16", seed=5, causal=True)
+    t = 137
+    dO = np.zeros_like(x["dO"])
+    dO[:, :, t] = x["dO"][:, :, t]
+    x["dO"] = dO
+    dQ, dK, dV = run_gpu(w, x)[:3]
+    rows = np.arange(300) != t
+    assert np.abs(dQ[:, :, rows]).max() == 0.0 and np.abs(dQ[:, :, t]).max() > 0
+    assert np.abs(dK[:, :, t + 1:]).max() == 0.0 and np.abs(dV[:, :, t + 1:]).max() == 0.0
+    assert np.abs(dK[:, :, :t + 1]).max() > 0 and np.abs(dV[:, :, :t + 1]).max() > 0
 
 
 def test_backward_is_deterministic():
@@ -124,9 +147,9 @@ def test_backward_is_deterministic():
 
 
 def test_backward_full_size_sampled():
-    # the 96-head N = 8192 workload: row gradients of two heads, parameter gradients of one
-    # head set (all eight batch entries through the oracle)
-    w = inputs.WORKLOADS["causal_bf16_n8192"]
+    # the 96-head N = 8192 workload (bidirectional): row gradients of two heads, parameter
+    # gradients of one head set (all eight batch entries through the oracle)
+    w = inputs.WORKLOADS["causal_bf16_n8192"].replace(causal=False)
     x = inputs.gen_all(w)
     x["dO"] = gen_dO((w.B, w.H, w.N, w.dv), "bf16", 8)
     got = run_gpu(w, x)
@@ -137,9 +160,6 @@ def test_backward_unsupported_and_empty():
     import gaussian_mixture_latent_gb300 as gma
     w, x = make(1, 2, 100, "bf16", seed=1)
     args = [to_device(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha", "dO")]
-    with pytest.raises(gma.GmaError) as e:
-        gma.gma_backward(*args, causal=True)
-    assert e.value.code == 2
     w2 = inputs.Workload("k128", B=1, H=2, N=100, d=64, K=128, dv=64, dtype="bf16", causal=False)
     x2 = inputs.gen_all(w2)
     x2["dO"] = x2["V"]
@@ -150,3 +170,35 @@ def test_backward_unsupported_and_empty():
     g = gma.gma_backward(*empty)
     torch.cuda.synchronize()
     assert all(float(t.abs().max()) == 0.0 for t in g[3:])
+
+
+def test_backward_identities_of_the_gpu_gradients():
+    # properties the exact gradients satisfy at any size, on the GPU's gradients of a
+    # 6-head N = 3000 problem: a common shift of every routing vector and every mean leaves
+    # each score unchanged, so sum_i dQx_i + sum_i dKx_i + sum_k dmu_k = 0 for every head
+    # set and dimension; O is homogeneous of degree one in V (Eq. 7-8), so
+    # sum dV * V = sum dO * O (Euler); and sum_k dalpha_k = 0 (Eq. 15)
+    import oracle
+    w, x = make(2, 3, 3000, "bf16", seed=12)
+    dQ, dK, dV, dmu, drho, dal = run_gpu(w, x)
+    shift = dQ.sum(axis=(0, 2)) + dK.sum(axis=(0, 2)) + dmu.sum(axis=1)           # [H, d]
+    scale = np.abs(dQ).sum(axis=(0, 2)) + np.abs(dK).sum(axis=(0, 2)) + np.abs(dmu).sum(axis=1)
+    assert (np.abs(shift) <= 1e-4 * scale).all(), np.abs(shift / scale).max()
+    O = oracle.forward(*(inputs.widen(x[n], w.dtype) for n in ("Qx", "Kx", "V")), x["mu"], x["rho"], x["alpha"],
+                       w.var_floor, w.eps, False, threads=4)
+    V, dO = inputs.widen(x["V"], w.dtype), inputs.widen(x["dO"], w.dtype)
+    for b in range(w.B):
+        for h in range(w.H):
+            lhs, rhs = float((dV[b, h] * V[b, h]).sum()), float((dO[b, h] * O[b, h]).sum())
+            assert abs(lhs - rhs) <= 1e-4 * np.abs(dO[b, h] * O[b, h]).sum(), (b, h, lhs, rhs)
+    assert (np.abs(dal.sum(axis=1)) <= 1e-4 * np.abs(dal).sum(axis=1)).all()
+
+
+def test_causal_backward_full_size_sampled():
+    # the same workload as a causal backward: row gradients of one head, parameter gradients
+    # of one head set
+    w = inputs.WORKLOADS["causal_bf16_n8192"]
+    x = inputs.gen_all(w)
+    x["dO"] = gen_dO((w.B, w.H, w.N, w.dv), "bf16", 9)
+    got = run_gpu(w, x)
+    check(w, x, got, heads=[(3, 4)], param_heads=[4])
