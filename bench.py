@@ -905,15 +905,15 @@ def bwd_flops_per_row(w):
     sc = 2 * 2 * w.d * w.K                                   # scores [x, x^2] . W
     mem = sc + 2 * w.K * (w.dv + 1)                          # memory pass
     rows = 4 * w.K * w.d + 4 * w.K * w.d                     # dX (two products) + parameter sums
-    if not w.causal:
+    if not w.causal:                                         # the key pass reuses the memory pass's gamma^K
         qry = sc + 4 * w.K * w.dv + 2 * w.K * (w.dv + 1) + rows
-        key = sc + 4 * w.K * w.dv + rows
+        key = 4 * w.K * w.dv + rows
         return mem + qry + key
     t = 2 * 64                                               # one 64-row tile product per row, per K/dv column
-    qry = 2 * sc + t * w.K + 2 * w.K * w.dv + t * w.dv + t * w.dv + 2 * w.dv * w.K + t * w.K \
-        + 2 * w.K * w.dv + 2 * w.K * w.dv                    # A, num, Bm, g^Q, [R | r] totals, state update
-    key = 2 * sc + t * w.dv + t * w.K + 2 * w.dv * w.K + t * w.K + t * w.dv + 2 * w.K * w.dv \
-        + 2 * w.K * w.dv                                     # Ct, g^K, Dt, dV, state update
+    qry = sc + t * w.K + 2 * w.K * w.dv + t * w.dv + t * w.dv + 2 * w.dv * w.K + t * w.K \
+        + 2 * w.K * w.dv + 2 * w.K * w.dv                    # gamma^Q, A, num, Bm, g^Q, [R | r] totals, state update
+    key = t * w.dv + t * w.K + 2 * w.dv * w.K + t * w.K + t * w.dv + 2 * w.K * w.dv \
+        + 2 * w.K * w.dv                                     # Ct, g^K, Dt, dV, state update (stored gammas)
     return mem + qry + key + 2 * rows
 
 

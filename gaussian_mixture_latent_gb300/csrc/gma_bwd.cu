@@ -74,6 +74,7 @@ struct BwdArgs {
     float *dV;                         // KEY                        [G][N][dv]
     float *part_m;                     // MEM, QRY: [G][C][K][W]
     float *part_p;                     // QRY, KEY: [G][C][K][2d + 1]
+    float *gam;                        // MEM writes, KEY reads gamma^K [G][N][K]
 };
 
 __device__ __forceinline__ float bwd_warp_sum(float v) {
@@ -231,14 +232,23 @@ __global__ void __launch_bounds__(kBT, 1) bwd_pass_kernel(BwdArgs a) {
         const int mv = min(kTN, row_end - t0);
         rx.store(xs + lm * kRS + lj);
         ru.store(us + lm * kRS + lj);
+        if (MODE == kKey) {                     // gamma^K as the memory pass left it
+            const float *gsrc = a.gam + ((size_t)g * a.N + t0) * kK;
+            for (int e = tid; e < kTN * (kK / 4); e += kBT) {
+                const int m = e / (kK / 4), q = e - m * (kK / 4);
+                reinterpret_cast<float4 *>(gs + m * kRS)[q] =
+                    m < mv ? reinterpret_cast<const float4 *>(gsrc + (size_t)m * kK)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         __syncthreads();
         if (t0 + kTN < row_end) {               // the next tile's rows, in flight during this tile
             const bool live = t0 + kTN + lm < row_end;
             rx.load(X + (size_t)(t0 + kTN + lm) * kD + lj, live);
             ru.load(U + (size_t)(t0 + kTN + lm) * kDV + lj, live);
         }
-        // Eq. 16, expanded: s = c' + x . (lambda mu) - (1/2) x^2 . lambda
-        {
+        // Eq. 16, expanded: s = c' + x . (lambda mu) - (1/2) x^2 . lambda (the key pass reuses the
+        // memory pass's responsibilities)
+        if (MODE != kKey) {
             float c[4][4];
             zero4x4(c);
             mm_rows<kD>(c, xs, kRS, r0, W, kK, c0);
@@ -259,7 +269,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_pass_kernel(BwdArgs a) {
         }
         __syncthreads();
         // Eq. 3b, a warp per row; rows past the end get gamma = 0 and so contribute nothing
-        for (int m = warp; m < kTN; m += kBT / 32) {
+        for (int m = warp; MODE != kKey && m < kTN; m += kBT / 32) {
             const float s0 = gs[m * kRS + lane], s1 = gs[m * kRS + lane + 32];
             const float mx = bwd_warp_max(fmaxf(s0, s1));
             float e0 = expf(s0 - mx), e1 = expf(s1 - mx);
@@ -269,6 +279,10 @@ __global__ void __launch_bounds__(kBT, 1) bwd_pass_kernel(BwdArgs a) {
             e1 = live ? e1 * inv : 0.f;
             gs[m * kRS + lane] = e0;
             gs[m * kRS + lane + 32] = e1;
+            if (MODE == kMem && live) {
+                a.gam[((size_t)g * a.N + t0 + m) * kK + lane] = e0;
+                a.gam[((size_t)g * a.N + t0 + m) * kK + lane + 32] = e1;
+            }
             if (MODE == kQry) {
                 const float z = bwd_warp_sum(e0 * zr[lane] + e1 * zr[lane + 32]);
                 if (lane == 0) den[m] = live ? z + a.eps : 1.f;      // rows past the end: a = b = 0 even at eps = 0
@@ -500,17 +514,19 @@ struct BwdCArgs {
     float *ds;                                    // [G][N][K]
     float *dV;                                    // keys: [G][N][dv]
     float *part_m;                                // queries: [G][C][K][W] chunk totals of [R | r]
+    const float *gk;                              // gamma^K [G][N][K] from the memory pass
+    float *gq;                                    // gamma^Q [G][N][K]: queries write, keys read
 };
 
-// W, c' (Eq. 16, expanded) and the chunk's starting memory, from global memory.
-__device__ void causal_prologue(const BwdCArgs &a, float *sm, int h, const float *mem_chunk) {
+// W, c' (Eq. 16, expanded; when `scores`) and the chunk's starting memory, from global memory.
+__device__ void causal_prologue(const BwdCArgs &a, float *sm, int h, const float *mem_chunk, bool scores) {
     const float *lam_h = a.lam + (size_t)h * kK * kD, *mu_h = a.mu + (size_t)h * kK * kD;
     float *W = sm + CC_W, *cp = sm + CC_CP, *M = sm + CC_M, *MT = sm + CC_MT, *zr = sm + CC_ZR;
-    for (int e = threadIdx.x; e < 2 * kD * kK; e += kBT) {
+    for (int e = threadIdx.x; scores && e < 2 * kD * kK; e += kBT) {
         const int q = e / kK, k = e % kK;
         W[e] = q < kD ? lam_h[k * kD + q] * mu_h[k * kD + q] : -0.5f * lam_h[k * kD + q - kD];
     }
-    if (threadIdx.x < kK) {
+    if (scores && threadIdx.x < kK) {
         const int k = threadIdx.x;
         float s = 0.f;
         for (int j = 0; j < kD; ++j) {
@@ -528,6 +544,22 @@ __device__ void causal_prologue(const BwdCArgs &a, float *sm, int h, const float
         } else {
             zr[k] = v;
         }
+    }
+}
+
+// Rows t0 .. t0 + mv - 1 of a [G][N][64] float32 array (head base `src`) into a tile buffer,
+// and its transpose into `dstT` when given; zeros below.
+__device__ __forceinline__ void load_tile_f32(float *dst, const float *src, int t0, int mv) {
+    for (int e = threadIdx.x; e < kTN * 16; e += kBT) {
+        const int m = e >> 4, q = e & 15;
+        reinterpret_cast<float4 *>(dst + m * kRS)[q] =
+            m < mv ? reinterpret_cast<const float4 *>(src + (size_t)(t0 + m) * 64)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+__device__ __forceinline__ void transpose_tile(float *dstT, const float *src) {
+    for (int e = threadIdx.x; e < kTN * 64; e += kBT) {
+        const int m = e % kTN, c = e / kTN;
+        dstT[c * kRS + m] = src[m * kRS + c];
     }
 }
 
@@ -613,11 +645,12 @@ __global__ void __launch_bounds__(kBT, 1) bwd_cq_kernel(BwdCArgs a) {
     float *GK = GQ + kTile, *GKT = GK + kTile, *AS = GKT + kTile, *GG = AS + kTile;
     float *den = sm + CC_DEN, *bb = sm + CC_B;
     const size_t slot = (size_t)g * a.C + ch;
-    causal_prologue(a, sm, h, a.mem + slot * kK * kW);
+    causal_prologue(a, sm, h, a.mem + slot * kK * kW, true);
     const TI *Qx = static_cast<const TI *>(a.Qx) + (size_t)g * a.N * kD;
-    const TI *Kx = static_cast<const TI *>(a.Kx) + (size_t)g * a.N * kD;
     const TI *V = static_cast<const TI *>(a.V) + (size_t)g * a.N * kDV;
     const TI *dO = static_cast<const TI *>(a.dO) + (size_t)g * a.N * kDV;
+    const float *gkg = a.gk + (size_t)g * a.N * kK;
+    float *gqg = a.gq + (size_t)g * a.N * kK;
     float *dsq = a.ds + (size_t)g * a.N * kK, *ab = a.ab + (size_t)g * a.N * kRS;
     float accM[4][4];
     zero4x4(accM);
@@ -626,29 +659,27 @@ __global__ void __launch_bounds__(kBT, 1) bwd_cq_kernel(BwdCArgs a) {
     const int row_begin = ch * a.rows_per_chunk, row_end = min(a.N, row_begin + a.rows_per_chunk);
     for (int t0 = row_begin; t0 < row_end; t0 += kTN) {
         const int mv = min(kTN, row_end - t0);
-        // the tile's keys: gamma^K (and its transpose), V (and its transpose)
-        load_tile(XS, Kx, t0, mv);
+        // the tile's keys: gamma^K (from the memory pass) and V, with their transposes; the
+        // tile's queries and dO
+        load_tile_f32(GK, gkg, t0, mv);
         load_tile(VS, V, t0, mv);
-        __syncthreads();
-        for (int e = tid; e < kTN * kDV; e += kBT) {
-            const int j = e % kTN, c = e / kTN;
-            VT[c * kRS + j] = VS[j * kRS + c];
-        }
-        tile_scores(W, cp, XS, GK, r0, c0);
-        __syncthreads();
-        tile_softmax(GK, GKT, mv);
-        __syncthreads();
-        // the tile's queries: gamma^Q, dO, den = gamma^Q . z (the causal part added below)
         load_tile(XS, Qx, t0, mv);
         load_tile(US, dO, t0, mv);
         __syncthreads();
+        transpose_tile(VT, VS);
+        transpose_tile(GKT, GK);
         tile_scores(W, cp, XS, GQ, r0, c0);
         __syncthreads();
         tile_softmax(GQ, nullptr, mv);
         __syncthreads();
         for (int m = warp; m < kTN; m += kBT / 32) {
-            const float z = bwd_warp_sum(GQ[m * kRS + lane] * zr[lane] + GQ[m * kRS + lane + 32] * zr[lane + 32]);
+            const float g0 = GQ[m * kRS + lane], g1 = GQ[m * kRS + lane + 32];
+            const float z = bwd_warp_sum(g0 * zr[lane] + g1 * zr[lane + 32]);
             if (lane == 0) den[m] = z;
+            if (m < mv) {                      // gamma^Q for the key pass
+                gqg[(size_t)(t0 + m) * kK + lane] = g0;
+                gqg[(size_t)(t0 + m) * kK + lane + 32] = g1;
+            }
         }
         {   // A = tril(gamma^Q gamma^K^T): rows i (queries), columns j (keys)
             float c[4][4];
@@ -757,14 +788,13 @@ __global__ void __launch_bounds__(kBT, 1) bwd_ck_kernel(BwdCArgs a) {
     const int tid = threadIdx.x;
     const int r0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
     const int ch = blockIdx.x, g = blockIdx.y, h = g % a.H;
-    float *W = sm + CC_W, *cp = sm + CC_CP, *M = sm + CC_M, *MT = sm + CC_MT, *zr = sm + CC_ZR;
-    float *XS = sm + CC_T, *GQ = XS + kTile, *GQT = GQ + kTile, *US = GQT + kTile, *AT = US + kTile;
+    float *M = sm + CC_M, *MT = sm + CC_MT, *zr = sm + CC_ZR;
+    float *GQ = sm + CC_T + kTile, *GQT = GQ + kTile, *US = GQT + kTile, *AT = US + kTile;   // tile 0 unused
     float *GK = AT + kTile, *VS = GK + kTile, *CM = VS + kTile, *GG = CM + kTile;
     const size_t slot = (size_t)g * a.C + ch;
-    causal_prologue(a, sm, h, a.mem + slot * kK * kW);
-    const TI *Qx = static_cast<const TI *>(a.Qx) + (size_t)g * a.N * kD;
-    const TI *Kx = static_cast<const TI *>(a.Kx) + (size_t)g * a.N * kD;
+    causal_prologue(a, sm, h, a.mem + slot * kK * kW, false);
     const TI *V = static_cast<const TI *>(a.V) + (size_t)g * a.N * kDV;
+    const float *gqg = a.gq + (size_t)g * a.N * kK, *gkg = a.gk + (size_t)g * a.N * kK;
     const float *ab = a.ab + (size_t)g * a.N * kRS;
     float *dsk = a.ds + (size_t)g * a.N * kK, *dV = a.dV + (size_t)g * a.N * kDV;
     __syncthreads();
@@ -772,29 +802,18 @@ __global__ void __launch_bounds__(kBT, 1) bwd_ck_kernel(BwdCArgs a) {
     const int ntiles = row_end > row_begin ? (row_end - row_begin + kTN - 1) / kTN : 0;
     for (int tt = ntiles - 1; tt >= 0; --tt) {
         const int t0 = row_begin + tt * kTN, mv = min(kTN, row_end - t0);
-        // the tile's queries: gamma^Q (and its transpose), a | b (and a's transpose)
-        load_tile(XS, Qx, t0, mv);
+        // the tile's queries: gamma^Q and a | b (with transposes); its keys: gamma^K and V
         for (int e = tid; e < kTN * (kRS / 4); e += kBT) {
             const int m = e / (kRS / 4), q = e - m * (kRS / 4);
             reinterpret_cast<float4 *>(US + m * kRS)[q] =
                 m < mv ? reinterpret_cast<const float4 *>(ab + (size_t)(t0 + m) * kRS)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        __syncthreads();
-        for (int e = tid; e < kTN * kDV; e += kBT) {
-            const int i = e % kTN, c = e / kTN;
-            AT[c * kRS + i] = US[i * kRS + c];
-        }
-        tile_scores(W, cp, XS, GQ, r0, c0);
-        __syncthreads();
-        tile_softmax(GQ, GQT, mv);
-        __syncthreads();
-        // the tile's keys: gamma^K, V
-        load_tile(XS, Kx, t0, mv);
+        load_tile_f32(GQ, gqg, t0, mv);
+        load_tile_f32(GK, gkg, t0, mv);
         load_tile(VS, V, t0, mv);
         __syncthreads();
-        tile_scores(W, cp, XS, GK, r0, c0);
-        __syncthreads();
-        tile_softmax(GK, nullptr, mv);
+        transpose_tile(AT, US);
+        transpose_tile(GQT, GQ);
         __syncthreads();
         {   // Ct[j][i] = [i >= j] (v_j . a_i + b_i): rows j (keys), columns i (queries)
             float c[4][4];
@@ -1020,14 +1039,16 @@ BwdLayout bwd_layout(const Problem &p) {
     L.part_m = align_up(L.mem_r + sizeof(float) * (size_t)p.G * kK * kW);
     L.part_q = align_up(L.part_m + sizeof(float) * (size_t)p.G * L.C * kK * kW);
     L.part_k = align_up(L.part_q + sizeof(float) * (size_t)p.G * L.C * kK * kPW);
-    L.total = align_up(L.part_k + sizeof(float) * (size_t)p.G * L.C * kK * kPW);
+    L.gk = align_up(L.part_k + sizeof(float) * (size_t)p.G * L.C * kK * kPW);
+    L.total = align_up(L.gk + sizeof(float) * (size_t)p.G * p.N * kK);
     if (p.causal) {     // per-chunk starting memories, a | b and ds of every row
         L.mem_pc = L.total;
         L.mem_rc = align_up(L.mem_pc + sizeof(float) * (size_t)p.G * L.C * kK * kW);
         L.ab = align_up(L.mem_rc + sizeof(float) * (size_t)p.G * L.C * kK * kW);
         L.dsq = align_up(L.ab + sizeof(float) * (size_t)p.G * p.N * kRS);
         L.dsk = align_up(L.dsq + sizeof(float) * (size_t)p.G * p.N * kK);
-        L.total = align_up(L.dsk + sizeof(float) * (size_t)p.G * p.N * kK);
+        L.gq = align_up(L.dsk + sizeof(float) * (size_t)p.G * p.N * kK);
+        L.total = align_up(L.gq + sizeof(float) * (size_t)p.G * p.N * kK);
     }
     return L;
 }
@@ -1050,6 +1071,7 @@ cudaError_t bwd_run(const Problem &p, const BwdLayout &L, const void *Qx, const 
     a.mu = mu;
     a.lam = lam;
     a.cdir = cdir;
+    a.gam = reinterpret_cast<float *>(ws + L.gk);
     const dim3 sum_grid((kK * kW + 255) / 256, p.G);
     if (p.causal) {
         float *mem_pc = reinterpret_cast<float *>(ws + L.mem_pc), *mem_rc = reinterpret_cast<float *>(ws + L.mem_rc);
@@ -1075,6 +1097,8 @@ cudaError_t bwd_run(const Problem &p, const BwdLayout &L, const void *Qx, const 
         c.lam = lam;
         c.cdir = cdir;
         c.ab = ab;
+        c.gk = a.gam;
+        c.gq = reinterpret_cast<float *>(ws + L.gq);
         // queries in order: ds^Q, a | b, chunk totals of [R | r]
         c.mem = mem_pc;
         c.ds = dsq;

@@ -94,7 +94,8 @@ struct BwdLayout {
     size_t part_m;               // [G][C][K][dv+1] per-chunk partials of either memory
     size_t part_q, part_k;       // [G][C][K][2d+1] per-chunk parameter sums over query / key rows
     size_t mem_pc, mem_rc;       // causal: [G][C][K][dv+1] memories before / after each chunk
-    size_t ab, dsq, dsk;         // causal: [G][N][68] a | b rows, [G][N][K] ds of queries / keys
+    size_t gk;                   // [G][N][K] gamma^K of the memory pass, reused by the key pass
+    size_t ab, dsq, dsk, gq;     // causal: [G][N][68] a | b rows, [G][N][K] ds of queries / keys, gamma^Q
     size_t total;
     int C, rows_per_chunk;       // row chunks per head
 };

@@ -135,8 +135,9 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
  * reductions).  causal = 1 differentiates the prefix memories of Eq. 6b / 8b
  * (each key collects the gradient of the rows at or after it).  Implemented for
  * d = dv = K = 64; GMA_ERR_UNSUPPORTED otherwise.  N = 0 writes zero parameter
- * gradients.  Workspace: gma_backward_workspace_size() (the causal workspace
- * also holds a | b and ds of every row, about 0.8 KB per row of a head).
+ * gradients.  Workspace: gma_backward_workspace_size() (it holds Gamma^K of
+ * every row, 256 B per row of a head; the causal one also a | b, Gamma^Q and ds,
+ * about 1.3 KB per row in all).
  * Errors as for gma_forward().
  */
 gma_status gma_backward_workspace_size(const gma_desc *desc, int causal, size_t *bytes);
