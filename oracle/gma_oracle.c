@@ -1,12 +1,13 @@
 /*
- * Plain fp64 CPU oracle for the Gaussian Mixture Attention (GMA) forward.
+ * Plain fp64 CPU oracle for the Gaussian Mixture Attention (GMA) forward, its
+ * cross-attention and diagnostics variants, and its backward pass.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
  * benchmark's CPU-baseline leg load this library.  The CUDA library shares no
  * code with it and never calls it.
  *
  * Source: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
- * Probabilistic Latent Routing" (Huang & Raza, 2026), section 3.  Every
+ * Probabilistic Latent Routing" (Huang & Raza, 2026), sections 3-5.  Every
  * function below evaluates the paper's definitions directly, in double
  * precision, in the order the equations are written:
  *
@@ -19,6 +20,8 @@
  *   Eq. (7-8) O_i = sum_k gamma^Q_{i,k} Vt_k / (sum_k gamma^Q_{i,k} Z_k + eps)
  *   Eq. (6b)  causal prefix memory: sums over j <= i (inclusive)
  *   Eq. (8b)  causal read from the prefix memory of position i
+ *   Eq. (24)-(29)  responsibility diagnostics (section 5.4)
+ *   Eq. (17)-(20)  backward pass (section 4.1; see gma_oracle_backward_head)
  *
  * Readings where the paper leaves a step open:
  *   - softplus is evaluated as max(w,0) + log1p(exp(-|w|)), which equals
