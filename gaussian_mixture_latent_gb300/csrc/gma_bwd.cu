@@ -13,10 +13,10 @@
 //   g^K_j = R v_j + r,        dV_j = R^T gamma^K_j.
 //
 // Three passes of one kernel over 64-row tiles (one CTA per (row chunk, head),
-// 256 threads), each recomputing the responsibilities of its rows:
-//   MEM  key rows:   [Vt | Z] partials  (Eq. 5-6)
-//   QRY  query rows: a, b, g^Q, ds, dQx; partials of [R | r] and of the parameter sums
-//   KEY  key rows:   g^K, dV, ds, dKx; partials of the parameter sums
+// 256 threads):
+//   MEM  key rows:   gamma^K (stored for the key pass), [Vt | Z] partials  (Eq. 5-6)
+//   QRY  query rows: gamma^Q, a, b, g^Q, ds, dQx; partials of [R | r] and of the parameter sums
+//   KEY  key rows:   gamma^K as stored, g^K, dV, ds, dKx; partials of the parameter sums
 // with fixed-order reductions of the partials in between and a finalize that
 // turns the parameter sums P1 = sum ds x, P2 = sum ds x^2, P0 = sum ds into
 // dmu, drho, dalpha.  Every product is a 4 x 4 register-blocked loop over
@@ -487,8 +487,9 @@ __global__ void __launch_bounds__(2 * kD) bwd_param_kernel(int B, int H, int C, 
 //   Bm = tril(a V^T + b 1^T),  g^Q = a S^T + b z^T + Bm G^K
 //   Ct = (tril(a V^T + b 1^T))^T,  g^K = Ct G^Q + V R^T + r
 //   Dt = (tril(G^Q G^K^T))^T,      dV  = Dt a + G^K R
-// ds of either side goes to global memory; bwd_rows_kernel turns it into dX and the
-// parameter sums.
+// The query pass takes gamma^K from the memory pass and stores gamma^Q; the key pass
+// reads both.  ds of either side goes to global memory; bwd_rows_kernel turns it into
+// dX and the parameter sums.
 
 constexpr int kTile = kTN * kRS;                  // one [TN][kRS] tile buffer
 constexpr int CC_W = 0;                           // [2d][K]
