@@ -85,3 +85,41 @@ def test_forward_rejects_bad_arguments_before_launching(lib):
     assert f(*args(wsb=16)) == 3
     assert gma.gma_status_string(3).startswith("GMA_ERR_WORKSPACE")
     assert lib.gma_version() >= 100
+
+
+def test_backward_and_decode_reject_bad_arguments_before_launching(lib):
+    # every call below fails validation: the placeholder pointers are never dereferenced
+    n = ctypes.c_size_t(0)
+    ok = _desc(d=64, K=64, dv=64)
+    assert lib.gma_backward_workspace_size(ctypes.byref(ok), 0, ctypes.byref(n)) == 0 and n.value > 0
+    bidir = n.value
+    assert lib.gma_backward_workspace_size(ctypes.byref(ok), 1, ctypes.byref(n)) == 0 and n.value > bidir
+    assert lib.gma_backward_workspace_size(ctypes.byref(ok), 2, ctypes.byref(n)) == 1
+    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(d=64, K=128, dv=64)), 0, ctypes.byref(n)) == 2
+    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(d=64, K=64, dv=64, out_dtype=0)), 0,
+                                           ctypes.byref(n)) == 2
+    p = ctypes.c_void_p(4096)
+    odd = ctypes.c_void_p(4100)
+    b = lib.gma_backward
+    args = lambda **o: [ctypes.byref(o.get("desc", ok)), o.get("causal", 0), o.get("Q", p), p, p, p, p, p,
+                        o.get("eps", 1e-6), o.get("dO", p), p, p, p, o.get("dmu", p), p, p,
+                        o.get("ws", p), o.get("wsb", 1 << 40), None]
+    assert b(*args(causal=2)) == 1
+    assert b(*args(eps=-1.0)) == 1
+    assert b(*args(Q=None)) == 1
+    assert b(*args(dO=odd)) == 1
+    assert b(*args(dmu=None)) == 1
+    assert b(*args(desc=_desc(d=64, K=128, dv=64))) == 2
+    assert b(*args(ws=None)) == 3
+    assert b(*args(wsb=16)) == 3
+    assert lib.gma_decode_workspace_size(ctypes.byref(ok), ctypes.byref(n)) == 0
+    assert lib.gma_decode_workspace_size(ctypes.byref(_desc(d=64, K=256, dv=256)), ctypes.byref(n)) == 2
+    dec = lib.gma_decode
+    dargs = lambda **o: [ctypes.byref(o.get("desc", ok)), p, p, p, p, p, p, o.get("eps", 1e-6),
+                         o.get("state", p), p, o.get("ws", p), o.get("wsb", 1 << 40), None]
+    assert dec(*dargs(eps=float("nan"))) == 1
+    assert dec(*dargs(state=None)) == 1
+    assert dec(*dargs(state=odd)) == 1
+    assert dec(*dargs(desc=_desc(d=64, K=256, dv=256))) == 2
+    assert dec(*dargs(ws=None)) == 3
+    assert dec(*dargs(wsb=1)) == 3
