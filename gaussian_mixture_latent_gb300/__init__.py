@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "GmaError", "gma_desc", "gma_workspace_size", "gma_workspace_init", "gma_forward",
     "gma_forward_ex", "gma_forward_plan",
-    "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_decode", "gma_backward", "gma_get_status", "gma_status_string", "gma_version",
+    "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_decode", "gma_backward", "gma_selftest_timeout", "gma_get_status", "gma_status_string", "gma_version",
     "Workspace", "library_path",
 ]
 
@@ -77,6 +77,7 @@ def _load():
     lib.gma_decode_workspace_size.argtypes = [dp, ctypes.POINTER(sz)]
     lib.gma_decode.argtypes = [dp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp, sz, vp]
     lib.gma_backward_workspace_size.argtypes = [dp, i, ctypes.POINTER(sz)]
+    lib.gma_selftest_timeout.argtypes = [vp, sz, vp]
     lib.gma_backward.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gma_get_status.argtypes = [vp, vp]
     lib.gma_status_string.argtypes = [i]
@@ -86,7 +87,7 @@ def _load():
                lib.gma_forward_ex, lib.gma_forward_plan, lib.gma_responsibilities, lib.gma_get_status, lib.gma_version,
                lib.gma_diagnostics_workspace_size, lib.gma_diagnostics, lib.gma_cross_workspace_size,
                lib.gma_forward_cross, lib.gma_decode_workspace_size, lib.gma_decode,
-               lib.gma_backward_workspace_size, lib.gma_backward):
+               lib.gma_backward_workspace_size, lib.gma_backward, lib.gma_selftest_timeout):
         fn.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -380,6 +381,16 @@ def gma_diagnostics(Qx, mu, rho, pi_logits, var_floor: float = 1e-4, z=True, wor
     if rc:
         raise GmaError(rc, "gma_diagnostics")
     return p, stats, zt
+
+
+def gma_selftest_timeout(workspace, stream=None):
+    """Launch a kernel whose bounded wait runs out (about one second): afterwards
+    gma_get_status(workspace) returns GMA_ERR_TIMEOUT (5).  `workspace` is a CUDA tensor
+    of at least 256 bytes."""
+    rc = _load().gma_selftest_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream_ptr(stream))
+    if rc:
+        raise GmaError(rc, "gma_selftest_timeout")
 
 
 def gma_get_status(workspace=None, stream=None) -> int:

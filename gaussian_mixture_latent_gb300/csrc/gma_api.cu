@@ -398,6 +398,12 @@ gma_status gma_diagnostics(const gma_desc *desc, const void *Qx, const float *mu
     return tc_diag_finalize(p, L, p_out, stats_out, ws, s) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
+gma_status gma_selftest_timeout(void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace || workspace_bytes < kHeaderBytes) return GMA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GMA_ERR_INVALID_ARG;
+    return selftest_timeout(workspace, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
 gma_status gma_get_status(void *workspace, void *stream) {
     if (!workspace) return GMA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -105,6 +105,9 @@ cudaError_t bwd_run(const Problem &p, const BwdLayout &L, const void *Qx, const 
                     const float *mu, const float *rho, const float *alpha, const void *dO, float *dQx, float *dKx,
                     float *dV, float *dmu, float *drho, float *dalpha, char *ws, cudaStream_t s);
 
+// ----- self-test of the bounded-wait failure path: gma_selftest.cu -----
+cudaError_t selftest_timeout(void *ws, cudaStream_t s);
+
 // ----- causal decode with a carried state: gma_decode.cu (one launch) -----
 bool decode_supported(const Problem &p);
 size_t decode_workspace(const Problem &p);

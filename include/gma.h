@@ -124,6 +124,16 @@ gma_status gma_responsibilities(const gma_desc *desc, const void *X, const float
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Test of the device-side failure path: launches one CTA whose bounded wait is on
+ * a barrier that nothing arrives at.  The wait gives up after about one second,
+ * as every wait in the library's kernels does, and posts GMA_ERR_TIMEOUT to the
+ * workspace's status word (read with gma_get_status()); the CUDA context stays
+ * usable.  workspace: at least 256 bytes, 16-byte aligned.  Returns GMA_OK when
+ * the kernel was launched.
+ */
+gma_status gma_selftest_timeout(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Backward pass ("Gaussian Mixture Attention", section 4.1, Eq. 17-20, through
  * Eq. 14-15 and the memory products of Eq. 5-8): given dO = dL/dO
  * [B, H, N, dv] for the forward output O = gma_forward(...), writes
