@@ -172,6 +172,14 @@ def _check(t: torch.Tensor, name: str, shape, dtypes):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+def _check_device_status(ws, stream, what: str) -> None:
+    """Synchronise `stream` and raise GmaError when a kernel of the call posted a
+    device error (a bounded wait that ran out) to the workspace's status word."""
+    rc = _load().gma_get_status(_ptr(ws), _stream_ptr(stream))
+    if rc:
+        raise GmaError(rc, what)
+
+
 def gma_forward_plan(B, H, N, d, K, dv, dtype=torch.bfloat16, causal=False, out_dtype=None,
                      var_floor: float = 1e-4, chunk: int = 0):
     """Kernel names gma_forward launches for this problem (nothing runs)."""
@@ -192,9 +200,13 @@ def gma_forward_ex(*args, events=None, **kw):
 
 def gma_forward(Qx, Kx, V, mu, rho, pi_logits, eps: float = 1e-6, causal: bool = False,
                 out=None, workspace=None, var_floor: float = 1e-4, out_dtype=None,
-                chunk: int = 0, stream=None, events=None):
+                chunk: int = 0, stream=None, events=None, check_status: bool = False):
     """GMA forward (Eq. 5-8; causal Eq. 6b, 8b).  Qx, Kx [B,H,N,d], V [B,H,N,dv]
-    (float32 or bfloat16), mu, rho [H,K,d], pi_logits [H,K] float32 -> out [B,H,N,dv]."""
+    (float32 or bfloat16), mu, rho [H,K,d], pi_logits [H,K] float32 -> out [B,H,N,dv].
+
+    The call is asynchronous.  Device-side errors are posted to the workspace's
+    status word, not returned: pass check_status=True to synchronise and raise
+    GmaError on one, or call gma_get_status() later."""
     B, H, N, d = Qx.shape
     dv = V.shape[-1]
     K = mu.shape[1]
@@ -223,6 +235,8 @@ def gma_forward(Qx, Kx, V, mu, rho, pi_logits, eps: float = 1e-6, causal: bool =
         rc = _load().gma_forward_ex(*common, handles, len(events))
     if rc:
         raise GmaError(rc, "gma_forward")
+    if check_status:
+        _check_device_status(ws, stream, "gma_forward")
     return out
 
 
@@ -250,7 +264,7 @@ def gma_responsibilities(X, mu, rho, pi_logits, var_floor: float = 1e-4, out=Non
 
 
 def gma_forward_cross(Qx, Ky, Vy, mu, rho, pi_logits, eps: float = 1e-6, var_floor: float = 1e-4, out=None,
-                      workspace=None, stream=None):
+                      workspace=None, stream=None, check_status: bool = False):
     """Cross-attention GMA (sections 3.1, 6): the queries Qx [B,H,N,d] read the memory of the
     context Ky [B,H,Nkv,d], Vy [B,H,Nkv,dv] -> out [B,H,N,dv] (bidirectional, Eq. 5-8)."""
     B, H, N, d = Qx.shape
@@ -277,11 +291,13 @@ def gma_forward_cross(Qx, Ky, Vy, mu, rho, pi_logits, eps: float = 1e-6, var_flo
                                    _stream_ptr(stream))
     if rc:
         raise GmaError(rc, "gma_forward_cross")
+    if check_status:
+        _check_device_status(ws, stream, "gma_forward_cross")
     return out
 
 
 def gma_backward(Qx, Kx, V, mu, rho, pi_logits, dO, eps: float = 1e-6, var_floor: float = 1e-4, causal=False,
-                 grads=None, workspace=None, stream=None):
+                 grads=None, workspace=None, stream=None, check_status: bool = False):
     """Backward pass (section 4.1, Eqs. 17-20): given dO = dL/dO [B,H,N,dv] of the forward
     gma_forward(Qx, Kx, V, mu, rho, pi_logits), returns the float32 gradients
     (dQx, dKx, dV, dmu, drho, dpi_logits); parameter gradients are summed over the batch.
@@ -315,11 +331,13 @@ def gma_backward(Qx, Kx, V, mu, rho, pi_logits, dO, eps: float = 1e-6, var_floor
                               _ptr(ws), ws.numel(), _stream_ptr(stream))
     if rc:
         raise GmaError(rc, "gma_backward")
+    if check_status:
+        _check_device_status(ws, stream, "gma_backward")
     return grads
 
 
 def gma_decode(Qx, Kx, V, mu, rho, pi_logits, state, eps: float = 1e-6, var_floor: float = 1e-4, out=None,
-               workspace=None, stream=None):
+               workspace=None, stream=None, check_status: bool = False):
     """Causal decode with a carried state (section 3.5, Eq. 6b / 8b as a recurrence): appends the
     N new positions of Qx, Kx [B,H,N,d], V [B,H,N,dv] to each head's sequence.  `state`
     [B,H,K,dv+1] float32 holds [S | z] of the positions so far and is updated in place;
@@ -347,13 +365,16 @@ def gma_decode(Qx, Kx, V, mu, rho, pi_logits, state, eps: float = 1e-6, var_floo
                             float(eps), _ptr(state), _ptr(out), _ptr(ws), ws.numel(), _stream_ptr(stream))
     if rc:
         raise GmaError(rc, "gma_decode")
+    if check_status:
+        _check_device_status(ws, stream, "gma_decode")
     return out
 
 
 _diag_ws_bytes = {}
 
 
-def gma_diagnostics(Qx, mu, rho, pi_logits, var_floor: float = 1e-4, z=True, workspace=None, stream=None):
+def gma_diagnostics(Qx, mu, rho, pi_logits, var_floor: float = 1e-4, z=True, workspace=None, stream=None,
+                    check_status: bool = False):
     """Responsibility diagnostics (section 5.4, Eqs. 24-29) of the query routing vectors
     Qx [B,H,N,d] (bf16, d = 64, K in {64, 128}) -> (p [K] float32, stats [3] float32 =
     (H_usage, H_token, R_max), z [B,N] int32 argmax or None), all on Qx's device."""
@@ -380,6 +401,8 @@ def gma_diagnostics(Qx, mu, rho, pi_logits, var_floor: float = 1e-4, z=True, wor
                                  ws.numel(), _stream_ptr(stream))
     if rc:
         raise GmaError(rc, "gma_diagnostics")
+    if check_status:
+        _check_device_status(ws, stream, "gma_diagnostics")
     return p, stats, zt
 
 

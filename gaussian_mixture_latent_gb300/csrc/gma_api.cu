@@ -104,6 +104,10 @@ gma_status build_forward_plan(const Problem &p, const Args *a, Plan &plan) {
         plan.add("tc_read", [=](cudaStream_t s) { return tc_read(p, T, A.Qx, A.out, ws, s); });
         return GMA_OK;
     }
+    // The tensor-core causal kernels scan in 128-row chunks (one MMA tile); they
+    // refuse any other requested chunk rather than silently using their own.
+    if ((tc_causal_supported(p) || tc_slice_supported(p)) && p.chunk != 0 && p.chunk != kTcChunkRows)
+        return GMA_ERR_UNSUPPORTED;
     if (tc_causal_supported(p)) {
         const TcLayout T = tc_causal_layout(p);
         plan.workspace = T.total;
@@ -264,6 +268,7 @@ gma_status gma_backward_workspace_size(const gma_desc *desc, int causal, size_t 
     if (!bytes || causal < 0 || causal > 1) return GMA_ERR_INVALID_ARG;
     const Problem p = make_problem(desc, causal, 0.f);
     if (!bwd_supported(p) || p.out_dtype != p.in_dtype) return GMA_ERR_UNSUPPORTED;
+    if (p.causal && p.chunk != 0 && p.chunk != kBwdChunkRows) return GMA_ERR_UNSUPPORTED;
     *bytes = bwd_layout(p).total;
     return GMA_OK;
 }
@@ -282,6 +287,7 @@ gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const 
         if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
     const Problem p = make_problem(desc, causal, eps);
     if (!bwd_supported(p) || p.out_dtype != p.in_dtype) return GMA_ERR_UNSUPPORTED;
+    if (p.causal && p.chunk != 0 && p.chunk != kBwdChunkRows) return GMA_ERR_UNSUPPORTED;
     const BwdLayout L = bwd_layout(p);
     if (!workspace || workspace_bytes < L.total) return GMA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

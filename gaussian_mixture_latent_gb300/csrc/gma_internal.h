@@ -15,6 +15,8 @@ enum : unsigned {
 };
 
 constexpr size_t kHeaderBytes = 256;
+constexpr int kTcChunkRows = 128;    // causal chunk of the tensor-core kernels (one MMA tile)
+constexpr int kBwdChunkRows = 64;    // row tile of the causal backward's masked products
 constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }

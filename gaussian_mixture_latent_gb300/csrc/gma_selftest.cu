@@ -1,7 +1,7 @@
 // Self-test of the device-side failure path: a bounded wait that runs out.
 //
-// Every mbarrier wait in the library's kernels gives up after about one second
-// (2e9 cycles), raises its CTA's abort flag and posts GMA_ERR_TIMEOUT to the
+// Every mbarrier wait in the library's kernels gives up after one second on the
+// global nanosecond timer, raises its CTA's abort flag and posts GMA_ERR_TIMEOUT to the
 // status word at the start of the workspace.  selftest_timeout_kernel waits, with
 // that same bounded wait, on a barrier that nothing arrives at, so the path can be
 // exercised without faulting or hanging the GPU: the kernel ends after the bound.

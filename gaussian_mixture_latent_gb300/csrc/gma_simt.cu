@@ -259,7 +259,9 @@ __global__ void read_kernel(int N, int K, int dv, float eps, const float *__rest
     }
 }
 
-constexpr int kCausalChunk = 16;
+constexpr int kCausalChunkDefault = 16;
+
+int causal_chunk_rows(const Problem &p) { return p.chunk > 0 ? p.chunk : kCausalChunkDefault; }
 
 // Eq. 6b / 8b for rows [p*rpp, min(N,(p+1)*rpp)) of head g, starting from the
 // exclusive prefix state prefix[g][p] = [Vt | Z] of all earlier rows.
@@ -269,11 +271,10 @@ constexpr int kCausalChunk = 16;
 //   out_i = num_i[:dv] / (num_i[dv] + eps)
 //   S    += gk^T Vaug                      (inclusive of the chunk)
 template <typename T, typename Tout>
-__global__ void causal_chunk_kernel(int N, int K, int dv, int P, int rpp, float eps,
+__global__ void causal_chunk_kernel(int N, int K, int dv, int P, int rpp, int C, float eps,
                                     const float *__restrict__ gq, const float *__restrict__ gk,
                                     const T *__restrict__ V, const float *__restrict__ prefix,
                                     Tout *__restrict__ out) {
-    constexpr int C = kCausalChunk;
     extern __shared__ float sm[];
     const int W = dv + 1;
     const int p = blockIdx.x, g = blockIdx.y;
@@ -410,15 +411,14 @@ cudaError_t read_t(const Problem &p, char *ws, const SimtLayout &L, void *out, c
 template <typename T, typename Tout>
 cudaError_t causal_t(const Problem &p, const void *V, char *ws, const SimtLayout &L, void *out,
                      cudaStream_t s) {
-    constexpr int C = kCausalChunk;
-    const int W = p.dv + 1;
+    const int C = causal_chunk_rows(p);
     const int rpp = (p.N + L.P - 1) / L.P;
-    const size_t smem = sizeof(float) * ((size_t)p.K * W + 2 * C * p.K + C * W + C * C + C * W);
+    const size_t smem = simt_causal_smem(p);
     auto kern = causal_chunk_kernel<T, Tout>;
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(L.P, p.G);
-    kern<<<grid, 256, smem, s>>>(p.N, p.K, p.dv, L.P, rpp, p.eps,
+    kern<<<grid, 256, smem, s>>>(p.N, p.K, p.dv, L.P, rpp, C, p.eps,
                                  reinterpret_cast<const float *>(ws + L.gq),
                                  reinterpret_cast<const float *>(ws + L.gk),
                                  static_cast<const T *>(V),
@@ -443,8 +443,8 @@ cudaError_t simt_causal(const Problem &p, const void *V, char *ws, const SimtLay
 }
 
 size_t simt_causal_smem(const Problem &p) {
-    constexpr int C = kCausalChunk;
-    const int W = p.dv + 1;
+    const size_t C = (size_t)causal_chunk_rows(p);
+    const size_t W = (size_t)p.dv + 1;
     return sizeof(float) * ((size_t)p.K * W + 2 * C * p.K + C * W + C * C + C * W);
 }
 

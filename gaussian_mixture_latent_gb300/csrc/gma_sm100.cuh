@@ -56,7 +56,7 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// A wait that gives up: after `limit` SM clock cycles, or as soon as another
+// A wait that gives up: after kWaitLimitNs nanoseconds, or as soon as another
 // thread of the CTA has raised *abort.  Returns true when the phase completed.
 // Waiting for the n-th completion (n = 0, 1, ...) of a barrier uses parity n & 1.
 struct Abort {
@@ -64,18 +64,26 @@ struct Abort {
     unsigned *status;        // global status word (device error bits)
 };
 
-constexpr long long kWaitLimitCycles = 2000000000LL;   // about one second at 2 GHz
+// Wait limits are measured on the global nanosecond timer, so that they do not
+// stretch when the SM clock drops (a power cap or a low application clock).
+constexpr long long kWaitLimitNs = 1000000000LL;       // one second
+
+__device__ __forceinline__ long long now_ns() {
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 // The spin loop is one out-of-line copy per kernel: a kernel has dozens of wait
 // sites, and inlining the loop at each of them grows the code that every warp
 // role cycles through (instruction-cache misses showed as no_instruction stalls).
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, volatile int *flag,
                                                    unsigned *status, unsigned err_bit) {
-    const long long t0 = clock64();
+    const long long t0 = now_ns();
     for (;;) {
         if (mbar_try_wait(a, parity)) return true;
         if (*flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (now_ns() - t0 > kWaitLimitNs) {
             *flag = 1;
             atomicOr(status, err_bit);
             return false;

@@ -194,7 +194,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             bulk_load(sm + C::OFF_P, A.params + (size_t)((t0 / A.T) % A.H) * A.param_stride, param_bytes(K),
                       &w_full[0]);
             int p_loaded = 0;
-            long long last = clock64();
+            long long last = now_ns();
             while ((cx.valid() || cv.valid()) && !*abort_flag) {
                 bool progress = false;
                 if (cx.valid()) {
@@ -228,10 +228,10 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     }
                 }
                 if (progress) {
-                    last = clock64();
+                    last = now_ns();
                 } else {
                     __nanosleep(64);                       // nothing to issue: yield the issue slots
-                    if (clock64() - last > kWaitLimitCycles) {
+                    if (now_ns() - last > kWaitLimitNs) {
                         *abort_flag = 1;
                         atomicOr(A.status, kDevErrTimeout);
                     }
@@ -515,7 +515,7 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 bulk_load(sm + C::OFF_M, A.mem + (size_t)g0 * A.mem_stride, mem_bytes(K), &w_full[0]);
             }
             int p_loaded = 0;
-            long long last = clock64();
+            long long last = now_ns();
             while (cx.valid() && !*abort_flag) {
                 bool progress = false;
                 const int xi = cx.i;
@@ -540,10 +540,10 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     progress = true;
                 }
                 if (progress) {
-                    last = clock64();
+                    last = now_ns();
                 } else {
                     __nanosleep(64);                       // nothing to issue: yield the issue slots
-                    if (clock64() - last > kWaitLimitCycles) {
+                    if (now_ns() - last > kWaitLimitNs) {
                         *abort_flag = 1;
                         atomicOr(A.status, kDevErrTimeout);
                     }

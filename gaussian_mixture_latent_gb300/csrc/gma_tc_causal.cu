@@ -212,7 +212,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 bulk_load(sm + C::OFF_P + param_wc_off(K), blk + param_wc_off(A.Kfull) + (size_t)ks * kWc, kWc, w_full);
                 bulk_load(sm + C::OFF_P + param_scale_off(K), blk + param_scale_off(A.Kfull), 16u, w_full);
             }
-            long long last = clock64();
+            long long last = now_ns();
             while ((qi < nch || ki < nch || vi < nch) && !*abort_flag) {
                 bool progress = false;
                 if (ki < nch && (ki < 2 || mbar_test(&kempty[ki & 1], ((ki >> 1) - 1) & 1))) {
@@ -234,10 +234,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     progress = true;
                 }
                 if (progress) {
-                    last = clock64();
+                    last = now_ns();
                 } else {
                     __nanosleep(64);
-                    if (clock64() - last > kWaitLimitCycles) {
+                    if (now_ns() - last > kWaitLimitNs) {
                         *abort_flag = 1;
                         atomicOr(A.status, kDevErrTimeout);
                     }

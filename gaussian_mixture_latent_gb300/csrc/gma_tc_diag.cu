@@ -129,7 +129,7 @@ tc_diag_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
         if (lane == 0 && nsteps > 0) {
             grid_dep_wait();                               // the parameter blocks are written
             int xs = 0, ws = 0;                            // next step to load: routing tile, parameters
-            long long last = clock64();
+            long long last = now_ns();
             while ((xs < nsteps || ws < nsteps) && !*abort_flag) {
                 bool progress = false;
                 if (ws < nsteps && (ws < 2 || mbar_test(&w_empty[ws & 1], ((ws >> 1) - 1) & 1))) {
@@ -148,10 +148,10 @@ tc_diag_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
                     progress = true;
                 }
                 if (progress) {
-                    last = clock64();
+                    last = now_ns();
                 } else {
                     __nanosleep(64);
-                    if (clock64() - last > kWaitLimitCycles) {
+                    if (now_ns() - last > kWaitLimitNs) {
                         *abort_flag = 1;
                         atomicOr(A.status, kDevErrTimeout);
                     }

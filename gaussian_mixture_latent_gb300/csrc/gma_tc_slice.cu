@@ -96,7 +96,7 @@ tc_rowstats_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             TileCursor cx(t0, n, A.T, 0, 1);
             int hp = -1;          // head whose parameters are loaded
             int nloads = 0;
-            long long last = clock64();
+            long long last = now_ns();
             while (cx.valid() && !*abort_flag) {
                 bool progress = false, can = true;
                 const int head = cx.g >> 1;
@@ -122,10 +122,10 @@ tc_rowstats_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     progress = true;
                 }
                 if (progress) {
-                    last = clock64();
+                    last = now_ns();
                 } else {
                     __nanosleep(64);
-                    if (clock64() - last > kWaitLimitCycles) {
+                    if (now_ns() - last > kWaitLimitNs) {
                         *abort_flag = 1;
                         atomicOr(A.status, kDevErrTimeout);
                     }

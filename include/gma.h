@@ -65,8 +65,29 @@ typedef struct {
     gma_dtype in_dtype; /* dtype of Qx, Kx and V                                  */
     gma_dtype out_dtype;/* dtype of out                                           */
     float var_floor;    /* eps_sigma of Eq. 14 (> 0)                              */
-    int chunk;          /* causal chunk length in rows; 0 = library's choice      */
+    int chunk;          /* causal chunk length in rows (see below); 0 = default   */
 } gma_desc;
+
+/*
+ * desc->chunk: the number of rows over which a causal forward forms the masked
+ * intra-chunk affinity before it folds the chunk into its carried prefix state
+ * (section 3.5, Eq. 6b / 9b).  It changes only the rounding of the result, never
+ * its value in exact arithmetic.
+ *   - bf16 tensor-core causal paths (d = 64, K and dv multiples of 64): 128 rows,
+ *     the MMA tile; chunk must be 0 or 128, any other value returns
+ *     GMA_ERR_UNSUPPORTED.
+ *   - the float32 CUDA-core causal path (every other shape): any chunk >= 1 whose
+ *     per-chunk tiles fit one CTA's shared memory (4 (K (dv + 1) + 2 chunk K
+ *     + 2 chunk (dv + 1) + chunk^2) bytes <= 227 KB); larger values return
+ *     GMA_ERR_UNSUPPORTED.  0 selects 16.
+ *   - gma_backward with causal = 1: 64-row tiles; chunk must be 0 or 64.
+ *   - bidirectional calls, decode, cross-attention and diagnostics have no
+ *     chunked scan and ignore the field.
+ * A negative chunk is GMA_ERR_INVALID_ARG everywhere.
+ *
+ * Status codes are positive (GMA_OK = 0, errors 1..5) so that a caller can test
+ * `if (status)`; their names, not their values, are the interface.
+ */
 
 /*
  * Size in bytes of the device workspace that gma_forward() needs for this

@@ -123,3 +123,33 @@ def test_backward_and_decode_reject_bad_arguments_before_launching(lib):
     assert dec(*dargs(desc=_desc(d=64, K=256, dv=256))) == 2
     assert dec(*dargs(ws=None)) == 3
     assert dec(*dargs(wsb=1)) == 3
+
+
+def test_chunk_is_honoured_or_refused(lib):
+    # desc.chunk is the causal scan's chunk length: the tensor-core causal paths run
+    # 128-row chunks and refuse any other value; the float32 CUDA-core path takes any
+    # chunk whose tiles fit shared memory; bidirectional calls ignore it.
+    n = ctypes.c_size_t(0)
+    names = (ctypes.c_char_p * 16)()
+    cnt = ctypes.c_int(0)
+    ws = lambda causal, **kw: lib.gma_workspace_size(ctypes.byref(_desc(**kw)), causal, ctypes.byref(n))
+    tc = dict(d=64, K=64, dv=64)
+    sliced = dict(d=64, K=256, dv=128)
+    for shape in (tc, sliced):
+        assert ws(1, chunk=0, **shape) == 0
+        assert ws(1, chunk=128, **shape) == 0
+        for bad in (1, 64, 127, 256):
+            assert ws(1, chunk=bad, **shape) == 2, (shape, bad)
+        assert ws(0, chunk=64, **shape) == 0                       # bidirectional: ignored
+        assert lib.gma_forward_plan(ctypes.byref(_desc(chunk=64, **shape)), 1, ctypes.byref(cnt), names, 16) == 2
+    f32 = dict(d=16, K=8, dv=32, in_dtype=0, out_dtype=0)
+    for good in (0, 1, 7, 16, 64, 128):
+        assert ws(1, chunk=good, **f32) == 0, good
+    assert ws(1, chunk=4096, **f32) == 2                            # tiles beyond shared memory
+    assert ws(1, chunk=-1, **f32) == 1
+    assert lib.gma_forward_plan(ctypes.byref(_desc(chunk=64, **f32)), 1, ctypes.byref(cnt), names, 16) == 0
+    assert [names[i].decode() for i in range(cnt.value)][-1] == "simt_causal_chunk"
+    bw = dict(d=64, K=64, dv=64)
+    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(chunk=64, **bw)), 1, ctypes.byref(n)) == 0
+    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(chunk=128, **bw)), 1, ctypes.byref(n)) == 2
+    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(chunk=128, **bw)), 0, ctypes.byref(n)) == 0

@@ -87,20 +87,21 @@ def test_diagnostics_parity_small(case):
     check(w, x, run_gpu(x, w.var_floor))
 
 
-def test_diagnostics_full_size_matches_the_oracle_on_one_sequence():
-    # the 96-head N = 8192 workload: the oracle on batch entry 0, the full call checked by
-    # invariants and by its per-token results equal to the one-sequence call's
+def test_diagnostics_full_size_matches_the_oracle():
+    # the 96-head N = 8192 workload, every batch entry against the oracle, plus the
+    # one-sequence call's per-token results equal to the full call's
     w = inputs.WORKLOADS["causal_bf16_n8192"]
     x = inputs.gen_all(w)
-    one = run_gpu(x, w.var_floor, B=1)
-    check(w, x, one, B=1)
-    p, stats, z = run_gpu(x, w.var_floor)
+    full = run_gpu(x, w.var_floor)
+    check(w, x, full)
+    p, stats, z = full
     K = w.K
     assert abs(p.sum() - 1.0) < 1e-3
     assert 0.0 <= stats[1] <= stats[0] <= 1.0 + 1e-6
     assert 1.0 / K - 1e-6 <= stats[2] <= 1.0
-    assert np.array_equal(z[0], one[2][0])
     assert z.min() >= 0 and z.max() < K
+    one = run_gpu(x, w.var_floor, B=1)
+    assert np.array_equal(z[0], one[2][0])
 
 
 def test_diagnostics_unsupported_and_empty():

@@ -45,3 +45,20 @@ def test_a_wait_that_runs_out_posts_a_timeout_and_the_context_stays_usable():
     got = out.float().cpu().numpy().astype(np.float64)
     for h in range(w.H):
         assert np.abs(got[0, h] - ref[0, h]).max() / np.abs(ref[0, h]).max() <= TOL["bf16"]
+
+
+def test_check_status_raises_on_a_posted_device_error():
+    # a device error already posted to a workspace's status word is raised by the next
+    # call made with check_status=True on that workspace, and the word is cleared
+    import gaussian_mixture_latent_gb300 as gma
+    w = inputs.Workload("chk", B=1, H=1, N=200, d=64, K=64, dv=64, dtype="bf16", causal=False)
+    x = inputs.gen_all(w)
+    args = [to_device(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha")]
+    desc = gma._make_desc(w.B, w.H, w.N, w.d, w.K, w.dv, torch.bfloat16, torch.bfloat16, w.var_floor, 0)
+    ws = torch.zeros(gma.gma_workspace_size(desc, False), dtype=torch.uint8, device="cuda")
+    gma.gma_forward(*args, eps=w.eps, workspace=ws, check_status=True)      # clean: no error
+    gma.gma_selftest_timeout(ws)
+    with pytest.raises(gma.GmaError) as e:
+        gma.gma_forward(*args, eps=w.eps, workspace=ws, check_status=True)
+    assert e.value.code == 5
+    gma.gma_forward(*args, eps=w.eps, workspace=ws, check_status=True)      # cleared by the read

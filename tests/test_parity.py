@@ -91,23 +91,21 @@ def test_parity_large_eps_and_zero_eps():
     check_heads(w0, x, run_gpu(w0, x), [0, 1])
 
 
-FULL = {
-    "bidir_f32_n256": None,
-    "bidir_bf16_n4096": None,
-    "causal_bf16_n8192": None,
-    "bidir_bf16_n65536": [0, 7, 15],
-    "causal_bf16_n131072": [0, 13],
-}
+FULL = ["bidir_f32_n256", "bidir_bf16_n4096", "causal_bf16_n8192", "bidir_bf16_n65536",
+        "causal_bf16_n131072"]
 
 
-@pytest.mark.parametrize("name", list(FULL))
+@pytest.mark.parametrize("name", FULL)
 def test_parity_full_size(name):
+    # every head of every workload against the oracle, in the launch configuration the
+    # benchmark times: persistent CTAs cross head boundaries at positions that differ
+    # from head to head, so no head is left to a finiteness check
     w = inputs.WORKLOADS[name]
     x = inputs.gen_all(w)
     out = run_gpu(w, x)
-    heads = FULL[name] if FULL[name] is not None else list(range(w.G))
+    heads = list(range(w.G))
     err = check_heads(w, x, out, heads)
-    print(f"{name}: max relative error {err:.3e} over heads {heads if len(heads) < 8 else len(heads)}")
+    print(f"{name}: max relative error {err:.3e} over all {len(heads)} heads")
 
 
 @pytest.mark.parametrize("K,dv", [(64, 64), (256, 128)], ids=["direct", "sliced"])
@@ -206,3 +204,24 @@ def test_back_to_back_forwards_do_not_interfere():
     assert gma.gma_get_status() == 0
     for i, causal, o in outs:
         assert np.array_equal(to_f64(o), alone[i, causal])
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 64, 100])
+def test_cuda_core_causal_honours_the_chunk(chunk):
+    # the float32 path scans in chunks of the requested length; every length gives the
+    # oracle's result (the chunk changes only the rounding) and a ragged final chunk
+    w = inputs.Workload("chunk_f32", B=1, H=2, N=301, d=16, K=8, dv=32, dtype="f32", causal=True, seed=9)
+    x = inputs.gen_all(w)
+    check_heads(w, x, run_gpu(w, x, chunk=chunk), [0, 1])
+
+
+def test_tensor_core_causal_chunk_128_equals_default_and_others_are_refused():
+    import gaussian_mixture_latent_gb300 as gma
+    w = inputs.Workload("chunk_tc", B=1, H=2, N=700, d=64, K=64, dv=64, dtype="bf16", causal=True, seed=9)
+    x = inputs.gen_all(w)
+    a, b = to_f64(run_gpu(w, x, chunk=0)), to_f64(run_gpu(w, x, chunk=128))
+    assert np.array_equal(a, b)
+    for bad in (64, 256):
+        with pytest.raises(gma.GmaError) as e:
+            run_gpu(w, x, chunk=bad)
+        assert e.value.code == 2
