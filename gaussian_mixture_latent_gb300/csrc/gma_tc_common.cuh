@@ -397,13 +397,13 @@ inline EncodeTiled encode_fn() {
     return fn;
 }
 
-// 3D bf16 tensor map over [G][N][width], box [1][128][64], 128-byte swizzle.
-inline bool make_map(CUtensorMap *m, const void *base, int G, int N, int width) {
+// 3D bf16 tensor map over [G][N][width], box [1][box_rows][64], 128-byte swizzle.
+inline bool make_map(CUtensorMap *m, const void *base, int G, int N, int width, int box_rows = TM) {
     EncodeTiled enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)N, (cuuint64_t)G};
     const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * N};
-    const cuuint32_t box[3] = {64, TM, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     const cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
