@@ -56,9 +56,17 @@ def parse():
                          "diagnostics: one step is gma_diagnostics over the workload's query vectors; "
                          "cross: one step is gma_forward_cross, the workload's queries reading a context; "
                          "decode: one step is gma_decode of one new token for every head")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override the workload's sequence length N (a reduced case for profiling)")
     ap.add_argument("--context", type=int, default=0,
                     help="context length of --direction cross (default: 4 x the workload's N)")
     return ap.parse_args()
+
+
+def workload(args):
+    """The named workload, with its sequence length replaced when --seq-len is given."""
+    w = inputs.WORKLOADS[args.workload]
+    return w.replace(N=args.seq_len) if args.seq_len else w
 
 
 def dist_env():
@@ -243,7 +251,7 @@ def cpu_baseline(w, dirs=(False, True), seconds=12.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    w = inputs.WORKLOADS[args.workload]
+    w = workload(args)
     import oracle
     oracle.build()
     cores = max(1, len(os.sched_getaffinity(0)))
@@ -299,7 +307,7 @@ def run_gpu(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     _build.build()
-    w = inputs.WORKLOADS[args.workload]
+    w = workload(args)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
 
     # two resident input sets (each larger than L2), generated on the host
@@ -541,7 +549,7 @@ def run_diagnostics(args, rank, world, local):
     import torch
     import gaussian_mixture_latent_gb300 as gma
     from gaussian_mixture_latent_gb300 import _build
-    w = inputs.WORKLOADS[args.workload]
+    w = workload(args)
     if args.impl == "reference":
         if rank != 0:
             return 0
@@ -697,7 +705,7 @@ def run_cross(args, rank, world, local):
     import torch
     import gaussian_mixture_latent_gb300 as gma
     from gaussian_mixture_latent_gb300 import _build
-    w = inputs.WORKLOADS[args.workload]
+    w = workload(args)
     Nkv = args.context or 4 * w.N
     if args.impl == "reference":
         if rank != 0:
@@ -821,7 +829,7 @@ def run_decode(args, rank, world, local):
     import torch
     import gaussian_mixture_latent_gb300 as gma
     from gaussian_mixture_latent_gb300 import _build
-    w = inputs.WORKLOADS[args.workload]
+    w = workload(args)
     if args.impl == "reference":
         if rank != 0:
             return 0
@@ -940,7 +948,7 @@ def run_backward(args, rank, world, local):
     import torch
     import gaussian_mixture_latent_gb300 as gma
     from gaussian_mixture_latent_gb300 import _build
-    w = inputs.WORKLOADS[args.workload].replace(causal=args.direction == "backward_causal")
+    w = workload(args).replace(causal=args.direction == "backward_causal")
     metric = BWD_METRIC.format("causal" if w.causal else "bidirectional")
     if args.impl == "reference":
         if rank != 0:
