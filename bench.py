@@ -58,6 +58,8 @@ def parse():
                          "decode: one step is gma_decode of one new token for every head")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's sequence length N (a reduced case for profiling)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size B")
     ap.add_argument("--context", type=int, default=0,
                     help="context length of --direction cross (default: 4 x the workload's N)")
     return ap.parse_args()
@@ -66,7 +68,9 @@ def parse():
 def workload(args):
     """The named workload, with its sequence length replaced when --seq-len is given."""
     w = inputs.WORKLOADS[args.workload]
-    return w.replace(N=args.seq_len) if args.seq_len else w
+    if args.seq_len:
+        w = w.replace(N=args.seq_len)
+    return w.replace(B=args.batch) if args.batch else w
 
 
 def dist_env():
@@ -115,6 +119,8 @@ def fp32_simt_peak_tflops(sm_mhz):
 # it includes.  A recorded traffic figure holds while these files are unchanged.
 KERNEL_SOURCES = {
     "tc_causal": ("gma_tc_causal.cu", "gma_tc_common.cuh", "gma_sm100.cuh"),
+    "tc_causal_seg": ("gma_tc_causal.cu", "gma_tc_common.cuh", "gma_sm100.cuh"),
+    "tc_prefix": ("gma_tc.cu", "gma_tc_common.cuh", "gma_sm100.cuh"),
     "tc_write": ("gma_tc.cu", "gma_tc_common.cuh", "gma_sm100.cuh"),
     "tc_read": ("gma_tc.cu", "gma_tc_common.cuh", "gma_sm100.cuh"),
 }

@@ -67,7 +67,8 @@ def kernel_work(name: str, G, N, d, K, dv, in_dtype="bf16", out_dtype="bf16", H=
         return "hbm", rows * (e_in * (d + dv)), "byte"
     if name == "tc_read":
         return "hbm", rows * (e_in * d + e_out * dv), "byte"
-    if name == "tc_causal":
+    if name in ("tc_causal", "tc_causal_seg"):
+        # every routing row and value in once, every output row out once
         return "hbm", rows * (e_in * (2 * d + dv) + e_out * dv), "byte"
     if name == "tc_causal_slices":
         # the component-sliced scan does all of the path's contractions

@@ -109,10 +109,23 @@ gma_status build_forward_plan(const Problem &p, const Args *a, Plan &plan) {
     if ((tc_causal_supported(p) || tc_slice_supported(p)) && p.chunk != 0 && p.chunk != kTcChunkRows)
         return GMA_ERR_UNSUPPORTED;
     if (tc_causal_supported(p)) {
-        const TcLayout T = tc_causal_layout(p);
-        plan.workspace = T.total;
         const Args A = a ? *a : z;
         char *ws = A.ws;
+        SegTable seg;
+        if (tc_seg_plan(p, seg)) {
+            // fewer heads than SMs: the segment-parallel scan over balanced chunk ranges, after
+            // the prefix pass for the ranges that start inside a head
+            const TcLayout T = tc_seg_layout(p, seg);
+            plan.workspace = T.total;
+            plan.add("tc_params", [=](cudaStream_t s) { return tc_params(p, T, A.mu, A.rho, A.alpha, ws, s); });
+            if (seg.np > 0)
+                plan.add("tc_prefix", [=](cudaStream_t s) { return tc_prefix(p, T, seg, A.Kx, A.V, ws, s); });
+            plan.add("tc_causal_seg", [=](cudaStream_t s) {
+                return tc_causal_seg(p, T, seg, A.Qx, A.Kx, A.V, A.out, ws, s); });
+            return GMA_OK;
+        }
+        const TcLayout T = tc_causal_layout(p);
+        plan.workspace = T.total;
         plan.add("tc_causal", [=](cudaStream_t s) {
             return tc_causal(p, T, A.Qx, A.Kx, A.V, A.mu, A.rho, A.alpha, A.out, ws, s); });
         return GMA_OK;

@@ -82,6 +82,34 @@ cudaError_t tc_combine(const Problem &p, const TcLayout &L, void *out, char *ws,
 cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
                       const float *mu, const float *rho, const float *alpha, void *out, char *ws, cudaStream_t s);
 
+// Segment-parallel form of the causal scan (d = dv = K = 64), for problems with fewer
+// heads than SMs: ns scan CTAs take balanced contiguous ranges of the (head, 128-row
+// chunk) list, so a range may start inside a head and may cross into the next.  A
+// range that starts at chunk a > 0 of head g needs the prefix state of chunks [0, a)
+// of g (Eq. 6b): the prefix pass (tc_write over "prefix segments") sums
+// gamma^K^T [V | 1] over each segment, where the segment of scan CTA i is the part of
+// CTA i-1's range that lies in the head where CTA i starts; CTA i adds the partial
+// slots of the segments of its head up to its own, in a fixed order.
+constexpr int kMaxScanCtas = 152;
+struct SegEntry {
+    int32_t g;               // head
+    int16_t a, len;          // chunks [a, a + len) of head g
+    int16_t plo, phi;        // prefix-pass CTAs plo..phi covered it (partial slots p + segment)
+};
+struct SegTable {
+    int32_t nseg, ns, np, nch, vtot;              // segments, scan CTAs, prefix-pass CTAs, chunks per head, total
+    SegEntry seg[kMaxScanCtas];                   // prefix segments in scan-CTA order
+    int16_t pre_v[kMaxScanCtas], pre_jj[kMaxScanCtas];   // prefix-pass CTA p starts at chunk pre_jj[p] of segment pre_v[p]
+    int16_t scan_seg[kMaxScanCtas];               // scan CTA i: the segment that ends at its start (-1: a head start)
+};
+// Fills the plan and returns true when the segment-parallel form applies (fewer heads than SMs).
+bool tc_seg_plan(const Problem &p, SegTable &T);
+TcLayout tc_seg_layout(const Problem &p, const SegTable &T);
+cudaError_t tc_prefix(const Problem &p, const TcLayout &L, const SegTable &T, const void *Kx, const void *V, char *ws,
+                      cudaStream_t s);
+cudaError_t tc_causal_seg(const Problem &p, const TcLayout &L, const SegTable &T, const void *Qx, const void *Kx,
+                          const void *V, void *out, char *ws, cudaStream_t s);
+
 // ----- responsibility diagnostics (section 5.4): gma_tc_diag.cu (uses tc_params) -----
 bool tc_diag_supported(const Problem &p);
 TcLayout tc_diag_layout(const Problem &p);

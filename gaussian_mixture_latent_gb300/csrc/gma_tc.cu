@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kParamThreads) tc_params_kernel(float var_floo
 
 // ------------------------------------------------------------------ tc_write
 
+
 template <int K>
 struct WriteCfg {
     static constexpr int KCH = (K + 63) / 64;
@@ -125,9 +126,13 @@ struct WriteCfg {
     static_assert(BYTES <= 232448 && COL_D2 + K <= TMEM_COLS, "write kernel exceeds shared memory or TMEM");
 };
 
-template <int K>
+// SEG = false: the CTA's range of the (head, tile) list, one partial slot per (CTA, head).
+// SEG = true: the prefix pass of the segment-parallel causal scan, the same walk over the
+// concatenated prefix segments of S, one partial slot per (CTA, segment).
+template <int K, bool SEG>
 __global__ void __launch_bounds__(WriteCfg<K>::THREADS, 1)
-tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, TcArgs A) {
+tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, TcArgs A,
+                const __grid_constant__ typename SegArg<SEG>::type S) {
     using C = WriteCfg<K>;
     constexpr int SX = C::SX, SV = C::SV, PN = C::PN, NW = C::NW;
     extern __shared__ uint8_t smem_raw[];
@@ -149,6 +154,10 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     int t0, t1;
     cta_range(A.Ttot, t0, t1);
     const int n = t1 - t0;
+    auto cursor = [&](int start, int step) {
+        if constexpr (SEG) return SegCursor(&S, blockIdx.x, n, start, step);
+        else return TileCursor(t0, n, A.T, start, step);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
@@ -179,7 +188,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
     if (warp == kWarpProducer) {
         if (lane == 0 && n > 0) {
-            TileCursor cx(t0, n, A.T, 0, 1), cv(t0, n, A.T, 0, 1);
+            auto cx = cursor(0, 1), cv = cursor(0, 1);
             // the first head's routing and value tiles do not depend on the previous kernel
             for (; cx.valid() && cx.hl == 0 && cx.i < SX; cx.next()) {
                 mbar_arrive_expect_tx(&xfull[cx.i], kTileBytes);
@@ -191,7 +200,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             grid_dep_wait();                               // the parameter blocks are written
             mbar_arrive_expect_tx(&w_full[0], param_bytes(K));
-            bulk_load(sm + C::OFF_P, A.params + (size_t)((t0 / A.T) % A.H) * A.param_stride, param_bytes(K),
+            bulk_load(sm + C::OFF_P, A.params + (size_t)(cursor(0, 1).g % A.H) * A.param_stride, param_bytes(K),
                       &w_full[0]);
             int p_loaded = 0;
             long long last = now_ns();
@@ -245,7 +254,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     } else if (warp == kWarpMma1) {
         // log-density MMAs: scores(i) = [x, x^2/256](i) . W^T into D1 of group i % NW
         if (n > 0) {                                 // the whole warp, converged
-            for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
+            for (auto c = cursor(0, 1); c.valid(); c.next()) {
                 const int i = c.i, b = c.hl % PN, w = i % NW;
                 if (c.first() && !mbar_wait_warp(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
                 if (!mbar_wait_warp(&a_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
@@ -263,7 +272,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         if (n > 0) {                                 // the whole warp, converged
             constexpr uint32_t idesc = idesc_f16(1, 1, 1, 1, TM, K);
             const uint32_t ones = smem_u32(sm + C::OFF_ONES);
-            for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
+            for (auto c = cursor(0, 1); c.valid(); c.next()) {
                 const int i = c.i, s = i % SV, w = i % NW;
                 if (!mbar_wait_warp(&g_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
                 if (!mbar_wait_warp(&vfull[s], (i / SV) & 1, ab, kDevErrTimeout)) break;
@@ -293,7 +302,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         rt.wtid = threadIdx.x - kWarpCompute * 32 - rt.wg * kWgThreads;
         const int w = rt.wg;
         const bool elected = rt.wtid == 0;
-        TileCursor c(t0, n, A.T, w, NW);
+        auto c = cursor(w, NW);
         for (; c.valid(); c.next()) {
             const int i = c.i, hl = c.hl;
             // convert tile i into this group's A operand
@@ -340,13 +349,12 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             tc_fence_before();
             wg_sync(rt);
             if (elected) mbar_arrive(&g_full[w]);
-            const int g = c.g;
             if (c.last()) {
-                // drain [Vt | Z]^T of this head into partial slot (cta + head)
+                // drain [Vt | Z]^T of this head (segment) into partial slot (cta + head)
                 ok = mbar_wait(&d2_full[hl % NW], (hl / NW) & 1, ab, kDevErrTimeout);
                 if (!wg_all(rt, ok)) break;
                 tc_fence_after();
-                float *dst = A.partials + ((size_t)(blockIdx.x + g) * (DVV + 1) + rt.r) * K;
+                float *dst = A.partials + ((size_t)(blockIdx.x + c.slot()) * (DVV + 1) + rt.r) * K;
                 uint32_t v[K];
 #pragma unroll
                 for (int cc = 0; cc < K / 32; ++cc) tmem_ld32(tmem + rt.lane_off + C::COL_D2 + 32 * cc, v + 32 * cc);
@@ -680,10 +688,11 @@ cudaError_t launch_write(const Problem &p, const TcLayout &L, const void *Kx, co
     a.params = reinterpret_cast<const uint8_t *>(ws + L.params); a.param_stride = L.param_stride;
     a.partials = reinterpret_cast<float *>(ws + L.part);
     a.status = reinterpret_cast<unsigned *>(ws);
-    auto kern = tc_write_kernel<K>;
+    auto kern = tc_write_kernel<K, false>;
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), WriteCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
-    return launch_dependent(kern, dim3(L.ncta_kv), dim3(WriteCfg<K>::THREADS), WriteCfg<K>::BYTES, s, tk, tv, a);
+    return launch_dependent(kern, dim3(L.ncta_kv), dim3(WriteCfg<K>::THREADS), WriteCfg<K>::BYTES, s, tk, tv, a,
+                            NoSeg{});
 }
 
 template <int K>
@@ -745,6 +754,22 @@ cudaError_t tc_params(const Problem &p, const TcLayout &L, const float *mu, cons
 cudaError_t tc_write(const Problem &p, const TcLayout &L, const void *Kx, const void *V, char *ws,
                      cudaStream_t s) {
     return p.K == 64 ? launch_write<64>(p, L, Kx, V, ws, s) : launch_write<128>(p, L, Kx, V, ws, s);
+}
+
+cudaError_t tc_prefix(const Problem &p, const TcLayout &L, const SegTable &T, const void *Kx, const void *V, char *ws,
+                      cudaStream_t s) {
+    if (T.np == 0) return cudaSuccess;
+    CUtensorMap tk, tv;
+    if (!make_map(&tk, Kx, p.G, p.N, DR) || !make_map(&tv, V, p.G, p.N, DVV)) return cudaErrorInvalidValue;
+    TcArgs a{};
+    a.G = p.G; a.H = p.H; a.N = p.N; a.T = T.nch; a.Ttot = T.vtot; a.K = 64;
+    a.params = reinterpret_cast<const uint8_t *>(ws + L.params); a.param_stride = L.param_stride;
+    a.partials = reinterpret_cast<float *>(ws + L.part);
+    a.status = reinterpret_cast<unsigned *>(ws);
+    auto kern = tc_write_kernel<64, true>;
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), WriteCfg<64>::BYTES);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(kern, dim3(T.np), dim3(WriteCfg<64>::THREADS), WriteCfg<64>::BYTES, s, tk, tv, a, T);
 }
 
 cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s) {

@@ -36,6 +36,9 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <cstring>
+
 #include "gma_internal.h"
 #include "gma_sm100.cuh"
 #include "gma_tc_common.cuh"
@@ -53,7 +56,7 @@ constexpr int kWProd = 0, kWIss1 = 1, kWIss2 = 2, kWGroups = 3;
 constexpr int NOUT = 80;               // [S | z | 1 | 0...] and [V | 1 | 0...] widths
 
 struct CausalArgs {
-    int G, H, N, nch;
+    int G, H, N, nch;      // nch: 128-row chunks per head
     const uint8_t *params;
     uint32_t param_stride;
     float eps;
@@ -68,6 +71,8 @@ struct CausalArgs {
     // one head per CTA: the CTA builds its head's parameter block from these
     const float *mu, *rho, *alpha;   // [H][K][d], [H][K][d], [H][K]
     float var_floor;
+    // segment-parallel form: the prefix pass's partial slots [slot][dv + 1][K] f32
+    const float *partials;
 };
 
 struct CausalCfg {
@@ -111,11 +116,16 @@ static __device__ __noinline__ void build_param_block_team(int tid, ParamLoads<K
 // log-sum-exp, e^Q is taken relative to the row's maximum over all components,
 // and the CTA writes its partial numerator and denominator, which the combine
 // kernel sums over component slices (every term is a sum over components).
-template <bool SLICE>
+// SEG = true (with SLICE = false): the segment-parallel form.  CTA i scans the
+// chunks [t0, t1) of the (head, chunk) list given by the plan S; a range that starts
+// inside a head first sums its prefix from the prefix pass's partial slots (into the
+// fp32 state and its bf16 snapshot), and at a head boundary inside the range the state
+// restarts from zero and the next head's parameter block is loaded.
+template <bool SLICE, bool SEG>
 __global__ void __launch_bounds__(kCThreads, 1)
 tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                 CausalArgs A) {
+                 CausalArgs A, const __grid_constant__ typename SegArg<SEG>::type S) {
     using C = CausalCfg;
     constexpr int K = KC;
     extern __shared__ uint8_t smem_raw[];
@@ -133,18 +143,35 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint64_t *tb_full = tb0_free + 1, *d3_full = tb_full + 1, *d3_empty = d3_full + 1, *eq_free = d3_empty + 1;
     uint64_t *s_upd = eq_free + 1, *s_ready = s_upd + 1, *sb_empty = s_ready + 2;
     uint64_t *fin1 = sb_empty + 2, *fin2 = fin1 + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
+    uint64_t *w_empty = fin2 + 1;                      // segment-parallel form: parameter block consumed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(w_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.x, nch = A.nch;
+    // this CTA's chunks: all chunks of head blockIdx.x, or (segment-parallel form) the range
+    // [t0c, t0c + nch) of the (head, chunk) list, which may start inside a head (mid) and
+    // cross into the next; local chunk c is chunk cc of head gh (locate)
+    const int hch = A.nch;
+    int t0c = (int)blockIdx.x * hch, nch = hch;
+    if constexpr (SEG) {
+        const long long tt = (long long)A.G * hch;
+        t0c = (int)(((long long)blockIdx.x * tt) / S.ns);
+        nch = (int)(((long long)(blockIdx.x + 1) * tt) / S.ns) - t0c;
+    }
+    const int g = t0c / hch, cc0 = t0c - g * hch;
+    const bool mid = SEG && cc0 != 0;
+    auto locate = [&](int c, int &gh, int &cc) {
+        cc = cc0 + c;
+        gh = g;
+        while (cc >= hch) { cc -= hch; ++gh; }
+    };
     const int ks = SLICE ? (int)blockIdx.y : 0, vs = SLICE ? (int)blockIdx.z : 0;   // component / value slice
     grid_dep_launch();
     // direct form: the compute groups put the head's parameter loads in flight before the prologue
     constexpr int kTeam = 3 * kWgThreads, kTeamBar = 4;
     const int ttid = (int)threadIdx.x - kWGroups * 32;
     ParamLoads<K, kTeam> pld;
-    if (!SLICE && ttid >= 0) {
+    if (!SLICE && !SEG && ttid >= 0) {
         const int h = g % A.H;
         pld.issue(ttid, A.mu + (size_t)h * K * DR, A.rho + (size_t)h * K * DR, A.alpha + (size_t)h * K);
     }
@@ -155,7 +182,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(&vfull[s], 1); mbar_init(&vempty[s], 1); mbar_init(&s_ready[s], 1); mbar_init(&sb_empty[s], 1);
         }
         for (uint64_t *b = w_full; b <= s_upd; ++b) mbar_init(b, 1);
-        mbar_init(fin1, 1); mbar_init(fin2, 1);
+        mbar_init(fin1, 1); mbar_init(fin2, 1); mbar_init(w_empty, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -182,23 +209,38 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Abort ab{abort_flag, A.status};
-    if (threadIdx.x == 0) mbar_arrive(&s_ready[0]);              // state operand for chunk 0 is ready
+    // the state operand for chunk 0 is ready (zero), unless the range starts inside a head
+    if (threadIdx.x == 0 && !mid) mbar_arrive(&s_ready[0]);
 
     if (warp == kWProd) {
         if (lane == 0) {
             // the first tiles do not depend on the previous kernel; the parameter block does
-            int qi = 0, ki = 0, vi = 0;
+            int qi = 0, ki = 0, vi = 0, gh, cc;
             for (; ki < 2 && ki < nch; ++ki) {
+                locate(ki, gh, cc);
                 mbar_arrive_expect_tx(&kfull[ki], kTileBytes);
-                tma_load_3d(sm + C::OFF_K + ki * kTileBytes, &tm_k, &kfull[ki], 0, ki * TM, g);
+                tma_load_3d(sm + C::OFF_K + ki * kTileBytes, &tm_k, &kfull[ki], 0, cc * TM, gh);
             }
             for (; qi < 2 && qi < nch; ++qi) {
+                locate(qi, gh, cc);
                 mbar_arrive_expect_tx(&qfull[qi], kTileBytes);
-                tma_load_3d(sm + C::OFF_Q + qi * kTileBytes, &tm_q, &qfull[qi], 0, qi * TM, g);
+                tma_load_3d(sm + C::OFF_Q + qi * kTileBytes, &tm_q, &qfull[qi], 0, cc * TM, gh);
             }
             for (; vi < 2 && vi < nch; ++vi) {
+                locate(vi, gh, cc);
                 mbar_arrive_expect_tx(&vfull[vi], kTileBytes);
-                tma_load_3d(sm + C::OFF_V + vi * kTileBytes, &tm_v, &vfull[vi], 64 * vs, vi * TM, g);
+                tma_load_3d(sm + C::OFF_V + vi * kTileBytes, &tm_v, &vfull[vi], 64 * vs, cc * TM, gh);
+            }
+            // segment-parallel form: the parameter blocks (tc_params) of the range's heads, one
+            // at a time through the one buffer, each once the previous head's MMAs are done with it
+            int p_loaded = 0;
+            int nheads = 0;
+            if (SEG) {
+                nheads = (cc0 + nch - 1) / hch + 1;
+                grid_dep_wait();
+                mbar_arrive_expect_tx(w_full, param_bytes(K));
+                bulk_load(sm + C::OFF_P, A.params + (size_t)(g % A.H) * A.param_stride, param_bytes(K), w_full);
+                p_loaded = 1;
             }
             if (SLICE) {
                 grid_dep_wait();
@@ -213,23 +255,33 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 bulk_load(sm + C::OFF_P + param_scale_off(K), blk + param_scale_off(A.Kfull), 16u, w_full);
             }
             long long last = now_ns();
-            while ((qi < nch || ki < nch || vi < nch) && !*abort_flag) {
+            while ((qi < nch || ki < nch || vi < nch || p_loaded < nheads) && !*abort_flag) {
                 bool progress = false;
+                if (SEG && p_loaded < nheads && mbar_test(w_empty, (p_loaded - 1) & 1)) {
+                    mbar_arrive_expect_tx(w_full, param_bytes(K));
+                    bulk_load(sm + C::OFF_P, A.params + (size_t)((g + p_loaded) % A.H) * A.param_stride,
+                              param_bytes(K), w_full);
+                    ++p_loaded;
+                    progress = true;
+                }
                 if (ki < nch && (ki < 2 || mbar_test(&kempty[ki & 1], ((ki >> 1) - 1) & 1))) {
+                    locate(ki, gh, cc);
                     mbar_arrive_expect_tx(&kfull[ki & 1], kTileBytes);
-                    tma_load_3d(sm + C::OFF_K + (ki & 1) * kTileBytes, &tm_k, &kfull[ki & 1], 0, ki * TM, g);
+                    tma_load_3d(sm + C::OFF_K + (ki & 1) * kTileBytes, &tm_k, &kfull[ki & 1], 0, cc * TM, gh);
                     ++ki;
                     progress = true;
                 }
                 if (qi < nch && (qi < 2 || mbar_test(&qempty[qi & 1], ((qi >> 1) - 1) & 1))) {
+                    locate(qi, gh, cc);
                     mbar_arrive_expect_tx(&qfull[qi & 1], kTileBytes);
-                    tma_load_3d(sm + C::OFF_Q + (qi & 1) * kTileBytes, &tm_q, &qfull[qi & 1], 0, qi * TM, g);
+                    tma_load_3d(sm + C::OFF_Q + (qi & 1) * kTileBytes, &tm_q, &qfull[qi & 1], 0, cc * TM, gh);
                     ++qi;
                     progress = true;
                 }
                 if (vi < nch && (vi < 2 || mbar_test(&vempty[vi & 1], ((vi >> 1) - 1) & 1))) {
+                    locate(vi, gh, cc);
                     mbar_arrive_expect_tx(&vfull[vi & 1], kTileBytes);
-                    tma_load_3d(sm + C::OFF_V + (vi & 1) * kTileBytes, &tm_v, &vfull[vi & 1], 64 * vs, vi * TM, g);
+                    tma_load_3d(sm + C::OFF_V + (vi & 1) * kTileBytes, &tm_v, &vfull[vi & 1], 64 * vs, cc * TM, gh);
                     ++vi;
                     progress = true;
                 }
@@ -247,6 +299,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             wind_down_ring(qfull, 2, qi, A.status);
             wind_down_ring(vfull, 2, vi, A.status);
             if (SLICE) wait_ignoring_abort(w_full, 0, A.status);
+            if (SEG && p_loaded > 0) wait_ignoring_abort(w_full, (p_loaded - 1) & 1, A.status);
         }
     } else if (warp == kWIss1) {
         // log-density MMAs: scores = [x, x^2/256] . W^T, keys then queries of each chunk
@@ -254,6 +307,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t pw = smem_u32(sm + C::OFF_P), ca = smem_u32(sm + C::OFF_CA);
             bool ok = mbar_wait_warp(w_full, 0, ab, kDevErrTimeout);
             for (int c = 0; c < nch && ok; ++c) {
+                int gh, cc;
+                locate(c, gh, cc);
+                // segment-parallel form: the next head's parameter block
+                if (SEG && c > 0 && cc == 0 && !(ok = mbar_wait_warp(w_full, (gh - g) & 1, ab, kDevErrTimeout))) break;
                 if (!(ok = mbar_wait_warp(ak_full, c & 1, ab, kDevErrTimeout))) break;
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::COL_D1K, tmem + C::COL_AK, pw, ca);
@@ -262,6 +319,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_after();
                 issue_logdensity<K>(tmem + C::COL_D1Q, tmem + C::COL_AQ, pw, ca);
                 mma_commit(d1q_full);
+                if (SEG && cc == hch - 1 && c + 1 < nch) mma_commit(w_empty);   // the head's last chunk
             }
             mma_commit(fin1);
             wait_ignoring_abort(fin1, 0, A.status);
@@ -308,10 +366,14 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_after();
                 const uint32_t va = smem_u32(sm + C::OFF_V + s * kTileBytes);
                 const uint64_t vd = sdesc_sw128(va, ones - va, 1024);
+                // the state restarts at a head's first chunk (a range starting inside a head holds its prefix)
+                int gh, cc;
+                locate(c, gh, cc);
+                const bool fresh = SEG ? cc == 0 : c == 0;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ss(tmem + C::COL_S, vd + (uint64_t)(ks * 128), gm + (uint64_t)(ks * 128), idesc_u,
-                           !(c == 0 && ks == 0));
+                           !(fresh && ks == 0));
                 mma_commit(s_upd);
                 mma_commit(g_empty);
                 // read(c) = mask(T) . [V | 1] + e^Q(c) . [S | z | 1]_{c-1}, in the order that frees
@@ -362,7 +424,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int row = c * TM + (int)rt.r;
             return row < A.N ? __ldg(A.mrow_q + (size_t)g * A.N + row) : 0.f;
         };
-        if (!SLICE) {
+        if (!SLICE && !SEG) {
             // The three groups build the head's parameter block straight into the operand block
             // the log-density MMAs read (scratch: the gamma buffer, which holds nothing yet).
             build_param_block_team(ttid, pld, A.var_floor, sm + C::OFF_P, reinterpret_cast<float *>(sm + C::OFF_G));
@@ -385,6 +447,52 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 return true;
             };
             bool ok = convert_k(0);
+            if constexpr (SEG) {
+                if (mid && ok) {
+                    // the prefix state of chunks [0, cc0) of head g: the partial slots of this head's
+                    // prefix segments up to this CTA's, in order, each over the prefix-pass CTAs that
+                    // covered it (fixed order); into the fp32 state in TMEM and the bf16 snapshot
+                    grid_dep_wait();
+                    const int s_last = S.scan_seg[blockIdx.x];
+                    int s_first = s_last;
+                    while (s_first > 0 && S.seg[s_first - 1].g == g) --s_first;
+                    uint32_t acc[K];
+#pragma unroll
+                    for (int k = 0; k < K; ++k) acc[k] = 0u;
+                    if (rt.r <= DVV) {
+                        for (int sg = s_first; sg <= s_last; ++sg)
+                            for (int p = S.seg[sg].plo; p <= S.seg[sg].phi; ++p) {
+                                const float4 *src = reinterpret_cast<const float4 *>(
+                                    A.partials + ((size_t)(p + sg) * (DVV + 1) + rt.r) * K);
+#pragma unroll
+                                for (int k = 0; k < K / 4; ++k) {
+                                    const float4 f = src[k];
+                                    acc[4 * k] = __float_as_uint(__uint_as_float(acc[4 * k]) + f.x);
+                                    acc[4 * k + 1] = __float_as_uint(__uint_as_float(acc[4 * k + 1]) + f.y);
+                                    acc[4 * k + 2] = __float_as_uint(__uint_as_float(acc[4 * k + 2]) + f.z);
+                                    acc[4 * k + 3] = __float_as_uint(__uint_as_float(acc[4 * k + 3]) + f.w);
+                                }
+                            }
+                        uint8_t *row = sm + C::OFF_SB;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            uint4 o;
+                            o.x = pack_bf16(__uint_as_float(acc[8 * j + 0]), __uint_as_float(acc[8 * j + 1]));
+                            o.y = pack_bf16(__uint_as_float(acc[8 * j + 2]), __uint_as_float(acc[8 * j + 3]));
+                            o.z = pack_bf16(__uint_as_float(acc[8 * j + 4]), __uint_as_float(acc[8 * j + 5]));
+                            o.w = pack_bf16(__uint_as_float(acc[8 * j + 6]), __uint_as_float(acc[8 * j + 7]));
+                            *reinterpret_cast<uint4 *>(row + sw128_off(rt.r, j)) = o;
+                        }
+                    }
+                    tmem_st32(tmem + rt.lane_off + C::COL_S, acc);
+                    tmem_st32(tmem + rt.lane_off + C::COL_S + 32, acc + 32);
+                    tmem_st_wait();
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    wg_sync(rt);
+                    if (elected) mbar_arrive(&s_ready[0]);
+                }
+            }
             for (int c = 0; c < nch && ok; ++c) {
                 bool w = mbar_wait(d1k_full, c & 1, ab, kDevErrTimeout);
                 if (c >= 1) w = w && mbar_wait(g_empty, (c - 1) & 1, ab, kDevErrTimeout);
@@ -394,6 +502,12 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     grid_dep_wait();
                     scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull);
                     stat_next = lse_row(0);
+                }
+                int gh, cc;
+                locate(c, gh, cc);
+                if (SEG && (c == 0 || cc == 0)) {
+                    if (c == 0) grid_dep_wait();
+                    scale = head_scale(A.params, A.param_stride, gh % A.H, K);
                 }
                 // gamma^K = softmax of the key scores; rows past the sequence end get 0
                 uint32_t e[K / 2];
@@ -414,7 +528,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     f2_unpack(acc[0], s0, s1); f2_unpack(acc[1], s2, s3);
                     f2_unpack(acc[2], s4, s5); f2_unpack(acc[3], s6, s7);
                     const float total = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-                    inv = c * TM + (int)rt.r < A.N ? 1.0f / total : 0.f;
+                    inv = cc * TM + (int)rt.r < A.N ? 1.0f / total : 0.f;
                 }
                 const uint64_t inv2 = f2_pack(inv, inv);
 #pragma unroll
@@ -444,6 +558,10 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tmem_ld32(tmem + rt.lane_off + C::COL_S, v);
                     tmem_ld32(tmem + rt.lane_off + C::COL_S + 32, v + 32);
                     tmem_ld_wait();
+                    if (SEG && cc == 0) {                    // a new head: its state before chunk 0 is zero
+#pragma unroll
+                        for (int k = 0; k < K; ++k) v[k] = 0u;
+                    }
                     if (rt.r <= DVV) {
                         uint8_t *row = sm + C::OFF_SB + b * C::SBB;
 #pragma unroll
@@ -529,7 +647,9 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 fence_proxy_async_smem();
                 wg_sync(rt);
                 if (elected) {
-                    tma_store_3d(&tm_o, ob, 0, c * TM, g);
+                    int gh, cc;
+                    locate(c, gh, cc);
+                    tma_store_3d(&tm_o, ob, 0, cc * TM, gh);
                     bulk_commit_group();
                 }
             };
@@ -543,6 +663,14 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         grid_dep_wait();
                         scale = head_scale(A.params, A.param_stride, g % A.H, A.Kfull);
                         stat_next = max_row(0);
+                    }
+                    if (SEG) {
+                        int gh, cc;
+                        locate(c, gh, cc);
+                        if (c == 0 || cc == 0) {
+                            if (c == 0) grid_dep_wait();
+                            scale = head_scale(A.params, A.param_stride, gh % A.H, K);
+                        }
                     }
                     uint32_t e[K / 2];
                     if (SLICE) {
@@ -689,7 +817,7 @@ TcLayout tc_slice_layout(const Problem &p) {
 
 static cudaError_t launch_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
                                  const float *mu, const float *rho, const float *alpha, void *out, char *ws,
-                                 cudaStream_t s, bool slices) {
+                                 cudaStream_t s, bool slices, const SegTable *seg) {
     CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, Qx, p.G, p.N, DR) || !make_map(&tk, Kx, p.G, p.N, DR) || !make_map(&tv, V, p.G, p.N, p.dv) ||
         !make_map(&to, slices ? V : out, p.G, p.N, p.dv))
@@ -710,27 +838,114 @@ static cudaError_t launch_causal(const Problem &p, const TcLayout &L, const void
     } else {
         a.mu = mu; a.rho = rho; a.alpha = alpha;
         a.var_floor = p.var_floor;
+        a.partials = reinterpret_cast<const float *>(ws + L.part);
     }
-    auto kern = slices ? tc_causal_kernel<true> : tc_causal_kernel<false>;
+    if (seg) {
+        auto kern = tc_causal_kernel<false, true>;
+        cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), CausalCfg::BYTES);
+        if (e != cudaSuccess) return e;
+        return launch_dependent(kern, dim3(seg->ns), dim3(kCThreads), CausalCfg::BYTES, s, tq, tk, tv, to, a, *seg);
+    }
+    auto kern = slices ? tc_causal_kernel<true, false> : tc_causal_kernel<false, false>;
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), CausalCfg::BYTES);
     if (e != cudaSuccess) return e;
     if (!slices) {
         // the first kernel of its forward: an ordinary launch, so that every input is final when
         // its CTAs start
-        kern<<<dim3(p.G), dim3(kCThreads), CausalCfg::BYTES, s>>>(tq, tk, tv, to, a);
+        kern<<<dim3(p.G), dim3(kCThreads), CausalCfg::BYTES, s>>>(tq, tk, tv, to, a, NoSeg{});
         return cudaGetLastError();
     }
-    return launch_dependent(kern, dim3(p.G, L.ns, L.nt), dim3(kCThreads), CausalCfg::BYTES, s, tq, tk, tv, to, a);
+    return launch_dependent(kern, dim3(p.G, L.ns, L.nt), dim3(kCThreads), CausalCfg::BYTES, s, tq, tk, tv, to, a,
+                            NoSeg{});
 }
 
 cudaError_t tc_causal(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
                       const float *mu, const float *rho, const float *alpha, void *out, char *ws, cudaStream_t s) {
-    return launch_causal(p, L, Qx, Kx, V, mu, rho, alpha, out, ws, s, false);
+    return launch_causal(p, L, Qx, Kx, V, mu, rho, alpha, out, ws, s, false, nullptr);
 }
 
 cudaError_t tc_causal_slices(const Problem &p, const TcLayout &L, const void *Qx, const void *Kx, const void *V,
                              char *ws, cudaStream_t s) {
-    return launch_causal(p, L, Qx, Kx, V, nullptr, nullptr, nullptr, nullptr, ws, s, true);
+    return launch_causal(p, L, Qx, Kx, V, nullptr, nullptr, nullptr, nullptr, ws, s, true, nullptr);
+}
+
+// ------------------------------------------------------------------ segment-parallel plan
+
+// Used when the heads fill at most half of the SMs.  (With every SM running the scan, its
+// instruction fetch, not its work, sets the chunk period: at 96 heads on 152 SMs the split
+// measured a 44 % longer period per chunk and no net gain, so more heads keep one CTA each.)
+// Scan ranges: ns CTAs, CTA i takes chunks [i Ttot / ns, (i + 1) Ttot / ns) of the (head,
+// chunk) list, at least kMinSegChunks each, and only when that gives more CTAs than heads.
+// Prefix segments: for each CTA i whose range starts at chunk a > 0 of head g, the chunks of
+// g before a that belong to CTA i - 1's range.  Prefix-pass ranges: np CTAs over the
+// concatenated segments, balanced the same way.
+bool tc_seg_plan(const Problem &p, SegTable &T) {
+    constexpr int kMinSegChunks = 4;
+    std::memset(&T, 0, sizeof(T));
+    const int nsm = sm_count();
+    const int nch = (p.N + TM - 1) / TM;
+    const long long tt = (long long)p.G * nch;
+    if (nsm <= 0 || tt <= 0 || 2 * p.G > nsm) return false;
+    const long long ns = std::min<long long>({(long long)std::min(nsm, kMaxScanCtas), tt / kMinSegChunks, tt});
+    if (ns <= p.G) return false;
+    T.ns = (int)ns;
+    T.nch = nch;
+    auto t0 = [&](long long i) { return (i * tt) / ns; };
+    T.scan_seg[0] = -1;
+    int vtot = 0;
+    for (int i = 1; i < T.ns; ++i) {
+        const long long a0 = t0(i), g = a0 / nch, a = a0 - g * nch;
+        if (a == 0) { T.scan_seg[i] = -1; continue; }
+        const long long st = std::max(t0(i - 1), g * nch) - g * nch;
+        SegEntry &e = T.seg[T.nseg];
+        e.g = (int32_t)g;
+        e.a = (int16_t)st;
+        e.len = (int16_t)(a - st);
+        T.scan_seg[i] = (int16_t)T.nseg++;
+        vtot += (int)(a - st);
+    }
+    T.vtot = vtot;
+    T.np = vtot > 0 ? std::min({nsm, kMaxScanCtas, vtot}) : 0;
+    // prefix-pass CTA p covers [p vtot / np, (p + 1) vtot / np) of the concatenated segments
+    int sg = 0, off = 0;                                  // segment and the virtual offset of its start
+    for (int q = 0; q < T.np; ++q) {
+        const int v0 = (int)(((long long)q * vtot) / T.np);
+        while (off + T.seg[sg].len <= v0) { off += T.seg[sg].len; ++sg; }
+        T.pre_v[q] = (int16_t)sg;
+        T.pre_jj[q] = (int16_t)(v0 - off);
+    }
+    off = 0;
+    for (int k = 0; k < T.nseg; ++k) {
+        const int lo = off, hi = off + T.seg[k].len - 1;   // virtual range of segment k
+        int plo = (int)(((long long)lo * T.np) / vtot), phi = (int)(((long long)hi * T.np) / vtot);
+        while (plo > 0 && ((long long)plo * vtot) / T.np > lo) --plo;
+        while (((long long)(plo + 1) * vtot) / T.np <= lo) ++plo;
+        while (phi > 0 && ((long long)phi * vtot) / T.np > hi) --phi;
+        while (((long long)(phi + 1) * vtot) / T.np <= hi) ++phi;
+        T.seg[k].plo = (int16_t)plo;
+        T.seg[k].phi = (int16_t)phi;
+        off += T.seg[k].len;
+    }
+    return true;
+}
+
+TcLayout tc_seg_layout(const Problem &p, const SegTable &T) {
+    TcLayout L{};
+    L.T = T.nch;
+    L.Ttot = T.nch * p.G;
+    L.ncta = T.ns;
+    L.ns = L.nt = 1;
+    L.param_stride = align1k(param_bytes(p.K));
+    L.params = align_up(kHeaderBytes);
+    L.part = align_up(L.params + (size_t)p.H * L.param_stride);        // [np + nseg][dv + 1][K] f32
+    L.mem = L.part;
+    L.total = align_up(L.part + sizeof(float) * (size_t)(T.np + T.nseg + 1) * (DVV + 1) * p.K);
+    return L;
+}
+
+cudaError_t tc_causal_seg(const Problem &p, const TcLayout &L, const SegTable &T, const void *Qx, const void *Kx,
+                          const void *V, void *out, char *ws, cudaStream_t s) {
+    return launch_causal(p, L, Qx, Kx, V, nullptr, nullptr, nullptr, out, ws, s, false, &T);
 }
 
 }  // namespace gma

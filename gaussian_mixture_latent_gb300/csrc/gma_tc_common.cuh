@@ -12,6 +12,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "gma_internal.h"
 #include "gma_sm100.cuh"
 
 namespace gma {
@@ -49,7 +50,8 @@ __host__ __device__ constexpr uint32_t nosw16_off(uint32_t row, uint32_t col) {
 __host__ __device__ constexpr uint32_t mem_bytes(int K) { return (uint32_t)((K + 63) / 64) * 80u * 128u; }
 
 // Walks the CTA's tiles in steps of `step` without dividing inside the loop:
-// i = local tile index, g = head, j = tile within the head, hl = g - first head.
+// i = local tile index, g = head, j = tile within the head, hl = g - first head;
+// slot() = the unit whose sum the tile belongs to (its head).
 struct TileCursor {
     int i, g, j, hl, T, n, step;
     __device__ TileCursor(int t0, int n_, int T_, int start, int step_) : T(T_), n(n_), step(step_) {
@@ -61,12 +63,49 @@ struct TileCursor {
     __device__ bool valid() const { return i < n; }
     __device__ bool first() const { return j == 0 || i == 0; }
     __device__ bool last() const { return j == T - 1 || i == n - 1; }
+    __device__ int slot() const { return g; }
     __device__ void next() {
         i += step;
         j += step;
         while (j >= T) { j -= T; ++g; ++hl; }
     }
 };
+
+// The same walk over the prefix segments of a segment-parallel causal scan: the CTA's
+// range of the concatenated segments (segment v = chunks [a, a + len) of head g), from
+// the start the plan recorded for it.  j = chunk within the head, hl = v - first
+// segment, slot() = v.
+struct SegCursor {
+    const SegTable *S;
+    int i, g, j, hl, n, step, v, jj;
+    __device__ SegCursor(const SegTable *S_, int cta, int n_, int start, int step_) : S(S_), n(n_), step(step_) {
+        v = S->pre_v[cta];
+        jj = S->pre_jj[cta];
+        i = start;
+        hl = 0;
+        jj += start;
+        settle();
+    }
+    __device__ void settle() {
+        while (v < S->nseg && jj >= S->seg[v].len) { jj -= S->seg[v].len; ++v; ++hl; }
+        if (v < S->nseg) { g = S->seg[v].g; j = S->seg[v].a + jj; }
+    }
+    __device__ bool valid() const { return i < n; }
+    __device__ bool first() const { return jj == 0 || i == 0; }
+    __device__ bool last() const { return jj == S->seg[v].len - 1 || i == n - 1; }
+    __device__ int slot() const { return v; }
+    __device__ void next() {
+        i += step;
+        jj += step;
+        settle();
+    }
+};
+
+// The segment table as a kernel parameter of the kernels that walk it (an empty
+// struct for the others).
+struct NoSeg {};
+template <bool SEG> struct SegArg { using type = NoSeg; };
+template <> struct SegArg<true> { using type = SegTable; };
 
 // ------------------------------------------------------------------ wind-down helpers
 

@@ -67,6 +67,11 @@ SMALL = [
     ("bf16_many_heads", 8, 64, 200, 64, 64, 64, "bf16", False),
     ("bf16_many_heads_k128", 4, 32, 300, 64, 128, 64, "bf16", False),
     ("bf16_many_heads_causal", 4, 48, 300, 64, 64, 64, "bf16", True),
+    # segment-parallel causal scan (fewer heads than SMs): ranges that start inside a head
+    # (prefix pass), cross into the next head, and long prefix chains
+    ("bf16_seg_cross_heads", 2, 4, 1100, 64, 64, 64, "bf16", True),
+    ("bf16_seg_long_chain", 1, 3, 5000, 64, 64, 64, "bf16", True),
+    ("bf16_seg_one_head", 1, 1, 9000, 64, 64, 64, "bf16", True),
     # component-sliced causal path: K > 64 or dv > 64
     ("bf16_k128_causal", 2, 3, 700, 64, 128, 64, "bf16", True),
     ("bf16_k192_causal_ragged", 1, 2, 301, 64, 192, 64, "bf16", True),
