@@ -25,13 +25,15 @@ __all__ = [
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_PKG, "libgma.so")
+# GMA_LIBRARY selects another build of the library, such as the index-checking debug
+# build (libgma_debug.so, _build.build(debug=True)).
+_LIB_PATH = os.environ.get("GMA_LIBRARY") or os.path.join(_PKG, "libgma.so")
 _lib = None
 
 GMA_F32, GMA_BF16 = 0, 1
 _DTYPES = {torch.float32: GMA_F32, torch.bfloat16: GMA_BF16}
 _STATUS = {0: "GMA_OK", 1: "GMA_ERR_INVALID_ARG", 2: "GMA_ERR_UNSUPPORTED",
-           3: "GMA_ERR_WORKSPACE", 4: "GMA_ERR_CUDA", 5: "GMA_ERR_TIMEOUT"}
+           3: "GMA_ERR_WORKSPACE", 4: "GMA_ERR_CUDA", 5: "GMA_ERR_TIMEOUT", 6: "GMA_ERR_BOUNDS"}
 
 
 class GmaError(RuntimeError):

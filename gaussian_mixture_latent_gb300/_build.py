@@ -2,7 +2,10 @@
 
 Each ``csrc/*.cu`` file compiles to its own object in parallel; the objects
 link into one shared library next to this file.  Rebuilds only when a
-source or header is newer than the library.
+source or header is newer than the library.  ``build(debug=True)`` makes the
+index-checking debug build ``libgma_debug.so`` (``GMA_DEBUG_BOUNDS``: the
+kernels check their global-memory indices and post GMA_ERR_BOUNDS instead of
+performing an access that fails).
 """
 from __future__ import annotations
 
@@ -16,6 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgma.so")
+LIB_DEBUG = os.path.join(PKG, "libgma_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -36,21 +40,23 @@ def _deps():
             + glob.glob(os.path.join(ROOT, "include", "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
-    flags = NVCC_FLAGS + list(extra_flags or [])
+def build(force: bool = False, verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    lib = LIB_DEBUG if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
+    objdir = os.path.join(OBJDIR, "debug") if debug else OBJDIR
+    os.makedirs(objdir, exist_ok=True)
+    flags = NVCC_FLAGS + list(extra_flags or []) + (["-DGMA_DEBUG_BOUNDS"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc()] + ARCH + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -62,13 +68,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     srcs = _sources()
     with ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -432,6 +432,7 @@ gma_status gma_get_status(void *workspace, void *stream) {
     if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return GMA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return GMA_ERR_CUDA;
     if (word & kDevErrTimeout) return GMA_ERR_TIMEOUT;
+    if (word & kDevErrBounds) return GMA_ERR_BOUNDS;
     return GMA_OK;
 }
 
@@ -443,6 +444,7 @@ const char *gma_status_string(gma_status status) {
         case GMA_ERR_WORKSPACE: return "GMA_ERR_WORKSPACE: workspace missing or too small";
         case GMA_ERR_CUDA: return "GMA_ERR_CUDA: CUDA runtime error or failed launch";
         case GMA_ERR_TIMEOUT: return "GMA_ERR_TIMEOUT: a device-side bounded wait ran out";
+        case GMA_ERR_BOUNDS: return "GMA_ERR_BOUNDS: a device-side index check failed (debug build)";
     }
     return "unknown gma_status";
 }

@@ -12,7 +12,17 @@ namespace gma {
 // Device status word bits (first 4 bytes of the workspace header).
 enum : unsigned {
     kDevErrTimeout = 1u,     // a bounded mbarrier / flag wait ran out
+    kDevErrBounds = 2u,      // a debug-build index check failed (the access was skipped)
 };
+
+// Index checks of the debug build (compiled with -DGMA_DEBUG_BOUNDS): a failed check
+// posts kDevErrBounds to the status word and yields false, so that the caller skips
+// the access; it never traps.  In the normal build every check is `true`.
+#ifdef GMA_DEBUG_BOUNDS
+#define GMA_IN_BOUNDS(cond, status) ((cond) ? true : (atomicOr((status), ::gma::kDevErrBounds), false))
+#else
+#define GMA_IN_BOUNDS(cond, status) true
+#endif
 
 constexpr size_t kHeaderBytes = 256;
 constexpr int kTcChunkRows = 128;    // causal chunk of the tensor-core kernels (one MMA tile)

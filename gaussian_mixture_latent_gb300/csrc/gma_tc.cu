@@ -73,6 +73,7 @@ struct TcArgs {
     uint32_t mem_stride;
     float eps;
     unsigned *status;
+    int nslots;              // partial slots in the workspace (index checks of the debug build)
 };
 
 __device__ __forceinline__ void cta_range(int Ttot, int &t0, int &t1) {
@@ -221,6 +222,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                         }
                     }
                     if (can && (xi < SX || mbar_test(&xempty[xi % SX], ((xi / SX) - 1) & 1))) {
+                        (void)GMA_IN_BOUNDS(cx.g < A.G && cx.j < A.T, A.status);
                         mbar_arrive_expect_tx(&xfull[xi % SX], kTileBytes);
                         tma_load_3d(sm + C::OFF_X + (xi % SX) * kTileBytes, &tm_k, &xfull[xi % SX], 0, cx.j * TM, cx.g);
                         cx.next();
@@ -354,12 +356,13 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 ok = mbar_wait(&d2_full[hl % NW], (hl / NW) & 1, ab, kDevErrTimeout);
                 if (!wg_all(rt, ok)) break;
                 tc_fence_after();
-                float *dst = A.partials + ((size_t)(blockIdx.x + c.slot()) * (DVV + 1) + rt.r) * K;
+                const int slot = (int)blockIdx.x + c.slot();
+                float *dst = A.partials + ((size_t)slot * (DVV + 1) + rt.r) * K;
                 uint32_t v[K];
 #pragma unroll
                 for (int cc = 0; cc < K / 32; ++cc) tmem_ld32(tmem + rt.lane_off + C::COL_D2 + 32 * cc, v + 32 * cc);
                 tmem_ld_wait();
-                if (rt.r <= DVV) {
+                if (rt.r <= DVV && GMA_IN_BOUNDS(slot < A.nslots && c.g < A.G, A.status)) {
 #pragma unroll
                     for (int t = 0; t < K; t += 4)
                         *reinterpret_cast<float4 *>(dst + t) = make_float4(
@@ -393,7 +396,8 @@ constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) tc_reduce_kernel(int K, int T, int Ttot, int ncta,
                                                                    const float *__restrict__ partials,
-                                                                   uint8_t *__restrict__ mem, uint32_t mem_stride) {
+                                                                   uint8_t *__restrict__ mem, uint32_t mem_stride,
+                                                                   int nslots, unsigned *status) {
     grid_dep_launch();
     const int g = blockIdx.y;
     const int q = blockIdx.x * blockDim.x + threadIdx.x;   // float4 index in the 80 x K operand
@@ -415,6 +419,7 @@ __global__ void __launch_bounds__(kReduceThreads) tc_reduce_kernel(int K, int T,
     const int kq = K / 4;
     if (q >= 80 * kq) return;
     const int c_lo = crange[0], c_hi = crange[1];
+    if (!GMA_IN_BOUNDS(c_lo >= 0 && c_hi + g <= nslots, status)) return;
     const int nrow = q / kq, k = 4 * (q % kq);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (nrow <= DVV) {
@@ -535,6 +540,7 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         mbar_arrive_expect_tx(&w_full[b], param_bytes(K) + mem_bytes(K));
                         bulk_load(sm + C::OFF_P + b * C::PB, A.params + (size_t)(cx.g % A.H) * A.param_stride,
                                   param_bytes(K), &w_full[b]);
+                        (void)GMA_IN_BOUNDS(cx.g < A.G, A.status);
                         bulk_load(sm + C::OFF_M + b * C::MB, A.mem + (size_t)cx.g * A.mem_stride, mem_bytes(K),
                                   &w_full[b]);
                         p_loaded = cx.hl;
@@ -688,6 +694,7 @@ cudaError_t launch_write(const Problem &p, const TcLayout &L, const void *Kx, co
     a.params = reinterpret_cast<const uint8_t *>(ws + L.params); a.param_stride = L.param_stride;
     a.partials = reinterpret_cast<float *>(ws + L.part);
     a.status = reinterpret_cast<unsigned *>(ws);
+    a.nslots = kMaxCtas + p.G;
     auto kern = tc_write_kernel<K, false>;
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), WriteCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
@@ -766,6 +773,7 @@ cudaError_t tc_prefix(const Problem &p, const TcLayout &L, const SegTable &T, co
     a.params = reinterpret_cast<const uint8_t *>(ws + L.params); a.param_stride = L.param_stride;
     a.partials = reinterpret_cast<float *>(ws + L.part);
     a.status = reinterpret_cast<unsigned *>(ws);
+    a.nslots = T.np + T.nseg + 1;
     auto kern = tc_write_kernel<64, true>;
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), WriteCfg<64>::BYTES);
     if (e != cudaSuccess) return e;
@@ -776,7 +784,7 @@ cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_
     dim3 grid((20 * p.K + kReduceThreads - 1) / kReduceThreads, p.G);
     return launch_dependent(tc_reduce_kernel, grid, dim3(kReduceThreads), 0, s, p.K, L.Tkv, L.Ttot_kv, L.ncta_kv,
                             reinterpret_cast<const float *>(ws + L.part), reinterpret_cast<uint8_t *>(ws + L.mem),
-                            L.mem_stride);
+                            L.mem_stride, kMaxCtas + p.G, reinterpret_cast<unsigned *>(ws));
 }
 
 cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,

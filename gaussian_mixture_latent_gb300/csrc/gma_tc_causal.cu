@@ -73,6 +73,7 @@ struct CausalArgs {
     float var_floor;
     // segment-parallel form: the prefix pass's partial slots [slot][dv + 1][K] f32
     const float *partials;
+    int nslots;            // partial slots in the workspace (index checks of the debug build)
 };
 
 struct CausalCfg {
@@ -266,6 +267,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 if (ki < nch && (ki < 2 || mbar_test(&kempty[ki & 1], ((ki >> 1) - 1) & 1))) {
                     locate(ki, gh, cc);
+                    (void)GMA_IN_BOUNDS(gh < A.G && cc < hch, A.status);
                     mbar_arrive_expect_tx(&kfull[ki & 1], kTileBytes);
                     tma_load_3d(sm + C::OFF_K + (ki & 1) * kTileBytes, &tm_k, &kfull[ki & 1], 0, cc * TM, gh);
                     ++ki;
@@ -462,6 +464,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (rt.r <= DVV) {
                         for (int sg = s_first; sg <= s_last; ++sg)
                             for (int p = S.seg[sg].plo; p <= S.seg[sg].phi; ++p) {
+                                if (!GMA_IN_BOUNDS(p + sg < A.nslots && S.seg[sg].g == g, A.status)) continue;
                                 const float4 *src = reinterpret_cast<const float4 *>(
                                     A.partials + ((size_t)(p + sg) * (DVV + 1) + rt.r) * K);
 #pragma unroll
@@ -609,7 +612,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     wg_sync(rt);
                     if (elected) mbar_arrive(d3_empty);
                     const int row = c * TM + (int)rt.r;
-                    if (row < A.N) {
+                    if (row < A.N && GMA_IN_BOUNDS(ks < A.Kfull / KC && g < A.G && 64 * vs < A.dvt, A.status)) {
                         const size_t pr = ((size_t)ks * A.G + g) * A.N + row;
                         uint4 *dst = reinterpret_cast<uint4 *>(A.pnum + pr * A.dvt + 64 * vs);
 #pragma unroll
@@ -649,6 +652,7 @@ tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (elected) {
                     int gh, cc;
                     locate(c, gh, cc);
+                    (void)GMA_IN_BOUNDS(gh < A.G && cc < hch, A.status);
                     tma_store_3d(&tm_o, ob, 0, cc * TM, gh);
                     bulk_commit_group();
                 }
@@ -839,6 +843,7 @@ static cudaError_t launch_causal(const Problem &p, const TcLayout &L, const void
         a.mu = mu; a.rho = rho; a.alpha = alpha;
         a.var_floor = p.var_floor;
         a.partials = reinterpret_cast<const float *>(ws + L.part);
+        a.nslots = seg ? seg->np + seg->nseg + 1 : 0;
     }
     if (seg) {
         auto kern = tc_causal_kernel<false, true>;

@@ -52,7 +52,8 @@ typedef enum {
     GMA_ERR_UNSUPPORTED = 2,   /* valid request outside the implemented range     */
     GMA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required      */
     GMA_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed     */
-    GMA_ERR_TIMEOUT = 5        /* a device-side bounded wait ran out              */
+    GMA_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out              */
+    GMA_ERR_BOUNDS = 6         /* a device-side index check failed (debug build)  */
 } gma_status;
 
 typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype;
@@ -266,7 +267,11 @@ gma_status gma_forward_noalloc(const gma_desc *desc, const void *Qx, const void 
 
 /*
  * Synchronises `stream`, reads the device status word of `workspace`, clears
- * it, and returns GMA_OK or the device error that was posted (GMA_ERR_TIMEOUT).
+ * it, and returns GMA_OK or the device error that was posted: GMA_ERR_TIMEOUT,
+ * or GMA_ERR_BOUNDS from a library built with GMA_DEBUG_BOUNDS defined, whose
+ * kernels check their global-memory indices (partial slots, heads, rows,
+ * tiles) against the problem and skip, rather than perform, an access that
+ * fails (a timeout is reported first when both were posted).
  */
 gma_status gma_get_status(void *workspace, void *stream);
 
