@@ -282,7 +282,7 @@ gma_status gma_backward_workspace_size(const gma_desc *desc, int causal, size_t 
     const Problem p = make_problem(desc, causal, 0.f);
     if (!bwd_supported(p) || p.out_dtype != p.in_dtype) return GMA_ERR_UNSUPPORTED;
     if (p.causal && p.chunk != 0 && p.chunk != kBwdChunkRows) return GMA_ERR_UNSUPPORTED;
-    *bytes = bwd_layout(p).total;
+    *bytes = bwd_tc_supported(p) ? bwd_tc_layout(p).total : bwd_layout(p).total;
     return GMA_OK;
 }
 
@@ -301,8 +301,10 @@ gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const 
     const Problem p = make_problem(desc, causal, eps);
     if (!bwd_supported(p) || p.out_dtype != p.in_dtype) return GMA_ERR_UNSUPPORTED;
     if (p.causal && p.chunk != 0 && p.chunk != kBwdChunkRows) return GMA_ERR_UNSUPPORTED;
-    const BwdLayout L = bwd_layout(p);
-    if (!workspace || workspace_bytes < L.total) return GMA_ERR_WORKSPACE;
+    // bidirectional bf16: the tensor-core passes; fp32 inputs and the causal form: CUDA cores
+    const bool tc = bwd_tc_supported(p);
+    const size_t need = tc ? bwd_tc_layout(p).total : bwd_layout(p).total;
+    if (!workspace || workspace_bytes < need) return GMA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p.N == 0) {     // the loss does not depend on the parameters
         const size_t kd = sizeof(float) * (size_t)p.H * p.K * p.d;
@@ -311,10 +313,11 @@ gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const 
             return GMA_ERR_CUDA;
         return GMA_OK;
     }
-    return bwd_run(p, L, Qx, Kx, V, mu, rho, pi_logits, dO, dQx, dKx, dV, dmu, drho, dpi_logits,
-                   static_cast<char *>(workspace), s) == cudaSuccess
-               ? GMA_OK
-               : GMA_ERR_CUDA;
+    char *ws = static_cast<char *>(workspace);
+    const cudaError_t e =
+        tc ? bwd_tc_run(p, bwd_tc_layout(p), Qx, Kx, V, mu, rho, pi_logits, dO, dQx, dKx, dV, dmu, drho, dpi_logits, ws, s)
+           : bwd_run(p, bwd_layout(p), Qx, Kx, V, mu, rho, pi_logits, dO, dQx, dKx, dV, dmu, drho, dpi_logits, ws, s);
+    return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
 gma_status gma_decode_workspace_size(const gma_desc *desc, size_t *bytes) {

@@ -1054,6 +1054,12 @@ BwdLayout bwd_layout(const Problem &p) {
     return L;
 }
 
+cudaError_t bwd_finalize(const Problem &p, int C, const float *pq, const float *pk, const float *mu, const float *lam,
+                         const float *rho, const float *alpha, float *dmu, float *drho, float *dalpha, cudaStream_t s) {
+    bwd_param_kernel<<<dim3(kK, p.H), 2 * kD, 0, s>>>(p.B, p.H, C, pq, pk, mu, lam, rho, alpha, dmu, drho, dalpha);
+    return cudaGetLastError();
+}
+
 cudaError_t bwd_run(const Problem &p, const BwdLayout &L, const void *Qx, const void *Kx, const void *V,
                     const float *mu, const float *rho, const float *alpha, const void *dO, float *dQx, float *dKx,
                     float *dV, float *dmu, float *drho, float *dalpha, char *ws, cudaStream_t s) {

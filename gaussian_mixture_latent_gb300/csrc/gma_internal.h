@@ -75,6 +75,10 @@ cudaError_t tc_params(const Problem &p, const TcLayout &L, const float *mu, cons
 cudaError_t tc_write(const Problem &p, const TcLayout &L, const void *Kx, const void *V, char *ws,
                      cudaStream_t s);
 cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s);
+// the same over the partial slots at workspace offset `part` into the operand at `mem`,
+// and (mem_lo != 0) its bf16 rounding remainder at `mem_lo`
+cudaError_t tc_reduce_split(const Problem &p, const TcLayout &L, size_t part, size_t mem, size_t mem_lo, char *ws,
+                            cudaStream_t s);
 cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,
                     cudaStream_t s);
 
@@ -144,6 +148,27 @@ BwdLayout bwd_layout(const Problem &p);
 cudaError_t bwd_run(const Problem &p, const BwdLayout &L, const void *Qx, const void *Kx, const void *V,
                     const float *mu, const float *rho, const float *alpha, const void *dO, float *dQx, float *dKx,
                     float *dV, float *dmu, float *drho, float *dalpha, char *ws, cudaStream_t s);
+// dmu, drho, dalpha from the parameter sums pq, pk ([G][C][K][2d+1]: P1, P2, P0 over the
+// query and key rows of C row chunks) and the fp32 lambda [H][K][d]
+cudaError_t bwd_finalize(const Problem &p, int C, const float *pq, const float *pk, const float *mu, const float *lam,
+                         const float *rho, const float *alpha, float *dmu, float *drho, float *dalpha, cudaStream_t s);
+
+// ----- backward pass, bidirectional bf16, tensor cores: gma_bwd_tc.cu (uses the tc_* forward kernels) -----
+struct BwdTcLayout {
+    TcLayout tc;                  // the forward's parameter blocks, memory partials and operand [Vt | Z]
+    size_t lam, cdir;             // fp32 lambda [H][K][d] and the prologue's constants
+    size_t lamb;                  // [H] bf16 [lambda | lambda mu] operands
+    size_t mem_lo;                // the bf16 remainder of [Vt | Z] (hi + lo: the two-term operand)
+    size_t part_r, mem_r, mem_rlo;  // [R | r] partial slots, its bf16 operand and remainder
+    size_t part_pq, part_pk;      // parameter-sum partial slots of the query and key passes
+    size_t pq, pk;                // [G][K][2d+1] parameter sums per head
+    size_t total;
+};
+bool bwd_tc_supported(const Problem &p);
+BwdTcLayout bwd_tc_layout(const Problem &p);
+cudaError_t bwd_tc_run(const Problem &p, const BwdTcLayout &L, const void *Qx, const void *Kx, const void *V,
+                       const float *mu, const float *rho, const float *alpha, const void *dO, float *dQx, float *dKx,
+                       float *dV, float *dmu, float *drho, float *dalpha, char *ws, cudaStream_t s);
 
 // ----- self-test of the bounded-wait failure path: gma_selftest.cu -----
 cudaError_t selftest_timeout(void *ws, cudaStream_t s);

@@ -388,7 +388,10 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 // Fixed-order sum over the CTAs that covered head g (blockIdx.y), then the bf16
 // B operand [n][k] of the read (n = value column, dv -> Z, dv+1 -> 1, rest 0)
-// in the K-major 128-byte-swizzled layout, ceil(K/64) chunks of 80 rows.  Each
+// in the K-major 128-byte-swizzled layout, ceil(K/64) chunks of 80 rows.  With
+// mem_lo given, the rounding remainder (the fp32 sum minus its bf16 value, itself
+// rounded to bf16) goes to the same layout there, so that hi + lo carries the sum
+// to about 16 significant bits (the backward's two-term operands).  Each
 // thread owns four consecutive k of one row (a float4 of every partial), so a
 // head takes 20 K / 4 threads and the grid fits on the GPU in one wave while
 // the write kernel drains.
@@ -396,8 +399,8 @@ constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) tc_reduce_kernel(int K, int T, int Ttot, int ncta,
                                                                    const float *__restrict__ partials,
-                                                                   uint8_t *__restrict__ mem, uint32_t mem_stride,
-                                                                   int nslots, unsigned *status) {
+                                                                   uint8_t *__restrict__ mem, uint8_t *__restrict__ mem_lo,
+                                                                   uint32_t mem_stride, int nslots, unsigned *status) {
     grid_dep_launch();
     const int g = blockIdx.y;
     const int q = blockIdx.x * blockDim.x + threadIdx.x;   // float4 index in the 80 x K operand
@@ -443,8 +446,12 @@ __global__ void __launch_bounds__(kReduceThreads) tc_reduce_kernel(int K, int T,
         v = make_float4(1.f, 1.f, 1.f, 1.f);
     }
     const uint32_t off = (uint32_t)(k >> 6) * 80u * 128u + sw128_off(nrow, (k & 63) >> 3) + (k & 7) * 2;
-    *reinterpret_cast<uint2 *>(mem + (size_t)g * mem_stride + off) =
-        make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+    const uint2 hi = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+    *reinterpret_cast<uint2 *>(mem + (size_t)g * mem_stride + off) = hi;
+    if (mem_lo)
+        *reinterpret_cast<uint2 *>(mem_lo + (size_t)g * mem_stride + off) =
+            make_uint2(pack_bf16(v.x - bf16_lo(hi.x), v.y - bf16_hi(hi.x)),
+                       pack_bf16(v.z - bf16_lo(hi.y), v.w - bf16_hi(hi.y)));
 }
 
 // ------------------------------------------------------------------ tc_read
@@ -781,10 +788,16 @@ cudaError_t tc_prefix(const Problem &p, const TcLayout &L, const SegTable &T, co
 }
 
 cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s) {
+    return tc_reduce_split(p, L, L.part, L.mem, 0, ws, s);
+}
+
+cudaError_t tc_reduce_split(const Problem &p, const TcLayout &L, size_t part, size_t mem, size_t mem_lo, char *ws,
+                            cudaStream_t s) {
     dim3 grid((20 * p.K + kReduceThreads - 1) / kReduceThreads, p.G);
     return launch_dependent(tc_reduce_kernel, grid, dim3(kReduceThreads), 0, s, p.K, L.Tkv, L.Ttot_kv, L.ncta_kv,
-                            reinterpret_cast<const float *>(ws + L.part), reinterpret_cast<uint8_t *>(ws + L.mem),
-                            L.mem_stride, kMaxCtas + p.G, reinterpret_cast<unsigned *>(ws));
+                            reinterpret_cast<const float *>(ws + part), reinterpret_cast<uint8_t *>(ws + mem),
+                            mem_lo ? reinterpret_cast<uint8_t *>(ws + mem_lo) : nullptr, L.mem_stride, kMaxCtas + p.G,
+                            reinterpret_cast<unsigned *>(ws));
 }
 
 cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,

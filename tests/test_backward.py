@@ -14,6 +14,18 @@ responsibilities and every gradient inherit that relative error.  A routing grad
 can be far smaller than its head's others when its exact value cancels (one row: the
 key gradient is O(eps)), so the row gradients are measured against at least 1e-2 of
 the head's largest routing gradient.
+
+The bidirectional backward of bf16 inputs runs on the tensor cores with bf16 operands
+(the responsibilities, a | b, ds, x^2 and [lambda | lambda mu], each rounded to 8
+significant bits, relative error <= 2^-9 ~ 2e-3; the two memory operands as two bf16
+terms; fp32 accumulation).  A gradient passes through up to five such roundings in
+sequence, and the softmax Jacobian of peaked responsibilities amplifies them (a rounding
+emulation of these operands against the oracle gives up to ~1e-2 over several seeds),
+so it is held to the bf16 bound, 2e-2, that the pages fix for bf16 inputs with fp32
+accumulation.  fp32 inputs and the causal backward
+run on the CUDA cores in fp32 and keep the 1e-3 bound, and so do heads of one 128-row
+tile (the single-row head, whose exact routing gradient is O(eps) because O = v for any
+responsibilities, is among them: bf16 operands could not resolve that cancellation).
 """
 import numpy as np
 import pytest
@@ -25,6 +37,12 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 TOL_BWD = 1e-3
+TOL_BWD_TC = 2e-2        # bidirectional, bf16 inputs: tensor-core operands
+
+
+def tol_for(w):
+    # the tensor-core passes take bidirectional bf16 heads of more than one 128-row tile
+    return TOL_BWD_TC if (w.dtype == "bf16" and not w.causal and w.N > 128) else TOL_BWD
 NAMES = ("Qx", "Kx", "V", "mu", "omega", "alpha")
 
 
@@ -94,7 +112,7 @@ def check(w, x, got, heads=None, param_heads=None):
     print(w.name, w.dtype, {k: f"{v:.2e}" for k, v in worst.items()})
     for g in got:
         assert np.isfinite(g).all()
-    assert max(worst.values()) <= TOL_BWD, worst
+    assert max(worst.values()) <= tol_for(w), worst
     return worst
 
 
@@ -107,6 +125,9 @@ CASES = [
     (1, 4, 1000, "f32", False, 1e-6),
     (3, 2, 777, "bf16", False, 1e-6),
     (1, 2, 130, "bf16", False, 0.0),
+    (2, 3, 9000, "bf16", False, 1e-6),     # persistent CTAs cross head boundaries; ragged last tile
+    (1, 1, 1, "bf16", False, 1e-6),       # one tile: the fp32 CUDA-core passes
+    (1, 2, 129, "bf16", False, 1e-6),     # two tiles, the second of one row: the tensor-core passes
     (1, 1, 1, "f32", True, 1e-6),
     (2, 3, 63, "f32", True, 1e-6),
     (1, 2, 65, "bf16", True, 1e-6),
@@ -172,26 +193,30 @@ def test_backward_unsupported_and_empty():
     assert all(float(t.abs().max()) == 0.0 for t in g[3:])
 
 
-def test_backward_identities_of_the_gpu_gradients():
+@pytest.mark.parametrize("dtype,bound", [("f32", 1e-4), ("bf16", 2e-3)])
+def test_backward_identities_of_the_gpu_gradients(dtype, bound):
     # properties the exact gradients satisfy at any size, on the GPU's gradients of a
     # 6-head N = 3000 problem: a common shift of every routing vector and every mean leaves
     # each score unchanged, so sum_i dQx_i + sum_i dKx_i + sum_k dmu_k = 0 for every head
     # set and dimension; O is homogeneous of degree one in V (Eq. 7-8), so
-    # sum dV * V = sum dO * O (Euler); and sum_k dalpha_k = 0 (Eq. 15)
+    # sum dV * V = sum dO * O (Euler); and sum_k dalpha_k = 0 (Eq. 15).  fp32 inputs take
+    # the fp32 CUDA-core passes (bound 1e-4 of the sum of magnitudes); bf16 inputs the
+    # tensor-core passes, whose bf16 operand roundings (2^-9 each, independent from term to
+    # term) leave the sums at a small multiple of 2^-9 of the sum of magnitudes: bound 2e-3
     import oracle
-    w, x = make(2, 3, 3000, "bf16", seed=12)
+    w, x = make(2, 3, 3000, dtype, seed=12)
     dQ, dK, dV, dmu, drho, dal = run_gpu(w, x)
     shift = dQ.sum(axis=(0, 2)) + dK.sum(axis=(0, 2)) + dmu.sum(axis=1)           # [H, d]
     scale = np.abs(dQ).sum(axis=(0, 2)) + np.abs(dK).sum(axis=(0, 2)) + np.abs(dmu).sum(axis=1)
-    assert (np.abs(shift) <= 1e-4 * scale).all(), np.abs(shift / scale).max()
+    assert (np.abs(shift) <= bound * scale).all(), np.abs(shift / scale).max()
     O = oracle.forward(*(inputs.widen(x[n], w.dtype) for n in ("Qx", "Kx", "V")), x["mu"], x["rho"], x["alpha"],
                        w.var_floor, w.eps, False, threads=4)
     V, dO = inputs.widen(x["V"], w.dtype), inputs.widen(x["dO"], w.dtype)
     for b in range(w.B):
         for h in range(w.H):
             lhs, rhs = float((dV[b, h] * V[b, h]).sum()), float((dO[b, h] * O[b, h]).sum())
-            assert abs(lhs - rhs) <= 1e-4 * np.abs(dO[b, h] * O[b, h]).sum(), (b, h, lhs, rhs)
-    assert (np.abs(dal.sum(axis=1)) <= 1e-4 * np.abs(dal).sum(axis=1)).all()
+            assert abs(lhs - rhs) <= bound * np.abs(dO[b, h] * O[b, h]).sum(), (b, h, lhs, rhs)
+    assert (np.abs(dal.sum(axis=1)) <= bound * np.abs(dal).sum(axis=1)).all()
 
 
 def test_causal_backward_full_size_sampled():
