@@ -931,6 +931,29 @@ def bwd_flops_per_row(w):
     return mem + qry + key + 2 * rows
 
 
+def bwd_tc_path(w):
+    """Whether gma_backward takes the tensor-core passes for this workload (bidirectional,
+    bf16, d = dv = K = 64, more than one 128-row tile per head)."""
+    return (not w.causal and w.dtype == "bf16" and w.d == 64 and w.dv == 64 and w.K == 64 and w.N > 128)
+
+
+def bwd_bytes_per_row(w):
+    """Bytes one row of one head must move at the least: the bf16 inputs Qx, Kx, V and dO read
+    once, the fp32 gradients dQx, dKx, dV written once."""
+    return 2 * (2 * w.d + 2 * w.dv) + 4 * (2 * w.d + w.dv)
+
+
+def bwd_tc_flops_per_row(w):
+    """Tensor-core flops of the tensor-core passes per row of one head (2 per multiply-add):
+    the write pass (log-density and [V | 1]^T Gamma), and per query and key row the
+    log-density, the two-term memory products, [a | b]^T Gamma (queries), dx and [x | x^2]^T ds."""
+    ld = 2 * (2 * w.d + 16) * w.K                     # [x, x^2/256] . W plus the constant k-step
+    write = ld + 2 * 128 * w.K
+    qry = ld + 2 * 2 * w.K * 80 + 2 * 2 * 80 * w.K + 2 * 128 * w.K + 2 * w.K * 2 * w.d + 2 * 128 * w.K
+    key = ld + 2 * 2 * 80 * w.K + 2 * 2 * w.K * w.dv + 2 * w.K * 2 * w.d + 2 * 128 * w.K
+    return write + qry + key
+
+
 def bwd_oracle_sample(w, seconds):
     """The oracle's backward of whole heads of the workload (one thread), repeated for about
     ``seconds``."""
@@ -1016,9 +1039,29 @@ def run_backward(args, rank, world, local):
         raise RuntimeError("device status after the timed region")
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     units = w.B * w.H * w.N
-    flops = units * bwd_flops_per_row(w)
-    alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12            # fp32 lanes x 2 flops x max SM clock, TFLOP/s
-    achieved = flops / (ms / 1e3) / 1e12
+    tc = bwd_tc_path(w)
+    launches = 9
+    if tc:
+        # tensor-core passes: bound by the bytes the call must move (HBM); the tensor-pipe
+        # fraction beside it
+        pk = peaks()
+        achieved = units * bwd_bytes_per_row(w) / (ms / 1e3) / 1e9
+        tflops = units * bwd_tc_flops_per_row(w) / (ms / 1e3) / 1e12
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                "kernel": f"gma_backward (whole call: {launches} launches)", "kernel_ms": ms,
+                "bytes_per_row": bwd_bytes_per_row(w), "peak_source": pk["source"],
+                "tensor": {"achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                           "frac": tflops / pk["bf16_tflops"], "flops_per_row": bwd_tc_flops_per_row(w)}}
+    else:
+        flops = units * bwd_flops_per_row(w)
+        alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12        # fp32 lanes x 2 flops x max SM clock, TFLOP/s
+        achieved = flops / (ms / 1e3) / 1e12
+        launches = 9 if w.causal else 7
+        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": achieved / alu_peak, "traffic": None,
+                "kernel": f"gma_backward (whole call: {launches} launches)", "kernel_ms": ms,
+                "flops_per_row": bwd_flops_per_row(w), "peak_source": "fp32 lanes x 2 x 2070 MHz"}
     cpu = None
     if not args.no_cpu_baseline:
         rate, reps, dt = bwd_oracle_sample(w, 12.0)
@@ -1026,18 +1069,15 @@ def run_backward(args, rank, world, local):
                "sample": f"one head of {w.name} (N = {w.N}), {reps} passes"}
     print(json.dumps({"metric": metric, "value": units / (ms / 1e3), "unit": "tokens·heads/s", "n_gpus": 1,
                       "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
-                      "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if tc else "f32",
+                      "data": "synthetic",
                       "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K, "dv": w.dv,
                                  "inputs": w.dtype,
                                  "step": f"{'causal' if w.causal else 'bidirectional'} backward, all gradients",
+                                 "path": "tensor-core passes" if tc else "CUDA-core passes (fp32)",
                                  "l2": "two alternating input sets (> 129 MB L2)", "parallelism": "single GPU"},
-                      "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                                   "frac": achieved / alu_peak, "traffic": None,
-                                   "kernel": f"gma_backward (whole call: {9 if w.causal else 7} launches)",
-                                   "kernel_ms": ms,
-                                   "flops_per_row": bwd_flops_per_row(w),
-                                   "peak_source": "fp32 lanes x 2 x 2070 MHz"},
-                      "clocks": clocks, "gpu_launches": (9 if w.causal else 7) * steps, "cpu_baseline": cpu}),
+                      "roofline": roof,
+                      "clocks": clocks, "gpu_launches": launches * steps, "cpu_baseline": cpu}),
           flush=True)
     return 0
 

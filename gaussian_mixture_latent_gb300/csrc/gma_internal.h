@@ -156,12 +156,12 @@ cudaError_t bwd_finalize(const Problem &p, int C, const float *pq, const float *
 // ----- backward pass, bidirectional bf16, tensor cores: gma_bwd_tc.cu (uses the tc_* forward kernels) -----
 struct BwdTcLayout {
     TcLayout tc;                  // the forward's parameter blocks, memory partials and operand [Vt | Z]
-    size_t lam, cdir;             // fp32 lambda [H][K][d] and the prologue's constants
+    size_t lam;                   // fp32 lambda [H][K][d]
     size_t lamb;                  // [H] bf16 [lambda | lambda mu] operands
     size_t mem_lo;                // the bf16 remainder of [Vt | Z] (hi + lo: the two-term operand)
     size_t part_r, mem_r, mem_rlo;  // [R | r] partial slots, its bf16 operand and remainder
     size_t part_pq, part_pk;      // parameter-sum partial slots of the query and key passes
-    size_t pq, pk;                // [G][K][2d+1] parameter sums per head
+    size_t psum;                  // [2][H][K][2d+1] parameter sums per head set, query rows then key rows
     size_t total;
 };
 bool bwd_tc_supported(const Problem &p);

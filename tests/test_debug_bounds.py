@@ -1,9 +1,9 @@
-"""The index-checking debug build (GMA_DEBUG_BOUNDS): every forward path runs with
-its global-memory indices checked on the device, on outputs and workspaces padded
-with canary bytes.  A failed check posts GMA_ERR_BOUNDS to the status word
-(instead of trapping), so the test asserts a clean status, untouched canaries on
-both sides of every output and after every workspace, and results that still
-match the fp64 oracle.  The debug library is loaded in a child process (the
+"""The index-checking debug build (GMA_DEBUG_BOUNDS): every forward path and the
+tensor-core backward run with their global-memory indices checked on the device, on
+outputs and workspaces padded with canary bytes.  A failed check posts GMA_ERR_BOUNDS
+to the status word (instead of trapping), so the test asserts a clean status,
+untouched canaries on both sides of every output and after every workspace, and
+results that still match the fp64 oracle.  The debug library is loaded in a child process (the
 GMA_LIBRARY override), so this process keeps the normal build."""
 import os
 import subprocess
@@ -75,6 +75,42 @@ for name, kw in cases:
     gma.gma_forward(*(to_device(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha")), eps=w.eps,
                     causal=w.causal, var_floor=w.var_floor, out=out, workspace=ws)
     check(name, w, x, out_flat, out, ws, need, [0, w.G - 1])
+
+# the tensor-core backward (bidirectional bf16; 252 tiles over the persistent CTAs, so CTAs
+# and both compute groups cross head boundaries): canary-padded gradients and workspace
+import ctypes
+w = inputs.Workload("bwd_tc", seed=7, B=1, H=4, N=8000, d=64, K=64, dv=64, dtype="bf16", causal=False)
+x = inputs.gen_all(w)
+x["dO"] = x["V"][:, ::-1].copy()
+desc = gma._make_desc(w.B, w.H, w.N, w.d, w.K, w.dv, torch.bfloat16, torch.bfloat16, w.var_floor, 0)
+nb = ctypes.c_size_t(0)
+assert gma._load().gma_backward_workspace_size(ctypes.byref(desc), 0, ctypes.byref(nb)) == 0
+need = nb.value
+ws = workspace(need)
+shapes = ((w.B, w.H, w.N, w.d), (w.B, w.H, w.N, w.d), (w.B, w.H, w.N, w.dv), (w.H, w.K, w.d), (w.H, w.K, w.d),
+          (w.H, w.K))
+pads = [padded(shp, torch.float32) for shp in shapes]
+grads = gma.gma_backward(*(to_device(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha", "dO")), eps=w.eps,
+                         var_floor=w.var_floor, grads=tuple(t for _, t in pads), workspace=ws)
+torch.cuda.synchronize()
+st = gma.gma_get_status(ws)
+assert st == 0, ("bwd_tc", gma.gma_status_string(st))
+assert all(canaries_ok(f, torch.float32) for f, _ in pads), ("bwd_tc", "gradient canaries")
+assert bool((ws[need:] == CANARY_BYTE).all()), ("bwd_tc", "workspace canaries")
+wid = lambda a: inputs.widen(a, "bf16")
+worst = 0.0
+for h in (0, 3):
+    ref = oracle.backward_head(wid(x["Qx"][0, h]), wid(x["Kx"][0, h]), wid(x["V"][0, h]), x["mu"][h], x["rho"][h],
+                               x["alpha"][h], w.var_floor, w.eps, False, wid(x["dO"][0, h]))
+    got = [t.double().cpu().numpy() for t in grads]
+    floor = 1e-2 * max(np.abs(ref["Qx"]).max(), np.abs(ref["Kx"]).max())
+    for i, nm in enumerate(("Qx", "Kx", "V")):
+        den = max(np.abs(ref[nm]).max(), floor if nm != "V" else 0.0)
+        worst = max(worst, float(np.abs(got[i][0, h] - ref[nm]).max() / den))
+    for i, nm in ((3, "mu"), (4, "omega"), (5, "alpha")):
+        worst = max(worst, float(np.abs(got[i][h] - ref[nm]).max() / np.abs(ref[nm]).max()))
+assert worst <= TOL["bf16"], ("bwd_tc", worst)
+print(f"bwd_tc: status clean, canaries intact, max relative error {worst:.2e}")
 print("ALL_OK")
 '''
 
