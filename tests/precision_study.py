@@ -9,7 +9,8 @@ max |x - x_ref| / max |x_ref|, the worst over the sampled heads.
 Forward: the log-density operands ([x, x^2/256] and W) are varied; Gamma, V and the memory
 [Vt | Z] are bf16 operands in every variant and the output is rounded to bf16, as in the
 tensor-core kernels.  Backward: the score operands, the memory and read products (Gamma, V,
-[Vt | Z]) and the gradient products (a, b, ds, R, lambda) are varied separately.
+[Vt | Z]) and the gradient products (a, b, ds, R, lambda) are varied separately; then the
+tensor-core backward as built, with its memory operands in one or two bf16 terms.
 """
 import os
 import sys
@@ -87,6 +88,33 @@ def backward(Q, K, V, mu, om, al, vf, eps, dO, mbits, sbits, gbits):
             "omega": dvar / (1 + np.exp(-om)), "alpha": P0 - np.exp(logpi) * P0.sum()}
 
 
+def backward_tc(Q, K, V, mu, om, al, vf, eps, dO, two_term):
+    """The tensor-core backward as built: normalised Gamma, a | b, ds, x^2 and [lambda | lambda mu]
+    rounded to bf16; the memories [Vt | Z] and [R | r] as one bf16 term or (two_term) as
+    hi + lo; den = Gamma Z + eps sum Gamma; exact scores (the log-density error is the
+    forward's)."""
+    mu, om, lam, logpi, c = params(mu, om, al, vf)
+    b16 = lambda t: rnd(t, BF16)
+    mem = (lambda t: b16(t) + b16(t - b16(t))) if two_term else b16
+    gq, gk = b16(gamma(Q, lam, mu, c, None)), b16(gamma(K, lam, mu, c, None))
+    Vt, Z = mem(gk.T @ V), mem(gk.sum(0))
+    num = gq @ Vt
+    den = gq @ Z + eps * gq.sum(1)
+    a, b = b16(dO / den[:, None]), b16(-(dO * num).sum(1) / den ** 2)
+    g_q = a @ Vt.T + b[:, None] * Z[None]
+    ds_q = b16(gq * (g_q - (gq * g_q).sum(1, keepdims=True)))
+    R, r = mem(gq.T @ a), mem(gq.T @ b)
+    g_k = V @ R.T + r[None]
+    ds_k = b16(gk * (g_k - (gk * g_k).sum(1, keepdims=True)))
+    dx = lambda ds, X: ds @ b16(lam * mu) - X * (ds @ b16(lam))
+    P1 = ds_q.T @ Q + ds_k.T @ K
+    P2 = ds_q.T @ b16(Q * Q) + ds_k.T @ b16(K * K)
+    P0 = ds_q.sum(0) + ds_k.sum(0)
+    dvar = 0.5 * (lam ** 2 * (P2 - 2 * mu * P1 + mu ** 2 * P0[:, None]) - lam * P0[:, None])
+    return {"Qx": dx(ds_q, Q), "Kx": dx(ds_k, K), "V": gk @ R, "mu": lam * (P1 - mu * P0[:, None]),
+            "omega": dvar / (1 + np.exp(-om)), "alpha": P0 - np.exp(logpi) * P0.sum()}
+
+
 def err(a, b):
     return float(np.abs(a - b).max() / np.abs(b).max())
 
@@ -132,6 +160,38 @@ def backward_study():
         print(f"  {vname:45s} {worst:.1e}")
 
 
+def backward_kernel_study():
+    """The tensor-core backward's operand precisions on small heads (peaked responsibilities,
+    where the softmax Jacobian cancels most), with the parity test's metric: row gradients
+    against at least 1e-2 of the head's largest routing gradient, parameter gradients summed
+    over the batch."""
+    cases = [(3, 2, 777, 777), (2, 2, 200, 200), (2, 2, 200, 11), (1, 4, 300, 5), (2, 2, 1000, 7), (1, 3, 130, 3)]
+    worst = {False: 0.0, True: 0.0}
+    for B, H, N, seed in cases:
+        w = inputs.Workload("bwd", B=B, H=H, N=N, d=64, K=64, dv=64, dtype="bf16", causal=False, seed=seed)
+        x = inputs.gen_all(w)
+        z = inputs.normal(inputs.stream_key(seed, "dO"), 0, B * H * N * 64).reshape(B, H, N, 64)
+        dO = inputs.bf16_bits_to_f64(inputs.f32_to_bf16_bits(z.astype(np.float32)))
+        for h in range(H):
+            refs = [oracle.backward_head(*(inputs.widen(x[n][b, h], "bf16") for n in ("Qx", "Kx", "V")), x["mu"][h],
+                                         x["rho"][h], x["alpha"][h], w.var_floor, w.eps, False, dO[b, h])
+                    for b in range(B)]
+            for two in (False, True):
+                gots = [backward_tc(*(inputs.widen(x[n][b, h], "bf16") for n in ("Qx", "Kx", "V")), x["mu"][h],
+                                    x["rho"][h], x["alpha"][h], w.var_floor, w.eps, dO[b, h], two) for b in range(B)]
+                for b in range(B):
+                    floor = 1e-2 * max(np.abs(refs[b]["Qx"]).max(), np.abs(refs[b]["Kx"]).max())
+                    for n in ("Qx", "Kx", "V"):
+                        den = max(np.abs(refs[b][n]).max(), floor if n != "V" else 0.0)
+                        worst[two] = max(worst[two], float(np.abs(gots[b][n] - refs[b][n]).max() / den))
+                for n in ("mu", "omega", "alpha"):
+                    worst[two] = max(worst[two], err(sum(g[n] for g in gots), sum(r[n] for r in refs)))
+    print("backward as built on the tensor cores, six small workloads (worst over gradients and heads)")
+    print(f"  memories [Vt | Z], [R | r] as one bf16 term       {worst[False]:.1e}")
+    print(f"  memories as two bf16 terms (the kernel)           {worst[True]:.1e}")
+
+
 if __name__ == "__main__":
     forward_study()
     backward_study()
+    backward_kernel_study()
