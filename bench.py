@@ -50,12 +50,14 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--direction", choices=["both", "bidir", "causal", "diagnostics", "cross", "decode", "backward",
-                                            "backward_causal"],
+                                            "backward_causal", "project"],
                     default="both",
                     help="which forward(s) one step runs (default: both, the headline step); "
                          "diagnostics: one step is gma_diagnostics over the workload's query vectors; "
                          "cross: one step is gma_forward_cross, the workload's queries reading a context; "
-                         "decode: one step is gma_decode of one new token for every head")
+                         "decode: one step is gma_decode of one new token for every head; "
+                         "project: one step is gma_project, the Q/K/V projections of the workload's rows "
+                         "from a model width of H d")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's sequence length N (a reduced case for profiling)")
     ap.add_argument("--batch", type=int, default=0,
@@ -1082,6 +1084,105 @@ def run_backward(args, rank, world, local):
     return 0
 
 
+PROJ_METRIC = "GMA Q/K/V projection token·heads/s (Eq. 4, bf16, model width H d)"
+
+
+def run_project(args, rank, world, local):
+    """Input projections (Eq. 4): one step is one gma_project call producing Qx, Kx and V of
+    every head of the workload from X [B, N, D], D = H d (the model width of a layer whose
+    heads split it evenly: a reading, the configurations give no D)."""
+    import torch
+    import gaussian_mixture_latent_gb300 as gma
+    from gaussian_mixture_latent_gb300 import _build
+    w = workload(args)
+    D = w.H * w.d
+    flops_per_row = 2 * D * w.H * (2 * w.d + w.dv)            # one token, every head
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import oracle
+        oracle.build()
+        rows = 64
+        x = inputs.normal(inputs.stream_key(0, "X"), 0, rows * D).reshape(1, rows, D)
+        ws = [inputs.normal(inputs.stream_key(0, n), 0, w.H * D * c).reshape(w.H, D, c) / D ** 0.5
+              for n, c in (("Wq", w.d), ("Wk", w.d), ("Wv", w.dv))]
+        reps, t0 = 0, time.perf_counter()
+        while reps == 0 or time.perf_counter() - t0 < 10.0:
+            oracle.project(x, *ws)
+            reps += 1
+        dt = (time.perf_counter() - t0) / reps
+        rate = rows * w.H / dt
+        print(json.dumps({"impl": "reference", "metric": PROJ_METRIC, "value": rate, "unit": "tokens·heads/s",
+                          "n_gpus": args.gpus, "steps": reps, "warmup": 0, "ms_per_step": dt * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": {"workload": w.name, "D": D, "step": "projection (sampled)"},
+                          "cpu_baseline": {"value": rate, "unit": "tokens·heads/s", "cores": 1, "kind": "oracle",
+                                           "sample": f"{rows} rows of X, {reps} passes"},
+                          "e2e": {"value": rate, "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+
+    def gen(seed, name, shape, std):
+        z = inputs.normal(inputs.stream_key(seed, name), 0, int(np.prod(shape))).reshape(shape) * std
+        return torch.from_numpy(inputs.f32_to_bf16_bits(z.astype(np.float32)).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    sets = [(gen(seed, "X", (w.B, w.N, D), 1.0), gen(seed, "Wq", (w.H, D, w.d), D ** -0.5),
+             gen(seed, "Wk", (w.H, D, w.d), D ** -0.5), gen(seed, "Wv", (w.H, D, w.dv), D ** -0.5))
+            for seed in (0, 1)]
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    outs = (torch.empty((w.B, w.H, w.N, w.d), **bf), torch.empty((w.B, w.H, w.N, w.d), **bf),
+            torch.empty((w.B, w.H, w.N, w.dv), **bf))
+    stream = torch.cuda.current_stream()
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+
+    def step(x):
+        gma.gma_project(*x, out=outs, workspace=ws)
+
+    warm = max(3, args.warmup)
+    for it in range(warm):
+        step(sets[it % 2])
+    torch.cuda.synchronize()
+    if gma.gma_get_status(ws):
+        raise RuntimeError("device status after warm-up")
+    steps = args.steps if args.steps is not None else 20
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(gpu_id_for(local))
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for it in range(steps):
+        evs[it][0].record(stream)
+        step(sets[it % 2])
+        evs[it][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if gma.gma_get_status(ws):
+        raise RuntimeError("device status after the timed region")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    rows = w.B * w.N
+    pk = peaks()
+    tflops = rows * flops_per_row / (ms / 1e3) / 1e12
+    hbm = rows * 2 * (D + w.H * (2 * w.d + w.dv)) / (ms / 1e3) / 1e9      # X read once, outputs written once
+    print(json.dumps({"metric": PROJ_METRIC, "value": rows * w.H / (ms / 1e3), "unit": "tokens·heads/s",
+                      "n_gpus": 1, "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": w.name, "B": w.B, "N": w.N, "D": D, "H": w.H, "d": w.d, "dv": w.dv,
+                                 "step": "gma_project (one launch)",
+                                 "l2": "two alternating input sets (> 129 MB L2)", "parallelism": "single GPU"},
+                      "roofline": {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"],
+                                   "unit": "TFLOP/s", "frac": tflops / pk["bf16_tflops"], "traffic": None,
+                                   "kernel": "proj_kernel", "kernel_ms": ms, "flops_per_row": flops_per_row,
+                                   "peak_source": pk["source"],
+                                   "hbm": {"achieved": hbm, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                           "frac": hbm / pk["hbm_gbs"]}},
+                      "clocks": clocks, "gpu_launches": steps, "cpu_baseline": None}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -1093,6 +1194,8 @@ def main():
         return run_cross(args, rank, world, local)
     if args.direction in ("backward", "backward_causal"):
         return run_backward(args, rank, world, local)
+    if args.direction == "project":
+        return run_project(args, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_gpu(args, rank, world, local)

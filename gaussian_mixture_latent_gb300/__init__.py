@@ -20,7 +20,8 @@ import torch
 __all__ = [
     "GmaError", "gma_desc", "gma_workspace_size", "gma_workspace_init", "gma_forward",
     "gma_forward_ex", "gma_forward_plan",
-    "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_decode", "gma_backward", "gma_selftest_timeout", "gma_get_status", "gma_status_string", "gma_version",
+    "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_decode", "gma_backward",
+    "gma_proj_desc", "gma_project", "gma_selftest_timeout", "gma_get_status", "gma_status_string", "gma_version",
     "Workspace", "library_path",
 ]
 
@@ -48,6 +49,12 @@ class gma_desc(ctypes.Structure):
                 ("d", ctypes.c_int), ("K", ctypes.c_int), ("dv", ctypes.c_int),
                 ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
                 ("var_floor", ctypes.c_float), ("chunk", ctypes.c_int)]
+
+
+class gma_proj_desc(ctypes.Structure):
+    """Mirror of ``gma_proj_desc`` in include/gma.h."""
+    _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("D", ctypes.c_int), ("H", ctypes.c_int),
+                ("d", ctypes.c_int), ("dv", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -81,6 +88,7 @@ def _load():
     lib.gma_backward_workspace_size.argtypes = [dp, i, ctypes.POINTER(sz)]
     lib.gma_selftest_timeout.argtypes = [vp, sz, vp]
     lib.gma_backward.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.gma_project.argtypes = [ctypes.POINTER(gma_proj_desc), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gma_get_status.argtypes = [vp, vp]
     lib.gma_status_string.argtypes = [i]
     lib.gma_status_string.restype = ctypes.c_char_p
@@ -89,7 +97,7 @@ def _load():
                lib.gma_forward_ex, lib.gma_forward_plan, lib.gma_responsibilities, lib.gma_get_status, lib.gma_version,
                lib.gma_diagnostics_workspace_size, lib.gma_diagnostics, lib.gma_cross_workspace_size,
                lib.gma_forward_cross, lib.gma_decode_workspace_size, lib.gma_decode,
-               lib.gma_backward_workspace_size, lib.gma_backward, lib.gma_selftest_timeout):
+               lib.gma_backward_workspace_size, lib.gma_backward, lib.gma_selftest_timeout, lib.gma_project):
         fn.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -336,6 +344,36 @@ def gma_backward(Qx, Kx, V, mu, rho, pi_logits, dO, eps: float = 1e-6, var_floor
     if check_status:
         _check_device_status(ws, stream, "gma_backward")
     return grads
+
+
+def gma_project(X, Wq, Wk, Wv, out=None, workspace=None, stream=None, check_status: bool = False):
+    """Input projections (section 3.1, Eq. 4): X [B, N, D], Wq and Wk [H, D, d], Wv [H, D, dv],
+    all bfloat16 -> (Qx, Kx [B, H, N, d], V [B, H, N, dv]) bfloat16, Qx[b, h] = X[b] Wq[h] with
+    fp32 accumulation (one tensor-core GEMM).  `out`, if given, is that tuple of preallocated
+    outputs (overwritten)."""
+    B, N, D = X.shape
+    H, _, d = Wq.shape
+    dv = Wv.shape[2]
+    bf = (torch.bfloat16,)
+    _check(X, "X", (B, N, D), bf)
+    _check(Wq, "Wq", (H, D, d), bf)
+    _check(Wk, "Wk", (H, D, d), bf)
+    _check(Wv, "Wv", (H, D, dv), bf)
+    if out is None:
+        out = (torch.empty((B, H, N, d), dtype=torch.bfloat16, device=X.device),
+               torch.empty((B, H, N, d), dtype=torch.bfloat16, device=X.device),
+               torch.empty((B, H, N, dv), dtype=torch.bfloat16, device=X.device))
+    for t, shp, name in zip(out, ((B, H, N, d), (B, H, N, d), (B, H, N, dv)), ("Qx", "Kx", "V")):
+        _check(t, name, shp, bf)
+    desc = gma_proj_desc(B, N, D, H, d, dv)
+    ws = _workspace_for(X.device, 256, workspace, stream)
+    rc = _load().gma_project(ctypes.byref(desc), _ptr(X), _ptr(Wq), _ptr(Wk), _ptr(Wv), *(_ptr(t) for t in out),
+                             _ptr(ws), ws.numel(), _stream_ptr(stream))
+    if rc:
+        raise GmaError(rc, "gma_project")
+    if check_status:
+        _check_device_status(ws, stream, "gma_project")
+    return out
 
 
 def gma_decode(Qx, Kx, V, mu, rho, pi_logits, state, eps: float = 1e-6, var_floor: float = 1e-4, out=None,

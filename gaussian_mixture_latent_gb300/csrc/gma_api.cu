@@ -320,6 +320,27 @@ gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const 
     return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
+gma_status gma_project(const gma_proj_desc *desc, const void *X, const void *Wq, const void *Wk, const void *Wv,
+                       void *Qx, void *Kx, void *V, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!desc) return GMA_ERR_INVALID_ARG;
+    const gma_proj_desc &d = *desc;
+    if (d.B < 0 || d.N < 0 || d.D <= 0 || d.H <= 0 || d.d <= 0 || d.dv <= 0) return GMA_ERR_INVALID_ARG;
+    if ((long long)d.B * d.H > (1LL << 30) || (long long)d.N > (1LL << 30)) return GMA_ERR_INVALID_ARG;
+    if (!proj_supported(d.B > 0 ? d.B : 1, d.N > 0 ? d.N : 1, d.D, d.H, d.d, d.dv)) return GMA_ERR_UNSUPPORTED;
+    if (!Wq || !Wk || !Wv) return GMA_ERR_INVALID_ARG;
+    const bool empty = d.B == 0 || d.N == 0;
+    if (!empty && (!X || !Qx || !Kx || !V)) return GMA_ERR_INVALID_ARG;
+    const void *ptrs[] = {X, Wq, Wk, Wv, Qx, Kx, V, workspace};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kHeaderBytes) return GMA_ERR_WORKSPACE;
+    if (empty) return GMA_OK;
+    return proj_run(d.B, d.N, d.D, d.H, d.d, d.dv, X, Wq, Wk, Wv, Qx, Kx, V, static_cast<char *>(workspace),
+                    static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GMA_OK
+               : GMA_ERR_CUDA;
+}
+
 gma_status gma_decode_workspace_size(const gma_desc *desc, size_t *bytes) {
     gma_status st = validate_desc(desc);
     if (st != GMA_OK) return st;

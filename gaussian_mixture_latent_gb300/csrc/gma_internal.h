@@ -170,6 +170,11 @@ cudaError_t bwd_tc_run(const Problem &p, const BwdTcLayout &L, const void *Qx, c
                        const float *mu, const float *rho, const float *alpha, const void *dO, float *dQx, float *dKx,
                        float *dV, float *dmu, float *drho, float *dalpha, char *ws, cudaStream_t s);
 
+// ----- Q/K/V input projections (Eq. 4): gma_proj.cu (one tcgen05 GEMM, bf16) -----
+bool proj_supported(int B, int N, int D, int H, int d, int dv);
+cudaError_t proj_run(int B, int N, int D, int H, int d, int dv, const void *X, const void *Wq, const void *Wk,
+                     const void *Wv, void *Qx, void *Kx, void *V, char *ws, cudaStream_t s);
+
 // ----- self-test of the bounded-wait failure path: gma_selftest.cu -----
 cudaError_t selftest_timeout(void *ws, cudaStream_t s);
 

@@ -47,6 +47,7 @@ STREAM = {
     "Qx_mix_sel": 7, "Qx_mix_comp": 8, "Qx_mix_noise": 9,
     "Kx_mix_sel": 10, "Kx_mix_comp": 11, "Kx_mix_noise": 12,
     "dO": 13,                    # upstream gradient of the backward pass
+    "X": 14, "Wq": 15, "Wk": 16, "Wv": 17,   # layer input and projection weights (Eq. 4)
 }
 
 

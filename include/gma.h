@@ -237,6 +237,27 @@ gma_status gma_diagnostics(const gma_desc *desc, const void *Qx, const float *mu
                            const float *pi_logits, float *p_out, float *stats_out, int *z_out,
                            void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Input projections ("Gaussian Mixture Attention", section 3.1, Eq. 4): the routing
+ * vectors and values of every head from the layer input,
+ *   Qx[b, h] = X[b] W_Q[h],   Kx[b, h] = X[b] W_K[h],   V[b, h] = X[b] W_V[h],
+ * bf16 operands with fp32 accumulation, results rounded to bf16.  Layouts (row-major,
+ * contiguous, 16-byte aligned, every tensor bf16):
+ *   X           [B, N, D]
+ *   Wq, Wk      [H, D, d]        Wv  [H, D, dv]
+ *   Qx, Kx      [B, H, N, d]     V   [B, H, N, dv]   (the layouts gma_forward() reads)
+ * Implemented for D, d and dv multiples of 64 (GMA_ERR_UNSUPPORTED otherwise); B, N, H
+ * any positive size.  N = 0 launches nothing.  The workspace holds only the status
+ * word: at least 256 bytes, initialised to zero (gma_workspace_init()).  One kernel
+ * launch (a persistent tcgen05 GEMM).
+ */
+typedef struct {
+    int B, N, D, H, d, dv;
+} gma_proj_desc;
+
+gma_status gma_project(const gma_proj_desc *desc, const void *X, const void *Wq, const void *Wk, const void *Wv,
+                       void *Qx, void *Kx, void *V, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Size of the fixed scratch buffer gma_forward_noalloc() uses: 32 MiB. */
 #define GMA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 

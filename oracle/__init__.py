@@ -6,8 +6,8 @@ benchmark's CPU-baseline leg may import this package; the product path
 
 The arithmetic lives in ``gma_oracle.c`` (double precision, written from the
 equations of "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
-Probabilistic Latent Routing", section 3 -- Eqs. 3, 3b, 5-8, 6b, 8b, 14-16 -- and,
-for the backward pass, section 4.1 -- Eqs. 17-20).
+Probabilistic Latent Routing", section 3 -- Eqs. 3, 3b, 5-8, 6b, 8b, 14-16, and the
+input projections of Eq. 4 -- and, for the backward pass, section 4.1 -- Eqs. 17-20).
 This module only marshals numpy arrays into it.
 
 Every function here is pinned by ``tests/test_oracle.py`` against things the
@@ -57,9 +57,10 @@ def _load():
         lib.gma_oracle_cross_head.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d, d, _dp]
         lib.gma_oracle_backward_head.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d, d, i, _dp,
                                                  _dp, _dp, _dp, _dp, _dp, _dp]
+        lib.gma_oracle_project.argtypes = [i, i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
         for fn in (lib.gma_oracle_scores, lib.gma_oracle_responsibilities,
                    lib.gma_oracle_forward_head, lib.gma_oracle_forward, lib.gma_oracle_diagnostics,
-                   lib.gma_oracle_cross_head, lib.gma_oracle_backward_head):
+                   lib.gma_oracle_cross_head, lib.gma_oracle_backward_head, lib.gma_oracle_project):
             fn.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -178,3 +179,19 @@ def backward_head(Qx, Kx, V, mu, omega, alpha, var_floor: float, eps: float, cau
                                             _p(g["Qx"]), _p(g["Kx"]), _p(g["V"]), _p(g["mu"]),
                                             _p(g["omega"]), _p(g["alpha"])), "backward_head")
     return g
+
+
+def project(X, Wq, Wk, Wv):
+    """Input projections (section 3.1, Eq. 4): X [B, N, D], Wq and Wk [H, D, d], Wv [H, D, dv]
+    -> (Qx, Kx [B, H, N, d], V [B, H, N, dv]), Qx[b, h] = X[b] Wq[h] and so on."""
+    X, Wq, Wk, Wv = map(_c, (X, Wq, Wk, Wv))
+    B, N, D = X.shape
+    H, _, d = Wq.shape
+    dv = Wv.shape[2]
+    Qx = np.empty((B, H, N, d))
+    Kx = np.empty((B, H, N, d))
+    V = np.empty((B, H, N, dv))
+    _check(_load().gma_oracle_project(B, N, D, H, d, dv, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Qx), _p(Kx), _p(V)),
+           "project")
+    return Qx, Kx, V
+

@@ -526,3 +526,37 @@ done:
     free(var); free(dvar); free(dlogpi); free(logpi);
     return rc;
 }
+
+/*
+ * Input projections (section 3.1, Eq. 4): for every batch entry b and head h,
+ *   Qx[b, h] = X[b] Wq[h],   Kx[b, h] = X[b] Wk[h],   V[b, h] = X[b] Wv[h],
+ * with X [B, N, D], Wq and Wk [H, D, d], Wv [H, D, dv], and the results in the
+ * [B, H, N, .] layout of the forward's inputs.  Each entry is a D-term dot product
+ * summed in order of the model dimension.
+ */
+int gma_oracle_project(int B, int N, int D, int H, int d, int dv, const double *X, const double *Wq,
+                       const double *Wk, const double *Wv, double *Qx, double *Kx, double *V)
+{
+    if (B < 0 || N < 0 || D <= 0 || H <= 0 || d <= 0 || dv <= 0) return 1;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int i = 0; i < N; ++i) {
+                const double *x = X + ((size_t)b * N + i) * D;
+                const size_t row = ((size_t)b * H + h) * N + i;
+                for (int c = 0; c < d; ++c) {
+                    double q = 0.0, k = 0.0;
+                    for (int m = 0; m < D; ++m) {
+                        q += x[m] * Wq[((size_t)h * D + m) * d + c];
+                        k += x[m] * Wk[((size_t)h * D + m) * d + c];
+                    }
+                    Qx[row * d + c] = q;
+                    Kx[row * d + c] = k;
+                }
+                for (int c = 0; c < dv; ++c) {
+                    double v = 0.0;
+                    for (int m = 0; m < D; ++m) v += x[m] * Wv[((size_t)h * D + m) * dv + c];
+                    V[row * dv + c] = v;
+                }
+            }
+    return 0;
+}

@@ -153,3 +153,30 @@ def test_chunk_is_honoured_or_refused(lib):
     assert lib.gma_backward_workspace_size(ctypes.byref(_desc(chunk=64, **bw)), 1, ctypes.byref(n)) == 0
     assert lib.gma_backward_workspace_size(ctypes.byref(_desc(chunk=128, **bw)), 1, ctypes.byref(n)) == 2
     assert lib.gma_backward_workspace_size(ctypes.byref(_desc(chunk=128, **bw)), 0, ctypes.byref(n)) == 0
+
+
+def test_project_rejects_bad_arguments_before_launching(lib):
+    # every call below fails validation or launches nothing: the placeholder pointers are
+    # never dereferenced
+    import gaussian_mixture_latent_gb300 as gma
+    p = ctypes.c_void_p(4096)
+    odd = ctypes.c_void_p(4100)
+    pr = lib.gma_project
+
+    def call(desc=(2, 300, 128, 3, 64, 64), X=p, Wq=p, ws=p, wsb=256):
+        d = gma.gma_proj_desc(*desc)
+        return pr(ctypes.byref(d), X, Wq, p, p, p, p, p, ws, wsb, None)
+
+    assert pr(None, p, p, p, p, p, p, p, p, 256, None) == 1
+    assert call(desc=(-1, 300, 128, 3, 64, 64)) == 1
+    assert call(desc=(2, 300, 0, 3, 64, 64)) == 1
+    assert call(desc=(2, 300, 100, 3, 64, 64)) == 2          # D not a multiple of 64
+    assert call(desc=(2, 300, 128, 3, 32, 64)) == 2          # d not a multiple of 64
+    assert call(desc=(2, 300, 128, 3, 64, 96)) == 2          # dv not a multiple of 64
+    assert call(Wq=None) == 1
+    assert call(X=None) == 1
+    assert call(X=odd) == 1
+    assert call(ws=None) == 3
+    assert call(wsb=16) == 3
+    assert call(desc=(0, 300, 128, 3, 64, 64), X=None) == 0  # B = 0: nothing to do
+    assert call(desc=(2, 0, 128, 3, 64, 64), X=None) == 0    # N = 0: nothing to do

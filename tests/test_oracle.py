@@ -488,3 +488,42 @@ def test_causal_backward_reaches_only_the_prefix():
     assert np.abs(g["Qx"][others]).max() == 0.0 and np.abs(g["Qx"][t]).max() > 0
     assert np.abs(g["Kx"][t + 1:]).max() == 0.0 and np.abs(g["V"][t + 1:]).max() == 0.0
     assert np.abs(g["Kx"][:t + 1]).max() > 0 and np.abs(g["V"][:t + 1]).max() > 0
+
+
+# ---- input projections (section 3.1, Eq. 4)
+
+def test_project_matches_brute_force_and_a_library_matmul():
+    # pure-Python triple loop on a tiny case, and numpy's einsum on a larger one
+    rng = np.random.default_rng(60)
+    B, N, D, H, d, dv = 2, 3, 5, 2, 2, 3
+    X, Wq, Wk, Wv = (rng.normal(size=s) for s in ((B, N, D), (H, D, d), (H, D, d), (H, D, dv)))
+    Qx, Kx, V = oracle.project(X, Wq, Wk, Wv)
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                for c in range(d):
+                    assert abs(Qx[b, h, i, c] - sum(X[b, i, m] * Wq[h, m, c] for m in range(D))) <= 1e-12
+                    assert abs(Kx[b, h, i, c] - sum(X[b, i, m] * Wk[h, m, c] for m in range(D))) <= 1e-12
+                for c in range(dv):
+                    assert abs(V[b, h, i, c] - sum(X[b, i, m] * Wv[h, m, c] for m in range(D))) <= 1e-12
+    B, N, D, H, d, dv = 2, 40, 96, 3, 8, 16
+    X, Wq, Wk, Wv = (rng.normal(size=s) for s in ((B, N, D), (H, D, d), (H, D, d), (H, D, dv)))
+    Qx, Kx, V = oracle.project(X, Wq, Wk, Wv)
+    for got, W in ((Qx, Wq), (Kx, Wk), (V, Wv)):
+        assert np.abs(got - np.einsum("bnm,hmc->bhnc", X, W)).max() <= 1e-12
+
+
+def test_project_with_unit_columns_selects_input_features():
+    # W with a single 1 per column picks features of X: head h's Qx column c is X[:, :, c + h]
+    rng = np.random.default_rng(61)
+    B, N, D, H, d = 1, 7, 6, 2, 3
+    X = rng.normal(size=(B, N, D))
+    Wq = np.zeros((H, D, d))
+    for h in range(H):
+        for c in range(d):
+            Wq[h, c + h, c] = 1.0
+    Qx, Kx, V = oracle.project(X, Wq, 2 * Wq, -Wq)
+    for h in range(H):
+        assert np.array_equal(Qx[0, h], X[0][:, h:h + d])
+        assert np.array_equal(Kx[0, h], 2 * X[0][:, h:h + d])
+        assert np.array_equal(V[0, h], -X[0][:, h:h + d])
