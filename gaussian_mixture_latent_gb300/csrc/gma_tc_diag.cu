@@ -13,8 +13,10 @@
 // tc_diag: persistent CTAs over 128-token tiles (batch entry b, rows j..j+127);
 // for each tile the CTA loops over the H heads: TMA load of that head's Qx tile,
 // the log-density MMA of section 4.1 (the same [x, x^2/256] . W^T + c form as the
-// forward, N = K score columns in TMEM), softmax in registers, and the head's
-// responsibilities added to a K-column fp32 accumulator in TMEM.  After the last
+// forward, N = K score columns in TMEM), the scores read once into registers (the
+// columns go back to the next head's MMA at once), softmax in registers, and the
+// head's responsibilities added to a K-wide fp32 sum over the heads (in registers
+// at K = 64, in TMEM columns at K = 128).  After the last
 // head each thread (one token) has gbar in registers: its entropy, maximum and
 // argmax, and a warp transpose-reduce adds the tile's column sums to per-warp
 // partials of p.  Responsibilities never leave the SM.
@@ -215,6 +217,8 @@ tc_diag_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
         wg_sync(rt);
         const uint32_t dcol = tmem + rt.lane_off + C::COL_D, acol = tmem + rt.lane_off + C::COL_ACC;
         float ent_sum = 0.f, max_sum = 0.f;       // over this thread's tokens
+        constexpr bool kRegAcc = K <= 64;          // the sum over heads in registers (else in TMEM)
+        float racc[kRegAcc ? K : 1];
         bool ok = true;
         for (int s = 0; s < nsteps && ok; ++s) {
             const int h = step_head(s), u = step_tile(s), b = u / A.T, j = u % A.T;
@@ -222,34 +226,28 @@ tc_diag_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
             const bool w = mbar_wait(d_full, s & 1, ab, kDevErrTimeout);
             if (!(ok = wg_all(rt, w))) break;
             tc_fence_after();
-            // this head's responsibilities (Eq. 3b), one 32-column chunk at a time: the row
-            // maximum, then fp32 exponentials written back over the scores (this step owns the
-            // score columns until d_empty) and their sum, then the normalised values
+            // this head's scores in registers (one TMEM round trip); the score columns go back to
+            // the MMA of the next head at once, so that it overlaps the softmax below
+            uint32_t v[K];
+#pragma unroll
+            for (int cc = 0; cc < K / 32; ++cc) tmem_ld32(dcol + 32 * cc, v + 32 * cc);
+            tmem_ld_wait();
+            tc_fence_before();
+            wg_sync(rt);
+            if (elected) mbar_arrive(d_empty);
+            // the head's responsibilities (Eq. 3b): the row maximum, fp32 exponentials and their
+            // sum, then the normalised values added to the sum over the heads
             float m = -INFINITY;
 #pragma unroll
-            for (int cc = 0; cc < K / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld32(dcol + 32 * cc, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int t = 0; t < 32; ++t) m = fmaxf(m, __uint_as_float(v[t]));
-            }
+            for (int t = 0; t < K; ++t) m = fmaxf(m, __uint_as_float(v[t]));
             const float M = m * scale;
             float sum = 0.f;
 #pragma unroll
-            for (int cc = 0; cc < K / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld32(dcol + 32 * cc, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const float x = ex2_approx(fmaf(__uint_as_float(v[t]), scale, -M));
-                    sum += x;
-                    v[t] = __float_as_uint(x);
-                }
-                tmem_st32(dcol + 32 * cc, v);
+            for (int t = 0; t < K; ++t) {
+                const float x = ex2_approx(fmaf(__uint_as_float(v[t]), scale, -M));
+                sum += x;
+                v[t] = __float_as_uint(x);
             }
-            tmem_st_wait();
             const float inv = 1.0f / sum;
             const bool last = h + 1 == A.H;
             const float invH = 1.0f / (float)A.H;
@@ -257,42 +255,59 @@ tc_diag_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
             const bool valid = row < A.N;
             float ent = 0.f, mx = -1.f;
             int arg = 0;
+            // gbar of this token on the last head (Eq. 24): entropy (Eq. 27), maximum and argmax
+            // (Eq. 28-29), and one 32-column chunk's column sums over the tile's tokens (Eq. 25),
+            // one partial per warp
+            auto finish_chunk = [&](float (&g)[32], int cc) {
 #pragma unroll
-            for (int cc = 0; cc < K / 32; ++cc) {
-                uint32_t v[32], acc[32];
-                tmem_ld32(dcol + 32 * cc, v);
-                if (h > 0) tmem_ld32(acol + 32 * cc, acc);
-                tmem_ld_wait();
-                float g[32];
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    g[t] = h > 0 ? fmaf(__uint_as_float(v[t]), inv, __uint_as_float(acc[t])) : __uint_as_float(v[t]) * inv;
-                if (!last) {
-                    // gamma added to the running sum over heads
-                    tmem_st32(acol + 32 * cc, reinterpret_cast<const uint32_t *>(g));
-                } else {
-                    // gbar of this token (Eq. 24): entropy (Eq. 27), maximum and argmax (Eq. 28-29),
-                    // and this chunk's column sums over the tile's tokens (Eq. 25), one partial per warp
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const float gb = g[t] * invH;
-                        ent -= gb > 0.f ? gb * __logf(gb) : 0.f;
-                        if (gb > mx) { mx = gb; arg = 32 * cc + t; }
-                        g[t] = valid ? gb : 0.f;
-                    }
-                    pacc[(warp & 3) * K + 32 * cc + lane] += warp_column_sums(g, lane);
+                for (int t = 0; t < 32; ++t) {
+                    const float gb = g[t] * invH;
+                    ent -= gb > 0.f ? gb * __logf(gb) : 0.f;
+                    if (gb > mx) { mx = gb; arg = 32 * cc + t; }
+                    g[t] = valid ? gb : 0.f;
                 }
+                pacc[(warp & 3) * K + 32 * cc + lane] += warp_column_sums(g, lane);
+            };
+            if constexpr (kRegAcc) {
+#pragma unroll
+                for (int t = 0; t < K; ++t)
+                    racc[t] = h > 0 ? fmaf(__uint_as_float(v[t]), inv, racc[t]) : __uint_as_float(v[t]) * inv;
+                if (last) {
+#pragma unroll
+                    for (int cc = 0; cc < K / 32; ++cc) {
+                        float g[32];
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) g[t] = racc[32 * cc + t];
+                        finish_chunk(g, cc);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < K / 32; ++cc) {
+                    float g[32];
+                    if (h > 0) {
+                        uint32_t acc[32];
+                        tmem_ld32(acol + 32 * cc, acc);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            g[t] = fmaf(__uint_as_float(v[32 * cc + t]), inv, __uint_as_float(acc[t]));
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) g[t] = __uint_as_float(v[32 * cc + t]) * inv;
+                    }
+                    if (!last)
+                        tmem_st32(acol + 32 * cc, reinterpret_cast<const uint32_t *>(g));   // the sum over heads
+                    else
+                        finish_chunk(g, cc);
+                }
+                if (!last) tmem_st_wait();
             }
-            if (!last) {
-                tmem_st_wait();
-            } else if (valid) {
+            if (last && valid) {
                 ent_sum += ent;
                 max_sum += mx;
                 if (A.z) A.z[(size_t)b * A.N + row] = arg;
             }
-            tc_fence_before();
-            wg_sync(rt);
-            if (elected) mbar_arrive(d_empty);
         }
         // this CTA's partials: column sums over the four warps, entropy and maximum sums over
         // the group (fixed orders); written even when the CTA had no tile
