@@ -1,10 +1,11 @@
-"""The index-checking debug build (GMA_DEBUG_BOUNDS): every forward path and the
-tensor-core backward run with their global-memory indices checked on the device, on
-outputs and workspaces padded with canary bytes.  A failed check posts GMA_ERR_BOUNDS
-to the status word (instead of trapping), so the test asserts a clean status,
-untouched canaries on both sides of every output and after every workspace, and
-results that still match the fp64 oracle.  The debug library is loaded in a child process (the
-GMA_LIBRARY override), so this process keeps the normal build."""
+"""The index-checking debug build (GMA_DEBUG_BOUNDS): every forward path, the
+tensor-core backward and the projection GEMM run with their global-memory indices
+checked on the device, on outputs and workspaces padded with canary bytes.  A failed
+check posts GMA_ERR_BOUNDS to the status word (instead of trapping), so the test
+asserts a clean status, untouched canaries on both sides of every output and after
+every workspace, and results that still match the fp64 oracle.  The debug library is
+loaded in a child process (the GMA_LIBRARY override), so this process keeps the normal
+build."""
 import os
 import subprocess
 import sys
@@ -111,6 +112,27 @@ for h in (0, 3):
         worst = max(worst, float(np.abs(got[i][h] - ref[nm]).max() / np.abs(ref[nm]).max()))
 assert worst <= TOL["bf16"], ("bwd_tc", worst)
 print(f"bwd_tc: status clean, canaries intact, max relative error {worst:.2e}")
+
+# the projection GEMM: canary-padded outputs (a ragged row tile and a partial column tile)
+B, N, D, H = 2, 300, 128, 3
+rng = np.random.default_rng(9)
+bf = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).cuda()
+Xh, Wqh, Wkh, Wvh = (rng.normal(size=s_) * c for s_, c in (((B, N, D), 1.0), ((H, D, 64), D ** -0.5),
+                                                            ((H, D, 64), D ** -0.5), ((H, D, 64), D ** -0.5)))
+ws = workspace(256)
+pads = [padded((B, H, N, 64), torch.bfloat16) for _ in range(3)]
+outs = gma.gma_project(bf(Xh), bf(Wqh), bf(Wkh), bf(Wvh), out=tuple(t for _, t in pads), workspace=ws)
+torch.cuda.synchronize()
+st = gma.gma_get_status(ws)
+assert st == 0, ("project", gma.gma_status_string(st))
+assert all(canaries_ok(f, torch.bfloat16) for f, _ in pads), ("project", "output canaries")
+assert bool((ws[256:] == CANARY_BYTE).all()), ("project", "workspace canaries")
+wd = lambda t: t.float().cpu().numpy().astype(np.float64)
+refs = oracle.project(*(wd(bf(a)) for a in (Xh, Wqh, Wkh, Wvh)))
+err = max(np.abs(wd(o)[b, h] - r[b, h]).max() / np.abs(r[b, h]).max() for o, r in zip(outs, refs)
+          for b in range(B) for h in range(H))
+assert err <= 5.5e-3, ("project", err)
+print(f"project: status clean, canaries intact, max relative error {err:.2e}")
 print("ALL_OK")
 '''
 
