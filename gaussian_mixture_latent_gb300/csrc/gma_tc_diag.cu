@@ -383,6 +383,278 @@ __global__ void __launch_bounds__(kFinGroups * kFinCols) tc_diag_finalize_kernel
     }
 }
 
+// ------------------------------------------------------------------ tc_diag2 (K = 64)
+//
+// The same computation at K = 64 with two epilogue groups: group w takes the CTA's tiles
+// w, w + 2, ... (each tile for all H heads, its head sum in registers) and converts its own
+// routing tiles, so that one group's softmax overlaps the other's log-density MMA and
+// conversion.  The MMA issuer interleaves the groups' steps, (group 0, step k), (group 1,
+// step k), ...; both use head k % H at step k, so one parameter block serves both.  Each
+// group converts step k + 1 once it has added step k's responsibilities to its head sum
+// (its one [x, x^2/256] operand is free once step k's MMA is done), so that MMA overlaps
+// the last head's statistics and the other group's work.
+constexpr int kDiag2Threads = 320;        // warps: producer, MMA, epilogue groups 0 and 1
+constexpr int kDiag2X = 6, kDiag2W = 4;   // routing-tile and parameter-block ring stages
+
+struct Diag2Cfg {
+    static constexpr int K = 64;
+    static constexpr uint32_t PB = align1k(param_bytes(K));
+    static constexpr uint32_t OFF_X = 0;
+    static constexpr uint32_t OFF_P = OFF_X + kDiag2X * kTileBytes;         // kDiag2W parameter buffers
+    static constexpr uint32_t OFF_CA = OFF_P + kDiag2W * PB;
+    static constexpr uint32_t OFF_SC = OFF_CA + kConstABytes;               // [kDiagMaxHeads] head scales
+    static constexpr uint32_t OFF_PACC = OFF_SC + 4 * kDiagMaxHeads;        // [8 warps][K] column sums
+    static constexpr uint32_t OFF_RED = OFF_PACC + 8 * 4 * K;               // [16]: entropy, maximum sums per warp
+    static constexpr uint32_t OFF_BAR = OFF_RED + 16 * 4;
+    static constexpr uint32_t BYTES = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t COL_GRP = 128, COL_A = 0, COL_D = 64;         // group w: operand, then K scores
+    static constexpr uint32_t TMEM_COLS = 256;
+    static_assert(BYTES <= 232448 && OFF_P % 1024 == 0, "diagnostics kernel layout");
+};
+
+__global__ void __launch_bounds__(kDiag2Threads, 1)
+tc_diag2_kernel(const __grid_constant__ CUtensorMap tm_q, DiagArgs A) {
+    using C = Diag2Cfg;
+    constexpr int K = C::K;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
+    uint64_t *xfull = bars, *xempty = xfull + kDiag2X, *w_full = xempty + kDiag2X, *w_empty = w_full + kDiag2W;
+    uint64_t *a_full = w_empty + kDiag2W, *d_full = a_full + 2, *d_empty = d_full + 2, *fin = d_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *scales = reinterpret_cast<float *>(sm + C::OFF_SC);
+    float *pacc = reinterpret_cast<float *>(sm + C::OFF_PACC);
+    float *red = reinterpret_cast<float *>(sm + C::OFF_RED);
+
+    grid_dep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // contiguous range of tiles; group w takes tiles u0 + w + 2 m, each for all H heads
+    const int u0 = (int)(((long long)blockIdx.x * A.Ttot) / gridDim.x);
+    const int u1 = (int)(((long long)(blockIdx.x + 1) * A.Ttot) / gridDim.x);
+    const int nt = u1 - u0;
+    const int n0 = ((nt + 1) / 2) * A.H, n1 = (nt / 2) * A.H;       // steps of groups 0 and 1 (n0 >= n1)
+    const int ntot = n0 + n1;
+    // global order of the steps: (0, k), (1, k) while both groups have steps, then group 0's rest
+    auto gidx = [&](int w, int k) { return k < n1 ? 2 * k + w : 2 * n1 + (k - n1); };
+    auto gstep = [&](int idx, int &w, int &k) {
+        if (idx < 2 * n1) { w = idx & 1; k = idx >> 1; } else { w = 0; k = n1 + (idx - 2 * n1); }
+    };
+    auto step_tile = [&](int w, int k) { return u0 + w + 2 * (k / A.H); };
+
+    if (threadIdx.x == 0) {
+        for (uint64_t *b = bars; b <= fin; ++b) mbar_init(b, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    init_const_a(sm + C::OFF_CA, threadIdx.x, blockDim.x);
+    for (int e = threadIdx.x; e < 8 * K; e += blockDim.x) pacc[e] = 0.f;
+    if (warp == 1) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Abort ab{abort_flag, A.status};
+
+    if (warp == 0) {
+        if (lane == 0 && ntot > 0) {
+            grid_dep_wait();                               // the parameter blocks are written
+            int xs = 0, ws = 0;                            // next to load: global step (routing tile), k (parameters)
+            long long last = now_ns();
+            while ((xs < ntot || ws < n0) && !*abort_flag) {
+                bool progress = false;
+                if (ws < n0 && (ws < kDiag2W || mbar_test(&w_empty[ws % kDiag2W], ((ws / kDiag2W) - 1) & 1))) {
+                    mbar_arrive_expect_tx(&w_full[ws % kDiag2W], param_bytes(K));
+                    bulk_load(sm + C::OFF_P + (ws % kDiag2W) * C::PB, A.params + (size_t)(ws % A.H) * A.param_stride,
+                              param_bytes(K), &w_full[ws % kDiag2W]);
+                    ++ws;
+                    progress = true;
+                }
+                if (xs < ntot && (xs < kDiag2X || mbar_test(&xempty[xs % kDiag2X], ((xs / kDiag2X) - 1) & 1))) {
+                    int w, k;
+                    gstep(xs, w, k);
+                    const int u = step_tile(w, k), b = u / A.T, j = u % A.T;
+                    (void)GMA_IN_BOUNDS(u < A.Ttot && b < A.B, A.status);
+                    mbar_arrive_expect_tx(&xfull[xs % kDiag2X], kTileBytes);
+                    tma_load_3d(sm + C::OFF_X + (xs % kDiag2X) * kTileBytes, &tm_q, &xfull[xs % kDiag2X], 0, j * TM,
+                                b * A.H + k % A.H);
+                    ++xs;
+                    progress = true;
+                }
+                if (progress) {
+                    last = now_ns();
+                } else {
+                    __nanosleep(64);
+                    if (now_ns() - last > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        atomicOr(A.status, kDevErrTimeout);
+                    }
+                }
+            }
+            wind_down_ring(xfull, kDiag2X, xs, A.status);
+            wind_down_ring(w_full, kDiag2W, ws, A.status);
+        }
+    } else if (warp == 1) {
+        // the log-density MMA of each step, in the global order, into the group's score columns
+        if (ntot > 0) {                               // the whole warp, converged
+            const uint32_t ca = smem_u32(sm + C::OFF_CA);
+            bool ok = true;
+            for (int idx = 0; idx < ntot && ok; ++idx) {
+                int w, k;
+                gstep(idx, w, k);
+                if (w == 0) ok = mbar_wait_warp(&w_full[k % kDiag2W], (k / kDiag2W) & 1, ab, kDevErrTimeout);
+                ok = ok && mbar_wait_warp(&a_full[w], k & 1, ab, kDevErrTimeout);
+                if (ok && k >= 1) ok = mbar_wait_warp(&d_empty[w], (k - 1) & 1, ab, kDevErrTimeout);
+                if (!ok) break;
+                tc_fence_after();
+                issue_logdensity<K>(tmem + w * C::COL_GRP + C::COL_D, tmem + w * C::COL_GRP + C::COL_A,
+                                    smem_u32(sm + C::OFF_P + (k % kDiag2W) * C::PB), ca);
+                mma_commit(&d_full[w]);
+                if (w == 1 || k >= n1) mma_commit(&w_empty[k % kDiag2W]);   // the last step to use parameters k
+            }
+            mma_commit(fin);
+            wait_ignoring_abort(fin, 0, A.status);
+        }
+    } else {
+        // ---------------- epilogue group w (warps 2-5, 6-9): one thread per token of the group's tiles
+        const int w = (warp - 2) >> 2;
+        RowThread rt;
+        rt.wg = w;
+        rt.r = 32u * (warp & 3) + lane;
+        rt.lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        rt.wtid = threadIdx.x - 64 - w * kWgThreads;
+        const bool elected = rt.wtid == 0;
+        const int nw = w == 0 ? n0 : n1;
+        grid_dep_wait();
+        const int hs = A.H < kDiagMaxHeads ? A.H : kDiagMaxHeads;
+        if (w == 0)
+            for (int h = rt.wtid; h < hs; h += kWgThreads) scales[h] = head_scale(A.params, A.param_stride, h, K);
+        group_sync(3, 2 * kWgThreads);                   // both groups, once, before any wait: the scales are in place
+        const uint32_t acol = tmem + rt.lane_off + w * C::COL_GRP + C::COL_A;
+        const uint32_t dcol = tmem + rt.lane_off + w * C::COL_GRP + C::COL_D;
+        float ent_sum = 0.f, max_sum = 0.f;
+        uint64_t racc[K / 2];                            // the sum over heads, as fp32 pairs
+        // step k's routing tile into the operand (once step k - 1's MMA is done: its scores are read)
+        auto convert = [&](int k) -> bool {
+            const int idx = gidx(w, k);
+            const bool ok = mbar_wait(&xfull[idx % kDiag2X], (idx / kDiag2X) & 1, ab, kDevErrTimeout);
+            if (!wg_all(rt, ok)) return false;
+            convert_row(sm + C::OFF_X + (idx % kDiag2X) * kTileBytes, rt.r, acol);
+            tmem_st_wait();
+            tc_fence_before();
+            wg_sync(rt);
+            if (elected) { mbar_arrive(&a_full[w]); mbar_arrive(&xempty[idx % kDiag2X]); }
+            return true;
+        };
+        bool ok = nw == 0 || convert(0);
+        for (int k = 0; k < nw && ok; ++k) {
+            const int h = k % A.H, u = step_tile(w, k), b = u / A.T, j = u % A.T;
+            const float scale = h < kDiagMaxHeads ? scales[h] : head_scale(A.params, A.param_stride, h, K);
+            const bool wt = mbar_wait(&d_full[w], k & 1, ab, kDevErrTimeout);
+            if (!(ok = wg_all(rt, wt))) break;
+            tc_fence_after();
+            uint32_t v[K];
+            tmem_ld32(dcol, v);
+            tmem_ld32(dcol + 32, v + 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            wg_sync(rt);
+            if (elected) mbar_arrive(&d_empty[w]);
+            // four independent chains for the maximum and the sum (fixed order), the exponent
+            // arguments and the head sum as fp32 pairs
+            float m4[4] = {__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]), __uint_as_float(v[3])};
+#pragma unroll
+            for (int t = 4; t < K; t += 4)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) m4[q] = fmaxf(m4[q], __uint_as_float(v[t + q]));
+            const float M = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;
+            const uint64_t sc2 = f2_pack(scale, scale), nm2 = f2_pack(-M, -M);
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint64_t e2[K / 2];
+#pragma unroll
+            for (int t = 0; t < K / 2; ++t) {
+                float xa, xb;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1])), sc2, nm2), xa, xb);
+                xa = ex2_approx(xa);
+                xb = ex2_approx(xb);
+                s4[(2 * t) & 3] += xa;
+                s4[(2 * t + 1) & 3] += xb;
+                e2[t] = f2_pack(xa, xb);
+            }
+            const float inv = 1.0f / ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+            const uint64_t inv2 = f2_pack(inv, inv);
+#pragma unroll
+            for (int t = 0; t < K / 2; ++t) racc[t] = h > 0 ? f2_fma(e2[t], inv2, racc[t]) : f2_mul(e2[t], inv2);
+            // the next step's operand (its MMA overlaps this step's statistics and the other group)
+            if (k + 1 < nw && !(ok = convert(k + 1))) break;
+            if (h + 1 == A.H) {
+                // gbar of this token (Eq. 24): entropy (Eq. 27), maximum and argmax (Eq. 28-29),
+                // and the tile's column sums (Eq. 25), one partial per warp
+                const float invH = 1.0f / (float)A.H;
+                const int row = j * TM + (int)rt.r;
+                const bool valid = row < A.N;
+                float ent4[4] = {0.f, 0.f, 0.f, 0.f}, mx = -1.f;
+                int arg = 0;
+#pragma unroll
+                for (int cc = 0; cc < K / 32; ++cc) {
+                    float g[32];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        float ga, gb2;
+                        f2_unpack(racc[16 * cc + t], ga, gb2);
+                        g[2 * t] = ga * invH;
+                        g[2 * t + 1] = gb2 * invH;
+                    }
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const float gb = g[t];
+                        ent4[t & 3] -= gb > 0.f ? gb * __logf(gb) : 0.f;
+                        if (gb > mx) { mx = gb; arg = 32 * cc + t; }
+                        g[t] = valid ? gb : 0.f;
+                    }
+                    pacc[(4 * w + (warp & 3)) * K + 32 * cc + lane] += warp_column_sums(g, lane);
+                }
+                const float ent = (ent4[0] + ent4[1]) + (ent4[2] + ent4[3]);
+                if (valid) {
+                    ent_sum += ent;
+                    max_sum += mx;
+                    if (A.z) A.z[(size_t)b * A.N + row] = arg;
+                }
+            }
+        }
+        for (int o = 16; o >= 1; o >>= 1) {
+            ent_sum += __shfl_xor_sync(~0u, ent_sum, o);
+            max_sum += __shfl_xor_sync(~0u, max_sum, o);
+        }
+        if (lane == 0) { red[4 * w + (warp & 3)] = ent_sum; red[8 + 4 * w + (warp & 3)] = max_sum; }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // this CTA's partials: column sums over the eight warps, entropy and maximum sums (fixed
+    // orders); written even when the CTA had no tile
+    if (warp >= 2 && warp < 6) {
+        const int t = threadIdx.x - 64;
+        float *dst = A.part + (size_t)blockIdx.x * (K + 2);
+        for (int k = t; k < K; k += kWgThreads) {
+            float acc = pacc[k];
+            for (int x = 1; x < 8; ++x) acc += pacc[x * K + k];
+            dst[k] = acc;
+        }
+        if (t == 0) {
+            float e = red[0], m = red[8];
+            for (int x = 1; x < 8; ++x) { e += red[x]; m += red[8 + x]; }
+            dst[K] = e;
+            dst[K + 1] = m;
+        }
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
 template <int K>
 cudaError_t launch_diag(const Problem &p, const TcLayout &L, const void *Qx, int *z, char *ws, cudaStream_t s) {
     CUtensorMap tq;
@@ -421,7 +693,19 @@ TcLayout tc_diag_layout(const Problem &p) {
 }
 
 cudaError_t tc_diag(const Problem &p, const TcLayout &L, const void *Qx, int *z, char *ws, cudaStream_t s) {
-    return p.K == 64 ? launch_diag<64>(p, L, Qx, z, ws, s) : launch_diag<128>(p, L, Qx, z, ws, s);
+    if (p.K != 64) return launch_diag<128>(p, L, Qx, z, ws, s);
+    CUtensorMap tq;
+    if (!make_map(&tq, Qx, p.G, p.N, DR)) return cudaErrorInvalidValue;
+    DiagArgs a{};
+    a.B = p.B; a.H = p.H; a.N = p.N; a.T = L.T; a.Ttot = L.Ttot;
+    a.params = reinterpret_cast<const uint8_t *>(ws + L.params);
+    a.param_stride = L.param_stride;
+    a.part = reinterpret_cast<float *>(ws + L.part);
+    a.z = z;
+    a.status = reinterpret_cast<unsigned *>(ws);
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(tc_diag2_kernel), Diag2Cfg::BYTES);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(tc_diag2_kernel, dim3(L.ncta), dim3(kDiag2Threads), Diag2Cfg::BYTES, s, tq, a);
 }
 
 cudaError_t tc_diag_finalize(const Problem &p, const TcLayout &L, float *p_out, float *stats_out, char *ws,

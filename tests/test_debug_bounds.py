@@ -1,11 +1,11 @@
 """The index-checking debug build (GMA_DEBUG_BOUNDS): every forward path, the
-tensor-core backward and the projection GEMM run with their global-memory indices
-checked on the device, on outputs and workspaces padded with canary bytes.  A failed
-check posts GMA_ERR_BOUNDS to the status word (instead of trapping), so the test
-asserts a clean status, untouched canaries on both sides of every output and after
-every workspace, and results that still match the fp64 oracle.  The debug library is
-loaded in a child process (the GMA_LIBRARY override), so this process keeps the normal
-build."""
+tensor-core backward, the projection GEMM and the diagnostics run with their
+global-memory indices checked on the device, on outputs and workspaces padded with
+canary bytes.  A failed check posts GMA_ERR_BOUNDS to the status word (instead of
+trapping), so the test asserts a clean status, untouched canaries on both sides of
+every output and after every workspace, and results that still match the fp64 oracle.
+The debug library is loaded in a child process (the GMA_LIBRARY override), so this
+process keeps the normal build."""
 import os
 import subprocess
 import sys
@@ -133,6 +133,29 @@ err = max(np.abs(wd(o)[b, h] - r[b, h]).max() / np.abs(r[b, h]).max() for o, r i
           for b in range(B) for h in range(H))
 assert err <= 5.5e-3, ("project", err)
 print(f"project: status clean, canaries intact, max relative error {err:.2e}")
+
+# the diagnostics (K = 64: two epilogue groups; K = 128: one), with the workspace padded
+for K_, N_ in ((64, 700), (128, 300)):
+    w = inputs.Workload(f"diag_k{K_}", seed=7, B=2, H=3, N=N_, d=64, K=K_, dv=64, dtype="bf16", causal=False)
+    x = inputs.gen_all(w)
+    desc = gma._make_desc(w.B, w.H, w.N, w.d, w.K, 1, torch.bfloat16, torch.bfloat16, w.var_floor, 0)
+    nb = ctypes.c_size_t(0)
+    assert gma._load().gma_diagnostics_workspace_size(ctypes.byref(desc), ctypes.byref(nb)) == 0
+    ws = workspace(nb.value)
+    p_, stats_, z_ = gma.gma_diagnostics(*(to_device(x[n]) for n in ("Qx", "mu", "rho", "alpha")),
+                                         var_floor=w.var_floor, workspace=ws)
+    torch.cuda.synchronize()
+    st = gma.gma_get_status(ws)
+    assert st == 0, (w.name, gma.gma_status_string(st))
+    assert bool((ws[nb.value:] == CANARY_BYTE).all()), (w.name, "workspace canaries")
+    rp, hu, ht, rm, rz = oracle.diagnostics(inputs.widen(x["Qx"], "bf16"), x["mu"], x["rho"], x["alpha"],
+                                            w.var_floor)
+    gp = p_.double().cpu().numpy()
+    err = max(float(np.abs(gp - rp).max() / rp.max()),
+              float(np.abs(stats_.double().cpu().numpy() - np.array([hu, ht, rm])).max()))
+    agree = float((z_.cpu().numpy() == rz).mean())
+    assert err <= 2e-2 and agree >= 0.99, (w.name, err, agree)
+    print(f"{w.name}: status clean, canaries intact, p/stats error {err:.2e}, argmax agreement {agree:.4f}")
 print("ALL_OK")
 '''
 
