@@ -7,8 +7,15 @@
 // the [B, H, N, .] layout gma_forward() reads.  A tile is 128 rows of one batch
 // entry by four 64-column blocks (N = 256), the k-loop runs over the model width
 // D in blocks of 64 through a 4-stage TMA ring, and two TMEM accumulators let the
-// epilogue of one tile overlap the MMAs of the next.  Tiles are taken in row-block
-// major order (the CTAs working at a time share their X rows in L2; W stays in L2).
+// epilogue of one tile overlap the MMAs of the next.
+//
+// CTAs work in clusters of two on tile pairs: two adjacent row tiles of the same
+// column blocks.  Each CTA loads its own X rows and half of the W blocks, which TMA
+// multicasts into both CTAs' stage, so a CTA pulls 32 KB per stage from L2 instead
+// of 48 KB.  A stage is refilled once both CTAs' MMAs have read it (each MMA commit
+// arrives on the stage's barrier in both CTAs).  Pairs are taken in row-block major
+// order (the clusters working at a time share their X rows in L2; W stays in L2); an
+// odd last row tile is paired with a copy of itself whose results are not stored.
 //
 // Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, 2-5 epilogue (thread r owns
 // accumulator row r).  Every wait is bounded; a timeout posts GMA_ERR_TIMEOUT.
@@ -28,6 +35,45 @@ using namespace sm100;
 using namespace tc;
 
 namespace {
+
+// ---- cluster helpers (a pair of CTAs)
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// TMA tile load written to the same shared-memory offset of every CTA in `mask`, each
+// CTA's barrier at `bar`'s offset receiving the bytes it got
+__device__ __forceinline__ void tma_load_3d_mc(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
+                                               int c2, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+        : "memory");
+}
+// Arrive on `bar` (same offset) in every CTA of `mask` once the MMAs issued so far have
+// completed.  Warp-collective, like mma_commit.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
+        ::"r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+// Arrive on the barrier at `bar`'s offset in CTA `peer` of the cluster.
+__device__ __forceinline__ void mbar_arrive_peer(uint64_t *bar, uint32_t peer) {
+    asm volatile(
+        "{\n\t.reg .b32 ra;\n\t"
+        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}"
+        ::"r"(smem_u32(bar)), "r"(peer)
+        : "memory");
+}
 
 constexpr int PM = 128;                       // rows per tile
 constexpr int PBN = 64;                       // output columns per block
@@ -54,7 +100,7 @@ static_assert(kStage % 1024 == 0 && ProjCfg::OFF_E % 1024 == 0, "operand blocks 
 struct ProjArgs {
     int B, N, H, nkb;             // nkb = D / 64
     int nqb, nvb, nbh;            // 64-column blocks per head: of W_Q (= of W_K), of W_V, in all
-    int mt_per_b, n_ntiles, n_tiles, nblocks;
+    int mt_per_b, n_mtiles, n_ntiles, n_pairs, nblocks;   // pairs: (row tiles 2 m, 2 m + 1; column tile)
     unsigned *status;
 };
 
@@ -81,28 +127,40 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
     uint64_t *full = bars, *empty = bars + PS, *acc_full = bars + 2 * PS, *acc_empty = acc_full + 2;
-    uint64_t *fin = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
+    uint64_t *fin = acc_empty + 2, *done = fin + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
+    const int cid = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
+    constexpr uint16_t kBoth = 0x3;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < PS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < PS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 2);                   // the MMAs of both CTAs have read the stage
+        }
         for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 1); }
         mbar_init(fin, 1);
+        mbar_init(done, 1);                            // the peer is done with this CTA's memory
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == kWMma) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();                                // both CTAs' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Abort ab{abort_flag, A.status};
-    auto tile_geom = [&](int t, int &b, int &n0, int &nt, int &nbt) {
-        const int m = t / A.n_ntiles;
-        nt = t - m * A.n_ntiles;
+    // pair q, this CTA's row tile: m = 2 mp + rank (an odd last row tile pairs with a copy of itself)
+    auto tile_geom = [&](int q, int &b, int &n0, int &nt, int &nbt, bool &store) {
+        const int mp = q / A.n_ntiles;
+        nt = q - mp * A.n_ntiles;
+        int m = 2 * mp + (int)rank;
+        store = m < A.n_mtiles;
+        if (!store) m = A.n_mtiles - 1;
         b = m / A.mt_per_b;
         n0 = (m - b * A.mt_per_b) * PM;
         nbt = min(PNB, A.nblocks - nt * PNB);
@@ -113,9 +171,10 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             grid_dep_wait();
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < A.n_tiles && ok; t += gridDim.x) {
+            for (int q = cid; q < A.n_pairs && ok; q += ncl) {
                 int b, n0, nt, nbt;
-                tile_geom(t, b, n0, nt, nbt);
+                bool store;
+                tile_geom(q, b, n0, nt, nbt, store);
                 (void)GMA_IN_BOUNDS(b < A.B && n0 < A.N, A.status);
                 for (int kb = 0; kb < A.nkb; ++kb, ++it) {
                     const int s = it % PS;
@@ -123,22 +182,26 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     uint8_t *st = sm + C::OFF_S + s * kStage;
                     mbar_arrive_expect_tx(&full[s], kABytes + nbt * kBBlk);
                     tma_load_3d(st, &tm_x, &full[s], kb * PKB, n0, b);
-                    for (int j = 0; j < nbt; ++j) {
+                    for (int j = (int)rank; j < nbt; j += 2) {     // this CTA's half of the W blocks, to both
                         const BlockMap m = map_block(A, nt * PNB + j);
                         const CUtensorMap *wm = m.which == 0 ? &tm_wq : (m.which == 1 ? &tm_wk : &tm_wv);
-                        tma_load_3d(st + kABytes + j * kBBlk, wm, &full[s], m.col * PBN, kb * PKB, m.h);
+                        tma_load_3d_mc(st + kABytes + j * kBBlk, wm, &full[s], m.col * PBN, kb * PKB, m.h, kBoth);
                     }
                 }
             }
+            // every fill has landed, and both CTAs' MMAs have released every stage (so neither
+            // CTA's multicast nor commit still targets this CTA)
             wind_down_ring(full, PS, it, A.status);
+            wind_down_ring(empty, PS, it, A.status);
         }
     } else if (warp == kWMma) {
         // the whole warp, converged
         int it = 0, lt = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < A.n_tiles && ok; t += gridDim.x, ++lt) {
+        for (int q = cid; q < A.n_pairs && ok; q += ncl, ++lt) {
             int b, n0, nt, nbt;
-            tile_geom(t, b, n0, nt, nbt);
+            bool store;
+            tile_geom(q, b, n0, nt, nbt, store);
             const int buf = lt & 1;
             if (lt >= 2 && !(ok = mbar_wait_warp(&acc_empty[buf], ((lt >> 1) - 1) & 1, ab, kDevErrTimeout))) break;
             tc_fence_after();
@@ -154,7 +217,7 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 #pragma unroll
                 for (int kk = 0; kk < PKB / 16; ++kk)
                     mma_ss(acc, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 128), idesc, (kb | kk) != 0);
-                mma_commit(&empty[s]);
+                mma_commit_mc(&empty[s], kBoth);      // the stage is free here and, for its multicast part, in the peer
             }
             if (ok) mma_commit(&acc_full[buf]);
         }
@@ -170,14 +233,15 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const bool elected = rt.wtid == 0;
         if (elected) grid_dep_wait();       // the previous kernel in the stream no longer reads the outputs
         int lt = 0, ec = 0;
-        for (int t = blockIdx.x; t < A.n_tiles; t += gridDim.x, ++lt) {
+        for (int q = cid; q < A.n_pairs; q += ncl, ++lt) {
             int b, n0, nt, nbt;
-            tile_geom(t, b, n0, nt, nbt);
+            bool store;
+            tile_geom(q, b, n0, nt, nbt, store);
             const int buf = lt & 1;
             const bool ok = mbar_wait(&acc_full[buf], (lt >> 1) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
-            for (int j = 0; j < nbt; ++j, ++ec) {
+            for (int j = 0; j < nbt && store; ++j, ++ec) {   // (the copy of an odd last row tile stores nothing)
                 uint32_t v0[32], v1[32];
                 const uint32_t ta = tmem + rt.lane_off + buf * C::ACC_COLS + j * PBN;
                 tmem_ld32(ta, v0);
@@ -187,13 +251,13 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 if (elected) bulk_wait_group_read<1>();       // the store that last used this buffer has read it
                 wg_sync(rt);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t *src = q < 4 ? v0 + 8 * q : v1 + 8 * (q - 4);
+                for (int qq = 0; qq < 8; ++qq) {
+                    const uint32_t *src = qq < 4 ? v0 + 8 * qq : v1 + 8 * (qq - 4);
                     uint32_t o[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
                         o[u] = pack_bf16(__uint_as_float(src[2 * u]), __uint_as_float(src[2 * u + 1]));
-                    *reinterpret_cast<uint4 *>(eb + sw128_off(rt.r, q)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(eb + sw128_off(rt.r, qq)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
                 fence_proxy_async_smem();
                 wg_sync(rt);
@@ -215,6 +279,13 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // neither CTA leaves while the other may still write into it: each tells the other it is
+    // done (its loads landed, its MMAs released every stage) and waits for the same, bounded
+    if (threadIdx.x == 0) {
+        mbar_arrive_peer(done, peer);
+        wait_ignoring_abort(done, 0, A.status);
+    }
+    __syncthreads();
     if (warp == kWMma) {
         __syncwarp();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -238,16 +309,37 @@ cudaError_t proj_run(int B, int N, int D, int H, int d, int dv, const void *X, c
     a.B = B; a.N = N; a.H = H; a.nkb = D / PKB;
     a.nqb = d / PBN; a.nvb = dv / PBN; a.nbh = 2 * a.nqb + a.nvb;
     a.mt_per_b = (N + PM - 1) / PM;
+    a.n_mtiles = B * a.mt_per_b;
     a.nblocks = H * a.nbh;
     a.n_ntiles = (a.nblocks + PNB - 1) / PNB;
-    a.n_tiles = B * a.mt_per_b * a.n_ntiles;
+    a.n_pairs = ((a.n_mtiles + 1) / 2) * a.n_ntiles;
     a.status = reinterpret_cast<unsigned *>(ws);
-    const int nsm = sm_count();
-    const int ncta = std::max(1, std::min(nsm > 0 ? nsm : kMaxCtas, a.n_tiles));
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(proj_kernel), ProjCfg::BYTES);
     if (e != cudaSuccess) return e;
-    return launch_dependent(proj_kernel, dim3(ncta), dim3(kPThreads), ProjCfg::BYTES, s, tx, twq, twk, twv, tq, tk,
-                            tv, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = ProjCfg::BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    // persistent clusters of two CTAs, as many as can be resident at once (pairs are assigned
+    // statically, so a second wave would double the tail)
+    const int nsm = sm_count();
+    int ncl = std::max(1, std::min((nsm > 0 ? nsm : kMaxCtas) / 2, a.n_pairs));
+    cfg.gridDim = dim3(2 * ncl);
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, reinterpret_cast<const void *>(proj_kernel), &cfg) == cudaSuccess &&
+        active > 0)
+        ncl = std::min(ncl, active);
+    cfg.gridDim = dim3(2 * ncl);
+    return cudaLaunchKernelEx(&cfg, proj_kernel, tx, twq, twk, twv, tq, tk, tv, a);
 }
 
 }  // namespace gma
