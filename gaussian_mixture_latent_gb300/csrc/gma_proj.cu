@@ -75,6 +75,7 @@ __device__ __forceinline__ void mbar_arrive_peer(uint64_t *bar, uint32_t peer) {
         : "memory");
 }
 
+constexpr int kCl = 4;                        // CTAs per cluster (row tiles sharing their W blocks)
 constexpr int PM = 128;                       // rows per tile
 constexpr int PBN = 64;                       // output columns per block
 constexpr int PNB = 4;                        // blocks per tile (MMA N up to 256)
@@ -100,7 +101,7 @@ static_assert(kStage % 1024 == 0 && ProjCfg::OFF_E % 1024 == 0, "operand blocks 
 struct ProjArgs {
     int B, N, H, nkb;             // nkb = D / 64
     int nqb, nvb, nbh;            // 64-column blocks per head: of W_Q (= of W_K), of W_V, in all
-    int mt_per_b, n_mtiles, n_ntiles, n_pairs, nblocks;   // pairs: (row tiles 2 m, 2 m + 1; column tile)
+    int mt_per_b, n_mtiles, n_ntiles, n_pairs, nblocks;   // groups: (row tiles kCl m .. kCl m + kCl - 1; column tile)
     unsigned *status;
 };
 
@@ -133,32 +134,32 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
-    const int cid = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
-    constexpr uint16_t kBoth = 0x3;
+    const uint32_t rank = cluster_rank();
+    const int cid = (int)(blockIdx.x / kCl), ncl = (int)(gridDim.x / kCl);
+    constexpr uint16_t kAll = (uint16_t)((1u << kCl) - 1u);
     if (threadIdx.x == 0) {
         for (int s = 0; s < PS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);                   // the MMAs of both CTAs have read the stage
+            mbar_init(&empty[s], kCl);                 // the MMAs of every CTA of the cluster have read the stage
         }
         for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 1); }
         mbar_init(fin, 1);
-        mbar_init(done, 1);                            // the peer is done with this CTA's memory
+        mbar_init(done, kCl - 1);                      // the other CTAs are done with this CTA's memory
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == kWMma) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();                                // both CTAs' barriers exist before any multicast
+    cluster_sync_all();                                // every CTA's barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Abort ab{abort_flag, A.status};
-    // pair q, this CTA's row tile: m = 2 mp + rank (an odd last row tile pairs with a copy of itself)
+    // group q, this CTA's row tile: m = kCl mp + rank (row tiles past the last are copies of it)
     auto tile_geom = [&](int q, int &b, int &n0, int &nt, int &nbt, bool &store) {
         const int mp = q / A.n_ntiles;
         nt = q - mp * A.n_ntiles;
-        int m = 2 * mp + (int)rank;
+        int m = kCl * mp + (int)rank;
         store = m < A.n_mtiles;
         if (!store) m = A.n_mtiles - 1;
         b = m / A.mt_per_b;
@@ -182,10 +183,10 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     uint8_t *st = sm + C::OFF_S + s * kStage;
                     mbar_arrive_expect_tx(&full[s], kABytes + nbt * kBBlk);
                     tma_load_3d(st, &tm_x, &full[s], kb * PKB, n0, b);
-                    for (int j = (int)rank; j < nbt; j += 2) {     // this CTA's half of the W blocks, to both
+                    for (int j = (int)rank; j < nbt; j += kCl) {   // this CTA's share of the W blocks, to all
                         const BlockMap m = map_block(A, nt * PNB + j);
                         const CUtensorMap *wm = m.which == 0 ? &tm_wq : (m.which == 1 ? &tm_wk : &tm_wv);
-                        tma_load_3d_mc(st + kABytes + j * kBBlk, wm, &full[s], m.col * PBN, kb * PKB, m.h, kBoth);
+                        tma_load_3d_mc(st + kABytes + j * kBBlk, wm, &full[s], m.col * PBN, kb * PKB, m.h, kAll);
                     }
                 }
             }
@@ -217,7 +218,7 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 #pragma unroll
                 for (int kk = 0; kk < PKB / 16; ++kk)
                     mma_ss(acc, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 128), idesc, (kb | kk) != 0);
-                mma_commit_mc(&empty[s], kBoth);      // the stage is free here and, for its multicast part, in the peer
+                mma_commit_mc(&empty[s], kAll);       // the stage is free here and, for its multicast parts, elsewhere
             }
             if (ok) mma_commit(&acc_full[buf]);
         }
@@ -241,7 +242,7 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const bool ok = mbar_wait(&acc_full[buf], (lt >> 1) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
-            for (int j = 0; j < nbt && store; ++j, ++ec) {   // (the copy of an odd last row tile stores nothing)
+            for (int j = 0; j < nbt && store; ++j, ++ec) {   // (a copy of the last row tile stores nothing)
                 uint32_t v0[32], v1[32];
                 const uint32_t ta = tmem + rt.lane_off + buf * C::ACC_COLS + j * PBN;
                 tmem_ld32(ta, v0);
@@ -279,10 +280,10 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // neither CTA leaves while the other may still write into it: each tells the other it is
-    // done (its loads landed, its MMAs released every stage) and waits for the same, bounded
+    // no CTA leaves while another may still write into it: each tells the others it is done
+    // (its loads landed, its MMAs released every stage) and waits for the same, bounded
     if (threadIdx.x == 0) {
-        mbar_arrive_peer(done, peer);
+        for (uint32_t o = 1; o < (uint32_t)kCl; ++o) mbar_arrive_peer(done, (rank + o) % kCl);
         wait_ignoring_abort(done, 0, A.status);
     }
     __syncthreads();
@@ -312,7 +313,7 @@ cudaError_t proj_run(int B, int N, int D, int H, int d, int dv, const void *X, c
     a.n_mtiles = B * a.mt_per_b;
     a.nblocks = H * a.nbh;
     a.n_ntiles = (a.nblocks + PNB - 1) / PNB;
-    a.n_pairs = ((a.n_mtiles + 1) / 2) * a.n_ntiles;
+    a.n_pairs = ((a.n_mtiles + kCl - 1) / kCl) * a.n_ntiles;
     a.status = reinterpret_cast<unsigned *>(ws);
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(proj_kernel), ProjCfg::BYTES);
     if (e != cudaSuccess) return e;
@@ -324,21 +325,21 @@ cudaError_t proj_run(int B, int N, int D, int H, int d, int dv, const void *X, c
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.x = kCl;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    // persistent clusters of two CTAs, as many as can be resident at once (pairs are assigned
+    // persistent clusters, as many as can be resident at once (tile groups are assigned
     // statically, so a second wave would double the tail)
     const int nsm = sm_count();
-    int ncl = std::max(1, std::min((nsm > 0 ? nsm : kMaxCtas) / 2, a.n_pairs));
-    cfg.gridDim = dim3(2 * ncl);
+    int ncl = std::max(1, std::min((nsm > 0 ? nsm : kMaxCtas) / kCl, a.n_pairs));
+    cfg.gridDim = dim3(kCl * ncl);
     int active = 0;
     if (cudaOccupancyMaxActiveClusters(&active, reinterpret_cast<const void *>(proj_kernel), &cfg) == cudaSuccess &&
         active > 0)
         ncl = std::min(ncl, active);
-    cfg.gridDim = dim3(2 * ncl);
+    cfg.gridDim = dim3(kCl * ncl);
     return cudaLaunchKernelEx(&cfg, proj_kernel, tx, twq, twk, twv, tq, tk, tv, a);
 }
 
