@@ -349,6 +349,7 @@ def run_gpu(args, rank, world, local):
 
     # warm-up with every launch bracketed by events: finds the dominant kernel
     per = {}
+    torch.cuda.nvtx.range_push("gma:warmup")          # coarse NVTX ranges, for ncu / nsys filters
     for it in range(max(3, args.warmup)):
         evs = {}
         for c in dirs:
@@ -385,6 +386,8 @@ def run_gpu(args, rank, world, local):
     sampler.start()
     time.sleep(0.3)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.nvtx.range_push("gma:timed")
     t_start.record(stream)
     for it in range(steps):
         x = dsets[it % 2]
@@ -397,6 +400,7 @@ def run_gpu(args, rank, world, local):
                 forward(x, c)
     t_end.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     clocks = sampler.stop()
     ms_per_step = max_over_ranks(t_start.elapsed_time(t_end) / steps, device=dev)
     if world > 1:
@@ -439,6 +443,7 @@ def run_gpu(args, rank, world, local):
     # end to end through the public API from pinned host memory
     e2e = None
     if args.e2e_steps > 0:
+        torch.cuda.nvtx.range_push("gma:e2e")
         # Pipelined like a serving loop: host->device copies, the forwards and device->host
         # copies run on three streams over two device buffer sets, so step i's uploads and
         # step i-1's downloads overlap step i-1 / i's kernels.  Every step still copies its
@@ -491,10 +496,13 @@ def run_gpu(args, rank, world, local):
         e2e_ms = max_over_ranks(a.elapsed_time(b) / args.e2e_steps, device=dev)
         e2e = {"value": whole_job_rate(units_per_step, world, e2e_ms), "unit": "tokens·heads/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        torch.cuda.nvtx.range_pop()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        torch.cuda.nvtx.range_push("gma:cpu_baseline")
         cpu = cpu_baseline(w, dirs)
+        torch.cuda.nvtx.range_pop()
 
     if rank == 0:
         launches = steps * sum(len(plan[c]) for c in dirs)
