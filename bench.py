@@ -58,6 +58,10 @@ def parse():
                          "decode: one step is gma_decode of one new token for every head; "
                          "project: one step is gma_project, the Q/K/V projections of the workload's rows "
                          "from a model width of H d")
+    ap.add_argument("--schedule", choices=["multi", "sequential"], default="multi",
+                    help="both directions: one gma_forward_multi request with the causal scan on a second "
+                         "stream beside the bidirectional forward (default), or two gma_forward calls one "
+                         "after the other on one stream")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's sequence length N (a reduced case for profiling)")
     ap.add_argument("--batch", type=int, default=0,
@@ -92,6 +96,20 @@ def max_over_ranks(x, device="cpu"):
     t = torch.tensor([float(x)], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def device_status(gma, ws=None, offsets=()):
+    """The device status of the library's default workspace, or of every call region of a
+    gma_forward_multi workspace (the first error found)."""
+    import torch
+    if ws is None:
+        return gma.gma_get_status()
+    stream = int(torch.cuda.current_stream().cuda_stream)
+    for off in offsets:
+        st = gma._load().gma_get_status(int(ws.data_ptr()) + int(off), stream)
+        if st:
+            return st
+    return 0
 
 
 def whole_job_rate(units_per_rank, world, ms_per_step):
@@ -347,22 +365,48 @@ def run_gpu(args, rank, world, local):
                                causal=causal, out=outs[causal], var_floor=w.var_floor,
                                events=events)
 
+    # The step's forwards: with two directions, one gma_forward_multi request whose causal
+    # scan (one CTA per head) runs on `aux` beside the bidirectional forward on `stream`.
+    multi = len(dirs) > 1 and args.schedule == "multi"
+    aux = torch.cuda.Stream(device=dev)
+    mws, moffs = torch.zeros(1, dtype=torch.uint8, device=dev), []
+
+    def step_forwards(x, evs=None, out=None, st=None):
+        evs = evs or {}
+        out = out or outs
+        if not multi:
+            for c in dirs:
+                gma.gma_forward(x["Qx"], x["Kx"], x["V"], x["mu"], x["rho"], x["alpha"], eps=w.eps, causal=c,
+                                out=out[c], var_floor=w.var_floor, events=evs.get(c), stream=st)
+            return
+        calls = [dict(Qx=x["Qx"], Kx=x["Kx"], V=x["V"], mu=x["mu"], rho=x["rho"], pi_logits=x["alpha"], eps=w.eps,
+                      causal=c, out=out[c], var_floor=w.var_floor, events=evs.get(c)) for c in dirs]
+        gma.gma_forward_multi(calls, workspace=mws, stream=st, aux_stream=aux)
+
+    if multi:
+        import ctypes
+        nb, offs = ctypes.c_size_t(0), (ctypes.c_size_t * len(dirs))()
+        calls = (gma.gma_forward_call * len(dirs))()
+        for k, c in enumerate(dirs):
+            calls[k].desc = gma._make_desc(w.B, w.H, w.N, w.d, w.K, w.dv, tdt, tdt, w.var_floor, 0)
+            calls[k].causal = int(c)
+        assert gma._load().gma_forward_multi_workspace_size(calls, len(dirs), ctypes.byref(nb), offs) == 0
+        mws, moffs = torch.zeros(nb.value, dtype=torch.uint8, device=dev), list(offs)
+
     # warm-up with every launch bracketed by events: finds the dominant kernel
     per = {}
     torch.cuda.nvtx.range_push("gma:warmup")          # coarse NVTX ranges, for ncu / nsys filters
     for it in range(max(3, args.warmup)):
-        evs = {}
-        for c in dirs:
-            evs[c] = [new_event() for _ in range(2 * len(plan[c]))]
-            # keep the GPU busy while the host enqueues, so the events bracket GPU time only
-            torch.cuda._sleep(2_000_000)
-            forward(dsets[it % 2], c, evs[c])
+        evs = {c: [new_event() for _ in range(2 * len(plan[c]))] for c in dirs}
+        # keep the GPU busy while the host enqueues, so the events bracket GPU time only
+        torch.cuda._sleep(2_000_000)
+        step_forwards(dsets[it % 2], evs)
         torch.cuda.synchronize()
         if it >= 1:
             for c in dirs:
                 for i, name in enumerate(plan[c]):
                     per.setdefault((c, name), []).append(evs[c][2 * i].elapsed_time(evs[c][2 * i + 1]))
-    status = gma.gma_get_status()
+    status = device_status(gma, mws if multi else None, moffs)
     if status:
         raise RuntimeError("device status after warm-up: " + gma.gma_status_string(status))
     share = {k: statistics.median(v) for k, v in per.items()}
@@ -390,14 +434,11 @@ def run_gpu(args, rank, world, local):
     torch.cuda.nvtx.range_push("gma:timed")
     t_start.record(stream)
     for it in range(steps):
-        x = dsets[it % 2]
-        for c in dirs:
-            if c == dom_c and it in dom_events:
-                evs = [None] * (2 * len(plan[c]))
-                evs[2 * dom_idx], evs[2 * dom_idx + 1] = dom_events[it]
-                forward(x, c, evs)
-            else:
-                forward(x, c)
+        evs = None
+        if it in dom_events:
+            evs = {dom_c: [None] * (2 * len(plan[dom_c]))}
+            evs[dom_c][2 * dom_idx], evs[dom_c][2 * dom_idx + 1] = dom_events[it]
+        step_forwards(dsets[it % 2], evs)
     t_end.record(stream)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
@@ -406,7 +447,7 @@ def run_gpu(args, rank, world, local):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    status = gma.gma_get_status()
+    status = device_status(gma, mws if multi else None, moffs)
     if status:
         raise RuntimeError("device status after timed region: " + gma.gma_status_string(status))
     dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom_events.values())
@@ -471,10 +512,7 @@ def run_gpu(args, rank, world, local):
                 up_done[b_].record(s_up)
             stream.wait_event(up_done[b_])
             stream.wait_event(down_done[b_])                     # the set's previous results were read
-            for c in dirs:
-                gma.gma_forward(staging[b_]["Qx"], staging[b_]["Kx"], staging[b_]["V"], staging[b_]["mu"],
-                                staging[b_]["rho"], staging[b_]["alpha"], eps=w.eps, causal=c,
-                                out=douts[b_][c], var_floor=w.var_floor)
+            step_forwards(staging[b_], out=douts[b_])
             comp_done[b_].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(comp_done[b_])
@@ -514,6 +552,8 @@ def run_gpu(args, rank, world, local):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K,
                        "dv": w.dv, "step": {"both": "bidirectional + causal forward", "bidir": "bidirectional forward",
                                 "causal": "causal forward"}[args.direction],
+                       "schedule": ("one gma_forward_multi request: the causal scan on a second stream beside "
+                                    "the bidirectional forward" if multi else "gma_forward calls in order, one stream"),
                        "l2": "two alternating input sets of %d MB each (> 129 MB L2)" %
                              (sum(v.numel() * v.element_size() for v in dsets[0].values()) // 2**20),
                        "parallelism": "replicas" if world > 1 else "single GPU"},

@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "GmaError", "gma_desc", "gma_workspace_size", "gma_workspace_init", "gma_forward",
-    "gma_forward_ex", "gma_forward_plan",
+    "gma_forward_ex", "gma_forward_plan", "gma_forward_call", "gma_forward_multi",
     "gma_responsibilities", "gma_diagnostics", "gma_forward_cross", "gma_decode", "gma_backward",
     "gma_proj_desc", "gma_project", "gma_selftest_timeout", "gma_get_status", "gma_status_string", "gma_version",
     "Workspace", "library_path",
@@ -49,6 +49,14 @@ class gma_desc(ctypes.Structure):
                 ("d", ctypes.c_int), ("K", ctypes.c_int), ("dv", ctypes.c_int),
                 ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
                 ("var_floor", ctypes.c_float), ("chunk", ctypes.c_int)]
+
+
+class gma_forward_call(ctypes.Structure):
+    """Mirror of ``gma_forward_call`` in include/gma.h."""
+    _fields_ = [("desc", gma_desc), ("causal", ctypes.c_int), ("eps", ctypes.c_float),
+                ("Qx", ctypes.c_void_p), ("Kx", ctypes.c_void_p), ("V", ctypes.c_void_p),
+                ("mu", ctypes.c_void_p), ("rho", ctypes.c_void_p), ("pi_logits", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("events", ctypes.POINTER(ctypes.c_void_p)), ("n_events", ctypes.c_int)]
 
 
 class gma_proj_desc(ctypes.Structure):
@@ -89,6 +97,9 @@ def _load():
     lib.gma_selftest_timeout.argtypes = [vp, sz, vp]
     lib.gma_backward.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gma_project.argtypes = [ctypes.POINTER(gma_proj_desc), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    cp = ctypes.POINTER(gma_forward_call)
+    lib.gma_forward_multi_workspace_size.argtypes = [cp, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.gma_forward_multi.argtypes = [cp, i, vp, sz, vp, vp]
     lib.gma_get_status.argtypes = [vp, vp]
     lib.gma_status_string.argtypes = [i]
     lib.gma_status_string.restype = ctypes.c_char_p
@@ -97,7 +108,8 @@ def _load():
                lib.gma_forward_ex, lib.gma_forward_plan, lib.gma_responsibilities, lib.gma_get_status, lib.gma_version,
                lib.gma_diagnostics_workspace_size, lib.gma_diagnostics, lib.gma_cross_workspace_size,
                lib.gma_forward_cross, lib.gma_decode_workspace_size, lib.gma_decode,
-               lib.gma_backward_workspace_size, lib.gma_backward, lib.gma_selftest_timeout, lib.gma_project):
+               lib.gma_backward_workspace_size, lib.gma_backward, lib.gma_selftest_timeout, lib.gma_project,
+               lib.gma_forward_multi_workspace_size, lib.gma_forward_multi):
         fn.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -248,6 +260,79 @@ def gma_forward(Qx, Kx, V, mu, rho, pi_logits, eps: float = 1e-6, causal: bool =
     if check_status:
         _check_device_status(ws, stream, "gma_forward")
     return out
+
+
+_multi_ws: dict = {}
+
+
+def gma_forward_multi(calls, workspace=None, stream=None, aux_stream=None, check_status: bool = False):
+    """Several independent forwards in one request (include/gma.h, gma_forward_multi).
+
+    calls: a list of dicts with gma_forward()'s tensor arguments Qx, Kx, V, mu, rho,
+    pi_logits and optional eps (1e-6), causal (False), out, var_floor (1e-4), out_dtype,
+    chunk (0), events.  With aux_stream (a torch.cuda.Stream) the library may run the
+    calls that it schedules as one CTA per head on aux_stream beside the others.
+    Returns the list of outputs.  workspace: None (a zeroed buffer of this module's
+    cache) or a uint8 tensor of gma_forward_multi_workspace_size() bytes whose regions'
+    first 256 bytes are zero.  check_status=True synchronises and raises GmaError when
+    a kernel of any call posted a device error."""
+    n = len(calls)
+    arr = (gma_forward_call * max(n, 1))()
+    outs, keep = [], []
+    for k, c in enumerate(calls):
+        Qx, Kx, V, mu, rho, pi = (c[name] for name in ("Qx", "Kx", "V", "mu", "rho", "pi_logits"))
+        B, H, N, d = Qx.shape
+        dv, K = V.shape[-1], mu.shape[1]
+        out_dtype = c.get("out_dtype") or Qx.dtype
+        _check(Qx, "Qx", (B, H, N, d), (torch.float32, torch.bfloat16))
+        _check(Kx, "Kx", (B, H, N, d), (Qx.dtype,))
+        _check(V, "V", (B, H, N, dv), (Qx.dtype,))
+        _check(mu, "mu", (H, K, d), (torch.float32,))
+        _check(rho, "rho", (H, K, d), (torch.float32,))
+        _check(pi, "pi_logits", (H, K), (torch.float32,))
+        out = c.get("out")
+        if out is None:
+            out = torch.empty((B, H, N, dv), dtype=out_dtype, device=Qx.device)
+        _check(out, "out", (B, H, N, dv), (out_dtype,))
+        outs.append(out)
+        arr[k].desc = _make_desc(B, H, N, d, K, dv, Qx.dtype, out_dtype, c.get("var_floor", 1e-4), c.get("chunk", 0))
+        arr[k].causal = int(bool(c.get("causal", False)))
+        arr[k].eps = float(c.get("eps", 1e-6))
+        for name, t in (("Qx", Qx), ("Kx", Kx), ("V", V), ("mu", mu), ("rho", rho), ("pi_logits", pi),
+                        ("out", out)):
+            setattr(arr[k], name, _ptr(t))
+        evs = c.get("events")
+        if evs is not None:
+            h = (ctypes.c_void_p * len(evs))(*[e.cuda_event if e is not None else None for e in evs])
+            keep.append(h)
+            arr[k].events = ctypes.cast(h, ctypes.POINTER(ctypes.c_void_p))
+            arr[k].n_events = len(evs)
+    lib = _load()
+    nbytes, offs = ctypes.c_size_t(0), (ctypes.c_size_t * max(n, 1))()
+    rc = lib.gma_forward_multi_workspace_size(arr, n, ctypes.byref(nbytes), offs)
+    if rc:
+        raise GmaError(rc, "gma_forward_multi_workspace_size")
+    if workspace is None:
+        dev = calls[0]["Qx"].device if n else torch.device("cuda")
+        key = dev.index if dev.index is not None else torch.cuda.current_device()
+        ws = _multi_ws.get(key)
+        if ws is None or ws.numel() < nbytes.value:
+            ws = torch.zeros(max(nbytes.value, 256), dtype=torch.uint8, device=torch.device("cuda", key))
+            _multi_ws[key] = ws
+    else:
+        ws = workspace
+        if ws.numel() < nbytes.value:
+            raise GmaError(3, "gma_forward_multi")
+    aux = None if aux_stream is None else int(aux_stream.cuda_stream)
+    rc = lib.gma_forward_multi(arr, n, _ptr(ws), ws.numel(), _stream_ptr(stream), aux)
+    if rc:
+        raise GmaError(rc, "gma_forward_multi")
+    if check_status:
+        for k in range(n):
+            st = lib.gma_get_status(_ptr(ws) + offs[k], _stream_ptr(stream))
+            if st:
+                raise GmaError(st, f"gma_forward_multi (call {k})")
+    return outs
 
 
 def gma_responsibilities(X, mu, rho, pi_logits, var_floor: float = 1e-4, out=None,

@@ -5,6 +5,7 @@
 // stream.  gma_forward() runs the plan; gma_forward_ex() runs it with
 // caller-owned CUDA events recorded around each launch (per-kernel timing);
 // gma_forward_plan() reports the launches without running anything.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -173,6 +174,37 @@ gma_status run_plan(const Plan &plan, cudaStream_t s, void *const *events, int n
     return GMA_OK;
 }
 
+// The fork and join events of gma_forward_multi: created once per host thread and
+// device, outside any stream capture that comes later, and reused (a stream wait takes
+// the event's state when it is enqueued, so re-recording it afterwards is safe).  Per
+// thread, so that requests from two threads never wait on each other's events.
+struct LaneEvents {
+    int dev;
+    cudaEvent_t fork, join;
+};
+thread_local std::vector<LaneEvents> tl_lane_events;
+
+cudaError_t lane_events(int dev, cudaEvent_t &fork, cudaEvent_t &join) {
+    for (const LaneEvents &e : tl_lane_events)
+        if (e.dev == dev) {
+            fork = e.fork;
+            join = e.join;
+            return cudaSuccess;
+        }
+    LaneEvents e{dev, nullptr, nullptr};
+    cudaError_t err = cudaEventCreateWithFlags(&e.fork, cudaEventDisableTiming);
+    if (err != cudaSuccess) return err;
+    err = cudaEventCreateWithFlags(&e.join, cudaEventDisableTiming);
+    if (err != cudaSuccess) {
+        cudaEventDestroy(e.fork);
+        return err;
+    }
+    tl_lane_events.push_back(e);
+    fork = e.fork;
+    join = e.join;
+    return cudaSuccess;
+}
+
 gma_status check_forward_args(const gma_desc *desc, const void *Qx, const void *Kx, const void *V,
                               const float *mu, const float *rho, const float *pi_logits, float eps,
                               int causal, void *out, void *workspace) {
@@ -234,6 +266,93 @@ gma_status gma_forward(const gma_desc *desc, const void *Qx, const void *Kx, con
                        void *stream) {
     return gma_forward_ex(desc, Qx, Kx, V, mu, rho, pi_logits, eps, causal, out, workspace,
                           workspace_bytes, stream, nullptr, 0);
+}
+
+gma_status gma_forward_multi_workspace_size(const gma_forward_call *calls, int n_calls, size_t *bytes,
+                                            size_t *offsets) {
+    if (!bytes || n_calls < 0 || (n_calls > 0 && !calls)) return GMA_ERR_INVALID_ARG;
+    size_t off = 0;
+    for (int i = 0; i < n_calls; ++i) {
+        if (calls[i].causal != 0 && calls[i].causal != 1) return GMA_ERR_INVALID_ARG;
+        size_t b = 0;
+        const gma_status st = gma_workspace_size(&calls[i].desc, calls[i].causal, &b);
+        if (st != GMA_OK) return st;
+        if (offsets) offsets[i] = off;
+        off += align_up(std::max(b, kHeaderBytes));
+    }
+    *bytes = off;
+    return GMA_OK;
+}
+
+gma_status gma_forward_multi(const gma_forward_call *calls, int n_calls, void *workspace, size_t workspace_bytes,
+                             void *stream, void *aux_stream) {
+    std::vector<size_t> off(n_calls > 0 ? n_calls : 1);
+    size_t need = 0;
+    gma_status st = gma_forward_multi_workspace_size(calls, n_calls, &need, off.data());
+    if (st != GMA_OK) return st;
+    if (n_calls == 0) return GMA_OK;
+    if (!workspace || workspace_bytes < need) return GMA_ERR_WORKSPACE;
+    char *base = static_cast<char *>(workspace);
+    for (int i = 0; i < n_calls; ++i) {
+        const gma_forward_call &c = calls[i];
+        st = check_forward_args(&c.desc, c.Qx, c.Kx, c.V, c.mu, c.rho, c.pi_logits, c.eps, c.causal, c.out,
+                                base + off[i]);
+        if (st != GMA_OK) return st;
+        if (c.n_events < 0 || (c.n_events > 0 && !c.events)) return GMA_ERR_INVALID_ARG;
+    }
+    // Which calls run as one CTA per head, and how many SMs those hold at once (the calls
+    // of the auxiliary lane run one after another).
+    std::vector<Problem> prob(n_calls);
+    std::vector<char> per_head(n_calls, 0);
+    int held = 0, n_head = 0, n_rest = 0;
+    for (int i = 0; i < n_calls; ++i) {
+        const gma_forward_call &c = calls[i];
+        prob[i] = make_problem(&c.desc, c.causal, c.eps);
+        Plan probe;
+        st = build_forward_plan(prob[i], nullptr, probe);
+        if (st != GMA_OK) return st;
+        if (prob[i].N == 0) continue;
+        per_head[i] = probe.n == 1 && std::strcmp(probe.step[0].name, "tc_causal") == 0;
+        if (per_head[i]) { held = std::max(held, prob[i].G); ++n_head; } else { ++n_rest; }
+    }
+    int nsm = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess)
+        return GMA_ERR_CUDA;
+    const bool side_by_side = aux_stream && n_head > 0 && n_rest > 0 && nsm - held >= nsm / 8;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t aux = static_cast<cudaStream_t>(aux_stream);
+    std::vector<Plan> plans(n_calls);
+    for (int i = 0; i < n_calls; ++i) {
+        const gma_forward_call &c = calls[i];
+        if (side_by_side && !per_head[i]) prob[i].sm_budget = nsm - held;
+        const Args a{c.Qx, c.Kx, c.V, c.mu, c.rho, c.pi_logits, c.out, base + off[i]};
+        st = build_forward_plan(prob[i], &a, plans[i]);
+        if (st != GMA_OK) return st;
+    }
+    if (!side_by_side) {
+        for (int i = 0; i < n_calls; ++i) {
+            if (prob[i].N == 0) continue;
+            st = run_plan(plans[i], s, calls[i].events, calls[i].n_events);
+            if (st != GMA_OK) return st;
+        }
+        return GMA_OK;
+    }
+    // Fork: aux_stream starts after the work queued on `stream`.  The per-head scans are
+    // enqueued first, so that their CTAs take their SMs before the other calls' grids
+    // spread over the rest.  Join: `stream` waits for aux_stream.
+    cudaEvent_t fork = nullptr, join = nullptr;
+    if (lane_events(dev, fork, join) != cudaSuccess) return GMA_ERR_CUDA;
+    st = GMA_OK;
+    if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(aux, fork, 0) != cudaSuccess) st = GMA_ERR_CUDA;
+    for (int i = 0; i < n_calls && st == GMA_OK; ++i)
+        if (per_head[i]) st = run_plan(plans[i], aux, calls[i].events, calls[i].n_events);
+    for (int i = 0; i < n_calls && st == GMA_OK; ++i)
+        if (!per_head[i] && prob[i].N > 0) st = run_plan(plans[i], s, calls[i].events, calls[i].n_events);
+    // the join is enqueued even after a failed launch, so that `stream` never runs ahead of aux_stream
+    if (cudaEventRecord(join, aux) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
+        st = GMA_ERR_CUDA;
+    return st;
 }
 
 gma_status gma_cross_workspace_size(const gma_desc *desc, int Nkv, size_t *bytes) {

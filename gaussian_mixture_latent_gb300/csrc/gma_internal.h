@@ -40,6 +40,8 @@ struct Problem {
     float eps;
     int causal;
     int chunk;
+    int sm_budget;               // > 0: SMs the call's persistent write kernel may use (a concurrent
+                                 // kernel holds the rest); 0: all of them
 };
 
 // ----- workspace carving (byte offsets from the workspace base) -----
@@ -62,6 +64,7 @@ cudaError_t set_dyn_smem(const void *kern, int bytes);
 constexpr int kMaxCtas = 256;        // upper bound on persistent CTAs (partial slots are sized for it)
 struct TcLayout {
     size_t params, part, mem, total;   // workspace byte offsets
+    size_t claim;                      // the read's unit counter (bidirectional path)
     size_t stats, pnum, pden;          // component-sliced causal path: row statistics, partials
     int ns, nt;                        // component slices and value slices of 64
     uint32_t param_stride, mem_stride;
@@ -76,9 +79,10 @@ cudaError_t tc_write(const Problem &p, const TcLayout &L, const void *Kx, const 
                      cudaStream_t s);
 cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s);
 // the same over the partial slots at workspace offset `part` into the operand at `mem`,
-// and (mem_lo != 0) its bf16 rounding remainder at `mem_lo`
+// and (mem_lo != 0) its bf16 rounding remainder at `mem_lo`; with claim != 0 it also
+// zeroes the read kernel's unit counter at that offset
 cudaError_t tc_reduce_split(const Problem &p, const TcLayout &L, size_t part, size_t mem, size_t mem_lo, char *ws,
-                            cudaStream_t s);
+                            cudaStream_t s, size_t claim = 0);
 cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,
                     cudaStream_t s);
 

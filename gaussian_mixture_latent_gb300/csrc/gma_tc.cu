@@ -74,6 +74,7 @@ struct TcArgs {
     float eps;
     unsigned *status;
     int nslots;              // partial slots in the workspace (index checks of the debug build)
+    int *claim;              // the read's unit counter (zeroed by tc_reduce)
 };
 
 __device__ __forceinline__ void cta_range(int Ttot, int &t0, int &t1) {
@@ -400,8 +401,12 @@ constexpr int kReduceThreads = 256;
 __global__ void __launch_bounds__(kReduceThreads) tc_reduce_kernel(int K, int T, int Ttot, int ncta,
                                                                    const float *__restrict__ partials,
                                                                    uint8_t *__restrict__ mem, uint8_t *__restrict__ mem_lo,
-                                                                   uint32_t mem_stride, int nslots, unsigned *status) {
+                                                                   uint32_t mem_stride, int nslots, int *claim,
+                                                                   unsigned *status) {
     grid_dep_launch();
+    // the read kernel that follows claims its tile units from this counter once this grid
+    // has completed; the read before it completed before this call's first kernel started
+    if (claim && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *claim = 0;
     const int g = blockIdx.y;
     const int q = blockIdx.x * blockDim.x + threadIdx.x;   // float4 index in the 80 x K operand
     // CTA c owns tiles [c*Ttot/ncta, (c+1)*Ttot/ncta): those meeting [g*T, (g+1)*T) are
@@ -455,6 +460,24 @@ __global__ void __launch_bounds__(kReduceThreads) tc_reduce_kernel(int K, int T,
 }
 
 // ------------------------------------------------------------------ tc_read
+//
+// The read takes its tiles dynamically.  The (head, tile) list is cut into units of
+// up to kReadUnit consecutive tiles of one head; each CTA's producer claims the next
+// unit from a counter in the workspace (tc_reduce zeroes it), so a CTA that starts
+// late, on an SM that another kernel held until then, takes fewer units, and every
+// SM that frees up joins in.  Each unit is a segment of its own: the producer loads
+// its head's parameter block and memory operand into one of two buffers.  The other
+// roles learn each tile's (head, tile, segment, flags) from a ring in shared memory
+// that the producer fills before the tile's full barrier completes; after the last
+// unit it posts one end marker per compute group, and the first marker's group
+// passes the end on to the two MMA issuers through its own barriers.
+
+constexpr int kReadUnit = 4;                   // tiles per claimed unit
+constexpr int kInfoRing = 16;                  // tile-info entries (>= X stages + compute groups)
+enum : int { kTileFirst = 1, kTileLast = 2, kTileEnd = 4, kTileEndFirst = 8 };
+struct TileInfo {
+    int g, j, seg, flags;
+};
 
 template <int K>
 struct ReadCfg {
@@ -469,7 +492,8 @@ struct ReadCfg {
     static constexpr uint32_t OFF_P = OFF_O + NW * kTileBytes;
     static constexpr uint32_t OFF_M = OFF_P + PN * PB;
     static constexpr uint32_t OFF_CA = OFF_M + PN * MB;                // constant [1, 1, 0...] A block
-    static constexpr uint32_t OFF_BAR = OFF_CA + kConstABytes;
+    static constexpr uint32_t OFF_INFO = OFF_CA + kConstABytes;        // tile-info ring
+    static constexpr uint32_t OFF_BAR = OFF_INFO + kInfoRing * sizeof(TileInfo);
     static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int NOUT = 80;                                    // [Vt | Z | 1 | 0...]
@@ -477,6 +501,10 @@ struct ReadCfg {
     static constexpr uint32_t col_a(int w) { return w * wg_cols; }     // A operand, later D2 (same columns)
     static constexpr uint32_t col_d1(int w) { return w * wg_cols + NOUT; }
     static_assert(BYTES <= 232448 && NW * wg_cols <= TMEM_COLS, "read kernel exceeds shared memory or TMEM");
+    // An entry is rewritten only after the tile kInfoRing places earlier has passed its
+    // read MMA: the producer waits for tile i - SX's conversion, which follows the
+    // epilogue (hence the read MMA) of tile i - SX - NW.
+    static_assert(kInfoRing >= SX + NW, "tile-info ring shorter than the tiles in flight");
 };
 
 template <int K>
@@ -493,12 +521,10 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint64_t *fin1 = w_empty + PN, *fin2 = fin1 + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    TileInfo *info = reinterpret_cast<TileInfo *>(sm + C::OFF_INFO);
 
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int t0, t1;
-    cta_range(A.Ttot, t0, t1);
-    const int n = t1 - t0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
@@ -520,93 +546,75 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const Abort ab{abort_flag, A.status};
 
     if (warp == kWarpProducer) {
-        if (lane == 0 && n > 0) {
-            TileCursor cx(t0, n, A.T, 0, 1);
-            // the first head's query tiles do not depend on the previous kernel
-            for (; cx.valid() && cx.hl == 0 && cx.i < SX; cx.next()) {
-                mbar_arrive_expect_tx(&xfull[cx.i], kTileBytes);
-                tma_load_3d(sm + C::OFF_X + cx.i * kTileBytes, &tm_q, &xfull[cx.i], 0, cx.j * TM, cx.g);
-            }
-            grid_dep_wait();                               // parameter blocks and read operands are written
-            {
-                const int g0 = t0 / A.T;
-                mbar_arrive_expect_tx(&w_full[0], param_bytes(K) + mem_bytes(K));
-                bulk_load(sm + C::OFF_P, A.params + (size_t)(g0 % A.H) * A.param_stride, param_bytes(K), &w_full[0]);
-                bulk_load(sm + C::OFF_M, A.mem + (size_t)g0 * A.mem_stride, mem_bytes(K), &w_full[0]);
-            }
-            int p_loaded = 0;
-            long long last = now_ns();
-            while (cx.valid() && !*abort_flag) {
-                bool progress = false;
-                const int xi = cx.i;
-                bool can = true;
-                if (cx.hl > p_loaded) {
-                    const int b = cx.hl % PN;
-                    if (cx.hl >= PN && !mbar_test(&w_empty[b], ((cx.hl / PN) - 1) & 1)) can = false;
-                    else {
-                        mbar_arrive_expect_tx(&w_full[b], param_bytes(K) + mem_bytes(K));
-                        bulk_load(sm + C::OFF_P + b * C::PB, A.params + (size_t)(cx.g % A.H) * A.param_stride,
-                                  param_bytes(K), &w_full[b]);
-                        (void)GMA_IN_BOUNDS(cx.g < A.G, A.status);
-                        bulk_load(sm + C::OFF_M + b * C::MB, A.mem + (size_t)cx.g * A.mem_stride, mem_bytes(K),
-                                  &w_full[b]);
-                        p_loaded = cx.hl;
-                        progress = true;
-                    }
-                }
-                if (can && (xi < SX || mbar_test(&xempty[xi % SX], ((xi / SX) - 1) & 1))) {
-                    mbar_arrive_expect_tx(&xfull[xi % SX], kTileBytes);
-                    tma_load_3d(sm + C::OFF_X + (xi % SX) * kTileBytes, &tm_q, &xfull[xi % SX], 0, cx.j * TM, cx.g);
-                    cx.next();
-                    progress = true;
-                }
-                if (progress) {
-                    last = now_ns();
-                } else {
-                    __nanosleep(64);                       // nothing to issue: yield the issue slots
-                    if (now_ns() - last > kWaitLimitNs) {
-                        *abort_flag = 1;
-                        atomicOr(A.status, kDevErrTimeout);
-                    }
+        if (lane == 0) {
+            const int uph = (A.T + kReadUnit - 1) / kReadUnit;      // units per head
+            const int nunits = A.G * uph;
+            grid_dep_wait();             // parameter blocks, memory operands and the zeroed unit counter
+            int i = 0, nseg = 0;         // tiles (and end markers) issued, segments started
+            bool ok = true;
+            while (ok && !*abort_flag) {
+                const int u = atomicAdd(A.claim, 1);
+                if (u >= nunits) break;
+                const int g = u / uph, ja = (u - g * uph) * kReadUnit, jb = min(ja + kReadUnit, A.T);
+                const int b = nseg % PN;
+                if (nseg >= PN && !(ok = mbar_wait(&w_empty[b], ((nseg / PN) - 1) & 1, ab, kDevErrTimeout))) break;
+                mbar_arrive_expect_tx(&w_full[b], param_bytes(K) + mem_bytes(K));
+                bulk_load(sm + C::OFF_P + b * C::PB, A.params + (size_t)(g % A.H) * A.param_stride, param_bytes(K),
+                          &w_full[b]);
+                (void)GMA_IN_BOUNDS(g < A.G, A.status);
+                bulk_load(sm + C::OFF_M + b * C::MB, A.mem + (size_t)g * A.mem_stride, mem_bytes(K), &w_full[b]);
+                const int seg = nseg++;
+                for (int j = ja; j < jb; ++j, ++i) {
+                    if (i >= SX && !(ok = mbar_wait(&xempty[i % SX], ((i / SX) - 1) & 1, ab, kDevErrTimeout))) break;
+                    info[i % kInfoRing] = TileInfo{g, j, seg, (j == ja ? kTileFirst : 0) | (j == jb - 1 ? kTileLast : 0)};
+                    mbar_arrive_expect_tx(&xfull[i % SX], kTileBytes);
+                    tma_load_3d(sm + C::OFF_X + (i % SX) * kTileBytes, &tm_q, &xfull[i % SX], 0, j * TM, g);
                 }
             }
-            wind_down_ring(xfull, SX, cx.i < n ? cx.i : n, A.status);
-            for (int hl = p_loaded - PN + 1 < 0 ? 0 : p_loaded - PN + 1; hl <= p_loaded; ++hl)
-                wait_ignoring_abort(&w_full[hl % PN], (hl / PN) & 1, A.status);
+            for (int k = 0; k < NW && ok; ++k, ++i) {
+                if (i >= SX && !(ok = mbar_wait(&xempty[i % SX], ((i / SX) - 1) & 1, ab, kDevErrTimeout))) break;
+                info[i % kInfoRing] = TileInfo{0, 0, 0, kTileEnd | (k == 0 ? kTileEndFirst : 0)};
+                mbar_arrive(&xfull[i % SX]);
+            }
+            wind_down_ring(xfull, SX, i, A.status);
+            for (int s = nseg - PN < 0 ? 0 : nseg - PN; s < nseg; ++s)
+                wait_ignoring_abort(&w_full[s % PN], (s / PN) & 1, A.status);
         }
     } else if (warp == kWarpMma1) {
-        if (n > 0) {                                 // the whole warp, converged
-            for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
-                const int i = c.i, b = c.hl % PN, w = i % NW;
-                if (c.first() && !mbar_wait_warp(&w_full[b], (c.hl / PN) & 1, ab, kDevErrTimeout)) break;
-                if (!mbar_wait_warp(&a_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
-                tc_fence_after();
-                issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
-                                    smem_u32(sm + C::OFF_CA));
-                mma_commit(&d1_full[w]);
-            }
-            mma_commit(fin1);
-            wait_ignoring_abort(fin1, 0, A.status);
+        for (int i = 0;; ++i) {                      // the whole warp, converged
+            const int w = i % NW;
+            if (!mbar_wait_warp(&a_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
+            const TileInfo t = info[i % kInfoRing];
+            if (t.flags & kTileEnd) break;
+            const int b = t.seg % PN;
+            if ((t.flags & kTileFirst) && !mbar_wait_warp(&w_full[b], (t.seg / PN) & 1, ab, kDevErrTimeout)) break;
+            tc_fence_after();
+            issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
+                                smem_u32(sm + C::OFF_CA));
+            mma_commit(&d1_full[w]);
         }
+        mma_commit(fin1);
+        wait_ignoring_abort(fin1, 0, A.status);
     } else if (warp == kWarpMma2) {
         // read MMAs: D2 (128 rows x 80) = e (rows x K, bf16 in TMEM) . [Vt | Z | 1 | 0] (K x 80)
-        if (n > 0) {                                 // the whole warp, converged
-            constexpr uint32_t idesc = idesc_f16(1, 1, 0, 0, TM, C::NOUT);
-            for (TileCursor c(t0, n, A.T, 0, 1); c.valid(); c.next()) {
-                const int i = c.i, b = c.hl % PN, w = i % NW;
-                if (!mbar_wait_warp(&e_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
-                tc_fence_after();
-                const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_M + b * C::MB), 16, 1024);
+        constexpr uint32_t idesc = idesc_f16(1, 1, 0, 0, TM, C::NOUT);
+        for (int i = 0;; ++i) {                      // the whole warp, converged
+            const int w = i % NW;
+            if (!mbar_wait_warp(&e_full[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
+            const TileInfo t = info[i % kInfoRing];
+            if (t.flags & kTileEnd) break;
+            const int b = t.seg % PN;
+            tc_fence_after();
+            const uint64_t bd = sdesc_sw128(smem_u32(sm + C::OFF_M + b * C::MB), 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < K / 16; ++ks)
-                    mma_ts(tmem + C::col_a(w), tmem + C::col_d1(w) + ks * 8,
-                           bd + (uint64_t)(((ks >> 2) * 80u * 128u + (ks & 3) * 32u) >> 4), idesc, ks > 0);
-                mma_commit(&d2_full[w]);
-                if (c.last()) mma_commit(&w_empty[b]);
-            }
-            mma_commit(fin2);
-            wait_ignoring_abort(fin2, 0, A.status);
+            for (int ks = 0; ks < K / 16; ++ks)
+                mma_ts(tmem + C::col_a(w), tmem + C::col_d1(w) + ks * 8,
+                       bd + (uint64_t)(((ks >> 2) * 80u * 128u + (ks & 3) * 32u) >> 4), idesc, ks > 0);
+            mma_commit(&d2_full[w]);
+            if (t.flags & kTileLast) mma_commit(&w_empty[b]);
         }
+        mma_commit(fin2);
+        wait_ignoring_abort(fin2, 0, A.status);
     } else {
         RowThread rt;
         rt.wg = (warp - kWarpCompute) >> 2;
@@ -615,18 +623,22 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         rt.wtid = threadIdx.x - kWarpCompute * 32 - rt.wg * kWgThreads;
         const int w = rt.wg;
         const bool elected = rt.wtid == 0;
-        TileCursor c(t0, n, A.T, w, NW);
-        for (; c.valid(); c.next()) {
-            const int i = c.i;
+        for (int i = w;; i += NW) {
             bool ok = mbar_wait(&xfull[i % SX], (i / SX) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
+            const TileInfo t = info[i % kInfoRing];
+            if (t.flags & kTileEnd) {
+                // the first end marker: the MMA issuers wait on this group's barriers next
+                if ((t.flags & kTileEndFirst) && elected) { mbar_arrive(&a_full[w]); mbar_arrive(&e_full[w]); }
+                break;
+            }
             convert_row(sm + C::OFF_X + (i % SX) * kTileBytes, rt.r, tmem + rt.lane_off + C::col_a(w));
             tmem_st_wait();
             tc_fence_before();
             wg_sync(rt);
             if (elected) { mbar_arrive(&a_full[w]); mbar_arrive(&xempty[i % SX]); }
             if (i < NW) grid_dep_wait();                   // the parameter blocks are written
-            const float scale = head_scale(A.params, A.param_stride, c.g % A.H, K);
+            const float scale = head_scale(A.params, A.param_stride, t.g % A.H, K);
             ok = mbar_wait(&d1_full[w], (i / NW) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
@@ -643,7 +655,6 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_before();
             wg_sync(rt);
             if (elected) mbar_arrive(&e_full[w]);
-            const int g = c.g, row0 = c.j * TM;
             // epilogue: out = num / (den + eps * sum_k e_k)
             ok = mbar_wait(&d2_full[w], (i / NW) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
@@ -674,7 +685,7 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_before();
             wg_sync(rt);
             if (elected) {
-                tma_store_3d(&tm_o, ob, 0, row0, g);
+                tma_store_3d(&tm_o, ob, 0, t.j * TM, t.g);
                 bulk_commit_group();
             }
         }
@@ -720,6 +731,7 @@ cudaError_t launch_read(const Problem &p, const TcLayout &L, const void *Qx, voi
     a.mem = reinterpret_cast<uint8_t *>(ws + L.mem); a.mem_stride = L.mem_stride;
     a.eps = p.eps;
     a.status = reinterpret_cast<unsigned *>(ws);
+    a.claim = reinterpret_cast<int *>(ws + L.claim);
     auto kern = tc_read_kernel<K>;
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), ReadCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
@@ -738,10 +750,14 @@ TcLayout tc_layout(const Problem &p) {
     L.T = (p.N + TM - 1) / TM;
     L.Ttot = L.T * p.G;
     const int nsm = sm_count();
-    L.ncta = std::max(1, std::min({nsm > 0 ? nsm : kMaxCtas, kMaxCtas, L.Ttot}));
+    const int units = p.G * ((L.T + kReadUnit - 1) / kReadUnit);
+    L.ncta = std::max(1, std::min({nsm > 0 ? nsm : kMaxCtas, kMaxCtas, units}));
     L.Tkv = (p.Nkv + TM - 1) / TM;
     L.Ttot_kv = L.Tkv * p.G;
-    L.ncta_kv = std::max(1, std::min({nsm > 0 ? nsm : kMaxCtas, kMaxCtas, L.Ttot_kv}));
+    // the write kernel's static ranges: on the SMs left free by a concurrent kernel when
+    // the call runs with an SM budget (gma_forward_multi), else on every SM
+    const int wsm = p.sm_budget > 0 && nsm > 0 ? std::min(nsm, p.sm_budget) : nsm;
+    L.ncta_kv = std::max(1, std::min({wsm > 0 ? wsm : kMaxCtas, kMaxCtas, L.Ttot_kv}));
     L.param_stride = align1k(param_bytes(p.K));
     L.mem_stride = align1k(mem_bytes(p.K));
     size_t off = kHeaderBytes;
@@ -751,6 +767,8 @@ TcLayout tc_layout(const Problem &p) {
     off = L.part + sizeof(float) * (size_t)(kMaxCtas + p.G) * (DVV + 1) * p.K;
     L.mem = align_up(off);
     off = L.mem + (size_t)p.G * L.mem_stride;
+    L.claim = align_up(off);
+    off = L.claim + 16;
     L.total = align_up(off);
     return L;
 }
@@ -788,16 +806,16 @@ cudaError_t tc_prefix(const Problem &p, const TcLayout &L, const SegTable &T, co
 }
 
 cudaError_t tc_reduce(const Problem &p, const TcLayout &L, char *ws, cudaStream_t s) {
-    return tc_reduce_split(p, L, L.part, L.mem, 0, ws, s);
+    return tc_reduce_split(p, L, L.part, L.mem, 0, ws, s, L.claim);
 }
 
 cudaError_t tc_reduce_split(const Problem &p, const TcLayout &L, size_t part, size_t mem, size_t mem_lo, char *ws,
-                            cudaStream_t s) {
+                            cudaStream_t s, size_t claim) {
     dim3 grid((20 * p.K + kReduceThreads - 1) / kReduceThreads, p.G);
     return launch_dependent(tc_reduce_kernel, grid, dim3(kReduceThreads), 0, s, p.K, L.Tkv, L.Ttot_kv, L.ncta_kv,
                             reinterpret_cast<const float *>(ws + part), reinterpret_cast<uint8_t *>(ws + mem),
                             mem_lo ? reinterpret_cast<uint8_t *>(ws + mem_lo) : nullptr, L.mem_stride, kMaxCtas + p.G,
-                            reinterpret_cast<unsigned *>(ws));
+                            claim ? reinterpret_cast<int *>(ws + claim) : nullptr, reinterpret_cast<unsigned *>(ws));
 }
 
 cudaError_t tc_read(const Problem &p, const TcLayout &L, const void *Qx, void *out, char *ws,

@@ -136,6 +136,67 @@ gma_status gma_forward_plan(const gma_desc *desc, int causal, int *n_launches, c
                             int capacity);
 
 /*
+ * Several independent forward calls in one request.  The paper's layers apply
+ * the forward of section 3.3 (Eq. 5-8) or of section 3.5 (Eq. 6b, 8b) to each
+ * head; a model that needs more than one of them at a time (a bidirectional
+ * and a causal mixer over the same batch, or several layers that do not depend
+ * on one another) can hand them over together, so that the library runs them
+ * side by side where one of them leaves SMs idle.
+ *
+ * Each call has gma_forward()'s arguments (its own inputs and output) and an
+ * optional list of CUDA events, recorded as by gma_forward_ex() on the stream
+ * where that call's kernels run.  No output may overlap any input or output of
+ * any call.
+ */
+typedef struct {
+    gma_desc desc;
+    int causal;                   /* 0 bidirectional, 1 causal                    */
+    float eps;
+    const void *Qx, *Kx, *V;
+    const float *mu, *rho, *pi_logits;
+    void *out;
+    void *const *events;          /* NULL, or n_events cudaEvent_t (as void*)     */
+    int n_events;
+} gma_forward_call;
+
+/*
+ * Workspace of gma_forward_multi(): one region per call, in call order, each
+ * 256-byte aligned and of that call's gma_workspace_size().  offsets (NULL, or
+ * n_calls entries) receives each region's byte offset; the first 4 bytes of a
+ * region are that call's device status word (gma_get_status(workspace +
+ * offsets[i], ...)).  Zero every region's first 256 bytes before the first use
+ * (zeroing the whole workspace does it); later calls keep them zero unless a
+ * device error was posted.
+ */
+gma_status gma_forward_multi_workspace_size(const gma_forward_call *calls, int n_calls, size_t *bytes,
+                                            size_t *offsets);
+
+/*
+ * Runs the calls; returns once everything is enqueued, with `stream` ordered
+ * after all of it.  Every call is validated before anything is launched; the
+ * first failing call's status is returned.
+ *
+ * Scheduling.  With aux_stream == NULL the calls run in order on `stream`,
+ * exactly as gma_forward() calls would.  Otherwise the calls that the library
+ * runs as one CTA per head (those whose gma_forward_plan() is the single launch
+ * "tc_causal": the bf16 causal scan with d = K = dv = 64 when the heads B*H
+ * fill more than half of the SMs or the sequences are short) run in order on
+ * aux_stream, and the other calls run in order on `stream`, both starting
+ * after the work already queued on `stream`.  While the scan holds one SM per
+ * head, the other calls' bidirectional tensor-core write kernels are sized to
+ * the SMs it leaves free (when that is at least an eighth of them), and their
+ * read kernels take tiles dynamically, so that they spread over every SM once
+ * the scan has finished.  Such a call's key-side memory is then summed from
+ * partial sums over different row ranges than gma_forward() would use: its
+ * output can differ from gma_forward()'s in the last bits (both are fixed-order
+ * sums; repeated calls with the same arguments on the same GPU give identical
+ * results).  Causal calls, and every call when no scan is among them, give
+ * exactly gma_forward()'s results.
+ */
+gma_status gma_forward_multi(const gma_forward_call *calls, int n_calls, void *workspace, size_t workspace_bytes,
+                             void *stream, void *aux_stream);
+
+/*
  * Responsibilities of the rows of X [B, H, N, d] (section 3.2, Eq. 3, in the
  * softmax form of Eq. 16 / 3b), written as float32 to gamma_out [B, H, N, K].
  * A diagnostic export: the forward never writes Gamma to memory.  Needs the

@@ -180,3 +180,50 @@ def test_project_rejects_bad_arguments_before_launching(lib):
     assert call(wsb=16) == 3
     assert call(desc=(0, 300, 128, 3, 64, 64), X=None) == 0  # B = 0: nothing to do
     assert call(desc=(2, 0, 128, 3, 64, 64), X=None) == 0    # N = 0: nothing to do
+
+
+def test_forward_multi_sizes_regions_and_rejects_bad_arguments_before_launching(lib):
+    import gaussian_mixture_latent_gb300 as gma
+    p = 4096                       # never dereferenced: every failing case fails validation first
+    calls = (gma.gma_forward_call * 3)()
+    descs = (_desc(), _desc(d=64, K=64, dv=64), _desc(N=0))
+    for k, (dsc, causal) in enumerate(zip(descs, (0, 1, 0))):
+        calls[k].desc = dsc
+        calls[k].causal = causal
+        calls[k].eps = 1e-6
+        for name in ("Qx", "Kx", "V", "mu", "rho", "pi_logits", "out"):
+            setattr(calls[k], name, p)
+    n, offs = ctypes.c_size_t(0), (ctypes.c_size_t * 3)()
+    assert lib.gma_forward_multi_workspace_size(calls, 3, ctypes.byref(n), offs) == 0
+    # one 256-byte aligned region per call, in order, each of the call's own workspace size
+    sizes = []
+    for k in range(3):
+        b = ctypes.c_size_t(0)
+        assert lib.gma_workspace_size(ctypes.byref(descs[k]), calls[k].causal, ctypes.byref(b)) == 0
+        sizes.append((b.value + 255) // 256 * 256)
+    assert list(offs) == [0, sizes[0], sizes[0] + sizes[1]] and n.value == sum(sizes)
+    assert lib.gma_forward_multi_workspace_size(calls, 3, ctypes.byref(n), None) == 0
+    assert lib.gma_forward_multi_workspace_size(calls, 3, None, None) == 1
+    assert lib.gma_forward_multi_workspace_size(None, 2, ctypes.byref(n), None) == 1
+    assert lib.gma_forward_multi_workspace_size(calls, -1, ctypes.byref(n), None) == 1
+    total = n.value
+    f = lib.gma_forward_multi
+    assert f(calls, 0, None, 0, None, None) == 0            # nothing to do
+    assert f(calls, 3, p, total - 1, None, None) == 3       # workspace too small
+    assert f(calls, 3, None, total, None, None) == 3
+    calls[1].causal = 2
+    assert f(calls, 3, p, total, None, None) == 1
+    calls[1].causal = 1
+    calls[0].Qx = None
+    assert f(calls, 3, p, total, None, None) == 1
+    calls[0].Qx = 4100                                       # not 16-byte aligned
+    assert f(calls, 3, p, total, None, None) == 1
+    calls[0].Qx = p
+    calls[2].n_events = 2                                    # events missing
+    assert f(calls, 3, p, total, None, None) == 1
+    calls[2].n_events = 0
+    calls[0].eps = -1.0
+    assert f(calls, 3, p, total, None, None) == 1
+    calls[0].eps = 1e-6
+    calls[1].desc = _desc(K=0)
+    assert f(calls, 3, p, total, None, None) == 1
