@@ -392,7 +392,7 @@ def gma_forward_cross(Qx, Ky, Vy, mu, rho, pi_logits, eps: float = 1e-6, var_flo
 
 
 def gma_backward(Qx, Kx, V, mu, rho, pi_logits, dO, eps: float = 1e-6, var_floor: float = 1e-4, causal=False,
-                 grads=None, workspace=None, stream=None, check_status: bool = False):
+                 grads=None, workspace=None, stream=None, check_status: bool = False, chunk: int = 0):
     """Backward pass (section 4.1, Eqs. 17-20): given dO = dL/dO [B,H,N,dv] of the forward
     gma_forward(Qx, Kx, V, mu, rho, pi_logits), returns the float32 gradients
     (dQx, dKx, dV, dmu, drho, dpi_logits); parameter gradients are summed over the batch.
@@ -415,7 +415,7 @@ def gma_backward(Qx, Kx, V, mu, rho, pi_logits, dO, eps: float = 1e-6, var_floor
     shapes = ((B, H, N, d), (B, H, N, d), (B, H, N, dv), (H, K, d), (H, K, d), (H, K))
     for t, shp, name in zip(grads, shapes, ("dQx", "dKx", "dV", "dmu", "drho", "dpi_logits")):
         _check(t, name, shp, (torch.float32,))
-    desc = _make_desc(B, H, N, d, K, dv, Qx.dtype, Qx.dtype, var_floor, 0)
+    desc = _make_desc(B, H, N, d, K, dv, Qx.dtype, Qx.dtype, var_floor, chunk)
     nbytes = ctypes.c_size_t(0)
     rc = _load().gma_backward_workspace_size(ctypes.byref(desc), int(bool(causal)), ctypes.byref(nbytes))
     if rc:

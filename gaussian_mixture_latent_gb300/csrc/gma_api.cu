@@ -205,6 +205,18 @@ cudaError_t lane_events(int dev, cudaEvent_t &fork, cudaEvent_t &join) {
     return cudaSuccess;
 }
 
+// The backward's path for a problem: the tensor-core passes (bidirectional bf16,
+// d = dv = K = 64, more than one 128-row tile), the CUDA-core kernels specialised to
+// d = dv = K = 64 (causal with their 64-row tiles), or the general CUDA-core path.
+enum class BwdPath { kNone, kTensor, kSimt64, kGeneral };
+
+BwdPath backward_path(const Problem &p) {
+    if (p.out_dtype != p.in_dtype) return BwdPath::kNone;
+    if (bwd_tc_supported(p)) return BwdPath::kTensor;
+    if (bwd_supported(p) && (!p.causal || p.chunk == 0 || p.chunk == kBwdChunkRows)) return BwdPath::kSimt64;
+    return gb_supported(p) ? BwdPath::kGeneral : BwdPath::kNone;
+}
+
 gma_status check_forward_args(const gma_desc *desc, const void *Qx, const void *Kx, const void *V,
                               const float *mu, const float *rho, const float *pi_logits, float eps,
                               int causal, void *out, void *workspace) {
@@ -399,10 +411,12 @@ gma_status gma_backward_workspace_size(const gma_desc *desc, int causal, size_t 
     if (st != GMA_OK) return st;
     if (!bytes || causal < 0 || causal > 1) return GMA_ERR_INVALID_ARG;
     const Problem p = make_problem(desc, causal, 0.f);
-    if (!bwd_supported(p) || p.out_dtype != p.in_dtype) return GMA_ERR_UNSUPPORTED;
-    if (p.causal && p.chunk != 0 && p.chunk != kBwdChunkRows) return GMA_ERR_UNSUPPORTED;
-    *bytes = bwd_tc_supported(p) ? bwd_tc_layout(p).total : bwd_layout(p).total;
-    return GMA_OK;
+    switch (backward_path(p)) {
+        case BwdPath::kTensor: *bytes = bwd_tc_layout(p).total; return GMA_OK;
+        case BwdPath::kSimt64: *bytes = bwd_layout(p).total; return GMA_OK;
+        case BwdPath::kGeneral: *bytes = gb_layout(p).total; return GMA_OK;
+        default: return GMA_ERR_UNSUPPORTED;
+    }
 }
 
 gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const void *Kx, const void *V,
@@ -418,11 +432,10 @@ gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const 
     for (const void *q : ptrs)
         if (q && !aligned16(q)) return GMA_ERR_INVALID_ARG;
     const Problem p = make_problem(desc, causal, eps);
-    if (!bwd_supported(p) || p.out_dtype != p.in_dtype) return GMA_ERR_UNSUPPORTED;
-    if (p.causal && p.chunk != 0 && p.chunk != kBwdChunkRows) return GMA_ERR_UNSUPPORTED;
-    // bidirectional bf16: the tensor-core passes; fp32 inputs and the causal form: CUDA cores
-    const bool tc = bwd_tc_supported(p);
-    const size_t need = tc ? bwd_tc_layout(p).total : bwd_layout(p).total;
+    const BwdPath path = backward_path(p);
+    if (path == BwdPath::kNone) return GMA_ERR_UNSUPPORTED;
+    const size_t need = path == BwdPath::kTensor ? bwd_tc_layout(p).total
+                      : path == BwdPath::kSimt64 ? bwd_layout(p).total : gb_layout(p).total;
     if (!workspace || workspace_bytes < need) return GMA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p.N == 0) {     // the loss does not depend on the parameters
@@ -434,8 +447,12 @@ gma_status gma_backward(const gma_desc *desc, int causal, const void *Qx, const 
     }
     char *ws = static_cast<char *>(workspace);
     const cudaError_t e =
-        tc ? bwd_tc_run(p, bwd_tc_layout(p), Qx, Kx, V, mu, rho, pi_logits, dO, dQx, dKx, dV, dmu, drho, dpi_logits, ws, s)
-           : bwd_run(p, bwd_layout(p), Qx, Kx, V, mu, rho, pi_logits, dO, dQx, dKx, dV, dmu, drho, dpi_logits, ws, s);
+        path == BwdPath::kTensor
+            ? bwd_tc_run(p, bwd_tc_layout(p), Qx, Kx, V, mu, rho, pi_logits, dO, dQx, dKx, dV, dmu, drho, dpi_logits,
+                         ws, s)
+        : path == BwdPath::kSimt64
+            ? bwd_run(p, bwd_layout(p), Qx, Kx, V, mu, rho, pi_logits, dO, dQx, dKx, dV, dmu, drho, dpi_logits, ws, s)
+            : gb_run(p, gb_layout(p), Qx, Kx, V, mu, rho, pi_logits, dO, dQx, dKx, dV, dmu, drho, dpi_logits, ws, s);
     return e == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 

@@ -135,6 +135,22 @@ cudaError_t tc_diag(const Problem &p, const TcLayout &L, const void *Qx, int *z,
 cudaError_t tc_diag_finalize(const Problem &p, const TcLayout &L, float *p_out, float *stats_out, char *ws,
                              cudaStream_t s);
 
+// ----- backward pass for every other shape (d, K, dv <= 256), CUDA cores, fp32: gma_bwd_simt.cu -----
+struct GbLayout {
+    size_t lam, cdir, lmu;           // lambda, the direction constants, [lambda mu | lambda] per head
+    size_t gq, gk, dsq, dsk;         // [G][N][K]: responsibilities and score gradients of both sides
+    size_t t, ab;                    // [G][N][max(dv + 1, 2 d)] products; [G][N][dv + 1] = [a | b]
+    size_t part, mem, memr;          // [G][P][K][dv + 1]: range partials; memory; [R | r]
+    size_t pq, pk;                   // [G][P][K][2 d + 1]: parameter sums per range of each side
+    size_t total;
+    int P, rpp, C;                   // row ranges, rows per range, causal chunk rows
+};
+bool gb_supported(const Problem &p);
+GbLayout gb_layout(const Problem &p);
+cudaError_t gb_run(const Problem &p, const GbLayout &L, const void *Qx, const void *Kx, const void *V,
+                   const float *mu, const float *rho, const float *alpha, const void *dO, float *dQx, float *dKx,
+                   float *dV, float *dmu, float *drho, float *dalpha, char *ws, cudaStream_t s);
+
 // ----- backward pass, bidirectional and causal, CUDA cores: gma_bwd.cu (uses simt_params) -----
 struct BwdLayout {
     size_t lam, cdir;            // parameter prologue outputs

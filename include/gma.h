@@ -81,7 +81,10 @@ typedef struct {
  *     per-chunk tiles fit one CTA's shared memory (4 (K (dv + 1) + 2 chunk K
  *     + 2 chunk (dv + 1) + chunk^2) bytes <= 227 KB); larger values return
  *     GMA_ERR_UNSUPPORTED.  0 selects 16.
- *   - gma_backward with causal = 1: 64-row tiles; chunk must be 0 or 64.
+ *   - gma_backward with causal = 1: at d = dv = K = 64, chunk 0 or 64 takes the
+ *     64-row tiles of that shape's kernels; any other chunk, and every other
+ *     shape, takes the general path's chunks of chunk rows (0 selects 16) within
+ *     its shared-memory bound (see gma_backward), GMA_ERR_UNSUPPORTED beyond.
  *   - bidirectional calls, decode, cross-attention and diagnostics have no
  *     chunked scan and ignore the field.
  * A negative chunk is GMA_ERR_INVALID_ARG everywhere.
@@ -223,14 +226,25 @@ gma_status gma_selftest_timeout(void *workspace, size_t workspace_bytes, void *s
  *   dQx, dKx [B, H, N, d], dV [B, H, N, dv]          (float32)
  *   dmu, drho [H, K, d], dpi_logits [H, K]            (float32, summed over the batch)
  * every output overwritten, not accumulated.  Qx, Kx, V in desc->in_dtype and
- * dO in desc->out_dtype, which must be the same type.  Responsibilities and
- * every product in fp32 on the CUDA cores; deterministic (fixed-order
- * reductions).  causal = 1 differentiates the prefix memories of Eq. 6b / 8b
- * (each key collects the gradient of the rows at or after it).  Implemented for
- * d = dv = K = 64; GMA_ERR_UNSUPPORTED otherwise.  N = 0 writes zero parameter
- * gradients.  Workspace: gma_backward_workspace_size() (it holds Gamma^K of
- * every row, 256 B per row of a head; the causal one also a | b, Gamma^Q and ds,
- * about 1.3 KB per row in all).
+ * dO in desc->out_dtype, which must be the same type.  Deterministic
+ * (fixed-order reductions).  causal = 1 differentiates the prefix memories of
+ * Eq. 6b / 8b (each key collects the gradient of the rows at or after it).
+ * Three paths, by shape:
+ *   - bidirectional, bf16, d = dv = K = 64, N > 128: tensor cores (bf16
+ *     operands, the two memory operands as two bf16 terms, fp32 accumulation,
+ *     softmax and epilogues);
+ *   - d = dv = K = 64 otherwise (fp32 inputs, one-tile heads, the causal form
+ *     with chunk 0 or 64): CUDA cores in fp32 over 64-row tiles;
+ *   - every other shape (d, K, dv up to 256): CUDA cores in fp32 over the
+ *     responsibilities of every row; the causal form in chunks of desc->chunk
+ *     rows (0 selects 16) while 4 (K (dv + 1) + 3 C K + 2 C (dv + 1) + C dv +
+ *     2 C^2) bytes (C the chunk) fit a CTA's 227 KB of shared memory, and
+ *     GMA_ERR_UNSUPPORTED beyond.
+ * N = 0 writes zero parameter gradients.  Workspace:
+ * gma_backward_workspace_size() (the first two paths hold Gamma^K of every row,
+ * 256 B per row of a head, the causal one also a | b, Gamma^Q and ds, about
+ * 1.3 KB per row in all; the third 4 (4 K + 2 (dv + 1) + max(dv + 1, 2 d))
+ * bytes per row and the partial sums).
  * Errors as for gma_forward().
  */
 gma_status gma_backward_workspace_size(const gma_desc *desc, int causal, size_t *bytes);

@@ -95,7 +95,10 @@ def test_backward_and_decode_reject_bad_arguments_before_launching(lib):
     bidir = n.value
     assert lib.gma_backward_workspace_size(ctypes.byref(ok), 1, ctypes.byref(n)) == 0 and n.value > bidir
     assert lib.gma_backward_workspace_size(ctypes.byref(ok), 2, ctypes.byref(n)) == 1
-    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(d=64, K=128, dv=64)), 0, ctypes.byref(n)) == 2
+    # every other shape takes the general path, except a causal state beyond shared memory
+    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(d=64, K=128, dv=64)), 0, ctypes.byref(n)) == 0
+    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(d=64, K=256, dv=256)), 0, ctypes.byref(n)) == 0
+    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(d=64, K=256, dv=256)), 1, ctypes.byref(n)) == 2
     assert lib.gma_backward_workspace_size(ctypes.byref(_desc(d=64, K=64, dv=64, out_dtype=0)), 0,
                                            ctypes.byref(n)) == 2
     p = ctypes.c_void_p(4096)
@@ -109,7 +112,7 @@ def test_backward_and_decode_reject_bad_arguments_before_launching(lib):
     assert b(*args(Q=None)) == 1
     assert b(*args(dO=odd)) == 1
     assert b(*args(dmu=None)) == 1
-    assert b(*args(desc=_desc(d=64, K=128, dv=64))) == 2
+    assert b(*args(desc=_desc(d=64, K=256, dv=256), causal=1)) == 2
     assert b(*args(ws=None)) == 3
     assert b(*args(wsb=16)) == 3
     assert lib.gma_decode_workspace_size(ctypes.byref(ok), ctypes.byref(n)) == 0
@@ -149,10 +152,17 @@ def test_chunk_is_honoured_or_refused(lib):
     assert ws(1, chunk=-1, **f32) == 1
     assert lib.gma_forward_plan(ctypes.byref(_desc(chunk=64, **f32)), 1, ctypes.byref(cnt), names, 16) == 0
     assert [names[i].decode() for i in range(cnt.value)][-1] == "simt_causal_chunk"
+    # the backward: 64-row tiles at d = dv = K = 64 (chunk 0 or 64), the general path's chunk
+    # otherwise while its tiles fit shared memory
+    bws = lambda causal, **kw: lib.gma_backward_workspace_size(ctypes.byref(_desc(**kw)), causal, ctypes.byref(n))
     bw = dict(d=64, K=64, dv=64)
-    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(chunk=64, **bw)), 1, ctypes.byref(n)) == 0
-    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(chunk=128, **bw)), 1, ctypes.byref(n)) == 2
-    assert lib.gma_backward_workspace_size(ctypes.byref(_desc(chunk=128, **bw)), 0, ctypes.byref(n)) == 0
+    for good in (0, 64, 16, 1, 32):
+        assert bws(1, chunk=good, **bw) == 0, good
+    assert bws(1, chunk=128, **bw) == 2
+    assert bws(0, chunk=128, **bw) == 0
+    for good in (0, 1, 16, 48):
+        assert bws(1, chunk=good, **f32) == 0, good
+    assert bws(1, chunk=4096, **f32) == 2
 
 
 def test_project_rejects_bad_arguments_before_launching(lib):

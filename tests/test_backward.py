@@ -41,8 +41,10 @@ TOL_BWD_TC = 2e-2        # bidirectional, bf16 inputs: tensor-core operands
 
 
 def tol_for(w):
-    # the tensor-core passes take bidirectional bf16 heads of more than one 128-row tile
-    return TOL_BWD_TC if (w.dtype == "bf16" and not w.causal and w.N > 128) else TOL_BWD
+    # the tensor-core passes take bidirectional bf16 heads of more than one 128-row tile at
+    # d = dv = K = 64; every other shape runs in fp32 on the CUDA cores
+    tc = w.dtype == "bf16" and not w.causal and w.N > 128 and w.d == w.K == w.dv == 64
+    return TOL_BWD_TC if tc else TOL_BWD
 NAMES = ("Qx", "Kx", "V", "mu", "omega", "alpha")
 
 
@@ -67,10 +69,17 @@ def make(B, H, N, dtype, seed, causal=False, eps=1e-6):
     return w, x
 
 
-def run_gpu(w, x):
+def make_shape(B, H, N, d, K, dv, dtype, seed, causal=False, eps=1e-6):
+    w = inputs.Workload("bwd_gen", B=B, H=H, N=N, d=d, K=K, dv=dv, dtype=dtype, causal=causal, seed=seed, eps=eps)
+    x = inputs.gen_all(w)
+    x["dO"] = gen_dO((B, H, N, dv), dtype, seed)
+    return w, x
+
+
+def run_gpu(w, x, chunk=0):
     import gaussian_mixture_latent_gb300 as gma
     g = gma.gma_backward(*(to_device(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha", "dO")), eps=w.eps,
-                         var_floor=w.var_floor, causal=w.causal)
+                         var_floor=w.var_floor, causal=w.causal, chunk=chunk)
     torch.cuda.synchronize()
     assert gma.gma_get_status() == 0
     return [t.double().cpu().numpy() for t in g]
@@ -145,6 +154,58 @@ def test_backward_parity(case):
     check(w, x, run_gpu(w, x))
 
 
+GENERAL = [
+    # the general CUDA-core path (every shape but d = dv = K = 64): B, H, N, d, K, dv, dtype, causal, chunk
+    (1, 2, 256, 16, 8, 32, "f32", False, 0),       # the small fp32 workload's shape
+    (1, 2, 256, 16, 8, 32, "f32", True, 0),
+    (2, 2, 333, 64, 128, 64, "bf16", False, 0),    # K = 128
+    (2, 2, 333, 64, 128, 64, "bf16", True, 0),
+    (1, 2, 300, 64, 256, 128, "bf16", True, 0),    # K = 256, dv = 128 (the long causal workload's shape)
+    (1, 2, 300, 64, 256, 128, "bf16", False, 0),
+    (1, 3, 257, 5, 7, 9, "f32", True, 0),          # odd sizes, ragged ranges and chunks
+    (1, 3, 257, 5, 7, 9, "f32", False, 0),
+    # one row: with eps = 1e-6 O = v for any responsibilities, the exact routing gradients are
+    # O(eps) and fp32 cannot resolve their cancellation (the paths at d = dv = K = 64 met the
+    # same); with eps = 0.5 they are O(1)
+    (1, 1, 1, 24, 40, 48, "bf16", False, 0, 0.5),
+    (1, 1, 1, 24, 40, 48, "bf16", True, 0, 0.5),
+    (2, 2, 300, 64, 64, 64, "bf16", True, 16),     # d = dv = K = 64 with a chunk of 16: the general path
+    (1, 2, 700, 32, 96, 48, "f32", True, 5),       # a chunk that does not divide the ranges
+    (4, 24, 200, 64, 128, 64, "bf16", False, 0),   # many head rows, several ranges each
+]
+
+
+@pytest.mark.parametrize("case", GENERAL, ids=[f"B{c[0]}H{c[1]}N{c[2]}d{c[3]}K{c[4]}dv{c[5]}_{c[6]}_"
+                                               f"{'causal' if c[7] else 'bidir'}{'_C%d' % c[8] if c[8] else ''}"
+                                               for c in GENERAL])
+def test_backward_general_shapes(case):
+    B, H, N, d, K, dv, dtype, causal, chunk = case[:9]
+    eps = case[9] if len(case) > 9 else 1e-6
+    w, x = make_shape(B, H, N, d, K, dv, dtype, seed=N + K, causal=causal, eps=eps)
+    got = run_gpu(w, x, chunk=chunk)
+    heads = [(b, h) for b in range(B) for h in range(H)][:8]
+    check(w, x, got, heads=heads, param_heads=list(range(min(H, 4))))
+
+
+def test_general_backward_causality_and_determinism():
+    # dO nonzero at row t only (K = 128): the exact gradient of every other query row and of
+    # every key and value row after t is zero, and the general path gives exact zeros
+    # there; a second call is bitwise equal
+    w, x = make_shape(1, 2, 300, 64, 128, 64, "bf16", seed=4, causal=True)
+    t = 141
+    dO = np.zeros_like(x["dO"])
+    dO[:, :, t] = x["dO"][:, :, t]
+    x["dO"] = dO
+    g1 = run_gpu(w, x)
+    dQ, dK, dV = g1[:3]
+    rows = np.arange(300) != t
+    assert np.abs(dQ[:, :, rows]).max() == 0.0 and np.abs(dQ[:, :, t]).max() > 0
+    assert np.abs(dK[:, :, t + 1:]).max() == 0.0 and np.abs(dV[:, :, t + 1:]).max() == 0.0
+    assert np.abs(dK[:, :, :t + 1]).max() > 0 and np.abs(dV[:, :, :t + 1]).max() > 0
+    for u, v in zip(g1, run_gpu(w, x)):
+        assert np.array_equal(u, v)
+
+
 def test_causal_backward_reaches_only_the_prefix():
     # dO nonzero at row t only: the exact gradient of every other query row, and of every key
     # and value row after t, is zero, and the kernels produce exact zeros there
@@ -181,11 +242,12 @@ def test_backward_unsupported_and_empty():
     import gaussian_mixture_latent_gb300 as gma
     w, x = make(1, 2, 100, "bf16", seed=1)
     args = [to_device(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha", "dO")]
-    w2 = inputs.Workload("k128", B=1, H=2, N=100, d=64, K=128, dv=64, dtype="bf16", causal=False)
+    # a causal state of K (dv + 1) = 256 x 257 floats does not fit a CTA's shared memory
+    w2 = inputs.Workload("k256", B=1, H=2, N=100, d=64, K=256, dv=256, dtype="bf16", causal=True)
     x2 = inputs.gen_all(w2)
     x2["dO"] = x2["V"]
     with pytest.raises(gma.GmaError) as e:
-        gma.gma_backward(*(to_device(x2[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha", "dO")))
+        gma.gma_backward(*(to_device(x2[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha", "dO")), causal=True)
     assert e.value.code == 2
     empty = [a[:, :, :0].contiguous() if a.dim() == 4 else a for a in args]
     g = gma.gma_backward(*empty)
