@@ -981,6 +981,26 @@ def bwd_flops_per_row(w):
     return mem + qry + key + 2 * rows
 
 
+def bwd_general_flops_per_row(w, C=16):
+    """fp32 flops the general backward path computes per row of one head (2 per multiply-add),
+    for shapes other than d = dv = K = 64: the responsibilities of both sides (3 flops per
+    component and coordinate), the memory, [num | den], g^Q, [R | r], g^K and dV products, dx
+    and the parameter sums; the causal walks add their chunk products (C rows, counted in
+    full) and the running-state updates in place of the bidirectional row-times-matrix tiles."""
+    K, d, dv, W = w.K, w.d, w.dv, w.dv + 1
+    common = 2 * 3 * K * d + 2 * K * W + 2 * (2 * K * 2 * d) + 2 * (2 * K * (2 * d + 1)) + 2 * K * W
+    if not w.causal:
+        return common + 2 * K * W + 2 * W * K + 2 * W * K + 2 * K * dv
+    qry = 2 * C * K + 2 * K * W + 2 * C * W + 2 * C * W + 2 * W * K + 2 * C * K + 2 * K * W
+    key = 2 * C * K + 2 * C * W + 2 * W * K + 2 * C * K + 2 * K * dv + 2 * C * dv + 2 * K * W
+    return common + qry + key
+
+
+def bwd_simt64_path(w):
+    """Whether gma_backward takes the CUDA-core kernels specialised to d = dv = K = 64."""
+    return w.d == 64 and w.dv == 64 and w.K == 64 and not bwd_tc_path(w)
+
+
 def bwd_tc_path(w):
     """Whether gma_backward takes the tensor-core passes for this workload (bidirectional,
     bf16, d = dv = K = 64, more than one 128-row tile per head)."""
@@ -1104,14 +1124,15 @@ def run_backward(args, rank, world, local):
                 "tensor": {"achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                            "frac": tflops / pk["bf16_tflops"], "flops_per_row": bwd_tc_flops_per_row(w)}}
     else:
-        flops = units * bwd_flops_per_row(w)
+        per_row = bwd_flops_per_row(w) if bwd_simt64_path(w) else bwd_general_flops_per_row(w)
+        flops = units * per_row
         alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12        # fp32 lanes x 2 flops x max SM clock, TFLOP/s
         achieved = flops / (ms / 1e3) / 1e12
-        launches = 9 if w.causal else 7
+        launches = (9 if w.causal else 7) if bwd_simt64_path(w) else (17 if w.causal else 22)
         roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
                 "frac": achieved / alu_peak, "traffic": None,
                 "kernel": f"gma_backward (whole call: {launches} launches)", "kernel_ms": ms,
-                "flops_per_row": bwd_flops_per_row(w), "peak_source": "fp32 lanes x 2 x 2070 MHz"}
+                "flops_per_row": per_row, "peak_source": "fp32 lanes x 2 x 2070 MHz"}
     cpu = None
     if not args.no_cpu_baseline:
         rate, reps, dt = bwd_oracle_sample(w, 12.0)
@@ -1124,7 +1145,8 @@ def run_backward(args, rank, world, local):
                       "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K, "dv": w.dv,
                                  "inputs": w.dtype,
                                  "step": f"{'causal' if w.causal else 'bidirectional'} backward, all gradients",
-                                 "path": "tensor-core passes" if tc else "CUDA-core passes (fp32)",
+                                 "path": "tensor-core passes" if tc else ("CUDA-core passes (fp32)" if bwd_simt64_path(w)
+                                                                          else "general CUDA-core path (fp32)"),
                                  "l2": "two alternating input sets (> 129 MB L2)", "parallelism": "single GPU"},
                       "roofline": roof,
                       "clocks": clocks, "gpu_launches": launches * steps, "cpu_baseline": cpu}),

@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
     extern __shared__ float sm[];
     const int K = a.K, dv = a.dv, W = dv + 1, C = a.C, N = a.N;
     const int p = blockIdx.x, g = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int RG = (C + 3) / 4, KG = (K + 3) / 4;       // groups of four rows, of four components
     float *S = sm, *gA = S + (size_t)K * W, *gB = gA + C * K, *gg = gB + C * K, *va = gg + C * K;
     float *ab = va + C * W, *dO = ab + C * W, *Am = dO + C * dv, *Bm = Am + C * C;
     const T *V = static_cast<const T *>(a.V), *DO = static_cast<const T *>(a.dO);
@@ -374,12 +375,24 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
             Am[e] = s;
         }
         __syncthreads();
-        for (int e = t; e < C * W; e += kGbThreads) {      // [num | den - eps] into ab
-            const int i = e / W, c = e % W;
-            float s = 0.f;
-            for (int k = 0; k < K; ++k) s = fmaf(gA[i * K + k], S[k * W + c], s);
-            for (int j = 0; j <= i; ++j) s = fmaf(Am[i * C + j], va[j * W + c], s);
-            ab[e] = s;
+        for (int e = t; e < RG * W; e += kGbThreads) {     // [num | den - eps] into ab, four rows a thread
+            const int c = e % W, i0q = (e / W) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < K; ++k) {
+                const float sv = S[k * W + c];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (i0q + q < C) acc[q] = fmaf(gA[(i0q + q) * K + k], sv, acc[q]);
+            }
+            for (int j = 0; j < C; ++j) {
+                const float v = va[j * W + c];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (j <= i0q + q && i0q + q < C) acc[q] = fmaf(Am[(i0q + q) * C + j], v, acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (i0q + q < C) ab[(i0q + q) * W + c] = acc[q];
         }
         __syncthreads();
         for (int i = warp; i < n; i += kGbThreads / 32) {  // a and b, one warp per row
@@ -401,12 +414,24 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
             Bm[e] = s;
         }
         __syncthreads();
-        for (int e = t; e < C * K; e += kGbThreads) {      // g^Q
-            const int i = e / K, k = e % K;
-            float s = 0.f;
-            for (int c = 0; c < W; ++c) s = fmaf(ab[i * W + c], S[k * W + c], s);
-            for (int j = 0; j <= i; ++j) s = fmaf(Bm[i * C + j], gB[j * K + k], s);
-            gg[e] = s;
+        for (int e = t; e < RG * K; e += kGbThreads) {     // g^Q, four rows a thread
+            const int k = e % K, i0q = (e / K) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c = 0; c < W; ++c) {
+                const float sv = S[k * W + c];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (i0q + q < C) acc[q] = fmaf(ab[(i0q + q) * W + c], sv, acc[q]);
+            }
+            for (int j = 0; j < C; ++j) {
+                const float gb = gB[j * K + k];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (j <= i0q + q && i0q + q < C) acc[q] = fmaf(Bm[(i0q + q) * C + j], gb, acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (i0q + q < C) gg[(i0q + q) * K + k] = acc[q];
         }
         __syncthreads();
         for (int i = warp; i < n; i += kGbThreads / 32) {  // ds^Q, one warp per row
@@ -415,11 +440,20 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
             s = gb_warp_sum(s);
             for (int k = lane; k < K; k += 32) a.ds[(row0 + i) * K + k] = gA[i * K + k] * (gg[i * K + k] - s);
         }
-        for (int e = t; e < K * W; e += kGbThreads) {      // the state after this chunk
-            const int k = e / W, c = e % W;
-            float s = S[e];
-            for (int j = 0; j < n; ++j) s = fmaf(gB[j * K + k], va[j * W + c], s);
-            S[e] = s;
+        for (int e = t; e < KG * W; e += kGbThreads) {     // the state after this chunk, four components a thread
+            const int c = e % W, k0q = (e / W) * 4;
+            float acc[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = k0q + q < K ? S[(k0q + q) * W + c] : 0.f;
+            for (int j = 0; j < n; ++j) {
+                const float v = va[j * W + c];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (k0q + q < K) acc[q] = fmaf(gB[j * K + k0q + q], v, acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (k0q + q < K) S[(k0q + q) * W + c] = acc[q];
         }
     }
 }
@@ -434,6 +468,7 @@ __global__ void __launch_bounds__(kGbThreads) gb_ck_kernel(GbCausalArgs a) {
     extern __shared__ float sm[];
     const int K = a.K, dv = a.dv, W = dv + 1, C = a.C, N = a.N;
     const int p = blockIdx.x, g = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int RG = (C + 3) / 4, KG = (K + 3) / 4;       // groups of four rows, of four components
     float *Rs = sm, *gQ = Rs + (size_t)K * W, *gK = gQ + C * K, *gg = gK + C * K, *va = gg + C * K;
     float *ab = va + C * W, *Am = ab + C * W + C * dv, *Bm = Am + C * C;
     const T *V = static_cast<const T *>(a.V);
@@ -468,19 +503,43 @@ __global__ void __launch_bounds__(kGbThreads) gb_ck_kernel(GbCausalArgs a) {
             Bm[e] = sb;
         }
         __syncthreads();
-        for (int e = t; e < C * K; e += kGbThreads) {      // g^K
-            const int j = e / K, k = e % K;
-            float s = 0.f;
-            for (int c = 0; c < W; ++c) s = fmaf(va[j * W + c], Rs[k * W + c], s);
-            for (int i = j; i < C; ++i) s = fmaf(Bm[i * C + j], gQ[i * K + k], s);
-            gg[e] = s;
+        for (int e = t; e < RG * K; e += kGbThreads) {     // g^K, four rows a thread
+            const int k = e % K, j0q = (e / K) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c = 0; c < W; ++c) {
+                const float rv = Rs[k * W + c];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (j0q + q < C) acc[q] = fmaf(va[(j0q + q) * W + c], rv, acc[q]);
+            }
+            for (int i = 0; i < C; ++i) {
+                const float gv = gQ[i * K + k];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (i >= j0q + q && j0q + q < C) acc[q] = fmaf(Bm[i * C + j0q + q], gv, acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (j0q + q < C) gg[(j0q + q) * K + k] = acc[q];
         }
-        for (int e = t; e < n * dv; e += kGbThreads) {     // dV
-            const int j = e / dv, v = e % dv;
-            float s = 0.f;
-            for (int k = 0; k < K; ++k) s = fmaf(gK[j * K + k], Rs[k * W + v], s);
-            for (int i = j; i < C; ++i) s = fmaf(Am[i * C + j], ab[i * W + v], s);
-            a.dV[(row0 + j) * dv + v] = s;
+        for (int e = t; e < RG * dv; e += kGbThreads) {    // dV, four rows a thread
+            const int v = e % dv, j0q = (e / dv) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < K; ++k) {
+                const float rv = Rs[k * W + v];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (j0q + q < C) acc[q] = fmaf(gK[(j0q + q) * K + k], rv, acc[q]);
+            }
+            for (int i = 0; i < C; ++i) {
+                const float av = ab[i * W + v];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (i >= j0q + q && j0q + q < C) acc[q] = fmaf(Am[i * C + j0q + q], av, acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (j0q + q < n) a.dV[(row0 + j0q + q) * dv + v] = acc[q];
         }
         __syncthreads();
         for (int j = warp; j < n; j += kGbThreads / 32) {  // ds^K, one warp per row
@@ -489,11 +548,20 @@ __global__ void __launch_bounds__(kGbThreads) gb_ck_kernel(GbCausalArgs a) {
             s = gb_warp_sum(s);
             for (int k = lane; k < K; k += 32) a.ds[(row0 + j) * K + k] = gK[j * K + k] * (gg[j * K + k] - s);
         }
-        for (int e = t; e < K * W; e += kGbThreads) {      // the state before this chunk
-            const int k = e / W, c = e % W;
-            float s = Rs[e];
-            for (int i = 0; i < n; ++i) s = fmaf(gQ[i * K + k], ab[i * W + c], s);
-            Rs[e] = s;
+        for (int e = t; e < KG * W; e += kGbThreads) {     // the state before this chunk, four components a thread
+            const int c = e % W, k0q = (e / W) * 4;
+            float acc[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = k0q + q < K ? Rs[(k0q + q) * W + c] : 0.f;
+            for (int i = 0; i < n; ++i) {
+                const float av = ab[i * W + c];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (k0q + q < K) acc[q] = fmaf(gQ[i * K + k0q + q], av, acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (k0q + q < K) Rs[(k0q + q) * W + c] = acc[q];
         }
     }
 }

@@ -13,7 +13,8 @@
 //
 // Steps (one launch each):
 //   params        Eq. 14-15: var = softplus(rho) + var_floor, log pi = log_softmax(alpha)
-//   gamma         Eq. 3 / 3b for every row of Qx and Kx, written to the workspace
+//   scores        Eq. 16 for tiles of rows x components of Qx and Kx, in the workspace
+//   softmax_rows  Eq. 3 / 3b over each row's scores, in place
 //   write_partial Eq. 5-6 over one N-range per block row: [Vt | Z] partials
 //   reduce        fixed-order sum of the partials (bidirectional) or their
 //                 exclusive prefix over segments (causal, Eq. 6b)
@@ -98,21 +99,71 @@ __global__ void params_kernel(int K, int d, float var_floor, const float *__rest
     }
 }
 
-// Eq. 3 / 3b.  One warp per row; lane l owns components l, l+32, ... (K <= 256).
+// Eq. 16 (direct form) for a tile of 32 rows x 64 components of head-row g
+// (blockIdx.z), written to s[g][i][k]: each thread owns four rows and two components
+// (lane and lane + 32 of the tile), and the coordinates m are staged through shared
+// memory 32 at a time.  Per (row, component) the operations and their order are the
+// ones of the per-row form: acc += (x_m - mu_km)^2 lam_km for m = 0 .. d - 1, then
+// s = c_k - acc / 2.
+constexpr int kScoreRows = 32, kScoreComps = 64;
+
 template <typename T>
-__global__ void gamma_kernel(int G, int H, int N, int d, int K, const T *__restrict__ X,
-                             const float *__restrict__ mu, const float *__restrict__ lam,
-                             const float *__restrict__ cdir, float *__restrict__ gamma) {
-    extern __shared__ float xs[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t row = (size_t)blockIdx.x * (blockDim.x >> 5) + warp;
-    if (row >= (size_t)G * N) return;   // whole warp leaves together; no block barrier below
-    float *x = xs + (size_t)warp * d;
-    for (int j = lane; j < d; j += 32) x[j] = load_elem(X, row * d + j);
-    __syncwarp();
-    const int h = (int)((row / N) % H);
-    const float *mu_h = mu + (size_t)h * K * d;
-    const float *lam_h = lam + (size_t)h * K * d;
+__global__ void __launch_bounds__(256) scores_kernel(int N, int H, int d, int K, const T *__restrict__ X,
+                                                     const float *__restrict__ mu, const float *__restrict__ lam,
+                                                     const float *__restrict__ cdir, float *__restrict__ out) {
+    __shared__ float xs[kScoreRows][33];
+    __shared__ float ms[kScoreComps][33];
+    __shared__ float ls[kScoreComps][33];
+    const int i0 = blockIdx.x * kScoreRows, k0 = blockIdx.y * kScoreComps, g = blockIdx.z, h = g % H;
+    const int lane = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const float *mu_h = mu + (size_t)h * K * d, *lam_h = lam + (size_t)h * K * d;
+    float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+    for (int j0 = 0; j0 < d; j0 += 32) {
+        for (int e = threadIdx.x; e < kScoreRows * 32; e += 256) {
+            const int r = e >> 5, jj = e & 31, i = i0 + r, j = j0 + jj;
+            xs[r][jj] = (i < N && j < d) ? load_elem(X, ((size_t)g * N + i) * d + j) : 0.f;
+        }
+        for (int e = threadIdx.x; e < kScoreComps * 32; e += 256) {
+            const int kk = e >> 5, jj = e & 31, k = k0 + kk, j = j0 + jj;
+            const bool ok = k < K && j < d;
+            ms[kk][jj] = ok ? mu_h[(size_t)k * d + j] : 0.f;
+            ls[kk][jj] = ok ? lam_h[(size_t)k * d + j] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int jj = 0; jj < 32; ++jj) {
+            const float m0 = ms[lane][jj], m1 = ms[lane + 32][jj];
+            const float l0 = ls[lane][jj], l1 = ls[lane + 32][jj];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float x = xs[ty * 4 + q][jj];
+                const float d0 = x - m0, d1 = x - m1;
+                acc[q][0] = fmaf(d0 * d0, l0, acc[q][0]);
+                acc[q][1] = fmaf(d1 * d1, l1, acc[q][1]);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int k = k0 + lane + 32 * c;
+        if (k >= K) continue;
+        const float ck = cdir[(size_t)h * K + k];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = i0 + ty * 4 + q;
+            if (i < N) out[((size_t)g * N + i) * K + k] = ck - 0.5f * acc[q][c];
+        }
+    }
+}
+
+// Eq. 3 / 3b over the scores of one row, in place: one warp per row, lane l owns
+// components l, l + 32, ... (K <= 256).
+__global__ void softmax_rows_kernel(size_t rows, int K, float *__restrict__ gamma) {
+    const size_t row = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float *gr = gamma + row * K;
     float s[8];
     float mx = -FLT_MAX;
 #pragma unroll
@@ -120,12 +171,7 @@ __global__ void gamma_kernel(int G, int H, int N, int d, int K, const T *__restr
         const int k = lane + 32 * t;
         s[t] = -FLT_MAX;
         if (k < K) {
-            float acc = 0.f;
-            for (int j = 0; j < d; ++j) {
-                const float diff = x[j] - mu_h[(size_t)k * d + j];
-                acc = fmaf(diff * diff, lam_h[(size_t)k * d + j], acc);
-            }
-            s[t] = cdir[(size_t)h * K + k] - 0.5f * acc;
+            s[t] = gr[k];
             mx = fmaxf(mx, s[t]);
         }
     }
@@ -144,7 +190,7 @@ __global__ void gamma_kernel(int G, int H, int N, int d, int K, const T *__restr
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
         const int k = lane + 32 * t;
-        if (k < K) gamma[row * K + k] = s[t] * inv;
+        if (k < K) gr[k] = s[t] * inv;
     }
 }
 
@@ -361,14 +407,17 @@ cudaError_t simt_gamma(const Problem &p, const void *X, const float *mu, const f
                        const float *cdir, float *gamma, cudaStream_t s) {
     const size_t rows = (size_t)p.G * p.N;
     if (rows == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)((rows + 7) / 8);
-    const size_t smem = sizeof(float) * 8 * p.d;
+    // scores by tiles of rows x components, then the softmax of every row in place
+    const dim3 grid((p.N + kScoreRows - 1) / kScoreRows, (p.K + kScoreComps - 1) / kScoreComps, p.G);
     if (p.in_dtype == GMA_F32)
-        gamma_kernel<float><<<blocks, 256, smem, s>>>(p.G, p.H, p.N, p.d, p.K,
-                                                      static_cast<const float *>(X), mu, lam, cdir, gamma);
+        scores_kernel<float><<<grid, 256, 0, s>>>(p.N, p.H, p.d, p.K, static_cast<const float *>(X), mu, lam, cdir,
+                                                  gamma);
     else
-        gamma_kernel<__nv_bfloat16><<<blocks, 256, smem, s>>>(
-            p.G, p.H, p.N, p.d, p.K, static_cast<const __nv_bfloat16 *>(X), mu, lam, cdir, gamma);
+        scores_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p.N, p.H, p.d, p.K, static_cast<const __nv_bfloat16 *>(X),
+                                                          mu, lam, cdir, gamma);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    softmax_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(rows, p.K, gamma);
     return cudaGetLastError();
 }
 
