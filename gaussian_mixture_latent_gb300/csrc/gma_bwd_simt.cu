@@ -38,6 +38,7 @@ namespace gma {
 namespace {
 
 constexpr int kGbThreads = 256;
+constexpr int kWalkThreads = 512;      // the causal walks: one CTA per SM (shared memory), 16 warps
 constexpr int kGbChunkDefault = 16;
 
 template <typename T>
@@ -341,7 +342,7 @@ size_t gb_causal_floats(int K, int dv, int C) {
 //   Bm_ij = [j <= i] ab_i . [V_j | 1],         g^Q_i = S ab_i + sum_j Bm_ij gamma^K_j,
 //   ds^Q_i = gamma^Q_i (g^Q_i - gamma^Q_i . g^Q_i),   S += sum_j gamma^K_j^T [V_j | 1].
 template <typename T>
-__global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
+__global__ void __launch_bounds__(kWalkThreads) gb_cq_kernel(GbCausalArgs a) {
     extern __shared__ float sm[];
     const int K = a.K, dv = a.dv, W = dv + 1, C = a.C, N = a.N;
     const int p = blockIdx.x, g = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -350,24 +351,24 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
     float *ab = va + C * W, *dO = ab + C * W, *Am = dO + C * dv, *Bm = Am + C * C;
     const T *V = static_cast<const T *>(a.V), *DO = static_cast<const T *>(a.dO);
     const float *m0 = a.mem + ((size_t)g * a.P + p) * K * W;
-    for (int e = t; e < K * W; e += kGbThreads) S[e] = m0[e];
+    for (int e = t; e < K * W; e += kWalkThreads) S[e] = m0[e];
     const int r0 = p * a.rpp, r1 = min(N, r0 + a.rpp);
     for (int i0 = r0; i0 < r1; i0 += C) {
         const int n = min(C, r1 - i0);
         const size_t row0 = (size_t)g * N + i0;
         __syncthreads();                                   // the previous chunk is done with the buffers
-        for (int e = t; e < C * K; e += kGbThreads) {
+        for (int e = t; e < C * K; e += kWalkThreads) {
             const int r = e / K;
             gA[e] = r < n ? a.gq[row0 * K + e] : 0.f;
             gB[e] = r < n ? a.gk[row0 * K + e] : 0.f;
         }
-        for (int e = t; e < C * W; e += kGbThreads) {
+        for (int e = t; e < C * W; e += kWalkThreads) {
             const int r = e / W, c = e % W;
             va[e] = r < n ? (c < dv ? gld(V, (row0 + r) * dv + c) : 1.f) : 0.f;
         }
-        for (int e = t; e < C * dv; e += kGbThreads) dO[e] = e / dv < n ? gld(DO, row0 * dv + e) : 0.f;
+        for (int e = t; e < C * dv; e += kWalkThreads) dO[e] = e / dv < n ? gld(DO, row0 * dv + e) : 0.f;
         __syncthreads();
-        for (int e = t; e < C * C; e += kGbThreads) {
+        for (int e = t; e < C * C; e += kWalkThreads) {
             const int i = e / C, j = e % C;
             float s = 0.f;
             if (j <= i)
@@ -375,9 +376,10 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
             Am[e] = s;
         }
         __syncthreads();
-        for (int e = t; e < RG * W; e += kGbThreads) {     // [num | den - eps] into ab, four rows a thread
+        for (int e = t; e < RG * W; e += kWalkThreads) {     // [num | den - eps] into ab, four rows a thread
             const int c = e % W, i0q = (e / W) * 4;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
             for (int k = 0; k < K; ++k) {
                 const float sv = S[k * W + c];
 #pragma unroll
@@ -395,7 +397,7 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
                 if (i0q + q < C) ab[(i0q + q) * W + c] = acc[q];
         }
         __syncthreads();
-        for (int i = warp; i < n; i += kGbThreads / 32) {  // a and b, one warp per row
+        for (int i = warp; i < n; i += kWalkThreads / 32) {  // a and b, one warp per row
             const float inv = 1.f / (ab[i * W + dv] + a.eps);
             float dot = 0.f;
             for (int v = lane; v < dv; v += 32) dot = fmaf(dO[i * dv + v], ab[i * W + v] * inv, dot);
@@ -405,8 +407,8 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
             if (lane == 0) ab[i * W + dv] = -dot * inv;
         }
         __syncthreads();
-        for (int e = t; e < n * W; e += kGbThreads) a.ab[row0 * W + e] = ab[e];
-        for (int e = t; e < C * C; e += kGbThreads) {
+        for (int e = t; e < n * W; e += kWalkThreads) a.ab[row0 * W + e] = ab[e];
+        for (int e = t; e < C * C; e += kWalkThreads) {
             const int i = e / C, j = e % C;
             float s = 0.f;
             if (j <= i && i < n)
@@ -414,9 +416,10 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
             Bm[e] = s;
         }
         __syncthreads();
-        for (int e = t; e < RG * K; e += kGbThreads) {     // g^Q, four rows a thread
+        for (int e = t; e < RG * K; e += kWalkThreads) {     // g^Q, four rows a thread
             const int k = e % K, i0q = (e / K) * 4;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
             for (int c = 0; c < W; ++c) {
                 const float sv = S[k * W + c];
 #pragma unroll
@@ -434,13 +437,13 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
                 if (i0q + q < C) gg[(i0q + q) * K + k] = acc[q];
         }
         __syncthreads();
-        for (int i = warp; i < n; i += kGbThreads / 32) {  // ds^Q, one warp per row
+        for (int i = warp; i < n; i += kWalkThreads / 32) {  // ds^Q, one warp per row
             float s = 0.f;
             for (int k = lane; k < K; k += 32) s = fmaf(gA[i * K + k], gg[i * K + k], s);
             s = gb_warp_sum(s);
             for (int k = lane; k < K; k += 32) a.ds[(row0 + i) * K + k] = gA[i * K + k] * (gg[i * K + k] - s);
         }
-        for (int e = t; e < KG * W; e += kGbThreads) {     // the state after this chunk, four components a thread
+        for (int e = t; e < KG * W; e += kWalkThreads) {     // the state after this chunk, four components a thread
             const int c = e % W, k0q = (e / W) * 4;
             float acc[4];
 #pragma unroll
@@ -464,7 +467,7 @@ __global__ void __launch_bounds__(kGbThreads) gb_cq_kernel(GbCausalArgs a) {
 //   g^K_j = Rs [V_j | 1] + sum_i Bm_ij gamma^Q_i,   dV_j = gamma^K_j Rs_V + sum_i Am_ij a_i,
 //   ds^K_j = gamma^K_j (g^K_j - gamma^K_j . g^K_j),  Rs += sum_i gamma^Q_i^T ab_i.
 template <typename T>
-__global__ void __launch_bounds__(kGbThreads) gb_ck_kernel(GbCausalArgs a) {
+__global__ void __launch_bounds__(kWalkThreads) gb_ck_kernel(GbCausalArgs a) {
     extern __shared__ float sm[];
     const int K = a.K, dv = a.dv, W = dv + 1, C = a.C, N = a.N;
     const int p = blockIdx.x, g = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(kGbThreads) gb_ck_kernel(GbCausalArgs a) {
     float *ab = va + C * W, *Am = ab + C * W + C * dv, *Bm = Am + C * C;
     const T *V = static_cast<const T *>(a.V);
     const float *m0 = a.mem + ((size_t)g * a.P + p) * K * W;
-    for (int e = t; e < K * W; e += kGbThreads) Rs[e] = m0[e];
+    for (int e = t; e < K * W; e += kWalkThreads) Rs[e] = m0[e];
     const int r0 = p * a.rpp, r1 = min(N, r0 + a.rpp);
     if (r1 <= r0) return;
     const int nch = (r1 - r0 + C - 1) / C;
@@ -481,18 +484,18 @@ __global__ void __launch_bounds__(kGbThreads) gb_ck_kernel(GbCausalArgs a) {
         const int i0 = r0 + ci * C, n = min(C, r1 - i0);
         const size_t row0 = (size_t)g * N + i0;
         __syncthreads();
-        for (int e = t; e < C * K; e += kGbThreads) {
+        for (int e = t; e < C * K; e += kWalkThreads) {
             const int r = e / K;
             gQ[e] = r < n ? a.gq[row0 * K + e] : 0.f;
             gK[e] = r < n ? a.gk[row0 * K + e] : 0.f;
         }
-        for (int e = t; e < C * W; e += kGbThreads) {
+        for (int e = t; e < C * W; e += kWalkThreads) {
             const int r = e / W, c = e % W;
             va[e] = r < n ? (c < dv ? gld(V, (row0 + r) * dv + c) : 1.f) : 0.f;
             ab[e] = r < n ? a.ab[row0 * W + e] : 0.f;
         }
         __syncthreads();
-        for (int e = t; e < C * C; e += kGbThreads) {
+        for (int e = t; e < C * C; e += kWalkThreads) {
             const int i = e / C, j = e % C;
             float sa = 0.f, sb = 0.f;
             if (j <= i) {
@@ -503,9 +506,10 @@ __global__ void __launch_bounds__(kGbThreads) gb_ck_kernel(GbCausalArgs a) {
             Bm[e] = sb;
         }
         __syncthreads();
-        for (int e = t; e < RG * K; e += kGbThreads) {     // g^K, four rows a thread
+        for (int e = t; e < RG * K; e += kWalkThreads) {     // g^K, four rows a thread
             const int k = e % K, j0q = (e / K) * 4;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
             for (int c = 0; c < W; ++c) {
                 const float rv = Rs[k * W + c];
 #pragma unroll
@@ -522,9 +526,10 @@ __global__ void __launch_bounds__(kGbThreads) gb_ck_kernel(GbCausalArgs a) {
             for (int q = 0; q < 4; ++q)
                 if (j0q + q < C) gg[(j0q + q) * K + k] = acc[q];
         }
-        for (int e = t; e < RG * dv; e += kGbThreads) {    // dV, four rows a thread
+        for (int e = t; e < RG * dv; e += kWalkThreads) {    // dV, four rows a thread
             const int v = e % dv, j0q = (e / dv) * 4;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
             for (int k = 0; k < K; ++k) {
                 const float rv = Rs[k * W + v];
 #pragma unroll
@@ -542,13 +547,13 @@ __global__ void __launch_bounds__(kGbThreads) gb_ck_kernel(GbCausalArgs a) {
                 if (j0q + q < n) a.dV[(row0 + j0q + q) * dv + v] = acc[q];
         }
         __syncthreads();
-        for (int j = warp; j < n; j += kGbThreads / 32) {  // ds^K, one warp per row
+        for (int j = warp; j < n; j += kWalkThreads / 32) {  // ds^K, one warp per row
             float s = 0.f;
             for (int k = lane; k < K; k += 32) s = fmaf(gK[j * K + k], gg[j * K + k], s);
             s = gb_warp_sum(s);
             for (int k = lane; k < K; k += 32) a.ds[(row0 + j) * K + k] = gK[j * K + k] * (gg[j * K + k] - s);
         }
-        for (int e = t; e < KG * W; e += kGbThreads) {     // the state before this chunk, four components a thread
+        for (int e = t; e < KG * W; e += kWalkThreads) {     // the state before this chunk, four components a thread
             const int c = e % W, k0q = (e / W) * 4;
             float acc[4];
 #pragma unroll
@@ -642,14 +647,14 @@ cudaError_t run_t(const Problem &p, const GbLayout &L, const void *Qx_, const vo
         GB_TRY(reduce(p, L, K * W, 1, part, mem, s));
         a.mem = mem; a.ds = dsq;
         GB_TRY(set_dyn_smem(reinterpret_cast<const void *>(gb_cq_kernel<T>), (int)smem));
-        gb_cq_kernel<T><<<dim3(L.P, p.G), kGbThreads, smem, s>>>(a);
+        gb_cq_kernel<T><<<dim3(L.P, p.G), kWalkThreads, smem, s>>>(a);
         GB_TRY(cudaGetLastError());
         // keys: [R | r] of the query rows after each range, then the walks
         GB_TRY(outer(p, L, W, gq, UPlain{ab, W}, part, s));
         GB_TRY(reduce(p, L, K * W, 2, part, memr, s));
         a.mem = memr; a.ds = dsk; a.dV = dV;
         GB_TRY(set_dyn_smem(reinterpret_cast<const void *>(gb_ck_kernel<T>), (int)smem));
-        gb_ck_kernel<T><<<dim3(L.P, p.G), kGbThreads, smem, s>>>(a);
+        gb_ck_kernel<T><<<dim3(L.P, p.G), kWalkThreads, smem, s>>>(a);
         GB_TRY(cudaGetLastError());
     }
     // dQx, dKx through ds [lambda mu | lambda]; the parameter sums of both sides
