@@ -331,7 +331,7 @@ gma_status gma_forward_multi(const gma_forward_call *calls, int n_calls, void *w
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) !=
                                                  cudaSuccess)
         return GMA_ERR_CUDA;
-    const bool side_by_side = aux_stream && n_head > 0 && n_rest > 0 && nsm - held >= nsm / 8;
+    const bool side_by_side = aux_stream && aux_stream != stream && n_head > 0 && n_rest > 0 && nsm - held >= nsm / 8;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaStream_t aux = static_cast<cudaStream_t>(aux_stream);
     std::vector<Plan> plans(n_calls);

@@ -179,8 +179,8 @@ gma_status gma_forward_multi_workspace_size(const gma_forward_call *calls, int n
  * after all of it.  Every call is validated before anything is launched; the
  * first failing call's status is returned.
  *
- * Scheduling.  With aux_stream == NULL the calls run in order on `stream`,
- * exactly as gma_forward() calls would.  Otherwise the calls that the library
+ * Scheduling.  With aux_stream == NULL (or equal to `stream`) the calls run in
+ * order on `stream`, exactly as gma_forward() calls would.  Otherwise the calls that the library
  * runs as one CTA per head (those whose gma_forward_plan() is the single launch
  * "tc_causal": the bf16 causal scan with d = K = dv = 64 when the heads B*H
  * fill more than half of the SMs or the sequences are short) run in order on

@@ -1,5 +1,6 @@
 """The index-checking debug build (GMA_DEBUG_BOUNDS): every forward path, the
-tensor-core backward, the projection GEMM and the diagnostics run with their
+tensor-core and general backward, the projection GEMM, the diagnostics and a
+gma_forward_multi request run with their
 global-memory indices checked on the device, on outputs and workspaces padded with
 canary bytes.  A failed check posts GMA_ERR_BOUNDS to the status word (instead of
 trapping), so the test asserts a clean status, untouched canaries on both sides of
@@ -156,6 +157,71 @@ for K_, N_ in ((64, 700), (128, 300)):
     agree = float((z_.cpu().numpy() == rz).mean())
     assert err <= 2e-2 and agree >= 0.99, (w.name, err, agree)
     print(f"{w.name}: status clean, canaries intact, p/stats error {err:.2e}, argmax agreement {agree:.4f}")
+# the general backward (causal, K = 128: the chunk walks and the tiled products)
+w = inputs.Workload("bwd_general", seed=7, B=1, H=2, N=300, d=64, K=128, dv=64, dtype="bf16", causal=True)
+x = inputs.gen_all(w)
+x["dO"] = x["V"][:, ::-1].copy()
+desc = gma._make_desc(w.B, w.H, w.N, w.d, w.K, w.dv, torch.bfloat16, torch.bfloat16, w.var_floor, 0)
+nb = ctypes.c_size_t(0)
+assert gma._load().gma_backward_workspace_size(ctypes.byref(desc), 1, ctypes.byref(nb)) == 0
+need = nb.value
+ws = workspace(need)
+shapes = ((w.B, w.H, w.N, w.d), (w.B, w.H, w.N, w.d), (w.B, w.H, w.N, w.dv), (w.H, w.K, w.d), (w.H, w.K, w.d),
+          (w.H, w.K))
+pads = [padded(shp, torch.float32) for shp in shapes]
+grads = gma.gma_backward(*(to_device(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha", "dO")), eps=w.eps,
+                         var_floor=w.var_floor, causal=True, grads=tuple(t for _, t in pads), workspace=ws)
+torch.cuda.synchronize()
+st = gma.gma_get_status(ws)
+assert st == 0, ("bwd_general", gma.gma_status_string(st))
+assert all(canaries_ok(f, torch.float32) for f, _ in pads), ("bwd_general", "gradient canaries")
+assert bool((ws[need:] == CANARY_BYTE).all()), ("bwd_general", "workspace canaries")
+worst = 0.0
+got = [t.double().cpu().numpy() for t in grads]
+for h in (0, 1):
+    ref = oracle.backward_head(wid(x["Qx"][0, h]), wid(x["Kx"][0, h]), wid(x["V"][0, h]), x["mu"][h], x["rho"][h],
+                               x["alpha"][h], w.var_floor, w.eps, True, wid(x["dO"][0, h]))
+    floor = 1e-2 * max(np.abs(ref["Qx"]).max(), np.abs(ref["Kx"]).max())
+    for i, nm in enumerate(("Qx", "Kx", "V")):
+        den = max(np.abs(ref[nm]).max(), floor if nm != "V" else 0.0)
+        worst = max(worst, float(np.abs(got[i][0, h] - ref[nm]).max() / den))
+    for i, nm in ((3, "mu"), (4, "omega"), (5, "alpha")):
+        worst = max(worst, float(np.abs(got[i][h] - ref[nm]).max() / np.abs(ref[nm]).max()))
+assert worst <= 1e-3, ("bwd_general", worst)
+print(f"bwd_general: status clean, canaries intact, max relative error {worst:.2e}")
+
+# a gma_forward_multi request: the per-head causal scan on a second stream beside the
+# bidirectional forward, canary-padded outputs, every region's header zero, canaries after
+w = inputs.Workload("multi", seed=7, B=2, H=48, N=300, d=64, K=64, dv=64, dtype="bf16", causal=True)
+x = inputs.gen_all(w)
+d_ = {n: to_device(x[n]) for n in ("Qx", "Kx", "V", "mu", "rho", "alpha")}
+pads = [padded((w.B, w.H, w.N, w.dv), torch.bfloat16) for _ in range(2)]
+calls = [dict(Qx=d_["Qx"], Kx=d_["Kx"], V=d_["V"], mu=d_["mu"], rho=d_["rho"], pi_logits=d_["alpha"], eps=w.eps,
+              causal=c, var_floor=w.var_floor, out=pads[k][1]) for k, c in enumerate((False, True))]
+arr = (gma.gma_forward_call * 2)()
+for k, c in enumerate((False, True)):
+    arr[k].desc = gma._make_desc(w.B, w.H, w.N, w.d, w.K, w.dv, torch.bfloat16, torch.bfloat16, w.var_floor, 0)
+    arr[k].causal = int(c)
+offs = (ctypes.c_size_t * 2)()
+assert gma._load().gma_forward_multi_workspace_size(arr, 2, ctypes.byref(nb), offs) == 0
+need = nb.value
+ws = workspace(need)
+for o in offs:
+    ws[o:o + 256] = 0
+gma.gma_forward_multi(calls, workspace=ws, aux_stream=torch.cuda.Stream())
+torch.cuda.synchronize()
+for o in offs:
+    st = gma._load().gma_get_status(int(ws.data_ptr()) + o, int(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, ("multi", gma.gma_status_string(st))
+assert all(canaries_ok(f, torch.bfloat16) for f, _ in pads), ("multi", "output canaries")
+assert bool((ws[need:] == CANARY_BYTE).all()), ("multi", "workspace canaries")
+worst = 0.0
+for (f, o), c in zip(pads, (False, True)):
+    wc = w.replace(causal=c)
+    gotc = to_f64(o).reshape(wc.G, wc.N, wc.dv)
+    worst = max(worst, max(head_rel_err(gotc[g], oracle_head(wc, x, g)) for g in (0, 47, 95)))
+assert worst <= TOL["bf16"], ("multi", worst)
+print(f"multi: status clean, canaries intact, max relative error {worst:.2e}")
 print("ALL_OK")
 '''
 

@@ -95,6 +95,10 @@ def test_without_an_auxiliary_stream_the_calls_run_as_gma_forward_does():
     ref_b, ref_c = single(w, d, False), single(w, d, True)
     ob, oc = gma.gma_forward_multi([call(w, d, False), call(w, d, True)], check_status=True)
     assert torch.equal(ob, ref_b) and torch.equal(oc, ref_c)
+    # the main stream passed as the auxiliary one: no second lane either
+    s = torch.cuda.current_stream()
+    ob, oc = gma.gma_forward_multi([call(w, d, False), call(w, d, True)], stream=s, aux_stream=s, check_status=True)
+    assert torch.equal(ob, ref_b) and torch.equal(oc, ref_c)
 
 
 def test_mixed_request_every_path_and_an_empty_call():
