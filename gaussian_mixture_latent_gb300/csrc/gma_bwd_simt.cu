@@ -687,8 +687,22 @@ GbLayout gb_layout(const Problem &p) {
     const long long want = (4LL * 160 + p.G - 1) / p.G;
     const long long by_rows = (p.N + 255) / 256;
     L.P = (int)std::max(1LL, std::min(want, by_rows));
-    L.rpp = std::max(1, (p.N + L.P - 1) / L.P);
     L.C = p.chunk > 0 ? p.chunk : kGbChunkDefault;
+    if (p.causal) {
+        // the walks hold one CTA per SM: pick the range count that minimises
+        // (waves of P G CTAs) x (chunks per range), the largest such count
+        int sms = 0, dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                     cudaSuccess || sms <= 0)
+            sms = 152;
+        long long best = -1;
+        for (long long P = 1; P <= std::max(1LL, std::min(4 * want, by_rows)); ++P) {
+            const long long rpp = (p.N + P - 1) / P;
+            const long long cost = ((P * p.G + sms - 1) / sms) * ((rpp + L.C - 1) / L.C);
+            if (best < 0 || cost <= best) { best = cost; L.P = (int)P; }
+        }
+    }
+    L.rpp = std::max(1, (p.N + L.P - 1) / L.P);
     const size_t K = p.K, d = p.d, W = (size_t)p.dv + 1, E = 2 * d + 1, G = p.G, N = p.N, P = L.P;
     const size_t rows = G * N;
     size_t off = kHeaderBytes;
