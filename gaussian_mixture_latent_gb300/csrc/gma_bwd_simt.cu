@@ -21,7 +21,7 @@
 // running state in shared memory.
 //
 // Kernels (all fp32 arithmetic, every reduction in a fixed order, so results are
-// deterministic): gb_rowmat (row-times-matrix tiles), gb_outer (per-range sums of
+// deterministic): gb_rowmat (row-times-matrix tiles of 64 x 64), gb_outer (per-range sums of
 // outer products), gb_reduce (sum / exclusive prefix / exclusive suffix over ranges),
 // gb_ab, gb_ds, gb_dx (per-row steps), gb_cq / gb_ck (the causal chunk walks),
 // gb_param (dmu, drho, dalpha).  The responsibilities come from the forward's CUDA-core
@@ -54,21 +54,24 @@ __device__ __forceinline__ float gld<__nv_bfloat16>(const __nv_bfloat16 *p, size
 //   A(g, i, k) = A[(g N + i) lda + k] for k < a_cols, 1 at k == a_cols when a_one, else 0;
 //   B(k, c)    = MT ? M[mo + c ldm + k] : M[mo + k ldm + c],  k < KA,
 //   mo = (m_per_head ? g % H : g) m_stride.
-// 32 x 32 output tile per CTA, 256 threads, four rows per thread.
+// 64 x 64 output tile per CTA, 256 threads, each four rows (ty + 16 q) by four columns
+// (tx + 16 j); k in steps of 32 through shared memory, in increasing order per output.
+constexpr int kRmTile = 64;
+
 template <typename TA, bool MT>
 __global__ void __launch_bounds__(kGbThreads) gb_rowmat_kernel(int N, int KA, int C, int H, int lda, int a_cols,
                                                                int a_one, const TA *__restrict__ A,
                                                                const float *__restrict__ M, int m_per_head,
                                                                size_t m_stride, int ldm, float *__restrict__ out,
                                                                int ldo) {
-    __shared__ float as[32][33];
-    __shared__ float bs[32][33];
-    const int i0 = blockIdx.x * 32, c0 = blockIdx.y * 32, g = blockIdx.z;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    __shared__ float as[kRmTile][33];
+    __shared__ float bs[32][kRmTile + 1];
+    const int i0 = blockIdx.x * kRmTile, c0 = blockIdx.y * kRmTile, g = blockIdx.z;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const float *Mg = M + (size_t)(m_per_head ? g % H : g) * m_stride;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4][4] = {};
     for (int k0 = 0; k0 < KA; k0 += 32) {
-        for (int e = threadIdx.x; e < 1024; e += kGbThreads) {
+        for (int e = threadIdx.x; e < kRmTile * 32; e += kGbThreads) {
             const int r = e >> 5, cc = e & 31;
             const int i = i0 + r, k = k0 + cc;
             float av = 0.f;
@@ -80,26 +83,34 @@ __global__ void __launch_bounds__(kGbThreads) gb_rowmat_kernel(int N, int KA, in
             if (MT) {          // element (k0 + cc, c0 + r): a warp reads consecutive k of one row of M
                 const int kk = k0 + cc, c = c0 + r;
                 bs[cc][r] = (kk < KA && c < C) ? Mg[(size_t)c * ldm + kk] : 0.f;
-            } else {
-                const int kk = k0 + r, c = c0 + cc;
-                bs[r][cc] = (kk < KA && c < C) ? Mg[(size_t)kk * ldm + c] : 0.f;
+            } else {           // element (k0 + (e >> 6), c0 + (e & 63))
+                const int kk = k0 + (e >> 6), c = c0 + (e & 63);
+                bs[e >> 6][e & 63] = (kk < KA && c < C) ? Mg[(size_t)kk * ldm + c] : 0.f;
             }
         }
         __syncthreads();
-#pragma unroll 8
+#pragma unroll 4
         for (int kk = 0; kk < 32; ++kk) {
-            const float b = bs[kk][tx];
+            float a[4], b[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[q] = fmaf(as[ty * 4 + q][kk], b, acc[q]);
+            for (int q = 0; q < 4; ++q) a[q] = as[ty + 16 * q][kk];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = bs[kk][tx + 16 * j];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[q][j] = fmaf(a[q], b[j], acc[q][j]);
         }
         __syncthreads();
     }
-    const int c = c0 + tx;
-    if (c < C) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = i0 + ty * 4 + q;
-            if (i < N) out[((size_t)g * N + i) * ldo + c] = acc[q];
+    for (int q = 0; q < 4; ++q) {
+        const int i = i0 + ty + 16 * q;
+        if (i >= N) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = c0 + tx + 16 * j;
+            if (c < C) out[((size_t)g * N + i) * ldo + c] = acc[q][j];
         }
     }
 }
@@ -133,42 +144,53 @@ struct USquares {              // [x | x^2 | 1]
 };
 
 // part[((g P + p) K + k) W + c] = sum over rows i of range p of A[(g N + i) K + k] U(g N + i, c),
-// k < K, c < W; range p = rows [p rpp, min(N, (p + 1) rpp)).  32 x 32 tile per CTA.
+// k < K, c < W; range p = rows [p rpp, min(N, (p + 1) rpp)).  64 x 64 output tile per CTA,
+// each thread four components (ty + 16 q) by four columns (tx + 16 j), rows in increasing
+// order through shared memory 32 at a time.
 template <typename U>
 __global__ void __launch_bounds__(kGbThreads) gb_outer_kernel(int N, int K, int W, int P, int rpp,
                                                               const float *__restrict__ A, U u,
                                                               float *__restrict__ part) {
-    __shared__ float as[32][33];
-    __shared__ float us[32][33];
-    const int ktiles = (K + 31) / 32;
+    __shared__ float as[32][kRmTile + 1];
+    __shared__ float us[32][kRmTile + 1];
+    const int ktiles = (K + kRmTile - 1) / kRmTile;
     const int kt = blockIdx.x % ktiles, ct = blockIdx.x / ktiles;
     const int p = blockIdx.y, g = blockIdx.z;
     const int r0 = p * rpp, r1 = min(N, r0 + rpp);
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int k0 = kt * kRmTile, c0 = ct * kRmTile;
+    float acc[4][4] = {};
     for (int j0 = r0; j0 < r1; j0 += 32) {
-        for (int e = threadIdx.x; e < 1024; e += kGbThreads) {
-            const int jr = e >> 5, cc = e & 31;
-            const int j = j0 + jr, k = kt * 32 + cc, c = ct * 32 + cc;
+        for (int e = threadIdx.x; e < 32 * kRmTile; e += kGbThreads) {
+            const int jr = e >> 6, cc = e & 63;
+            const int j = j0 + jr, k = k0 + cc, c = c0 + cc;
             const size_t row = (size_t)g * N + j;
             as[jr][cc] = (j < r1 && k < K) ? A[row * K + k] : 0.f;
             us[jr][cc] = (j < r1 && c < W) ? u(row, c) : 0.f;
         }
         __syncthreads();
-#pragma unroll 8
+#pragma unroll 4
         for (int jr = 0; jr < 32; ++jr) {
-            const float v = us[jr][tx];
+            float a[4], v[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[q] = fmaf(as[jr][ty * 4 + q], v, acc[q]);
+            for (int q = 0; q < 4; ++q) a[q] = as[jr][ty + 16 * q];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) v[jj] = us[jr][tx + 16 * jj];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) acc[q][jj] = fmaf(a[q], v[jj], acc[q][jj]);
         }
         __syncthreads();
     }
-    const int c = ct * 32 + tx;
-    if (c < W) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int k = kt * 32 + ty * 4 + q;
-            if (k < K) part[(((size_t)g * P + p) * K + k) * W + c] = acc[q];
+    for (int q = 0; q < 4; ++q) {
+        const int k = k0 + ty + 16 * q;
+        if (k >= K) continue;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int c = c0 + tx + 16 * jj;
+            if (c < W) part[(((size_t)g * P + p) * K + k) * W + c] = acc[q][jj];
         }
     }
 }
@@ -578,7 +600,7 @@ unsigned blocks_for(size_t n, int per) { return (unsigned)((n + per - 1) / per);
 template <typename TA, bool MT>
 cudaError_t rowmat(const Problem &p, int KA, int C, int lda, int a_cols, int a_one, const TA *A, const float *M,
                    int m_per_head, size_t m_stride, int ldm, float *out, int ldo, cudaStream_t s) {
-    dim3 grid((p.N + 31) / 32, (C + 31) / 32, p.G);
+    dim3 grid((p.N + kRmTile - 1) / kRmTile, (C + kRmTile - 1) / kRmTile, p.G);
     gb_rowmat_kernel<TA, MT><<<grid, kGbThreads, 0, s>>>(p.N, KA, C, p.H, lda, a_cols, a_one, A, M, m_per_head,
                                                          m_stride, ldm, out, ldo);
     return cudaGetLastError();
@@ -586,7 +608,7 @@ cudaError_t rowmat(const Problem &p, int KA, int C, int lda, int a_cols, int a_o
 
 template <typename U>
 cudaError_t outer(const Problem &p, const GbLayout &L, int W, const float *A, U u, float *part, cudaStream_t s) {
-    dim3 grid(((p.K + 31) / 32) * ((W + 31) / 32), L.P, p.G);
+    dim3 grid(((p.K + kRmTile - 1) / kRmTile) * ((W + kRmTile - 1) / kRmTile), L.P, p.G);
     gb_outer_kernel<U><<<grid, kGbThreads, 0, s>>>(p.N, p.K, W, L.P, L.rpp, A, u, part);
     return cudaGetLastError();
 }
