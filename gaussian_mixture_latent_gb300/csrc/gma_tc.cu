@@ -75,6 +75,7 @@ struct TcArgs {
     unsigned *status;
     int nslots;              // partial slots in the workspace (index checks of the debug build)
     int *claim;              // the read's unit counter (zeroed by tc_reduce)
+    int dyn;                 // the read takes units from the counter (1) or a static range (0)
 };
 
 __device__ __forceinline__ void cta_range(int Ttot, int &t0, int &t1) {
@@ -461,16 +462,18 @@ __global__ void __launch_bounds__(kReduceThreads) tc_reduce_kernel(int K, int T,
 
 // ------------------------------------------------------------------ tc_read
 //
-// The read takes its tiles dynamically.  The (head, tile) list is cut into units of
-// up to kReadUnit consecutive tiles of one head; each CTA's producer claims the next
-// unit from a counter in the workspace (tc_reduce zeroes it), so a CTA that starts
-// late, on an SM that another kernel held until then, takes fewer units, and every
-// SM that frees up joins in.  Each unit is a segment of its own: the producer loads
-// its head's parameter block and memory operand into one of two buffers.  The other
-// roles learn each tile's (head, tile, segment, flags) from a ring in shared memory
-// that the producer fills before the tile's full barrier completes; after the last
-// unit it posts one end marker per compute group, and the first marker's group
-// passes the end on to the two MMA issuers through its own barriers.
+// The read's tiles come in runs of one head.  Alone, a CTA walks a static contiguous
+// range of the (head, tile) list, one run per head it meets.  Beside a concurrent
+// kernel (gma_forward_multi), the list is cut into units of up to kReadUnit tiles of
+// one head, and each CTA's producer claims the next unit from a counter in the
+// workspace (tc_reduce zeroes it), so a CTA that starts late, on an SM that the other
+// kernel held until then, takes fewer units, and every SM that frees up joins in.
+// Each run is a segment of its own: the producer loads its head's parameter block and
+// memory operand into one of two buffers.  The other roles learn each tile's (head,
+// tile, segment, flags) from a ring in shared memory that the producer fills before
+// the tile's full barrier completes; after the last run it posts one end marker per
+// compute group, and the first marker's group passes the end on to the two MMA
+// issuers through its own barriers.
 
 constexpr int kReadUnit = 4;                   // tiles per claimed unit
 constexpr int kInfoRing = 16;                  // tile-info entries (>= X stages + compute groups)
@@ -549,13 +552,44 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane == 0) {
             const int uph = (A.T + kReadUnit - 1) / kReadUnit;      // units per head
             const int nunits = A.G * uph;
+            int t = 0, t_end = 0;
+            if (!A.dyn) {
+                t = (int)(((long long)blockIdx.x * A.Ttot) / gridDim.x);
+                t_end = (int)(((long long)(blockIdx.x + 1) * A.Ttot) / gridDim.x);
+            }
+            // the next run of tiles [ja, jb) of head g: a claimed unit, or the part of the CTA's
+            // static range that lies in the next head
+            auto next_run = [&](int &g, int &ja, int &jb) -> bool {
+                if (A.dyn) {
+                    const int u = atomicAdd(A.claim, 1);
+                    if (u >= nunits) return false;
+                    g = u / uph;
+                    ja = (u - g * uph) * kReadUnit;
+                    jb = min(ja + kReadUnit, A.T);
+                    return true;
+                }
+                if (t >= t_end) return false;
+                g = t / A.T;
+                ja = t - g * A.T;
+                jb = min(A.T, ja + (t_end - t));
+                t += jb - ja;
+                return true;
+            };
+            int i = 0, nseg = 0, g = 0, ja = 0, jb = 0, pre = 0;   // tiles (and end markers) issued, segments
+            bool have = false, ok = true;
+            if (!A.dyn) {
+                // a static range: its first query tiles do not depend on the previous kernel
+                have = next_run(g, ja, jb);
+                for (; have && pre < SX && ja + pre < jb; ++pre, ++i) {
+                    const int j = ja + pre;
+                    info[i] = TileInfo{g, j, 0, (pre == 0 ? kTileFirst : 0) | (j == jb - 1 ? kTileLast : 0)};
+                    mbar_arrive_expect_tx(&xfull[i], kTileBytes);
+                    tma_load_3d(sm + C::OFF_X + i * kTileBytes, &tm_q, &xfull[i], 0, j * TM, g);
+                }
+            }
             grid_dep_wait();             // parameter blocks, memory operands and the zeroed unit counter
-            int i = 0, nseg = 0;         // tiles (and end markers) issued, segments started
-            bool ok = true;
-            while (ok && !*abort_flag) {
-                const int u = atomicAdd(A.claim, 1);
-                if (u >= nunits) break;
-                const int g = u / uph, ja = (u - g * uph) * kReadUnit, jb = min(ja + kReadUnit, A.T);
+            if (A.dyn) have = next_run(g, ja, jb);
+            while (ok && have && !*abort_flag) {
                 const int b = nseg % PN;
                 if (nseg >= PN && !(ok = mbar_wait(&w_empty[b], ((nseg / PN) - 1) & 1, ab, kDevErrTimeout))) break;
                 mbar_arrive_expect_tx(&w_full[b], param_bytes(K) + mem_bytes(K));
@@ -564,12 +598,14 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 (void)GMA_IN_BOUNDS(g < A.G, A.status);
                 bulk_load(sm + C::OFF_M + b * C::MB, A.mem + (size_t)g * A.mem_stride, mem_bytes(K), &w_full[b]);
                 const int seg = nseg++;
-                for (int j = ja; j < jb; ++j, ++i) {
+                for (int j = ja + pre; j < jb; ++j, ++i) {
                     if (i >= SX && !(ok = mbar_wait(&xempty[i % SX], ((i / SX) - 1) & 1, ab, kDevErrTimeout))) break;
                     info[i % kInfoRing] = TileInfo{g, j, seg, (j == ja ? kTileFirst : 0) | (j == jb - 1 ? kTileLast : 0)};
                     mbar_arrive_expect_tx(&xfull[i % SX], kTileBytes);
                     tma_load_3d(sm + C::OFF_X + (i % SX) * kTileBytes, &tm_q, &xfull[i % SX], 0, j * TM, g);
                 }
+                pre = 0;
+                if (ok) have = next_run(g, ja, jb);
             }
             for (int k = 0; k < NW && ok; ++k, ++i) {
                 if (i >= SX && !(ok = mbar_wait(&xempty[i % SX], ((i / SX) - 1) & 1, ab, kDevErrTimeout))) break;
@@ -732,6 +768,7 @@ cudaError_t launch_read(const Problem &p, const TcLayout &L, const void *Qx, voi
     a.eps = p.eps;
     a.status = reinterpret_cast<unsigned *>(ws);
     a.claim = reinterpret_cast<int *>(ws + L.claim);
+    a.dyn = p.sm_budget > 0;
     auto kern = tc_read_kernel<K>;
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), ReadCfg<K>::BYTES);
     if (e != cudaSuccess) return e;
@@ -750,8 +787,10 @@ TcLayout tc_layout(const Problem &p) {
     L.T = (p.N + TM - 1) / TM;
     L.Ttot = L.T * p.G;
     const int nsm = sm_count();
+    // the read: static ranges when the call runs alone, units claimed from a counter beside
+    // a concurrent kernel (a CTA that starts late takes fewer)
     const int units = p.G * ((L.T + kReadUnit - 1) / kReadUnit);
-    L.ncta = std::max(1, std::min({nsm > 0 ? nsm : kMaxCtas, kMaxCtas, units}));
+    L.ncta = std::max(1, std::min({nsm > 0 ? nsm : kMaxCtas, kMaxCtas, p.sm_budget > 0 ? units : L.Ttot}));
     L.Tkv = (p.Nkv + TM - 1) / TM;
     L.Ttot_kv = L.Tkv * p.G;
     // the write kernel's static ranges: on the SMs left free by a concurrent kernel when
