@@ -17,27 +17,30 @@
 // responsibilities.  Operands are fp16 (x exact; x^2 and W rounded to 11
 // bits; W carries a per-head power-of-two scale), accumulation fp32.
 //
-// Kernels (tc_write / tc_read are persistent, one CTA per SM, each CTA owns a
-// contiguous range of the (head, 128-row tile) list):
+// Kernels (tc_write / tc_read are persistent, one CTA per SM):
 //   tc_params  per head: fp16 W in the MMA's shared-memory layout, c, scale
-//   tc_write   per tile of Kx, V:  [x, x^2] -> TMEM; MMA -> scores in TMEM;
+//   tc_write   per tile of Kx, V (each CTA a contiguous range of the (head,
+//              128-row tile) list):  [x, x^2] -> TMEM; MMA -> scores in TMEM;
 //              softmax -> Gamma^K (bf16, shared memory); MMA accumulates
 //              [V | 1]^T Gamma^K (= [Vt | Z]^T) in TMEM; drained per head to a
 //              fp32 partial slot (slot index = cta + head)
 //   tc_reduce  per head: fixed-order sum of the partial slots -> [Vt | Z | 1]^T
 //              as the bf16 B operand of the read
-//   tc_read    per tile of Qx: scores as above; unnormalised exp2 -> TMEM (bf16);
-//              MMA with [Vt | Z | 1]; out = num / (den + eps * sum) -> TMA store
+//   tc_read    per tile of Qx (a contiguous range per CTA, or, beside a
+//              concurrent kernel, units of tiles claimed from a counter):
+//              scores as above; unnormalised exp2 -> TMEM (bf16); MMA with
+//              [Vt | Z | 1]; out = num / (den + eps * sum) -> TMA store
 //
-// Warp roles inside tc_write / tc_read (352 threads): warp 0 issues every TMA
-// and bulk copy from one thread that polls its rings without blocking; warp 1
-// allocates TMEM and issues the log-density MMAs; warp 2 issues the
-// write / read MMAs (two issuers, because an MMA issue blocks while the tensor
-// pipe fills); warps 3-10 are two compute warpgroups that take alternate
-// tiles (one thread per row), each with its own TMEM columns, so one group's
-// softmax overlaps the other's MMAs.  Every mbarrier wait is bounded; a
-// timeout posts GMA_ERR_TIMEOUT to the workspace status word and the CTA
-// winds down.
+// Warp roles inside tc_write / tc_read ((3 + 4 NW) warps, NW = 3 compute groups
+// at K = 64 and 2 at K = 128): warp 0 issues every TMA and bulk copy from one
+// thread (the write's producer polls its rings without blocking; the read's
+// waits on one ring slot at a time); warp 1 allocates TMEM and issues the
+// log-density MMAs; warp 2 issues the write / read MMAs (two issuers, because an
+// MMA issue blocks while the tensor pipe fills); warps 3 onwards are the NW
+// compute warpgroups that take tiles in turn (one thread per row), each with its
+// own TMEM columns, so one group's softmax overlaps the others' MMAs.  Every
+// mbarrier wait is bounded; a timeout posts GMA_ERR_TIMEOUT to the workspace
+// status word and the CTA winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
