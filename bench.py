@@ -436,13 +436,16 @@ def run_gpu(args, rank, world, local):
     torch.cuda.nvtx.range_push("gma:timed")
     # a GPU spin ahead of the start event lets the host enqueue the first steps before the GPU
     # reaches them, so the timed region starts with work queued (device time, not the host's
-    # first launches); about the steps' estimated time, at most 20 ms.  The first step after
-    # an idle GPU runs its causal scan slower once (about 160 us more, measured), so PRE_ROLL
-    # untimed warm-up steps run between the spin and the start event.
+    # first launches); about the steps' estimated time, at most 20 ms.  PRE_ROLL untimed
+    # warm-up steps run between the spin and the start event.
     torch.cuda._sleep(int(2.0e6 * min(20.0, (steps + PRE_ROLL) * max(step_ms_est, 0.1))))
     for it in range(PRE_ROLL):
         step_forwards(dsets[it % 2])
     t_start.record(stream)
+    # a kernel between the timing event and the first request's fork: with the fork recorded
+    # right after a timing event, that step's causal scan measured about 160 us slower (once);
+    # a ~0.5 us spin in between removes it
+    torch.cuda._sleep(1000)
     for it in range(steps):
         evs = None
         if it in dom_events:
