@@ -9,13 +9,13 @@
 // D in blocks of 64 through a 4-stage TMA ring, and two TMEM accumulators let the
 // epilogue of one tile overlap the MMAs of the next.
 //
-// CTAs work in clusters of two on tile pairs: two adjacent row tiles of the same
-// column blocks.  Each CTA loads its own X rows and half of the W blocks, which TMA
-// multicasts into both CTAs' stage, so a CTA pulls 32 KB per stage from L2 instead
-// of 48 KB.  A stage is refilled once both CTAs' MMAs have read it (each MMA commit
-// arrives on the stage's barrier in both CTAs).  Pairs are taken in row-block major
-// order (the clusters working at a time share their X rows in L2; W stays in L2); an
-// odd last row tile is paired with a copy of itself whose results are not stored.
+// CTAs work in clusters of kCl = 4 on tile groups: four adjacent row tiles of the same
+// column blocks.  Each CTA loads its own X rows and a quarter of the W blocks, which TMA
+// multicasts into every CTA's stage, so a CTA pulls 24 KB per stage from L2 instead of
+// 48 KB.  A stage is refilled once every CTA's MMAs have read it (each MMA commit
+// arrives on the stage's barrier in every CTA of the cluster).  Groups are taken in
+// row-block major order (the clusters working at a time share their X rows in L2; W
+// stays in L2); row tiles past the last are copies of it whose results are not stored.
 //
 // Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, 2-5 epilogue (thread r owns
 // accumulator row r).  Every wait is bounded; a timeout posts GMA_ERR_TIMEOUT.
@@ -36,7 +36,7 @@ using namespace tc;
 
 namespace {
 
-// ---- cluster helpers (a pair of CTAs)
+// ---- cluster helpers
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
