@@ -313,12 +313,20 @@ def gma_forward_multi(calls, workspace=None, stream=None, aux_stream=None, check
     if rc:
         raise GmaError(rc, "gma_forward_multi_workspace_size")
     if workspace is None:
+        # the cached buffer's regions move with the request's calls: when the layout differs
+        # from the buffer's last request, this request's region headers are zeroed first
         dev = calls[0]["Qx"].device if n else torch.device("cuda")
         key = dev.index if dev.index is not None else torch.cuda.current_device()
-        ws = _multi_ws.get(key)
+        ws, last = _multi_ws.get(key, (None, None))
         if ws is None or ws.numel() < nbytes.value:
-            ws = torch.zeros(max(nbytes.value, 256), dtype=torch.uint8, device=torch.device("cuda", key))
-            _multi_ws[key] = ws
+            ws, last = torch.zeros(max(nbytes.value, 256), dtype=torch.uint8, device=torch.device("cuda", key)), None
+        layout = tuple(offs[k] for k in range(n))
+        if last is not None and last != layout:
+            for o in layout:
+                rc = lib.gma_workspace_init(_ptr(ws) + o, ws.numel() - o, _stream_ptr(stream))
+                if rc:
+                    raise GmaError(rc, "gma_workspace_init")
+        _multi_ws[key] = (ws, layout)
     else:
         ws = workspace
         if ws.numel() < nbytes.value:

@@ -169,3 +169,35 @@ def test_a_request_captured_in_a_cuda_graph_replays_the_same_results():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(ob, eb) and torch.equal(oc, ec)
+
+
+def test_several_scans_and_several_other_calls_in_one_request():
+    # two per-head causal scans (the auxiliary lane runs them in order) beside two
+    # bidirectional calls and a cross-shaped pair of problems of different lengths, with
+    # events on every call: every output against gma_forward (bitwise for the scans and the
+    # unbudgeted calls, within the partial-sum rounding for the budgeted writes) and the oracle
+    import gaussian_mixture_latent_gb300 as gma
+    wl = [
+        inputs.Workload("s_scan_a", B=2, H=48, N=256, d=64, K=64, dv=64, dtype="bf16", causal=True, seed=21),
+        inputs.Workload("s_bidir_a", B=1, H=40, N=700, d=64, K=64, dv=64, dtype="bf16", causal=False, seed=22),
+        inputs.Workload("s_scan_b", B=1, H=80, N=300, d=64, K=64, dv=64, dtype="bf16", causal=True, seed=23),
+        inputs.Workload("s_bidir_b", B=2, H=3, N=1000, d=64, K=128, dv=64, dtype="bf16", causal=False, seed=24),
+    ]
+    xs = [inputs.gen_all(w) for w in wl]
+    ds = [device_inputs(x) for x in xs]
+    refs = [single(w, d, w.causal) for w, d in zip(wl, ds)]
+    aux = torch.cuda.Stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in wl]
+    for e in sum(evs, []):
+        e.record()
+    outs = gma.gma_forward_multi([call(w, d, w.causal, events=e) for w, d, e in zip(wl, ds, evs)], aux_stream=aux,
+                                 check_status=True)
+    for w, x, o, r in zip(wl, xs, outs, refs):
+        if w.causal:
+            assert torch.equal(o, r), w.name
+        else:
+            close_to(o, r, w)
+        err = oracle_check(w, x, o, list(range(w.G)))
+        print(f"{w.name}: max relative error {err:.2e}")
+    torch.cuda.synchronize()
+    assert all(e[0].elapsed_time(e[1]) > 0 for e in evs)
