@@ -168,8 +168,10 @@ typedef struct {
  * n_calls entries) receives each region's byte offset; the first 4 bytes of a
  * region are that call's device status word (gma_get_status(workspace +
  * offsets[i], ...)).  Zero every region's first 256 bytes before the first use
- * (zeroing the whole workspace does it); later calls keep them zero unless a
- * device error was posted.
+ * (zeroing the whole workspace does it); later requests of the same calls keep
+ * them zero unless a device error was posted.  A request of other calls or
+ * shapes moves the regions: zero its regions' headers again before it runs
+ * (gma_workspace_init(workspace + offsets[i], ...) for each i).
  */
 gma_status gma_forward_multi_workspace_size(const gma_forward_call *calls, int n_calls, size_t *bytes,
                                             size_t *offsets);
