@@ -485,11 +485,18 @@ struct TileInfo {
     int g, j, seg, flags;
 };
 
-template <int K>
+// HV: the K = 128 scores are formed in two parts of 64 components through one
+// 64-column region (a fourth issuer warp, kWarpMma1b, issues the second parts), so
+// that three compute groups fit in TMEM instead of two.
+constexpr bool kReadHalves = true;
+constexpr int kWarpMma1b = kWarpCompute;
+
+template <int K, bool HV = (K == 128 && kReadHalves)>
 struct ReadCfg {
-    static constexpr int NW = groups_for(K);
-    static constexpr int THREADS = (kWarpCompute + 4 * NW) * 32;
-    static constexpr int SX = K <= 64 ? 6 : 4;
+    static constexpr int NW = HV ? 3 : groups_for(K);
+    static constexpr int WC = HV ? kWarpCompute + 1 : kWarpCompute;    // first compute warp
+    static constexpr int THREADS = (WC + 4 * NW) * 32;
+    static constexpr int SX = K <= 64 ? 6 : (HV ? 3 : 4);
     static constexpr int PN = 2;
     static constexpr uint32_t PB = align1k(param_bytes(K));
     static constexpr uint32_t MB = align1k(mem_bytes(K));
@@ -503,7 +510,7 @@ struct ReadCfg {
     static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int NOUT = 80;                                    // [Vt | Z | 1 | 0...]
-    static constexpr uint32_t wg_cols = NOUT + K;
+    static constexpr uint32_t wg_cols = NOUT + (HV ? 64 : K);          // D2 | scores (then e)
     static constexpr uint32_t col_a(int w) { return w * wg_cols; }     // A operand, later D2 (same columns)
     static constexpr uint32_t col_d1(int w) { return w * wg_cols + NOUT; }
     static_assert(BYTES <= 232448 && NW * wg_cols <= TMEM_COLS, "read kernel exceeds shared memory or TMEM");
@@ -513,10 +520,10 @@ struct ReadCfg {
     static_assert(kInfoRing >= SX + NW, "tile-info ring shorter than the tiles in flight");
 };
 
-template <int K>
-__global__ void __launch_bounds__(ReadCfg<K>::THREADS, 1)
+template <int K, bool HV>
+__global__ void __launch_bounds__(ReadCfg<K, HV>::THREADS, 1)
 tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o, TcArgs A) {
-    using C = ReadCfg<K>;
+    using C = ReadCfg<K, HV>;
     constexpr int SX = C::SX, PN = C::PN, NW = C::NW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -524,8 +531,9 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint64_t *xfull = bars, *xempty = xfull + SX;
     uint64_t *a_full = xempty + SX, *d1_full = a_full + NW, *e_full = d1_full + NW, *d2_full = e_full + NW;
     uint64_t *w_full = d2_full + NW, *w_empty = w_full + PN;
-    uint64_t *fin1 = w_empty + PN, *fin2 = fin1 + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin2 + 1);
+    uint64_t *d1b_full = w_empty + PN, *d1_free = d1b_full + NW;       // the second score parts (HV)
+    uint64_t *fin1 = d1_free + NW, *fin2 = fin1 + 1, *fin3 = fin2 + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin3 + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     TileInfo *info = reinterpret_cast<TileInfo *>(sm + C::OFF_INFO);
 
@@ -536,9 +544,10 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
         for (int b = 0; b < NW; ++b) {
             mbar_init(&a_full[b], 1); mbar_init(&d1_full[b], 1); mbar_init(&e_full[b], 1); mbar_init(&d2_full[b], 1);
+            mbar_init(&d1b_full[b], 1); mbar_init(&d1_free[b], 1);
         }
         for (int b = 0; b < PN; ++b) { mbar_init(&w_full[b], 1); mbar_init(&w_empty[b], 1); }
-        mbar_init(fin1, 1); mbar_init(fin2, 1);
+        mbar_init(fin1, 1); mbar_init(fin2, 1); mbar_init(fin3, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -628,12 +637,31 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const int b = t.seg % PN;
             if ((t.flags & kTileFirst) && !mbar_wait_warp(&w_full[b], (t.seg / PN) & 1, ab, kDevErrTimeout)) break;
             tc_fence_after();
-            issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
-                                smem_u32(sm + C::OFF_CA));
+            if constexpr (HV)
+                issue_logdensity_part<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
+                                         smem_u32(sm + C::OFF_CA), 0);
+            else
+                issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
+                                    smem_u32(sm + C::OFF_CA));
             mma_commit(&d1_full[w]);
         }
         mma_commit(fin1);
         wait_ignoring_abort(fin1, 0, A.status);
+    } else if (HV && warp == kWarpMma1b) {
+        // second score parts: the group has read the first part out of the region
+        for (int i = 0;; ++i) {                      // the whole warp, converged
+            const int w = i % NW;
+            if (!mbar_wait_warp(&d1_free[w], (i / NW) & 1, ab, kDevErrTimeout)) break;
+            const TileInfo t = info[i % kInfoRing];
+            if (t.flags & kTileEnd) break;
+            const int b = t.seg % PN;
+            tc_fence_after();
+            issue_logdensity_part<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
+                                     smem_u32(sm + C::OFF_CA), 1);
+            mma_commit(&d1b_full[w]);
+        }
+        mma_commit(fin3);
+        wait_ignoring_abort(fin3, 0, A.status);
     } else if (warp == kWarpMma2) {
         // read MMAs: D2 (128 rows x 80) = e (rows x K, bf16 in TMEM) . [Vt | Z | 1 | 0] (K x 80)
         constexpr uint32_t idesc = idesc_f16(1, 1, 0, 0, TM, C::NOUT);
@@ -656,10 +684,10 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         wait_ignoring_abort(fin2, 0, A.status);
     } else {
         RowThread rt;
-        rt.wg = (warp - kWarpCompute) >> 2;
+        rt.wg = (warp - C::WC) >> 2;
         rt.r = 32u * (warp & 3) + lane;
         rt.lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        rt.wtid = threadIdx.x - kWarpCompute * 32 - rt.wg * kWgThreads;
+        rt.wtid = threadIdx.x - C::WC * 32 - rt.wg * kWgThreads;
         const int w = rt.wg;
         const bool elected = rt.wtid == 0;
         for (int i = w;; i += NW) {
@@ -668,7 +696,11 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const TileInfo t = info[i % kInfoRing];
             if (t.flags & kTileEnd) {
                 // the first end marker: the MMA issuers wait on this group's barriers next
-                if ((t.flags & kTileEndFirst) && elected) { mbar_arrive(&a_full[w]); mbar_arrive(&e_full[w]); }
+                if ((t.flags & kTileEndFirst) && elected) {
+                    mbar_arrive(&a_full[w]);
+                    mbar_arrive(&e_full[w]);
+                    if (HV) mbar_arrive(&d1_free[w]);
+                }
                 break;
             }
             convert_row(sm + C::OFF_X + (i % SX) * kTileBytes, rt.r, tmem + rt.lane_off + C::col_a(w));
@@ -682,7 +714,21 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
             const uint32_t d1 = tmem + rt.lane_off + C::col_d1(w);
-            {
+            if constexpr (HV) {
+                // the two parts of 64 scores through the one region: e of part 0 stays in
+                // registers while the second part's MMA writes the region
+                uint32_t ea[32], eb[32];
+                const float ma = row_exp_part0(d1, scale, ea);
+                tc_fence_before();
+                wg_sync(rt);
+                if (elected) mbar_arrive(&d1_free[w]);
+                ok = mbar_wait(&d1b_full[w], (i / NW) & 1, ab, kDevErrTimeout);
+                if (!wg_all(rt, ok)) break;
+                tc_fence_after();
+                row_exp_part1(d1, scale, ma, ea, eb);
+                tmem_st32(d1, ea);
+                tmem_st32(d1 + 32, eb);
+            } else {
                 // unnormalised responsibilities (the row scale cancels in num / den),
                 // bf16 pairs written over the first K/2 score columns
                 uint32_t e[K / 2];
@@ -772,10 +818,11 @@ cudaError_t launch_read(const Problem &p, const TcLayout &L, const void *Qx, voi
     a.status = reinterpret_cast<unsigned *>(ws);
     a.claim = reinterpret_cast<int *>(ws + L.claim);
     a.dyn = p.sm_budget > 0;
-    auto kern = tc_read_kernel<K>;
-    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), ReadCfg<K>::BYTES);
+    using C = ReadCfg<K>;
+    auto kern = tc_read_kernel<K, (K == 128 && kReadHalves)>;
+    cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), C::BYTES);
     if (e != cudaSuccess) return e;
-    return launch_dependent(kern, dim3(L.ncta), dim3(ReadCfg<K>::THREADS), ReadCfg<K>::BYTES, s, tq, to, a);
+    return launch_dependent(kern, dim3(L.ncta), dim3(C::THREADS), C::BYTES, s, tq, to, a);
 }
 
 }  // namespace
