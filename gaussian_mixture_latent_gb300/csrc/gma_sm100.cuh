@@ -391,6 +391,11 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// 16-byte store to a shared-memory address (32-bit, as smem_u32 gives).
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // Byte offset of 16-byte chunk j of row r inside a 128-byte-swizzled block.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t j) {
     return r * 128u + ((j ^ (r & 7u)) << 4);

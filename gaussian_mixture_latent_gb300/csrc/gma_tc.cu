@@ -339,7 +339,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             const bool valid = c.j * TM + (int)rt.r < A.N;
             const float inv = valid ? 1.0f / total : 0.f;
             const uint64_t inv2 = f2_pack(inv, inv);
-            uint8_t *gbuf = sm + C::OFF_G + w * C::KCH * kTileBytes;
+            const uint32_t gsm = smem_u32(sm + C::OFF_G + w * C::KCH * kTileBytes);
 #pragma unroll
             for (int j = 0; j < K / 8; ++j) {
                 uint32_t wv[4];
@@ -349,8 +349,7 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     f2_unpack(f2_mul(f2_pack(bf16_lo(e[4 * j + u]), bf16_hi(e[4 * j + u])), inv2), ga, gb);
                     wv[u] = pack_bf16(ga, gb);
                 }
-                *reinterpret_cast<uint4 *>(gbuf + (j >> 3) * kTileBytes + sw128_off(rt.r, j & 7)) =
-                    make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                st_shared_v4(gsm + (j >> 3) * kTileBytes + sw128_off(rt.r, j & 7), wv[0], wv[1], wv[2], wv[3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -363,16 +362,19 @@ tc_write_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 tc_fence_after();
                 const int slot = (int)blockIdx.x + c.slot();
                 float *dst = A.partials + ((size_t)slot * (DVV + 1) + rt.r) * K;
-                uint32_t v[K];
+                const bool store = rt.r <= DVV && GMA_IN_BOUNDS(slot < A.nslots && c.g < A.G, A.status);
+#pragma unroll 1
+                for (int cc = 0; cc < K / 32; ++cc) {         // 32 columns at a time (few live registers)
+                    uint32_t v[32];
+                    tmem_ld32(tmem + rt.lane_off + C::COL_D2 + 32 * cc, v);
+                    tmem_ld_wait();
+                    if (store) {
 #pragma unroll
-                for (int cc = 0; cc < K / 32; ++cc) tmem_ld32(tmem + rt.lane_off + C::COL_D2 + 32 * cc, v + 32 * cc);
-                tmem_ld_wait();
-                if (rt.r <= DVV && GMA_IN_BOUNDS(slot < A.nslots && c.g < A.G, A.status)) {
-#pragma unroll
-                    for (int t = 0; t < K; t += 4)
-                        *reinterpret_cast<float4 *>(dst + t) = make_float4(
-                            __uint_as_float(v[t]), __uint_as_float(v[t + 1]), __uint_as_float(v[t + 2]),
-                            __uint_as_float(v[t + 3]));
+                        for (int t = 0; t < 32; t += 4)
+                            *reinterpret_cast<float4 *>(dst + 32 * cc + t) = make_float4(
+                                __uint_as_float(v[t]), __uint_as_float(v[t + 1]), __uint_as_float(v[t + 2]),
+                                __uint_as_float(v[t + 3]));
+                    }
                 }
                 tc_fence_before();
                 wg_sync(rt);

@@ -235,28 +235,36 @@ __device__ __forceinline__ float row_exp_part0(uint32_t taddr, float scale, uint
 // 2^(scale * (m_a - m)) <= 1 (a second bf16 rounding, 2^-9 relative, on those only).
 __device__ __forceinline__ void row_exp_part1(uint32_t taddr, float scale, float ma, uint32_t (&ea)[32],
                                               uint32_t (&eb)[32]) {
-    uint32_t d[64];
-    tmem_ld32(taddr, d);
-    tmem_ld32(taddr + 32, d + 32);
-    tmem_ld_wait();
-    float m[4] = {__uint_as_float(d[0]), __uint_as_float(d[1]), __uint_as_float(d[2]), __uint_as_float(d[3])};
+    // two passes over the region, 32 scores live at a time (the part-0 values are live too)
+    float m[4] = {ma, ma, ma, ma};
 #pragma unroll
-    for (int t = 4; t < 64; t += 4) {
-        m[0] = fmaxf(m[0], __uint_as_float(d[t]));
-        m[1] = fmaxf(m[1], __uint_as_float(d[t + 1]));
-        m[2] = fmaxf(m[2], __uint_as_float(d[t + 2]));
-        m[3] = fmaxf(m[3], __uint_as_float(d[t + 3]));
+    for (int h = 0; h < 2; ++h) {
+        uint32_t d[32];
+        tmem_ld32(taddr + 32 * h, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 32; t += 4) {
+            m[0] = fmaxf(m[0], __uint_as_float(d[t]));
+            m[1] = fmaxf(m[1], __uint_as_float(d[t + 1]));
+            m[2] = fmaxf(m[2], __uint_as_float(d[t + 2]));
+            m[3] = fmaxf(m[3], __uint_as_float(d[t + 3]));
+        }
     }
-    const float mb = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
-    const float mx = fmaxf(ma, mb);
+    const float mx = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
     const uint64_t sc2 = f2_pack(scale, scale), nm2 = f2_pack(-mx * scale, -mx * scale);
 #pragma unroll
-    for (int t = 0; t < 64; t += 2) {
-        float a, b;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(d[t]), __uint_as_float(d[t + 1])), sc2, nm2), a, b);
-        eb[t / 2] = pack_bf16(ex2_approx(a), ex2_approx(b));
+    for (int h = 0; h < 2; ++h) {
+        uint32_t d[32];
+        tmem_ld32(taddr + 32 * h, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+            float a, b;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(d[t]), __uint_as_float(d[t + 1])), sc2, nm2), a, b);
+            eb[16 * h + t / 2] = pack_bf16(ex2_approx(a), ex2_approx(b));
+        }
     }
-    if (mb > ma) {
+    if (mx > ma) {
         const float f = ex2_approx(fmaf(ma, scale, -mx * scale));
         const uint64_t f2 = f2_pack(f, f);
 #pragma unroll
