@@ -487,14 +487,16 @@ struct TileInfo {
     int g, j, seg, flags;
 };
 
-// HV: the K = 128 scores are formed in two parts of 64 components through one
+// HV (K = 128): the scores are formed in two parts of 64 components through one
 // 64-column region (a fourth issuer warp, kWarpMma1b, issues the second parts), so
-// that three compute groups fit in TMEM instead of two.
+// that three compute groups fit in TMEM instead of two.  (At K = 64 the same form
+// gives four groups instead of three, but measured slower: 96 registers a thread.)
 constexpr bool kReadHalves = true;
 constexpr int kWarpMma1b = kWarpCompute;
 
 template <int K, bool HV = (K == 128 && kReadHalves)>
 struct ReadCfg {
+    static constexpr bool HALVES = HV;
     static constexpr int NW = HV ? 3 : groups_for(K);
     static constexpr int WC = HV ? kWarpCompute + 1 : kWarpCompute;    // first compute warp
     static constexpr int THREADS = (WC + 4 * NW) * 32;
@@ -512,7 +514,7 @@ struct ReadCfg {
     static constexpr uint32_t BYTES = OFF_BAR + 512 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int NOUT = 80;                                    // [Vt | Z | 1 | 0...]
-    static constexpr uint32_t wg_cols = NOUT + (HV ? 64 : K);          // D2 | scores (then e)
+    static constexpr uint32_t wg_cols = NOUT + (HV ? K / 2 : K);       // D2 | scores (then e)
     static constexpr uint32_t col_a(int w) { return w * wg_cols; }     // A operand, later D2 (same columns)
     static constexpr uint32_t col_d1(int w) { return w * wg_cols + NOUT; }
     static_assert(BYTES <= 232448 && NW * wg_cols <= TMEM_COLS, "read kernel exceeds shared memory or TMEM");
@@ -640,8 +642,8 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if ((t.flags & kTileFirst) && !mbar_wait_warp(&w_full[b], (t.seg / PN) & 1, ab, kDevErrTimeout)) break;
             tc_fence_after();
             if constexpr (HV)
-                issue_logdensity_part<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
-                                         smem_u32(sm + C::OFF_CA), 0);
+                issue_logdensity_part<K, K / 2>(tmem + C::col_d1(w), tmem + C::col_a(w),
+                                                smem_u32(sm + C::OFF_P + b * C::PB), smem_u32(sm + C::OFF_CA), 0);
             else
                 issue_logdensity<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
                                     smem_u32(sm + C::OFF_CA));
@@ -658,8 +660,8 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (t.flags & kTileEnd) break;
             const int b = t.seg % PN;
             tc_fence_after();
-            issue_logdensity_part<K>(tmem + C::col_d1(w), tmem + C::col_a(w), smem_u32(sm + C::OFF_P + b * C::PB),
-                                     smem_u32(sm + C::OFF_CA), 1);
+            issue_logdensity_part<K, K / 2>(tmem + C::col_d1(w), tmem + C::col_a(w),
+                                            smem_u32(sm + C::OFF_P + b * C::PB), smem_u32(sm + C::OFF_CA), 1);
             mma_commit(&d1b_full[w]);
         }
         mma_commit(fin3);
@@ -717,19 +719,21 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_after();
             const uint32_t d1 = tmem + rt.lane_off + C::col_d1(w);
             if constexpr (HV) {
-                // the two parts of 64 scores through the one region: e of part 0 stays in
+                // the two parts of K/2 scores through the one region: e of part 0 stays in
                 // registers while the second part's MMA writes the region
-                uint32_t ea[32], eb[32];
-                const float ma = row_exp_part0(d1, scale, ea);
+                uint32_t e[K / 2];
+                uint32_t (&ea)[K / 4] = *reinterpret_cast<uint32_t (*)[K / 4]>(&e[0]);
+                uint32_t (&eb)[K / 4] = *reinterpret_cast<uint32_t (*)[K / 4]>(&e[K / 4]);
+                const float ma = row_exp_part0<K / 2>(d1, scale, ea);
                 tc_fence_before();
                 wg_sync(rt);
                 if (elected) mbar_arrive(&d1_free[w]);
                 ok = mbar_wait(&d1b_full[w], (i / NW) & 1, ab, kDevErrTimeout);
                 if (!wg_all(rt, ok)) break;
                 tc_fence_after();
-                row_exp_part1(d1, scale, ma, ea, eb);
-                tmem_st32(d1, ea);
-                tmem_st32(d1 + 32, eb);
+                row_exp_part1<K / 2>(d1, scale, ma, ea, eb);
+#pragma unroll
+                for (int cc = 0; cc < K / 64; ++cc) tmem_st32(d1 + 32 * cc, e + 32 * cc);
             } else {
                 // unnormalised responsibilities (the row scale cancels in num / den),
                 // bf16 pairs written over the first K/2 score columns
@@ -746,27 +750,34 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ok = mbar_wait(&d2_full[w], (i / NW) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
-            uint32_t v0[32], v1[32], dz[4];
-            tmem_ld32(tmem + rt.lane_off + C::col_a(w), v0);
-            tmem_ld32(tmem + rt.lane_off + C::col_a(w) + 32, v1);
-            tmem_ld4(tmem + rt.lane_off + C::col_a(w) + 64, dz);
-            tmem_ld_wait();
-            const float rd = 1.0f / (__uint_as_float(dz[0]) + A.eps * __uint_as_float(dz[1]));
-            const uint64_t rd2 = f2_pack(rd, rd);
             uint8_t *ob = sm + C::OFF_O + w * kTileBytes;
-            if (elected) bulk_wait_group_read<0>();          // this group's previous store left the buffer
-            wg_sync(rt);
+            // 16-byte chunks j0 .. j0 + 3 of the output row from 32 value columns
+            auto put = [&](const uint32_t *v, int j0, uint64_t rd2) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t *src = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
-                uint32_t o[4];
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t o[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float oa, obv;
-                    f2_unpack(f2_mul(f2_pack(__uint_as_float(src[2 * u]), __uint_as_float(src[2 * u + 1])), rd2), oa, obv);
-                    o[u] = pack_bf16(oa, obv);
+                    for (int u = 0; u < 4; ++u) {
+                        float oa, obv;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(v[8 * j + 2 * u]), __uint_as_float(v[8 * j + 2 * u + 1])),
+                                         rd2), oa, obv);
+                        o[u] = pack_bf16(oa, obv);
+                    }
+                    *reinterpret_cast<uint4 *>(ob + sw128_off(rt.r, j0 + j)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
-                *reinterpret_cast<uint4 *>(ob + sw128_off(rt.r, j)) = make_uint4(o[0], o[1], o[2], o[3]);
+            };
+            {
+                uint32_t v0[32], v1[32], dz[4];
+                tmem_ld32(tmem + rt.lane_off + C::col_a(w), v0);
+                tmem_ld32(tmem + rt.lane_off + C::col_a(w) + 32, v1);
+                tmem_ld4(tmem + rt.lane_off + C::col_a(w) + 64, dz);
+                tmem_ld_wait();
+                const float rd = 1.0f / (__uint_as_float(dz[0]) + A.eps * __uint_as_float(dz[1]));
+                const uint64_t rd2 = f2_pack(rd, rd);
+                if (elected) bulk_wait_group_read<0>();      // this group's previous store left the buffer
+                wg_sync(rt);
+                put(v0, 0, rd2);
+                put(v1, 4, rd2);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -821,7 +832,7 @@ cudaError_t launch_read(const Problem &p, const TcLayout &L, const void *Qx, voi
     a.claim = reinterpret_cast<int *>(ws + L.claim);
     a.dyn = p.sm_budget > 0;
     using C = ReadCfg<K>;
-    auto kern = tc_read_kernel<K, (K == 128 && kReadHalves)>;
+    auto kern = tc_read_kernel<K, C::HALVES>;
     cudaError_t e = set_dyn_smem(reinterpret_cast<const void *>(kern), C::BYTES);
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, dim3(L.ncta), dim3(C::THREADS), C::BYTES, s, tq, to, a);

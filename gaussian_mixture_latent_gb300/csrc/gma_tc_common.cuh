@@ -189,31 +189,33 @@ __device__ __forceinline__ void issue_logdensity(uint32_t d_tmem, uint32_t a_tme
     mma_ss(d_tmem, sdesc_none(consta, 128, 256), sdesc_none(pblk + param_wc_off(K), 128, 256), idesc, 1);
 }
 
-// The log-density MMA of one 64-component part (components 64 part .. 64 part + 63)
-// of a K-component head: N = 64 columns at d_tmem.  Each score is the same dot
-// product as in the full-width MMA above.
-template <int K>
+// The log-density MMA of part `part` of NP components (components NP part ..
+// NP part + NP - 1) of a K-component head: N = NP columns at d_tmem.  Each score
+// is the same dot product as in the full-width MMA above.
+template <int K, int NP>
 __device__ __forceinline__ void issue_logdensity_part(uint32_t d_tmem, uint32_t a_tmem, uint32_t pblk, uint32_t consta,
                                                       int part) {
-    constexpr uint32_t idesc = idesc_f16(0, 0, 0, 0, TM, 64);
-    const uint64_t wd = sdesc_sw128(pblk + (uint32_t)part * 64u * 128u, 16, 1024);
+    static_assert(NP % 32 == 0 && K % NP == 0, "parts of 32 or 64 components");
+    constexpr uint32_t idesc = idesc_f16(0, 0, 0, 0, TM, NP);
+    const uint64_t wd = sdesc_sw128(pblk + (uint32_t)part * NP * 128u, 16, 1024);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
         mma_ts(d_tmem, a_tmem + ks * 8, wd + (uint64_t)(((ks >> 2) * 128u * K + (ks & 3) * 32u) >> 4), idesc, ks > 0);
     mma_ss(d_tmem, sdesc_none(consta, 128, 256),
-           sdesc_none(pblk + param_wc_off(K) + nosw16_off(64u * (uint32_t)part, 0), 128, 256), idesc, 1);
+           sdesc_none(pblk + param_wc_off(K) + nosw16_off((uint32_t)(NP * part), 0), 128, 256), idesc, 1);
 }
 
-// A row's K = 128 scores in two parts of 64 through one 64-column TMEM region.
-// Part 0: e_a = 2^(scale * (d - m_a)) as 32 bf16 pairs; returns m_a, the part's maximum.
-__device__ __forceinline__ float row_exp_part0(uint32_t taddr, float scale, uint32_t (&e)[32]) {
-    uint32_t d[64];
-    tmem_ld32(taddr, d);
-    tmem_ld32(taddr + 32, d + 32);
+// A row's scores in two parts of NP through one NP-column TMEM region.
+// Part 0: e_a = 2^(scale * (d - m_a)) as NP/2 bf16 pairs; returns m_a, the part's maximum.
+template <int NP>
+__device__ __forceinline__ float row_exp_part0(uint32_t taddr, float scale, uint32_t (&e)[NP / 2]) {
+    uint32_t d[NP];
+#pragma unroll
+    for (int cc = 0; cc < NP / 32; ++cc) tmem_ld32(taddr + 32 * cc, d + 32 * cc);
     tmem_ld_wait();
     float m[4] = {__uint_as_float(d[0]), __uint_as_float(d[1]), __uint_as_float(d[2]), __uint_as_float(d[3])};
 #pragma unroll
-    for (int t = 4; t < 64; t += 4) {
+    for (int t = 4; t < NP; t += 4) {
         m[0] = fmaxf(m[0], __uint_as_float(d[t]));
         m[1] = fmaxf(m[1], __uint_as_float(d[t + 1]));
         m[2] = fmaxf(m[2], __uint_as_float(d[t + 2]));
@@ -222,7 +224,7 @@ __device__ __forceinline__ float row_exp_part0(uint32_t taddr, float scale, uint
     const float mx = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
     const uint64_t sc2 = f2_pack(scale, scale), nm2 = f2_pack(-mx * scale, -mx * scale);
 #pragma unroll
-    for (int t = 0; t < 64; t += 2) {
+    for (int t = 0; t < NP; t += 2) {
         float a, b;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(d[t]), __uint_as_float(d[t + 1])), sc2, nm2), a, b);
         e[t / 2] = pack_bf16(ex2_approx(a), ex2_approx(b));
@@ -233,12 +235,13 @@ __device__ __forceinline__ float row_exp_part0(uint32_t taddr, float scale, uint
 // Part 1: with m = max(m_a, m_b), e_b = 2^(scale * (d - m)); where m_b > m_a the
 // part-0 values are brought to the common offset by one more factor
 // 2^(scale * (m_a - m)) <= 1 (a second bf16 rounding, 2^-9 relative, on those only).
-__device__ __forceinline__ void row_exp_part1(uint32_t taddr, float scale, float ma, uint32_t (&ea)[32],
-                                              uint32_t (&eb)[32]) {
-    // two passes over the region, 32 scores live at a time (the part-0 values are live too)
+// Two passes over the region, 32 scores live at a time (the part-0 values are live too).
+template <int NP>
+__device__ __forceinline__ void row_exp_part1(uint32_t taddr, float scale, float ma, uint32_t (&ea)[NP / 2],
+                                              uint32_t (&eb)[NP / 2]) {
     float m[4] = {ma, ma, ma, ma};
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NP / 32; ++h) {
         uint32_t d[32];
         tmem_ld32(taddr + 32 * h, d);
         tmem_ld_wait();
@@ -253,7 +256,7 @@ __device__ __forceinline__ void row_exp_part1(uint32_t taddr, float scale, float
     const float mx = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
     const uint64_t sc2 = f2_pack(scale, scale), nm2 = f2_pack(-mx * scale, -mx * scale);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NP / 32; ++h) {
         uint32_t d[32];
         tmem_ld32(taddr + 32 * h, d);
         tmem_ld_wait();
@@ -268,7 +271,7 @@ __device__ __forceinline__ void row_exp_part1(uint32_t taddr, float scale, float
         const float f = ex2_approx(fmaf(ma, scale, -mx * scale));
         const uint64_t f2 = f2_pack(f, f);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
+        for (int t = 0; t < NP / 2; ++t) {
             float a, b;
             f2_unpack(f2_mul(f2_pack(bf16_lo(ea[t]), bf16_hi(ea[t])), f2), a, b);
             ea[t] = pack_bf16(a, b);
