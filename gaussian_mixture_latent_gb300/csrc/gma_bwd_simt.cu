@@ -21,7 +21,7 @@
 // running state in shared memory.
 //
 // Kernels (all fp32 arithmetic, every reduction in a fixed order, so results are
-// deterministic): gb_rowmat (row-times-matrix tiles of 64 x 64), gb_outer (per-range sums of
+// deterministic): gb_rowmat (row-times-matrix tiles of 64 x 64 or 64 x 80), gb_outer (per-range sums of
 // outer products), gb_reduce (sum / exclusive prefix / exclusive suffix over ranges),
 // gb_ab, gb_ds, gb_dx (per-row steps), gb_cq / gb_ck (the causal chunk walks),
 // gb_param (dmu, drho, dalpha).  The responsibilities come from the forward's CUDA-core
@@ -54,22 +54,25 @@ __device__ __forceinline__ float gld<__nv_bfloat16>(const __nv_bfloat16 *p, size
 //   A(g, i, k) = A[(g N + i) lda + k] for k < a_cols, 1 at k == a_cols when a_one, else 0;
 //   B(k, c)    = MT ? M[mo + c ldm + k] : M[mo + k ldm + c],  k < KA,
 //   mo = (m_per_head ? g % H : g) m_stride.
-// 64 x 64 output tile per CTA, 256 threads, each four rows (ty + 16 q) by four columns
-// (tx + 16 j); k in steps of 32 through shared memory, in increasing order per output.
+// 64-row x 16 JN-column output tile per CTA, 256 threads, each four rows (ty + 16 q) by JN
+// columns (tx + 16 j); k in steps of 32 through shared memory, in increasing order per
+// output (the last step only over the k that exist).  JN = 5 serves widths such as dv + 1
+// and 2 d + 1 in fewer tiles than 64-column ones would.
 constexpr int kRmTile = 64;
 
-template <typename TA, bool MT>
+template <typename TA, bool MT, int JN>
 __global__ void __launch_bounds__(kGbThreads) gb_rowmat_kernel(int N, int KA, int C, int H, int lda, int a_cols,
                                                                int a_one, const TA *__restrict__ A,
                                                                const float *__restrict__ M, int m_per_head,
                                                                size_t m_stride, int ldm, float *__restrict__ out,
                                                                int ldo) {
+    constexpr int CW = 16 * JN;
     __shared__ float as[kRmTile][33];
-    __shared__ float bs[32][kRmTile + 1];
-    const int i0 = blockIdx.x * kRmTile, c0 = blockIdx.y * kRmTile, g = blockIdx.z;
+    __shared__ float bs[32][CW + 1];
+    const int i0 = blockIdx.x * kRmTile, c0 = blockIdx.y * CW, g = blockIdx.z;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const float *Mg = M + (size_t)(m_per_head ? g % H : g) * m_stride;
-    float acc[4][4] = {};
+    float acc[4][JN] = {};
     for (int k0 = 0; k0 < KA; k0 += 32) {
         for (int e = threadIdx.x; e < kRmTile * 32; e += kGbThreads) {
             const int r = e >> 5, cc = e & 31;
@@ -80,26 +83,35 @@ __global__ void __launch_bounds__(kGbThreads) gb_rowmat_kernel(int N, int KA, in
                 else if (a_one && k == a_cols) av = 1.f;
             }
             as[r][cc] = av;
+        }
+        for (int e = threadIdx.x; e < CW * 32; e += kGbThreads) {
             if (MT) {          // element (k0 + cc, c0 + r): a warp reads consecutive k of one row of M
+                const int r = e >> 5, cc = e & 31;
                 const int kk = k0 + cc, c = c0 + r;
                 bs[cc][r] = (kk < KA && c < C) ? Mg[(size_t)c * ldm + kk] : 0.f;
-            } else {           // element (k0 + (e >> 6), c0 + (e & 63))
-                const int kk = k0 + (e >> 6), c = c0 + (e & 63);
-                bs[e >> 6][e & 63] = (kk < KA && c < C) ? Mg[(size_t)kk * ldm + c] : 0.f;
+            } else {           // element (k0 + e / CW, c0 + e % CW)
+                const int kr = e / CW, cc = e - kr * CW;
+                const int kk = k0 + kr, c = c0 + cc;
+                bs[kr][cc] = (kk < KA && c < C) ? Mg[(size_t)kk * ldm + c] : 0.f;
             }
         }
         __syncthreads();
-#pragma unroll 4
-        for (int kk = 0; kk < 32; ++kk) {
-            float a[4], b[4];
+        auto step = [&](int kk) {
+            float a[4], b[JN];
 #pragma unroll
             for (int q = 0; q < 4; ++q) a[q] = as[ty + 16 * q][kk];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = bs[kk][tx + 16 * j];
+            for (int j = 0; j < JN; ++j) b[j] = bs[kk][tx + 16 * j];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[q][j] = fmaf(a[q], b[j], acc[q][j]);
+                for (int j = 0; j < JN; ++j) acc[q][j] = fmaf(a[q], b[j], acc[q][j]);
+        };
+        if (KA - k0 >= 32) {
+#pragma unroll 4
+            for (int kk = 0; kk < 32; ++kk) step(kk);
+        } else {
+            for (int kk = 0; kk < KA - k0; ++kk) step(kk);
         }
         __syncthreads();
     }
@@ -108,7 +120,7 @@ __global__ void __launch_bounds__(kGbThreads) gb_rowmat_kernel(int N, int KA, in
         const int i = i0 + ty + 16 * q;
         if (i >= N) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < JN; ++j) {
             const int c = c0 + tx + 16 * j;
             if (c < C) out[((size_t)g * N + i) * ldo + c] = acc[q][j];
         }
@@ -144,42 +156,52 @@ struct USquares {              // [x | x^2 | 1]
 };
 
 // part[((g P + p) K + k) W + c] = sum over rows i of range p of A[(g N + i) K + k] U(g N + i, c),
-// k < K, c < W; range p = rows [p rpp, min(N, (p + 1) rpp)).  64 x 64 output tile per CTA,
-// each thread four components (ty + 16 q) by four columns (tx + 16 j), rows in increasing
-// order through shared memory 32 at a time.
-template <typename U>
+// k < K, c < W; range p = rows [p rpp, min(N, (p + 1) rpp)).  64-component x 16 JN-column
+// output tile per CTA, each thread four components (ty + 16 q) by JN columns (tx + 16 j),
+// rows in increasing order through shared memory 32 at a time (the last block only over
+// the rows that exist).
+template <typename U, int JN>
 __global__ void __launch_bounds__(kGbThreads) gb_outer_kernel(int N, int K, int W, int P, int rpp,
                                                               const float *__restrict__ A, U u,
                                                               float *__restrict__ part) {
+    constexpr int CW = 16 * JN;
     __shared__ float as[32][kRmTile + 1];
-    __shared__ float us[32][kRmTile + 1];
+    __shared__ float us[32][CW + 1];
     const int ktiles = (K + kRmTile - 1) / kRmTile;
     const int kt = blockIdx.x % ktiles, ct = blockIdx.x / ktiles;
     const int p = blockIdx.y, g = blockIdx.z;
     const int r0 = p * rpp, r1 = min(N, r0 + rpp);
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int k0 = kt * kRmTile, c0 = ct * kRmTile;
-    float acc[4][4] = {};
+    const int k0 = kt * kRmTile, c0 = ct * CW;
+    float acc[4][JN] = {};
     for (int j0 = r0; j0 < r1; j0 += 32) {
         for (int e = threadIdx.x; e < 32 * kRmTile; e += kGbThreads) {
             const int jr = e >> 6, cc = e & 63;
-            const int j = j0 + jr, k = k0 + cc, c = c0 + cc;
-            const size_t row = (size_t)g * N + j;
-            as[jr][cc] = (j < r1 && k < K) ? A[row * K + k] : 0.f;
-            us[jr][cc] = (j < r1 && c < W) ? u(row, c) : 0.f;
+            const int j = j0 + jr, k = k0 + cc;
+            as[jr][cc] = (j < r1 && k < K) ? A[((size_t)g * N + j) * K + k] : 0.f;
+        }
+        for (int e = threadIdx.x; e < 32 * CW; e += kGbThreads) {
+            const int jr = e / CW, cc = e - jr * CW;
+            const int j = j0 + jr, c = c0 + cc;
+            us[jr][cc] = (j < r1 && c < W) ? u((size_t)g * N + j, c) : 0.f;
         }
         __syncthreads();
-#pragma unroll 4
-        for (int jr = 0; jr < 32; ++jr) {
-            float a[4], v[4];
+        auto step = [&](int jr) {
+            float a[4], v[JN];
 #pragma unroll
             for (int q = 0; q < 4; ++q) a[q] = as[jr][ty + 16 * q];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) v[jj] = us[jr][tx + 16 * jj];
+            for (int jj = 0; jj < JN; ++jj) v[jj] = us[jr][tx + 16 * jj];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) acc[q][jj] = fmaf(a[q], v[jj], acc[q][jj]);
+                for (int jj = 0; jj < JN; ++jj) acc[q][jj] = fmaf(a[q], v[jj], acc[q][jj]);
+        };
+        if (r1 - j0 >= 32) {
+#pragma unroll 4
+            for (int jr = 0; jr < 32; ++jr) step(jr);
+        } else {
+            for (int jr = 0; jr < r1 - j0; ++jr) step(jr);
         }
         __syncthreads();
     }
@@ -188,7 +210,7 @@ __global__ void __launch_bounds__(kGbThreads) gb_outer_kernel(int N, int K, int 
         const int k = k0 + ty + 16 * q;
         if (k >= K) continue;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
+        for (int jj = 0; jj < JN; ++jj) {
             const int c = c0 + tx + 16 * jj;
             if (c < W) part[(((size_t)g * P + p) * K + k) * W + c] = acc[q][jj];
         }
@@ -597,19 +619,35 @@ __global__ void __launch_bounds__(kWalkThreads) gb_ck_kernel(GbCausalArgs a) {
 
 unsigned blocks_for(size_t n, int per) { return (unsigned)((n + per - 1) / per); }
 
+// Column tile of the product kernels: 80 columns (5 a thread) where that takes fewer
+// columns in all than 64-column tiles (the widths dv + 1, 2 d + 1), else 64.
+int col_tile_for(int C) {
+    const int t64 = (C + 63) / 64 * 64, t80 = (C + 79) / 80 * 80;
+    return t80 < t64 ? 80 : 64;
+}
+
 template <typename TA, bool MT>
 cudaError_t rowmat(const Problem &p, int KA, int C, int lda, int a_cols, int a_one, const TA *A, const float *M,
                    int m_per_head, size_t m_stride, int ldm, float *out, int ldo, cudaStream_t s) {
-    dim3 grid((p.N + kRmTile - 1) / kRmTile, (C + kRmTile - 1) / kRmTile, p.G);
-    gb_rowmat_kernel<TA, MT><<<grid, kGbThreads, 0, s>>>(p.N, KA, C, p.H, lda, a_cols, a_one, A, M, m_per_head,
-                                                         m_stride, ldm, out, ldo);
+    const int cw = col_tile_for(C);
+    dim3 grid((p.N + kRmTile - 1) / kRmTile, (C + cw - 1) / cw, p.G);
+    if (cw == 80)
+        gb_rowmat_kernel<TA, MT, 5><<<grid, kGbThreads, 0, s>>>(p.N, KA, C, p.H, lda, a_cols, a_one, A, M,
+                                                                m_per_head, m_stride, ldm, out, ldo);
+    else
+        gb_rowmat_kernel<TA, MT, 4><<<grid, kGbThreads, 0, s>>>(p.N, KA, C, p.H, lda, a_cols, a_one, A, M,
+                                                                m_per_head, m_stride, ldm, out, ldo);
     return cudaGetLastError();
 }
 
 template <typename U>
 cudaError_t outer(const Problem &p, const GbLayout &L, int W, const float *A, U u, float *part, cudaStream_t s) {
-    dim3 grid(((p.K + kRmTile - 1) / kRmTile) * ((W + kRmTile - 1) / kRmTile), L.P, p.G);
-    gb_outer_kernel<U><<<grid, kGbThreads, 0, s>>>(p.N, p.K, W, L.P, L.rpp, A, u, part);
+    const int cw = col_tile_for(W);
+    dim3 grid(((p.K + kRmTile - 1) / kRmTile) * ((W + cw - 1) / cw), L.P, p.G);
+    if (cw == 80)
+        gb_outer_kernel<U, 5><<<grid, kGbThreads, 0, s>>>(p.N, p.K, W, L.P, L.rpp, A, u, part);
+    else
+        gb_outer_kernel<U, 4><<<grid, kGbThreads, 0, s>>>(p.N, p.K, W, L.P, L.rpp, A, u, part);
     return cudaGetLastError();
 }
 
