@@ -750,34 +750,27 @@ tc_read_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ok = mbar_wait(&d2_full[w], (i / NW) & 1, ab, kDevErrTimeout);
             if (!wg_all(rt, ok)) break;
             tc_fence_after();
+            uint32_t v0[32], v1[32], dz[4];
+            tmem_ld32(tmem + rt.lane_off + C::col_a(w), v0);
+            tmem_ld32(tmem + rt.lane_off + C::col_a(w) + 32, v1);
+            tmem_ld4(tmem + rt.lane_off + C::col_a(w) + 64, dz);
+            tmem_ld_wait();
+            const float rd = 1.0f / (__uint_as_float(dz[0]) + A.eps * __uint_as_float(dz[1]));
+            const uint64_t rd2 = f2_pack(rd, rd);
             uint8_t *ob = sm + C::OFF_O + w * kTileBytes;
-            // 16-byte chunks j0 .. j0 + 3 of the output row from 32 value columns
-            auto put = [&](const uint32_t *v, int j0, uint64_t rd2) {
+            if (elected) bulk_wait_group_read<0>();          // this group's previous store left the buffer
+            wg_sync(rt);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t o[4];
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t *src = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+                uint32_t o[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        float oa, obv;
-                        f2_unpack(f2_mul(f2_pack(__uint_as_float(v[8 * j + 2 * u]), __uint_as_float(v[8 * j + 2 * u + 1])),
-                                         rd2), oa, obv);
-                        o[u] = pack_bf16(oa, obv);
-                    }
-                    *reinterpret_cast<uint4 *>(ob + sw128_off(rt.r, j0 + j)) = make_uint4(o[0], o[1], o[2], o[3]);
+                for (int u = 0; u < 4; ++u) {
+                    float oa, obv;
+                    f2_unpack(f2_mul(f2_pack(__uint_as_float(src[2 * u]), __uint_as_float(src[2 * u + 1])), rd2), oa, obv);
+                    o[u] = pack_bf16(oa, obv);
                 }
-            };
-            {
-                uint32_t v0[32], v1[32], dz[4];
-                tmem_ld32(tmem + rt.lane_off + C::col_a(w), v0);
-                tmem_ld32(tmem + rt.lane_off + C::col_a(w) + 32, v1);
-                tmem_ld4(tmem + rt.lane_off + C::col_a(w) + 64, dz);
-                tmem_ld_wait();
-                const float rd = 1.0f / (__uint_as_float(dz[0]) + A.eps * __uint_as_float(dz[1]));
-                const uint64_t rd2 = f2_pack(rd, rd);
-                if (elected) bulk_wait_group_read<0>();      // this group's previous store left the buffer
-                wg_sync(rt);
-                put(v0, 0, rd2);
-                put(v1, 4, rd2);
+                *reinterpret_cast<uint4 *>(ob + sw128_off(rt.r, j)) = make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
