@@ -38,9 +38,12 @@
 // log-density MMAs; warp 2 issues the write / read MMAs (two issuers, because an
 // MMA issue blocks while the tensor pipe fills); warps 3 onwards are the NW
 // compute warpgroups that take tiles in turn (one thread per row), each with its
-// own TMEM columns, so one group's softmax overlaps the others' MMAs.  Every
-// mbarrier wait is bounded; a timeout posts GMA_ERR_TIMEOUT to the workspace
-// status word and the CTA winds down.
+// own TMEM columns, so one group's softmax overlaps the others' MMAs.  The read
+// at K = 128 forms a tile's scores in two parts of 64 components through one
+// 64-column region, so that three groups fit in TMEM: warp 1 issues the first
+// parts, warp 3 the second ones, and the compute groups are warps 4 onwards
+// ((4 + 4 * 3) warps).  Every mbarrier wait is bounded; a timeout posts
+// GMA_ERR_TIMEOUT to the workspace status word and the CTA winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
