@@ -133,6 +133,10 @@ struct WriteCfg {
     static constexpr uint32_t col_d1(int w) { return w * wg_cols + 64; }
     static constexpr uint32_t COL_D2 = NW * wg_cols;
     static_assert(BYTES <= 232448 && COL_D2 + K <= TMEM_COLS, "write kernel exceeds shared memory or TMEM");
+    // A group waits on tile i's routing stage by parity; the stage's previous tile (i - SX)
+    // must then be its own or one whose conversion it has seen (the log-density MMA of its
+    // previous tile i - NW follows the conversion of tile i - NW - 1), so SX >= NW.
+    static_assert(SX >= NW, "fewer routing stages than compute groups");
 };
 
 // SEG = false: the CTA's range of the (head, tile) list, one partial slot per (CTA, head).
@@ -525,6 +529,9 @@ struct ReadCfg {
     // read MMA: the producer waits for tile i - SX's conversion, which follows the
     // epilogue (hence the read MMA) of tile i - SX - NW.
     static_assert(kInfoRing >= SX + NW, "tile-info ring shorter than the tiles in flight");
+    // A group waits on tile i's routing stage by parity: the stage's previous tile (i - SX)
+    // must be its own or one whose conversion it has seen, so SX >= NW.
+    static_assert(SX >= NW, "fewer routing stages than compute groups");
 };
 
 template <int K, bool HV>
