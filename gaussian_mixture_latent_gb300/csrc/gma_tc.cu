@@ -66,8 +66,9 @@ namespace {
 
 constexpr int kWarpProducer = 0, kWarpMma1 = 1, kWarpMma2 = 2, kWarpCompute = 3;
 // Compute groups per CTA: three at K = 64 (TMEM holds three groups' operands and
-// scores), two at K = 128.  More groups hide more of each group's serial
-// convert -> log-density MMA -> softmax latency.
+// scores), two at K = 128 (the read fits three there by forming its scores in two
+// parts, ReadCfg).  More groups hide more of each group's serial convert ->
+// log-density MMA -> softmax latency.
 __host__ __device__ constexpr int groups_for(int K) { return K <= 64 ? 3 : 2; }
 
 struct TcArgs {
